@@ -1,0 +1,193 @@
+"""CPU oracle for block-quantized matvec -- TEST INFRASTRUCTURE ONLY.
+
+Only the test suite, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
+``bench.py`` may import this package.  The product library never does: it
+has no CPU fallback, and it shares no code with this oracle.
+
+The arithmetic lives in ``qbw_oracle.c`` (scalar C, fp64 accumulation in
+ascending k).  This module only compiles it with gcc and marshals numpy
+arrays through ctypes.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "qbw_oracle.c")
+_OUT_DIR = os.path.join(_HERE, "_build")
+_LIB_PATH = os.path.join(_OUT_DIR, "liboracle.so")
+_lock = threading.Lock()
+_lib = None
+
+F32, BF16 = 0, 1
+_FMT = {"q8_0": 0, "q4_0": 1}
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle into ``oracle/_build/liboracle.so`` (plain gcc, no SIMD flags)."""
+    os.makedirs(_OUT_DIR, exist_ok=True)
+    if force or not os.path.exists(_LIB_PATH) or os.path.getmtime(_LIB_PATH) < os.path.getmtime(_SRC):
+        tmp = _LIB_PATH + f".{os.getpid()}.tmp"
+        subprocess.check_call([
+            "gcc", "-O2", "-std=c11", "-ffp-contract=off", "-fno-fast-math", "-fPIC", "-shared",
+            "-Wall", "-Wextra", "-o", tmp, _SRC, "-lm"])
+        os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def lib():
+    """The loaded oracle.  ``QBW_ORACLE_LIB`` points at another build of the
+    same source (the mutation tests use it to load a deliberately broken copy)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            path = os.environ.get("QBW_ORACLE_LIB") or build()
+            _lib = ctypes.CDLL(path)
+            _declare(_lib)
+    return _lib
+
+
+def _declare(L):
+    P = ctypes.c_void_p
+    i64 = ctypes.c_int64
+    L.oracle_fp16_to_f64.restype = ctypes.c_double
+    L.oracle_fp16_to_f64.argtypes = [ctypes.c_uint16]
+    L.oracle_bf16_to_f64.restype = ctypes.c_double
+    L.oracle_bf16_to_f64.argtypes = [ctypes.c_uint16]
+    L.oracle_round_bf16.restype = ctypes.c_uint16
+    L.oracle_round_bf16.argtypes = [ctypes.c_double]
+    for name in ("oracle_round_bf16_array", "oracle_fp16_to_f64_array", "oracle_bf16_to_f64_array",
+                 "oracle_gelu_tanh_array", "oracle_gelu_tanh_deriv_array"):
+        getattr(L, name).restype = None
+        getattr(L, name).argtypes = [P, i64, P]
+    L.oracle_gelu_tanh.restype = ctypes.c_double
+    L.oracle_gelu_tanh.argtypes = [ctypes.c_double]
+    L.oracle_dequant.restype = ctypes.c_int
+    L.oracle_dequant.argtypes = [ctypes.c_int, P, i64, i64, P]
+    L.oracle_qmv.restype = ctypes.c_int
+    L.oracle_qmv.argtypes = [ctypes.c_int, P, P, ctypes.c_int, i64, i64, P, P]
+    L.oracle_qmv_rows.restype = ctypes.c_int
+    L.oracle_qmv_rows.argtypes = [ctypes.c_int, P, P, ctypes.c_int, i64, i64, i64, P, P]
+    L.oracle_gateup_q4_0.restype = ctypes.c_int
+    L.oracle_gateup_q4_0.argtypes = [P, P, P, ctypes.c_int, i64, i64, P, P, P, P, P]
+    L.oracle_qmm_q4_0.restype = ctypes.c_int
+    L.oracle_qmm_q4_0.argtypes = [P, P, ctypes.c_int, i64, i64, i64, P, P]
+
+
+def _ptr(a: np.ndarray):
+    return a.ctypes.data_as(ctypes.c_void_p)
+
+
+def _act(x: np.ndarray):
+    """Return (contiguous array, dtype code): float32 values or uint16 bf16 bits."""
+    x = np.ascontiguousarray(x)
+    if x.dtype == np.float32:
+        return x, F32
+    if x.dtype == np.uint16:
+        return x, BF16
+    raise TypeError(f"activations must be float32 or uint16 (bf16 bits), got {x.dtype}")
+
+
+def _check(rc: int, what: str):
+    if rc != 0:
+        raise ValueError(f"{what}: oracle returned {rc}")
+
+
+# ---------------------------------------------------------------- scalars
+
+def fp16_to_f64(bits) -> np.ndarray:
+    b = np.ascontiguousarray(bits, dtype=np.uint16)
+    out = np.empty(b.shape, dtype=np.float64)
+    lib().oracle_fp16_to_f64_array(_ptr(b), b.size, _ptr(out))
+    return out
+
+
+def bf16_to_f64(bits) -> np.ndarray:
+    b = np.ascontiguousarray(bits, dtype=np.uint16)
+    out = np.empty(b.shape, dtype=np.float64)
+    lib().oracle_bf16_to_f64_array(_ptr(b), b.size, _ptr(out))
+    return out
+
+
+def round_bf16(v) -> np.ndarray:
+    v = np.ascontiguousarray(v, dtype=np.float64)
+    out = np.empty(v.shape, dtype=np.uint16)
+    lib().oracle_round_bf16_array(_ptr(v), v.size, _ptr(out))
+    return out
+
+
+def gelu_tanh(v) -> np.ndarray:
+    v = np.ascontiguousarray(v, dtype=np.float64)
+    out = np.empty(v.shape, dtype=np.float64)
+    lib().oracle_gelu_tanh_array(_ptr(v), v.size, _ptr(out))
+    return out
+
+
+def gelu_tanh_deriv(v) -> np.ndarray:
+    v = np.ascontiguousarray(v, dtype=np.float64)
+    out = np.empty(v.shape, dtype=np.float64)
+    lib().oracle_gelu_tanh_deriv_array(_ptr(v), v.size, _ptr(out))
+    return out
+
+
+# ---------------------------------------------------------------- products
+
+def _weights(w: np.ndarray) -> np.ndarray:
+    w = np.ascontiguousarray(w)
+    if w.dtype != np.uint8:
+        raise TypeError("weights must be raw uint8 block bytes")
+    return w
+
+
+def dequant(fmt: str, w: np.ndarray, N: int, K: int) -> np.ndarray:
+    w = _weights(w)
+    out = np.empty((N, K), dtype=np.float32)
+    _check(lib().oracle_dequant(_FMT[fmt], _ptr(w), N, K, _ptr(out)), "dequant")
+    return out
+
+
+def qmv(fmt: str, w: np.ndarray, x: np.ndarray, N: int, K: int):
+    """y = W x and S = sum_k |w x| for every row (fp64)."""
+    w = _weights(w)
+    x, xt = _act(x)
+    y = np.empty(N, dtype=np.float64)
+    S = np.empty(N, dtype=np.float64)
+    _check(lib().oracle_qmv(_FMT[fmt], _ptr(w), _ptr(x), xt, N, K, _ptr(y), _ptr(S)), "qmv")
+    return y, S
+
+
+def qmv_rows(fmt: str, w: np.ndarray, x: np.ndarray, n0: int, n1: int, K: int):
+    """Rows [n0, n1) of y = W x, with S; ``w`` still holds the whole matrix."""
+    w = _weights(w)
+    x, xt = _act(x)
+    y = np.empty(n1 - n0, dtype=np.float64)
+    S = np.empty(n1 - n0, dtype=np.float64)
+    _check(lib().oracle_qmv_rows(_FMT[fmt], _ptr(w), _ptr(x), xt, n0, n1, K, _ptr(y), _ptr(S)),
+           "qmv_rows")
+    return y, S
+
+
+def gateup_q4_0(wg: np.ndarray, wu: np.ndarray, x: np.ndarray, N: int, K: int):
+    """Returns dict with g, u, out = gelu_tanh(g) * u, Sg, Su (all fp64)."""
+    wg, wu = _weights(wg), _weights(wu)
+    x, xt = _act(x)
+    r = {k: np.empty(N, dtype=np.float64) for k in ("g", "u", "out", "Sg", "Su")}
+    _check(lib().oracle_gateup_q4_0(_ptr(wg), _ptr(wu), _ptr(x), xt, N, K, _ptr(r["g"]), _ptr(r["u"]),
+                                    _ptr(r["out"]), _ptr(r["Sg"]), _ptr(r["Su"])), "gateup")
+    return r
+
+
+def qmm_q4_0(w: np.ndarray, X: np.ndarray, M: int, N: int, K: int):
+    """Y[m, n] = sum_k X[m, k] W[n, k] and S[m, n] (fp64)."""
+    w = _weights(w)
+    X, xt = _act(X)
+    Y = np.empty((M, N), dtype=np.float64)
+    S = np.empty((M, N), dtype=np.float64)
+    _check(lib().oracle_qmm_q4_0(_ptr(w), _ptr(X), xt, M, N, K, _ptr(Y), _ptr(S)), "qmm")
+    return Y, S

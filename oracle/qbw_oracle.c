@@ -1,0 +1,300 @@
+/*
+ * qbw_oracle.c -- the plain, slow CPU oracle for block-quantized weight
+ * matrix-vector products (GGUF Q8_0 / Q4_0).
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing in the product library calls, links or
+ * includes this file; only the test suite, the smoke check and the benchmark's
+ * CPU-baseline leg use it.  It shares no code, header, table or constant with
+ * the CUDA path: it has its own fp16/bf16 decoders, its own nibble unpacking
+ * and its own GELU.
+ *
+ * Everything is scalar C, accumulated in double precision in ascending k, with
+ * no SIMD intrinsics and no reordering beyond the textbook definition.
+ *
+ * What is computed, and where the pages define it:
+ *  - Q8_0 block: w = d * q, d an IEEE binary16 scale, q a signed byte
+ *    (jouleclaw-loader-gguf BENCHMARKS, "Matmul throughput -- Q8_0 scalar vs
+ *    NEON"; gem architecture, "M4 Max operating assumptions").
+ *  - Q4_0 block: w = d * (q - 8), q a 4-bit code, 32 codes + scale in
+ *    18 bytes (gem architecture, "M4 Max operating assumptions").  Nibble
+ *    order follows the GGUF block_q4_0 record: code j in the low nibble of
+ *    byte j, code j+16 in the high nibble.
+ *  - Matrix-vector product y = W x with W stored [out, in] row-major
+ *    (SafeC Gemma 4 design notes, "Math primitives implementation status").
+ *  - Gated FFN projection out = gelu_tanh(Wg x) * (Wu x) with the tanh form
+ *    of GELU (SafeC Gemma 4 design notes, "Gated FFN").
+ *  - Small-M product Y = X W^T for a few token rows (gem architecture,
+ *    "Ownership boundaries": prompt tiles up to 32 tokens).
+ *
+ * Error scale: next to every output the oracle also returns
+ * S = sum_k |w_k * x_k| (fp64), the scale the parity tolerances use.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#define ORACLE_QK 32
+#define ORACLE_PI 3.14159265358979323846
+
+/* ---------------------------------------------------------------- decoders */
+
+/* IEEE 754 binary16: 1 sign, 5 exponent (bias 15), 10 fraction bits. */
+double oracle_fp16_to_f64(uint16_t h)
+{
+    int sign = (h >> 15) & 1;
+    int e = (h >> 10) & 0x1f;
+    int m = h & 0x3ff;
+    double v;
+    if (e == 0)
+        v = ldexp((double)m, -24);               /* subnormal: m * 2^-24 */
+    else if (e == 31)
+        v = m ? NAN : INFINITY;
+    else
+        v = ldexp((double)(1024 + m), e - 25);   /* (1 + m/2^10) * 2^(e-15) */
+    return sign ? -v : v;
+}
+
+/* bfloat16: 1 sign, 8 exponent (bias 127), 7 fraction bits. */
+double oracle_bf16_to_f64(uint16_t b)
+{
+    int sign = (b >> 15) & 1;
+    int e = (b >> 7) & 0xff;
+    int m = b & 0x7f;
+    double v;
+    if (e == 0)
+        v = ldexp((double)m, -133);              /* subnormal: m * 2^-133 */
+    else if (e == 255)
+        v = m ? NAN : INFINITY;
+    else
+        v = ldexp((double)(128 + m), e - 134);   /* (1 + m/2^7) * 2^(e-127) */
+    return sign ? -v : v;
+}
+
+/* Round a double to the nearest bfloat16 (ties to even), return its bits. */
+uint16_t oracle_round_bf16(double v)
+{
+    if (isnan(v))
+        return 0x7fc0;
+    int neg = signbit(v) ? 1 : 0;
+    double a = fabs(v);
+    uint16_t s = (uint16_t)(neg << 15);
+    if (a == 0.0)
+        return s;
+    if (isinf(a))
+        return (uint16_t)(s | 0x7f80);
+    int ex;
+    frexp(a, &ex);                     /* a in [2^(ex-1), 2^ex) */
+    int q = ex - 8;                    /* quantum of 8 significant bits */
+    if (q < -133)
+        q = -133;                      /* subnormal quantum */
+    double r = ldexp(a, -q);           /* exact: power-of-two scaling */
+    double fl = floor(r);
+    double frac = r - fl;
+    if (frac > 0.5 || (frac == 0.5 && fmod(fl, 2.0) != 0.0))
+        fl += 1.0;
+    double res = ldexp(fl, q);
+    /* largest finite bf16 is (2 - 2^-7) * 2^127 */
+    if (res > ldexp(255.0, 120))
+        return (uint16_t)(s | 0x7f80);
+    if (res == 0.0)
+        return s;
+    /* encode: res = M * 2^E with M in [128, 256) for normals */
+    int er;
+    frexp(res, &er);                   /* res in [2^(er-1), 2^er) */
+    int E = er - 1;                    /* unbiased exponent */
+    if (E < -126) {                    /* subnormal: res = m * 2^-133 */
+        int m = (int)ldexp(res, 133);
+        return (uint16_t)(s | (uint16_t)m);
+    }
+    int m = (int)ldexp(res, 7 - E) - 128;
+    return (uint16_t)(s | (uint16_t)((E + 127) << 7) | (uint16_t)m);
+}
+
+void oracle_round_bf16_array(const double *v, int64_t n, uint16_t *out)
+{
+    for (int64_t i = 0; i < n; i++)
+        out[i] = oracle_round_bf16(v[i]);
+}
+
+void oracle_fp16_to_f64_array(const uint16_t *h, int64_t n, double *out)
+{
+    for (int64_t i = 0; i < n; i++)
+        out[i] = oracle_fp16_to_f64(h[i]);
+}
+
+void oracle_bf16_to_f64_array(const uint16_t *b, int64_t n, double *out)
+{
+    for (int64_t i = 0; i < n; i++)
+        out[i] = oracle_bf16_to_f64(b[i]);
+}
+
+/* Activation dtype codes: 0 = fp32 values, 1 = bf16 bit patterns. */
+static double *widen_activations(const void *x, int xdtype, int64_t n)
+{
+    double *out = (double *)malloc((size_t)n * sizeof(double));
+    if (!out)
+        return NULL;
+    for (int64_t i = 0; i < n; i++) {
+        if (xdtype == 0)
+            out[i] = (double)((const float *)x)[i];
+        else
+            out[i] = oracle_bf16_to_f64(((const uint16_t *)x)[i]);
+    }
+    return out;
+}
+
+/* ------------------------------------------------------------ block decode */
+
+static uint16_t read_u16le(const uint8_t *p)
+{
+    return (uint16_t)(p[0] | (p[1] << 8));
+}
+
+/* fmt: 0 = Q8_0, 1 = Q4_0 */
+static int block_size(int fmt) { return fmt == 0 ? 34 : 18; }
+
+/* Decode the 32 weights of one block into w[0..31]. */
+static void decode_block(int fmt, const uint8_t *blk, double *w)
+{
+    double d = oracle_fp16_to_f64(read_u16le(blk));
+    for (int k = 0; k < ORACLE_QK; k++) {
+        if (fmt == 0) {
+            w[k] = d * (double)(int)(int8_t)blk[2 + k];
+        } else {
+            uint8_t byte = blk[2 + (k % 16)];
+            int code = (k < 16) ? (byte & 0x0f) : (byte >> 4);
+            w[k] = d * (double)(code - 8);
+        }
+    }
+}
+
+/* Dequantize a whole matrix to fp32.  Every d*q fits in 24 bits of
+ * significand (11-bit scale times a code of at most 8 bits), so the double
+ * product converts to float exactly. */
+int oracle_dequant(int fmt, const uint8_t *w, int64_t N, int64_t K, float *out)
+{
+    if (K % ORACLE_QK)
+        return -1;
+    int64_t nb = K / ORACLE_QK;
+    double wb[ORACLE_QK];
+    for (int64_t n = 0; n < N; n++)
+        for (int64_t b = 0; b < nb; b++) {
+            decode_block(fmt, w + (n * nb + b) * block_size(fmt), wb);
+            for (int k = 0; k < ORACLE_QK; k++)
+                out[n * K + b * ORACLE_QK + k] = (float)wb[k];
+        }
+    return 0;
+}
+
+/* ------------------------------------------------------------- products */
+
+/* y[n] = sum_k w[n,k] * x[k], S[n] = sum_k |w[n,k] * x[k]|, k ascending. */
+static void matvec_rows(int fmt, const uint8_t *w, const double *x,
+                        int64_t n0, int64_t n1, int64_t K, double *y, double *S)
+{
+    int64_t nb = K / ORACLE_QK;
+    double wb[ORACLE_QK];
+    for (int64_t n = n0; n < n1; n++) {
+        double acc = 0.0, sabs = 0.0;
+        for (int64_t b = 0; b < nb; b++) {
+            decode_block(fmt, w + (n * nb + b) * block_size(fmt), wb);
+            for (int k = 0; k < ORACLE_QK; k++) {
+                double p = wb[k] * x[b * ORACLE_QK + k];
+                acc += p;
+                sabs += fabs(p);
+            }
+        }
+        y[n - n0] = acc;
+        if (S)
+            S[n - n0] = sabs;
+    }
+}
+
+int oracle_qmv(int fmt, const uint8_t *w, const void *x, int xdtype,
+               int64_t N, int64_t K, double *y, double *S)
+{
+    if (K % ORACLE_QK)
+        return -1;
+    double *xd = widen_activations(x, xdtype, K);
+    if (!xd)
+        return -2;
+    matvec_rows(fmt, w, xd, 0, N, K, y, S);
+    free(xd);
+    return 0;
+}
+
+/* Same product for a subset of rows [n0, n1): used to time and to sample. */
+int oracle_qmv_rows(int fmt, const uint8_t *w, const void *x, int xdtype,
+                    int64_t n0, int64_t n1, int64_t K, double *y, double *S)
+{
+    if (K % ORACLE_QK)
+        return -1;
+    double *xd = widen_activations(x, xdtype, K);
+    if (!xd)
+        return -2;
+    matvec_rows(fmt, w, xd, n0, n1, K, y, S);
+    free(xd);
+    return 0;
+}
+
+/* gelu_tanh(v) = 0.5 v (1 + tanh(sqrt(2/pi) (v + 0.044715 v^3))) */
+double oracle_gelu_tanh(double v)
+{
+    const double c = sqrt(2.0 / ORACLE_PI);
+    return 0.5 * v * (1.0 + tanh(c * (v + 0.044715 * v * v * v)));
+}
+
+/* d/dv gelu_tanh(v); used only to scale the gate+up tolerance. */
+double oracle_gelu_tanh_deriv(double v)
+{
+    const double c = sqrt(2.0 / ORACLE_PI);
+    double z = c * (v + 0.044715 * v * v * v);
+    double t = tanh(z);
+    return 0.5 * (1.0 + t) + 0.5 * v * (1.0 - t * t) * c * (1.0 + 3.0 * 0.044715 * v * v);
+}
+
+void oracle_gelu_tanh_array(const double *v, int64_t n, double *out)
+{
+    for (int64_t i = 0; i < n; i++)
+        out[i] = oracle_gelu_tanh(v[i]);
+}
+
+void oracle_gelu_tanh_deriv_array(const double *v, int64_t n, double *out)
+{
+    for (int64_t i = 0; i < n; i++)
+        out[i] = oracle_gelu_tanh_deriv(v[i]);
+}
+
+/* g = Wg x, u = Wu x, out = gelu_tanh(g) * u (both matrices Q4_0). */
+int oracle_gateup_q4_0(const uint8_t *wg, const uint8_t *wu, const void *x, int xdtype,
+                       int64_t N, int64_t K, double *g, double *u, double *out,
+                       double *Sg, double *Su)
+{
+    if (K % ORACLE_QK)
+        return -1;
+    double *xd = widen_activations(x, xdtype, K);
+    if (!xd)
+        return -2;
+    matvec_rows(1, wg, xd, 0, N, K, g, Sg);
+    matvec_rows(1, wu, xd, 0, N, K, u, Su);
+    for (int64_t n = 0; n < N; n++)
+        out[n] = oracle_gelu_tanh(g[n]) * u[n];
+    free(xd);
+    return 0;
+}
+
+/* Y[m, n] = sum_k X[m, k] * W[n, k] for m < M (W is Q4_0, X row-major). */
+int oracle_qmm_q4_0(const uint8_t *w, const void *X, int xdtype,
+                    int64_t M, int64_t N, int64_t K, double *Y, double *S)
+{
+    if (K % ORACLE_QK)
+        return -1;
+    double *xd = widen_activations(X, xdtype, M * K);
+    if (!xd)
+        return -2;
+    for (int64_t m = 0; m < M; m++)
+        matvec_rows(1, w, xd + m * K, 0, N, K, Y + m * N, S + m * N);
+    free(xd);
+    return 0;
+}

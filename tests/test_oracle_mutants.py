@@ -1,0 +1,67 @@
+"""The oracle's pins must catch plausible mistakes.
+
+Each case copies the oracle source, plants one mistake (a swapped nibble
+order, a dropped term, a wrong sign, index, bias or constant), compiles the
+copy with gcc and runs the oracle pin tests against it in a subprocess.  The
+pins pass on the real oracle and must fail on every mutant.  Everything
+happens on the CPU.
+"""
+import os
+import subprocess
+import sys
+
+import pytest
+
+from conftest import ROOT
+
+SRC = os.path.join(ROOT, "oracle", "qbw_oracle.c")
+
+MUTANTS = {
+    "nibble_order_swapped": ("int code = (k < 16) ? (byte & 0x0f) : (byte >> 4);",
+                             "int code = (k < 16) ? (byte >> 4) : (byte & 0x0f);"),
+    "q4_offset_dropped": ("w[k] = d * (double)(code - 8);", "w[k] = d * (double)(code);"),
+    "q4_offset_sign": ("w[k] = d * (double)(code - 8);", "w[k] = d * (double)(code + 8);"),
+    "q8_unsigned_codes": ("w[k] = d * (double)(int)(int8_t)blk[2 + k];", "w[k] = d * (double)(int)blk[2 + k];"),
+    "q4_byte_index_off": ("uint8_t byte = blk[2 + (k % 16)];", "uint8_t byte = blk[1 + (k % 16)];"),
+    "scale_read_at_end": ("double d = oracle_fp16_to_f64(read_u16le(blk));",
+                          "double d = oracle_fp16_to_f64(read_u16le(blk + 16));"),
+    "fp16_subnormal_scale": ("v = ldexp((double)m, -24);", "v = ldexp((double)m, -14);"),
+    "fp16_bias_off_by_one": ("v = ldexp((double)(1024 + m), e - 25);", "v = ldexp((double)(1024 + m), e - 24);"),
+    "fp16_implicit_bit_dropped": ("v = ldexp((double)(1024 + m), e - 25);", "v = ldexp((double)(m), e - 25);"),
+    "bf16_bias_off_by_one": ("v = ldexp((double)(128 + m), e - 134);", "v = ldexp((double)(128 + m), e - 133);"),
+    "round_ties_away": ("(frac == 0.5 && fmod(fl, 2.0) != 0.0)", "(frac == 0.5)"),
+    "abs_dropped_from_scale": ("sabs += fabs(p);", "sabs += p;"),
+    "first_block_skipped": ("for (int64_t b = 0; b < nb; b++) {\n            decode_block(fmt, w + (n * nb + b) * "
+                            "block_size(fmt), wb);\n            for (int k = 0; k < ORACLE_QK; k++) {",
+                            "for (int64_t b = 1; b < nb; b++) {\n            decode_block(fmt, w + (n * nb + b) * "
+                            "block_size(fmt), wb);\n            for (int k = 0; k < ORACLE_QK; k++) {"),
+    "dequant_block_index": ("out[n * K + b * ORACLE_QK + k] = (float)wb[k];", "out[n * K + b + k] = (float)wb[k];"),
+    "gelu_cubic_constant": ("return 0.5 * v * (1.0 + tanh(c * (v + 0.044715 * v * v * v)));",
+                            "return 0.5 * v * (1.0 + tanh(c * (v + 0.04715 * v * v * v)));"),
+    "gelu_linear_term_dropped": ("return 0.5 * v * (1.0 + tanh(c * (v + 0.044715 * v * v * v)));",
+                                 "return 0.5 * v * (1.0 + tanh(c * (0.044715 * v * v * v)));"),
+    "gelu_erf_form": ("return 0.5 * v * (1.0 + tanh(c * (v + 0.044715 * v * v * v)));",
+                      "return 0.5 * v * (1.0 + erf(v / sqrt(2.0)));"),
+    "qmm_operand_transposed": ("matvec_rows(1, w, xd + m * K, 0, N, K, Y + m * N, S + m * N);",
+                               "matvec_rows(1, w, xd + m, 0, N, K, Y + m * N, S + m * N);"),
+    "gateup_gate_on_up": ("out[n] = oracle_gelu_tanh(g[n]) * u[n];", "out[n] = oracle_gelu_tanh(u[n]) * g[n];"),
+}
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_pins_catch_mutant(name, tmp_path):
+    before, after = MUTANTS[name]
+    src = open(SRC).read()
+    assert src.count(before) == 1, f"pattern for {name} not found exactly once"
+    mutated = src.replace(before, after)
+    c = tmp_path / "mutant.c"
+    so = tmp_path / "libmutant.so"
+    c.write_text(mutated)
+    subprocess.check_call(["gcc", "-O2", "-std=c11", "-ffp-contract=off", "-fPIC", "-shared", "-w",
+                           "-o", str(so), str(c), "-lm"])
+    env = dict(os.environ, QBW_ORACLE_LIB=str(so))
+    r = subprocess.run([sys.executable, "-m", "pytest", "-x", "-q", "-p", "no:cacheprovider",
+                        os.path.join(ROOT, "tests", "test_oracle_scalars.py"),
+                        os.path.join(ROOT, "tests", "test_oracle_products.py")],
+                       cwd=ROOT, env=env, capture_output=True, text=True, timeout=600)
+    assert r.returncode != 0, f"mutant {name} survived the pins:\n{r.stdout[-2000:]}"
