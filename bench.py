@@ -1,0 +1,588 @@
+#!/usr/bin/env python
+"""Benchmark of the block-quantized decode path on GB300.
+
+One step = one decode token through a 60-layer weight sweep shaped like the
+gem 31B profile (gem docs/research/architecture.md, "Fixed model profiles"):
+per layer the Q4_0 matrices q [5376->8192], k [5376->4096], v [5376->4096],
+o [8192->5376], gate/up [5376->21504] (one fused gate+up+GELU launch) and down
+[21504->5376], M = 1, with bf16 activations chained from one matrix to the
+next (o consumes q's output, standing in for attention).  The 420 weight
+matrices (16,164,126,720 bytes, far larger than L2) stay resident in HBM; the
+whole step is replayed as one CUDA graph.
+
+Printed (rank 0, one JSON line): effective HBM GB/s of the sweep (algorithmic
+bytes / time), tokens/s, the end-to-end rate with the token's activation
+copied in from pinned host memory and the result copied back every step, the
+roofline of the dominant kernel, SM clocks sampled during the timed region,
+the CPU oracle as a baseline, and supplementary per-kernel numbers for the
+single-matrix workloads (2048x2048 Q8_0, 21504x5376 Q4_0, gate+up, small-M).
+
+``--impl reference`` times the CPU oracle instead (on a bounded sample of the
+same workload per step) and prints the same line with ``"impl": "reference"``.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+import synth  # noqa: E402
+
+METRIC = "achieved HBM GB/s (% of GB300 peak) for M=1 Q4_0/Q8_0 matvec; layer-sweep tok/s"
+UNIT = "GB/s"
+NOMINAL_HBM_GBS = 8000.0
+LAYERS = 60
+SEED = 4
+HIDDEN, QDIM, KVDIM, FFN = 5376, 8192, 4096, 21504
+# (name, N out, K in, input buffer, output buffer); gate and up share one launch
+MATRICES = [("q", QDIM, HIDDEN), ("k", KVDIM, HIDDEN), ("v", KVDIM, HIDDEN), ("o", HIDDEN, QDIM),
+            ("gate", FFN, HIDDEN), ("up", FFN, HIDDEN), ("down", HIDDEN, FFN)]
+WORKLOAD = "decode weight sweep: 60 layers x Q4_0 {q 5376->8192, k 5376->4096, v 5376->4096, " \
+           "o 8192->5376, gate/up 5376->21504 fused, down 21504->5376}, M=1, chained bf16 activations"
+
+
+def log(*a):
+    print(*a, file=sys.stderr, flush=True)
+
+
+def weight_bytes(N, K):
+    return synth.matrix_bytes("q4_0", N, K)
+
+
+def sweep_bytes_per_layer():
+    """Algorithmic bytes of one layer: every weight byte once, plus activation
+    reads and output writes (bf16) of each launch."""
+    wb = sum(weight_bytes(N, K) for _, N, K in MATRICES)
+    act = 0
+    act += 3 * (2 * HIDDEN) + 2 * QDIM + 2 * 2 * KVDIM          # q, k, v read h, write outputs
+    act += 2 * QDIM + 2 * HIDDEN                                 # o
+    act += 2 * HIDDEN + 2 * FFN                                  # gate+up
+    act += 2 * FFN + 2 * HIDDEN                                  # down
+    return wb, act
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return float(d["hbm_gbs"]), "measured", d
+    return 6800.0, "fallback", {}
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "block_quantized_weight_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        h.update(f.encode())
+        h.update(open(os.path.join(csrc, f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(kernel: str):
+    """DRAM bytes per launch from the committed ncu summary, or None when the
+    kernel sources changed since it was captured."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    d = json.load(open(p))
+    ent = d.get(kernel)
+    if not ent or ent.get("source_hash") != kernel_source_hash():
+        return None
+    return ent.get("dram_bytes_per_launch")
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id: str):
+        self.gpu = gpu_id
+        self.samples = []
+        self.proc = None
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) >= 9:
+                self.samples.append((time.time(), parts))
+
+    def stop(self):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self, t0, t1):
+        def num(s):
+            try:
+                return float(s)
+            except ValueError:
+                return None
+        window = [p for t, p in self.samples if t0 <= t <= t1]
+        used = "timed"
+        if len(window) < 3:
+            window = [p for _, p in self.samples]
+            used = "bench"
+        if not window:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0, "window": "none"}
+        sm = [num(p[1]) for p in window if num(p[1]) is not None]
+        smax = [num(p[2]) for p in window if num(p[2]) is not None]
+        reasons = set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for p in window:
+            for name, v in zip(names, p[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(window), "window": used,
+                "power_w_max": max((num(p[3]) or 0.0) for p in window)}
+
+
+# ------------------------------------------------------------------ GPU arm
+class Sweep:
+    """The 420 resident weight matrices and the chained activation buffers."""
+
+    def __init__(self, torch, qbw, device):
+        self.torch, self.qbw, self.dev = torch, qbw, device
+        self.offsets = {}
+        total = 0
+        for layer in range(LAYERS):
+            for mi, (name, N, K) in enumerate(MATRICES):
+                self.offsets[(layer, name)] = total
+                total += weight_bytes(N, K)
+        self.total_weight_bytes = total
+        self.w = torch.empty(total, dtype=torch.uint8, device=device)
+        bf = torch.bfloat16
+        self.h = torch.empty(HIDDEN, dtype=bf, device=device)
+        self.q = torch.empty(QDIM, dtype=bf, device=device)
+        self.k = torch.empty(KVDIM, dtype=bf, device=device)
+        self.v = torch.empty(KVDIM, dtype=bf, device=device)
+        self.o = torch.empty(HIDDEN, dtype=bf, device=device)
+        self.a = torch.empty(FFN, dtype=bf, device=device)
+        self.layer0_host = {}
+
+    def fill(self, threads=None):
+        import concurrent.futures as cf
+        torch = self.torch
+        threads = threads or min(16, os.cpu_count() or 1)
+
+        def gen(layer):
+            return layer, [synth.q4_0_weights(N, K, seed=SEED, stream=mi, layer=layer)
+                           for mi, (_, N, K) in enumerate(MATRICES)]
+
+        t0 = time.time()
+        with cf.ThreadPoolExecutor(threads) as ex:
+            for layer, mats in ex.map(gen, range(LAYERS)):
+                for (name, N, K), arr in zip(MATRICES, mats):
+                    off = self.offsets[(layer, name)]
+                    self.w[off:off + arr.size].copy_(torch.from_numpy(arr))
+                    if layer == 0:
+                        self.layer0_host[name] = arr
+        torch.cuda.synchronize()
+        log(f"weights: {self.total_weight_bytes / 1e9:.2f} GB generated and resident in {time.time() - t0:.1f} s")
+
+    def view(self, layer, name):
+        N, K = {n: (N, K) for n, N, K in MATRICES}[name]
+        off = self.offsets[(layer, name)]
+        return self.w[off:off + weight_bytes(N, K)]
+
+    def launches(self, stream=None):
+        """Enqueue one token: 6 launches per layer, 360 in all."""
+        qbw = self.qbw
+        for layer in range(LAYERS):
+            qbw.qmv_q4_0(self.view(layer, "q"), self.h, self.q, 1, QDIM, HIDDEN, stream)
+            qbw.qmv_q4_0(self.view(layer, "k"), self.h, self.k, 1, KVDIM, HIDDEN, stream)
+            qbw.qmv_q4_0(self.view(layer, "v"), self.h, self.v, 1, KVDIM, HIDDEN, stream)
+            qbw.qmv_q4_0(self.view(layer, "o"), self.q, self.o, 1, HIDDEN, QDIM, stream)
+            qbw.qmv_gateup_q4_0(self.view(layer, "gate"), self.view(layer, "up"), self.o, self.a, 1, FFN, HIDDEN,
+                                stream)
+            qbw.qmv_q4_0(self.view(layer, "down"), self.a, self.h, 1, HIDDEN, FFN, stream)
+
+    LAUNCHES_PER_STEP = LAYERS * 6
+
+    def per_kernel_pass(self):
+        """One eager step with CUDA events around every launch (same stream)."""
+        torch, qbw = self.torch, self.qbw
+        s = torch.cuda.current_stream()
+        rec = []
+        specs = []
+        for layer in range(LAYERS):
+            specs += [("qmv_q4_0", lambda L=layer: qbw.qmv_q4_0(self.view(L, "q"), self.h, self.q, 1, QDIM, HIDDEN),
+                       weight_bytes(QDIM, HIDDEN) + 2 * HIDDEN + 2 * QDIM),
+                      ("qmv_q4_0", lambda L=layer: qbw.qmv_q4_0(self.view(L, "k"), self.h, self.k, 1, KVDIM, HIDDEN),
+                       weight_bytes(KVDIM, HIDDEN) + 2 * HIDDEN + 2 * KVDIM),
+                      ("qmv_q4_0", lambda L=layer: qbw.qmv_q4_0(self.view(L, "v"), self.h, self.v, 1, KVDIM, HIDDEN),
+                       weight_bytes(KVDIM, HIDDEN) + 2 * HIDDEN + 2 * KVDIM),
+                      ("qmv_q4_0", lambda L=layer: qbw.qmv_q4_0(self.view(L, "o"), self.q, self.o, 1, HIDDEN, QDIM),
+                       weight_bytes(HIDDEN, QDIM) + 2 * QDIM + 2 * HIDDEN),
+                      ("qmv_gateup_q4_0", lambda L=layer: qbw.qmv_gateup_q4_0(self.view(L, "gate"), self.view(L, "up"),
+                                                                             self.o, self.a, 1, FFN, HIDDEN),
+                       2 * weight_bytes(FFN, HIDDEN) + 2 * HIDDEN + 2 * FFN),
+                      ("qmv_q4_0", lambda L=layer: qbw.qmv_q4_0(self.view(L, "down"), self.a, self.h, 1, HIDDEN, FFN),
+                       weight_bytes(HIDDEN, FFN) + 2 * FFN + 2 * HIDDEN)]
+        for name, fn, nbytes in specs:
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(s)
+            fn()
+            e1.record(s)
+            rec.append((name, nbytes, e0, e1))
+        torch.cuda.synchronize()
+        out = {}
+        for name, nbytes, e0, e1 in rec:
+            d = out.setdefault(name, {"launches": 0, "bytes": 0, "ms": 0.0})
+            d["launches"] += 1
+            d["bytes"] += nbytes
+            d["ms"] += e0.elapsed_time(e1)
+        return out
+
+
+def time_graph(torch, graph, steps, stream):
+    """Replay ``graph`` ``steps`` times on ``stream``; events on the same stream."""
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(steps):
+            graph.replay()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1)
+
+
+def capture(torch, fn, stream):
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(stream):
+        fn()                      # warm every kernel outside capture
+    torch.cuda.synchronize()
+    with torch.cuda.graph(g, stream=stream):
+        fn()
+    torch.cuda.synchronize()
+    return g
+
+
+def supplementary_kernels(torch, qbw, hbm_peak):
+    """Single-matrix workloads, each cycled over rotating weight copies whose
+    total exceeds twice the L2 size, replayed from a CUDA graph."""
+    dev = torch.device("cuda")
+    res = {}
+    l2 = torch.cuda.get_device_properties(0).L2_cache_size
+
+    def bf16(a):
+        return torch.from_numpy(a.view(np.int16).copy()).view(torch.bfloat16).to(dev)
+
+    def run(name, nbytes_call, copies, make_call, flops=None):
+        calls = [make_call(i) for i in range(copies)]
+        s = torch.cuda.Stream()
+        g = capture(torch, lambda: [c() for c in calls], s)
+        with torch.cuda.stream(s):
+            for _ in range(3):
+                g.replay()
+        reps = max(3, int(2e9 / (nbytes_call * copies)))
+        ms = time_graph(torch, g, reps, s)
+        us = ms * 1e3 / (reps * copies)
+        gbs = nbytes_call / (us * 1e3)
+        entry = {"us_per_call": round(us, 3), "GB_per_s": round(gbs, 1), "frac_of_measured_hbm": round(gbs / hbm_peak, 4),
+                 "frac_of_8TBps": round(gbs / NOMINAL_HBM_GBS, 4), "bytes_per_call": nbytes_call,
+                 "weight_copies": copies, "rotating_bytes": nbytes_call * copies, "l2_bytes": l2}
+        if flops:
+            entry["TFLOP_per_s"] = round(flops / (us * 1e-6) / 1e12, 2)
+        res[name] = entry
+        log(f"{name}: {us:.2f} us/call  {gbs:.0f} GB/s")
+
+    # 2048 x 2048 Q8_0, fp32 in/out
+    N = K = 2048
+    w = torch.from_numpy(synth.q8_0_weights(N, K, seed=0)).to(dev)
+    copies = max(2, int(np.ceil(2.2 * l2 / w.numel())))
+    ws = [w.clone() for _ in range(copies)]
+    x = torch.from_numpy(synth.activations(K, seed=0)).to(dev)
+    y = torch.empty(N, device=dev)
+    run("qmv_q8_0 2048x2048 f32", w.numel() + 4 * K + 4 * N, copies,
+        lambda i: (lambda: qbw.qmv_q8_0(ws[i], x, y, 1, N, K)))
+    del ws, w
+    # 21504 x 5376 Q4_0, fp32 in/out
+    N, K = 21504, 5376
+    w = torch.from_numpy(synth.q4_0_weights(N, K, seed=1)).to(dev)
+    copies = max(2, int(np.ceil(2.2 * l2 / w.numel())))
+    ws = [w.clone() for _ in range(copies)]
+    x = torch.from_numpy(synth.activations(K, seed=1)).to(dev)
+    y = torch.empty(N, device=dev)
+    run("qmv_q4_0 21504x5376 f32", w.numel() + 4 * K + 4 * N, copies,
+        lambda i: (lambda: qbw.qmv_q4_0(ws[i], x, y, 1, N, K)))
+    # gate+up on two such matrices, bf16 in, fp32 out
+    wu = torch.from_numpy(synth.q4_0_weights(N, K, seed=2, stream=1)).to(dev)
+    wus = [wu.clone() for _ in range(copies)]
+    xb = bf16(synth.activations(K, seed=2, dtype="bf16"))
+    run("qmv_gateup_q4_0 2x21504x5376 bf16->f32", 2 * w.numel() + 2 * K + 4 * N, copies,
+        lambda i: (lambda: qbw.qmv_gateup_q4_0(ws[i], wus[i], xb, y, 1, N, K)))
+    del ws, wus, w, wu
+    # small-M tiles
+    for (N, K) in ((5376, 5376), (5376, 21504)):
+        w = torch.from_numpy(synth.q4_0_weights(N, K, seed=3)).to(dev)
+        copies = max(2, int(np.ceil(2.2 * l2 / w.numel())))
+        ws = [w.clone() for _ in range(copies)]
+        for M in (8, 16, 32):
+            X = bf16(synth.activations((M, K), seed=3, dtype="bf16"))
+            Y = torch.empty(M, N, dtype=torch.bfloat16, device=dev)
+            wsb = qbw.qmm_q4_0_smallM_workspace_bytes(M, N, K)
+            work = torch.zeros(max(wsb, 1), dtype=torch.uint8, device=dev)
+            run(f"qmm_q4_0_smallM M={M} {N}x{K} bf16", w.numel() + 2 * M * K + 2 * M * N, copies,
+                lambda i, X=X, Y=Y, M=M, N=N, K=K, work=work: (lambda: qbw.qmm_q4_0_smallM(ws[i], X, Y, M, N, K, work)),
+                flops=2.0 * M * N * K)
+        del ws, w
+    torch.cuda.empty_cache()
+    return res
+
+
+def cpu_baseline(layer0_host, x_bits, budget_s):
+    """The oracle, as it stands, on a bounded sample of the sweep: rows of
+    layer 0's matrices in order, in chunks, until ``budget_s`` elapse."""
+    import oracle
+    oracle.lib()
+    done_bytes = 0
+    rows_done = {}
+    t0 = time.time()
+    xs = {"q": x_bits, "k": x_bits, "v": x_bits}
+    rng = np.random.default_rng(0)
+    for name, N, K in MATRICES:
+        x = xs.get(name)
+        if x is None:
+            x = synth.f32_to_bf16_bits(rng.standard_normal(K).astype(np.float32))
+        rb = synth.row_bytes("q4_0", K)
+        n = 0
+        while n < N and time.time() - t0 < budget_s:
+            n1 = min(N, n + 256)
+            oracle.qmv_rows("q4_0", layer0_host[name], x, n, n1, K)
+            done_bytes += (n1 - n) * rb
+            n = n1
+        rows_done[name] = n
+        if time.time() - t0 >= budget_s:
+            break
+    dt = time.time() - t0
+    return done_bytes / dt / 1e9, dt, done_bytes, rows_done
+
+
+def gpu_arm(args):
+    import torch
+    import block_quantized_weight_gb300 as qbw
+
+    ws, rank, local = dist_env()
+    if ws > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    else:
+        torch.cuda.set_device(0)
+    dev = torch.device("cuda", torch.cuda.current_device())
+    qbw.load()
+    hbm_peak, peak_kind, peaks = load_peaks()
+
+    sweep = Sweep(torch, qbw, dev)
+    sweep.fill()
+    x0 = synth.activations(HIDDEN, seed=SEED, dtype="bf16")
+    x0_dev = torch.from_numpy(x0.view(np.int16).copy()).view(torch.bfloat16).to(dev)
+    sweep.h.copy_(x0_dev)
+
+    stream = torch.cuda.Stream()
+
+    def step():
+        sweep.launches()
+
+    graph = capture(torch, step, stream)
+    props = torch.cuda.get_device_properties(torch.cuda.current_device())
+    uuid = str(getattr(props, "uuid", ""))
+    clocks = ClockSampler(uuid if uuid.startswith("GPU-") else (f"GPU-{uuid}" if uuid else "0"))
+    clocks.start()
+    time.sleep(0.3)
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            sweep.h.copy_(x0_dev)
+            graph.replay()
+        sweep.h.copy_(x0_dev)
+    torch.cuda.synchronize()
+    if ws > 1:
+        torch.distributed.barrier()
+    t_start = time.time()
+    ms = time_graph(torch, graph, args.steps, stream)
+    t_end = time.time()
+    if ws > 1:
+        t = torch.tensor([ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms = float(t.item())
+    assert qbw.fault_read(clear=True, stream=stream) == 0, "a kernel recorded a fault"
+
+    # end to end: the token's activation in from pinned host memory, the
+    # step's result out to pinned host memory, every step
+    h_in = torch.from_numpy(x0.view(np.int16).copy()).view(torch.bfloat16).pin_memory()
+    h_out = torch.empty(HIDDEN, dtype=torch.bfloat16).pin_memory()
+    e2e_steps = max(3, min(args.steps, 200))
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    with torch.cuda.stream(stream):
+        for _ in range(e2e_steps):
+            sweep.h.copy_(h_in, non_blocking=True)
+            graph.replay()
+            h_out.copy_(sweep.h, non_blocking=True)
+            stream.synchronize()
+    e2e_s = time.perf_counter() - t0
+    clocks.stop()
+
+    per_kernel = sweep.per_kernel_pass()
+    wb, ab = sweep_bytes_per_layer()
+    step_bytes = LAYERS * (wb + ab)
+    value = step_bytes * args.steps * ws / (ms * 1e-3) / 1e9
+    tok_s = args.steps * ws / (ms * 1e-3)
+    e2e_value = step_bytes * e2e_steps * ws / e2e_s / 1e9
+
+    dom = max(per_kernel, key=lambda k: per_kernel[k]["ms"])
+    pk = per_kernel[dom]
+    achieved = pk["bytes"] / pk["launches"] / (pk["ms"] / pk["launches"] * 1e-3) / 1e9
+    traffic = profiled_traffic(dom)
+    roofline = {"bound": "hbm", "kernel": dom, "achieved": round(achieved, 1), "peak": hbm_peak, "unit": "GB/s",
+                "frac": round(achieved / hbm_peak, 4), "peak_kind": f"{peak_kind} copy bandwidth (hbm_gbs)",
+                "frac_of_8TBps": round(achieved / NOMINAL_HBM_GBS, 4),
+                "bytes_per_launch": round(pk["bytes"] / pk["launches"]), "launches": pk["launches"],
+                "us_per_launch": round(pk["ms"] / pk["launches"] * 1e3, 3),
+                "traffic": traffic,
+                "share_of_step": {k: round(v["ms"] / sum(d["ms"] for d in per_kernel.values()), 4)
+                                  for k, v in per_kernel.items()},
+                "measured": "CUDA events around every launch of one eager sweep step after the timed region"}
+    if rank != 0:
+        if ws > 1:
+            torch.distributed.destroy_process_group()
+        return
+
+    supp = {} if args.no_kernels else supplementary_kernels(torch, qbw, hbm_peak)
+    cpu = None
+    if not args.no_cpu and ws == 1:
+        v, dt, nbytes, rows = cpu_baseline(sweep.layer0_host, x0, args.cpu_seconds)
+        cpu = {"value": round(v, 4), "unit": UNIT, "cores": 1, "kind": "oracle",
+               "sample": f"oracle qmv_q4_0 over {nbytes} weight bytes of layer 0 (rows per matrix: {rows}), "
+                         f"{dt:.1f} s single-threaded on the host"}
+    line = {
+        "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": ws, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms / args.steps, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "layers": LAYERS, "bytes_per_step": step_bytes,
+                   "weight_bytes_per_step": LAYERS * wb, "tok_per_s": round(tok_s, 2),
+                   "frac_of_measured_hbm": round(value / hbm_peak, 4), "frac_of_8TBps": round(value / NOMINAL_HBM_GBS, 4),
+                   "l2": "inputs larger than L2: 16.16 GB of weights streamed per step, no flush needed",
+                   "parallelism": "replicas" if ws > 1 else "single GPU", "graph": "one CUDA graph per step",
+                   "seed": SEED},
+        "e2e": {"value": round(e2e_value, 1), "unit": UNIT, "tok_per_s": round(e2e_steps * ws / e2e_s, 2),
+                "h2d_bytes_per_step": 2 * HIDDEN, "d2h_bytes_per_step": 2 * HIDDEN, "steps": e2e_steps,
+                "path": "pinned host -> device copy, graph replay of the C-ABI launches, device -> pinned host copy, "
+                        "stream sync, every step"},
+        "gpu_launches": Sweep.LAUNCHES_PER_STEP * args.steps,
+        "roofline": roofline,
+        "clocks": clocks.summary(t_start - 0.05, t_end + 0.05),
+        "cpu_baseline": cpu,
+        "kernels": supp,
+        "per_kernel_in_sweep": {k: {"launches": v["launches"], "ms": round(v["ms"], 4),
+                                    "GB_per_s": round(v["bytes"] / (v["ms"] * 1e-3) / 1e9, 1)}
+                                for k, v in per_kernel.items()},
+        "gpu": torch.cuda.get_device_name(),
+    }
+    print(json.dumps(line), flush=True)
+    if ws > 1:
+        torch.distributed.destroy_process_group()
+
+
+# ------------------------------------------------------------------ reference arm
+def reference_arm(args):
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return
+    import oracle
+    oracle.lib()
+    # one layer's first matrices, regenerated exactly as the GPU arm does
+    mats = {name: synth.q4_0_weights(N, K, seed=SEED, stream=mi, layer=0) for mi, (name, N, K) in enumerate(MATRICES)
+            if name in ("q", "k", "v")}
+    x = synth.activations(HIDDEN, seed=SEED, dtype="bf16")
+    rb = synth.row_bytes("q4_0", HIDDEN)
+    # size one step so that warmup + steps stay within about two minutes
+    t0 = time.time()
+    oracle.qmv_rows("q4_0", mats["q"], x, 0, 64, HIDDEN)
+    per_row = (time.time() - t0) / 64
+    step_s = min(1.0, 120.0 / max(1, args.steps + args.warmup))
+    rows = max(8, int(step_s / per_row))
+    rows = min(rows, QDIM)
+
+    def one_step():
+        oracle.qmv_rows("q4_0", mats["q"], x, 0, rows, HIDDEN)
+
+    for _ in range(args.warmup):
+        one_step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        one_step()
+    dt = time.perf_counter() - t0
+    nbytes = rows * rb
+    value = nbytes * args.steps / dt / 1e9
+    sample = (f"oracle qmv_q4_0 on the first {rows} rows of layer 0's q matrix (5376 inputs) per step, "
+              f"single-threaded")
+    line = {"impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": UNIT, "n_gpus": ws,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt * 1e3 / args.steps, 3),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": WORKLOAD, "sample_bytes_per_step": nbytes},
+            "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "cores": 1, "kind": "oracle", "sample": sample},
+            "e2e": {"value": round(value, 4), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=400)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["qbw", "reference"], default="qbw")
+    ap.add_argument("--no-kernels", action="store_true", help="skip the single-matrix supplementary numbers")
+    ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    if args.impl == "reference":
+        reference_arm(args)
+    else:
+        gpu_arm(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,172 @@
+"""block_quantized_weight_gb300 -- Python binding of libqbw, the C ABI declared
+in ``include/qbw.h`` (block-quantized GGUF Q8_0/Q4_0 matrix-vector products on
+GB300).
+
+This module only marshals arguments: it turns torch tensors into device
+pointers, dtype codes and the current CUDA stream, calls the C function of the
+same name and raises ``QbwError`` on a non-zero status.  Every step of the
+computation runs in the library's CUDA kernels; there is no CPU fallback, and
+importing a function whose library is missing raises immediately.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+__all__ = [
+    "QbwError", "load", "lib_path",
+    "qmv_q8_0", "qmv_q4_0", "qmv_gateup_q4_0", "qmm_q4_0_smallM", "qmm_q4_0_smallM_workspace_bytes",
+    "qdequant_q8_0", "qdequant_q4_0", "fault_read", "status_str", "version",
+    "F32", "BF16",
+]
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_LIB = os.path.join(_HERE, "_build", "libqbw.so")
+_lock = threading.Lock()
+_lib = None
+
+F32, BF16 = 0, 1
+QBW_OK = 0
+
+
+class QbwError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {status_str(status)}")
+
+
+def lib_path() -> str:
+    return _LIB
+
+
+def load():
+    """Load libqbw.so (raises if it has not been built)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(_LIB):
+                raise RuntimeError(f"libqbw.so is not built ({_LIB}); run "
+                                   "`python -m block_quantized_weight_gb300.build`")
+            L = ctypes.CDLL(_LIB)
+            _declare(L)
+            _lib = L
+    return _lib
+
+
+def _declare(L):
+    P, i64, i32, sz = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_size_t
+    L.qbw_status_str.restype = ctypes.c_char_p
+    L.qbw_status_str.argtypes = [i32]
+    L.qbw_version.restype = ctypes.c_uint32
+    L.qbw_version.argtypes = []
+    for name in ("qmv_q8_0", "qmv_q4_0"):
+        getattr(L, name).restype = i32
+        getattr(L, name).argtypes = [P, P, i32, P, i32, i64, i64, i64, P]
+    L.qmv_gateup_q4_0.restype = i32
+    L.qmv_gateup_q4_0.argtypes = [P, P, P, i32, P, i32, i64, i64, i64, P]
+    L.qmm_q4_0_smallM_workspace_bytes.restype = sz
+    L.qmm_q4_0_smallM_workspace_bytes.argtypes = [i64, i64, i64]
+    L.qmm_q4_0_smallM.restype = i32
+    L.qmm_q4_0_smallM.argtypes = [P, P, i32, P, i32, i64, i64, i64, P, sz, P]
+    for name in ("qdequant_q8_0", "qdequant_q4_0"):
+        getattr(L, name).restype = i32
+        getattr(L, name).argtypes = [P, P, i64, i64, P]
+    L.qbw_fault_read.restype = i32
+    L.qbw_fault_read.argtypes = [ctypes.POINTER(ctypes.c_uint32), i32, P]
+
+
+def status_str(status: int) -> str:
+    return load().qbw_status_str(int(status)).decode()
+
+
+def version() -> int:
+    return int(load().qbw_version())
+
+
+# ------------------------------------------------------------------ marshalling
+def _dtype_code(t) -> int:
+    import torch
+    if t.dtype == torch.float32:
+        return F32
+    if t.dtype == torch.bfloat16:
+        return BF16
+    return 99  # rejected by the library with QBW_EDTYPE
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(int(getattr(stream, "cuda_stream", stream)))
+
+
+def _check(status: int, where: str):
+    if status != QBW_OK:
+        raise QbwError(status, where)
+
+
+def qmv_q8_0(w, x, y, M: int, N: int, K: int, stream=None):
+    """y = W x for raw Q8_0 blocks ``w`` (uint8), activations ``x`` and outputs ``y`` (fp32/bf16)."""
+    L = load()
+    _check(L.qmv_q8_0(_ptr(w), _ptr(x), _dtype_code(x), _ptr(y), _dtype_code(y), M, N, K, _stream(stream)),
+           "qmv_q8_0")
+    return y
+
+
+def qmv_q4_0(w, x, y, M: int, N: int, K: int, stream=None):
+    """y = W x for raw Q4_0 blocks ``w`` (uint8)."""
+    L = load()
+    _check(L.qmv_q4_0(_ptr(w), _ptr(x), _dtype_code(x), _ptr(y), _dtype_code(y), M, N, K, _stream(stream)),
+           "qmv_q4_0")
+    return y
+
+
+def qmv_gateup_q4_0(w_gate, w_up, x, out, M: int, N: int, K: int, stream=None):
+    """out = gelu_tanh(Wg x) * (Wu x) for two raw Q4_0 matrices."""
+    L = load()
+    _check(L.qmv_gateup_q4_0(_ptr(w_gate), _ptr(w_up), _ptr(x), _dtype_code(x), _ptr(out), _dtype_code(out),
+                             M, N, K, _stream(stream)), "qmv_gateup_q4_0")
+    return out
+
+
+def qmm_q4_0_smallM_workspace_bytes(M: int, N: int, K: int) -> int:
+    return int(load().qmm_q4_0_smallM_workspace_bytes(M, N, K))
+
+
+def qmm_q4_0_smallM(w, X, Y, M: int, N: int, K: int, workspace=None, stream=None):
+    """Y[M, N] = X[M, K] W^T for raw Q4_0 blocks ``w`` on the tensor cores.
+
+    ``workspace`` is a zero-filled uint8 device tensor of at least
+    ``qmm_q4_0_smallM_workspace_bytes(M, N, K)`` bytes (left zero-filled).
+    """
+    L = load()
+    wbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(L.qmm_q4_0_smallM(_ptr(w), _ptr(X), _dtype_code(X), _ptr(Y), _dtype_code(Y), M, N, K,
+                             _ptr(workspace), wbytes, _stream(stream)), "qmm_q4_0_smallM")
+    return Y
+
+
+def qdequant_q8_0(w, out, N: int, K: int, stream=None):
+    L = load()
+    _check(L.qdequant_q8_0(_ptr(w), _ptr(out), N, K, _stream(stream)), "qdequant_q8_0")
+    return out
+
+
+def qdequant_q4_0(w, out, N: int, K: int, stream=None):
+    L = load()
+    _check(L.qdequant_q4_0(_ptr(w), _ptr(out), N, K, _stream(stream)), "qdequant_q4_0")
+    return out
+
+
+def fault_read(clear: bool = True, stream=None) -> int:
+    """Synchronize ``stream`` and return (and optionally clear) the device fault word."""
+    L = load()
+    code = ctypes.c_uint32(0)
+    _check(L.qbw_fault_read(ctypes.byref(code), 1 if clear else 0, _stream(stream)), "qbw_fault_read")
+    return int(code.value)

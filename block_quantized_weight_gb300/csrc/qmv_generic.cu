@@ -1,0 +1,164 @@
+// qmv_generic.cu -- the exact-but-plain kernels: the matrix-vector fallback for
+// shapes or alignments the streaming kernel does not take (K % 256 != 0, or a
+// weight pointer not 16-byte aligned), and the whole-matrix dequantizer.
+#include <cstdint>
+
+#include "qbw_device.cuh"
+#include "qbw_internal.h"
+
+namespace qbw {
+namespace {
+
+template <int FMT>
+__device__ __forceinline__ float code_at(const uint8_t* blk, int k) {
+    if constexpr (FMT == kFmtQ8) {
+        return (float)(int)(int8_t)blk[2 + k];
+    } else {
+        const uint32_t byte = blk[2 + (k & 15)];
+        const uint32_t code = (k < 16) ? (byte & 0x0Fu) : (byte >> 4);
+        return (float)((int)code - 8);
+    }
+}
+
+// One warp per output row; lane l takes blocks l, l+32, ...; byte loads only.
+template <int FMT, int NMAT>
+__global__ void __launch_bounds__(256) qmv_generic_kernel(const uint8_t* w0, const uint8_t* w1, const void* x,
+                                                          int x_bf16, void* y, int y_bf16, int64_t N, int64_t K) {
+    constexpr int BPB = (FMT == kFmtQ4) ? 18 : 34;
+    const int lane = threadIdx.x & 31;
+    const int64_t nb = K / 32;
+    const int64_t row_bytes = nb * BPB;
+    const int64_t warps = (int64_t)gridDim.x * (blockDim.x >> 5);
+    for (int64_t n = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); n < N; n += warps) {
+        float acc[NMAT];
+#pragma unroll
+        for (int m = 0; m < NMAT; ++m) acc[m] = 0.f;
+        for (int64_t b = lane; b < nb; b += 32) {
+#pragma unroll
+            for (int m = 0; m < NMAT; ++m) {
+                const uint8_t* blk = ((m == 0) ? w0 : w1) + n * row_bytes + b * BPB;
+                const float d = half_bits_to_float((uint32_t)blk[0] | ((uint32_t)blk[1] << 8));
+                float s = 0.f;
+                for (int k = 0; k < 32; ++k) {
+                    const int64_t i = b * 32 + k;
+                    const float xv = x_bf16 ? load_act<__nv_bfloat16>(x, i) : load_act<float>(x, i);
+                    s = fmaf(code_at<FMT>(blk, k), xv, s);
+                }
+                acc[m] = fmaf(d, s, acc[m]);
+            }
+        }
+        float v = 0.f;
+#pragma unroll
+        for (int m = 0; m < NMAT; ++m) {
+            float t = acc[m];
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
+            acc[m] = t;
+        }
+        v = acc[0];
+        if constexpr (NMAT == 2) v = gelu_tanh(acc[0]) * acc[1];
+        if (lane == 0) {
+            if (y_bf16) store_out<__nv_bfloat16>(y, n, v);
+            else store_out<float>(y, n, v);
+        }
+    }
+}
+
+// One thread per block: out[n*K + 32b + k] = d * code (exact in fp32).
+template <int FMT>
+__global__ void __launch_bounds__(256) dequant_kernel(const uint8_t* w, float* out, int64_t N, int64_t K) {
+    constexpr int BPB = (FMT == kFmtQ4) ? 18 : 34;
+    const int64_t nb = K / 32;
+    const int64_t total = N * nb;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
+         i += (int64_t)gridDim.x * blockDim.x) {
+        const uint8_t* blk = w + i * BPB;
+        const float d = half_bits_to_float((uint32_t)blk[0] | ((uint32_t)blk[1] << 8));
+        const int64_t n = i / nb, b = i - n * nb;
+        float* o = out + n * K + b * 32;
+#pragma unroll 8
+        for (int k = 0; k < 32; ++k) o[k] = d * code_at<FMT>(blk, k);
+    }
+}
+
+// Small-M fallback: one warp per weight row, X rows in groups of 8, exact
+// codes times bf16 activations in fp32, scale applied per block.
+__global__ void __launch_bounds__(256) qmm_generic_kernel(const uint8_t* w, const void* X, void* Y, int y_bf16,
+                                                          int64_t M, int64_t N, int64_t K) {
+    const int lane = threadIdx.x & 31;
+    const int64_t nb = K / 32;
+    const int64_t row_bytes = nb * 18;
+    const int64_t warps = (int64_t)gridDim.x * (blockDim.x >> 5);
+    for (int64_t n = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); n < N; n += warps) {
+        for (int64_t m0 = 0; m0 < M; m0 += 8) {
+            float acc[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) acc[i] = 0.f;
+            for (int64_t b = lane; b < nb; b += 32) {
+                const uint8_t* blk = w + n * row_bytes + b * 18;
+                const float d = half_bits_to_float((uint32_t)blk[0] | ((uint32_t)blk[1] << 8));
+                float s[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) s[i] = 0.f;
+                for (int k = 0; k < 32; ++k) {
+                    const float c = code_at<kFmtQ4>(blk, k);
+#pragma unroll
+                    for (int i = 0; i < 8; ++i)
+                        if (m0 + i < M) s[i] = fmaf(c, load_act<__nv_bfloat16>(X, (m0 + i) * K + b * 32 + k), s[i]);
+                }
+#pragma unroll
+                for (int i = 0; i < 8; ++i) acc[i] = fmaf(d, s[i], acc[i]);
+            }
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                float t = acc[i];
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
+                if (lane == 0 && m0 + i < M) {
+                    if (y_bf16) store_out<__nv_bfloat16>(Y, (m0 + i) * N + n, t);
+                    else store_out<float>(Y, (m0 + i) * N + n, t);
+                }
+            }
+        }
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_qmm_generic(const uint8_t* w, const void* X, void* Y, int y_bf16, int64_t M, int64_t N,
+                               int64_t K, int sm_count, cudaStream_t stream) {
+    const int64_t want = (N + 7) / 8;
+    const int ctas = (int)(want < (int64_t)sm_count * 8 ? want : (int64_t)sm_count * 8);
+    qmm_generic_kernel<<<ctas, 256, 0, stream>>>(w, X, Y, y_bf16, M, N, K);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_qmv_generic(int fmt, int nmat, const uint8_t* w0, const uint8_t* w1, const void* x,
+                               int x_bf16, void* y, int y_bf16, int64_t N, int64_t K, int sm_count,
+                               cudaStream_t stream) {
+    const int threads = 256;
+    const int64_t want = (N + 7) / 8;
+    const int ctas = (int)(want < (int64_t)sm_count * 8 ? want : (int64_t)sm_count * 8);
+    if (fmt == kFmtQ8)
+        qmv_generic_kernel<kFmtQ8, 1><<<ctas, threads, 0, stream>>>(w0, w1, x, x_bf16, y, y_bf16, N, K);
+    else if (nmat == 1)
+        qmv_generic_kernel<kFmtQ4, 1><<<ctas, threads, 0, stream>>>(w0, w1, x, x_bf16, y, y_bf16, N, K);
+    else
+        qmv_generic_kernel<kFmtQ4, 2><<<ctas, threads, 0, stream>>>(w0, w1, x, x_bf16, y, y_bf16, N, K);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_dequant(int fmt, const uint8_t* w, float* out, int64_t N, int64_t K, int sm_count,
+                           cudaStream_t stream) {
+    const int threads = 256;
+    const int64_t blocks = N * (K / 32);
+    const int64_t want = (blocks + threads - 1) / threads;
+    const int ctas = (int)(want < (int64_t)sm_count * 16 ? want : (int64_t)sm_count * 16);
+    if (fmt == kFmtQ8)
+        dequant_kernel<kFmtQ8><<<ctas, threads, 0, stream>>>(w, out, N, K);
+    else
+        dequant_kernel<kFmtQ4><<<ctas, threads, 0, stream>>>(w, out, N, K);
+    return cudaGetLastError();
+}
+
+}  // namespace qbw

@@ -1,0 +1,174 @@
+/*
+ * qbw.h -- block-quantized weight matrix-vector products for NVIDIA GB300
+ * (sm_103a).  C ABI: plain pointers, sizes and an opaque CUDA stream.
+ *
+ * Weights are raw GGUF block bytes, exactly as a GGUF file stores them:
+ *
+ *   Q8_0 block, 34 bytes: fp16 scale d (little-endian), then 32 int8 codes q;
+ *        weight = d * q.
+ *   Q4_0 block, 18 bytes: fp16 scale d, then 16 bytes qs; code j (0..15) is the
+ *        low nibble of qs[j], code j+16 the high nibble; weight = d * (code - 8).
+ *
+ * (gem docs/research/architecture.md, "M4 Max operating assumptions": Q4_0 is
+ * the "32-element/18-byte block" the decode matrix-vector kernel streams, Q8_0
+ * the token-table and quality-baseline format.  The nibble order is the GGUF
+ * block_q4_0 record's.)
+ *
+ * A weight matrix W with N output rows and K inputs (K a multiple of 32) is N
+ * rows of K/32 consecutive blocks, rows back to back with no padding: the
+ * [out, in] row-major layout of a linear layer (SafeC Gemma 4 design notes,
+ * "Math primitives implementation status").  Row n holds output n's weights.
+ *
+ * Activations are fp32 or bf16 (QBW_F32 / QBW_BF16); they are never quantized.
+ * Products accumulate in fp32.
+ *
+ * Pointers.  Every w, x, y, out, X, Y, workspace pointer is a DEVICE pointer
+ * (or managed memory) on the current CUDA device.  The caller owns every
+ * buffer: the library allocates nothing, frees nothing and keeps no pointer
+ * after a call returns.  Outputs must not overlap inputs.
+ *
+ * Streams.  `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ * stream).  Work is enqueued asynchronously; a call never synchronizes.
+ *
+ * Errors.  Arguments are validated on the host before anything is launched; a
+ * rejected call returns its status and launches nothing.  After a launch,
+ * cudaGetLastError() != cudaSuccess returns QBW_ECUDA.  Errors raised while a
+ * kernel runs surface at the caller's next synchronization, as with any CUDA
+ * call.  There is no CPU fallback.
+ *
+ * Determinism.  Each kernel reduces in a fixed order: identical inputs give
+ * bit-identical outputs from run to run.
+ *
+ * Fast path.  When K % 256 == 0 and the weight pointers are 16-byte aligned,
+ * rows are streamed with bulk asynchronous copies; any other K % 32 == 0 shape
+ * or alignment takes a slower, equally exact path.
+ */
+#ifndef QBW_H
+#define QBW_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum qbw_dtype {
+    QBW_F32 = 0,   /* IEEE fp32 */
+    QBW_BF16 = 1   /* bfloat16 */
+} qbw_dtype;
+
+typedef enum qbw_status {
+    QBW_OK = 0,
+    QBW_EINVAL = 1,      /* null pointer or otherwise invalid argument */
+    QBW_ESHAPE = 2,      /* M, N or K out of range, or K % 32 != 0 */
+    QBW_EDTYPE = 3,      /* activation or output dtype not supported here */
+    QBW_EALIGN = 4,      /* activation/output pointer not aligned to its dtype */
+    QBW_ECUDA = 5,       /* a CUDA runtime call or a launch failed */
+    QBW_EWORKSPACE = 6,  /* workspace missing, too small or misaligned */
+    QBW_EDEVICE = 7      /* the current device is not a compute capability 10.3 GPU */
+} qbw_status;
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char *qbw_status_str(qbw_status s);
+
+/* Library ABI version, (major << 16) | minor. */
+uint32_t qbw_version(void);
+
+/*
+ * qmv_q8_0 -- y = W x for a Q8_0 weight matrix, one token (M == 1).
+ *
+ * The decode-step matrix-vector product: every weight byte is read once per
+ * token (SafeC Gemma 4 design notes, "Batched decode"; jouleclaw-loader-gguf
+ * BENCHMARKS, "Matmul throughput -- Q8_0 scalar vs NEON").
+ *
+ *   w  : N * (K/32) * 34 bytes of Q8_0 blocks, any alignment
+ *   x  : K activations of dtype xt, aligned to the dtype
+ *   y  : N outputs of dtype yt (QBW_F32 or QBW_BF16; bf16 is rounded to
+ *        nearest-even from the fp32 accumulator)
+ *   M  : must be 1                         (else QBW_ESHAPE)
+ *   N  : 1 .. 2^31-1, K: 32 .. 2^24, K % 32 == 0   (else QBW_ESHAPE)
+ */
+qbw_status qmv_q8_0(const void *w, const void *x, qbw_dtype xt, void *y, qbw_dtype yt,
+                    int64_t M, int64_t N, int64_t K, void *stream);
+
+/*
+ * qmv_q4_0 -- y = W x for a Q4_0 weight matrix, one token (M == 1).
+ *
+ * The bandwidth-bound decode projection (gem docs/research/architecture.md,
+ * "M4 Max operating assumptions" and the "dedicated four-output-row
+ * matrix-vector path" of "Ownership boundaries").  Arguments as qmv_q8_0,
+ * with w holding N * (K/32) * 18 bytes of Q4_0 blocks.
+ */
+qbw_status qmv_q4_0(const void *w, const void *x, qbw_dtype xt, void *y, qbw_dtype yt,
+                    int64_t M, int64_t N, int64_t K, void *stream);
+
+/*
+ * qmv_gateup_q4_0 -- out = gelu_tanh(Wg x) * (Wu x), one pass over both
+ * matrices, one token (M == 1).
+ *
+ * The gated FFN's gate and up projections fused with its activation, where
+ * gelu_tanh(v) = 0.5 v (1 + tanh(sqrt(2/pi) (v + 0.044715 v^3))) (SafeC Gemma
+ * 4 design notes, "Gated FFN"; fusing gate and up into one dispatch:
+ * "Performance optimizations: fusion ..."; the GPU-chained gated GELU and its
+ * large-gate regression: "Further optimization: QKV projection fusion, fully
+ * GPU-chained FFN").
+ *
+ *   w_gate, w_up : two Q4_0 matrices of N rows and K inputs each.  A fused
+ *                  [gate ; up] buffer works too: pass w_up = w_gate + N*K/32*18.
+ *   x            : K activations (xt);   out : N outputs (ot)
+ *   M == 1; N, K as for qmv_q4_0.
+ */
+qbw_status qmv_gateup_q4_0(const void *w_gate, const void *w_up, const void *x, qbw_dtype xt,
+                           void *out, qbw_dtype ot, int64_t M, int64_t N, int64_t K, void *stream);
+
+/*
+ * qmm_q4_0_smallM -- Y = X W^T for a few token rows (prefill tiles), on the
+ * tensor cores.
+ *
+ * Prompt tiles of up to 32 tokens share one read of each Q4_0 weight and run
+ * on matrix units (gem docs/research/architecture.md, "Ownership
+ * boundaries"); dequantize-then-matrix-unit wins from m of about 8
+ * (jouleclaw-loader-gguf BENCHMARKS, "Q8_0 matmul -- NEON direct vs
+ * AMX-tiled").  Weights are dequantized to bf16 on chip and multiplied in
+ * bf16 with fp32 accumulation.
+ *
+ *   w : Q4_0 matrix, N rows x K inputs        X : [M, K] row-major, QBW_BF16
+ *   Y : [M, N] row-major, QBW_BF16 or QBW_F32
+ *   M : 1 .. 32 (tuned for 8, 16, 32)          N >= 1, K % 32 == 0
+ *   workspace : device scratch of at least
+ *               qmm_q4_0_smallM_workspace_bytes(M, N, K) bytes, 256-byte
+ *               aligned, ZERO-FILLED before its first use; every call leaves
+ *               it zero-filled again.  Calls that share one workspace must
+ *               not run concurrently.  May be NULL when the size query
+ *               returns 0.
+ */
+size_t qmm_q4_0_smallM_workspace_bytes(int64_t M, int64_t N, int64_t K);
+qbw_status qmm_q4_0_smallM(const void *w, const void *X, qbw_dtype xt, void *Y, qbw_dtype yt,
+                           int64_t M, int64_t N, int64_t K, void *workspace, size_t workspace_bytes,
+                           void *stream);
+
+/*
+ * qdequant_q8_0 / qdequant_q4_0 -- expand a whole matrix to fp32:
+ * out[n*K + k] = w[n, k].  Every product d*q is exact in fp32, so the result is
+ * bit-exact.  Meant for testing and inspection, not for the hot path.
+ *
+ *   w : N rows of K/32 blocks, any alignment;   out : N*K floats, 4-byte aligned
+ */
+qbw_status qdequant_q8_0(const void *w, float *out, int64_t N, int64_t K, void *stream);
+qbw_status qdequant_q4_0(const void *w, float *out, int64_t N, int64_t K, void *stream);
+
+/*
+ * qbw_fault_read -- read the library's device fault word for the current
+ * device.  A kernel whose bounded wait for an asynchronous copy runs out (about
+ * two seconds) writes a nonzero code here and returns early instead of
+ * hanging; outputs of that call are then undefined.  Synchronizes `stream`,
+ * stores the word in *code and, if clear != 0, resets it to zero.
+ */
+qbw_status qbw_fault_read(uint32_t *code, int clear, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* QBW_H */

@@ -1,0 +1,118 @@
+"""The C ABI on the CPU: the library loads, exports every entry point that
+include/qbw.h declares, and rejects invalid arguments on the host before
+touching a GPU (validation returns before any CUDA call)."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+from conftest import ROOT
+
+HEADER = os.path.join(ROOT, "include", "qbw.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    import block_quantized_weight_gb300 as qbw
+    if not os.path.exists(qbw.lib_path()):
+        from block_quantized_weight_gb300 import build as b
+        b.build()
+    return qbw.load()
+
+
+def declared_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?[\w\s\*]+?\b(\w+)\s*\(", src, flags=re.M)) - {"if"})
+
+
+def test_header_declares_the_entry_points():
+    names = declared_functions()
+    for n in ("qmv_q8_0", "qmv_q4_0", "qmv_gateup_q4_0", "qmm_q4_0_smallM", "qmm_q4_0_smallM_workspace_bytes",
+              "qdequant_q8_0", "qdequant_q4_0", "qbw_status_str", "qbw_version", "qbw_fault_read"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    import block_quantized_weight_gb300 as qbw
+    out = subprocess.run(["nm", "-D", "--defined-only", qbw.lib_path()], capture_output=True, text=True).stdout
+    exported = {line.split()[-1] for line in out.splitlines() if line.strip()}
+    for n in declared_functions():
+        assert n in exported, n
+        assert getattr(lib, n) is not None
+
+
+def test_library_has_no_oracle_code(lib):
+    import block_quantized_weight_gb300 as qbw
+    out = subprocess.run(["nm", "-D", qbw.lib_path()], capture_output=True, text=True).stdout
+    assert "oracle" not in out
+    csrc = os.path.join(ROOT, "block_quantized_weight_gb300", "csrc")
+    for f in os.listdir(csrc):
+        assert "oracle" not in open(os.path.join(csrc, f)).read().lower(), f
+
+
+def test_status_strings(lib):
+    import block_quantized_weight_gb300 as qbw
+    for s in range(8):
+        assert qbw.status_str(s).startswith("QBW_")
+    assert qbw.version() >= 0x10000
+
+
+F32, BF16 = 0, 1
+P = ctypes.c_void_p
+ADDR = 0x7F0000000000  # never dereferenced: every case below fails validation first
+
+
+def qmv(lib, name, w=ADDR, x=ADDR + (1 << 30), xt=F32, y=ADDR + (2 << 30), yt=F32, M=1, N=16, K=256):
+    return getattr(lib, name)(P(w) if w else None, P(x) if x else None, xt, P(y) if y else None, yt, M, N, K, None)
+
+
+@pytest.mark.parametrize("name", ["qmv_q8_0", "qmv_q4_0"])
+def test_qmv_validation(lib, name):
+    assert qmv(lib, name, w=0) == 1
+    assert qmv(lib, name, x=0) == 1
+    assert qmv(lib, name, y=0) == 1
+    assert qmv(lib, name, xt=7) == 3
+    assert qmv(lib, name, yt=-1) == 3
+    assert qmv(lib, name, M=2) == 2
+    assert qmv(lib, name, M=0) == 2
+    assert qmv(lib, name, N=0) == 2
+    assert qmv(lib, name, K=0) == 2
+    assert qmv(lib, name, K=48) == 2
+    assert qmv(lib, name, K=1 << 25) == 2
+    assert qmv(lib, name, N=1 << 31) == 2
+    assert qmv(lib, name, x=ADDR + (1 << 30) + 2, xt=F32) == 4
+    assert qmv(lib, name, y=ADDR + (2 << 30) + 1, yt=BF16) == 4
+    # output overlapping the activations or the weights
+    assert qmv(lib, name, y=ADDR + (1 << 30) + 64) == 1
+    assert qmv(lib, name, y=ADDR + 16) == 1
+
+
+def test_gateup_validation(lib):
+    f = lib.qmv_gateup_q4_0
+    a, b, x, y = ADDR, ADDR + (1 << 28), ADDR + (1 << 30), ADDR + (2 << 30)
+    assert f(P(a), None, P(x), F32, P(y), F32, 1, 16, 256, None) == 1
+    assert f(P(a), P(b), P(x), F32, P(y), F32, 3, 16, 256, None) == 2
+    assert f(P(a), P(b), P(x), F32, P(b + 8), F32, 1, 16, 256, None) == 1
+
+
+def test_qmm_validation(lib):
+    f = lib.qmm_q4_0_smallM
+    w, X, Y = ADDR, ADDR + (1 << 30), ADDR + (2 << 30)
+    assert f(None, P(X), BF16, P(Y), BF16, 8, 64, 256, None, 0, None) == 1
+    assert f(P(w), P(X), F32, P(Y), BF16, 8, 64, 256, None, 0, None) == 3
+    assert f(P(w), P(X), BF16, P(Y), BF16, 0, 64, 256, None, 0, None) == 2
+    assert f(P(w), P(X), BF16, P(Y), BF16, 33, 64, 256, None, 0, None) == 2
+    assert f(P(w), P(X), BF16, P(Y), BF16, 8, 64, 100, None, 0, None) == 2
+    assert f(P(w), P(X + 1), BF16, P(Y), BF16, 8, 64, 256, None, 0, None) == 4
+
+
+def test_dequant_validation(lib):
+    for name in ("qdequant_q8_0", "qdequant_q4_0"):
+        f = getattr(lib, name)
+        assert f(None, P(ADDR + (1 << 30)), 4, 64, None) == 1
+        assert f(P(ADDR), P(ADDR + (1 << 30)), 4, 40, None) == 2
+        assert f(P(ADDR), P(ADDR + (1 << 30) + 2), 4, 64, None) == 4
+        assert f(P(ADDR), P(ADDR + 8), 4, 64, None) == 1
