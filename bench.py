@@ -524,6 +524,66 @@ def gpu_arm(args):
         torch.distributed.destroy_process_group()
 
 
+def profile_case(args):
+    """A small, self-contained run of one kernel for profiler captures: the
+    single-matrix workload named by --profile, ``warmup + steps`` calls over
+    a few rotating weight copies (well under 1 GB on the device)."""
+    import torch
+    import block_quantized_weight_gb300 as qbw
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
+    qbw.load()
+    name = args.profile
+    copies = 4
+    if name == "q8_0":
+        N = K = 2048
+        ws = [torch.from_numpy(synth.q8_0_weights(N, K, seed=0)).to(dev) for _ in range(copies)]
+        x = torch.from_numpy(synth.activations(K, seed=0)).to(dev)
+        y = torch.empty(N, device=dev)
+        call = lambda i: qbw.qmv_q8_0(ws[i % copies], x, y, 1, N, K)
+        nbytes = ws[0].numel() + 4 * K + 4 * N
+    elif name == "q4_0":
+        N, K = 21504, 5376
+        ws = [torch.from_numpy(synth.q4_0_weights(N, K, seed=1)).to(dev) for _ in range(copies)]
+        x = torch.from_numpy(synth.activations(K, seed=1)).to(dev)
+        y = torch.empty(N, device=dev)
+        call = lambda i: qbw.qmv_q4_0(ws[i % copies], x, y, 1, N, K)
+        nbytes = ws[0].numel() + 4 * K + 4 * N
+    elif name == "gateup":
+        N, K = 21504, 5376
+        wg = [torch.from_numpy(synth.q4_0_weights(N, K, seed=2, stream=0)).to(dev) for _ in range(2)]
+        wu = [torch.from_numpy(synth.q4_0_weights(N, K, seed=2, stream=1)).to(dev) for _ in range(2)]
+        xb = torch.from_numpy(synth.activations(K, seed=2, dtype="bf16").view(np.int16).copy()).view(
+            torch.bfloat16).to(dev)
+        y = torch.empty(N, device=dev)
+        call = lambda i: qbw.qmv_gateup_q4_0(wg[i % 2], wu[i % 2], xb, y, 1, N, K)
+        nbytes = 2 * wg[0].numel() + 2 * K + 4 * N
+    elif name == "qmm":
+        M, N, K = 32, 5376, 21504
+        ws = [torch.from_numpy(synth.q4_0_weights(N, K, seed=3)).to(dev) for _ in range(copies)]
+        X = torch.from_numpy(synth.activations((M, K), seed=3, dtype="bf16").view(np.int16).copy()).view(
+            torch.bfloat16).to(dev)
+        Y = torch.empty(M, N, dtype=torch.bfloat16, device=dev)
+        work = torch.zeros(max(1, qbw.qmm_q4_0_smallM_workspace_bytes(M, N, K)), dtype=torch.uint8, device=dev)
+        call = lambda i: qbw.qmm_q4_0_smallM(ws[i % copies], X, Y, M, N, K, work)
+        nbytes = ws[0].numel() + 2 * M * K + 2 * M * N
+    else:
+        raise SystemExit(f"unknown --profile case {name}")
+    for i in range(args.warmup):
+        call(i)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for i in range(args.steps):
+        call(args.warmup + i)
+    e1.record()
+    torch.cuda.synchronize()
+    us = e0.elapsed_time(e1) * 1e3 / args.steps
+    assert qbw.fault_read(clear=True) == 0, "a kernel recorded a fault"
+    print(json.dumps({"profile_case": name, "calls": args.steps, "us_per_call": round(us, 3),
+                      "GB_per_s": round(nbytes / (us * 1e3), 1)}), flush=True)
+
+
 # ------------------------------------------------------------------ reference arm
 def reference_arm(args):
     ws, rank, _ = dist_env()
@@ -575,7 +635,12 @@ def main():
     ap.add_argument("--no-kernels", action="store_true", help="skip the single-matrix supplementary numbers")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--profile", choices=["q8_0", "q4_0", "gateup", "qmm"],
+                    help="run only one small single-matrix case (for profiler captures)")
     args = ap.parse_args()
+    if args.profile:
+        profile_case(args)
+        return
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
     if args.impl == "reference":

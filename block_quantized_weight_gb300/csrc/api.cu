@@ -96,8 +96,7 @@ bool plan_stream(int fmt, int nmat, int64_t N, int64_t K, const DeviceInfo& di, 
     const int nfull = (int)(npairs / 32);
     const int tail = (int)(npairs % 32);
     const size_t xs_bytes = (size_t)K * 4;
-    const size_t corr_bytes = (fmt == kFmtQ4) ? (size_t)npairs * 8 : 0;
-    const size_t fixed = align_up(xs_bytes + corr_bytes, 128);
+    const size_t fixed = align_up(xs_bytes, 128);
     const int Rs_1[] = {8, 4, 2, 1};
     const int Rs_2[] = {4, 2, 1};
     const int* Rs = (nmat == 2) ? Rs_2 : Rs_1;
@@ -150,7 +149,6 @@ bool plan_stream(int fmt, int nmat, int64_t N, int64_t K, const DeviceInfo& di, 
     p.nfull = nfull;
     p.tail_pairs = tail;
     p.depth = out->depth;
-    p.corr_off = (uint32_t)xs_bytes;
     p.ring_off = (uint32_t)fixed;
     p.stage_bytes = (uint32_t)((size_t)nmat * out->R * chunk_bytes(fmt));
     p.bar_off = (uint32_t)(fixed + (size_t)out->warps * out->depth * p.stage_bytes);

@@ -36,7 +36,6 @@ struct StreamParams {
     int32_t y_bf16;        // outputs are bf16 (else fp32)
     uint32_t ring_off;     // byte offsets inside dynamic shared memory
     uint32_t bar_off;
-    uint32_t corr_off;
     uint32_t stage_bytes;  // NMAT * R * chunk bytes
 };
 

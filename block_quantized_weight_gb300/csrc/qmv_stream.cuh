@@ -21,15 +21,14 @@
 //
 // Code -> fp32 without an integer-to-float instruction: a code sitting at bit
 // p of a word is masked and OR-ed with the exponent of 2^(23-p), which is the
-// float 2^(23-p) + code exactly; subtracting 2^(23-p) (packed fp32x2 add)
-// leaves the code.  Q4_0 codes at bit 16 keep a +128 offset instead, folded
-// into a per-block correction computed with the staged activations.  Q8_0
-// bytes are flipped to offset binary (q + 128) inside the same LOP3, and the
-// subtraction removes 2^(23-p) + 128.
+// float 2^(23-p) + code exactly (p = 16 gives 128 + code); one packed fp32x2
+// add of -(2^(23-p) + 8) then leaves exactly code - 8, the Q4_0 weight over
+// its scale.  Q8_0 bytes are flipped to offset binary (q + 128) inside the
+// same LOP3 and the add removes 2^(23-p) + 128, leaving exactly q.  Every
+// product code * x is therefore the exact weight-over-scale times x, and a
+// block whose weights are all zero contributes exactly zero.
 //
-// Per block: y += d * (sum_j f_j x_j - corr), f_j the decoded code, with
-// corr = 8 * sum_j x_j + 128 * (sum of x_j over the +128 slots) for Q4_0
-// (w = d (q - 8)) and corr = 0 for Q8_0 (w = d q).
+// Per block: y += d * sum_j c_j x_j, accumulated in fp32 (packed pairs).
 #pragma once
 
 #include <cstdint>
@@ -46,14 +45,12 @@ template <>
 struct Fmt<kFmtQ4> {
     static constexpr int kPairBytes = pair_bytes(kFmtQ4);
     static constexpr int kChunkBytes = chunk_bytes(kFmtQ4);
-    static constexpr bool kHasCorr = true;
 };
 
 template <>
 struct Fmt<kFmtQ8> {
     static constexpr int kPairBytes = pair_bytes(kFmtQ8);
     static constexpr int kChunkBytes = chunk_bytes(kFmtQ8);
-    static constexpr bool kHasCorr = false;
 };
 
 // ---------------------------------------------------------------- slot order
@@ -65,7 +62,6 @@ struct Fmt<kFmtQ8> {
 // j..j+3 of block X gives two chunks:
 //   L: codes at bits 0, 4, 8, 12          -> X(j), X(16+j), X(j+1), X(17+j)
 //   H: codes at bits 20, 24, 16, 28       -> X(18+j), X(j+3), X(j+2), X(19+j)
-//      (the last two keep their +128 offset)
 // Chunk 0 = H(V0) (qs bytes 0, 1 at the top of the word, i.e. j = -2),
 // chunks 1..6 = L,H of V1..V3, chunk 7 = L(V4) (j = 14), chunks 8..15 = L,H
 // of V5..V8.
@@ -79,22 +75,15 @@ __host__ __device__ constexpr bool q4_chunk_loads_word(int c) {
     return c == 0 || c == 7 || (c < 7 ? (c - 1) % 2 == 0 : (c - 8) % 2 == 0);
 }
 
-// Element (0..63) of the pair multiplied by slot `slot`; *plus128 tells
-// whether that slot's decoded code carries the +128 offset.
-__host__ __device__ constexpr int q4_slot_element(int slot, bool* plus128) {
+// Element (0..63) of the pair multiplied by slot `slot`.
+__host__ __device__ constexpr int q4_slot_element(int slot) {
     const int c = slot >> 2, i = slot & 3;
     const int w = q4_chunk_word(c);
     const int blk = (c >= 8) ? 1 : 0;
     const int j0 = (c == 0) ? -2 : (blk ? 4 * (w - 5) : 4 * w - 2);
     int e = 0;
-    bool off = false;
-    if (!q4_chunk_is_h(c)) {
-        e = (i == 0) ? j0 : (i == 1) ? 16 + j0 : (i == 2) ? j0 + 1 : 17 + j0;
-    } else {
-        e = (i == 0) ? 18 + j0 : (i == 1) ? j0 + 3 : (i == 2) ? j0 + 2 : 19 + j0;
-        off = (i >= 2);
-    }
-    if (plus128) *plus128 = off;
+    if (!q4_chunk_is_h(c)) e = (i == 0) ? j0 : (i == 1) ? 16 + j0 : (i == 2) ? j0 + 1 : 17 + j0;
+    else e = (i == 0) ? 18 + j0 : (i == 1) ? j0 + 3 : (i == 2) ? j0 + 2 : 19 + j0;
     return blk * 32 + e;
 }
 
@@ -117,20 +106,22 @@ __device__ __forceinline__ uint32_t lop3_select(uint32_t a, uint32_t b, uint32_t
     return r;
 }
 
-// Q4_0 L chunk of word v: codes at bits 0, 4, 8, 12 -> exact floats.
+// Q4_0 L chunk of word v: codes at bits 0, 4, 8, 12 -> exact (code - 8).
 __device__ __forceinline__ void q4_chunk_L(uint32_t v, uint64_t& fa, uint64_t& fb) {
-    const uint64_t k01 = 0xC9000000CB000000ull;   // (-2^23, -2^19)
-    const uint64_t k23 = 0xC5000000C7000000ull;   // (-2^15, -2^11)
+    const uint64_t k01 = 0xC9000080CB000008ull;   // (-(2^23 + 8), -(2^19 + 8))
+    const uint64_t k23 = 0xC5008000C7000800ull;   // (-(2^15 + 8), -(2^11 + 8))
     fa = fadd2(pack2((v & 0x0000000Fu) | 0x4B000000u, (v & 0x000000F0u) | 0x49000000u), k01);
     fb = fadd2(pack2((v & 0x00000F00u) | 0x47000000u, (v & 0x0000F000u) | 0x45000000u), k23);
 }
 
-// Q4_0 H chunk of word v: codes at bits 20, 24 exact; bits 16, 28 as 128 + code.
+// Q4_0 H chunk of word v: codes at bits 20, 24 (shifted to 8, 12) and 16, 28
+// (16 in place, 28 shifted to 16) -> exact (code - 8).
 __device__ __forceinline__ void q4_chunk_H(uint32_t v, uint64_t& fa, uint64_t& fb) {
-    const uint64_t k23 = 0xC5000000C7000000ull;   // (-2^15, -2^11)
+    const uint64_t k23 = 0xC5008000C7000800ull;   // (-(2^15 + 8), -(2^11 + 8))
+    const uint64_t k16 = 0xC3080000C3080000ull;   // (-(128 + 8), -(128 + 8))
     const uint32_t s = v >> 12;
     fa = fadd2(pack2((s & 0x00000F00u) | 0x47000000u, (s & 0x0000F000u) | 0x45000000u), k23);
-    fb = pack2((v & 0x000F0000u) | 0x43000000u, (s & 0x000F0000u) | 0x43000000u);
+    fb = fadd2(pack2((v & 0x000F0000u) | 0x43000000u, (s & 0x000F0000u) | 0x43000000u), k16);
 }
 
 // Q8_0: the signed bytes 0 and 1 of word v -> exact floats.
@@ -146,7 +137,7 @@ __device__ __forceinline__ uint64_t q8_bytes01(uint32_t v) {
 // rowaddr(m, r) is the shared-memory address of the pair in row (m, r).
 template <int FMT, int NMAT, int NR, typename RowAddr>
 __device__ __forceinline__ void pair_dot(const RowAddr& rowaddr, uint32_t xaddr, uint32_t swz,
-                                         float2 corr, float (&acc)[NMAT][NR]) {
+                                         float (&acc)[NMAT][NR]) {
     uint64_t bacc[NMAT][NR];
     uint32_t vw[NMAT][NR];
     uint32_t dA[NMAT][NR], dB[NMAT][NR];
@@ -191,8 +182,7 @@ __device__ __forceinline__ void pair_dot(const RowAddr& rowaddr, uint32_t xaddr,
                 ffma2(bacc[m][r], fb, x23);
                 if (c == 7 || c == 15) {
                     const float2 s = unpack2f(bacc[m][r]);
-                    float t = s.x + s.y;
-                    if constexpr (Fmt<FMT>::kHasCorr) t -= (c == 7) ? corr.x : corr.y;
+                    const float t = s.x + s.y;
                     const float d = half_bits_to_float(c == 7 ? dA[m][r] : dB[m][r]);
                     acc[m][r] = fmaf(d, t, acc[m][r]);
                     bacc[m][r] = 0ull;
@@ -207,35 +197,20 @@ __device__ __forceinline__ float warp_sum(float v) {
     return v;
 }
 
-// Stage the activations in slot order (64 fp32 per pair, 16-byte chunks
+// Stage the activations in slot order: 64 fp32 per pair, 16-byte chunks
 // XOR-swizzled by pair index so that 8 lanes reading 8 consecutive pairs hit 8
-// distinct bank groups) and, for Q4_0, the two per-block corrections per pair.
+// distinct bank groups.
 template <int FMT>
 __device__ __forceinline__ void stage_activations(const StreamParams& p, uint8_t* smem) {
+    float* xs = reinterpret_cast<float*>(smem);
     for (int q = threadIdx.x; q < p.npairs; q += blockDim.x) {
         const uint32_t swz = (uint32_t)q & 7u;
-        double sumA = 0.0, sumB = 0.0, offA = 0.0, offB = 0.0;
 #pragma unroll 4
         for (int s = 0; s < 64; ++s) {
-            bool plus128 = false;
-            const int e = (FMT == kFmtQ4) ? q4_slot_element(s, &plus128) : q8_slot_element(s);
+            const int e = (FMT == kFmtQ4) ? q4_slot_element(s) : q8_slot_element(s);
             const int64_t k = (int64_t)q * 64 + e;
             const float xv = p.x_bf16 ? load_act<__nv_bfloat16>(p.x, k) : load_act<float>(p.x, k);
-            const uint32_t off = (uint32_t)q * 256u + ((((uint32_t)(s >> 2)) ^ swz) << 4) + 4u * (uint32_t)(s & 3);
-            reinterpret_cast<float*>(smem)[off >> 2] = xv;
-            if (e < 32) {
-                sumA += xv;
-                if (plus128) offA += xv;
-            } else {
-                sumB += xv;
-                if (plus128) offB += xv;
-            }
-        }
-        if constexpr (Fmt<FMT>::kHasCorr) {
-            float2 cr;
-            cr.x = (float)(8.0 * sumA + 128.0 * offA);
-            cr.y = (float)(8.0 * sumB + 128.0 * offB);
-            reinterpret_cast<float2*>(smem + p.corr_off)[q] = cr;
+            xs[q * 64 + (int)((((uint32_t)(s >> 2)) ^ swz) << 2) + (s & 3)] = xv;
         }
     }
 }
@@ -253,7 +228,6 @@ __global__ void __launch_bounds__(512, 1) qmv_stream_kernel(const StreamParams p
 
     const uint32_t sbase = smem_u32(smem);
     const uint32_t xs = sbase;                                    // 64 fp32 per pair
-    const uint32_t corr_s = sbase + p.corr_off;                   // float2 per pair (Q4_0)
     const uint32_t ring = sbase + p.ring_off + (uint32_t)warp * (uint32_t)D * p.stage_bytes;
     const uint32_t bars = sbase + p.bar_off + (uint32_t)warp * (uint32_t)D * 8u;
 
@@ -314,12 +288,10 @@ __global__ void __launch_bounds__(512, 1) qmv_stream_kernel(const StreamParams p
         if (c < p.nfull) {
             const int q = c * 32 + lane;
             const uint32_t poff = (uint32_t)lane * (uint32_t)F::kPairBytes;
-            float2 cr = make_float2(0.f, 0.f);
-            if constexpr (F::kHasCorr) cr = lds64f(corr_s + 8u * (uint32_t)q);
             auto rowaddr = [&](int m, int r) {
                 return stage + (uint32_t)(m * R + r) * (uint32_t)F::kChunkBytes + poff;
             };
-            pair_dot<FMT, NMAT, R>(rowaddr, xs + (uint32_t)q * 256u, (uint32_t)q & 7u, cr, acc);
+            pair_dot<FMT, NMAT, R>(rowaddr, xs + (uint32_t)q * 256u, (uint32_t)q & 7u, acc);
         } else {
             // tail chunk: (row, pair) items spread over the lanes
             const int items = R * p.tail_pairs;
@@ -327,8 +299,6 @@ __global__ void __launch_bounds__(512, 1) qmv_stream_kernel(const StreamParams p
                 const int r = it / p.tail_pairs;
                 const int qq = it - r * p.tail_pairs;
                 const int q = c * 32 + qq;
-                float2 cr = make_float2(0.f, 0.f);
-                if constexpr (F::kHasCorr) cr = lds64f(corr_s + 8u * (uint32_t)q);
                 float part[NMAT][1];
 #pragma unroll
                 for (int m = 0; m < NMAT; ++m) part[m][0] = 0.f;
@@ -336,7 +306,7 @@ __global__ void __launch_bounds__(512, 1) qmv_stream_kernel(const StreamParams p
                     return stage + (uint32_t)(m * R + r) * (uint32_t)F::kChunkBytes +
                            (uint32_t)qq * (uint32_t)F::kPairBytes;
                 };
-                pair_dot<FMT, NMAT, 1>(rowaddr, xs + (uint32_t)q * 256u, (uint32_t)q & 7u, cr, part);
+                pair_dot<FMT, NMAT, 1>(rowaddr, xs + (uint32_t)q * 256u, (uint32_t)q & 7u, part);
 #pragma unroll
                 for (int m = 0; m < NMAT; ++m)
 #pragma unroll
