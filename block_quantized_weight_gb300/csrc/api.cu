@@ -7,9 +7,11 @@
 #include <cstring>
 #include <mutex>
 
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 
-#include "../../include/qbw.h"
+#include "qbw.h"
 #include "qbw_internal.h"
 
 namespace qbw {
@@ -87,71 +89,118 @@ struct StreamPlan {
 
 size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
-// Choose rows per task R, warps per CTA and ring depth for one streaming call.
-// The model: every SM runs one CTA; time ~ (rounds of tasks per warp) x R rows,
-// inflated by the activation reloads that small R pays, by an uneven final
-// chunk, and by too few bytes in flight per SM or too few warps.
+struct StageLayout {
+    size_t half, mat, stage;
+};
+StageLayout stage_layout(int fmt, int nmat, int R) {
+    return {stage_half_bytes(fmt, R), stage_mat_bytes(fmt, R), stage_bytes_of(fmt, nmat, R)};
+}
+
+// cuTensorMapEncodeTiled, fetched once from the driver.
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* f = nullptr;
+        cudaDriverEntryPointQueryResult q{};
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+    });
+    return fn;
+}
+
+// View a weight matrix as [N][row_bytes / 8] 8-byte words; box = (box_words, R).
+bool encode_weight_map(CUtensorMap* m, const void* w, int64_t N, int64_t row_bytes, int fmt, int R) {
+    PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+    if (!enc) return false;
+    cuuint64_t dims[2] = {(cuuint64_t)(row_bytes / 8), (cuuint64_t)N};
+    cuuint64_t strides[1] = {(cuuint64_t)row_bytes};
+    cuuint32_t box[2] = {(cuuint32_t)box_words(fmt), (cuuint32_t)R};
+    cuuint32_t estr[2] = {1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT64, 2, const_cast<void*>(w), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Choose rows per group R, warps per CTA W and ring depth D for one streaming
+// call.  Every SM runs one CTA owning ceil(groups / SMs) groups at most; its
+// (group, chunk) items are dealt round-robin to the W warps.  The estimate of
+// the makespan: the busiest warp's work (a full chunk costs R pair-rows per
+// lane, the short final chunk ceil(R * tail / 32) without activation reuse),
+// times W (the warps share the SM), divided by how well the SM is fed: enough
+// warps to hide latency, enough bytes in flight, activation reuse across R.
 bool plan_stream(int fmt, int nmat, int64_t N, int64_t K, const DeviceInfo& di, StreamPlan* out) {
     const int64_t npairs = K / 64;
     const int nfull = (int)(npairs / 32);
     const int tail = (int)(npairs % 32);
+    const int nitems = nfull + (tail ? 1 : 0);
     const size_t xs_bytes = (size_t)K * 4;
     const size_t fixed = align_up(xs_bytes, 128);
     const int Rs_1[] = {8, 4, 2, 1};
     const int Rs_2[] = {4, 2, 1};
     const int* Rs = (nmat == 2) ? Rs_2 : Rs_1;
     const int nR = (nmat == 2) ? 3 : 4;
-    const int warp_opts[] = {16, 14, 12, 11, 10, 9, 8, 7, 6, 5, 4};
-    double best = -1.0;
+    double best = 0.0;
+    bool found = false;
     for (int ir = 0; ir < nR; ++ir) {
         const int R = Rs[ir];
-        const size_t stage = (size_t)nmat * R * chunk_bytes(fmt);
-        const int64_t ntasks = (N + R - 1) / R;
-        const double frac_tail = npairs ? (double)tail / (double)npairs : 0.0;
-        double tail_eff = 1.0;
-        if (tail) {
-            const int items = R * tail;
-            tail_eff = (double)items / (32.0 * (double)((items + 31) / 32));
-        }
-        const double k_eff = 1.0 / ((1.0 - frac_tail) + frac_tail / tail_eff);
-        for (int w : warp_opts) {
-            for (int depth = 4; depth >= 2; --depth) {
-                const size_t ring = (size_t)w * depth * stage;
-                const size_t bars = (size_t)w * depth * 8;
-                const size_t smem = fixed + ring + bars;
+        const size_t stage = stage_layout(fmt, nmat, R).stage;
+        const int64_t groups = (N + R - 1) / R;
+        const int64_t gmax = (groups + di.sm_count - 1) / di.sm_count;
+        const int64_t items = gmax * nitems;
+        const size_t part_bytes = align_up((size_t)items * nmat * R * 4, 128);
+        const double full_cost = (double)R;
+        const double tail_cost = tail ? 1.15 * (double)((R * tail + 31) / 32) : 0.0;
+        for (int W = 16; W >= 4; --W) {
+            double warp_cost[16] = {};
+            for (int64_t it = 0; it < items; ++it)
+                warp_cost[it % W] += ((it % nitems) < nfull) ? full_cost : tail_cost;
+            double makespan = 0.0;
+            for (int w = 0; w < W; ++w) makespan = std::max(makespan, warp_cost[w]);
+            for (int D = 4; D >= 2; --D) {
+                const size_t smem = fixed + (size_t)W * D * stage + (size_t)W * D * 8 + part_bytes + 128;
                 if (smem > di.smem_optin) continue;
-                const int64_t P = (int64_t)di.sm_count * w;
-                const int64_t rounds = (ntasks + P - 1) / P;
-                const double eff = (double)ntasks / (double)(P * rounds);
+                const double sat = std::min(1.0, W / 12.0);
+                const double lat = std::sqrt(std::min(1.0, (double)W * (D - 1) * (double)stage / 65536.0));
                 const double reuse = 1.0 / (1.0 + 0.12 / R);
-                const double inflight = (double)w * (depth - 1) * (double)stage;
-                const double lat = std::sqrt(std::min(1.0, inflight / 65536.0));
-                const double occ = std::min(1.0, w / 8.0);
-                const double score = eff * k_eff * reuse * lat * occ;
-                if (score > best + 1e-9) {
-                    best = score;
+                const double t = makespan * W / (sat * lat * reuse);
+                if (!found || t < best - 1e-9) {
+                    found = true;
+                    best = t;
                     out->R = R;
-                    out->warps = w;
-                    out->depth = depth;
+                    out->warps = W;
+                    out->depth = D;
                     out->smem = smem;
                 }
             }
         }
     }
-    if (best < 0) return false;
+    if (!found) return false;
     out->ctas = di.sm_count;
     StreamParams& p = out->p;
+    const StageLayout L = stage_layout(fmt, nmat, out->R);
+    const size_t stage = L.stage;
     p.row_bytes = (K / 32) * block_bytes(fmt);
     p.N = (int32_t)N;
     p.K = (int32_t)K;
     p.npairs = (int32_t)npairs;
-    p.ntasks = (int32_t)((N + out->R - 1) / out->R);
+    p.ngroups = (int32_t)((N + out->R - 1) / out->R);
     p.nfull = nfull;
     p.tail_pairs = tail;
     p.depth = out->depth;
     p.ring_off = (uint32_t)fixed;
-    p.stage_bytes = (uint32_t)((size_t)nmat * out->R * chunk_bytes(fmt));
-    p.bar_off = (uint32_t)(fixed + (size_t)out->warps * out->depth * p.stage_bytes);
+    p.stage_bytes = (uint32_t)stage;
+    p.mat_bytes = (uint32_t)L.mat;
+    p.half_bytes = (uint32_t)L.half;
+    p.bar_off = (uint32_t)(fixed + (size_t)out->warps * out->depth * stage);
+    p.part_off = (uint32_t)(p.bar_off + (size_t)out->warps * out->depth * 8);
+    {
+        const int64_t groups = (N + out->R - 1) / out->R;
+        const int64_t gmax = (groups + di.sm_count - 1) / di.sm_count;
+        p.slot_off = (uint32_t)(p.part_off + align_up((size_t)gmax * nitems * nmat * out->R * 4, 128));
+    }
     p.fault = di.fault;
     return true;
 }
@@ -197,12 +246,15 @@ qbw_status qmv_common(int fmt, int nmat, const void* w0, const void* w1, const v
     const bool aligned = ((uintptr_t)w0 % 16 == 0) && (nmat == 1 || (uintptr_t)w1 % 16 == 0);
     if (K % 256 == 0 && aligned) {
         StreamPlan plan;
-        if (plan_stream(fmt, nmat, N, K, *di, &plan)) {
+        if (plan_stream(fmt, nmat, N, K, *di, &plan) &&
+            encode_weight_map(&plan.p.tmap[0], w0, N, plan.p.row_bytes, fmt, plan.R) &&
+            (nmat == 1 || encode_weight_map(&plan.p.tmap[1], w1, N, plan.p.row_bytes, fmt, plan.R))) {
             plan.p.w0 = static_cast<const uint8_t*>(w0);
             plan.p.w1 = static_cast<const uint8_t*>(nmat == 2 ? w1 : w0);
             plan.p.x = x;
             plan.p.y = y;
             plan.p.x_bf16 = (xt == QBW_BF16);
+            plan.p.x_vec = ((uintptr_t)x % (xt == QBW_BF16 ? 8 : 16)) == 0;
             plan.p.y_bf16 = (yt == QBW_BF16);
             return launch_streaming(fmt, nmat, *di, plan, s);
         }

@@ -6,6 +6,7 @@
 #include <cstddef>
 #include <cstdint>
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 namespace qbw {
@@ -18,7 +19,10 @@ enum FaultCode : unsigned int {
 enum : int { kFmtQ8 = 0, kFmtQ4 = 1 };
 
 // Launch parameters of the streaming M = 1 kernel (qmv_stream.cuh).
+// tmap[m] views weight matrix m as a 2-D array of 8-byte elements,
+// [N rows][row_bytes / 8], with a box of (chunk or half-chunk) x R rows.
 struct StreamParams {
+    CUtensorMap tmap[2];   // weights (gate, up for gate+up)
     const uint8_t* w0;     // weights (gate matrix for gate+up)
     const uint8_t* w1;     // up matrix (gate+up only)
     const void* x;         // activations [K]
@@ -28,21 +32,37 @@ struct StreamParams {
     int32_t N;
     int32_t K;
     int32_t npairs;        // K/64
-    int32_t ntasks;        // ceil(N / R)
+    int32_t ngroups;       // row groups of R rows: ceil(N / R)
     int32_t nfull;         // full 64-block chunks per row (npairs / 32)
     int32_t tail_pairs;    // npairs % 32
     int32_t depth;         // ring stages per warp
     int32_t x_bf16;        // activations are bf16 (else fp32)
+    int32_t x_vec;         // x is aligned for 4-element vector loads (16 B fp32, 8 B bf16)
     int32_t y_bf16;        // outputs are bf16 (else fp32)
     uint32_t ring_off;     // byte offsets inside dynamic shared memory
     uint32_t bar_off;
-    uint32_t stage_bytes;  // NMAT * R * chunk bytes
+    uint32_t part_off;     // per-item row partials (fp32)
+    uint32_t slot_off;     // 64-byte table: slot of each pair element
+    uint32_t stage_bytes;  // bytes of one ring stage (all matrices, all rows)
+    uint32_t mat_bytes;    // bytes of one matrix's rows within a stage
+    uint32_t half_bytes;   // Q8_0: bytes of one half-chunk box (R rows), 128-aligned
 };
 
 // Block-pair geometry of the streaming kernel.
 constexpr int pair_bytes(int fmt) { return fmt == kFmtQ4 ? 36 : 68; }
 constexpr int chunk_bytes(int fmt) { return 32 * pair_bytes(fmt); }
 constexpr int block_bytes(int fmt) { return fmt == kFmtQ4 ? 18 : 34; }
+// Tensor-copy boxes per chunk: Q4_0 one box of 144 8-byte words (1152 bytes);
+// Q8_0 two boxes of 136 words (1088 bytes, 16 pairs each), as a box row may
+// hold at most 256 elements.
+constexpr int boxes_per_chunk(int fmt) { return fmt == kFmtQ4 ? 1 : 2; }
+constexpr int box_words(int fmt) { return fmt == kFmtQ4 ? 144 : 136; }
+constexpr int pairs_per_box(int fmt) { return fmt == kFmtQ4 ? 32 : 16; }
+// Shared-memory layout of one ring stage: per matrix, per box, R rows of
+// box_words * 8 bytes; every box starts on a 128-byte boundary.
+constexpr uint32_t stage_half_bytes(int fmt, int R) { return (uint32_t)((R * box_words(fmt) * 8 + 127) / 128 * 128); }
+constexpr uint32_t stage_mat_bytes(int fmt, int R) { return stage_half_bytes(fmt, R) * boxes_per_chunk(fmt); }
+constexpr uint32_t stage_bytes_of(int fmt, int nmat, int R) { return stage_mat_bytes(fmt, R) * nmat; }
 
 // Each returns the cudaError_t of the launch (cudaGetLastError after it).
 cudaError_t launch_qmv_stream(int fmt, int nmat, int R, const StreamParams& p, int ctas, int warps,

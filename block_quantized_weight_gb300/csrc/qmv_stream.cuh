@@ -3,16 +3,21 @@
 // HBM through shared memory with 1-D bulk asynchronous copies.
 //
 // Work decomposition (one persistent CTA per SM, W warps per CTA):
-//  * a "task" is R consecutive output rows (R rows of each matrix for
-//    gate+up).  Warp g of P takes tasks g, g+P, g+2P, ...;
-//  * each task streams its rows in chunks of 64 blocks (32 block pairs); a warp
-//    keeps a private ring of D stages, lane 0 issues the bulk copies for the
-//    stage D ahead and every lane waits on that stage's mbarrier;
-//  * lane l owns block pair l of the chunk for all rows of the task, so the
-//    activation slice it needs is loaded from shared memory once and reused
+//  * rows form groups of R consecutive rows (R rows of each matrix for
+//    gate+up); each CTA owns a contiguous range of groups;
+//  * a row is cut into chunks of 64 blocks (32 block pairs); the CTA's work
+//    items are (group, chunk) pairs, dealt round-robin to its warps, so the
+//    items of one group run on different warps at the same time;
+//  * each warp keeps a private ring of D shared-memory stages: lane 0 issues
+//    the bulk copies of the item D ahead, every lane waits on that stage's
+//    mbarrier (bounded wait);
+//  * within an item, lane l owns block pair l of the chunk for all R rows, so
+//    the activation slice it needs is read from shared memory once and reused
 //    R times (the gem decode path's "four-output-row" reuse, generalised);
-//  * a final chunk shorter than 64 blocks (K % 2048 != 0) is spread over
-//    (row, pair) items so every lane still has work.
+//    a final chunk shorter than 64 blocks is spread over (row, pair) items;
+//  * each item's R row partials are reduced across the warp and stored in
+//    shared memory; at the end the CTA adds every row's partials in chunk
+//    order (a fixed order: results are bit-reproducible) and writes y.
 //
 // A block pair is 36 bytes (Q4_0) or 68 bytes (Q8_0): 4-byte aligned, and its
 // internal byte layout is the same for every lane, so all word positions,
@@ -99,44 +104,73 @@ __host__ __device__ constexpr int q8_slot_element(int slot) {
 }
 
 // ---------------------------------------------------------------- decode
-__device__ __forceinline__ uint32_t lop3_select(uint32_t a, uint32_t b, uint32_t c) {
-    // per bit: c ? (a ^ b) : b
-    uint32_t r;
-    asm("lop3.b32 %0, %1, %2, %3, 0x6C;" : "=r"(r) : "r"(a), "r"(b), "r"(c));
+// Exponent fields of 2^23, 2^19, 2^15, 2^11, 2^7: OR-ed above a code sitting at
+// bit 0, 4, 8, 12, 16 they make the float 2^e + code.
+constexpr uint32_t kMag23 = 0x4B000000u, kMag19 = 0x49000000u, kMag15 = 0x47000000u, kMag11 = 0x45000000u,
+                   kMag7 = 0x43000000u;
+// Packed (lo, hi) fp32 constants subtracted after the OR: -(2^e + 8) for Q4_0.
+constexpr uint64_t kSubQ4_23_19 = 0xC9000080CB000008ull;   // (-(2^23 + 8), -(2^19 + 8))
+constexpr uint64_t kSubQ4_15_11 = 0xC5008000C7000800ull;   // (-(2^15 + 8), -(2^11 + 8))
+constexpr uint64_t kSubQ4_7_7 = 0xC3080000C3080000ull;     // (-(2^7 + 8), -(2^7 + 8))
+// Q8_0: -(2^e + 128) undoes the magic and the offset-binary flip.
+constexpr uint64_t kSubQ8 = 0xC7008000CB000080ull;         // (-(2^23 + 128), -(2^15 + 128))
+
+// Two codes -> one fp32x2 register pair, in one asm block so that the two
+// LOP3 results land directly in the pair the packed add reads:
+//   lo = (a & ML) | gl,  hi = (b & MH) | gh,  result = (lo, hi) + k.
+template <uint32_t ML, uint32_t MH>
+__device__ __forceinline__ uint64_t codes2(uint32_t a, uint32_t b, uint32_t gl, uint32_t gh, uint64_t k) {
+    uint64_t r;
+    asm("{\n\t.reg .b32 lo, hi;\n\t.reg .b64 t;\n\t"
+        "lop3.b32 lo, %1, %5, %3, 0xEA;\n\t"
+        "lop3.b32 hi, %2, %6, %4, 0xEA;\n\t"
+        "mov.b64 t, {lo, hi};\n\t"
+        "add.rn.f32x2 %0, t, %7;\n\t}"
+        : "=l"(r)
+        : "r"(a), "r"(b), "r"(gl), "r"(gh), "n"(ML), "n"(MH), "l"(k));
     return r;
 }
 
+// Q8_0: bytes at bits 0 and 8 of a and b, signed -> (q_lo, q_hi) exactly.
+// Per bit: mask ? (v ^ g) : g, with g = exponent | 0x80 flip bit (LOP3 0x6C).
+__device__ __forceinline__ uint64_t q8_codes2(uint32_t a, uint32_t b, uint32_t gl, uint32_t gh) {
+    uint64_t r;
+    asm("{\n\t.reg .b32 lo, hi;\n\t.reg .b64 t;\n\t"
+        "lop3.b32 lo, %1, %3, 0x000000FF, 0x6C;\n\t"
+        "lop3.b32 hi, %2, %4, 0x0000FF00, 0x6C;\n\t"
+        "mov.b64 t, {lo, hi};\n\t"
+        "add.rn.f32x2 %0, t, %5;\n\t}"
+        : "=l"(r)
+        : "r"(a), "r"(b), "r"(gl), "r"(gh), "l"(kSubQ8));
+    return r;
+}
+
+// Register-resident magic constants (materialised once per thread).
+struct Mags {
+    uint32_t m23, m19, m15, m11, m7, q8a, q8b;
+    __device__ __forceinline__ Mags()
+        : m23(kMag23), m19(kMag19), m15(kMag15), m11(kMag11), m7(kMag7), q8a(0x4B000080u), q8b(0x47008000u) {}
+};
+
 // Q4_0 L chunk of word v: codes at bits 0, 4, 8, 12 -> exact (code - 8).
-__device__ __forceinline__ void q4_chunk_L(uint32_t v, uint64_t& fa, uint64_t& fb) {
-    const uint64_t k01 = 0xC9000080CB000008ull;   // (-(2^23 + 8), -(2^19 + 8))
-    const uint64_t k23 = 0xC5008000C7000800ull;   // (-(2^15 + 8), -(2^11 + 8))
-    fa = fadd2(pack2((v & 0x0000000Fu) | 0x4B000000u, (v & 0x000000F0u) | 0x49000000u), k01);
-    fb = fadd2(pack2((v & 0x00000F00u) | 0x47000000u, (v & 0x0000F000u) | 0x45000000u), k23);
+__device__ __forceinline__ void q4_chunk_L(uint32_t v, const Mags& g, uint64_t& fa, uint64_t& fb) {
+    fa = codes2<0x0000000Fu, 0x000000F0u>(v, v, g.m23, g.m19, kSubQ4_23_19);
+    fb = codes2<0x00000F00u, 0x0000F000u>(v, v, g.m15, g.m11, kSubQ4_15_11);
 }
 
-// Q4_0 H chunk of word v: codes at bits 20, 24 (shifted to 8, 12) and 16, 28
-// (16 in place, 28 shifted to 16) -> exact (code - 8).
-__device__ __forceinline__ void q4_chunk_H(uint32_t v, uint64_t& fa, uint64_t& fb) {
-    const uint64_t k23 = 0xC5008000C7000800ull;   // (-(2^15 + 8), -(2^11 + 8))
-    const uint64_t k16 = 0xC3080000C3080000ull;   // (-(128 + 8), -(128 + 8))
+// Q4_0 H chunk of word v: codes at bits 20, 24 (shifted down by 12 to 8, 12)
+// and at bits 16 (in place) and 28 (shifted to 16) -> exact (code - 8).
+__device__ __forceinline__ void q4_chunk_H(uint32_t v, const Mags& g, uint64_t& fa, uint64_t& fb) {
     const uint32_t s = v >> 12;
-    fa = fadd2(pack2((s & 0x00000F00u) | 0x47000000u, (s & 0x0000F000u) | 0x45000000u), k23);
-    fb = fadd2(pack2((v & 0x000F0000u) | 0x43000000u, (s & 0x000F0000u) | 0x43000000u), k16);
-}
-
-// Q8_0: the signed bytes 0 and 1 of word v -> exact floats.
-__device__ __forceinline__ uint64_t q8_bytes01(uint32_t v) {
-    const uint64_t k = 0xC7008000CB000080ull;     // (-(2^23 + 128), -(2^15 + 128))
-    const uint32_t a = lop3_select(v, 0x4B000080u, 0x000000FFu);   // 2^23 + (q0 + 128)
-    const uint32_t b = lop3_select(v, 0x47008000u, 0x0000FF00u);   // 2^15 + (q1 + 128)
-    return fadd2(pack2(a, b), k);
+    fa = codes2<0x00000F00u, 0x0000F000u>(s, s, g.m15, g.m11, kSubQ4_15_11);
+    fb = codes2<0x000F0000u, 0x000F0000u>(v, s, g.m7, g.m7, kSubQ4_7_7);
 }
 
 // ---------------------------------------------------------------- one pair
 // Accumulate one block pair of NR rows of NMAT matrices into acc.
 // rowaddr(m, r) is the shared-memory address of the pair in row (m, r).
 template <int FMT, int NMAT, int NR, typename RowAddr>
-__device__ __forceinline__ void pair_dot(const RowAddr& rowaddr, uint32_t xaddr, uint32_t swz,
+__device__ __forceinline__ void pair_dot(const RowAddr& rowaddr, uint32_t xaddr, uint32_t swz, const Mags& g,
                                          float (&acc)[NMAT][NR]) {
     uint64_t bacc[NMAT][NR];
     uint32_t vw[NMAT][NR];
@@ -162,20 +196,22 @@ __device__ __forceinline__ void pair_dot(const RowAddr& rowaddr, uint32_t xaddr,
                     const uint32_t v = vw[m][r];
                     if (c == 0) dA[m][r] = v;
                     if (c == 7) dB[m][r] = v >> 16;
-                    if (q4_chunk_is_h(c)) q4_chunk_H(v, fa, fb);
-                    else q4_chunk_L(v, fa, fb);
+                    if (q4_chunk_is_h(c)) q4_chunk_H(v, g, fa, fb);
+                    else q4_chunk_L(v, g, fa, fb);
                 } else {
                     if (c == 0) {
                         const uint32_t v0 = lds32(base);
                         const uint32_t v8 = lds32(base + 32u);
                         dA[m][r] = v0;
                         dB[m][r] = v8 >> 16;
-                        fa = q8_bytes01(v0 >> 16);
-                        fb = q8_bytes01(v8);
+                        const uint32_t h0 = v0 >> 16;
+                        fa = q8_codes2(h0, h0, g.q8a, g.q8b);
+                        fb = q8_codes2(v8, v8, g.q8a, g.q8b);
                     } else {
                         const uint32_t v = lds32(base + 4u * (uint32_t)((c < 8) ? c : c + 1));
-                        fa = q8_bytes01(v);
-                        fb = q8_bytes01(v >> 16);
+                        const uint32_t h = v >> 16;
+                        fa = q8_codes2(v, v, g.q8a, g.q8b);
+                        fb = q8_codes2(h, h, g.q8a, g.q8b);
                     }
                 }
                 ffma2(bacc[m][r], fa, x01);
@@ -191,170 +227,286 @@ __device__ __forceinline__ void pair_dot(const RowAddr& rowaddr, uint32_t xaddr,
     }
 }
 
-__device__ __forceinline__ float warp_sum(float v) {
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-    return v;
-}
-
 // Stage the activations in slot order: 64 fp32 per pair, 16-byte chunks
 // XOR-swizzled by pair index so that 8 lanes reading 8 consecutive pairs hit 8
-// distinct bank groups.
+// distinct bank groups.  slot_of[e] is the slot of pair element e (filled by
+// the caller).  Every thread first issues all of its loads of 4 consecutive
+// elements (vector loads when x is aligned for them), then scatters them.
 template <int FMT>
-__device__ __forceinline__ void stage_activations(const StreamParams& p, uint8_t* smem) {
+__device__ __forceinline__ void stage_activations(const StreamParams& p, uint8_t* smem, const uint8_t* slot_of) {
     float* xs = reinterpret_cast<float*>(smem);
-    for (int q = threadIdx.x; q < p.npairs; q += blockDim.x) {
-        const uint32_t swz = (uint32_t)q & 7u;
-#pragma unroll 4
-        for (int s = 0; s < 64; ++s) {
-            const int e = (FMT == kFmtQ4) ? q4_slot_element(s) : q8_slot_element(s);
-            const int64_t k = (int64_t)q * 64 + e;
-            const float xv = p.x_bf16 ? load_act<__nv_bfloat16>(p.x, k) : load_act<float>(p.x, k);
-            xs[q * 64 + (int)((((uint32_t)(s >> 2)) ^ swz) << 2) + (s & 3)] = xv;
+    const int n4 = p.K >> 2;
+    constexpr int U = 4;
+    for (int i0 = threadIdx.x; i0 < n4; i0 += U * blockDim.x) {
+        float v[U][4];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int i = i0 + u * blockDim.x;
+            if (i >= n4) break;
+            if (p.x_bf16) {
+                uint32_t lo, hi;
+                if (p.x_vec) {
+                    const uint2 raw = __ldg(reinterpret_cast<const uint2*>(p.x) + i);
+                    lo = raw.x;
+                    hi = raw.y;
+                } else {
+                    const unsigned short* h = reinterpret_cast<const unsigned short*>(p.x) + 4 * i;
+                    lo = (uint32_t)__ldg(h) | ((uint32_t)__ldg(h + 1) << 16);
+                    hi = (uint32_t)__ldg(h + 2) | ((uint32_t)__ldg(h + 3) << 16);
+                }
+                v[u][0] = __uint_as_float(lo << 16);
+                v[u][1] = __uint_as_float(lo & 0xFFFF0000u);
+                v[u][2] = __uint_as_float(hi << 16);
+                v[u][3] = __uint_as_float(hi & 0xFFFF0000u);
+            } else if (p.x_vec) {
+                const float4 f = __ldg(reinterpret_cast<const float4*>(p.x) + i);
+                v[u][0] = f.x; v[u][1] = f.y; v[u][2] = f.z; v[u][3] = f.w;
+            } else {
+                const float* f = reinterpret_cast<const float*>(p.x) + 4 * i;
+                v[u][0] = __ldg(f); v[u][1] = __ldg(f + 1); v[u][2] = __ldg(f + 2); v[u][3] = __ldg(f + 3);
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int i = i0 + u * blockDim.x;
+            if (i >= n4) break;
+            const int q = i >> 4;              // pair (64 elements = 16 groups of 4)
+            const uint32_t swz = (uint32_t)q & 7u;
+#pragma unroll
+            for (int t = 0; t < 4; ++t) {
+                const int s = slot_of[((i & 15) << 2) + t];
+                xs[q * 64 + (int)((((uint32_t)(s >> 2)) ^ swz) << 2) + (s & 3)] = v[u][t];
+            }
         }
     }
 }
 
+// Sum V values per lane across the 32 lanes of the warp.  Returns, in every
+// lane, the total of value index value_of_lane(lane); the exchange pattern is
+// fixed, so the result is bit-reproducible.
+template <int V>
+__device__ __forceinline__ float transpose_reduce(float (&v)[V], int lane) {
+    int off = 16;
+#pragma unroll
+    for (int half = V / 2; half >= 1; half /= 2, off >>= 1) {
+        const bool upper = (lane & off) != 0;
+#pragma unroll
+        for (int i = 0; i < half; ++i) {
+            const float send = upper ? v[i] : v[i + half];
+            const float keep = upper ? v[i + half] : v[i];
+            v[i] = keep + __shfl_xor_sync(0xffffffffu, send, off);
+        }
+    }
+    float t = v[0];
+#pragma unroll
+    for (; off >= 1; off >>= 1) t += __shfl_xor_sync(0xffffffffu, t, off);
+    return t;
+}
+
+// Value index a lane holds after transpose_reduce<V>.
+template <int V>
+__device__ __forceinline__ int value_of_lane(int lane) {
+    int idx = 0, off = 16;
+#pragma unroll
+    for (int half = V / 2; half >= 1; half /= 2, off >>= 1) idx = (idx << 1) | ((lane & off) ? 1 : 0);
+    return idx;
+}
+
 // ---------------------------------------------------------------- the kernel
 template <int FMT, int NMAT, int R>
-__global__ void __launch_bounds__(512, 1) qmv_stream_kernel(const StreamParams p) {
+__global__ void __launch_bounds__(512, 1) qmv_stream_kernel(const __grid_constant__ StreamParams p) {
     using F = Fmt<FMT>;
+    constexpr int V = NMAT * R;                 // row partials per item
+    constexpr uint32_t kHalf = stage_half_bytes(FMT, R);
+    constexpr uint32_t kMat = stage_mat_bytes(FMT, R);
+    constexpr uint32_t kStage = stage_bytes_of(FMT, NMAT, R);
     extern __shared__ __align__(1024) uint8_t smem[];
+    uint8_t* slot_of = smem + p.slot_off;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int nwarps = blockDim.x >> 5;
-    const int gw = blockIdx.x * nwarps + warp;
-    const int P = gridDim.x * nwarps;
+    const int W = blockDim.x >> 5;
     const int D = p.depth;
 
     const uint32_t sbase = smem_u32(smem);
     const uint32_t xs = sbase;                                    // 64 fp32 per pair
-    const uint32_t ring = sbase + p.ring_off + (uint32_t)warp * (uint32_t)D * p.stage_bytes;
+    const uint32_t ring = sbase + p.ring_off + (uint32_t)warp * (uint32_t)D * kStage;
     const uint32_t bars = sbase + p.bar_off + (uint32_t)warp * (uint32_t)D * 8u;
+    float* part = reinterpret_cast<float*>(smem + p.part_off);
 
+    // this CTA's groups and items
+    const int g0 = (int)((int64_t)p.ngroups * blockIdx.x / gridDim.x);
+    const int g1 = (int)((int64_t)p.ngroups * (blockIdx.x + 1) / gridDim.x);
     const int nitems = p.nfull + (p.tail_pairs ? 1 : 0);
-    const int my_tasks = (p.ntasks > gw) ? (p.ntasks - gw + P - 1) / P : 0;
-    const int total = my_tasks * nitems;
+    const int n_items = (g1 - g0) * nitems;
+    const int mine = (n_items > warp) ? (n_items - warp + W - 1) / W : 0;
     const uint64_t policy = policy_evict_first();
 
-    // Lane 0 only: copy item j (task j / nitems, chunk j % nitems) into stage j % D.
-    auto issue = [&](int j) {
-        const int ti = j / nitems, c = j - ti * nitems;
-        const int64_t row0 = (int64_t)(gw + ti * P) * R;
-        const int64_t left = (int64_t)p.N - row0;
-        const int rows = left < R ? (int)left : R;
-        const uint32_t bytes = (c < p.nfull) ? (uint32_t)F::kChunkBytes
-                                             : (uint32_t)(p.tail_pairs * F::kPairBytes);
-        const int s = j % D;
-        const uint32_t bar = bars + 8u * (uint32_t)s;
-        const uint32_t dst0 = ring + (uint32_t)s * p.stage_bytes;
-        mbar_arrive_expect_tx(bar, bytes * (uint32_t)(rows * NMAT));
+    // Lane 0 only: copy item (group g0 + lg, chunk c) into stage `st` with
+    // one tensor copy per matrix and box; rows past N and words past the end
+    // of a row arrive as zeros, and every box counts in full.
+    auto issue = [&](int lg, int c, int st) {
+        const uint32_t bar = bars + 8u * (uint32_t)st;
+        const uint32_t dst0 = ring + (uint32_t)st * kStage;
+        mbar_arrive_expect_tx(bar, (uint32_t)(NMAT * boxes_per_chunk(FMT) * box_words(FMT) * 8 * R));
+        const int y = (g0 + lg) * R;
 #pragma unroll
-        for (int m = 0; m < NMAT; ++m) {
-            const uint8_t* wm = (m == 0) ? p.w0 : p.w1;
-            for (int r = 0; r < rows; ++r) {
-                const uint8_t* src = wm + (row0 + r) * p.row_bytes + (int64_t)c * F::kChunkBytes;
-                bulk_g2s(dst0 + (uint32_t)(m * R + r) * (uint32_t)F::kChunkBytes, src, bytes, bar, policy);
-            }
-        }
+        for (int m = 0; m < NMAT; ++m)
+#pragma unroll
+            for (int h = 0; h < boxes_per_chunk(FMT); ++h)
+                tma_load_2d(dst0 + (uint32_t)m * kMat + (uint32_t)h * kHalf, &p.tmap[m],
+                            (c * boxes_per_chunk(FMT) + h) * box_words(FMT), y, bar, policy);
+    };
+
+    // the item after (lg, c) for this warp: c advances by W chunks
+    auto next_item = [&](int& lg_, int& c_) {
+        c_ += W;
+        while (c_ >= nitems) { c_ -= nitems; ++lg_; }
     };
 
     if (lane == 0) {
         for (int s = 0; s < D; ++s) mbar_init(bars + 8u * (uint32_t)s, 1);
         fence_mbar_init();
+        prefetch_tmap(&p.tmap[0]);
+        if (NMAT == 2) prefetch_tmap(&p.tmap[1]);
     }
     __syncwarp();
+    // producer cursor (lane 0): the item D ahead of the consumer
+    int plg = warp / nitems, pc = warp - (warp / nitems) * nitems, pst = 0;
     if (lane == 0)
-        for (int j = 0; j < min(D, total); ++j) issue(j);
+        for (int j = 0; j < min(D, mine); ++j) {
+            issue(plg, pc, pst);
+            next_item(plg, pc);
+            if (++pst == D) pst = 0;
+        }
 
-    stage_activations<FMT>(p, smem);
+    if (threadIdx.x < 64)
+        slot_of[FMT == kFmtQ4 ? q4_slot_element(threadIdx.x) : q8_slot_element(threadIdx.x)] = (uint8_t)threadIdx.x;
+    // Everything above touched only the weights (already in flight) and this
+    // CTA's shared memory.  The activations may come from the preceding grid.
+    grid_dependency_wait();
     __syncthreads();
+    stage_activations<FMT>(p, smem, slot_of);
+    __syncthreads();
+    grid_launch_dependents();
 
-    float acc[NMAT][R];
-#pragma unroll
-    for (int m = 0; m < NMAT; ++m)
-#pragma unroll
-        for (int r = 0; r < R; ++r) acc[m][r] = 0.f;
-
-    int j = 0;
-    for (; j < total; ++j) {
-        const int s = j % D;
-        const uint32_t parity = (uint32_t)(j / D) & 1u;
+    const Mags g;
+    // (row, pair) of this lane's first short-chunk item, and the step per 32 items
+    const int tail_tp = p.tail_pairs > 0 ? p.tail_pairs : 1;
+    const int tail_r0 = lane / tail_tp, tail_q0 = lane - (lane / tail_tp) * tail_tp;
+    const int tail_dr = 32 / tail_tp, tail_dq = 32 - (32 / tail_tp) * tail_tp;
+    int j = 0, s = 0, lg = warp / nitems, c = warp - (warp / nitems) * nitems;
+    uint32_t parity = 0;
+    for (; j < mine; ++j) {
         const bool arrived = mbar_wait_bounded(bars + 8u * (uint32_t)s, parity, p.fault, kFaultBulkWaitTimeout);
         if (!__all_sync(0xffffffffu, arrived)) break;
 
-        const int ti = j / nitems, c = j - ti * nitems;
-        const int64_t row0 = (int64_t)(gw + ti * P) * R;
-        const uint32_t stage = ring + (uint32_t)s * p.stage_bytes;
+        const int it = lg * nitems + c;
+        const uint32_t stage = ring + (uint32_t)s * kStage;
+        float acc[NMAT][R];
+#pragma unroll
+        for (int m = 0; m < NMAT; ++m)
+#pragma unroll
+            for (int r = 0; r < R; ++r) acc[m][r] = 0.f;
         if (c < p.nfull) {
             const int q = c * 32 + lane;
-            const uint32_t poff = (uint32_t)lane * (uint32_t)F::kPairBytes;
+            const uint32_t poff = (FMT == kFmtQ4)
+                                      ? (uint32_t)lane * (uint32_t)F::kPairBytes
+                                      : (uint32_t)(lane >> 4) * kHalf + (uint32_t)(lane & 15) * F::kPairBytes;
+            constexpr uint32_t kRowBytes = (uint32_t)(box_words(FMT) * 8);
             auto rowaddr = [&](int m, int r) {
-                return stage + (uint32_t)(m * R + r) * (uint32_t)F::kChunkBytes + poff;
+                return stage + (uint32_t)m * kMat + (uint32_t)r * kRowBytes + poff;
             };
-            pair_dot<FMT, NMAT, R>(rowaddr, xs + (uint32_t)q * 256u, (uint32_t)q & 7u, acc);
+            pair_dot<FMT, NMAT, R>(rowaddr, xs + (uint32_t)q * 256u, (uint32_t)q & 7u, g, acc);
         } else {
-            // tail chunk: (row, pair) items spread over the lanes
+            // final short chunk: (row, pair) items spread over the lanes
             const int items = R * p.tail_pairs;
-            for (int it = lane; it < items; it += 32) {
-                const int r = it / p.tail_pairs;
-                const int qq = it - r * p.tail_pairs;
+            int r = tail_r0, qq = tail_q0;
+            for (int t = lane; t < items; t += 32) {
                 const int q = c * 32 + qq;
-                float part[NMAT][1];
+                float one[NMAT][1];
 #pragma unroll
-                for (int m = 0; m < NMAT; ++m) part[m][0] = 0.f;
-                auto rowaddr = [&](int m, int) {
-                    return stage + (uint32_t)(m * R + r) * (uint32_t)F::kChunkBytes +
-                           (uint32_t)qq * (uint32_t)F::kPairBytes;
-                };
-                pair_dot<FMT, NMAT, 1>(rowaddr, xs + (uint32_t)q * 256u, (uint32_t)q & 7u, part);
+                for (int m = 0; m < NMAT; ++m) one[m][0] = 0.f;
+                const uint32_t poff = (FMT == kFmtQ4)
+                                          ? (uint32_t)qq * (uint32_t)F::kPairBytes
+                                          : (uint32_t)(qq >> 4) * kHalf + (uint32_t)(qq & 15) * F::kPairBytes;
+                const uint32_t rbase = stage + (uint32_t)r * (uint32_t)(box_words(FMT) * 8) + poff;
+                auto rowaddr = [&](int m, int) { return rbase + (uint32_t)m * kMat; };
+                pair_dot<FMT, NMAT, 1>(rowaddr, xs + (uint32_t)q * 256u, (uint32_t)q & 7u, g, one);
 #pragma unroll
                 for (int m = 0; m < NMAT; ++m)
 #pragma unroll
                     for (int rr = 0; rr < R; ++rr)
-                        if (rr == r) acc[m][rr] += part[m][0];
+                        if (rr == r) acc[m][rr] += one[m][0];
+                // next item of this lane: t + 32 = (r + tail_dr) rows, (qq + tail_dq) pairs
+                r += tail_dr;
+                qq += tail_dq;
+                if (qq >= p.tail_pairs) { qq -= p.tail_pairs; ++r; }
             }
         }
         __syncwarp();
-        if (lane == 0 && j + D < total) {
+        if (lane == 0 && j + D < mine) {
             fence_proxy_async_smem();
-            issue(j + D);
+            issue(plg, pc, pst);
+            next_item(plg, pc);
+            if (++pst == D) pst = 0;
         }
-        if (c == nitems - 1) {
-            float outv = 0.f;
+        // reduce the item's V row partials across the warp, store them
+        float vals[V];
 #pragma unroll
-            for (int r = 0; r < R; ++r) {
-                const float g = warp_sum(acc[0][r]);
-                float v = g;
-                if constexpr (NMAT == 2) {
-                    const float u = warp_sum(acc[1][r]);
-                    v = gelu_tanh(g) * u;
-                }
-                if (lane == r) outv = v;
-            }
-            if (lane < R && row0 + lane < p.N) {
-                if (p.y_bf16) store_out<__nv_bfloat16>(p.y, row0 + lane, outv);
-                else store_out<float>(p.y, row0 + lane, outv);
-            }
+        for (int m = 0; m < NMAT; ++m)
 #pragma unroll
-            for (int m = 0; m < NMAT; ++m)
-#pragma unroll
-                for (int r = 0; r < R; ++r) acc[m][r] = 0.f;
-        }
+            for (int r = 0; r < R; ++r) vals[m * R + r] = acc[m][r];
+        const float tot = transpose_reduce<V>(vals, lane);
+        if ((lane & (32 / V - 1)) == 0) part[(size_t)it * V + value_of_lane<V>(lane)] = tot;
+        // advance: next stage of the ring, next item of this warp
+        if (++s == D) { s = 0; parity ^= 1u; }
+        next_item(lg, c);
     }
-    if (j < total && lane == 0) {
-        // A copy never arrived.  Before leaving, give the other stages already
-        // in flight the same bounded time to land in this CTA's shared memory.
-        for (int jj = j + 1; jj < min(total, j + D); ++jj)
+    if (j < mine && lane == 0) {
+        // A copy never arrived.  Give the stages already in flight the same
+        // bounded time to land in this CTA's shared memory before leaving.
+        for (int jj = j + 1; jj < min(mine, j + D); ++jj)
             mbar_wait_bounded(bars + 8u * (uint32_t)(jj % D), (uint32_t)(jj / D) & 1u, p.fault,
                               kFaultBulkWaitTimeout);
     }
+    __syncthreads();
+
+    // every row of this CTA: add its partials in chunk order, write the output
+    const int nrows = (g1 - g0) * R;
+    for (int t = threadIdx.x; t < nrows; t += blockDim.x) {
+        const int lg = t / R, r = t - lg * R;
+        const int64_t row = (int64_t)(g0 + lg) * R + r;
+        if (row >= p.N) continue;
+        float sum[NMAT];
+#pragma unroll
+        for (int m = 0; m < NMAT; ++m) {
+            float a = 0.f;
+            for (int c = 0; c < nitems; ++c) a += part[(size_t)(lg * nitems + c) * V + m * R + r];
+            sum[m] = a;
+        }
+        float v = sum[0];
+        if constexpr (NMAT == 2) v = gelu_tanh(sum[0]) * sum[1];
+        if (p.y_bf16) store_out<__nv_bfloat16>(p.y, row, v);
+        else store_out<float>(p.y, row, v);
+    }
 }
 
-// Host-side launch of one instantiation.
+// Host-side launch of one instantiation, as a programmatic dependent of the
+// preceding kernel on the stream (the kernel waits for it before reading x).
 template <int FMT, int NMAT, int R>
 cudaError_t launch_stream_instance(const StreamParams& p, int ctas, int warps, size_t smem,
                                    cudaStream_t stream) {
-    qmv_stream_kernel<FMT, NMAT, R><<<ctas, warps * 32, smem, stream>>>(p);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)ctas);
+    cfg.blockDim = dim3((unsigned)(warps * 32));
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, qmv_stream_kernel<FMT, NMAT, R>, p);
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 

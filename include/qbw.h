@@ -30,6 +30,16 @@
  * Streams.  `stream` is a cudaStream_t passed as void* (NULL = legacy default
  * stream).  Work is enqueued asynchronously; a call never synchronizes.
  *
+ * Overlap with the preceding kernel.  The fast-path M = 1 kernels are launched
+ * as programmatic dependents of the kernel enqueued just before them on the
+ * same stream: they may start, and begin streaming their WEIGHT matrices,
+ * while that kernel is still finishing.  Activations are read, and outputs
+ * written, only after it has completed.  Therefore the weight matrix of a call
+ * must not be written by the kernel immediately preceding the call on its
+ * stream; if it is, put any other stream operation in between (another
+ * kernel, a memset, an event record).  Weights loaded with cudaMemcpy are
+ * always safe.
+ *
  * Errors.  Arguments are validated on the host before anything is launched; a
  * rejected call returns its status and launches nothing.  After a launch,
  * cudaGetLastError() != cudaSuccess returns QBW_ECUDA.  Errors raised while a
@@ -40,8 +50,8 @@
  * bit-identical outputs from run to run.
  *
  * Fast path.  When K % 256 == 0 and the weight pointers are 16-byte aligned,
- * rows are streamed with bulk asynchronous copies; any other K % 32 == 0 shape
- * or alignment takes a slower, equally exact path.
+ * weight rows are streamed into shared memory with tensor copies (TMA); any
+ * other K % 32 == 0 shape or alignment takes a slower, equally exact path.
  */
 #ifndef QBW_H
 #define QBW_H

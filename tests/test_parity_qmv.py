@@ -234,3 +234,17 @@ def test_dequant_bit_exact(qbw, oracle, fmt, N, K):
 
 def test_no_fault_recorded(qbw):
     assert qbw.fault_read(clear=True) == 0
+
+
+@pytest.mark.parametrize("xdt,offset", [("f32", 1), ("f32", 2), ("bf16", 1), ("bf16", 3)])
+def test_activations_not_vector_aligned(qbw, oracle, xdt, offset):
+    # x aligned to its dtype only: the staging falls back to scalar loads
+    N, K = 300, 2304
+    w = synth.q4_0_weights(N, K, seed=40)
+    x = synth.activations(K, seed=40, dtype=xdt)
+    full = dev_act(np.concatenate([x[:offset], x]))   # x starts `offset` elements in
+    y = torch.empty(N, device="cuda")
+    qbw.qmv_q4_0(dev_u8(w), full[offset:], y, 1, N, K)
+    torch.cuda.synchronize()
+    y_ref, S = oracle.qmv("q4_0", w, x, N, K)
+    check_matvec(to_f64(y), y_ref, S, what=f"x offset {offset}")

@@ -1,0 +1,128 @@
+"""GPU parity of the chained decode sweep: per layer q, k, v = W h; o = Wo q
+(o consumes q, standing in for attention); a = gelu_tanh(Wg o) * (Wu o); the
+next layer's h = Wd a; every activation bf16.  The launches of all layers are
+enqueued back to back on one stream, so each kernel starts while the previous
+one finishes and must still read the previous output only after it is
+complete.
+
+The oracle runs the same chain on its own: each step in fp64 on the oracle's
+previous bf16-rounded output, rounded to bf16 itself.  The GPU chain is
+compared with it step by step with the matvec rule (2e-3 of the row's sum of
+|w x| plus the bf16 output rounding; the gate+up rule for a).  The two chains
+can differ by an ulp of bf16 at a rounding boundary and carry that forward;
+relative to S such differences stay far inside the bound.
+"""
+import numpy as np
+import pytest
+
+import synth
+from tolerance import check_gateup, check_matvec, to_f64
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+
+
+def shapes(hidden, qdim, kvdim, ffn):
+    return {"q": (qdim, hidden), "k": (kvdim, hidden), "v": (kvdim, hidden), "o": (hidden, qdim),
+            "gate": (ffn, hidden), "up": (ffn, hidden), "down": (hidden, ffn)}
+
+
+ORDER = ["q", "k", "v", "o", "gate", "up", "down"]
+
+
+def bf16_dev(bits):
+    return torch.from_numpy(bits.view(np.int16).copy()).view(torch.bfloat16).cuda()
+
+
+def run_chain(qbw, oracle, dims, layers, seed):
+    shp = shapes(*dims)
+    hidden = dims[0]
+    W = [{n: synth.q4_0_weights(*shp[n], seed=seed, stream=i, layer=l) for i, n in enumerate(ORDER)}
+         for l in range(layers)]
+    Wd = [{n: torch.from_numpy(W[l][n]).cuda() for n in ORDER} for l in range(layers)]
+    h0 = synth.activations(hidden, seed=seed, dtype="bf16")
+    bf = torch.bfloat16
+    buf = {"h": bf16_dev(h0), "q": torch.empty(shp["q"][0], dtype=bf, device="cuda"),
+           "k": torch.empty(shp["k"][0], dtype=bf, device="cuda"), "v": torch.empty(shp["v"][0], dtype=bf, device="cuda"),
+           "o": torch.empty(shp["o"][0], dtype=bf, device="cuda"), "a": torch.empty(shp["gate"][0], dtype=bf, device="cuda")}
+    snaps = []
+
+    def layer(l, keep):
+        qbw.qmv_q4_0(Wd[l]["q"], buf["h"], buf["q"], 1, *shp["q"])
+        qbw.qmv_q4_0(Wd[l]["k"], buf["h"], buf["k"], 1, *shp["k"])
+        qbw.qmv_q4_0(Wd[l]["v"], buf["h"], buf["v"], 1, *shp["v"])
+        qbw.qmv_q4_0(Wd[l]["o"], buf["q"], buf["o"], 1, *shp["o"])
+        qbw.qmv_gateup_q4_0(Wd[l]["gate"], Wd[l]["up"], buf["o"], buf["a"], 1, *shp["gate"])
+        qbw.qmv_q4_0(Wd[l]["down"], buf["a"], buf["h"], 1, *shp["down"])
+        if keep:
+            snaps.append({n: buf[n].clone() for n in ("q", "k", "v", "o", "a", "h")})
+
+    # all layers enqueued back to back, snapshots taken on the same stream
+    for l in range(layers):
+        layer(l, keep=True)
+    torch.cuda.synchronize()
+    assert qbw.fault_read(clear=True) == 0
+
+    # the oracle's own chain
+    h = h0
+    for l in range(layers):
+        got = {n: to_f64(snaps[l][n]) for n in snaps[l]}
+        y, S = oracle.qmv("q4_0", W[l]["q"], h, *shp["q"])
+        check_matvec(got["q"], y, S, out_bf16=True, what=f"layer {l} q")
+        q = oracle.round_bf16(y)
+        for n in ("k", "v"):
+            y, S = oracle.qmv("q4_0", W[l][n], h, *shp[n])
+            check_matvec(got[n], y, S, out_bf16=True, what=f"layer {l} {n}")
+        y, S = oracle.qmv("q4_0", W[l]["o"], q, *shp["o"])
+        check_matvec(got["o"], y, S, out_bf16=True, what=f"layer {l} o")
+        o = oracle.round_bf16(y)
+        r = oracle.gateup_q4_0(W[l]["gate"], W[l]["up"], o, *shp["gate"])
+        check_gateup(got["a"], r, oracle, out_bf16=True, what=f"layer {l} gate+up")
+        a = oracle.round_bf16(r["out"])
+        y, S = oracle.qmv("q4_0", W[l]["down"], a, *shp["down"])
+        check_matvec(got["h"], y, S, out_bf16=True, what=f"layer {l} down")
+        h = oracle.round_bf16(y)
+    return snaps
+
+
+def test_sweep_two_layers_full_shapes(qbw, oracle):
+    # the 31B profile's shapes: hidden 5376, q 8192, k/v 4096, FFN 21504
+    run_chain(qbw, oracle, (5376, 8192, 4096, 21504), layers=2, seed=4)
+
+
+# fp16 scale pools for a chain of 512 -> 768 -> 512 ... Q4_0 matvecs whose
+# gain stays near one (the codes' mean of -1/2 makes the all-ones direction
+# grow by about K d / 2 per step): activations stay O(1) over 48 steps
+POOL_512 = np.array([0x1A41, 0x1B09, 0x1BD1, 0x1C4C, 0x1CB0], dtype=np.uint16)
+POOL_768 = np.array([0x1919, 0x19BC, 0x1A60, 0x1B03, 0x1BA6], dtype=np.uint16)
+
+
+def test_many_dependent_launches(qbw, oracle):
+    # 48 back-to-back launches, each consuming the previous one's bf16 output
+    steps, seed = 48, 11
+    mats = []
+    for i in range(steps):
+        N, K, pool = (768, 512, POOL_512) if i % 2 == 0 else (512, 768, POOL_768)
+        mats.append((N, K, synth.random_with_scale_bits("q4_0", N, K, seed * 100 + i, pool)))
+    h0 = synth.activations(512, seed=seed, dtype="bf16")
+    bufs = [bf16_dev(h0)] + [torch.empty(N, dtype=torch.bfloat16, device="cuda") for N, _, _ in mats]
+    wd = [torch.from_numpy(w).cuda() for _, _, w in mats]
+    for i, (N, K, _) in enumerate(mats):
+        qbw.qmv_q4_0(wd[i], bufs[i], bufs[i + 1], 1, N, K)
+    torch.cuda.synchronize()
+    h = h0
+    for i, (N, K, w) in enumerate(mats):
+        y, S = oracle.qmv("q4_0", w, h, N, K)
+        check_matvec(to_f64(bufs[i + 1]), y, S, out_bf16=True, what=f"step {i}")
+        h = oracle.round_bf16(y)
+    rms = float(np.sqrt(np.mean(oracle.bf16_to_f64(h) ** 2)))
+    assert 1e-2 < rms < 1e2
+
+
+def test_sweep_chain_is_deterministic(qbw, oracle):
+    a = run_chain(qbw, oracle, (512, 768, 256, 2048), layers=2, seed=12)
+    b = run_chain(qbw, oracle, (512, 768, 256, 2048), layers=2, seed=12)
+    for sa, sb in zip(a, b):
+        for n in sa:
+            assert torch.equal(sa[n].view(torch.int16), sb[n].view(torch.int16))
