@@ -136,7 +136,7 @@ bool plan_stream(int fmt, int nmat, int64_t N, int64_t K, const DeviceInfo& di, 
     const int nfull = (int)(npairs / 32);
     const int tail = (int)(npairs % 32);
     const int nitems = nfull + (tail ? 1 : 0);
-    const size_t xs_bytes = (size_t)K * 4;
+    const size_t xs_bytes = (size_t)npairs * 68 * 4;   // 64 activations per pair, padded to 68
     const size_t fixed = align_up(xs_bytes, 128);
     const int Rs_1[] = {8, 4, 2, 1};
     const int Rs_2[] = {4, 2, 1};

@@ -168,116 +168,146 @@ __device__ __forceinline__ void q4_chunk_H(uint32_t v, const Mags& g, uint64_t& 
 
 // ---------------------------------------------------------------- one pair
 // Accumulate one block pair of NR rows of NMAT matrices into acc.
-// rowaddr(m, r) is the shared-memory address of the pair in row (m, r).
+// rowaddr(m, r) is the shared-memory address of the pair in row (m, r); xaddr
+// the pair's 16 chunks of 4 activations.  Block A (chunks 0..7) of every row,
+// then block B (chunks 8..15): each row loads only the words of the block at
+// hand, and the scale is a half of one of them.
 template <int FMT, int NMAT, int NR, typename RowAddr>
-__device__ __forceinline__ void pair_dot(const RowAddr& rowaddr, uint32_t xaddr, uint32_t swz, const Mags& g,
+__device__ __forceinline__ void pair_dot(const RowAddr& rowaddr, uint32_t xaddr, const Mags& g,
                                          float (&acc)[NMAT][NR]) {
-    uint64_t bacc[NMAT][NR];
-    uint32_t vw[NMAT][NR];
-    uint32_t dA[NMAT][NR], dB[NMAT][NR];
 #pragma unroll
-    for (int m = 0; m < NMAT; ++m)
+    for (int blk = 0; blk < 2; ++blk) {
+        uint64_t xv[8][2];
 #pragma unroll
-        for (int r = 0; r < NR; ++r) { bacc[m][r] = 0ull; vw[m][r] = 0u; dA[m][r] = 0u; dB[m][r] = 0u; }
-
-#pragma unroll
-    for (int c = 0; c < 16; ++c) {
-        const float4 xv = lds128f(xaddr + (((uint32_t)c ^ swz) << 4));
-        const uint64_t x01 = pack2f(xv.x, xv.y);
-        const uint64_t x23 = pack2f(xv.z, xv.w);
+        for (int k = 0; k < 8; ++k) {
+            const float4 f = lds128f(xaddr + 16u * (uint32_t)(8 * blk + k));
+            xv[k][0] = pack2f(f.x, f.y);
+            xv[k][1] = pack2f(f.z, f.w);
+        }
 #pragma unroll
         for (int m = 0; m < NMAT; ++m)
 #pragma unroll
             for (int r = 0; r < NR; ++r) {
                 const uint32_t base = rowaddr(m, r);
-                uint64_t fa, fb;
+                uint64_t bacc = 0ull;
+                uint32_t dbits;
                 if constexpr (FMT == kFmtQ4) {
-                    if (q4_chunk_loads_word(c)) vw[m][r] = lds32(base + 4u * (uint32_t)q4_chunk_word(c));
-                    const uint32_t v = vw[m][r];
-                    if (c == 0) dA[m][r] = v;
-                    if (c == 7) dB[m][r] = v >> 16;
-                    if (q4_chunk_is_h(c)) q4_chunk_H(v, g, fa, fb);
-                    else q4_chunk_L(v, g, fa, fb);
+                    // block A: V0 (hi half), V1..V3, V4 (lo half); block B: V5..V8, dB in V4's hi half
+                    uint32_t v[5];
+#pragma unroll
+                    for (int i = 0; i < 5; ++i) v[i] = lds32(base + 4u * (uint32_t)(blk == 0 ? i : 4 + i));
+                    dbits = (blk == 0) ? v[0] : (v[0] >> 16);
+#pragma unroll
+                    for (int k = 0; k < 8; ++k) {
+                        const int c = 8 * blk + k;
+                        const uint32_t w = v[q4_chunk_word(c) - (blk == 0 ? 0 : 4)];
+                        uint64_t fa, fb;
+                        if (q4_chunk_is_h(c)) q4_chunk_H(w, g, fa, fb);
+                        else q4_chunk_L(w, g, fa, fb);
+                        ffma2(bacc, fa, xv[k][0]);
+                        ffma2(bacc, fb, xv[k][1]);
+                    }
                 } else {
-                    if (c == 0) {
-                        const uint32_t v0 = lds32(base);
-                        const uint32_t v8 = lds32(base + 32u);
-                        dA[m][r] = v0;
-                        dB[m][r] = v8 >> 16;
-                        const uint32_t h0 = v0 >> 16;
-                        fa = q8_codes2(h0, h0, g.q8a, g.q8b);
-                        fb = q8_codes2(v8, v8, g.q8a, g.q8b);
-                    } else {
-                        const uint32_t v = lds32(base + 4u * (uint32_t)((c < 8) ? c : c + 1));
-                        const uint32_t h = v >> 16;
-                        fa = q8_codes2(v, v, g.q8a, g.q8b);
-                        fb = q8_codes2(h, h, g.q8a, g.q8b);
+                    // block A: V0 (hi half), V1..V7, V8 (lo half); block B: V9..V16, dB in V8's hi half
+                    uint32_t v[9];
+#pragma unroll
+                    for (int i = 0; i < 9; ++i) v[i] = lds32(base + 4u * (uint32_t)(blk == 0 ? i : 8 + i));
+                    dbits = (blk == 0) ? v[0] : (v[0] >> 16);
+#pragma unroll
+                    for (int k = 0; k < 8; ++k) {
+                        uint64_t fa, fb;
+                        if (blk == 0 && k == 0) {
+                            const uint32_t h0 = v[0] >> 16;
+                            fa = q8_codes2(h0, h0, g.q8a, g.q8b);
+                            fb = q8_codes2(v[8], v[8], g.q8a, g.q8b);
+                        } else {
+                            const uint32_t w = v[blk == 0 ? k : k + 1];
+                            const uint32_t h = w >> 16;
+                            fa = q8_codes2(w, w, g.q8a, g.q8b);
+                            fb = q8_codes2(h, h, g.q8a, g.q8b);
+                        }
+                        ffma2(bacc, fa, xv[k][0]);
+                        ffma2(bacc, fb, xv[k][1]);
                     }
                 }
-                ffma2(bacc[m][r], fa, x01);
-                ffma2(bacc[m][r], fb, x23);
-                if (c == 7 || c == 15) {
-                    const float2 s = unpack2f(bacc[m][r]);
-                    const float t = s.x + s.y;
-                    const float d = half_bits_to_float(c == 7 ? dA[m][r] : dB[m][r]);
-                    acc[m][r] = fmaf(d, t, acc[m][r]);
-                    bacc[m][r] = 0ull;
-                }
+                const float2 sv = unpack2f(bacc);
+                acc[m][r] = fmaf(half_bits_to_float(dbits), sv.x + sv.y, acc[m][r]);
             }
     }
 }
 
-// Stage the activations in slot order: 64 fp32 per pair, 16-byte chunks
-// XOR-swizzled by pair index so that 8 lanes reading 8 consecutive pairs hit 8
-// distinct bank groups.  slot_of[e] is the slot of pair element e (filled by
-// the caller).  Every thread first issues all of its loads of 4 consecutive
-// elements (vector loads when x is aligned for them), then scatters them.
-template <int FMT>
-__device__ __forceinline__ void stage_activations(const StreamParams& p, uint8_t* smem, const uint8_t* slot_of) {
-    float* xs = reinterpret_cast<float*>(smem);
+// Activations of one pair in shared memory: 64 fp32 in slot order, padded to
+// 68 (272 bytes, 17 bank groups of 16 bytes), so 8 lanes reading the same
+// chunk of 8 consecutive pairs hit 8 distinct bank groups.
+constexpr int kXsPairFloats = 68;
+
+// Stage the activations in slot order.  slot_of[e] is the slot of pair element
+// e (filled by the caller).  Each thread loads groups of 4 consecutive
+// elements (vector loads when x is aligned for them); the first batch of
+// loads is issued by stage_activations_begin, before the caller starts the
+// weight copies, so that the activations are not queued behind them.
+constexpr int kStageBatch = 4;
+
+struct StageBatch {
+    float v[kStageBatch][4];
+};
+
+__device__ __forceinline__ void load_x4(const StreamParams& p, int i, float (&v)[4]) {
+    if (p.x_bf16) {
+        uint32_t lo, hi;
+        if (p.x_vec) {
+            const uint2 raw = __ldg(reinterpret_cast<const uint2*>(p.x) + i);
+            lo = raw.x;
+            hi = raw.y;
+        } else {
+            const unsigned short* h = reinterpret_cast<const unsigned short*>(p.x) + 4 * i;
+            lo = (uint32_t)__ldg(h) | ((uint32_t)__ldg(h + 1) << 16);
+            hi = (uint32_t)__ldg(h + 2) | ((uint32_t)__ldg(h + 3) << 16);
+        }
+        v[0] = __uint_as_float(lo << 16);
+        v[1] = __uint_as_float(lo & 0xFFFF0000u);
+        v[2] = __uint_as_float(hi << 16);
+        v[3] = __uint_as_float(hi & 0xFFFF0000u);
+    } else if (p.x_vec) {
+        const float4 f = __ldg(reinterpret_cast<const float4*>(p.x) + i);
+        v[0] = f.x; v[1] = f.y; v[2] = f.z; v[3] = f.w;
+    } else {
+        const float* f = reinterpret_cast<const float*>(p.x) + 4 * i;
+        v[0] = __ldg(f); v[1] = __ldg(f + 1); v[2] = __ldg(f + 2); v[3] = __ldg(f + 3);
+    }
+}
+
+__device__ __forceinline__ void load_batch(const StreamParams& p, int i0, StageBatch& bt) {
     const int n4 = p.K >> 2;
-    constexpr int U = 4;
-    for (int i0 = threadIdx.x; i0 < n4; i0 += U * blockDim.x) {
-        float v[U][4];
 #pragma unroll
-        for (int u = 0; u < U; ++u) {
-            const int i = i0 + u * blockDim.x;
-            if (i >= n4) break;
-            if (p.x_bf16) {
-                uint32_t lo, hi;
-                if (p.x_vec) {
-                    const uint2 raw = __ldg(reinterpret_cast<const uint2*>(p.x) + i);
-                    lo = raw.x;
-                    hi = raw.y;
-                } else {
-                    const unsigned short* h = reinterpret_cast<const unsigned short*>(p.x) + 4 * i;
-                    lo = (uint32_t)__ldg(h) | ((uint32_t)__ldg(h + 1) << 16);
-                    hi = (uint32_t)__ldg(h + 2) | ((uint32_t)__ldg(h + 3) << 16);
-                }
-                v[u][0] = __uint_as_float(lo << 16);
-                v[u][1] = __uint_as_float(lo & 0xFFFF0000u);
-                v[u][2] = __uint_as_float(hi << 16);
-                v[u][3] = __uint_as_float(hi & 0xFFFF0000u);
-            } else if (p.x_vec) {
-                const float4 f = __ldg(reinterpret_cast<const float4*>(p.x) + i);
-                v[u][0] = f.x; v[u][1] = f.y; v[u][2] = f.z; v[u][3] = f.w;
-            } else {
-                const float* f = reinterpret_cast<const float*>(p.x) + 4 * i;
-                v[u][0] = __ldg(f); v[u][1] = __ldg(f + 1); v[u][2] = __ldg(f + 2); v[u][3] = __ldg(f + 3);
-            }
-        }
+    for (int u = 0; u < kStageBatch; ++u) {
+        const int i = i0 + u * (int)blockDim.x;
+        if (i < n4) load_x4(p, i, bt.v[u]);
+    }
+}
+
+__device__ __forceinline__ void store_batch(const StreamParams& p, int i0, const StageBatch& bt, float* xs,
+                                            const uint8_t* slot_of) {
+    const int n4 = p.K >> 2;
 #pragma unroll
-        for (int u = 0; u < U; ++u) {
-            const int i = i0 + u * blockDim.x;
-            if (i >= n4) break;
-            const int q = i >> 4;              // pair (64 elements = 16 groups of 4)
-            const uint32_t swz = (uint32_t)q & 7u;
+    for (int u = 0; u < kStageBatch; ++u) {
+        const int i = i0 + u * (int)blockDim.x;
+        if (i >= n4) break;
+        const int q = i >> 4;              // pair (64 elements = 16 groups of 4)
 #pragma unroll
-            for (int t = 0; t < 4; ++t) {
-                const int s = slot_of[((i & 15) << 2) + t];
-                xs[q * 64 + (int)((((uint32_t)(s >> 2)) ^ swz) << 2) + (s & 3)] = v[u][t];
-            }
-        }
+        for (int t = 0; t < 4; ++t) xs[q * kXsPairFloats + slot_of[((i & 15) << 2) + t]] = bt.v[u][t];
+    }
+}
+
+// Finish staging: store the first batch, then load and store the rest.
+__device__ __forceinline__ void stage_activations_end(const StreamParams& p, const StageBatch& first, float* xs,
+                                                      const uint8_t* slot_of) {
+    store_batch(p, (int)threadIdx.x, first, xs, slot_of);
+    const int n4 = p.K >> 2;
+    for (int i0 = (int)threadIdx.x + kStageBatch * (int)blockDim.x; i0 < n4; i0 += kStageBatch * (int)blockDim.x) {
+        StageBatch bt;
+        load_batch(p, i0, bt);
+        store_batch(p, i0, bt, xs, slot_of);
     }
 }
 
@@ -327,14 +357,17 @@ __global__ void __launch_bounds__(512, 1) qmv_stream_kernel(const __grid_constan
     const int D = p.depth;
 
     const uint32_t sbase = smem_u32(smem);
-    const uint32_t xs = sbase;                                    // 64 fp32 per pair
+    const uint32_t xs = sbase;                                    // kXsPairFloats fp32 per pair
     const uint32_t ring = sbase + p.ring_off + (uint32_t)warp * (uint32_t)D * kStage;
     const uint32_t bars = sbase + p.bar_off + (uint32_t)warp * (uint32_t)D * 8u;
     float* part = reinterpret_cast<float*>(smem + p.part_off);
 
     // this CTA's groups and items
-    const int g0 = (int)((int64_t)p.ngroups * blockIdx.x / gridDim.x);
-    const int g1 = (int)((int64_t)p.ngroups * (blockIdx.x + 1) / gridDim.x);
+    // groups [g0, g1): ngroups split into gridDim.x near-equal contiguous ranges
+    const int gq = p.ngroups / (int)gridDim.x, gr = p.ngroups - gq * (int)gridDim.x;
+    const int b = (int)blockIdx.x;
+    const int g0 = b * gq + (b < gr ? b : gr);
+    const int g1 = g0 + gq + (b < gr ? 1 : 0);
     const int nitems = p.nfull + (p.tail_pairs ? 1 : 0);
     const int n_items = (g1 - g0) * nitems;
     const int mine = (n_items > warp) ? (n_items - warp + W - 1) / W : 0;
@@ -357,9 +390,11 @@ __global__ void __launch_bounds__(512, 1) qmv_stream_kernel(const __grid_constan
     };
 
     // the item after (lg, c) for this warp: c advances by W chunks
+    const int step_g = W / nitems, step_c = W - (W / nitems) * nitems;
     auto next_item = [&](int& lg_, int& c_) {
-        c_ += W;
-        while (c_ >= nitems) { c_ -= nitems; ++lg_; }
+        lg_ += step_g;
+        c_ += step_c;
+        if (c_ >= nitems) { c_ -= nitems; ++lg_; }
     };
 
     if (lane == 0) {
@@ -368,7 +403,17 @@ __global__ void __launch_bounds__(512, 1) qmv_stream_kernel(const __grid_constan
         prefetch_tmap(&p.tmap[0]);
         if (NMAT == 2) prefetch_tmap(&p.tmap[1]);
     }
+    if (threadIdx.x < 64)
+        slot_of[FMT == kFmtQ4 ? q4_slot_element(threadIdx.x) : q8_slot_element(threadIdx.x)] = (uint8_t)threadIdx.x;
     __syncwarp();
+
+    // The activations may come from the preceding grid: wait for it, then
+    // issue their loads before the weight copies so they are not queued
+    // behind them.
+    grid_dependency_wait();
+    StageBatch first;
+    load_batch(p, (int)threadIdx.x, first);
+
     // producer cursor (lane 0): the item D ahead of the consumer
     int plg = warp / nitems, pc = warp - (warp / nitems) * nitems, pst = 0;
     if (lane == 0)
@@ -378,13 +423,8 @@ __global__ void __launch_bounds__(512, 1) qmv_stream_kernel(const __grid_constan
             if (++pst == D) pst = 0;
         }
 
-    if (threadIdx.x < 64)
-        slot_of[FMT == kFmtQ4 ? q4_slot_element(threadIdx.x) : q8_slot_element(threadIdx.x)] = (uint8_t)threadIdx.x;
-    // Everything above touched only the weights (already in flight) and this
-    // CTA's shared memory.  The activations may come from the preceding grid.
-    grid_dependency_wait();
-    __syncthreads();
-    stage_activations<FMT>(p, smem, slot_of);
+    __syncthreads();                    // slot table complete
+    stage_activations_end(p, first, reinterpret_cast<float*>(smem), slot_of);
     __syncthreads();
     grid_launch_dependents();
 
@@ -415,7 +455,7 @@ __global__ void __launch_bounds__(512, 1) qmv_stream_kernel(const __grid_constan
             auto rowaddr = [&](int m, int r) {
                 return stage + (uint32_t)m * kMat + (uint32_t)r * kRowBytes + poff;
             };
-            pair_dot<FMT, NMAT, R>(rowaddr, xs + (uint32_t)q * 256u, (uint32_t)q & 7u, g, acc);
+            pair_dot<FMT, NMAT, R>(rowaddr, xs + (uint32_t)q * (4u * kXsPairFloats), g, acc);
         } else {
             // final short chunk: (row, pair) items spread over the lanes
             const int items = R * p.tail_pairs;
@@ -430,7 +470,7 @@ __global__ void __launch_bounds__(512, 1) qmv_stream_kernel(const __grid_constan
                                           : (uint32_t)(qq >> 4) * kHalf + (uint32_t)(qq & 15) * F::kPairBytes;
                 const uint32_t rbase = stage + (uint32_t)r * (uint32_t)(box_words(FMT) * 8) + poff;
                 auto rowaddr = [&](int m, int) { return rbase + (uint32_t)m * kMat; };
-                pair_dot<FMT, NMAT, 1>(rowaddr, xs + (uint32_t)q * 256u, (uint32_t)q & 7u, g, one);
+                pair_dot<FMT, NMAT, 1>(rowaddr, xs + (uint32_t)q * (4u * kXsPairFloats), g, one);
 #pragma unroll
                 for (int m = 0; m < NMAT; ++m)
 #pragma unroll
