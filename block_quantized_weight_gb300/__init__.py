@@ -142,8 +142,9 @@ def qmm_q4_0_smallM_workspace_bytes(M: int, N: int, K: int) -> int:
 def qmm_q4_0_smallM(w, X, Y, M: int, N: int, K: int, workspace=None, stream=None):
     """Y[M, N] = X[M, K] W^T for raw Q4_0 blocks ``w`` on the tensor cores.
 
-    ``workspace`` is a zero-filled uint8 device tensor of at least
-    ``qmm_q4_0_smallM_workspace_bytes(M, N, K)`` bytes (left zero-filled).
+    ``workspace`` is a uint8 device tensor of at least
+    ``qmm_q4_0_smallM_workspace_bytes(M, N, K)`` bytes, zero-filled once when
+    allocated (the library returns its counters to zero after every call).
     """
     L = load()
     wbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()

@@ -24,6 +24,11 @@ cudaError_t prepare_stream_q8(int R, size_t smem);
 cudaError_t prepare_stream_gateup(int R, size_t smem);
 cudaError_t launch_qmm_generic(const uint8_t* w, const void* X, void* Y, int y_bf16, int64_t M, int64_t N,
                                int64_t K, int sm_count, cudaStream_t stream);
+cudaError_t launch_qmm_tc(const CUtensorMap& tmap_w, const CUtensorMap& tmap_x, void* y, int y_bf16, float* partials,
+                          unsigned int* counters, unsigned int* fault, int M, int N, int K, int splits,
+                          cudaStream_t stream);
+int qmm_tc_tile_rows();
+int qmm_tc_group_k();
 
 namespace {
 
@@ -205,6 +210,46 @@ bool plan_stream(int fmt, int nmat, int64_t N, int64_t K, const DeviceInfo& di, 
     return true;
 }
 
+// X [M][K] bf16 row-major as a 2-D tensor; box (64, nt) with the 128-byte
+// swizzle of the tensor-core B operand.
+bool encode_x_map(CUtensorMap* m, const void* X, int64_t M, int64_t K, int nt) {
+    PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+    if (!enc) return false;
+    cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)M};
+    cuuint64_t strides[1] = {(cuuint64_t)(K * 2)};
+    cuuint32_t box[2] = {64, (cuuint32_t)nt};
+    cuuint32_t estr[2] = {1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(X), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Split-K plan of the tensor-core small-M kernel: 128-row tiles, each split
+// over `splits` CTAs (at most one CTA per SM in all), K-groups of 256.
+struct QmmPlan {
+    bool tc = false;
+    int tiles = 0, splits = 1;
+    size_t partial_bytes = 0, counter_off = 0, workspace = 0;
+};
+
+QmmPlan plan_qmm(int64_t M, int64_t N, int64_t K, int sm_count) {
+    QmmPlan q;
+    if (M < 1 || M > 32 || K % 256 != 0 || N < 1) return q;
+    q.tc = true;
+    q.tiles = (int)((N + qmm_tc_tile_rows() - 1) / qmm_tc_tile_rows());
+    const int groups = (int)(K / qmm_tc_group_k());
+    int splits = sm_count / q.tiles;
+    if (splits < 1) splits = 1;
+    if (splits > groups) splits = groups;
+    q.splits = splits;
+    if (splits > 1) {
+        q.partial_bytes = align_up((size_t)splits * (size_t)M * (size_t)N * 4, 256);
+        q.counter_off = q.partial_bytes;
+        q.workspace = q.partial_bytes + align_up((size_t)q.tiles * 4, 256);
+    }
+    return q;
+}
+
 int r_index(int R) { return R == 1 ? 0 : R == 2 ? 1 : R == 4 ? 2 : 3; }
 
 qbw_status launch_streaming(int fmt, int nmat, DeviceInfo& di, const StreamPlan& plan, cudaStream_t s) {
@@ -303,16 +348,13 @@ qbw_status qmv_gateup_q4_0(const void* w_gate, const void* w_up, const void* x, 
 }
 
 size_t qmm_q4_0_smallM_workspace_bytes(int64_t M, int64_t N, int64_t K) {
-    (void)M;
-    (void)N;
-    (void)K;
-    return 0;
+    DeviceInfo* di = nullptr;
+    if (device_info(&di) != QBW_OK) return 0;
+    return plan_qmm(M, N, K, di->sm_count).workspace;
 }
 
 qbw_status qmm_q4_0_smallM(const void* w, const void* X, qbw_dtype xt, void* Y, qbw_dtype yt, int64_t M,
                            int64_t N, int64_t K, void* workspace, size_t workspace_bytes, void* stream) {
-    (void)workspace;
-    (void)workspace_bytes;
     if (!w || !X || !Y) return QBW_EINVAL;
     if (xt != QBW_BF16 || !valid_dtype(yt)) return QBW_EDTYPE;
     if (M < 1 || M > 32 || N < 1 || N > INT32_MAX || K < 32 || K % 32 != 0 || K > (int64_t(1) << 24))
@@ -324,8 +366,38 @@ qbw_status qmm_q4_0_smallM(const void* w, const void* X, qbw_dtype xt, void* Y, 
     DeviceInfo* di = nullptr;
     qbw_status st = device_info(&di);
     if (st != QBW_OK) return st;
-    cudaError_t e = launch_qmm_generic(static_cast<const uint8_t*>(w), X, Y, yt == QBW_BF16, M, N, K, di->sm_count,
-                                       static_cast<cudaStream_t>(stream));
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const QmmPlan q = plan_qmm(M, N, K, di->sm_count);
+    if (q.tc && (uintptr_t)w % 16 == 0 && (uintptr_t)X % 16 == 0) {
+        if (q.workspace) {
+            if (!workspace || workspace_bytes < q.workspace || (uintptr_t)workspace % 256) return QBW_EWORKSPACE;
+            if (overlaps(workspace, q.workspace, Y, ybytes) || overlaps(workspace, q.workspace, X, (size_t)M * K * 2) ||
+                overlaps(workspace, q.workspace, w, (size_t)N * (K / 32) * 18))
+                return QBW_EINVAL;
+        }
+        CUtensorMap tw, tx;
+        const int nt = (int)((M + 15) / 16 * 16);
+        PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+        bool maps = enc != nullptr;
+        if (maps) {
+            cuuint64_t dims[2] = {(cuuint64_t)((K / 32) * 18 / 8), (cuuint64_t)N};
+            cuuint64_t strides[1] = {(cuuint64_t)((K / 32) * 18)};
+            cuuint32_t box[2] = {(cuuint32_t)(144 / 8), (cuuint32_t)qmm_tc_tile_rows()};
+            cuuint32_t estr[2] = {1, 1};
+            maps = enc(&tw, CU_TENSOR_MAP_DATA_TYPE_UINT64, 2, const_cast<void*>(w), dims, strides, box, estr,
+                       CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                       CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS &&
+                   encode_x_map(&tx, X, M, K, nt);
+        }
+        if (maps) {
+            uint8_t* ws = static_cast<uint8_t*>(workspace);
+            cudaError_t e = launch_qmm_tc(tw, tx, Y, yt == QBW_BF16, q.workspace ? reinterpret_cast<float*>(ws) : nullptr,
+                                          q.workspace ? reinterpret_cast<unsigned int*>(ws + q.counter_off) : nullptr,
+                                          di->fault, (int)M, (int)N, (int)K, q.splits, s);
+            return e == cudaSuccess ? QBW_OK : QBW_ECUDA;
+        }
+    }
+    cudaError_t e = launch_qmm_generic(static_cast<const uint8_t*>(w), X, Y, yt == QBW_BF16, M, N, K, di->sm_count, s);
     return e == cudaSuccess ? QBW_OK : QBW_ECUDA;
 }
 

@@ -147,11 +147,16 @@ qbw_status qmv_gateup_q4_0(const void *w_gate, const void *w_up, const void *x, 
  *   Y : [M, N] row-major, QBW_BF16 or QBW_F32
  *   M : 1 .. 32 (tuned for 8, 16, 32)          N >= 1, K % 32 == 0
  *   workspace : device scratch of at least
- *               qmm_q4_0_smallM_workspace_bytes(M, N, K) bytes, 256-byte
- *               aligned, ZERO-FILLED before its first use; every call leaves
- *               it zero-filled again.  Calls that share one workspace must
- *               not run concurrently.  May be NULL when the size query
- *               returns 0.
+ *               qmm_q4_0_smallM_workspace_bytes(M, N, K) bytes (size for the
+ *               current device), 256-byte aligned, ZERO-FILLED once before
+ *               its first use.  It holds the split-K partial sums and one
+ *               arrival counter per 128-row tile; every call returns the
+ *               counters to zero, so the single zero-fill at allocation is
+ *               enough.  Calls that share one workspace must not run
+ *               concurrently.  May be NULL when the size query returns 0.
+ *
+ * Fast path: K % 256 == 0 and w, X 16-byte aligned (tcgen05 tensor cores);
+ * other shapes take an exact CUDA-core path that needs no workspace.
  */
 size_t qmm_q4_0_smallM_workspace_bytes(int64_t M, int64_t N, int64_t K);
 qbw_status qmm_q4_0_smallM(const void *w, const void *X, qbw_dtype xt, void *Y, qbw_dtype yt,

@@ -1,0 +1,112 @@
+"""GPU parity of the small-M tensor-core product qmm_q4_0_smallM (prefill
+tiles of up to 32 tokens) against the CPU oracle on the same seeded bytes.
+
+The pass rule is 1e-2 of S = sum_k |x w| per output (weights are rounded to
+bf16 once on chip: at most 2^-8 relative; the bf16 activations are exact),
+plus half an ulp of bf16 when the output is bf16.  Small shapes are compared
+in full; the full-size shapes (5376 x 5376 and 5376 x 21504, M = 8, 16, 32)
+on row ranges from the first, a middle and the last 128-row tile.
+"""
+import numpy as np
+import pytest
+
+import synth
+from tolerance import check_matvec, to_f64
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+
+
+def dev_u8(a):
+    return torch.from_numpy(np.ascontiguousarray(a)).cuda()
+
+
+def dev_bf16(bits):
+    return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16).copy()).view(torch.bfloat16).cuda()
+
+
+def workspace(qbw, M, N, K):
+    nbytes = qbw.qmm_q4_0_smallM_workspace_bytes(M, N, K)
+    return torch.zeros(max(nbytes, 256), dtype=torch.uint8, device="cuda"), nbytes
+
+
+def run_qmm(qbw, w, X, M, N, K, odt, calls=2):
+    # several calls on one workspace: its counters must come back to zero
+    ws, nbytes = workspace(qbw, M, N, K)
+    wd, Xd = dev_u8(w), dev_bf16(X)
+    outs = []
+    for _ in range(calls):
+        Y = torch.full((M, N), float("nan"), dtype=odt, device="cuda")
+        qbw.qmm_q4_0_smallM(wd, Xd, Y, M, N, K, workspace=ws)
+        outs.append(Y)
+    torch.cuda.synchronize()
+    assert qbw.fault_read(clear=True) == 0
+    for Y in outs[1:]:
+        assert torch.equal(Y.view(torch.int16) if odt == torch.bfloat16 else Y.view(torch.int32),
+                           outs[0].view(torch.int16) if odt == torch.bfloat16 else outs[0].view(torch.int32))
+    return to_f64(outs[0])
+
+
+@pytest.mark.parametrize("M", [1, 3, 8, 16, 17, 32])
+@pytest.mark.parametrize("N,K", [(128, 256), (300, 512), (1000, 2304), (129, 4096), (64, 96)])
+@pytest.mark.parametrize("odt", [torch.bfloat16, torch.float32])
+def test_qmm_small(qbw, oracle, M, N, K, odt):
+    w = synth.q4_0_weights(N, K, seed=N + K + M)
+    X = synth.activations((M, K), seed=M * 31 + K, dtype="bf16")
+    Y = run_qmm(qbw, w, X, M, N, K, odt)
+    Y_ref, S = oracle.qmm_q4_0(w, X, M, N, K)
+    check_matvec(Y, Y_ref, S, rel=1e-2, out_bf16=(odt == torch.bfloat16), what=f"qmm M={M} N={N} K={K}")
+
+
+@pytest.mark.parametrize("M", [8, 16, 32])
+@pytest.mark.parametrize("K", [5376, 21504])
+def test_qmm_full_size_sampled(qbw, oracle, M, K):
+    N = 5376
+    w = synth.q4_0_weights(N, K, seed=3)
+    X = synth.activations((M, K), seed=3, dtype="bf16")
+    Y = run_qmm(qbw, w, X, M, N, K, torch.bfloat16)
+    for n0, n1 in ((0, 128), (2600, 2728), (N - 128, N)):
+        for m in range(M):
+            y_ref, S = oracle.qmv_rows("q4_0", w, X[m], n0, n1, K)
+            check_matvec(Y[m, n0:n1], y_ref, S, rel=1e-2, out_bf16=True, what=f"qmm full M={M} K={K} m={m}")
+
+
+def test_qmm_deterministic(qbw):
+    M, N, K = 32, 1024, 5376
+    w = dev_u8(synth.q4_0_weights(N, K, seed=9))
+    X = dev_bf16(synth.activations((M, K), seed=9, dtype="bf16"))
+    ws, _ = workspace(qbw, M, N, K)
+    Y1 = torch.empty(M, N, device="cuda")
+    Y2 = torch.empty(M, N, device="cuda")
+    qbw.qmm_q4_0_smallM(w, X, Y1, M, N, K, workspace=ws)
+    qbw.qmm_q4_0_smallM(w, X, Y2, M, N, K, workspace=ws)
+    torch.cuda.synchronize()
+    assert torch.equal(Y1.view(torch.int32), Y2.view(torch.int32))
+
+
+def test_qmm_constant_weights_closed_form(qbw, oracle):
+    # every weight d * (c - 8) with d = 0.5, c = 11: Y[m, n] = 1.5 * sum_k X[m, k]
+    M, N, K = 8, 256, 2048
+    w = synth.constant_blocks("q4_0", N, K, 0x3800, 11)
+    X = synth.activations((M, K), seed=2, dtype="bf16")
+    Y = run_qmm(qbw, w, X, M, N, K, torch.float32)
+    Y_ref, S = oracle.qmm_q4_0(w, X, M, N, K)
+    check_matvec(Y, Y_ref, S, rel=1e-2, what="constant")
+    zero = synth.constant_blocks("q4_0", N, K, 0x3C00, 8)
+    Yz = run_qmm(qbw, zero, X, M, N, K, torch.float32)
+    assert np.all(Yz == 0.0)
+
+
+def test_qmm_workspace_too_small_is_rejected(qbw):
+    M, N, K = 16, 5376, 5376
+    need = qbw.qmm_q4_0_smallM_workspace_bytes(M, N, K)
+    if need == 0:
+        pytest.skip("this device plans no split for the shape")
+    w = dev_u8(synth.q4_0_weights(N, K, seed=1))
+    X = dev_bf16(synth.activations((M, K), seed=1, dtype="bf16"))
+    Y = torch.empty(M, N, dtype=torch.bfloat16, device="cuda")
+    small = torch.zeros(need // 2, dtype=torch.uint8, device="cuda")
+    with pytest.raises(qbw.QbwError) as e:
+        qbw.qmm_q4_0_smallM(w, X, Y, M, N, K, workspace=small)
+    assert e.value.status == 6
