@@ -226,10 +226,16 @@ bool encode_x_map(CUtensorMap* m, const void* X, int64_t M, int64_t K, int nt) {
 
 // Split-K plan of the tensor-core small-M kernel: 128-row tiles, each split
 // over `splits` CTAs (at most one CTA per SM in all), K-groups of 256.
+//
+// Workspace layout, the same for every shape so that one workspace can serve
+// calls of different shapes: the tile arrival counters first, in a fixed
+// region of kQmmCounterBytes, then the partial sums.  Each call returns its
+// counters to zero, and no call's partial sums ever land on a counter.
+constexpr size_t kQmmCounterBytes = 4096;
 struct QmmPlan {
     bool tc = false;
     int tiles = 0, splits = 1;
-    size_t partial_bytes = 0, counter_off = 0, workspace = 0;
+    size_t partial_off = 0, workspace = 0;
 };
 
 QmmPlan plan_qmm(int64_t M, int64_t N, int64_t K, int sm_count) {
@@ -241,11 +247,11 @@ QmmPlan plan_qmm(int64_t M, int64_t N, int64_t K, int sm_count) {
     int splits = sm_count / q.tiles;
     if (splits < 1) splits = 1;
     if (splits > groups) splits = groups;
+    if ((size_t)q.tiles * 4 > kQmmCounterBytes) splits = 1;
     q.splits = splits;
     if (splits > 1) {
-        q.partial_bytes = align_up((size_t)splits * (size_t)M * (size_t)N * 4, 256);
-        q.counter_off = q.partial_bytes;
-        q.workspace = q.partial_bytes + align_up((size_t)q.tiles * 4, 256);
+        q.partial_off = kQmmCounterBytes;
+        q.workspace = kQmmCounterBytes + align_up((size_t)splits * (size_t)M * (size_t)N * 4, 256);
     }
     return q;
 }
@@ -391,8 +397,9 @@ qbw_status qmm_q4_0_smallM(const void* w, const void* X, qbw_dtype xt, void* Y, 
         }
         if (maps) {
             uint8_t* ws = static_cast<uint8_t*>(workspace);
-            cudaError_t e = launch_qmm_tc(tw, tx, Y, yt == QBW_BF16, q.workspace ? reinterpret_cast<float*>(ws) : nullptr,
-                                          q.workspace ? reinterpret_cast<unsigned int*>(ws + q.counter_off) : nullptr,
+            cudaError_t e = launch_qmm_tc(tw, tx, Y, yt == QBW_BF16,
+                                          q.workspace ? reinterpret_cast<float*>(ws + q.partial_off) : nullptr,
+                                          q.workspace ? reinterpret_cast<unsigned int*>(ws) : nullptr,
                                           di->fault, (int)M, (int)N, (int)K, q.splits, s);
             return e == cudaSuccess ? QBW_OK : QBW_ECUDA;
         }

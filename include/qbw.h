@@ -149,11 +149,13 @@ qbw_status qmv_gateup_q4_0(const void *w_gate, const void *w_up, const void *x, 
  *   workspace : device scratch of at least
  *               qmm_q4_0_smallM_workspace_bytes(M, N, K) bytes (size for the
  *               current device), 256-byte aligned, ZERO-FILLED once before
- *               its first use.  It holds the split-K partial sums and one
- *               arrival counter per 128-row tile; every call returns the
- *               counters to zero, so the single zero-fill at allocation is
- *               enough.  Calls that share one workspace must not run
- *               concurrently.  May be NULL when the size query returns 0.
+ *               its first use.  It holds one arrival counter per 128-row
+ *               tile in a fixed 4096-byte region at its start, then the
+ *               split-K partial sums.  Every call returns the counters to
+ *               zero, so the single zero-fill at allocation is enough, also
+ *               when one workspace serves calls of different shapes.  Calls
+ *               that share one workspace must not run concurrently.  May be
+ *               NULL when the size query returns 0.
  *
  * Fast path: K % 256 == 0 and w, X 16-byte aligned (tcgen05 tensor cores);
  * other shapes take an exact CUDA-core path that needs no workspace.

@@ -110,3 +110,26 @@ def test_qmm_workspace_too_small_is_rejected(qbw):
     with pytest.raises(qbw.QbwError) as e:
         qbw.qmm_q4_0_smallM(w, X, Y, M, N, K, workspace=small)
     assert e.value.status == 6
+
+
+def test_qmm_workspace_shared_across_shapes(qbw):
+    # One workspace, zero-filled once, serves calls of different shapes in turn:
+    # every call must find its arrival counters at zero, whatever the partial
+    # sums of an earlier shape left behind.
+    shapes = [(16, 5376, 5376), (17, 256, 2048), (32, 128, 21504), (8, 640, 4096), (32, 1024, 5376),
+              (16, 5376, 5376)]
+    size = max(qbw.qmm_q4_0_smallM_workspace_bytes(M, N, K) for M, N, K in shapes)
+    if size == 0:
+        pytest.skip("this device plans no split for these shapes")
+    shared = torch.zeros(size, dtype=torch.uint8, device="cuda")
+    for i, (M, N, K) in enumerate(shapes):
+        w = dev_u8(synth.q4_0_weights(N, K, seed=40 + i))
+        X = dev_bf16(synth.activations((M, K), seed=40 + i, dtype="bf16"))
+        fresh, _ = workspace(qbw, M, N, K)
+        Y_fresh = torch.empty(M, N, device="cuda")
+        Y_shared = torch.empty(M, N, device="cuda")
+        qbw.qmm_q4_0_smallM(w, X, Y_fresh, M, N, K, workspace=fresh)
+        qbw.qmm_q4_0_smallM(w, X, Y_shared, M, N, K, workspace=shared)
+        torch.cuda.synchronize()
+        assert torch.equal(Y_shared.view(torch.int32), Y_fresh.view(torch.int32)), (M, N, K)
+    assert qbw.fault_read(clear=True) == 0
