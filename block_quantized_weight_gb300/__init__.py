@@ -18,7 +18,7 @@ import threading
 __all__ = [
     "QbwError", "load", "lib_path",
     "qmv_q8_0", "qmv_q4_0", "qmv_gateup_q4_0", "qmm_q4_0_smallM", "qmm_q4_0_smallM_workspace_bytes",
-    "qdequant_q8_0", "qdequant_q4_0", "fault_read", "status_str", "version",
+    "qmm_q4_0_smallM_noalloc", "NOALLOC_SCRATCH_BYTES", "qdequant_q8_0", "qdequant_q4_0", "fault_read", "status_str", "version",
     "F32", "BF16",
 ]
 
@@ -28,6 +28,7 @@ _lock = threading.Lock()
 _lib = None
 
 F32, BF16 = 0, 1
+NOALLOC_SCRATCH_BYTES = 4 << 20  # QBW_QMM_NOALLOC_SCRATCH_BYTES
 QBW_OK = 0
 
 
@@ -70,6 +71,8 @@ def _declare(L):
     L.qmm_q4_0_smallM_workspace_bytes.argtypes = [i64, i64, i64]
     L.qmm_q4_0_smallM.restype = i32
     L.qmm_q4_0_smallM.argtypes = [P, P, i32, P, i32, i64, i64, i64, P, sz, P]
+    L.qmm_q4_0_smallM_noalloc.restype = i32
+    L.qmm_q4_0_smallM_noalloc.argtypes = [P, P, i32, P, i32, i64, i64, i64, P]
     for name in ("qdequant_q8_0", "qdequant_q4_0"):
         getattr(L, name).restype = i32
         getattr(L, name).argtypes = [P, P, i64, i64, P]
@@ -150,6 +153,15 @@ def qmm_q4_0_smallM(w, X, Y, M: int, N: int, K: int, workspace=None, stream=None
     wbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     _check(L.qmm_q4_0_smallM(_ptr(w), _ptr(X), _dtype_code(X), _ptr(Y), _dtype_code(Y), M, N, K,
                              _ptr(workspace), wbytes, _stream(stream)), "qmm_q4_0_smallM")
+    return Y
+
+
+def qmm_q4_0_smallM_noalloc(w, X, Y, M: int, N: int, K: int, stream=None):
+    """qmm_q4_0_smallM with the library's static scratch instead of a caller
+    workspace, for callers that cannot allocate device memory.  Calls on one
+    device must not overlap in time; the first one does a one-time set-up."""
+    _check(load().qmm_q4_0_smallM_noalloc(_ptr(w), _ptr(X), _dtype_code(X), _ptr(Y), _dtype_code(Y), M, N, K,
+                                          _stream(stream)), "qmm_q4_0_smallM_noalloc")
     return Y
 
 

@@ -166,6 +166,34 @@ qbw_status qmm_q4_0_smallM(const void *w, const void *X, qbw_dtype xt, void *Y, 
                            void *stream);
 
 /*
+ * qmm_q4_0_smallM_noalloc -- qmm_q4_0_smallM without a workspace argument, for
+ * callers that cannot allocate device memory at the call (an engine that has
+ * handed all of HBM to weights and KV cache up front, a plain C host program
+ * with no device allocator of its own).  The published descriptions of the
+ * method have no counterpart to this call; it is a convenience of this library.
+ *
+ * The split-K scratch is a static device array of QBW_QMM_NOALLOC_SCRATCH_BYTES
+ * inside the library; nothing is allocated or freed.  A request that needs more
+ * scratch than that (qmm_q4_0_smallM_workspace_bytes(M, N, K) > the limit)
+ * returns QBW_EWORKSPACE and launches nothing.  On a 152-SM GB300 every legal
+ * shape needs at most 2,494,464 bytes, so the limit is only reached on parts
+ * with more SMs.
+ *
+ * The first call on each device that needs scratch does a one-time set-up: it
+ * looks up the array's address on that device and zero-fills it on `stream`
+ * (the arrival counters must start at zero; every completed call leaves them at
+ * zero).  Make that first call before any stream capture.
+ *
+ * All calls on one device share the one array: calls that may overlap in time
+ * (different streams without ordering, several host threads) race on it and
+ * give wrong results.  Arguments, results and errors are otherwise those of
+ * qmm_q4_0_smallM, and the results are bit-identical to it.
+ */
+#define QBW_QMM_NOALLOC_SCRATCH_BYTES ((size_t)4 << 20)
+qbw_status qmm_q4_0_smallM_noalloc(const void *w, const void *X, qbw_dtype xt, void *Y, qbw_dtype yt,
+                                   int64_t M, int64_t N, int64_t K, void *stream);
+
+/*
  * qdequant_q8_0 / qdequant_q4_0 -- expand a whole matrix to fp32:
  * out[n*K + k] = w[n, k].  Every product d*q is exact in fp32, so the result is
  * bit-exact.  Meant for testing and inspection, not for the hot path.
