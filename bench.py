@@ -88,26 +88,35 @@ def load_peaks():
     return 6800.0, "fallback", {}
 
 
-def kernel_source_hash():
+# Sources whose change voids a kernel's profiled DRAM traffic (device code and
+# the host-side launch plan).
+KERNEL_SOURCES = {
+    "qmv_q4_0": ("qbw_device.cuh", "qbw_internal.h", "qmv_stream.cuh", "qmv_stream_q4.cu", "api.cu"),
+    "qmv_gateup_q4_0": ("qbw_device.cuh", "qbw_internal.h", "qmv_stream.cuh", "qmv_stream_gateup.cu", "api.cu"),
+}
+TRAFFIC_SUMMARY = os.path.join(ROOT, "profiles", "qmv_sweep_layer_traffic.txt")
+
+
+def kernel_source_hash(kernel: str):
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "block_quantized_weight_gb300", "csrc")
-    for f in sorted(os.listdir(csrc)):
+    for f in KERNEL_SOURCES[kernel]:
         h.update(f.encode())
         h.update(open(os.path.join(csrc, f), "rb").read())
     return h.hexdigest()[:16]
 
 
 def profiled_traffic(kernel: str):
-    """DRAM bytes per launch from the committed ncu summary, or None when the
-    kernel sources changed since it was captured."""
-    p = os.path.join(ROOT, "profiles", "traffic.json")
-    if not os.path.exists(p):
+    """DRAM bytes per launch of ``kernel`` in the sweep, from the committed ncu
+    summary (lines ``traffic <kernel> <bytes per launch> <source hash>``), or
+    None when the kernel's sources changed since the capture."""
+    if kernel not in KERNEL_SOURCES or not os.path.exists(TRAFFIC_SUMMARY):
         return None
-    d = json.load(open(p))
-    ent = d.get(kernel)
-    if not ent or ent.get("source_hash") != kernel_source_hash():
-        return None
-    return ent.get("dram_bytes_per_launch")
+    for line in open(TRAFFIC_SUMMARY):
+        f = line.split()
+        if len(f) == 4 and f[0] == "traffic" and f[1] == kernel:
+            return int(f[2]) if f[3] == kernel_source_hash(kernel) else None
+    return None
 
 
 # ------------------------------------------------------------------ clocks
@@ -177,11 +186,12 @@ class ClockSampler:
 class Sweep:
     """The 420 resident weight matrices and the chained activation buffers."""
 
-    def __init__(self, torch, qbw, device):
+    def __init__(self, torch, qbw, device, layers=LAYERS):
         self.torch, self.qbw, self.dev = torch, qbw, device
+        self.layers = layers
         self.offsets = {}
         total = 0
-        for layer in range(LAYERS):
+        for layer in range(layers):
             for mi, (name, N, K) in enumerate(MATRICES):
                 self.offsets[(layer, name)] = total
                 total += weight_bytes(N, K)
@@ -195,6 +205,7 @@ class Sweep:
         self.o = torch.empty(HIDDEN, dtype=bf, device=device)
         self.a = torch.empty(FFN, dtype=bf, device=device)
         self.layer0_host = {}
+        self._specs = self.specs()
 
     def fill(self, threads=None):
         import concurrent.futures as cf
@@ -207,7 +218,7 @@ class Sweep:
 
         t0 = time.time()
         with cf.ThreadPoolExecutor(threads) as ex:
-            for layer, mats in ex.map(gen, range(LAYERS)):
+            for layer, mats in ex.map(gen, range(self.layers)):
                 for (name, N, K), arr in zip(MATRICES, mats):
                     off = self.offsets[(layer, name)]
                     self.w[off:off + arr.size].copy_(torch.from_numpy(arr))
@@ -221,54 +232,49 @@ class Sweep:
         off = self.offsets[(layer, name)]
         return self.w[off:off + weight_bytes(N, K)]
 
-    def launches(self, stream=None):
-        """Enqueue one token: 6 launches per layer, 360 in all."""
+    def specs(self):
+        """The step's launches in order, 6 per layer: (kernel, call(stream),
+        algorithmic bytes = weights + bf16 activation reads + bf16 writes)."""
         qbw = self.qbw
-        for layer in range(LAYERS):
-            qbw.qmv_q4_0(self.view(layer, "q"), self.h, self.q, 1, QDIM, HIDDEN, stream)
-            qbw.qmv_q4_0(self.view(layer, "k"), self.h, self.k, 1, KVDIM, HIDDEN, stream)
-            qbw.qmv_q4_0(self.view(layer, "v"), self.h, self.v, 1, KVDIM, HIDDEN, stream)
-            qbw.qmv_q4_0(self.view(layer, "o"), self.q, self.o, 1, HIDDEN, QDIM, stream)
-            qbw.qmv_gateup_q4_0(self.view(layer, "gate"), self.view(layer, "up"), self.o, self.a, 1, FFN, HIDDEN,
-                                stream)
-            qbw.qmv_q4_0(self.view(layer, "down"), self.a, self.h, 1, HIDDEN, FFN, stream)
+
+        def mv(layer, name, x, y, N, K):
+            return ("qmv_q4_0", lambda s: qbw.qmv_q4_0(self.view(layer, name), x, y, 1, N, K, s),
+                    weight_bytes(N, K) + 2 * K + 2 * N)
+
+        out = []
+        for layer in range(self.layers):
+            out += [mv(layer, "q", self.h, self.q, QDIM, HIDDEN),
+                    mv(layer, "k", self.h, self.k, KVDIM, HIDDEN),
+                    mv(layer, "v", self.h, self.v, KVDIM, HIDDEN),
+                    mv(layer, "o", self.q, self.o, HIDDEN, QDIM),
+                    ("qmv_gateup_q4_0",
+                     lambda s, L=layer: qbw.qmv_gateup_q4_0(self.view(L, "gate"), self.view(L, "up"), self.o, self.a,
+                                                            1, FFN, HIDDEN, s),
+                     2 * weight_bytes(FFN, HIDDEN) + 2 * HIDDEN + 2 * FFN),
+                    mv(layer, "down", self.a, self.h, HIDDEN, FFN)]
+        return out
+
+    def launches(self, stream=None, kernel=None):
+        """Enqueue one token (or only the launches of one kernel)."""
+        for k, call, _ in self._specs:
+            if kernel is None or k == kernel:
+                call(stream)
 
     LAUNCHES_PER_STEP = LAYERS * 6
 
-    def per_kernel_pass(self):
-        """One eager step with CUDA events around every launch (same stream)."""
-        torch, qbw = self.torch, self.qbw
-        s = torch.cuda.current_stream()
-        rec = []
-        specs = []
-        for layer in range(LAYERS):
-            specs += [("qmv_q4_0", lambda L=layer: qbw.qmv_q4_0(self.view(L, "q"), self.h, self.q, 1, QDIM, HIDDEN),
-                       weight_bytes(QDIM, HIDDEN) + 2 * HIDDEN + 2 * QDIM),
-                      ("qmv_q4_0", lambda L=layer: qbw.qmv_q4_0(self.view(L, "k"), self.h, self.k, 1, KVDIM, HIDDEN),
-                       weight_bytes(KVDIM, HIDDEN) + 2 * HIDDEN + 2 * KVDIM),
-                      ("qmv_q4_0", lambda L=layer: qbw.qmv_q4_0(self.view(L, "v"), self.h, self.v, 1, KVDIM, HIDDEN),
-                       weight_bytes(KVDIM, HIDDEN) + 2 * HIDDEN + 2 * KVDIM),
-                      ("qmv_q4_0", lambda L=layer: qbw.qmv_q4_0(self.view(L, "o"), self.q, self.o, 1, HIDDEN, QDIM),
-                       weight_bytes(HIDDEN, QDIM) + 2 * QDIM + 2 * HIDDEN),
-                      ("qmv_gateup_q4_0", lambda L=layer: qbw.qmv_gateup_q4_0(self.view(L, "gate"), self.view(L, "up"),
-                                                                             self.o, self.a, 1, FFN, HIDDEN),
-                       2 * weight_bytes(FFN, HIDDEN) + 2 * HIDDEN + 2 * FFN),
-                      ("qmv_q4_0", lambda L=layer: qbw.qmv_q4_0(self.view(L, "down"), self.a, self.h, 1, HIDDEN, FFN),
-                       weight_bytes(HIDDEN, FFN) + 2 * FFN + 2 * HIDDEN)]
-        for name, fn, nbytes in specs:
-            e0 = torch.cuda.Event(enable_timing=True)
-            e1 = torch.cuda.Event(enable_timing=True)
-            e0.record(s)
-            fn()
-            e1.record(s)
-            rec.append((name, nbytes, e0, e1))
-        torch.cuda.synchronize()
+    def kernel_timing(self, stream, replays):
+        """Average launch duration of each kernel as it runs in the sweep: its
+        own launches of one step, in step order on the same buffers, captured
+        as one graph and replayed on ``stream`` between CUDA events."""
+        torch = self.torch
         out = {}
-        for name, nbytes, e0, e1 in rec:
-            d = out.setdefault(name, {"launches": 0, "bytes": 0, "ms": 0.0})
-            d["launches"] += 1
-            d["bytes"] += nbytes
-            d["ms"] += e0.elapsed_time(e1)
+        for kernel in sorted({k for k, _, _ in self._specs}):
+            sel = [(c, b) for k, c, b in self._specs if k == kernel]
+            g = capture(torch, lambda: self.launches(None, kernel), stream)
+            time_graph(torch, g, 2, stream)
+            ms = time_graph(torch, g, replays, stream) / replays
+            out[kernel] = {"launches": len(sel), "bytes": sum(b for _, b in sel), "ms": ms}
+            del g
         return out
 
 
@@ -371,31 +377,30 @@ def supplementary_kernels(torch, qbw, hbm_peak):
 
 
 def cpu_baseline(layer0_host, x_bits, budget_s):
-    """The oracle, as it stands, on a bounded sample of the sweep: rows of
-    layer 0's matrices in order, in chunks, until ``budget_s`` elapse."""
+    """The oracle, as it stands, on a bounded sample of the sweep: layer 0's
+    seven matrices in order, in chunks of 256 rows, repeated until
+    ``budget_s`` elapse."""
     import oracle
     oracle.lib()
-    done_bytes = 0
-    rows_done = {}
-    t0 = time.time()
-    xs = {"q": x_bits, "k": x_bits, "v": x_bits}
     rng = np.random.default_rng(0)
-    for name, N, K in MATRICES:
-        x = xs.get(name)
-        if x is None:
-            x = synth.f32_to_bf16_bits(rng.standard_normal(K).astype(np.float32))
-        rb = synth.row_bytes("q4_0", K)
-        n = 0
-        while n < N and time.time() - t0 < budget_s:
-            n1 = min(N, n + 256)
-            oracle.qmv_rows("q4_0", layer0_host[name], x, n, n1, K)
-            done_bytes += (n1 - n) * rb
-            n = n1
-        rows_done[name] = n
-        if time.time() - t0 >= budget_s:
-            break
+    xs = {name: (x_bits if name in ("q", "k", "v") else
+                 synth.f32_to_bf16_bits(rng.standard_normal(K).astype(np.float32)))
+          for name, N, K in MATRICES}
+    done_bytes, passes = 0, 0.0
+    t0 = time.time()
+    while time.time() - t0 < budget_s:
+        for name, N, K in MATRICES:
+            rb = synth.row_bytes("q4_0", K)
+            for n in range(0, N, 256):
+                n1 = min(N, n + 256)
+                oracle.qmv_rows("q4_0", layer0_host[name], xs[name], n, n1, K)
+                done_bytes += (n1 - n) * rb
+                if time.time() - t0 >= budget_s:
+                    break
+            if time.time() - t0 >= budget_s:
+                break
     dt = time.time() - t0
-    return done_bytes / dt / 1e9, dt, done_bytes, rows_done
+    return done_bytes / dt / 1e9, dt, done_bytes, done_bytes / sum(weight_bytes(N, K) for _, N, K in MATRICES)
 
 
 def gpu_arm(args):
@@ -461,9 +466,10 @@ def gpu_arm(args):
             h_out.copy_(sweep.h, non_blocking=True)
             stream.synchronize()
     e2e_s = time.perf_counter() - t0
+    per_kernel = sweep.kernel_timing(stream, replays=max(5, min(args.steps, 50)))
     clocks.stop()
+    assert qbw.fault_read(clear=True, stream=stream) == 0, "a kernel recorded a fault"
 
-    per_kernel = sweep.per_kernel_pass()
     wb, ab = sweep_bytes_per_layer()
     step_bytes = LAYERS * (wb + ab)
     value = step_bytes * args.steps * ws / (ms * 1e-3) / 1e9
@@ -472,7 +478,8 @@ def gpu_arm(args):
 
     dom = max(per_kernel, key=lambda k: per_kernel[k]["ms"])
     pk = per_kernel[dom]
-    achieved = pk["bytes"] / pk["launches"] / (pk["ms"] / pk["launches"] * 1e-3) / 1e9
+    achieved = pk["bytes"] / (pk["ms"] * 1e-3) / 1e9
+    step_ms = ms / args.steps
     traffic = profiled_traffic(dom)
     roofline = {"bound": "hbm", "kernel": dom, "achieved": round(achieved, 1), "peak": hbm_peak, "unit": "GB/s",
                 "frac": round(achieved / hbm_peak, 4), "peak_kind": f"{peak_kind} copy bandwidth (hbm_gbs)",
@@ -480,9 +487,9 @@ def gpu_arm(args):
                 "bytes_per_launch": round(pk["bytes"] / pk["launches"]), "launches": pk["launches"],
                 "us_per_launch": round(pk["ms"] / pk["launches"] * 1e3, 3),
                 "traffic": traffic,
-                "share_of_step": {k: round(v["ms"] / sum(d["ms"] for d in per_kernel.values()), 4)
-                                  for k, v in per_kernel.items()},
-                "measured": "CUDA events around every launch of one eager sweep step after the timed region"}
+                "share_of_step": {k: round(v["ms"] / step_ms, 4) for k, v in per_kernel.items()},
+                "measured": "the kernel's own launches of one step, in step order on the sweep's buffers, captured "
+                            "as one CUDA graph and replayed between CUDA events on the launching stream"}
     if rank != 0:
         if ws > 1:
             torch.distributed.destroy_process_group()
@@ -493,8 +500,8 @@ def gpu_arm(args):
     if not args.no_cpu and ws == 1:
         v, dt, nbytes, rows = cpu_baseline(sweep.layer0_host, x0, args.cpu_seconds)
         cpu = {"value": round(v, 4), "unit": UNIT, "cores": 1, "kind": "oracle",
-               "sample": f"oracle qmv_q4_0 over {nbytes} weight bytes of layer 0 (rows per matrix: {rows}), "
-                         f"{dt:.1f} s single-threaded on the host"}
+               "sample": f"oracle qmv_q4_0 over layer 0's seven matrices, {rows:.2f} passes "
+                         f"({nbytes} weight bytes) in {dt:.1f} s, single-threaded on the host"}
     line = {
         "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": ws, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms / args.steps, 4), "higher_is_better": True,
@@ -525,9 +532,10 @@ def gpu_arm(args):
 
 
 def profile_case(args):
-    """A small, self-contained run of one kernel for profiler captures: the
-    single-matrix workload named by --profile, ``warmup + steps`` calls over
-    a few rotating weight copies (well under 1 GB on the device)."""
+    """A small, self-contained run for profiler captures: the single-matrix
+    workload named by --profile, ``warmup + steps`` calls over a few rotating
+    weight copies (well under 1 GB on the device), or ``--profile sweep``: the
+    sweep's own launches over 6 layers (1.6 GB), 36 launches per call."""
     import torch
     import block_quantized_weight_gb300 as qbw
     torch.cuda.set_device(0)
@@ -558,6 +566,14 @@ def profile_case(args):
         y = torch.empty(N, device=dev)
         call = lambda i: qbw.qmv_gateup_q4_0(wg[i % 2], wu[i % 2], xb, y, 1, N, K)
         nbytes = 2 * wg[0].numel() + 2 * K + 4 * N
+    elif name == "sweep":
+        # the sweep's own launches over a few layers (1.6 GB of weights)
+        sweep = Sweep(torch, qbw, dev, layers=6)
+        sweep.fill()
+        sweep.h.copy_(torch.from_numpy(synth.activations(HIDDEN, seed=SEED, dtype="bf16").view(np.int16).copy())
+                      .view(torch.bfloat16).to(dev))
+        call = lambda i: sweep.launches()
+        nbytes = sum(b for _, _, b in sweep._specs)
     elif name == "qmm":
         M, N, K = 32, 5376, 21504
         ws = [torch.from_numpy(synth.q4_0_weights(N, K, seed=3)).to(dev) for _ in range(copies)]
@@ -635,8 +651,9 @@ def main():
     ap.add_argument("--no-kernels", action="store_true", help="skip the single-matrix supplementary numbers")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
-    ap.add_argument("--profile", choices=["q8_0", "q4_0", "gateup", "qmm"],
-                    help="run only one small single-matrix case (for profiler captures)")
+    ap.add_argument("--profile", choices=["q8_0", "q4_0", "gateup", "qmm", "sweep"],
+                    help="run only one small case (for profiler captures): a single-matrix workload, or the "
+                         "sweep's launches over 6 layers")
     args = ap.parse_args()
     if args.profile:
         profile_case(args)
