@@ -251,7 +251,10 @@ QmmPlan plan_qmm(int64_t M, int64_t N, int64_t K, int sm_count) {
     q.splits = splits;
     if (splits > 1) {
         q.partial_off = kQmmCounterBytes;
-        q.workspace = kQmmCounterBytes + align_up((size_t)splits * (size_t)M * (size_t)N * 4, 256);
+        // partial tiles [split][tile][128 rows][M rounded up to 4] fp32
+        const size_t mp = (size_t)((M + 3) / 4 * 4);
+        q.workspace = kQmmCounterBytes +
+                      align_up((size_t)splits * (size_t)q.tiles * (size_t)qmm_tc_tile_rows() * mp * 4, 256);
     }
     return q;
 }

@@ -14,19 +14,29 @@
 //   * raw Q4_0 bytes arrive by TMA in K-groups of 256 (8 blocks = 144 bytes
 //     per row), a box of 128 rows x 144 bytes.
 //
-// Warp roles: warps 0..15 dequantize (warp w: TMEM lanes 32 (w % 4) .. +31,
-// block pair w / 4 of each K-group); warp 16 lane 0 issues the TMA copies;
-// warp 17 lane 0 issues the MMAs.  Warps 0..3 also read the accumulator back.
+// Warp roles: three sets of four dequantizing warps (warps 0..11).  Set g
+// takes the CTA's K-groups g, g + 3, g + 6, ... and owns TMEM A stage g;
+// warp 4g + q of the set handles rows 32q .. 32q + 31 (the TMEM lanes of its
+// quarter) over the whole group.  Warp 12 lane 0 issues the TMA copies.
+// Warps 13 and 14 (lane 0) issue the MMAs: issuer j takes K-steps j, j + 2,
+// ... of every group into its own accumulator D_j, because one thread issues
+// a narrow (N <= 32) MMA only about every 50 cycles, well below what the
+// tensor core retires.  Warps 0..3 read D_0 + D_1 back.
 //
-// Dequantization, per weight pair: the code sits at bit 8, 12 or 16 of a word
-// (shifted there if needed), is OR-ed with the exponent of 2^15, 2^11 or 2^7
-// (giving 2^E + code exactly), and fma(f, d, -(2^E + 8) d) yields exactly
-// d (code - 8): (2^E + 8) d needs at most 24 significant bits for E <= 15.
-// The only rounding is the final conversion of the weight to bf16.
+// Dequantization to bf16, two adjacent weights j, j + 1 of a block at a time:
+// a byte permute puts qs[j] and qs[j + 1] in bytes 0 and 2 of a word; a LOP3
+// keeps their low nibbles and ORs in the bf16 exponent of 128, which gives
+// the pair (128 + c_j, 128 + c_j+1) exactly; the same after a 4-bit shift
+// gives codes j + 16 and j + 17.  A packed bf16 add of -128 leaves the exact
+// integers c, and one packed bf16 fma gives c d - 8 d = d (c - 8), rounded
+// once, with d the block's fp16 scale rounded to bf16.  Each weight is thus
+// within 2^-7 of its exact value relative (two roundings to 8 significant
+// bits, 2^-8 each), inside the 1e-2 bound on sum |w x| of the tensor-core path.
 //
-// Split K: each CTA writes its 128 x M partial tile to the workspace; the last
-// CTA of a tile (counted with an atomic) adds the partials in split order and
-// writes Y, then resets the counter so the workspace stays zero-filled.
+// Split K: each CTA writes its partial tile (128 rows x M, M padded to 4, one
+// row per lane as 16-byte vectors) to the workspace; the last CTA of a tile
+// (counted with an atomic) adds the partials in split order and writes Y, then
+// resets the counter so the workspace stays zero-filled.
 #include <cstdint>
 
 #include "qbw_device.cuh"
@@ -38,14 +48,23 @@ namespace {
 constexpr int kTileRows = 128;
 constexpr int kGroupK = 256;                  // K per pipeline stage (8 Q4_0 blocks)
 constexpr int kGroupBytes = 144;              // raw bytes per row per K-group
-constexpr int kDequantWarps = 16;
-constexpr int kThreads = (kDequantWarps + 2) * 32;
-constexpr int kStages = 4;                    // shared-memory stages (raw W + X)
-constexpr int kAStages = 2;                   // TMEM A stages
+constexpr int kSets = 3;                      // dequantizing warp sets = TMEM A stages
+constexpr int kDequantWarps = 4 * kSets;
+constexpr int kProducerWarp = kDequantWarps;
+constexpr int kMmaWarp0 = kDequantWarps + 1;  // and kMmaWarp0 + 1
+constexpr int kIssuers = 2;
+constexpr int kThreads = (kDequantWarps + 1 + kIssuers) * 32;
+constexpr int kStages = 6;                    // shared-memory stages (raw W + X)
+constexpr int kAStages = kSets;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kAColsPerStage = kGroupK / 2;          // 2 bf16 per 32-bit column
-constexpr uint32_t kDCol = kAStages * kAColsPerStage;     // accumulator columns start
+constexpr uint32_t kDCol = kAStages * kAColsPerStage;     // accumulator D_j at kDCol + 32 j
 constexpr uint32_t kRawStageBytes = kTileRows * kGroupBytes;   // 18432
+constexpr int kReduceItems = 3;               // row x 4-column items per thread in the split-K sum: 480 x 3 >= 128 x 8
+
+// bf16x2 constants
+constexpr uint32_t kBf16Minus128 = 0xC300C300u;
+constexpr uint32_t kBf16Minus8 = 0xC100C100u;
 
 // smem descriptor of a K-major, 128-byte-swizzled bf16 tile (8-row groups
 // 1024 bytes apart), tcgen05 format.
@@ -114,72 +133,208 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&v)[16]) {
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
-// f = (v & mask) | magic for one code each, then fma with the pair (d, d) and
-// the pair constant k: exactly d (code - 8) per lane.
-template <uint32_t ML, uint32_t MH>
-__device__ __forceinline__ uint64_t wpair(uint32_t a, uint32_t b, uint32_t gl, uint32_t gh, uint64_t dd,
-                                          uint64_t k) {
-    uint64_t r;
-    asm("{\n\t.reg .b32 lo, hi;\n\t.reg .b64 t;\n\t"
-        "lop3.b32 lo, %1, %6, %3, 0xEA;\n\t"
-        "lop3.b32 hi, %2, %7, %4, 0xEA;\n\t"
-        "mov.b64 t, {lo, hi};\n\t"
-        "fma.rn.f32x2 %0, t, %5, %8;\n\t}"
-        : "=l"(r)
-        : "r"(a), "r"(b), "r"(gl), "r"(gh), "l"(dd), "n"(ML), "n"(MH), "l"(k));
+__device__ __forceinline__ uint4 lds128(uint32_t addr) {
+    uint4 v;
+    asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
+    return v;
+}
+
+// ---------------------------------------------------------------- dequantization
+// Bytes B and B + 1 of word w (B = 0 or 2) hold qs[j] and qs[j + 1]:
+// lo = bf16x2 (128 + c_j, 128 + c_j+1) of their low nibbles, hi = the same of
+// their high nibbles (codes j + 16, j + 17).
+template <int B>
+__device__ __forceinline__ void nibble_pairs(uint32_t w, uint32_t& lo, uint32_t& hi) {
+    constexpr uint32_t sel = (B == 0) ? 0x1100u : 0x3322u;   // bytes B, B + 1 -> positions 0, 2
+    uint32_t t;
+    asm("prmt.b32 %0, %1, %1, %2;" : "=r"(t) : "r"(w), "n"(sel));
+    asm("lop3.b32 %0, %1, 0x000F000F, 0x43004300, 0xEA;" : "=r"(lo) : "r"(t));
+    asm("lop3.b32 %0, %1, 0x000F000F, 0x43004300, 0xEA;" : "=r"(hi) : "r"(t >> 4));
+}
+
+// (128 + c) pair -> d (c - 8) pair: (t - 128) is the exact integer c, and
+// fma(c, d, -8 d) rounds once (-8 d is exact).
+__device__ __forceinline__ uint32_t scale_pair(uint32_t t, uint32_t dd, uint32_t m8dd, uint32_t m128) {
+    uint32_t c, r;
+    asm("add.rn.bf16x2 %0, %1, %2;" : "=r"(c) : "r"(t), "r"(m128));
+    asm("fma.rn.bf16x2 %0, %1, %2, %3;" : "=r"(r) : "r"(c), "r"(dd), "r"(m8dd));
     return r;
 }
 
-// bf16x2 of a fp32 pair: low half = first lane, high half = second lane
-__device__ __forceinline__ uint32_t to_bf16x2(uint64_t p) {
-    const float2 f = unpack2f(p);
-    uint32_t r;
-    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(f.y), "f"(f.x));
-    return r;
-}
-
-// One Q4_0 block: scale d (fp16 bits) and qs words q0..q3 (qs bytes 4t..4t+3
-// in word t).  Writes the 16 bf16x2 columns of the block's 32 weights in K
-// order: column t' holds elements 2t' (low) and 2t'+1 (high).
-__device__ __forceinline__ void dequant_block(uint32_t dbits, uint32_t q0, uint32_t q1, uint32_t q2, uint32_t q3,
-                                              uint32_t* col) {
+// One Q4_0 block of a row whose 144 bytes of the K-group are the words v[].
+// OFF is the byte offset of the block's qs[0]; the fp16 scale is half SH of
+// word SW.  Writes the block's 16 bf16x2 columns in K order: column t holds
+// elements 2t (low half) and 2t + 1 (high half).
+template <int OFF, int SW, int SH>
+__device__ __forceinline__ void dequant_block(const uint32_t (&v)[36], uint32_t* col) {
+    const uint32_t dbits = SH ? (v[SW] >> 16) : (v[SW] & 0xFFFFu);
     const float d = half_bits_to_float(dbits);
-    const uint32_t m15 = 0x47000000u, m11 = 0x45000000u, m7 = 0x43000000u;
-    const float k15 = -32776.0f * d, k11 = -2056.0f * d, k7 = -136.0f * d;   // exact: <= 24 bits
-    const uint64_t dd = pack2f(d, d);
-    const uint64_t k15_15 = pack2f(k15, k15), k7_11 = pack2f(k7, k11), k11_11 = pack2f(k11, k11),
-                   k15_7 = pack2f(k15, k7);
-    const uint32_t q[4] = {q0, q1, q2, q3};
+    const uint32_t m128 = kBf16Minus128, m8 = kBf16Minus8;
+    uint32_t dd, m8dd;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %1;" : "=r"(dd) : "f"(d));
+    asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(m8dd) : "r"(dd), "r"(m8));   // (-8 d, -8 d): exact
 #pragma unroll
-    for (int t = 0; t < 4; ++t) {
-        // word q[t] = qs bytes 4t..4t+3; nibble n_i at bits 4i:
-        //   n0 = elem 4t (lo of byte 0), n1 = elem 16+4t, n2 = elem 4t+1, n3 = elem 17+4t,
-        //   n4 = elem 4t+2, n5 = elem 18+4t, n6 = elem 4t+3, n7 = elem 19+4t
-        const uint32_t v = q[t];
-        const uint32_t lft = v << 8;          // n0 at bit 8, n1 at bit 12
-        const uint32_t rgt = v >> 12;         // n5 at bit 8, n6 at bit 12, n7 at bit 16
-        // (elem 4t, 4t+1) = (n0 @8 of lft, n2 @8 of v)
-        col[2 * t] = to_bf16x2(wpair<0x00000F00u, 0x00000F00u>(lft, v, m15, m15, dd, k15_15));
-        // (elem 4t+2, 4t+3) = (n4 @16 of v, n6 @12 of rgt)
-        col[2 * t + 1] = to_bf16x2(wpair<0x000F0000u, 0x0000F000u>(v, rgt, m7, m11, dd, k7_11));
-        // (elem 16+4t, 17+4t) = (n1 @12 of lft, n3 @12 of v)
-        col[8 + 2 * t] = to_bf16x2(wpair<0x0000F000u, 0x0000F000u>(lft, v, m11, m11, dd, k11_11));
-        // (elem 18+4t, 19+4t) = (n5 @8 of rgt, n7 @16 of rgt)
-        col[8 + 2 * t + 1] = to_bf16x2(wpair<0x00000F00u, 0x000F0000u>(rgt, rgt, m15, m7, dd, k15_7));
+    for (int j = 0; j < 16; j += 2) {
+        // qs[j] and qs[j + 1] share a word: OFF + j is even and OFF % 4 is 0 or 2
+        const int byte = OFF + j;
+        uint32_t lo, hi;
+        if ((byte & 3) == 0) nibble_pairs<0>(v[byte >> 2], lo, hi);
+        else nibble_pairs<2>(v[byte >> 2], lo, hi);
+        col[j >> 1] = scale_pair(lo, dd, m8dd, m128);         // elements j, j + 1
+        col[8 + (j >> 1)] = scale_pair(hi, dd, m8dd, m128);   // elements 16 + j, 17 + j
     }
+}
+
+// Block pair P (blocks 2P, 2P + 1) of the row's K-group -> 32 columns.  Pair
+// P starts at byte 36P: scale A in the low half of word 9P, qs A from byte
+// 36P + 2, scale B in the high half of word 9P + 4, qs B from byte 36P + 20.
+template <int P>
+__device__ __forceinline__ void dequant_pair(const uint32_t (&v)[36], uint32_t (&col)[32]) {
+    dequant_block<36 * P + 2, 9 * P, 0>(v, col);
+    dequant_block<36 * P + 20, 9 * P + 4, 1>(v, col + 16);
+}
+
+// Barrier layout shared by every role: full[kStages], empty[kStages],
+// afull[kAStages], aempty[kAStages], dfull, 8 bytes each from bar0.
+__device__ __forceinline__ uint32_t full_bar_at(uint32_t bar0, int s) { return bar0 + 8u * (uint32_t)s; }
+__device__ __forceinline__ uint32_t empty_bar_at(uint32_t bar0, int s) { return bar0 + 8u * (uint32_t)(kStages + s); }
+__device__ __forceinline__ uint32_t afull_bar_at(uint32_t bar0, int a) {
+    return bar0 + 8u * (uint32_t)(2 * kStages + a);
+}
+__device__ __forceinline__ uint32_t aempty_bar_at(uint32_t bar0, int a) {
+    return bar0 + 8u * (uint32_t)(2 * kStages + kAStages + a);
+}
+__device__ __forceinline__ uint32_t dfull_bar_at(uint32_t bar0) {
+    return bar0 + 8u * (uint32_t)(2 * kStages + 2 * kAStages);
+}
+
+// One dequantizing warp of set g over the CTA's K-groups g, g + 3, ...
+// Per group: wait for the raw stage; read the lane's 144 bytes with nine
+// 16-byte loads (8 consecutive lanes = 8 rows 144 bytes apart hit 8 distinct
+// 16-byte bank groups: conflict-free); release the stage; decode the four
+// block pairs into two alternating register buffers and store each into TMEM
+// A stage g.  A buffer is rewritten only after a tcgen05.wait::st covering
+// its previous store.  raw_row: the row's byte offset within a stage;
+// a_taddr: TMEM address of the quarter's lanes, A stage g, column 0.
+__device__ __forceinline__ bool dequant_warp(int g, uint32_t raw_row, uint32_t a_taddr, uint32_t sbase,
+                                             uint32_t stage_bytes, uint32_t bar0, int lane, int ng,
+                                             unsigned int* fault) {
+    for (int i = g; i < ng; i += kSets) {
+        const int s = i % kStages;
+        const bool got = mbar_wait_bounded(full_bar_at(bar0, s), (uint32_t)(i / kStages) & 1u, fault,
+                                           kFaultBulkWaitTimeout);
+        if (!__all_sync(0xffffffffu, got)) return false;
+        const uint32_t src = sbase + (uint32_t)s * stage_bytes + raw_row;
+        uint32_t v[36];
+#pragma unroll
+        for (int j = 0; j < 9; ++j) {
+            const uint4 q = lds128(src + 16u * (uint32_t)j);
+            v[4 * j] = q.x;
+            v[4 * j + 1] = q.y;
+            v[4 * j + 2] = q.z;
+            v[4 * j + 3] = q.w;
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(empty_bar_at(bar0, s));     // raw W of stage s read
+        uint32_t c0[32], c1[32];
+        dequant_pair<0>(v, c0);
+        if (i >= kSets) {
+            // the MMAs of group i - 3 have finished reading A stage g
+            const bool free = mbar_wait_bounded(aempty_bar_at(bar0, g), (uint32_t)((i / kSets) - 1) & 1u, fault,
+                                                kFaultMmaWaitTimeout);
+            if (!__all_sync(0xffffffffu, free)) return false;
+            tc_fence_after();
+        }
+        tmem_st32(a_taddr, c0);
+        dequant_pair<1>(v, c1);
+        tmem_wait_st();
+        tmem_st32(a_taddr + 32u, c1);
+        dequant_pair<2>(v, c0);
+        tmem_wait_st();
+        tmem_st32(a_taddr + 64u, c0);
+        dequant_pair<3>(v, c1);
+        tmem_wait_st();
+        tmem_st32(a_taddr + 96u, c1);
+        tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(afull_bar_at(bar0, g));
+    }
+    return true;
+}
+
+// One MMA issuer (lane 0 of its warp): K-steps J, J + 2, ... of each of the
+// CTA's ng K-groups into accumulator D_J.  Every operand of a group's eight
+// MMAs is formed before its barrier waits, and stage and phase are carried
+// incrementally, so that once the A stage is published the eight MMAs go out
+// back to back: this thread shares its SM sub-partition with three busy
+// dequantizing warps, and every instruction between two MMAs costs issue slots.
+template <int J>
+__device__ __forceinline__ bool issue_mmas(uint32_t tmem, uint32_t sbase, uint32_t stage_bytes, uint32_t bar0, int nt,
+                                           int ng, unsigned int* fault) {
+    constexpr int kSteps = kGroupK / 16 / kIssuers;          // 8 MMAs per group per issuer
+    const uint32_t idesc = idesc_bf16(kTileRows, nt);
+    const uint32_t d_tmem = tmem + kDCol + 32u * (uint32_t)J;
+    // X of stage s, atom t, 16-element slice c: descriptor start field advances
+    // by stage_bytes / 16, nt * 128 / 16 and 32 / 16 respectively
+    const uint64_t atom_step = (uint64_t)((uint32_t)nt * 8u);
+    const uint64_t stage_step = (uint64_t)(stage_bytes >> 4);
+    uint64_t koff[kSteps];
+#pragma unroll
+    for (int kk = 0; kk < kSteps; ++kk) {
+        const int k = kIssuers * kk + J;
+        koff[kk] = (uint64_t)(k >> 2) * atom_step + (uint64_t)((k & 3) * 2);
+    }
+    uint64_t ds = sw128_desc(sbase + kRawStageBytes);
+    int s = 0, a = 0;
+    uint32_t sphase = 0, aphase = 0;
+    bool ok = true;
+    for (int i = 0; i < ng; ++i) {
+        uint64_t dk[kSteps];
+#pragma unroll
+        for (int kk = 0; kk < kSteps; ++kk) dk[kk] = ds + koff[kk];
+        const uint32_t a_tmem = tmem + (uint32_t)a * kAColsPerStage + (uint32_t)J * 8u;
+        ok = mbar_wait_bounded(full_bar_at(bar0, s), sphase, fault, kFaultMmaWaitTimeout) &&
+             mbar_wait_bounded(afull_bar_at(bar0, a), aphase, fault, kFaultMmaWaitTimeout);
+        if (!ok) break;
+        tc_fence_after();
+        const uint32_t acc0 = (i > 0) ? 1u : 0u;
+        tc_mma(d_tmem, a_tmem, dk[0], idesc, acc0);
+#pragma unroll
+        for (int kk = 1; kk < kSteps; ++kk)
+            tc_mma(d_tmem, a_tmem + (uint32_t)(kIssuers * kk) * 8u, dk[kk], idesc, 1u);
+        tc_commit(empty_bar_at(bar0, s));     // X tile of stage s consumed
+        tc_commit(aempty_bar_at(bar0, a));    // TMEM A stage a consumed
+        if (++s == kStages) {
+            s = 0;
+            sphase ^= 1u;
+            ds -= (uint64_t)(kStages - 1) * stage_step;
+        } else {
+            ds += stage_step;
+        }
+        if (++a == kAStages) {
+            a = 0;
+            aphase ^= 1u;
+        }
+    }
+    // completes when every MMA issued above has finished, even after a
+    // timeout (the accumulator is then not read, only TMEM released)
+    tc_commit(dfull_bar_at(bar0));
+    return ok;
 }
 
 struct QmmParams {
     CUtensorMap tmap_w;     // Q4_0 rows as 8-byte words, box (18, 128)
     CUtensorMap tmap_x;     // X [M][K] bf16, box (64, NT), 128-byte swizzle
     void* y;
-    float* partials;        // [splits][M][N] fp32 (splits > 1)
+    float* partials;        // [splits][tiles][128][M rounded up to 4] fp32 (splits > 1)
     unsigned int* counters; // [tiles] (splits > 1)
     unsigned int* fault;
     int32_t M, N, K;
     int32_t NT;             // MMA N: M rounded up to 16
     int32_t groups;         // K / 256
     int32_t splits;
+    int32_t tiles;          // ceil(N / 128)
     int32_t y_bf16;
 };
 
@@ -196,146 +351,115 @@ __global__ void __launch_bounds__(kThreads, 1) qmm_q4_0_tc_kernel(const __grid_c
     const uint32_t stage_bytes = kRawStageBytes + xbytes;            // multiple of 1024
     const uint32_t sbase = smem_u32(smem);
     const uint32_t bar0 = sbase + kStages * stage_bytes;
-    // barriers: full[kStages], empty[kStages], afull[kAStages], aempty[kAStages], dfull
-    auto full_bar = [&](int s) { return bar0 + 8u * (uint32_t)s; };
-    auto empty_bar = [&](int s) { return bar0 + 8u * (uint32_t)(kStages + s); };
-    auto afull_bar = [&](int a) { return bar0 + 8u * (uint32_t)(2 * kStages + a); };
-    auto aempty_bar = [&](int a) { return bar0 + 8u * (uint32_t)(2 * kStages + kAStages + a); };
-    const uint32_t dfull_bar = bar0 + 8u * (uint32_t)(2 * kStages + 2 * kAStages);
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kStages * stage_bytes + 8 * (2 * kStages + 2 * kAStages + 1));
-
-    if (threadIdx.x == 0) {
-        for (int s = 0; s < kStages; ++s) {
-            mbar_init(full_bar(s), 1);
-            mbar_init(empty_bar(s), kDequantWarps + 1);
-        }
-        for (int a = 0; a < kAStages; ++a) {
-            mbar_init(afull_bar(a), kDequantWarps);
-            mbar_init(aempty_bar(a), 1);
-        }
-        mbar_init(dfull_bar, 1);
-        fence_mbar_init();
-    }
-    if (warp == 0) {
-        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
-                     "n"(kTmemCols));
-        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
-    }
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    const uint32_t tmem = *tmem_slot;
+    const uint32_t dfull_bar = dfull_bar_at(bar0);
+    uint32_t* tmem_slot =
+        reinterpret_cast<uint32_t*>(smem + kStages * stage_bytes + 8 * (2 * kStages + 2 * kAStages + 1));
     bool ok = true;
 
-    if (warp == kDequantWarps) {
-        // ---------------- producer: raw W and X tiles by TMA
+    // K-group i of this CTA -> stage i % kStages: raw W box and the 4 X boxes
+    auto issue = [&](int i) {
+        const int s = i % kStages;
+        const int g = g_begin + i;
+        const uint32_t st = sbase + (uint32_t)s * stage_bytes;
+        mbar_arrive_expect_tx(full_bar_at(bar0, s), kRawStageBytes + xbytes);
+        tma_load_2d(st, &p.tmap_w, g * (kGroupBytes / 8), tile * kTileRows, full_bar_at(bar0, s),
+                    policy_evict_first());
+#pragma unroll
+        for (int a = 0; a < 4; ++a)
+            tma_load_2d(st + kRawStageBytes + (uint32_t)a * (uint32_t)p.NT * 128u, &p.tmap_x, g * kGroupK + a * 64, 0,
+                        full_bar_at(bar0, s), 0ull);
+    };
+
+    // The producer initialises the barriers, releases everyone else through
+    // named barrier 1 without waiting there itself, and starts the first
+    // copies while warp 0 allocates TMEM.
+    if (warp == kProducerWarp) {
         if (lane == 0) {
-            const uint64_t pol_w = policy_evict_first();
+            for (int s = 0; s < kStages; ++s) {
+                mbar_init(full_bar_at(bar0, s), 1);
+                mbar_init(empty_bar_at(bar0, s), 4 + kIssuers);   // the group's 4 dequantizing warps + the MMA commits
+            }
+            for (int a = 0; a < kAStages; ++a) {
+                mbar_init(afull_bar_at(bar0, a), 4);
+                mbar_init(aempty_bar_at(bar0, a), kIssuers);
+            }
+            mbar_init(dfull_bar, kIssuers);
+            fence_mbar_init();
+        }
+        __syncwarp();
+        asm volatile("bar.arrive 1, %0;" ::"n"(kThreads) : "memory");
+        if (lane == 0) {
             prefetch_tmap(&p.tmap_w);
             prefetch_tmap(&p.tmap_x);
             for (int i = 0; i < ng && ok; ++i) {
                 const int s = i % kStages;
                 if (i >= kStages)
-                    ok = mbar_wait_bounded(empty_bar(s), (uint32_t)((i / kStages) - 1) & 1u, p.fault,
+                    ok = mbar_wait_bounded(empty_bar_at(bar0, s), (uint32_t)((i / kStages) - 1) & 1u, p.fault,
                                            kFaultBulkWaitTimeout);
-                if (!ok) break;
-                const int g = g_begin + i;
-                const uint32_t st = sbase + (uint32_t)s * stage_bytes;
-                mbar_arrive_expect_tx(full_bar(s), kRawStageBytes + xbytes);
-                tma_load_2d(st, &p.tmap_w, g * (kGroupBytes / 8), tile * kTileRows, full_bar(s), pol_w);
-#pragma unroll
-                for (int a = 0; a < 4; ++a)
-                    tma_load_2d(st + kRawStageBytes + (uint32_t)a * (uint32_t)p.NT * 128u, &p.tmap_x,
-                                g * kGroupK + a * 64, 0, full_bar(s), 0ull);
+                if (ok) issue(i);
             }
-        }
-    } else if (warp == kDequantWarps + 1) {
-        // ---------------- MMA issuer
-        if (lane == 0) {
-            const uint32_t idesc = idesc_bf16(kTileRows, p.NT);
-            for (int i = 0; i < ng && ok; ++i) {
-                const int s = i % kStages, a = i % kAStages;
-                ok = mbar_wait_bounded(full_bar(s), (uint32_t)(i / kStages) & 1u, p.fault, kFaultMmaWaitTimeout) &&
-                     mbar_wait_bounded(afull_bar(a), (uint32_t)(i / kAStages) & 1u, p.fault, kFaultMmaWaitTimeout);
-                if (!ok) break;
-                tc_fence_after();
-                const uint32_t xs = sbase + (uint32_t)s * stage_bytes + kRawStageBytes;
-#pragma unroll
-                for (int k = 0; k < kGroupK / 16; ++k) {
-                    const uint32_t a_tmem = tmem + (uint32_t)a * kAColsPerStage + (uint32_t)k * 8u;
-                    const uint64_t bdesc = sw128_desc(xs + (uint32_t)(k >> 2) * (uint32_t)p.NT * 128u +
-                                                      (uint32_t)(k & 3) * 32u);
-                    tc_mma(tmem + kDCol, a_tmem, bdesc, idesc, (i > 0 || k > 0) ? 1u : 0u);
-                }
-                tc_commit(empty_bar(s));     // X tile of stage s consumed
-                tc_commit(aempty_bar(a));    // TMEM A stage a consumed
-            }
-            // completes when every MMA issued above has finished, even after a
-            // timeout (the accumulator is then not read, only TMEM released)
-            tc_commit(dfull_bar);
         }
     } else {
-        // ---------------- dequantizing warps
-        const int quarter = warp & 3;                 // TMEM lanes 32 quarter .. +31
-        const int pair = warp >> 2;                   // block pair of each K-group
-        const int row = quarter * 32 + lane;          // weight row within the tile
-        for (int i = 0; i < ng && ok; ++i) {
-            const int s = i % kStages, a = i % kAStages;
-            const bool got_w = mbar_wait_bounded(full_bar(s), (uint32_t)(i / kStages) & 1u, p.fault,
-                                                 kFaultBulkWaitTimeout);
-            const bool got_a = (i < kAStages) ||
-                               mbar_wait_bounded(aempty_bar(a), (uint32_t)((i / kAStages) - 1) & 1u, p.fault,
-                                                 kFaultMmaWaitTimeout);
-            if (!__all_sync(0xffffffffu, got_w && got_a)) {
-                ok = false;
-                break;
-            }
-            tc_fence_after();
-            // the pair's 36 bytes: V0 = [dA, qsA0, qsA1], V1..V3, V4 = [qsA14, qsA15, dB], V5..V8
-            const uint32_t src = sbase + (uint32_t)s * stage_bytes + (uint32_t)row * kGroupBytes + (uint32_t)pair * 36u;
-            uint32_t v[9];
-#pragma unroll
-            for (int w = 0; w < 9; ++w) v[w] = lds32(src + 4u * (uint32_t)w);
-            uint32_t col[32];
-            // block A: d = V0 lo; qs words (bytes 2..17 of the pair) realigned by 16 bits
-            dequant_block(v[0] & 0xFFFFu, __funnelshift_r(v[0], v[1], 16), __funnelshift_r(v[1], v[2], 16),
-                          __funnelshift_r(v[2], v[3], 16), __funnelshift_r(v[3], v[4], 16), col);
-            // block B: d = V4 hi; qs words V5..V8
-            dequant_block(v[4] >> 16, v[5], v[6], v[7], v[8], col + 16);
-            __syncwarp();
-            if (lane == 0) mbar_arrive(empty_bar(s));     // raw W of stage s read
-            tmem_st32(tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)a * kAColsPerStage + (uint32_t)pair * 32u,
-                      col);
-            tmem_wait_st();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(afull_bar(a));
+        if (warp == 0) {
+            asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                             smem_u32(tmem_slot)),
+                         "n"(kTmemCols));
+            asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
         }
-        // ---------------- epilogue: warps 0..3 read D (128 rows x NT) and emit
+        tc_fence_before();
+        asm volatile("bar.sync 1, %0;" ::"n"(kThreads) : "memory");
+        tc_fence_after();
+    }
+
+    if (warp >= kMmaWarp0) {
+        // ---------------- MMA issuers: issuer j takes K-steps j, j + 2, ... of every group
+        const uint32_t tmem = *tmem_slot;
+        if (lane == 0) {
+            if (warp == kMmaWarp0) ok = issue_mmas<0>(tmem, sbase, stage_bytes, bar0, p.NT, ng, p.fault);
+            else ok = issue_mmas<1>(tmem, sbase, stage_bytes, bar0, p.NT, ng, p.fault);
+        }
+    } else if (warp < kDequantWarps) {
+        // ---------------- dequantizing warps
+        const uint32_t tmem = *tmem_slot;
+        const int set = warp >> 2, quarter = warp & 3;   // TMEM lanes 32 quarter .. +31
+        const int row = quarter * 32 + lane;             // weight row within the tile
+        ok = dequant_warp(set, (uint32_t)row * kGroupBytes,
+                          tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)set * kAColsPerStage, sbase,
+                          stage_bytes, bar0, lane, ng, p.fault);
+        // ---------------- epilogue: warps 0..3 read D_0 + D_1 (128 rows x NT) and emit
         if (warp < 4) {
             const bool got = ok && mbar_wait_bounded(dfull_bar, 0u, p.fault, kFaultMmaWaitTimeout);
             if (__all_sync(0xffffffffu, got)) {
                 tc_fence_after();
                 const int n = tile * kTileRows + row;
-                float* part = p.partials + (size_t)split * p.M * p.N;
+                const int mp = (p.M + 3) & ~3;
+                float* part = p.partials + ((size_t)(split * p.tiles + tile) * kTileRows + row) * (size_t)mp;
                 for (int c0 = 0; c0 < p.NT; c0 += 16) {
-                    uint32_t dv[16];
-                    tmem_ld16(tmem + ((uint32_t)(quarter * 32) << 16) + kDCol + (uint32_t)c0, dv);
+                    uint32_t d0[16], d1[16];
+                    const uint32_t lane_base = tmem + ((uint32_t)(quarter * 32) << 16) + kDCol + (uint32_t)c0;
+                    tmem_ld16(lane_base, d0);
+                    tmem_ld16(lane_base + 32u, d1);
                     tmem_wait_ld();
-                    if (n < p.N) {
+                    float v[16];
 #pragma unroll
-                        for (int j = 0; j < 16; ++j) {
-                            const int m = c0 + j;
-                            if (m < p.M) {
-                                const float val = __uint_as_float(dv[j]);
-                                if (p.splits == 1) {
-                                    if (p.y_bf16) store_out<__nv_bfloat16>(p.y, (int64_t)m * p.N + n, val);
-                                    else store_out<float>(p.y, (int64_t)m * p.N + n, val);
-                                } else {
-                                    part[(size_t)m * p.N + n] = val;
+                    for (int q = 0; q < 16; ++q) v[q] = __uint_as_float(d0[q]) + __uint_as_float(d1[q]);
+                    if (p.splits == 1) {
+                        if (n < p.N) {
+#pragma unroll
+                            for (int q = 0; q < 16; ++q) {
+                                const int m = c0 + q;
+                                if (m < p.M) {
+                                    if (p.y_bf16) store_out<__nv_bfloat16>(p.y, (int64_t)m * p.N + n, v[q]);
+                                    else store_out<float>(p.y, (int64_t)m * p.N + n, v[q]);
                                 }
                             }
                         }
+                    } else {
+                        // this row's columns c0 .. c0 + 15 below mp, as 16-byte vectors
+#pragma unroll
+                        for (int q = 0; q < 16; q += 4)
+                            if (c0 + q < mp)
+                                *reinterpret_cast<float4*>(part + c0 + q) = make_float4(v[q], v[q + 1], v[q + 2], v[q + 3]);
                     }
                 }
                 __threadfence();              // partials visible before the split counter moves
@@ -349,6 +473,7 @@ __global__ void __launch_bounds__(kThreads, 1) qmm_q4_0_tc_kernel(const __grid_c
     __syncthreads();
     if (warp == 0) {
         // no MMA may still be writing TMEM when it is released
+        const uint32_t tmem = *tmem_slot;
         mbar_wait_bounded(dfull_bar, 0u, p.fault, kFaultMmaWaitTimeout);
         tc_fence_after();
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "n"(kTmemCols));
@@ -365,14 +490,48 @@ __global__ void __launch_bounds__(kThreads, 1) qmm_q4_0_tc_kernel(const __grid_c
         if (last) {
             __threadfence();
             const int rows = min(kTileRows, p.N - tile * kTileRows);
-            for (int t = threadIdx.x; t < rows * p.M; t += blockDim.x) {
-                const int m = t / rows, r = t - m * rows;
-                const int n = tile * kTileRows + r;
-                float sum = 0.f;
-                for (int s = 0; s < p.splits; ++s)
-                    sum += __ldcg(p.partials + (size_t)s * p.M * p.N + (size_t)m * p.N + n);
-                if (p.y_bf16) store_out<__nv_bfloat16>(p.y, (int64_t)m * p.N + n, sum);
-                else store_out<float>(p.y, (int64_t)m * p.N + n, sum);
+            const int mp = (p.M + 3) & ~3;
+            const int quads = mp / 4;
+            const int items = kTileRows * quads;      // (row, 4 columns); rows past N are skipped at the store
+            // each thread owns up to kReduceItems (row, quad) items and loads
+            // them for one split together: one L2 round trip per split
+            float4 acc[kReduceItems];
+#pragma unroll
+            for (int e = 0; e < kReduceItems; ++e) acc[e] = make_float4(0.f, 0.f, 0.f, 0.f);
+            for (int s = 0; s < p.splits; ++s) {
+                const float4* src =
+                    reinterpret_cast<const float4*>(p.partials + (size_t)(s * p.tiles + tile) * kTileRows * (size_t)mp);
+                float4 val[kReduceItems];
+#pragma unroll
+                for (int e = 0; e < kReduceItems; ++e) {
+                    const int t = (int)threadIdx.x + e * kThreads;   // t = quad * 128 + row
+                    const int r = t & (kTileRows - 1), q = t / kTileRows;
+                    val[e] = (t < items) ? __ldcg(src + (size_t)r * quads + q) : make_float4(0.f, 0.f, 0.f, 0.f);
+                }
+#pragma unroll
+                for (int e = 0; e < kReduceItems; ++e) {
+                    acc[e].x += val[e].x;
+                    acc[e].y += val[e].y;
+                    acc[e].z += val[e].z;
+                    acc[e].w += val[e].w;
+                }
+            }
+#pragma unroll
+            for (int e = 0; e < kReduceItems; ++e) {
+                const int t = (int)threadIdx.x + e * kThreads;
+                const int r = t & (kTileRows - 1), q = t / kTileRows;
+                if (t < items && r < rows) {
+                    const int n = tile * kTileRows + r;
+                    const float o[4] = {acc[e].x, acc[e].y, acc[e].z, acc[e].w};
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {
+                        const int m = 4 * q + c;
+                        if (m < p.M) {
+                            if (p.y_bf16) store_out<__nv_bfloat16>(p.y, (int64_t)m * p.N + n, o[c]);
+                            else store_out<float>(p.y, (int64_t)m * p.N + n, o[c]);
+                        }
+                    }
+                }
             }
             if (threadIdx.x == 0) p.counters[tile] = 0u;
         }
@@ -408,6 +567,7 @@ cudaError_t launch_qmm_tc(const CUtensorMap& tmap_w, const CUtensorMap& tmap_x, 
     p.NT = (M + 15) / 16 * 16;
     p.groups = K / kGroupK;
     p.splits = splits;
+    p.tiles = (N + kTileRows - 1) / kTileRows;
     p.y_bf16 = y_bf16;
     const size_t smem = qmm_tc_smem_bytes(p.NT);
     static thread_local int prepared_device = -1;
@@ -419,8 +579,7 @@ cudaError_t launch_qmm_tc(const CUtensorMap& tmap_w, const CUtensorMap& tmap_x, 
         if (e != cudaSuccess) return e;
         prepared_device = dev;
     }
-    const int tiles = (N + kTileRows - 1) / kTileRows;
-    qmm_q4_0_tc_kernel<<<tiles * splits, kThreads, smem, stream>>>(p);
+    qmm_q4_0_tc_kernel<<<p.tiles * splits, kThreads, smem, stream>>>(p);
     return cudaGetLastError();
 }
 
