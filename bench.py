@@ -3,10 +3,11 @@
 
 One step = one decode token through a 60-layer weight sweep shaped like the
 gem 31B profile (gem docs/research/architecture.md, "Fixed model profiles"):
-per layer the Q4_0 matrices q [5376->8192], k [5376->4096], v [5376->4096],
-o [8192->5376], gate/up [5376->21504] (one fused gate+up+GELU launch) and down
-[21504->5376], M = 1, with bf16 activations chained from one matrix to the
-next (o consumes q's output, standing in for attention).  The 420 weight
+per layer the Q4_0 matrices q [5376->8192], k [5376->4096], v [5376->4096]
+(stored back to back and read by one launch of 16384 rows, since they share
+their input), o [8192->5376], gate/up [5376->21504] (one fused gate+up+GELU
+launch) and down [21504->5376], M = 1, with bf16 activations chained from one
+matrix to the next (o consumes q's output, standing in for attention).  The 420 weight
 matrices (16,164,126,720 bytes, far larger than L2) stay resident in HBM; the
 whole step is replayed as one CUDA graph.
 
@@ -49,7 +50,7 @@ HIDDEN, QDIM, KVDIM, FFN = 5376, 8192, 4096, 21504
 # (name, N out, K in, input buffer, output buffer); gate and up share one launch
 MATRICES = [("q", QDIM, HIDDEN), ("k", KVDIM, HIDDEN), ("v", KVDIM, HIDDEN), ("o", HIDDEN, QDIM),
             ("gate", FFN, HIDDEN), ("up", FFN, HIDDEN), ("down", HIDDEN, FFN)]
-WORKLOAD = "decode weight sweep: 60 layers x Q4_0 {q 5376->8192, k 5376->4096, v 5376->4096, " \
+WORKLOAD = "decode weight sweep: 60 layers x Q4_0 {q 5376->8192, k 5376->4096, v 5376->4096 (one launch), " \
            "o 8192->5376, gate/up 5376->21504 fused, down 21504->5376}, M=1, chained bf16 activations"
 
 
@@ -66,7 +67,7 @@ def sweep_bytes_per_layer():
     reads and output writes (bf16) of each launch."""
     wb = sum(weight_bytes(N, K) for _, N, K in MATRICES)
     act = 0
-    act += 3 * (2 * HIDDEN) + 2 * QDIM + 2 * 2 * KVDIM          # q, k, v read h, write outputs
+    act += 2 * HIDDEN + 2 * QDIM + 2 * 2 * KVDIM                # q, k, v (one launch) read h, write outputs
     act += 2 * QDIM + 2 * HIDDEN                                 # o
     act += 2 * HIDDEN + 2 * FFN                                  # gate+up
     act += 2 * FFN + 2 * HIDDEN                                  # down
@@ -199,9 +200,8 @@ class Sweep:
         self.w = torch.empty(total, dtype=torch.uint8, device=device)
         bf = torch.bfloat16
         self.h = torch.empty(HIDDEN, dtype=bf, device=device)
-        self.q = torch.empty(QDIM, dtype=bf, device=device)
-        self.k = torch.empty(KVDIM, dtype=bf, device=device)
-        self.v = torch.empty(KVDIM, dtype=bf, device=device)
+        self.qkv = torch.empty(QDIM + 2 * KVDIM, dtype=bf, device=device)
+        self.q, self.k, self.v = self.qkv[:QDIM], self.qkv[QDIM:QDIM + KVDIM], self.qkv[QDIM + KVDIM:]
         self.o = torch.empty(HIDDEN, dtype=bf, device=device)
         self.a = torch.empty(FFN, dtype=bf, device=device)
         self.layer0_host = {}
@@ -232,26 +232,28 @@ class Sweep:
         off = self.offsets[(layer, name)]
         return self.w[off:off + weight_bytes(N, K)]
 
+    def qkv_view(self, layer):
+        """q, k and v of a layer, stored back to back: one [16384, 5376] matrix."""
+        off = self.offsets[(layer, "q")]
+        return self.w[off:off + weight_bytes(QDIM + 2 * KVDIM, HIDDEN)]
+
     def specs(self):
-        """The step's launches in order, 6 per layer: (kernel, call(stream),
+        """The step's launches in order, 4 per layer: (kernel, call(stream),
         algorithmic bytes = weights + bf16 activation reads + bf16 writes)."""
         qbw = self.qbw
 
-        def mv(layer, name, x, y, N, K):
-            return ("qmv_q4_0", lambda s: qbw.qmv_q4_0(self.view(layer, name), x, y, 1, N, K, s),
-                    weight_bytes(N, K) + 2 * K + 2 * N)
+        def mv(w, x, y, N, K):
+            return ("qmv_q4_0", lambda s: qbw.qmv_q4_0(w, x, y, 1, N, K, s), weight_bytes(N, K) + 2 * K + 2 * N)
 
         out = []
         for layer in range(self.layers):
-            out += [mv(layer, "q", self.h, self.q, QDIM, HIDDEN),
-                    mv(layer, "k", self.h, self.k, KVDIM, HIDDEN),
-                    mv(layer, "v", self.h, self.v, KVDIM, HIDDEN),
-                    mv(layer, "o", self.q, self.o, HIDDEN, QDIM),
+            out += [mv(self.qkv_view(layer), self.h, self.qkv, QDIM + 2 * KVDIM, HIDDEN),
+                    mv(self.view(layer, "o"), self.q, self.o, HIDDEN, QDIM),
                     ("qmv_gateup_q4_0",
                      lambda s, L=layer: qbw.qmv_gateup_q4_0(self.view(L, "gate"), self.view(L, "up"), self.o, self.a,
                                                             1, FFN, HIDDEN, s),
                      2 * weight_bytes(FFN, HIDDEN) + 2 * HIDDEN + 2 * FFN),
-                    mv(layer, "down", self.a, self.h, HIDDEN, FFN)]
+                    mv(self.view(layer, "down"), self.a, self.h, HIDDEN, FFN)]
         return out
 
     def launches(self, stream=None, kernel=None):
@@ -260,7 +262,7 @@ class Sweep:
             if kernel is None or k == kernel:
                 call(stream)
 
-    LAUNCHES_PER_STEP = LAYERS * 6
+    LAUNCHES_PER_STEP = LAYERS * 4
 
     def kernel_timing(self, stream, replays):
         """Average launch duration of each kernel as it runs in the sweep: its

@@ -261,6 +261,43 @@ QmmPlan plan_qmm(int64_t M, int64_t N, int64_t K, int sm_count) {
 
 int r_index(int R) { return R == 1 ? 0 : R == 2 ? 1 : R == 4 ? 2 : 3; }
 
+// Plans are a pure function of (format, matrices, N, K) on a device, and the
+// search above is not free on the host, so the last few are kept per device.
+constexpr int kPlanCache = 16;
+struct PlanEntry {
+    bool valid = false, ok = false;
+    int fmt = 0, nmat = 0;
+    int64_t N = 0, K = 0;
+    StreamPlan plan;
+};
+PlanEntry g_plans[kMaxDevices][kPlanCache];
+int g_plan_next[kMaxDevices] = {};
+
+bool plan_stream_cached(int fmt, int nmat, int64_t N, int64_t K, const DeviceInfo& di, StreamPlan* out) {
+    const int dev = (int)(&di - g_dev);
+    {
+        std::lock_guard<std::mutex> lk(g_mu);
+        for (const PlanEntry& e : g_plans[dev])
+            if (e.valid && e.fmt == fmt && e.nmat == nmat && e.N == N && e.K == K) {
+                if (e.ok) *out = e.plan;
+                return e.ok;
+            }
+    }
+    StreamPlan plan;
+    const bool ok = plan_stream(fmt, nmat, N, K, di, &plan);
+    std::lock_guard<std::mutex> lk(g_mu);
+    PlanEntry& e = g_plans[dev][g_plan_next[dev]++ % kPlanCache];
+    e.valid = true;
+    e.ok = ok;
+    e.fmt = fmt;
+    e.nmat = nmat;
+    e.N = N;
+    e.K = K;
+    e.plan = plan;
+    if (ok) *out = plan;
+    return ok;
+}
+
 qbw_status launch_streaming(int fmt, int nmat, DeviceInfo& di, const StreamPlan& plan, cudaStream_t s) {
     const int which = (nmat == 2) ? 2 : (fmt == kFmtQ4 ? 0 : 1);
     {
@@ -300,7 +337,7 @@ qbw_status qmv_common(int fmt, int nmat, const void* w0, const void* w1, const v
     const bool aligned = ((uintptr_t)w0 % 16 == 0) && (nmat == 1 || (uintptr_t)w1 % 16 == 0);
     if (K % 256 == 0 && aligned) {
         StreamPlan plan;
-        if (plan_stream(fmt, nmat, N, K, *di, &plan) &&
+        if (plan_stream_cached(fmt, nmat, N, K, *di, &plan) &&
             encode_weight_map(&plan.p.tmap[0], w0, N, plan.p.row_bytes, fmt, plan.R) &&
             (nmat == 1 || encode_weight_map(&plan.p.tmap[1], w1, N, plan.p.row_bytes, fmt, plan.R))) {
             plan.p.w0 = static_cast<const uint8_t*>(w0);

@@ -1,6 +1,7 @@
-"""GPU parity of the chained decode sweep: per layer q, k, v = W h; o = Wo q
-(o consumes q, standing in for attention); a = gelu_tanh(Wg o) * (Wu o); the
-next layer's h = Wd a; every activation bf16.  The launches of all layers are
+"""GPU parity of the chained decode sweep: per layer q, k, v = W h (one launch
+over the three matrices stored back to back); o = Wo q (o consumes q, standing
+in for attention); a = gelu_tanh(Wg o) * (Wu o); the next layer's h = Wd a;
+every activation bf16.  The launches of all layers are
 enqueued back to back on one stream, so each kernel starts while the previous
 one finishes and must still read the previous output only after it is
 complete.
@@ -41,17 +42,18 @@ def run_chain(qbw, oracle, dims, layers, seed):
     W = [{n: synth.q4_0_weights(*shp[n], seed=seed, stream=i, layer=l) for i, n in enumerate(ORDER)}
          for l in range(layers)]
     Wd = [{n: torch.from_numpy(W[l][n]).cuda() for n in ORDER} for l in range(layers)]
+    # q, k, v stored back to back: one launch of nq + nk + nv rows off the same input
+    Wqkv = [torch.from_numpy(np.concatenate([W[l]["q"], W[l]["k"], W[l]["v"]])).cuda() for l in range(layers)]
+    nq, nk, nv = shp["q"][0], shp["k"][0], shp["v"][0]
     h0 = synth.activations(hidden, seed=seed, dtype="bf16")
     bf = torch.bfloat16
-    buf = {"h": bf16_dev(h0), "q": torch.empty(shp["q"][0], dtype=bf, device="cuda"),
-           "k": torch.empty(shp["k"][0], dtype=bf, device="cuda"), "v": torch.empty(shp["v"][0], dtype=bf, device="cuda"),
+    qkv = torch.empty(nq + nk + nv, dtype=bf, device="cuda")
+    buf = {"h": bf16_dev(h0), "q": qkv[:nq], "k": qkv[nq:nq + nk], "v": qkv[nq + nk:],
            "o": torch.empty(shp["o"][0], dtype=bf, device="cuda"), "a": torch.empty(shp["gate"][0], dtype=bf, device="cuda")}
     snaps = []
 
     def layer(l, keep):
-        qbw.qmv_q4_0(Wd[l]["q"], buf["h"], buf["q"], 1, *shp["q"])
-        qbw.qmv_q4_0(Wd[l]["k"], buf["h"], buf["k"], 1, *shp["k"])
-        qbw.qmv_q4_0(Wd[l]["v"], buf["h"], buf["v"], 1, *shp["v"])
+        qbw.qmv_q4_0(Wqkv[l], buf["h"], qkv, 1, nq + nk + nv, hidden)
         qbw.qmv_q4_0(Wd[l]["o"], buf["q"], buf["o"], 1, *shp["o"])
         qbw.qmv_gateup_q4_0(Wd[l]["gate"], Wd[l]["up"], buf["o"], buf["a"], 1, *shp["gate"])
         qbw.qmv_q4_0(Wd[l]["down"], buf["a"], buf["h"], 1, *shp["down"])
