@@ -374,6 +374,20 @@ def supplementary_kernels(torch, qbw, hbm_peak):
                 lambda i, X=X, Y=Y, M=M, N=N, K=K, work=work: (lambda: qbw.qmm_q4_0_smallM(ws[i], X, Y, M, N, K, work)),
                 flops=2.0 * M * N * K)
         del ws, w
+    # the Q8_0 token table of the 31B profile (262144 x 5376, 1.5 GB, larger
+    # than L2): tied LM head matvec, and the embedding-row gather of a token
+    N, K = 262144, 5376
+    w = torch.from_numpy(synth.q8_0_weights(N, K, seed=12)).to(dev)
+    xb = bf16(synth.activations(K, seed=12, dtype="bf16"))
+    y = torch.empty(N, device=dev)
+    run("qmv_q8_0 262144x5376 bf16->f32 (token table as LM head)", w.numel() + 2 * K + 4 * N, 1,
+        lambda i: (lambda: qbw.qmv_q8_0(w, xb, y, 1, N, K)))
+    for n_ids in (1, 32):
+        ids = torch.from_numpy(np.arange(0, N, N // n_ids, dtype=np.int32)[:n_ids]).to(dev)
+        out = torch.empty(n_ids, K, dtype=torch.bfloat16, device=dev)
+        run(f"qembed_q8_0 {n_ids} rows of 262144x5376 -> bf16", n_ids * (K // 32 * 34 + 2 * K) + 4 * n_ids, 1,
+            lambda i, ids=ids, out=out: (lambda: qbw.qembed_q8_0(w, ids, out, N, K)))
+    del w
     torch.cuda.empty_cache()
     return res
 

@@ -18,7 +18,7 @@ import threading
 __all__ = [
     "QbwError", "load", "lib_path",
     "qmv_q8_0", "qmv_q4_0", "qmv_gateup_q4_0", "qmm_q4_0_smallM", "qmm_q4_0_smallM_workspace_bytes",
-    "qmm_q4_0_smallM_noalloc", "NOALLOC_SCRATCH_BYTES", "qdequant_q8_0", "qdequant_q4_0", "fault_read", "status_str", "version",
+    "qmm_q4_0_smallM_noalloc", "NOALLOC_SCRATCH_BYTES", "qembed_q8_0", "qdequant_q8_0", "qdequant_q4_0", "fault_read", "status_str", "version",
     "F32", "BF16",
 ]
 
@@ -71,6 +71,8 @@ def _declare(L):
     L.qmm_q4_0_smallM_workspace_bytes.argtypes = [i64, i64, i64]
     L.qmm_q4_0_smallM.restype = i32
     L.qmm_q4_0_smallM.argtypes = [P, P, i32, P, i32, i64, i64, i64, P, sz, P]
+    L.qembed_q8_0.restype = i32
+    L.qembed_q8_0.argtypes = [P, P, i64, P, i32, i64, i64, P]
     L.qmm_q4_0_smallM_noalloc.restype = i32
     L.qmm_q4_0_smallM_noalloc.argtypes = [P, P, i32, P, i32, i64, i64, i64, P]
     for name in ("qdequant_q8_0", "qdequant_q4_0"):
@@ -163,6 +165,14 @@ def qmm_q4_0_smallM_noalloc(w, X, Y, M: int, N: int, K: int, stream=None):
     _check(load().qmm_q4_0_smallM_noalloc(_ptr(w), _ptr(X), _dtype_code(X), _ptr(Y), _dtype_code(Y), M, N, K,
                                           _stream(stream)), "qmm_q4_0_smallM_noalloc")
     return Y
+
+
+def qembed_q8_0(w, ids, out, N: int, K: int, stream=None):
+    """out[i, :] = dequantized row ids[i] of the Q8_0 matrix ``w`` (N x K);
+    ``ids`` an int32 device tensor, ``out`` fp32 or bf16 [len(ids), K]."""
+    _check(load().qembed_q8_0(_ptr(w), _ptr(ids), ids.numel(), _ptr(out), _dtype_code(out), N, K, _stream(stream)),
+           "qembed_q8_0")
+    return out
 
 
 def qdequant_q8_0(w, out, N: int, K: int, stream=None):

@@ -469,6 +469,26 @@ qbw_status qdequant_q4_0(const void* w, float* out, int64_t N, int64_t K, void* 
     return dequant_common(kFmtQ4, w, out, N, K, stream);
 }
 
+qbw_status qembed_q8_0(const void* w, const int32_t* ids, int64_t n_ids, void* out, qbw_dtype ot, int64_t N, int64_t K,
+                       void* stream) {
+    if (!w) return QBW_EINVAL;
+    if (!valid_dtype(ot)) return QBW_EDTYPE;
+    if (n_ids < 0 || n_ids > INT32_MAX || N < 1 || N > INT32_MAX || K < 32 || K % 32 != 0 || K > (int64_t(1) << 24))
+        return QBW_ESHAPE;
+    if (n_ids == 0) return QBW_OK;          // ids and out may be NULL
+    if (!ids || !out) return QBW_EINVAL;
+    if ((uintptr_t)ids % 4 || (uintptr_t)out % dtype_size(ot)) return QBW_EALIGN;
+    const size_t obytes = (size_t)n_ids * (size_t)K * dtype_size(ot);
+    if (overlaps(out, obytes, w, (size_t)N * (K / 32) * 34) || overlaps(out, obytes, ids, (size_t)n_ids * 4))
+        return QBW_EINVAL;
+    DeviceInfo* di = nullptr;
+    qbw_status st = device_info(&di);
+    if (st != QBW_OK) return st;
+    cudaError_t e = launch_embed(kFmtQ8, static_cast<const uint8_t*>(w), ids, n_ids, N, K, out, ot == QBW_BF16,
+                                 di->fault, di->sm_count, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? QBW_OK : QBW_ECUDA;
+}
+
 qbw_status qbw_fault_read(uint32_t* code, int clear, void* stream) {
     if (!code) return QBW_EINVAL;
     DeviceInfo* di = nullptr;

@@ -14,6 +14,7 @@ namespace qbw {
 enum FaultCode : unsigned int {
     kFaultBulkWaitTimeout = 1,   // an mbarrier guarding a bulk copy never completed
     kFaultMmaWaitTimeout = 2,    // an mbarrier guarding tensor-core work never completed
+    kFaultBadIndex = 3,          // a token-table row index outside [0, N)
 };
 
 enum : int { kFmtQ8 = 0, kFmtQ4 = 1 };
@@ -72,6 +73,8 @@ cudaError_t launch_qmv_generic(int fmt, int nmat, const uint8_t* w0, const uint8
                                cudaStream_t stream);
 cudaError_t launch_dequant(int fmt, const uint8_t* w, float* out, int64_t N, int64_t K, int sm_count,
                            cudaStream_t stream);
+cudaError_t launch_embed(int fmt, const uint8_t* w, const int32_t* ids, int64_t n_ids, int64_t N, int64_t K, void* out,
+                         int out_bf16, unsigned int* fault, int sm_count, cudaStream_t stream);
 
 // Largest dynamic shared memory the streaming kernels may request.
 cudaError_t prepare_qmv_stream(int fmt, int nmat, int R, size_t smem);

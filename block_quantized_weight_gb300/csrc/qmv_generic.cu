@@ -1,6 +1,7 @@
 // qmv_generic.cu -- the exact-but-plain kernels: the matrix-vector fallback for
 // shapes or alignments the streaming kernel does not take (K % 256 != 0, or a
-// weight pointer not 16-byte aligned), and the whole-matrix dequantizer.
+// weight pointer not 16-byte aligned), the whole-matrix dequantizer and the
+// token-table row gather.
 #include <cstdint>
 
 #include "qbw_device.cuh"
@@ -81,6 +82,38 @@ __global__ void __launch_bounds__(256) dequant_kernel(const uint8_t* w, float* o
     }
 }
 
+// Token-table gather: one thread per (output row, block, 8 consecutive
+// elements); out[i, 32b + k] = d * q of block b of row ids[i], exact in fp32
+// (bf16: rounded to nearest even).  An index outside [0, N) gives zeros and
+// fault code 3.
+template <int FMT, typename T>
+__global__ void __launch_bounds__(256) embed_kernel(const uint8_t* w, const int32_t* ids, int64_t n_ids, int64_t N,
+                                                    int64_t K, T* out, unsigned int* fault) {
+    constexpr int BPB = (FMT == kFmtQ4) ? 18 : 34;
+    const int64_t nb = K / 32;
+    const int64_t total = n_ids * nb * 4;
+    for (int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; t < total; t += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t ib = t >> 2;                 // (row, block)
+        const int k0 = (int)(t & 3) * 8;           // first of this thread's 8 elements
+        const int64_t i = ib / nb, b = ib - i * nb;
+        const int64_t id = ids[i];
+        T* o = out + i * K + b * 32 + k0;
+        float v[8];
+        if (id < 0 || id >= N) {
+            if (k0 == 0) record_fault(fault, kFaultBadIndex);
+#pragma unroll
+            for (int k = 0; k < 8; ++k) v[k] = 0.f;
+        } else {
+            const uint8_t* blk = w + (id * nb + b) * BPB;
+            const float d = half_bits_to_float((uint32_t)blk[0] | ((uint32_t)blk[1] << 8));
+#pragma unroll
+            for (int k = 0; k < 8; ++k) v[k] = d * code_at<FMT>(blk, k0 + k);
+        }
+#pragma unroll
+        for (int k = 0; k < 8; ++k) store_out<T>(o, k, v[k]);
+    }
+}
+
 // Small-M fallback: one warp per weight row, X rows in groups of 8, exact
 // codes times bf16 activations in fp32, scale applied per block.
 __global__ void __launch_bounds__(256) qmm_generic_kernel(const uint8_t* w, const void* X, void* Y, int y_bf16,
@@ -158,6 +191,28 @@ cudaError_t launch_dequant(int fmt, const uint8_t* w, float* out, int64_t N, int
         dequant_kernel<kFmtQ8><<<ctas, threads, 0, stream>>>(w, out, N, K);
     else
         dequant_kernel<kFmtQ4><<<ctas, threads, 0, stream>>>(w, out, N, K);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_embed(int fmt, const uint8_t* w, const int32_t* ids, int64_t n_ids, int64_t N, int64_t K, void* out,
+                         int out_bf16, unsigned int* fault, int sm_count, cudaStream_t stream) {
+    const int threads = 256;
+    const int64_t items = n_ids * (K / 32) * 4;
+    const int64_t want = (items + threads - 1) / threads;
+    const int ctas = (int)(want < (int64_t)sm_count * 8 ? want : (int64_t)sm_count * 8);
+    if (fmt == kFmtQ8) {
+        if (out_bf16)
+            embed_kernel<kFmtQ8, __nv_bfloat16>
+                <<<ctas, threads, 0, stream>>>(w, ids, n_ids, N, K, static_cast<__nv_bfloat16*>(out), fault);
+        else
+            embed_kernel<kFmtQ8, float><<<ctas, threads, 0, stream>>>(w, ids, n_ids, N, K, static_cast<float*>(out), fault);
+    } else {
+        if (out_bf16)
+            embed_kernel<kFmtQ4, __nv_bfloat16>
+                <<<ctas, threads, 0, stream>>>(w, ids, n_ids, N, K, static_cast<__nv_bfloat16*>(out), fault);
+        else
+            embed_kernel<kFmtQ4, float><<<ctas, threads, 0, stream>>>(w, ids, n_ids, N, K, static_cast<float*>(out), fault);
+    }
     return cudaGetLastError();
 }
 

@@ -204,11 +204,35 @@ qbw_status qdequant_q8_0(const void *w, float *out, int64_t N, int64_t K, void *
 qbw_status qdequant_q4_0(const void *w, float *out, int64_t N, int64_t K, void *stream);
 
 /*
+ * qembed_q8_0 -- token-table lookup: out[i, :] = W[ids[i], :], dequantized.
+ *
+ * The embedding side of the Q8_0 token table that the decode loop reads once
+ * per token (gem docs/research/architecture.md, "M4 Max operating
+ * assumptions": Q4_0 matrices and a Q8_0 token table; the same table serves
+ * as the tied LM head through qmv_q8_0).
+ *
+ *   w   : Q8_0 matrix, N rows x K inputs, any alignment
+ *   ids : n_ids row indices (int32, device memory, 4-byte aligned)
+ *   out : [n_ids, K] of ot; QBW_F32 holds d * q exactly, QBW_BF16 that value
+ *         rounded to nearest even
+ *   n_ids >= 0 (0 launches nothing; ids and out may then be NULL), N >= 1,
+ *   K % 32 == 0
+ * An index outside [0, N) gives a row of zeros and sets fault bit 1 << 3
+ * (see qbw_fault_read); nothing is read out of bounds.
+ */
+qbw_status qembed_q8_0(const void *w, const int32_t *ids, int64_t n_ids, void *out, qbw_dtype ot, int64_t N,
+                       int64_t K, void *stream);
+
+/*
  * qbw_fault_read -- read the library's device fault word for the current
- * device.  A kernel whose bounded wait for an asynchronous copy runs out (about
- * two seconds) writes a nonzero code here and returns early instead of
- * hanging; outputs of that call are then undefined.  Synchronizes `stream`,
- * stores the word in *code and, if clear != 0, resets it to zero.
+ * device.  Kernels report problems found while they run by setting bit
+ * (1 << c) of this word, then return early (outputs of that call are then
+ * undefined) instead of hanging or trapping:
+ *   c = 1  a bounded wait for an asynchronous copy ran out (about two seconds)
+ *   c = 2  a bounded wait for tensor-core work ran out
+ *   c = 3  qembed_q8_0 met a row index outside [0, N)
+ * Synchronizes `stream`, stores the word in *code and, if clear != 0, resets
+ * it to zero.
  */
 qbw_status qbw_fault_read(uint32_t *code, int clear, void *stream);
 
