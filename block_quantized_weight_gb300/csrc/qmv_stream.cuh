@@ -243,10 +243,12 @@ constexpr int kXsPairFloats = 68;
 
 // Stage the activations in slot order.  slot_of[e] is the slot of pair element
 // e (filled by the caller).  Each thread loads groups of 4 consecutive
-// elements (vector loads when x is aligned for them); the first batch of
-// loads is issued by stage_activations_begin, before the caller starts the
-// weight copies, so that the activations are not queued behind them.
-constexpr int kStageBatch = 4;
+// elements (vector loads when x is aligned for them): group i of thread t is
+// i = t + u * blockDim.  All the loads of the first batch, which covers every
+// activation of K up to 4 * kStageBatch * blockDim (21504 at 12 warps), are
+// issued before the caller starts the weight copies: loads issued after them
+// wait behind a full ring of weight traffic.
+constexpr int kStageBatch = 16;
 
 struct StageBatch {
     float v[kStageBatch][4];
@@ -286,28 +288,34 @@ __device__ __forceinline__ void load_batch(const StreamParams& p, int i0, StageB
     }
 }
 
+// Group i covers elements 4 (i % 16) .. +3 of pair i / 16.  blockDim is a
+// multiple of 32, so i % 16 is the same for all of a thread's groups and the
+// four slots sl[] are looked up once.
 __device__ __forceinline__ void store_batch(const StreamParams& p, int i0, const StageBatch& bt, float* xs,
-                                            const uint8_t* slot_of) {
+                                            const int (&sl)[4]) {
     const int n4 = p.K >> 2;
 #pragma unroll
     for (int u = 0; u < kStageBatch; ++u) {
         const int i = i0 + u * (int)blockDim.x;
         if (i >= n4) break;
-        const int q = i >> 4;              // pair (64 elements = 16 groups of 4)
+        float* q = xs + (i >> 4) * kXsPairFloats;
 #pragma unroll
-        for (int t = 0; t < 4; ++t) xs[q * kXsPairFloats + slot_of[((i & 15) << 2) + t]] = bt.v[u][t];
+        for (int t = 0; t < 4; ++t) q[sl[t]] = bt.v[u][t];
     }
 }
 
 // Finish staging: store the first batch, then load and store the rest.
 __device__ __forceinline__ void stage_activations_end(const StreamParams& p, const StageBatch& first, float* xs,
                                                       const uint8_t* slot_of) {
-    store_batch(p, (int)threadIdx.x, first, xs, slot_of);
+    int sl[4];
+#pragma unroll
+    for (int t = 0; t < 4; ++t) sl[t] = slot_of[((threadIdx.x & 15) << 2) + t];
+    store_batch(p, (int)threadIdx.x, first, xs, sl);
     const int n4 = p.K >> 2;
     for (int i0 = (int)threadIdx.x + kStageBatch * (int)blockDim.x; i0 < n4; i0 += kStageBatch * (int)blockDim.x) {
         StageBatch bt;
         load_batch(p, i0, bt);
-        store_batch(p, i0, bt, xs, slot_of);
+        store_batch(p, i0, bt, xs, sl);
     }
 }
 
