@@ -374,6 +374,20 @@ def supplementary_kernels(torch, qbw, hbm_peak):
                 lambda i, X=X, Y=Y, M=M, N=N, K=K, work=work: (lambda: qbw.qmm_q4_0_smallM(ws[i], X, Y, M, N, K, work)),
                 flops=2.0 * M * N * K)
         del ws, w
+    # batched decode: M = 2 and 4 sequences sharing one read of the q|k|v and
+    # down weights (the tensor-core small-M path)
+    for (N, K) in ((16384, 5376), (5376, 21504)):
+        w = torch.from_numpy(synth.q4_0_weights(N, K, seed=5)).to(dev)
+        copies = max(2, int(np.ceil(2.2 * l2 / w.numel())))
+        ws = [w.clone() for _ in range(copies)]
+        for M in (2, 4):
+            X = bf16(synth.activations((M, K), seed=5, dtype="bf16"))
+            Y = torch.empty(M, N, dtype=torch.bfloat16, device=dev)
+            wsb = qbw.qmm_q4_0_smallM_workspace_bytes(M, N, K)
+            work = torch.zeros(max(wsb, 1), dtype=torch.uint8, device=dev)
+            run(f"batched decode qmm_q4_0_smallM M={M} {N}x{K} bf16", w.numel() + 2 * M * K + 2 * M * N, copies,
+                lambda i, X=X, Y=Y, M=M, N=N, K=K, work=work: (lambda: qbw.qmm_q4_0_smallM(ws[i], X, Y, M, N, K, work)))
+        del ws, w
     # the Q8_0 token table of the 31B profile (262144 x 5376, 1.5 GB, larger
     # than L2): tied LM head matvec, and the embedding-row gather of a token
     N, K = 262144, 5376

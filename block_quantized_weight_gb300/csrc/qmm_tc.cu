@@ -493,28 +493,34 @@ __global__ void __launch_bounds__(kThreads, 1) qmm_q4_0_tc_kernel(const __grid_c
             const int mp = (p.M + 3) & ~3;
             const int quads = mp / 4;
             const int items = kTileRows * quads;      // (row, 4 columns); rows past N are skipped at the store
-            // each thread owns up to kReduceItems (row, quad) items and loads
-            // them for one split together: one L2 round trip per split
+            // each thread owns up to kReduceItems (row, quad) items
             float4 acc[kReduceItems];
 #pragma unroll
             for (int e = 0; e < kReduceItems; ++e) acc[e] = make_float4(0.f, 0.f, 0.f, 0.f);
-            for (int s = 0; s < p.splits; ++s) {
-                const float4* src =
-                    reinterpret_cast<const float4*>(p.partials + (size_t)(s * p.tiles + tile) * kTileRows * (size_t)mp);
-                float4 val[kReduceItems];
+            // up to four splits' loads in flight at once, added in split order
+            for (int s0 = 0; s0 < p.splits; s0 += 4) {
+                float4 val[4][kReduceItems];
 #pragma unroll
-                for (int e = 0; e < kReduceItems; ++e) {
-                    const int t = (int)threadIdx.x + e * kThreads;   // t = quad * 128 + row
-                    const int r = t & (kTileRows - 1), q = t / kTileRows;
-                    val[e] = (t < items) ? __ldcg(src + (size_t)r * quads + q) : make_float4(0.f, 0.f, 0.f, 0.f);
+                for (int u = 0; u < 4; ++u) {
+                    const float4* src = reinterpret_cast<const float4*>(
+                        p.partials + (size_t)((s0 + u) * p.tiles + tile) * kTileRows * (size_t)mp);
+#pragma unroll
+                    for (int e = 0; e < kReduceItems; ++e) {
+                        const int t = (int)threadIdx.x + e * kThreads;   // t = quad * 128 + row
+                        const int r = t & (kTileRows - 1), q = t / kTileRows;
+                        val[u][e] = (s0 + u < p.splits && t < items) ? __ldcg(src + (size_t)r * quads + q)
+                                                                     : make_float4(0.f, 0.f, 0.f, 0.f);
+                    }
                 }
 #pragma unroll
-                for (int e = 0; e < kReduceItems; ++e) {
-                    acc[e].x += val[e].x;
-                    acc[e].y += val[e].y;
-                    acc[e].z += val[e].z;
-                    acc[e].w += val[e].w;
-                }
+                for (int u = 0; u < 4; ++u)
+#pragma unroll
+                    for (int e = 0; e < kReduceItems; ++e) {
+                        acc[e].x += val[u][e].x;
+                        acc[e].y += val[u][e].y;
+                        acc[e].z += val[u][e].z;
+                        acc[e].w += val[u][e].w;
+                    }
             }
 #pragma unroll
             for (int e = 0; e < kReduceItems; ++e) {
