@@ -26,7 +26,8 @@ cudaError_t launch_qmm_generic(const uint8_t* w, const void* X, void* Y, int y_b
                                int64_t K, int sm_count, cudaStream_t stream);
 cudaError_t launch_qmm_tc(const CUtensorMap& tmap_w, const CUtensorMap& tmap_x, void* y, int y_bf16, float* partials,
                           unsigned int* counters, unsigned int* fault, int M, int N, int K, int splits,
-                          cudaStream_t stream);
+                          int cluster, cudaStream_t stream);
+int qmm_tc_max_active_clusters(int nt, int cluster);
 int qmm_tc_tile_rows();
 int qmm_tc_group_k();
 
@@ -45,6 +46,9 @@ struct DeviceInfo {
     unsigned int* fault = nullptr;
     // streaming-kernel instantiations whose shared-memory limit was raised
     bool stream_prepared[3][9] = {};
+    // co-resident clusters of the small-M kernel, + 1 (0: not asked yet),
+    // by MMA width (16, 32) and cluster size (0 .. 8)
+    int qmm_clusters[2][9] = {};
 };
 
 std::mutex g_mu;
@@ -232,21 +236,39 @@ bool encode_x_map(CUtensorMap* m, const void* X, int64_t M, int64_t K, int nt) {
 // region of kQmmCounterBytes, then the partial sums.  Each call returns its
 // counters to zero, and no call's partial sums ever land on a counter.
 constexpr size_t kQmmCounterBytes = 4096;
+//
+// With 2 .. 8 splits per tile, and room on the device for all tiles' clusters
+// at once, the splits of a tile run as one cluster and add their partial sums
+// in distributed shared memory: no workspace.
+constexpr int kQmmMaxCluster = 8;
 struct QmmPlan {
-    bool tc = false;
+    bool tc = false, cluster = false;
     int tiles = 0, splits = 1;
     size_t partial_off = 0, workspace = 0;
 };
 
-QmmPlan plan_qmm(int64_t M, int64_t N, int64_t K, int sm_count) {
+int qmm_clusters_fit(DeviceInfo& di, int nt, int cluster) {
+    std::lock_guard<std::mutex> lk(g_mu);
+    int& c = di.qmm_clusters[nt > 16 ? 1 : 0][cluster];
+    if (c == 0) c = qmm_tc_max_active_clusters(nt, cluster) + 1;
+    return c - 1;
+}
+
+QmmPlan plan_qmm(int64_t M, int64_t N, int64_t K, DeviceInfo& di) {
     QmmPlan q;
     if (M < 1 || M > 32 || K % 256 != 0 || N < 1) return q;
     q.tc = true;
     q.tiles = (int)((N + qmm_tc_tile_rows() - 1) / qmm_tc_tile_rows());
     const int groups = (int)(K / qmm_tc_group_k());
-    int splits = sm_count / q.tiles;
+    int splits = di.sm_count / q.tiles;
     if (splits < 1) splits = 1;
     if (splits > groups) splits = groups;
+    if (splits >= 2 && splits <= kQmmMaxCluster &&
+        qmm_clusters_fit(di, (int)((M + 15) / 16 * 16), splits) >= q.tiles) {
+        q.splits = splits;
+        q.cluster = true;
+        return q;
+    }
     if ((size_t)q.tiles * 4 > kQmmCounterBytes) splits = 1;
     q.splits = splits;
     if (splits > 1) {
@@ -396,7 +418,7 @@ qbw_status qmv_gateup_q4_0(const void* w_gate, const void* w_up, const void* x, 
 size_t qmm_q4_0_smallM_workspace_bytes(int64_t M, int64_t N, int64_t K) {
     DeviceInfo* di = nullptr;
     if (device_info(&di) != QBW_OK) return 0;
-    return plan_qmm(M, N, K, di->sm_count).workspace;
+    return plan_qmm(M, N, K, *di).workspace;
 }
 
 qbw_status qmm_q4_0_smallM(const void* w, const void* X, qbw_dtype xt, void* Y, qbw_dtype yt, int64_t M,
@@ -413,7 +435,7 @@ qbw_status qmm_q4_0_smallM(const void* w, const void* X, qbw_dtype xt, void* Y, 
     qbw_status st = device_info(&di);
     if (st != QBW_OK) return st;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    const QmmPlan q = plan_qmm(M, N, K, di->sm_count);
+    const QmmPlan q = plan_qmm(M, N, K, *di);
     if (q.tc && (uintptr_t)w % 16 == 0 && (uintptr_t)X % 16 == 0) {
         if (q.workspace) {
             if (!workspace || workspace_bytes < q.workspace || (uintptr_t)workspace % 256) return QBW_EWORKSPACE;
@@ -440,7 +462,7 @@ qbw_status qmm_q4_0_smallM(const void* w, const void* X, qbw_dtype xt, void* Y, 
             cudaError_t e = launch_qmm_tc(tw, tx, Y, yt == QBW_BF16,
                                           q.workspace ? reinterpret_cast<float*>(ws + q.partial_off) : nullptr,
                                           q.workspace ? reinterpret_cast<unsigned int*>(ws) : nullptr,
-                                          di->fault, (int)M, (int)N, (int)K, q.splits, s);
+                                          di->fault, (int)M, (int)N, (int)K, q.splits, q.cluster ? 1 : 0, s);
             return e == cudaSuccess ? QBW_OK : QBW_ECUDA;
         }
     }

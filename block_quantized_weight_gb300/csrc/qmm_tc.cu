@@ -33,10 +33,16 @@
 // within 2^-7 of its exact value relative (two roundings to 8 significant
 // bits, 2^-8 each), inside the 1e-2 bound on sum |w x| of the tensor-core path.
 //
-// Split K: each CTA writes its partial tile (128 rows x M, M padded to 4, one
-// row per lane as 16-byte vectors) to the workspace; the last CTA of a tile
-// (counted with an atomic) adds the partials in split order and writes Y, then
-// resets the counter so the workspace stays zero-filled.
+// Split K, two ways.  With at most 8 splits per tile, the splits of a tile run
+// as one thread-block cluster: each CTA leaves its partial tile (128 rows x M,
+// M padded to 4) in its own shared memory, which the pipeline no longer needs
+// once the last MMA has completed; after a cluster barrier each CTA sums a
+// slice of the tile over all CTAs of the cluster (distributed shared memory),
+// in split order, and writes it to Y; a second cluster barrier keeps every
+// CTA's shared memory alive until its peers have read it.  With more splits,
+// each CTA writes its partial tile to the workspace; the last CTA of a tile
+// (counted with an atomic) adds the partials in split order and writes Y,
+// then resets the counter so the workspace stays zero-filled.
 #include <cstdint>
 
 #include "qbw_device.cuh"
@@ -336,7 +342,27 @@ struct QmmParams {
     int32_t splits;
     int32_t tiles;          // ceil(N / 128)
     int32_t y_bf16;
+    int32_t cluster;        // 1: the splits of a tile are one cluster (no workspace)
 };
+
+__device__ __forceinline__ void cluster_sync_all() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void st_shared_f4(uint32_t a, float4 v) {
+    asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(a), "f"(v.x), "f"(v.y), "f"(v.z), "f"(v.w)
+                 : "memory");
+}
+
+// 16 bytes at shared-memory address `a` of the cluster's CTA `rank`
+__device__ __forceinline__ float4 ld_dsmem_f4(uint32_t a, uint32_t rank) {
+    uint32_t ra;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(ra) : "r"(a), "r"(rank));
+    float4 v;
+    asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(ra) : "memory");
+    return v;
+}
 
 __global__ void __launch_bounds__(kThreads, 1) qmm_q4_0_tc_kernel(const __grid_constant__ QmmParams p) {
     extern __shared__ __align__(1024) uint8_t smem[];
@@ -454,6 +480,14 @@ __global__ void __launch_bounds__(kThreads, 1) qmm_q4_0_tc_kernel(const __grid_c
                                 }
                             }
                         }
+                    } else if (p.cluster) {
+                        // column quad u of this row at byte (u * 128 + row) * 16 of
+                        // the CTA's shared memory: a warp stores 512 contiguous bytes
+#pragma unroll
+                        for (int q = 0; q < 16; q += 4)
+                            if (c0 + q < mp)
+                                st_shared_f4(sbase + (uint32_t)(((c0 + q) / 4 * kTileRows + row) * 16),
+                                             make_float4(v[q], v[q + 1], v[q + 2], v[q + 3]));
                     } else {
                         // this row's columns c0 .. c0 + 15 below mp, as 16-byte vectors
 #pragma unroll
@@ -462,7 +496,7 @@ __global__ void __launch_bounds__(kThreads, 1) qmm_q4_0_tc_kernel(const __grid_c
                                 *reinterpret_cast<float4*>(part + c0 + q) = make_float4(v[q], v[q + 1], v[q + 2], v[q + 3]);
                     }
                 }
-                __threadfence();              // partials visible before the split counter moves
+                if (!p.cluster) __threadfence();   // partials visible before the split counter moves
             } else {
                 ok = false;
             }
@@ -477,6 +511,44 @@ __global__ void __launch_bounds__(kThreads, 1) qmm_q4_0_tc_kernel(const __grid_c
         mbar_wait_bounded(dfull_bar, 0u, p.fault, kFaultMmaWaitTimeout);
         tc_fence_after();
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "n"(kTmemCols));
+    }
+
+    if (p.splits > 1 && p.cluster) {
+        // every partial tile of the cluster is in place after this barrier
+        cluster_sync_all();
+        const int mp = (p.M + 3) & ~3;
+        const int items = kTileRows * (mp / 4);           // (row, column quad), item t = quad * 128 + row
+        const int lo = items * split / p.splits, hi = items * (split + 1) / p.splits;
+        for (int t = lo + (int)threadIdx.x; t < hi; t += kThreads) {
+            float4 val[8];
+#pragma unroll
+            for (int s = 0; s < 8; ++s)
+                val[s] = s < p.splits ? ld_dsmem_f4(sbase + (uint32_t)t * 16u, (uint32_t)s) : make_float4(0.f, 0.f, 0.f, 0.f);
+            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+            for (int s = 0; s < 8; ++s) {
+                acc.x += val[s].x;
+                acc.y += val[s].y;
+                acc.z += val[s].z;
+                acc.w += val[s].w;
+            }
+            const int r = t & (kTileRows - 1), q = t / kTileRows;
+            const int n = tile * kTileRows + r;
+            if (n < p.N) {
+                const float o[4] = {acc.x, acc.y, acc.z, acc.w};
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    const int m = 4 * q + c;
+                    if (m < p.M) {
+                        if (p.y_bf16) store_out<__nv_bfloat16>(p.y, (int64_t)m * p.N + n, o[c]);
+                        else store_out<float>(p.y, (int64_t)m * p.N + n, o[c]);
+                    }
+                }
+            }
+        }
+        // no CTA leaves while a peer may still read its shared memory
+        cluster_sync_all();
+        return;
     }
 
     // split K: the last CTA of this tile adds the partials in split order
@@ -559,7 +631,7 @@ int qmm_tc_group_k() { return kGroupK; }
 
 cudaError_t launch_qmm_tc(const CUtensorMap& tmap_w, const CUtensorMap& tmap_x, void* y, int y_bf16, float* partials,
                           unsigned int* counters, unsigned int* fault, int M, int N, int K, int splits,
-                          cudaStream_t stream) {
+                          int cluster, cudaStream_t stream) {
     QmmParams p;
     p.tmap_w = tmap_w;
     p.tmap_x = tmap_x;
@@ -575,6 +647,7 @@ cudaError_t launch_qmm_tc(const CUtensorMap& tmap_w, const CUtensorMap& tmap_x, 
     p.splits = splits;
     p.tiles = (N + kTileRows - 1) / kTileRows;
     p.y_bf16 = y_bf16;
+    p.cluster = cluster;
     const size_t smem = qmm_tc_smem_bytes(p.NT);
     static thread_local int prepared_device = -1;
     int dev = 0;
@@ -585,8 +658,48 @@ cudaError_t launch_qmm_tc(const CUtensorMap& tmap_w, const CUtensorMap& tmap_x, 
         if (e != cudaSuccess) return e;
         prepared_device = dev;
     }
-    qmm_q4_0_tc_kernel<<<p.tiles * splits, kThreads, smem, stream>>>(p);
-    return cudaGetLastError();
+    if (!cluster) {
+        qmm_q4_0_tc_kernel<<<p.tiles * splits, kThreads, smem, stream>>>(p);
+        return cudaGetLastError();
+    }
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = (unsigned)splits;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.gridDim = dim3((unsigned)(p.tiles * splits));
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, qmm_q4_0_tc_kernel, p);
+}
+
+// Clusters of `cluster` CTAs (MMA width nt) that the device holds at once; 0
+// when such a launch is not possible.
+int qmm_tc_max_active_clusters(int nt, int cluster) {
+    if (cudaFuncSetAttribute(qmm_q4_0_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)qmm_tc_smem_bytes(32)) != cudaSuccess)
+        return 0;
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = (unsigned)cluster;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.gridDim = dim3((unsigned)cluster);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = qmm_tc_smem_bytes(nt);
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, qmm_q4_0_tc_kernel, &cfg) != cudaSuccess) {
+        cudaGetLastError();
+        return 0;
+    }
+    return n;
 }
 
 }  // namespace qbw

@@ -155,7 +155,10 @@ qbw_status qmv_gateup_q4_0(const void *w_gate, const void *w_up, const void *x, 
  *               zero, so the single zero-fill at allocation is enough, also
  *               when one workspace serves calls of different shapes.  Calls
  *               that share one workspace must not run concurrently.  May be
- *               NULL when the size query returns 0.
+ *               NULL when the size query returns 0: so it does for one K-split
+ *               per tile, and for 2 .. 8 splits when the device holds all the
+ *               tiles' thread-block clusters at once (the splits of a tile
+ *               then add their partial sums in distributed shared memory).
  *
  * Fast path: K % 256 == 0 and w, X 16-byte aligned (tcgen05 tensor cores);
  * other shapes take an exact CUDA-core path that needs no workspace.

@@ -72,6 +72,29 @@ def test_qmm_full_size_sampled(qbw, oracle, M, K):
             check_matvec(Y[m, n0:n1], y_ref, S, rel=1e-2, out_bf16=True, what=f"qmm full M={M} K={K} m={m}")
 
 
+# (M, N, K, whether a 152-SM GB300 runs the K-splits of a tile as one cluster).
+# Splits per tile = min(152 // tiles, K / 256); one CTA per SM holds clusters
+# of 2, 3, 4, 5, 6 and 7 CTAs 76, 46, 36, 28, 23 and 15 at a time, so 20 tiles
+# of 7 splits do not all fit and take the workspace path.
+CLUSTER_CASES = [(8, 4352, 2048, True), (32, 3328, 2048, True), (5, 2816, 1536, True), (16, 300, 512, True),
+                 (32, 8192, 1024, True), (8, 2560, 2048, False)]
+
+
+@pytest.mark.parametrize("M,N,K,cluster", CLUSTER_CASES)
+def test_qmm_cluster_split_shapes(qbw, oracle, M, N, K, cluster):
+    # 2 .. 8 K-splits per 128-row tile: the splits of a tile add their partial
+    # sums in distributed shared memory, with no workspace, when all the
+    # tiles' clusters fit on the device at once
+    if torch.cuda.get_device_properties(0).multi_processor_count == 152:
+        assert (qbw.qmm_q4_0_smallM_workspace_bytes(M, N, K) == 0) == cluster
+    w = synth.q4_0_weights(N, K, seed=N + M)
+    X = synth.activations((M, K), seed=M + 7, dtype="bf16")
+    Y_ref, S = oracle.qmm_q4_0(w, X, M, N, K)
+    for odt in (torch.float32, torch.bfloat16):
+        Y = run_qmm(qbw, w, X, M, N, K, odt, calls=3)
+        check_matvec(Y, Y_ref, S, rel=1e-2, out_bf16=(odt == torch.bfloat16), what=f"qmm cluster M={M} N={N} K={K}")
+
+
 def test_qmm_deterministic(qbw):
     M, N, K = 32, 1024, 5376
     w = dev_u8(synth.q4_0_weights(N, K, seed=9))
@@ -99,7 +122,8 @@ def test_qmm_constant_weights_closed_form(qbw, oracle):
 
 
 def test_qmm_workspace_too_small_is_rejected(qbw):
-    M, N, K = 16, 5376, 5376
+    # 5 tiles of 128 rows, 16 K-splits each: more splits than one cluster takes
+    M, N, K = 16, 640, 4096
     need = qbw.qmm_q4_0_smallM_workspace_bytes(M, N, K)
     if need == 0:
         pytest.skip("this device plans no split for the shape")

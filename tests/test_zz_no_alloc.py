@@ -54,8 +54,10 @@ def compare_with_workspace_path(qbw, M, N, K, odt, seed):
                                    (17, 256, 2048), (32, 128, 21504)])
 @pytest.mark.parametrize("odt", [torch.bfloat16, torch.float32])
 def test_noalloc_matches_workspace_entry(qbw, M, N, K, odt):
+    # the 5376-row shapes split K inside one cluster (no scratch) on a 152-SM
+    # part; the other two take the workspace path
     _, _, _, need = compare_with_workspace_path(qbw, M, N, K, odt, seed=M + N + K)
-    assert 0 < need <= qbw.NOALLOC_SCRATCH_BYTES
+    assert need <= qbw.NOALLOC_SCRATCH_BYTES
 
 
 def test_noalloc_against_oracle(qbw, oracle):
