@@ -28,6 +28,9 @@ cudaError_t launch_qmm_tc(const CUtensorMap& tmap_w, const CUtensorMap& tmap_x, 
                           unsigned int* counters, unsigned int* fault, int M, int N, int K, int splits,
                           int cluster, cudaStream_t stream);
 int qmm_tc_max_active_clusters(int nt, int cluster);
+bool qmv_tc_supported(int64_t N, int64_t K, int sm_count);
+cudaError_t launch_qmv_tc(const CUtensorMap& tmap_w, const void* x, int x_bf16, void* y, int y_bf16, int N, int K,
+                          int sm_count, unsigned int* fault, cudaStream_t stream);
 int qmm_tc_tile_rows();
 int qmm_tc_group_k();
 
@@ -216,6 +219,20 @@ bool plan_stream(int fmt, int nmat, int64_t N, int64_t K, const DeviceInfo& di, 
 
 // X [M][K] bf16 row-major as a 2-D tensor; box (64, nt) with the 128-byte
 // swizzle of the tensor-core B operand.
+// Q4_0 rows as 8-byte words in 128-row tiles of one 256-element K-group
+// (144 bytes per row): the raw-weight box of the tensor-core kernels.
+bool encode_q4_tile_map(CUtensorMap* m, const void* w, int64_t N, int64_t K) {
+    PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+    if (!enc) return false;
+    cuuint64_t dims[2] = {(cuuint64_t)((K / 32) * 18 / 8), (cuuint64_t)N};
+    cuuint64_t strides[1] = {(cuuint64_t)((K / 32) * 18)};
+    cuuint32_t box[2] = {(cuuint32_t)(144 / 8), (cuuint32_t)qmm_tc_tile_rows()};
+    cuuint32_t estr[2] = {1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT64, 2, const_cast<void*>(w), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 bool encode_x_map(CUtensorMap* m, const void* X, int64_t M, int64_t K, int nt) {
     PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
     if (!enc) return false;
@@ -357,6 +374,15 @@ qbw_status qmv_common(int fmt, int nmat, const void* w0, const void* w1, const v
     if (st != QBW_OK) return st;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const bool aligned = ((uintptr_t)w0 % 16 == 0) && (nmat == 1 || (uintptr_t)w1 % 16 == 0);
+    if (fmt == kFmtQ4 && nmat == 1 && K % 256 == 0 && aligned && (uintptr_t)x % 16 == 0 &&
+        qmv_tc_supported(N, K, di->sm_count)) {
+        CUtensorMap tw;
+        if (encode_q4_tile_map(&tw, w0, N, K)) {
+            cudaError_t e = launch_qmv_tc(tw, x, xt == QBW_BF16, y, yt == QBW_BF16, (int)N, (int)K, di->sm_count,
+                                          di->fault, s);
+            return e == cudaSuccess ? QBW_OK : QBW_ECUDA;
+        }
+    }
     if (K % 256 == 0 && aligned) {
         StreamPlan plan;
         if (plan_stream_cached(fmt, nmat, N, K, *di, &plan) &&
@@ -445,19 +471,7 @@ qbw_status qmm_q4_0_smallM(const void* w, const void* X, qbw_dtype xt, void* Y, 
         }
         CUtensorMap tw, tx;
         const int nt = (int)((M + 15) / 16 * 16);
-        PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
-        bool maps = enc != nullptr;
-        if (maps) {
-            cuuint64_t dims[2] = {(cuuint64_t)((K / 32) * 18 / 8), (cuuint64_t)N};
-            cuuint64_t strides[1] = {(cuuint64_t)((K / 32) * 18)};
-            cuuint32_t box[2] = {(cuuint32_t)(144 / 8), (cuuint32_t)qmm_tc_tile_rows()};
-            cuuint32_t estr[2] = {1, 1};
-            maps = enc(&tw, CU_TENSOR_MAP_DATA_TYPE_UINT64, 2, const_cast<void*>(w), dims, strides, box, estr,
-                       CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                       CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS &&
-                   encode_x_map(&tx, X, M, K, nt);
-        }
-        if (maps) {
+        if (encode_q4_tile_map(&tw, w, N, K) && encode_x_map(&tx, X, M, K, nt)) {
             uint8_t* ws = static_cast<uint8_t*>(workspace);
             cudaError_t e = launch_qmm_tc(tw, tx, Y, yt == QBW_BF16,
                                           q.workspace ? reinterpret_cast<float*>(ws + q.partial_off) : nullptr,

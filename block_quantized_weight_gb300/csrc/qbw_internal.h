@@ -15,6 +15,7 @@ enum FaultCode : unsigned int {
     kFaultBulkWaitTimeout = 1,   // an mbarrier guarding a bulk copy never completed
     kFaultMmaWaitTimeout = 2,    // an mbarrier guarding tensor-core work never completed
     kFaultBadIndex = 3,          // a token-table row index outside [0, N)
+    kFaultShareWaitTimeout = 4,  // a split tile's share from another CTA never arrived
 };
 
 enum : int { kFmtQ8 = 0, kFmtQ4 = 1 };

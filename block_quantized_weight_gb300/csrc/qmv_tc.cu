@@ -1,0 +1,571 @@
+// qmv_tc.cu -- the M = 1 Q4_0 matrix-vector product y = W x on the fifth-
+// generation tensor cores (tcgen05), for K a multiple of 256.
+//
+// Why tensor cores for one token: on CUDA cores every weight costs a code
+// extraction, an exact conversion to fp32 and a multiply-add, about 2.1
+// instructions, and that instruction stream, not HBM, bounds the CUDA-core
+// kernel.  Here a weight costs about 1.6 instructions: two codes become one
+// exact bf16x2 pair (byte permute, LOP3 with the exponent of 128, one packed
+// add of -136 that leaves c - 8 exactly), and the products and sums run on the
+// tensor core.
+//
+// Exact block scales.  A = the integer codes c - 8 (exact in bf16); the scale
+// d of each block is applied after the MMA, in fp32, so no weight is rounded.
+// The MMA's N dimension carries one column pair per block instead of one per
+// token: for a K-group of 256 (8 blocks), B is 16 columns x 256 K where column
+// 2j holds x_hi and column 2j + 1 holds x_lo over block j's 32 elements and
+// zeros elsewhere.  x_hi = bf16(x), x_lo = bf16(x - x_hi): their sum is x to
+// 2^-17 relative (bf16 activations are exact: x_lo = 0).  So after the 16 MMAs
+// of a group, D[row][2j] + D[row][2j + 1] is the block's exact-code dot
+// product sum_i (c_i - 8) x_i in fp32, and the row's thread adds
+// d_j * (D[2j] + D[2j + 1]) for j = 0..7, in that order.
+//
+// Work split (stream-K): the units are (128-row tile, K-group) pairs in
+// tile-major order; CTA c of C takes units [c U / C, (c + 1) U / C).  A tile
+// that a CTA covers in full is written to y by that CTA.  A tile split between
+// CTAs is finished by the CTA that covers its first unit (it reaches the tile
+// last, at the end of its range).  Every other CTA on the tile starts its range
+// inside it, completes its share early and publishes it then: one 64-bit word
+// per row, (value, 1).  The finisher waits for those words (bounded), adds
+// them after its own share in CTA order, writes y and marks them consumed
+// (tag 0).  Results are therefore bit-reproducible.
+//
+// Warp roles (16 warps): warps 0..11 are three sets of four dequantizing
+// warps; set s takes the CTA's units s, s + 3, ...; warp 4s + q owns rows
+// 32q .. 32q + 31 (its TMEM lane quarter) and, lanes 0..7, one eighth of the
+// group's B operand.  Warp 12 lane 0 issues the TMA copies of the raw rows
+// (128 rows x 144 bytes per unit) into a 6-stage ring.  Warp 13 + s lane 0
+// issues set s's MMAs (M = 128, N = 16, K = 16; 16 per unit) into set s's
+// accumulator.  Each set's rows read D back one unit later, while the next
+// unit's codes are already decoded in registers.
+#include <atomic>
+#include <cstdint>
+
+#include "qbw_device.cuh"
+#include "qbw_internal.h"
+#include "tc_common.cuh"
+
+namespace qbw {
+
+// Split-tile scratch, one slot per call in flight: each CTA's published
+// share of its first tile, per row (fp32 bits, tag) with tag 1 = published,
+// 0 = consumed (all zero at load).
+constexpr int kQtcSlots = 16;
+constexpr int kQtcMaxCtas = 160;
+constexpr int kQtcMaxTiles = 4096;
+__device__ unsigned long long g_qtc_share[kQtcSlots][kQtcMaxCtas][128];
+
+namespace {
+
+using namespace tc;
+
+constexpr int kTileRows = 128;
+constexpr int kGroupK = 256;
+constexpr int kGroupWords = 18;                  // 144 raw bytes per row per group, as 8-byte TMA words
+constexpr int kSets = 3;
+constexpr int kProducerWarp = 12;
+constexpr int kMmaWarp0 = 13;                    // set s's issuer: warp 13 + s
+constexpr int kThreads = 16 * 32;
+constexpr int kStages = 6;                       // a multiple of kSets: stage s always serves set s % 3
+constexpr int kN = 16;
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kACols = kGroupK / 2;         // 128 TMEM columns of A per set
+constexpr uint32_t kDCol = kSets * kACols;       // set s's two D buffers at columns 384 + 32 s (+ 16)
+constexpr uint32_t kRawStageBytes = kTileRows * 144;
+constexpr uint32_t kBBytes = kN * kGroupK * 2;   // 8 KB: 4 swizzle atoms of 16 rows x 128 B
+constexpr int kMaxLocalTiles = 8;
+constexpr uint32_t kBf16Minus136 = 0xC308C308u;
+
+constexpr uint32_t kOffB = kStages * kRawStageBytes;                          // 1024-aligned
+constexpr uint32_t kOffPart = kOffB + kSets * kBBytes;
+constexpr uint32_t kOffBar = kOffPart + kSets * kMaxLocalTiles * kTileRows * 4;
+constexpr int kBars = 2 * kStages + 2 * kSets + 1;
+constexpr uint32_t kOffSlot = kOffBar + 8 * kBars;
+constexpr uint32_t kSmemBytes = kOffSlot + 16;
+
+static_assert(kStages % kSets == 0, "stage s must serve set s % 3");
+static_assert(kOffB % 1024 == 0, "B operand needs 1024-byte alignment");
+
+struct QtcParams {
+    CUtensorMap tmap_w;      // Q4_0 rows as 8-byte words, box (18, 128)
+    const void* x;
+    void* y;
+    unsigned int* fault;
+    int32_t N, K;
+    int32_t tiles, groups, units;
+    int32_t slot;
+    int32_t x_bf16, y_bf16;
+};
+
+__device__ __forceinline__ uint32_t full_bar(uint32_t b0, int s) { return b0 + 8u * (uint32_t)s; }
+__device__ __forceinline__ uint32_t empty_bar(uint32_t b0, int s) { return b0 + 8u * (uint32_t)(kStages + s); }
+__device__ __forceinline__ uint32_t afull_bar(uint32_t b0, int a) { return b0 + 8u * (uint32_t)(2 * kStages + a); }
+__device__ __forceinline__ uint32_t aempty_bar(uint32_t b0, int a) {
+    return b0 + 8u * (uint32_t)(2 * kStages + kSets + a);
+}
+__device__ __forceinline__ uint32_t done_bar(uint32_t b0) { return b0 + 8u * (uint32_t)(2 * kStages + 2 * kSets); }
+
+__device__ __forceinline__ void st_relaxed_u64(unsigned long long* p, unsigned long long v) {
+    asm volatile("st.relaxed.gpu.global.b64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+__device__ __forceinline__ unsigned long long ld_relaxed_u64(const unsigned long long* p) {
+    unsigned long long v;
+    asm volatile("ld.relaxed.gpu.global.b64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ int unit_begin(int c, int units, int ctas) {
+    return (int)(((int64_t)units * c) / ctas);
+}
+
+// the CTA whose unit range holds unit u
+__device__ __forceinline__ int owner_of(int u, int units, int ctas) {
+    int c = (int)(((int64_t)u * ctas) / units);
+    while (c + 1 < ctas && unit_begin(c + 1, units, ctas) <= u) ++c;
+    while (c > 0 && unit_begin(c, units, ctas) > u) --c;
+    return c;
+}
+
+// One Q4_0 block of the row's group (qs[0] at byte OFF of the words v[]) ->
+// 16 bf16x2 columns of exact codes c - 8 in K order: column t holds elements
+// 2t and 2t + 1 (t < 8) or 16 + 2(t - 8) and 17 + 2(t - 8).
+template <int OFF>
+__device__ __forceinline__ void codes_block(const uint32_t (&v)[36], uint32_t* col) {
+    const uint32_t m136 = kBf16Minus136;
+#pragma unroll
+    for (int j = 0; j < 16; j += 2) {
+        const int byte = OFF + j;
+        uint32_t lo, hi;
+        if ((byte & 3) == 0) nibble_pairs<0>(v[byte >> 2], lo, hi);
+        else nibble_pairs<2>(v[byte >> 2], lo, hi);
+        asm("add.rn.bf16x2 %0, %1, %2;" : "=r"(col[j >> 1]) : "r"(lo), "r"(m136));
+        asm("add.rn.bf16x2 %0, %1, %2;" : "=r"(col[8 + (j >> 1)]) : "r"(hi), "r"(m136));
+    }
+}
+
+// Block pair P (blocks 2P, 2P + 1) of the group -> 32 columns
+template <int P>
+__device__ __forceinline__ void codes_pair(const uint32_t (&v)[36], uint32_t (&col)[32]) {
+    codes_block<36 * P + 2>(v, col);
+    codes_block<36 * P + 20>(v, col + 16);
+}
+
+// fp16 scales of blocks 2P (low half) and 2P + 1 (high half) of the group:
+// block 2P's in the low half of word 9P, block 2P + 1's in the high half of
+// word 9P + 4.
+__device__ __forceinline__ uint32_t scale_pair(const uint32_t (&v)[36], int P) {
+    uint32_t r;
+    asm("prmt.b32 %0, %1, %2, 0x7610;" : "=r"(r) : "r"(v[9 * P]), "r"(v[9 * P + 4]));
+    return r;
+}
+
+__device__ __forceinline__ float2 half2_to_float2(uint32_t h) {
+    float2 f;
+    asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %2;\n\tcvt.f32.f16 %0, lo;\n\tcvt.f32.f16 %1, hi;\n\t}"
+        : "=f"(f.x), "=f"(f.y)
+        : "r"(h));
+    return f;
+}
+
+// sum_j d_j (D[2j] + D[2j + 1]) of one unit, j = 0..7 in order
+__device__ __forceinline__ float unit_dot(const uint32_t (&dv)[16], const uint32_t (&dd)[4]) {
+    float r = 0.f;
+#pragma unroll
+    for (int p = 0; p < 4; ++p) {
+        const float2 d = half2_to_float2(dd[p]);
+        r = fmaf(d.x, __uint_as_float(dv[4 * p]) + __uint_as_float(dv[4 * p + 1]), r);
+        r = fmaf(d.y, __uint_as_float(dv[4 * p + 2]) + __uint_as_float(dv[4 * p + 3]), r);
+    }
+    return r;
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+    uint32_t r;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+__device__ __forceinline__ float bf16_lo_to_float(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi_to_float(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+__device__ __forceinline__ void sts128(uint32_t addr, uint4 v) {
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+                 : "memory");
+}
+
+// Byte offset, in the B operand (K-major, 128-byte swizzle, 16 rows), of the
+// 16-byte chunk holding elements 8c .. 8c + 7 of swizzle atom a, row n.
+__device__ __forceinline__ uint32_t b_chunk(int a, int n, int c) {
+    return (uint32_t)(a * 2048 + (n >> 3) * 1024 + (n & 7) * 128 + ((c ^ (n & 7)) << 4));
+}
+
+__global__ void __launch_bounds__(kThreads, 1) qmv_q4_0_tc_kernel(const __grid_constant__ QtcParams p) {
+    extern __shared__ __align__(1024) uint8_t smem[];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int ctas = (int)gridDim.x, cta = (int)blockIdx.x;
+    const int G = p.groups;
+    const int u0 = unit_begin(cta, p.units, ctas), u1 = unit_begin(cta + 1, p.units, ctas);
+    const int n = u1 - u0;
+    const int tile0 = u0 / G;
+    // this CTA starts inside its first tile: it publishes its share of it early
+    const bool contrib0 = n > 0 && tile0 * G < u0;
+    __shared__ unsigned int qcount[4];
+    if (threadIdx.x < 4) qcount[threadIdx.x] = 0u;
+    unsigned long long* share = &g_qtc_share[p.slot][0][0];
+
+    const uint32_t sbase = smem_u32(smem);
+    const uint32_t bar0 = sbase + kOffBar;
+    float* part = reinterpret_cast<float*>(smem + kOffPart);      // [set][local tile][row]
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffSlot);
+    bool ok = true;
+
+    // zero B operands (only their fixed activation positions are ever written
+    // again) and the per-set partial rows
+    for (int i = threadIdx.x; i < (int)(kSets * kBBytes / 16); i += kThreads)
+        sts128(sbase + kOffB + 16u * (uint32_t)i, make_uint4(0u, 0u, 0u, 0u));
+    for (int i = threadIdx.x; i < kSets * kMaxLocalTiles * kTileRows; i += kThreads) part[i] = 0.f;
+
+    if (warp == kProducerWarp) {
+        if (lane == 0) {
+            for (int s = 0; s < kStages; ++s) {
+                mbar_init(full_bar(bar0, s), 1);
+                mbar_init(empty_bar(bar0, s), 4);
+            }
+            for (int a = 0; a < kSets; ++a) {
+                mbar_init(afull_bar(bar0, a), 4);
+                mbar_init(aempty_bar(bar0, a), 1);
+            }
+            mbar_init(done_bar(bar0), kSets);
+            fence_mbar_init();
+        }
+        __syncwarp();
+        fence_proxy_async_smem();
+        asm volatile("bar.arrive 1, %0;" ::"n"(kThreads) : "memory");
+        if (lane == 0) {
+            prefetch_tmap(&p.tmap_w);
+            // weights do not depend on the preceding grid: start streaming now
+            for (int i = 0; i < n && ok; ++i) {
+                const int s = i % kStages;
+                if (i >= kStages)
+                    ok = mbar_wait_bounded(empty_bar(bar0, s), (uint32_t)((i / kStages) - 1) & 1u, p.fault,
+                                           kFaultBulkWaitTimeout);
+                if (!ok) break;
+                const int u = u0 + i, t = u / G, g = u - t * G;
+                mbar_arrive_expect_tx(full_bar(bar0, s), kRawStageBytes);
+                tma_load_2d(sbase + (uint32_t)s * kRawStageBytes, &p.tmap_w, g * kGroupWords, t * kTileRows,
+                            full_bar(bar0, s), policy_evict_first());
+            }
+        }
+    } else {
+        if (warp == 0) {
+            asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                             smem_u32(tmem_slot)),
+                         "n"(kTmemCols));
+            asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+        }
+        fence_proxy_async_smem();
+        tc_fence_before();
+        asm volatile("bar.sync 1, %0;" ::"n"(kThreads) : "memory");
+        tc_fence_after();
+    }
+    // x and y belong to the preceding grid's stream order
+    grid_dependency_wait();
+    grid_launch_dependents();
+
+    if (warp >= kMmaWarp0) {
+        // ---------------- MMA issuer of set s: 16 K-steps per unit into D_s
+        const int set = warp - kMmaWarp0;
+        const uint32_t tmem = *tmem_slot;
+        if (lane == 0) {
+            const uint32_t idesc = idesc_bf16(kTileRows, kN);
+            const uint32_t a_tmem = tmem + (uint32_t)set * kACols;
+            const uint64_t b0 = sw128_desc(sbase + kOffB + (uint32_t)set * kBBytes);
+            uint32_t phase = 0;
+            for (int i = set; i < n; i += kSets) {
+                // the set's k-th unit accumulates into D buffer k % 2
+                const uint32_t d_tmem = tmem + kDCol + 32u * (uint32_t)set + 16u * phase;
+                ok = mbar_wait_bounded(afull_bar(bar0, set), phase, p.fault, kFaultMmaWaitTimeout);
+                if (!ok) break;
+                tc_fence_after();
+#pragma unroll
+                for (int k = 0; k < kGroupK / 16; ++k)
+                    tc_mma(d_tmem, a_tmem + 8u * (uint32_t)k, b0 + (uint64_t)((k >> 2) * 128 + (k & 3) * 2), idesc,
+                           k > 0 ? 1u : 0u);
+                tc_commit(aempty_bar(bar0, set));
+                phase ^= 1u;
+            }
+            // completes when every MMA issued above has finished
+            tc_commit(done_bar(bar0));
+        }
+    } else if (warp < kProducerWarp) {
+        // ---------------- dequantizing warp: set s, lane quarter q
+        const int set = warp >> 2, q = warp & 3;
+        const uint32_t tmem = *tmem_slot;
+        const uint32_t lanes = (uint32_t)(32 * q) << 16;
+        const uint32_t a_taddr = tmem + lanes + (uint32_t)set * kACols;
+        const uint32_t d_taddr = tmem + lanes + kDCol + 32u * (uint32_t)set;   // + 16 (k % 2)
+        const uint32_t raw_row = (uint32_t)(32 * q + lane) * 144u;
+        const uint32_t bbuf = sbase + kOffB + (uint32_t)set * kBBytes;
+        // B chunk of this lane (lanes 0..7): elements 64q + 8 lane .. + 7 of
+        // the group, in block j = 2q + lane / 4, rows 2j (x_hi) and 2j + 1 (x_lo)
+        const int bj = 2 * q + (lane >> 2);
+        const uint32_t b_hi = bbuf + b_chunk(q, 2 * bj, lane & 7);
+        const uint32_t b_lo = bbuf + b_chunk(q, 2 * bj + 1, lane & 7);
+        const int row = 32 * q + lane;
+        bool counted = !contrib0;
+        // after the three sets' shares of the first tile are in part[][0][], the
+        // last of a quarter's three warps publishes the quarter's rows
+        auto count_in = [&]() {
+            __syncwarp();
+            unsigned int old = 0;
+            if (lane == 0) {
+                __threadfence_block();
+                old = atomicAdd(&qcount[q], 1u);
+            }
+            old = __shfl_sync(0xffffffffu, old, 0);
+            if (old == kSets - 1) {
+                __threadfence_block();
+                const float v = part[(0 * kMaxLocalTiles) * kTileRows + row] +
+                                part[(1 * kMaxLocalTiles) * kTileRows + row] +
+                                part[(2 * kMaxLocalTiles) * kTileRows + row];
+                st_relaxed_u64(share + (size_t)cta * kTileRows + row,
+                               (unsigned long long)__float_as_uint(v) | (1ull << 32));
+            }
+            counted = true;
+        };
+        float acc = 0.f;
+        int acc_tile = -1, pend_tile = -1;
+        uint32_t pend_dd[4] = {0u, 0u, 0u, 0u};
+        uint32_t phase = 0;
+        int k = 0;
+        for (int i = set; i < n; i += kSets, ++k) {
+            const int u = u0 + i, t = u / G, g = u - t * G;
+            const int s = i % kStages;
+            // this lane's eight activations of the group, loaded before the waits
+            uint4 xr0 = make_uint4(0u, 0u, 0u, 0u), xr1 = xr0;
+            if (lane < 8) {
+                const int e = g * kGroupK + 64 * q + 8 * lane;
+                if (p.x_bf16) {
+                    xr0 = __ldg(reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p.x) + e));
+                } else {
+                    xr0 = __ldg(reinterpret_cast<const uint4*>(static_cast<const float*>(p.x) + e));
+                    xr1 = __ldg(reinterpret_cast<const uint4*>(static_cast<const float*>(p.x) + e + 4));
+                }
+            }
+            const bool got = mbar_wait_bounded(full_bar(bar0, s), (uint32_t)(i / kStages) & 1u, p.fault,
+                                               kFaultBulkWaitTimeout);
+            if (!__all_sync(0xffffffffu, got)) {
+                ok = false;
+                break;
+            }
+            const uint32_t src = sbase + (uint32_t)s * kRawStageBytes + raw_row;
+            uint32_t v[36];
+#pragma unroll
+            for (int j = 0; j < 9; ++j) {
+                const uint4 w = lds128(src + 16u * (uint32_t)j);
+                v[4 * j] = w.x;
+                v[4 * j + 1] = w.y;
+                v[4 * j + 2] = w.z;
+                v[4 * j + 3] = w.w;
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(empty_bar(bar0, s));     // raw rows of stage s read
+            uint32_t dd[4];
+#pragma unroll
+            for (int P = 0; P < 4; ++P) dd[P] = scale_pair(v, P);
+            uint32_t c0[32], c1[32];
+            codes_pair<0>(v, c0);
+            if (k > 0) {
+                // the MMAs of this set's previous unit are done: A, B free, its D final
+                const bool free = mbar_wait_bounded(aempty_bar(bar0, set), phase, p.fault, kFaultMmaWaitTimeout);
+                if (!__all_sync(0xffffffffu, free)) {
+                    ok = false;
+                    break;
+                }
+                phase ^= 1u;
+                tc_fence_after();
+            }
+            if (lane < 8) {
+                uint4 hi, lo;
+                if (p.x_bf16) {
+                    hi = xr0;
+                    lo = make_uint4(0u, 0u, 0u, 0u);
+                } else {
+                    const float f[8] = {__uint_as_float(xr0.x), __uint_as_float(xr0.y), __uint_as_float(xr0.z),
+                                        __uint_as_float(xr0.w), __uint_as_float(xr1.x), __uint_as_float(xr1.y),
+                                        __uint_as_float(xr1.z), __uint_as_float(xr1.w)};
+                    uint32_t h[4], l[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        h[e] = pack_bf16x2(f[2 * e], f[2 * e + 1]);
+                        l[e] = pack_bf16x2(f[2 * e] - bf16_lo_to_float(h[e]), f[2 * e + 1] - bf16_hi_to_float(h[e]));
+                    }
+                    hi = make_uint4(h[0], h[1], h[2], h[3]);
+                    lo = make_uint4(l[0], l[1], l[2], l[3]);
+                }
+                sts128(b_hi, hi);
+                sts128(b_lo, lo);
+                fence_proxy_async_smem();     // B visible to the tensor core
+            }
+            tmem_st32(a_taddr, c0);
+            codes_pair<1>(v, c1);
+            tmem_wait_st();
+            tmem_st32(a_taddr + 32u, c1);
+            codes_pair<2>(v, c0);
+            tmem_wait_st();
+            tmem_st32(a_taddr + 64u, c0);
+            codes_pair<3>(v, c1);
+            tmem_wait_st();
+            tmem_st32(a_taddr + 96u, c1);
+            tmem_wait_st();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(afull_bar(bar0, set));
+            if (k > 0) {
+                // the previous unit's D (buffer (k - 1) % 2), while the MMAs of
+                // this unit run into the other buffer
+                uint32_t dv[16];
+                tmem_ld16(d_taddr + 16u * (phase ^ 1u), dv);
+                tmem_wait_ld();
+                const float r = unit_dot(dv, pend_dd);
+                if (pend_tile != acc_tile) {
+                    if (acc_tile >= 0) part[(set * kMaxLocalTiles + (acc_tile - tile0)) * kTileRows + row] = acc;
+                    acc = 0.f;
+                    acc_tile = pend_tile;
+                    if (!counted && pend_tile > tile0) count_in();
+                }
+                acc += r;
+            }
+#pragma unroll
+            for (int P = 0; P < 4; ++P) pend_dd[P] = dd[P];
+            pend_tile = t;
+        }
+        if (ok && k > 0) {
+            // the set's last unit
+            const bool fin = mbar_wait_bounded(aempty_bar(bar0, set), phase, p.fault, kFaultMmaWaitTimeout);
+            if (__all_sync(0xffffffffu, fin)) {
+                tc_fence_after();
+                uint32_t dv[16];
+                tmem_ld16(d_taddr + 16u * phase, dv);
+                tmem_wait_ld();
+                const float r = unit_dot(dv, pend_dd);
+                if (pend_tile != acc_tile) {
+                    if (acc_tile >= 0) part[(set * kMaxLocalTiles + (acc_tile - tile0)) * kTileRows + row] = acc;
+                    acc = 0.f;
+                    acc_tile = pend_tile;
+                    if (!counted && pend_tile > tile0) count_in();
+                }
+                acc += r;
+            }
+        }
+        if (acc_tile >= 0) part[(set * kMaxLocalTiles + (acc_tile - tile0)) * kTileRows + row] = acc;
+        if (!counted) count_in();
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) {
+        // no MMA may still be writing TMEM when it is released
+        const uint32_t tmem = *tmem_slot;
+        mbar_wait_bounded(done_bar(bar0), 0u, p.fault, kFaultMmaWaitTimeout);
+        tc_fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "n"(kTmemCols));
+    }
+    if (n <= 0) return;
+
+    // ---------------- the range's tiles: whole ones -> y; the last one, when
+    // this CTA covers its first unit but not its last, is finished here
+    const int tile1 = (u1 - 1) / G;
+    const bool fin1 = (tile1 + 1) * G > u1 && tile1 * G >= u0;
+    const int r = threadIdx.x;
+    if (r < kTileRows) {
+        for (int t = tile0; t <= tile1; ++t) {
+            if (t == tile0 && contrib0) continue;                 // published already
+            const int lt = t - tile0;
+            float v = part[(0 * kMaxLocalTiles + lt) * kTileRows + r] +
+                      part[(1 * kMaxLocalTiles + lt) * kTileRows + r] +
+                      part[(2 * kMaxLocalTiles + lt) * kTileRows + r];
+            if (t == tile1 && fin1) {
+                const int c_last = owner_of((t + 1) * G - 1, p.units, ctas);
+                for (int c = cta + 1; c <= c_last; ++c) {
+                    unsigned long long* src = share + (size_t)c * kTileRows + r;
+                    unsigned long long w = ld_relaxed_u64(src);
+                    if (!(w >> 32)) {
+                        const uint64_t t0 = globaltimer_ns();
+                        while (!((w = ld_relaxed_u64(src)) >> 32)) {
+                            if (globaltimer_ns() - t0 > kWaitLimitNs) {
+                                record_fault(p.fault, kFaultShareWaitTimeout);
+                                break;
+                            }
+                        }
+                    }
+                    v += __uint_as_float((uint32_t)w);
+                    st_relaxed_u64(src, 0ull);                     // consumed
+                }
+            }
+            const int64_t yrow = (int64_t)t * kTileRows + r;
+            if (yrow < p.N) {
+                if (p.y_bf16) store_out<__nv_bfloat16>(p.y, yrow, v);
+                else store_out<float>(p.y, yrow, v);
+            }
+        }
+    }
+}
+
+}  // namespace
+
+// The tensor-core M = 1 path takes K % 256 == 0, at most kQtcMaxTiles tiles
+// and kQtcMaxCtas CTAs, and unit ranges that span at most kMaxLocalTiles
+// tiles per CTA.
+bool qmv_tc_supported(int64_t N, int64_t K, int sm_count) {
+    if (K % kGroupK != 0 || K < kGroupK || N < 1 || sm_count < 1 || sm_count > kQtcMaxCtas) return false;
+    const int64_t tiles = (N + kTileRows - 1) / kTileRows;
+    if (tiles > kQtcMaxTiles) return false;
+    const int64_t units = tiles * (K / kGroupK);
+    const int64_t ctas = units < sm_count ? units : sm_count;
+    const int64_t per = (units + ctas - 1) / ctas;
+    return per / (K / kGroupK) + 2 <= kMaxLocalTiles;
+}
+
+size_t qmv_tc_smem_bytes() { return kSmemBytes; }
+
+cudaError_t launch_qmv_tc(const CUtensorMap& tmap_w, const void* x, int x_bf16, void* y, int y_bf16, int N, int K,
+                          int sm_count, unsigned int* fault, cudaStream_t stream) {
+    static std::atomic<unsigned int> calls{0};
+    QtcParams p;
+    p.tmap_w = tmap_w;
+    p.x = x;
+    p.y = y;
+    p.fault = fault;
+    p.N = N;
+    p.K = K;
+    p.tiles = (N + kTileRows - 1) / kTileRows;
+    p.groups = K / kGroupK;
+    p.units = p.tiles * p.groups;
+    p.slot = (int)(calls.fetch_add(1u) % kQtcSlots);
+    p.x_bf16 = x_bf16;
+    p.y_bf16 = y_bf16;
+    const int ctas = p.units < sm_count ? p.units : sm_count;
+    static thread_local int prepared_device = -1;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (prepared_device != dev) {
+        cudaError_t e =
+            cudaFuncSetAttribute(qmv_q4_0_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+        if (e != cudaSuccess) return e;
+        prepared_device = dev;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.gridDim = dim3((unsigned)ctas);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = kSmemBytes;
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, qmv_q4_0_tc_kernel, p);
+}
+
+}  // namespace qbw

@@ -234,6 +234,8 @@ qbw_status qembed_q8_0(const void *w, const int32_t *ids, int64_t n_ids, void *o
  *   c = 1  a bounded wait for an asynchronous copy ran out (about two seconds)
  *   c = 2  a bounded wait for tensor-core work ran out
  *   c = 3  qembed_q8_0 met a row index outside [0, N)
+ *   c = 4  qmv_q4_0 waited in vain (about two seconds) for another CTA's share
+ *          of a 128-row tile split between CTAs
  * Synchronizes `stream`, stores the word in *code and, if clear != 0, resets
  * it to zero.
  */
