@@ -28,9 +28,9 @@ cudaError_t launch_qmm_tc(const CUtensorMap& tmap_w, const CUtensorMap& tmap_x, 
                           unsigned int* counters, unsigned int* fault, int M, int N, int K, int splits,
                           int cluster, cudaStream_t stream);
 int qmm_tc_max_active_clusters(int nt, int cluster);
-bool qmv_tc_supported(int64_t N, int64_t K, int sm_count);
-cudaError_t launch_qmv_tc(const CUtensorMap& tmap_w, const void* x, int x_bf16, void* y, int y_bf16, int N, int K,
-                          int sm_count, unsigned int* fault, cudaStream_t stream);
+bool qmv_tc_supported(int nmat, int64_t N, int64_t K, int sm_count);
+cudaError_t launch_qmv_tc(int nmat, const CUtensorMap* tmap_w, const void* x, int x_bf16, void* y, int y_bf16,
+                          int N, int K, int sm_count, unsigned int* fault, cudaStream_t stream);
 int qmm_tc_tile_rows();
 int qmm_tc_group_k();
 
@@ -374,12 +374,12 @@ qbw_status qmv_common(int fmt, int nmat, const void* w0, const void* w1, const v
     if (st != QBW_OK) return st;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const bool aligned = ((uintptr_t)w0 % 16 == 0) && (nmat == 1 || (uintptr_t)w1 % 16 == 0);
-    if (fmt == kFmtQ4 && nmat == 1 && K % 256 == 0 && aligned && (uintptr_t)x % 16 == 0 &&
-        qmv_tc_supported(N, K, di->sm_count)) {
-        CUtensorMap tw;
-        if (encode_q4_tile_map(&tw, w0, N, K)) {
-            cudaError_t e = launch_qmv_tc(tw, x, xt == QBW_BF16, y, yt == QBW_BF16, (int)N, (int)K, di->sm_count,
-                                          di->fault, s);
+    if (fmt == kFmtQ4 && K % 256 == 0 && aligned && (uintptr_t)x % 16 == 0 &&
+        qmv_tc_supported(nmat, N, K, di->sm_count)) {
+        CUtensorMap tw[2];
+        if (encode_q4_tile_map(&tw[0], w0, N, K) && (nmat == 1 || encode_q4_tile_map(&tw[1], w1, N, K))) {
+            cudaError_t e = launch_qmv_tc(nmat, tw, x, xt == QBW_BF16, y, yt == QBW_BF16, (int)N, (int)K,
+                                          di->sm_count, di->fault, s);
             return e == cudaSuccess ? QBW_OK : QBW_ECUDA;
         }
     }

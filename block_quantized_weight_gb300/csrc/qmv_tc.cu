@@ -53,7 +53,7 @@ namespace qbw {
 constexpr int kQtcSlots = 16;
 constexpr int kQtcMaxCtas = 160;
 constexpr int kQtcMaxTiles = 4096;
-__device__ unsigned long long g_qtc_share[kQtcSlots][kQtcMaxCtas][128];
+__device__ unsigned long long g_qtc_share[kQtcSlots][kQtcMaxCtas][2][128];
 
 namespace {
 
@@ -78,8 +78,8 @@ constexpr uint32_t kBf16Minus136 = 0xC308C308u;
 
 constexpr uint32_t kOffB = kStages * kRawStageBytes;                          // 1024-aligned
 constexpr uint32_t kOffPart = kOffB + kSets * kBBytes;
-constexpr uint32_t kOffBar = kOffPart + kSets * kMaxLocalTiles * kTileRows * 4;
-constexpr int kBars = 2 * kStages + 2 * kSets + 1;
+constexpr uint32_t kOffBar = kOffPart + kSets * kMaxLocalTiles * 2 * kTileRows * 4;
+constexpr int kBars = 2 * kStages + 4 * kSets + 1;
 constexpr uint32_t kOffSlot = kOffBar + 8 * kBars;
 constexpr uint32_t kSmemBytes = kOffSlot + 16;
 
@@ -87,23 +87,27 @@ static_assert(kStages % kSets == 0, "stage s must serve set s % 3");
 static_assert(kOffB % 1024 == 0, "B operand needs 1024-byte alignment");
 
 struct QtcParams {
-    CUtensorMap tmap_w;      // Q4_0 rows as 8-byte words, box (18, 128)
+    CUtensorMap tmap_w[2];   // Q4_0 rows as 8-byte words, box (18, 128); [1]: the up matrix of gate+up
     const void* x;
     void* y;
     unsigned int* fault;
     int32_t N, K;
-    int32_t tiles, groups, units;
+    int32_t tiles, groups, units;     // units = tiles x groups x matrices
     int32_t slot;
     int32_t x_bf16, y_bf16;
 };
 
 __device__ __forceinline__ uint32_t full_bar(uint32_t b0, int s) { return b0 + 8u * (uint32_t)s; }
 __device__ __forceinline__ uint32_t empty_bar(uint32_t b0, int s) { return b0 + 8u * (uint32_t)(kStages + s); }
-__device__ __forceinline__ uint32_t afull_bar(uint32_t b0, int a) { return b0 + 8u * (uint32_t)(2 * kStages + a); }
-__device__ __forceinline__ uint32_t aempty_bar(uint32_t b0, int a) {
-    return b0 + 8u * (uint32_t)(2 * kStages + kSets + a);
+// afull(a, h): half h (K 128h .. 128h + 127) of set a's A and B operands is
+// written; aempty(a, h): the MMAs reading that half have completed.
+__device__ __forceinline__ uint32_t afull_bar(uint32_t b0, int a, int h) {
+    return b0 + 8u * (uint32_t)(2 * kStages + 2 * a + h);
 }
-__device__ __forceinline__ uint32_t done_bar(uint32_t b0) { return b0 + 8u * (uint32_t)(2 * kStages + 2 * kSets); }
+__device__ __forceinline__ uint32_t aempty_bar(uint32_t b0, int a, int h) {
+    return b0 + 8u * (uint32_t)(2 * kStages + 2 * kSets + 2 * a + h);
+}
+__device__ __forceinline__ uint32_t done_bar(uint32_t b0) { return b0 + 8u * (uint32_t)(2 * kStages + 4 * kSets); }
 
 __device__ __forceinline__ void st_relaxed_u64(unsigned long long* p, unsigned long long v) {
     asm volatile("st.relaxed.gpu.global.b64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
@@ -112,6 +116,11 @@ __device__ __forceinline__ unsigned long long ld_relaxed_u64(const unsigned long
     unsigned long long v;
     asm volatile("ld.relaxed.gpu.global.b64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
     return v;
+}
+
+// per-set partial rows in shared memory: [set][local tile][matrix][row]
+__device__ __forceinline__ int part_at(int set, int lt, int m, int row) {
+    return ((set * kMaxLocalTiles + lt) * 2 + m) * kTileRows + row;
 }
 
 __device__ __forceinline__ int unit_begin(int c, int units, int ctas) {
@@ -199,23 +208,26 @@ __device__ __forceinline__ uint32_t b_chunk(int a, int n, int c) {
     return (uint32_t)(a * 2048 + (n >> 3) * 1024 + (n & 7) * 128 + ((c ^ (n & 7)) << 4));
 }
 
+// NMAT = 1: y = W x.  NMAT = 2: out = gelu_tanh(Wg x) * (Wu x); the units of a
+// (tile, group) are its gate and up halves, in that order.
+template <int NMAT>
 __global__ void __launch_bounds__(kThreads, 1) qmv_q4_0_tc_kernel(const __grid_constant__ QtcParams p) {
     extern __shared__ __align__(1024) uint8_t smem[];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int ctas = (int)gridDim.x, cta = (int)blockIdx.x;
-    const int G = p.groups;
+    const int G = p.groups, GU = p.groups * NMAT;    // K-groups, units per tile
     const int u0 = unit_begin(cta, p.units, ctas), u1 = unit_begin(cta + 1, p.units, ctas);
     const int n = u1 - u0;
-    const int tile0 = u0 / G;
+    const int tile0 = u0 / GU;
     // this CTA starts inside its first tile: it publishes its share of it early
-    const bool contrib0 = n > 0 && tile0 * G < u0;
+    const bool contrib0 = n > 0 && tile0 * GU < u0;
     __shared__ unsigned int qcount[4];
     if (threadIdx.x < 4) qcount[threadIdx.x] = 0u;
-    unsigned long long* share = &g_qtc_share[p.slot][0][0];
+    unsigned long long* share = &g_qtc_share[p.slot][0][0][0];   // [cta][matrix][row]
 
     const uint32_t sbase = smem_u32(smem);
     const uint32_t bar0 = sbase + kOffBar;
-    float* part = reinterpret_cast<float*>(smem + kOffPart);      // [set][local tile][row]
+    float* part = reinterpret_cast<float*>(smem + kOffPart);      // [set][local tile][matrix][row]
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffSlot);
     bool ok = true;
 
@@ -223,7 +235,7 @@ __global__ void __launch_bounds__(kThreads, 1) qmv_q4_0_tc_kernel(const __grid_c
     // again) and the per-set partial rows
     for (int i = threadIdx.x; i < (int)(kSets * kBBytes / 16); i += kThreads)
         sts128(sbase + kOffB + 16u * (uint32_t)i, make_uint4(0u, 0u, 0u, 0u));
-    for (int i = threadIdx.x; i < kSets * kMaxLocalTiles * kTileRows; i += kThreads) part[i] = 0.f;
+    for (int i = threadIdx.x; i < kSets * kMaxLocalTiles * 2 * kTileRows; i += kThreads) part[i] = 0.f;
 
     if (warp == kProducerWarp) {
         if (lane == 0) {
@@ -231,10 +243,11 @@ __global__ void __launch_bounds__(kThreads, 1) qmv_q4_0_tc_kernel(const __grid_c
                 mbar_init(full_bar(bar0, s), 1);
                 mbar_init(empty_bar(bar0, s), 4);
             }
-            for (int a = 0; a < kSets; ++a) {
-                mbar_init(afull_bar(bar0, a), 4);
-                mbar_init(aempty_bar(bar0, a), 1);
-            }
+            for (int a = 0; a < kSets; ++a)
+                for (int h = 0; h < 2; ++h) {
+                    mbar_init(afull_bar(bar0, a, h), 4);
+                    mbar_init(aempty_bar(bar0, a, h), 1);
+                }
             mbar_init(done_bar(bar0), kSets);
             fence_mbar_init();
         }
@@ -242,7 +255,8 @@ __global__ void __launch_bounds__(kThreads, 1) qmv_q4_0_tc_kernel(const __grid_c
         fence_proxy_async_smem();
         asm volatile("bar.arrive 1, %0;" ::"n"(kThreads) : "memory");
         if (lane == 0) {
-            prefetch_tmap(&p.tmap_w);
+            prefetch_tmap(&p.tmap_w[0]);
+            if (NMAT == 2) prefetch_tmap(&p.tmap_w[1]);
             // weights do not depend on the preceding grid: start streaming now
             for (int i = 0; i < n && ok; ++i) {
                 const int s = i % kStages;
@@ -250,9 +264,9 @@ __global__ void __launch_bounds__(kThreads, 1) qmv_q4_0_tc_kernel(const __grid_c
                     ok = mbar_wait_bounded(empty_bar(bar0, s), (uint32_t)((i / kStages) - 1) & 1u, p.fault,
                                            kFaultBulkWaitTimeout);
                 if (!ok) break;
-                const int u = u0 + i, t = u / G, g = u - t * G;
+                const int u = u0 + i, ug = u / NMAT, mat = u - ug * NMAT, t = ug / G, g = ug - t * G;
                 mbar_arrive_expect_tx(full_bar(bar0, s), kRawStageBytes);
-                tma_load_2d(sbase + (uint32_t)s * kRawStageBytes, &p.tmap_w, g * kGroupWords, t * kTileRows,
+                tma_load_2d(sbase + (uint32_t)s * kRawStageBytes, &p.tmap_w[mat], g * kGroupWords, t * kTileRows,
                             full_bar(bar0, s), policy_evict_first());
             }
         }
@@ -284,14 +298,23 @@ __global__ void __launch_bounds__(kThreads, 1) qmv_q4_0_tc_kernel(const __grid_c
             for (int i = set; i < n; i += kSets) {
                 // the set's k-th unit accumulates into D buffer k % 2
                 const uint32_t d_tmem = tmem + kDCol + 32u * (uint32_t)set + 16u * phase;
-                ok = mbar_wait_bounded(afull_bar(bar0, set), phase, p.fault, kFaultMmaWaitTimeout);
+                // K-steps 0..7 as soon as the first half is written, 8..15 after the second
+                ok = mbar_wait_bounded(afull_bar(bar0, set, 0), phase, p.fault, kFaultMmaWaitTimeout);
                 if (!ok) break;
                 tc_fence_after();
 #pragma unroll
-                for (int k = 0; k < kGroupK / 16; ++k)
+                for (int k = 0; k < 8; ++k)
                     tc_mma(d_tmem, a_tmem + 8u * (uint32_t)k, b0 + (uint64_t)((k >> 2) * 128 + (k & 3) * 2), idesc,
                            k > 0 ? 1u : 0u);
-                tc_commit(aempty_bar(bar0, set));
+                tc_commit(aempty_bar(bar0, set, 0));
+                ok = mbar_wait_bounded(afull_bar(bar0, set, 1), phase, p.fault, kFaultMmaWaitTimeout);
+                if (!ok) break;
+                tc_fence_after();
+#pragma unroll
+                for (int k = 8; k < 16; ++k)
+                    tc_mma(d_tmem, a_tmem + 8u * (uint32_t)k, b0 + (uint64_t)((k >> 2) * 128 + (k & 3) * 2), idesc,
+                           1u);
+                tc_commit(aempty_bar(bar0, set, 1));
                 phase ^= 1u;
             }
             // completes when every MMA issued above has finished
@@ -325,21 +348,39 @@ __global__ void __launch_bounds__(kThreads, 1) qmv_q4_0_tc_kernel(const __grid_c
             old = __shfl_sync(0xffffffffu, old, 0);
             if (old == kSets - 1) {
                 __threadfence_block();
-                const float v = part[(0 * kMaxLocalTiles) * kTileRows + row] +
-                                part[(1 * kMaxLocalTiles) * kTileRows + row] +
-                                part[(2 * kMaxLocalTiles) * kTileRows + row];
-                st_relaxed_u64(share + (size_t)cta * kTileRows + row,
-                               (unsigned long long)__float_as_uint(v) | (1ull << 32));
+#pragma unroll
+                for (int m = 0; m < NMAT; ++m) {
+                    const float v = part[part_at(0, 0, m, row)] + part[part_at(1, 0, m, row)] +
+                                    part[part_at(2, 0, m, row)];
+                    st_relaxed_u64(share + ((size_t)cta * 2 + m) * kTileRows + row,
+                                   (unsigned long long)__float_as_uint(v) | (1ull << 32));
+                }
             }
             counted = true;
         };
-        float acc = 0.f;
-        int acc_tile = -1, pend_tile = -1;
+        // the row's sums of the tile being accumulated, one per matrix
+        float acc[NMAT];
+#pragma unroll
+        for (int m = 0; m < NMAT; ++m) acc[m] = 0.f;
+        int acc_tile = -1, pend_tile = -1, pend_mat = 0;
+        auto add_unit = [&](float r) {
+            if (pend_tile != acc_tile) {
+                if (acc_tile >= 0)
+#pragma unroll
+                    for (int m = 0; m < NMAT; ++m) part[part_at(set, acc_tile - tile0, m, row)] = acc[m];
+#pragma unroll
+                for (int m = 0; m < NMAT; ++m) acc[m] = 0.f;
+                acc_tile = pend_tile;
+                if (!counted && pend_tile > tile0) count_in();
+            }
+#pragma unroll
+            for (int m = 0; m < NMAT; ++m)
+                if (m == pend_mat) acc[m] += r;
+        };
         uint32_t pend_dd[4] = {0u, 0u, 0u, 0u};
-        uint32_t phase = 0;
         int k = 0;
         for (int i = set; i < n; i += kSets, ++k) {
-            const int u = u0 + i, t = u / G, g = u - t * G;
+            const int u = u0 + i, ug = u / NMAT, mat = u - ug * NMAT, t = ug / G, g = ug - t * G;
             const int s = i % kStages;
             // this lane's eight activations of the group, loaded before the waits
             uint4 xr0 = make_uint4(0u, 0u, 0u, 0u), xr1 = xr0;
@@ -374,22 +415,12 @@ __global__ void __launch_bounds__(kThreads, 1) qmv_q4_0_tc_kernel(const __grid_c
 #pragma unroll
             for (int P = 0; P < 4; ++P) dd[P] = scale_pair(v, P);
             uint32_t c0[32], c1[32];
-            codes_pair<0>(v, c0);
-            if (k > 0) {
-                // the MMAs of this set's previous unit are done: A, B free, its D final
-                const bool free = mbar_wait_bounded(aempty_bar(bar0, set), phase, p.fault, kFaultMmaWaitTimeout);
-                if (!__all_sync(0xffffffffu, free)) {
-                    ok = false;
-                    break;
-                }
-                phase ^= 1u;
-                tc_fence_after();
-            }
+            // B chunk of this lane (lanes 0..7): x_hi and x_lo as bf16, written
+            // in the half (q / 2) the chunk belongs to
+            uint4 bhi = make_uint4(0u, 0u, 0u, 0u), blo = bhi;
             if (lane < 8) {
-                uint4 hi, lo;
                 if (p.x_bf16) {
-                    hi = xr0;
-                    lo = make_uint4(0u, 0u, 0u, 0u);
+                    bhi = xr0;
                 } else {
                     const float f[8] = {__uint_as_float(xr0.x), __uint_as_float(xr0.y), __uint_as_float(xr0.z),
                                         __uint_as_float(xr0.w), __uint_as_float(xr1.x), __uint_as_float(xr1.y),
@@ -400,19 +431,49 @@ __global__ void __launch_bounds__(kThreads, 1) qmv_q4_0_tc_kernel(const __grid_c
                         h[e] = pack_bf16x2(f[2 * e], f[2 * e + 1]);
                         l[e] = pack_bf16x2(f[2 * e] - bf16_lo_to_float(h[e]), f[2 * e + 1] - bf16_hi_to_float(h[e]));
                     }
-                    hi = make_uint4(h[0], h[1], h[2], h[3]);
-                    lo = make_uint4(l[0], l[1], l[2], l[3]);
+                    bhi = make_uint4(h[0], h[1], h[2], h[3]);
+                    blo = make_uint4(l[0], l[1], l[2], l[3]);
                 }
-                sts128(b_hi, hi);
-                sts128(b_lo, lo);
+            }
+            const uint32_t prev = (uint32_t)(k - 1) & 1u;     // completion parity of the previous unit
+            // ---- half 0: K 0..127 (block pairs 0, 1; B atoms 0, 1 written by warps 0, 1)
+            codes_pair<0>(v, c0);
+            if (k > 0) {
+                const bool free = mbar_wait_bounded(aempty_bar(bar0, set, 0), prev, p.fault, kFaultMmaWaitTimeout);
+                if (!__all_sync(0xffffffffu, free)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+            }
+            if (q < 2 && lane < 8) {
+                sts128(b_hi, bhi);
+                sts128(b_lo, blo);
                 fence_proxy_async_smem();     // B visible to the tensor core
             }
             tmem_st32(a_taddr, c0);
             codes_pair<1>(v, c1);
             tmem_wait_st();
             tmem_st32(a_taddr + 32u, c1);
-            codes_pair<2>(v, c0);
             tmem_wait_st();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(afull_bar(bar0, set, 0));
+            // ---- half 1: K 128..255 (block pairs 2, 3; B atoms 2, 3 written by warps 2, 3)
+            codes_pair<2>(v, c0);
+            if (k > 0) {
+                const bool free = mbar_wait_bounded(aempty_bar(bar0, set, 1), prev, p.fault, kFaultMmaWaitTimeout);
+                if (!__all_sync(0xffffffffu, free)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+            }
+            if (q >= 2 && lane < 8) {
+                sts128(b_hi, bhi);
+                sts128(b_lo, blo);
+                fence_proxy_async_smem();
+            }
             tmem_st32(a_taddr + 64u, c0);
             codes_pair<3>(v, c1);
             tmem_wait_st();
@@ -420,45 +481,35 @@ __global__ void __launch_bounds__(kThreads, 1) qmv_q4_0_tc_kernel(const __grid_c
             tmem_wait_st();
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(afull_bar(bar0, set));
+            if (lane == 0) mbar_arrive(afull_bar(bar0, set, 1));
             if (k > 0) {
-                // the previous unit's D (buffer (k - 1) % 2), while the MMAs of
-                // this unit run into the other buffer
+                // the previous unit's D (buffer (k - 1) % 2; complete since its
+                // second half's MMAs are), while this unit's MMAs use the other
                 uint32_t dv[16];
-                tmem_ld16(d_taddr + 16u * (phase ^ 1u), dv);
+                tmem_ld16(d_taddr + 16u * prev, dv);
                 tmem_wait_ld();
-                const float r = unit_dot(dv, pend_dd);
-                if (pend_tile != acc_tile) {
-                    if (acc_tile >= 0) part[(set * kMaxLocalTiles + (acc_tile - tile0)) * kTileRows + row] = acc;
-                    acc = 0.f;
-                    acc_tile = pend_tile;
-                    if (!counted && pend_tile > tile0) count_in();
-                }
-                acc += r;
+                add_unit(unit_dot(dv, pend_dd));
             }
 #pragma unroll
             for (int P = 0; P < 4; ++P) pend_dd[P] = dd[P];
             pend_tile = t;
+            pend_mat = mat;
         }
         if (ok && k > 0) {
-            // the set's last unit
-            const bool fin = mbar_wait_bounded(aempty_bar(bar0, set), phase, p.fault, kFaultMmaWaitTimeout);
+            // the set's last unit (k - 1)
+            const uint32_t last_par = (uint32_t)(k - 1) & 1u;
+            const bool fin = mbar_wait_bounded(aempty_bar(bar0, set, 1), last_par, p.fault, kFaultMmaWaitTimeout);
             if (__all_sync(0xffffffffu, fin)) {
                 tc_fence_after();
                 uint32_t dv[16];
-                tmem_ld16(d_taddr + 16u * phase, dv);
+                tmem_ld16(d_taddr + 16u * last_par, dv);
                 tmem_wait_ld();
-                const float r = unit_dot(dv, pend_dd);
-                if (pend_tile != acc_tile) {
-                    if (acc_tile >= 0) part[(set * kMaxLocalTiles + (acc_tile - tile0)) * kTileRows + row] = acc;
-                    acc = 0.f;
-                    acc_tile = pend_tile;
-                    if (!counted && pend_tile > tile0) count_in();
-                }
-                acc += r;
+                add_unit(unit_dot(dv, pend_dd));
             }
         }
-        if (acc_tile >= 0) part[(set * kMaxLocalTiles + (acc_tile - tile0)) * kTileRows + row] = acc;
+        if (acc_tile >= 0)
+#pragma unroll
+            for (int m = 0; m < NMAT; ++m) part[part_at(set, acc_tile - tile0, m, row)] = acc[m];
         if (!counted) count_in();
     }
 
@@ -475,38 +526,43 @@ __global__ void __launch_bounds__(kThreads, 1) qmv_q4_0_tc_kernel(const __grid_c
 
     // ---------------- the range's tiles: whole ones -> y; the last one, when
     // this CTA covers its first unit but not its last, is finished here
-    const int tile1 = (u1 - 1) / G;
-    const bool fin1 = (tile1 + 1) * G > u1 && tile1 * G >= u0;
+    const int tile1 = (u1 - 1) / GU;
+    const bool fin1 = (tile1 + 1) * GU > u1 && tile1 * GU >= u0;
     const int r = threadIdx.x;
     if (r < kTileRows) {
         for (int t = tile0; t <= tile1; ++t) {
             if (t == tile0 && contrib0) continue;                 // published already
             const int lt = t - tile0;
-            float v = part[(0 * kMaxLocalTiles + lt) * kTileRows + r] +
-                      part[(1 * kMaxLocalTiles + lt) * kTileRows + r] +
-                      part[(2 * kMaxLocalTiles + lt) * kTileRows + r];
+            float v[NMAT];
+#pragma unroll
+            for (int m = 0; m < NMAT; ++m)
+                v[m] = part[part_at(0, lt, m, r)] + part[part_at(1, lt, m, r)] + part[part_at(2, lt, m, r)];
             if (t == tile1 && fin1) {
-                const int c_last = owner_of((t + 1) * G - 1, p.units, ctas);
-                for (int c = cta + 1; c <= c_last; ++c) {
-                    unsigned long long* src = share + (size_t)c * kTileRows + r;
-                    unsigned long long w = ld_relaxed_u64(src);
-                    if (!(w >> 32)) {
-                        const uint64_t t0 = globaltimer_ns();
-                        while (!((w = ld_relaxed_u64(src)) >> 32)) {
-                            if (globaltimer_ns() - t0 > kWaitLimitNs) {
-                                record_fault(p.fault, kFaultShareWaitTimeout);
-                                break;
+                const int c_last = owner_of((t + 1) * GU - 1, p.units, ctas);
+                for (int c = cta + 1; c <= c_last; ++c)
+#pragma unroll
+                    for (int m = 0; m < NMAT; ++m) {
+                        unsigned long long* src = share + ((size_t)c * 2 + m) * kTileRows + r;
+                        unsigned long long w = ld_relaxed_u64(src);
+                        if (!(w >> 32)) {
+                            const uint64_t t0 = globaltimer_ns();
+                            while (!((w = ld_relaxed_u64(src)) >> 32)) {
+                                if (globaltimer_ns() - t0 > kWaitLimitNs) {
+                                    record_fault(p.fault, kFaultShareWaitTimeout);
+                                    break;
+                                }
                             }
                         }
+                        v[m] += __uint_as_float((uint32_t)w);
+                        st_relaxed_u64(src, 0ull);                 // consumed
                     }
-                    v += __uint_as_float((uint32_t)w);
-                    st_relaxed_u64(src, 0ull);                     // consumed
-                }
             }
             const int64_t yrow = (int64_t)t * kTileRows + r;
             if (yrow < p.N) {
-                if (p.y_bf16) store_out<__nv_bfloat16>(p.y, yrow, v);
-                else store_out<float>(p.y, yrow, v);
+                float o = v[0];
+                if constexpr (NMAT == 2) o = gelu_tanh(v[0]) * v[1];
+                if (p.y_bf16) store_out<__nv_bfloat16>(p.y, yrow, o);
+                else store_out<float>(p.y, yrow, o);
             }
         }
     }
@@ -517,23 +573,27 @@ __global__ void __launch_bounds__(kThreads, 1) qmv_q4_0_tc_kernel(const __grid_c
 // The tensor-core M = 1 path takes K % 256 == 0, at most kQtcMaxTiles tiles
 // and kQtcMaxCtas CTAs, and unit ranges that span at most kMaxLocalTiles
 // tiles per CTA.
-bool qmv_tc_supported(int64_t N, int64_t K, int sm_count) {
+bool qmv_tc_supported(int nmat, int64_t N, int64_t K, int sm_count) {
+    if (nmat < 1 || nmat > 2) return false;
     if (K % kGroupK != 0 || K < kGroupK || N < 1 || sm_count < 1 || sm_count > kQtcMaxCtas) return false;
     const int64_t tiles = (N + kTileRows - 1) / kTileRows;
     if (tiles > kQtcMaxTiles) return false;
-    const int64_t units = tiles * (K / kGroupK);
+    const int64_t per_tile = (K / kGroupK) * nmat;
+    const int64_t units = tiles * per_tile;
+    if (units > INT32_MAX) return false;
     const int64_t ctas = units < sm_count ? units : sm_count;
     const int64_t per = (units + ctas - 1) / ctas;
-    return per / (K / kGroupK) + 2 <= kMaxLocalTiles;
+    return per / per_tile + 2 <= kMaxLocalTiles;
 }
 
 size_t qmv_tc_smem_bytes() { return kSmemBytes; }
 
-cudaError_t launch_qmv_tc(const CUtensorMap& tmap_w, const void* x, int x_bf16, void* y, int y_bf16, int N, int K,
-                          int sm_count, unsigned int* fault, cudaStream_t stream) {
+cudaError_t launch_qmv_tc(int nmat, const CUtensorMap* tmap_w, const void* x, int x_bf16, void* y, int y_bf16,
+                          int N, int K, int sm_count, unsigned int* fault, cudaStream_t stream) {
     static std::atomic<unsigned int> calls{0};
     QtcParams p;
-    p.tmap_w = tmap_w;
+    p.tmap_w[0] = tmap_w[0];
+    p.tmap_w[1] = tmap_w[nmat == 2 ? 1 : 0];
     p.x = x;
     p.y = y;
     p.fault = fault;
@@ -541,17 +601,21 @@ cudaError_t launch_qmv_tc(const CUtensorMap& tmap_w, const void* x, int x_bf16, 
     p.K = K;
     p.tiles = (N + kTileRows - 1) / kTileRows;
     p.groups = K / kGroupK;
-    p.units = p.tiles * p.groups;
+    p.units = p.tiles * p.groups * nmat;
     p.slot = (int)(calls.fetch_add(1u) % kQtcSlots);
     p.x_bf16 = x_bf16;
     p.y_bf16 = y_bf16;
     const int ctas = p.units < sm_count ? p.units : sm_count;
+    auto kernel = nmat == 2 ? qmv_q4_0_tc_kernel<2> : qmv_q4_0_tc_kernel<1>;
     static thread_local int prepared_device = -1;
     int dev = 0;
     cudaGetDevice(&dev);
     if (prepared_device != dev) {
-        cudaError_t e =
-            cudaFuncSetAttribute(qmv_q4_0_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+        cudaError_t e = cudaFuncSetAttribute(qmv_q4_0_tc_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (int)kSmemBytes);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(qmv_q4_0_tc_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     (int)kSmemBytes);
         if (e != cudaSuccess) return e;
         prepared_device = dev;
     }
@@ -565,7 +629,7 @@ cudaError_t launch_qmv_tc(const CUtensorMap& tmap_w, const void* x, int x_bf16, 
     cfg.stream = stream;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, qmv_q4_0_tc_kernel, p);
+    return cudaLaunchKernelEx(&cfg, kernel, p);
 }
 
 }  // namespace qbw
