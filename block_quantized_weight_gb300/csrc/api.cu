@@ -374,7 +374,12 @@ qbw_status qmv_common(int fmt, int nmat, const void* w0, const void* w1, const v
     if (st != QBW_OK) return st;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const bool aligned = ((uintptr_t)w0 % 16 == 0) && (nmat == 1 || (uintptr_t)w1 % 16 == 0);
-    if (fmt == kFmtQ4 && K % 256 == 0 && aligned && (uintptr_t)x % 16 == 0 &&
+    // Q4_0 goes to the tensor cores from about 15 MB of weights (one matrix)
+    // or 32 MB (gate + up); below that the streaming kernel's shorter start-up
+    // wins (GB300, CUDA-graph replay: 5376 x 5376 8.3 vs 8.7 us, 4096 x 4096
+    // 6.7 vs 6.1 us; gate+up 21504 x 5376 30.8 vs 34.4 us, 8192 x 2048 9.9 vs 8.3 us).
+    const bool tc_size = (double)wbytes * nmat >= (nmat == 2 ? 32e6 : 15e6);
+    if (fmt == kFmtQ4 && tc_size && K % 256 == 0 && aligned && (uintptr_t)x % 16 == 0 &&
         qmv_tc_supported(nmat, N, K, di->sm_count)) {
         CUtensorMap tw[2];
         if (encode_q4_tile_map(&tw[0], w0, N, K) && (nmat == 1 || encode_q4_tile_map(&tw[1], w1, N, K))) {

@@ -92,6 +92,25 @@ def test_qmv_q4_0_full_21504x5376(qbw, oracle):
     assert worst < 1e-4
 
 
+# Shapes that take the tensor-core path (K % 256 == 0, at least 15 MB of Q4_0
+# weights, 32 MB for gate+up): a ragged last 128-row tile, K-groups split over
+# many CTAs (N = 600, K = 65536: every tile is shared by about 30 CTAs), and
+# both activation and output dtypes.
+TC_SHAPES = [(5413, 5376), (3000, 10240), (600, 65536)]
+
+
+@pytest.mark.parametrize("N,K", TC_SHAPES)
+@pytest.mark.parametrize("xdt,odt", [("f32", "f32"), ("bf16", "bf16")])
+def test_qmv_q4_0_tensor_core_shapes(qbw, oracle, N, K, xdt, odt):
+    w = synth.q4_0_weights(N, K, seed=N + K)
+    x = synth.activations(K, seed=K + 11, dtype=xdt)
+    y_ref, S = oracle.qmv("q4_0", w, x, N, K)
+    for _ in range(2):   # the second call must find the split-tile scratch consumed
+        y = run_qmv(qbw, "q4_0", w, x, N, K, odt)
+        check_matvec(y, y_ref, S, out_bf16=(odt == "bf16"), what=f"q4_0 tc N={N} K={K}")
+    assert qbw.fault_read(clear=True) == 0
+
+
 def run_gateup(qbw, wg, wu, x, N, K, odt):
     out = Guarded((N,), ODT[odt])
     qbw.qmv_gateup_q4_0(dev_u8(wg), dev_u8(wu), dev_act(x), out.t, 1, N, K)
@@ -119,6 +138,18 @@ def test_gateup_full_21504x5376(qbw, oracle):
     o = run_gateup(qbw, wg, wu, x, N, K, "f32")
     ref = oracle.gateup_q4_0(wg, wu, x, N, K)
     check_gateup(o, ref, oracle, what="gateup full")
+
+
+@pytest.mark.parametrize("odt", ["f32", "bf16"])
+def test_gateup_tensor_core_ragged(qbw, oracle, odt):
+    # 5413 rows: the last 128-row tile holds 37; 2 x 16.4 MB of weights
+    N, K = 5413, 5376
+    wg = synth.q4_0_weights(N, K, seed=51, stream=0)
+    wu = synth.q4_0_weights(N, K, seed=51, stream=1)
+    x = synth.activations(K, seed=51, dtype="bf16")
+    o = run_gateup(qbw, wg, wu, x, N, K, odt)
+    ref = oracle.gateup_q4_0(wg, wu, x, N, K)
+    check_gateup(o, ref, oracle, out_bf16=(odt == "bf16"), what="gateup tc ragged")
 
 
 def test_gateup_fused_buffer_and_large_gate(qbw, oracle):
