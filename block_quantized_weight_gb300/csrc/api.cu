@@ -29,8 +29,8 @@ cudaError_t launch_qmm_tc(const CUtensorMap& tmap_w, const CUtensorMap& tmap_x, 
                           int cluster, cudaStream_t stream);
 int qmm_tc_max_active_clusters(int nt, int cluster);
 bool qmv_tc_supported(int nmat, int64_t N, int64_t K, int sm_count);
-cudaError_t launch_qmv_tc(int nmat, const CUtensorMap* tmap_w, const void* x, int x_bf16, void* y, int y_bf16,
-                          int N, int K, int sm_count, unsigned int* fault, cudaStream_t stream);
+cudaError_t launch_qmv_tc(int nmat, int ntok, const CUtensorMap* tmap_w, const void* x, int x_bf16, void* y,
+                          int y_bf16, int N, int K, int sm_count, unsigned int* fault, cudaStream_t stream);
 int qmm_tc_tile_rows();
 int qmm_tc_group_k();
 
@@ -260,6 +260,7 @@ constexpr size_t kQmmCounterBytes = 4096;
 constexpr int kQmmMaxCluster = 8;
 struct QmmPlan {
     bool tc = false, cluster = false;
+    bool exact = false;    // one or two token rows on the exact-code M = 1 kernel (qmv_tc.cu)
     int tiles = 0, splits = 1;
     size_t partial_off = 0, workspace = 0;
 };
@@ -274,6 +275,13 @@ int qmm_clusters_fit(DeviceInfo& di, int nt, int cluster) {
 QmmPlan plan_qmm(int64_t M, int64_t N, int64_t K, DeviceInfo& di) {
     QmmPlan q;
     if (M < 1 || M > 32 || K % 256 != 0 || N < 1) return q;
+    // One or two tokens: the exact-code kernel carries them in its per-block
+    // B columns at the cost of one (same size threshold as qmv_q4_0).
+    if (M <= 2 && (double)N * (double)(K / 32) * 18.0 >= 15e6 && qmv_tc_supported(1, N, K, di.sm_count)) {
+        q.tc = true;
+        q.exact = true;
+        return q;
+    }
     q.tc = true;
     q.tiles = (int)((N + qmm_tc_tile_rows() - 1) / qmm_tc_tile_rows());
     const int groups = (int)(K / qmm_tc_group_k());
@@ -383,7 +391,7 @@ qbw_status qmv_common(int fmt, int nmat, const void* w0, const void* w1, const v
         qmv_tc_supported(nmat, N, K, di->sm_count)) {
         CUtensorMap tw[2];
         if (encode_q4_tile_map(&tw[0], w0, N, K) && (nmat == 1 || encode_q4_tile_map(&tw[1], w1, N, K))) {
-            cudaError_t e = launch_qmv_tc(nmat, tw, x, xt == QBW_BF16, y, yt == QBW_BF16, (int)N, (int)K,
+            cudaError_t e = launch_qmv_tc(nmat, 1, tw, x, xt == QBW_BF16, y, yt == QBW_BF16, (int)N, (int)K,
                                           di->sm_count, di->fault, s);
             return e == cudaSuccess ? QBW_OK : QBW_ECUDA;
         }
@@ -467,7 +475,15 @@ qbw_status qmm_q4_0_smallM(const void* w, const void* X, qbw_dtype xt, void* Y, 
     if (st != QBW_OK) return st;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const QmmPlan q = plan_qmm(M, N, K, *di);
-    if (q.tc && (uintptr_t)w % 16 == 0 && (uintptr_t)X % 16 == 0) {
+    if (q.exact && (uintptr_t)w % 16 == 0 && (uintptr_t)X % 16 == 0) {
+        CUtensorMap tw[2];
+        if (encode_q4_tile_map(&tw[0], w, N, K)) {
+            cudaError_t e = launch_qmv_tc(1, (int)M, tw, X, 1, Y, yt == QBW_BF16, (int)N, (int)K, di->sm_count,
+                                          di->fault, s);
+            return e == cudaSuccess ? QBW_OK : QBW_ECUDA;
+        }
+    }
+    if (q.tc && !q.exact && (uintptr_t)w % 16 == 0 && (uintptr_t)X % 16 == 0) {
         if (q.workspace) {
             if (!workspace || workspace_bytes < q.workspace || (uintptr_t)workspace % 256) return QBW_EWORKSPACE;
             if (overlaps(workspace, q.workspace, Y, ybytes) || overlaps(workspace, q.workspace, X, (size_t)M * K * 2) ||

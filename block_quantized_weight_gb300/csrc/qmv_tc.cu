@@ -176,16 +176,26 @@ __device__ __forceinline__ float2 half2_to_float2(uint32_t h) {
     return f;
 }
 
-// sum_j d_j (D[2j] + D[2j + 1]) of one unit, j = 0..7 in order
-__device__ __forceinline__ float unit_dot(const uint32_t (&dv)[16], const uint32_t (&dd)[4]) {
-    float r = 0.f;
+// One token (NTOK = 1): r0 = sum_j d_j (D[2j] + D[2j + 1]), the x_hi and x_lo
+// columns of block j.  Two tokens: r0 = sum_j d_j D[2j], r1 = sum_j d_j
+// D[2j + 1].  j = 0..7 in order.
+template <int NTOK>
+__device__ __forceinline__ void unit_dot(const uint32_t (&dv)[16], const uint32_t (&dd)[4], float& r0, float& r1) {
+    r0 = 0.f;
+    r1 = 0.f;
 #pragma unroll
     for (int p = 0; p < 4; ++p) {
         const float2 d = half2_to_float2(dd[p]);
-        r = fmaf(d.x, __uint_as_float(dv[4 * p]) + __uint_as_float(dv[4 * p + 1]), r);
-        r = fmaf(d.y, __uint_as_float(dv[4 * p + 2]) + __uint_as_float(dv[4 * p + 3]), r);
+        if constexpr (NTOK == 1) {
+            r0 = fmaf(d.x, __uint_as_float(dv[4 * p]) + __uint_as_float(dv[4 * p + 1]), r0);
+            r0 = fmaf(d.y, __uint_as_float(dv[4 * p + 2]) + __uint_as_float(dv[4 * p + 3]), r0);
+        } else {
+            r0 = fmaf(d.x, __uint_as_float(dv[4 * p]), r0);
+            r1 = fmaf(d.x, __uint_as_float(dv[4 * p + 1]), r1);
+            r0 = fmaf(d.y, __uint_as_float(dv[4 * p + 2]), r0);
+            r1 = fmaf(d.y, __uint_as_float(dv[4 * p + 3]), r1);
+        }
     }
-    return r;
 }
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
@@ -209,9 +219,14 @@ __device__ __forceinline__ uint32_t b_chunk(int a, int n, int c) {
 }
 
 // NMAT = 1: y = W x.  NMAT = 2: out = gelu_tanh(Wg x) * (Wu x); the units of a
-// (tile, group) are its gate and up halves, in that order.
-template <int NMAT>
+// (tile, group) are its gate and up halves, in that order.  NTOK = 2 (with
+// NMAT = 1 and bf16 activations): Y[m] = W X[m] for two token rows, which take
+// the two B columns of each block that x_hi and x_lo take for one token.
+// Each row keeps NCH = NMAT * NTOK sums (channels).
+template <int NMAT, int NTOK>
 __global__ void __launch_bounds__(kThreads, 1) qmv_q4_0_tc_kernel(const __grid_constant__ QtcParams p) {
+    constexpr int NCH = NMAT * NTOK;
+    static_assert(NCH <= 2, "at most two sums per row");
     extern __shared__ __align__(1024) uint8_t smem[];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int ctas = (int)gridDim.x, cta = (int)blockIdx.x;
@@ -349,7 +364,7 @@ __global__ void __launch_bounds__(kThreads, 1) qmv_q4_0_tc_kernel(const __grid_c
             if (old == kSets - 1) {
                 __threadfence_block();
 #pragma unroll
-                for (int m = 0; m < NMAT; ++m) {
+                for (int m = 0; m < NCH; ++m) {
                     const float v = part[part_at(0, 0, m, row)] + part[part_at(1, 0, m, row)] +
                                     part[part_at(2, 0, m, row)];
                     st_relaxed_u64(share + ((size_t)cta * 2 + m) * kTileRows + row,
@@ -359,23 +374,28 @@ __global__ void __launch_bounds__(kThreads, 1) qmv_q4_0_tc_kernel(const __grid_c
             counted = true;
         };
         // the row's sums of the tile being accumulated, one per matrix
-        float acc[NMAT];
+        float acc[NCH];
 #pragma unroll
-        for (int m = 0; m < NMAT; ++m) acc[m] = 0.f;
+        for (int m = 0; m < NCH; ++m) acc[m] = 0.f;
         int acc_tile = -1, pend_tile = -1, pend_mat = 0;
-        auto add_unit = [&](float r) {
+        auto add_unit = [&](float r0, float r1) {
             if (pend_tile != acc_tile) {
                 if (acc_tile >= 0)
 #pragma unroll
-                    for (int m = 0; m < NMAT; ++m) part[part_at(set, acc_tile - tile0, m, row)] = acc[m];
+                    for (int m = 0; m < NCH; ++m) part[part_at(set, acc_tile - tile0, m, row)] = acc[m];
 #pragma unroll
-                for (int m = 0; m < NMAT; ++m) acc[m] = 0.f;
+                for (int m = 0; m < NCH; ++m) acc[m] = 0.f;
                 acc_tile = pend_tile;
                 if (!counted && pend_tile > tile0) count_in();
             }
+            if constexpr (NTOK == 2) {
+                acc[0] += r0;
+                acc[1] += r1;
+            } else {
 #pragma unroll
-            for (int m = 0; m < NMAT; ++m)
-                if (m == pend_mat) acc[m] += r;
+                for (int m = 0; m < NMAT; ++m)
+                    if (m == pend_mat) acc[m] += r0;
+            }
         };
         uint32_t pend_dd[4] = {0u, 0u, 0u, 0u};
         int k = 0;
@@ -386,7 +406,10 @@ __global__ void __launch_bounds__(kThreads, 1) qmv_q4_0_tc_kernel(const __grid_c
             uint4 xr0 = make_uint4(0u, 0u, 0u, 0u), xr1 = xr0;
             if (lane < 8) {
                 const int e = g * kGroupK + 64 * q + 8 * lane;
-                if (p.x_bf16) {
+                if (NTOK == 2) {
+                    xr0 = __ldg(reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p.x) + e));
+                    xr1 = __ldg(reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p.x) + p.K + e));
+                } else if (p.x_bf16) {
                     xr0 = __ldg(reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p.x) + e));
                 } else {
                     xr0 = __ldg(reinterpret_cast<const uint4*>(static_cast<const float*>(p.x) + e));
@@ -419,7 +442,10 @@ __global__ void __launch_bounds__(kThreads, 1) qmv_q4_0_tc_kernel(const __grid_c
             // in the half (q / 2) the chunk belongs to
             uint4 bhi = make_uint4(0u, 0u, 0u, 0u), blo = bhi;
             if (lane < 8) {
-                if (p.x_bf16) {
+                if (NTOK == 2) {
+                    bhi = xr0;    // token 0 in the x_hi column, token 1 in the x_lo column
+                    blo = xr1;
+                } else if (p.x_bf16) {
                     bhi = xr0;
                 } else {
                     const float f[8] = {__uint_as_float(xr0.x), __uint_as_float(xr0.y), __uint_as_float(xr0.z),
@@ -488,7 +514,9 @@ __global__ void __launch_bounds__(kThreads, 1) qmv_q4_0_tc_kernel(const __grid_c
                 uint32_t dv[16];
                 tmem_ld16(d_taddr + 16u * prev, dv);
                 tmem_wait_ld();
-                add_unit(unit_dot(dv, pend_dd));
+                float r0, r1;
+                unit_dot<NTOK>(dv, pend_dd, r0, r1);
+                add_unit(r0, r1);
             }
 #pragma unroll
             for (int P = 0; P < 4; ++P) pend_dd[P] = dd[P];
@@ -504,12 +532,14 @@ __global__ void __launch_bounds__(kThreads, 1) qmv_q4_0_tc_kernel(const __grid_c
                 uint32_t dv[16];
                 tmem_ld16(d_taddr + 16u * last_par, dv);
                 tmem_wait_ld();
-                add_unit(unit_dot(dv, pend_dd));
+                float r0, r1;
+                unit_dot<NTOK>(dv, pend_dd, r0, r1);
+                add_unit(r0, r1);
             }
         }
         if (acc_tile >= 0)
 #pragma unroll
-            for (int m = 0; m < NMAT; ++m) part[part_at(set, acc_tile - tile0, m, row)] = acc[m];
+            for (int m = 0; m < NCH; ++m) part[part_at(set, acc_tile - tile0, m, row)] = acc[m];
         if (!counted) count_in();
     }
 
@@ -533,15 +563,15 @@ __global__ void __launch_bounds__(kThreads, 1) qmv_q4_0_tc_kernel(const __grid_c
         for (int t = tile0; t <= tile1; ++t) {
             if (t == tile0 && contrib0) continue;                 // published already
             const int lt = t - tile0;
-            float v[NMAT];
+            float v[NCH];
 #pragma unroll
-            for (int m = 0; m < NMAT; ++m)
+            for (int m = 0; m < NCH; ++m)
                 v[m] = part[part_at(0, lt, m, r)] + part[part_at(1, lt, m, r)] + part[part_at(2, lt, m, r)];
             if (t == tile1 && fin1) {
                 const int c_last = owner_of((t + 1) * GU - 1, p.units, ctas);
                 for (int c = cta + 1; c <= c_last; ++c)
 #pragma unroll
-                    for (int m = 0; m < NMAT; ++m) {
+                    for (int m = 0; m < NCH; ++m) {
                         unsigned long long* src = share + ((size_t)c * 2 + m) * kTileRows + r;
                         unsigned long long w = ld_relaxed_u64(src);
                         if (!(w >> 32)) {
@@ -559,10 +589,20 @@ __global__ void __launch_bounds__(kThreads, 1) qmv_q4_0_tc_kernel(const __grid_c
             }
             const int64_t yrow = (int64_t)t * kTileRows + r;
             if (yrow < p.N) {
-                float o = v[0];
-                if constexpr (NMAT == 2) o = gelu_tanh(v[0]) * v[1];
-                if (p.y_bf16) store_out<__nv_bfloat16>(p.y, yrow, o);
-                else store_out<float>(p.y, yrow, o);
+                if constexpr (NTOK == 2) {
+                    if (p.y_bf16) {
+                        store_out<__nv_bfloat16>(p.y, yrow, v[0]);
+                        store_out<__nv_bfloat16>(p.y, (int64_t)p.N + yrow, v[1]);
+                    } else {
+                        store_out<float>(p.y, yrow, v[0]);
+                        store_out<float>(p.y, (int64_t)p.N + yrow, v[1]);
+                    }
+                } else {
+                    float o = v[0];
+                    if constexpr (NMAT == 2) o = gelu_tanh(v[0]) * v[1];
+                    if (p.y_bf16) store_out<__nv_bfloat16>(p.y, yrow, o);
+                    else store_out<float>(p.y, yrow, o);
+                }
             }
         }
     }
@@ -588,9 +628,12 @@ bool qmv_tc_supported(int nmat, int64_t N, int64_t K, int sm_count) {
 
 size_t qmv_tc_smem_bytes() { return kSmemBytes; }
 
-cudaError_t launch_qmv_tc(int nmat, const CUtensorMap* tmap_w, const void* x, int x_bf16, void* y, int y_bf16,
-                          int N, int K, int sm_count, unsigned int* fault, cudaStream_t stream) {
+// nmat = 2: gate + up (one token).  ntok = 2 (nmat = 1, bf16 X of two rows
+// of K, Y of two rows of N): two tokens.
+cudaError_t launch_qmv_tc(int nmat, int ntok, const CUtensorMap* tmap_w, const void* x, int x_bf16, void* y,
+                          int y_bf16, int N, int K, int sm_count, unsigned int* fault, cudaStream_t stream) {
     static std::atomic<unsigned int> calls{0};
+    if (nmat * ntok > 2 || (ntok == 2 && !x_bf16)) return cudaErrorInvalidValue;
     QtcParams p;
     p.tmap_w[0] = tmap_w[0];
     p.tmap_w[1] = tmap_w[nmat == 2 ? 1 : 0];
@@ -606,17 +649,15 @@ cudaError_t launch_qmv_tc(int nmat, const CUtensorMap* tmap_w, const void* x, in
     p.x_bf16 = x_bf16;
     p.y_bf16 = y_bf16;
     const int ctas = p.units < sm_count ? p.units : sm_count;
-    auto kernel = nmat == 2 ? qmv_q4_0_tc_kernel<2> : qmv_q4_0_tc_kernel<1>;
+    auto kernel = nmat == 2 ? qmv_q4_0_tc_kernel<2, 1> : (ntok == 2 ? qmv_q4_0_tc_kernel<1, 2> : qmv_q4_0_tc_kernel<1, 1>);
     static thread_local int prepared_device = -1;
     int dev = 0;
     cudaGetDevice(&dev);
     if (prepared_device != dev) {
-        cudaError_t e = cudaFuncSetAttribute(qmv_q4_0_tc_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             (int)kSmemBytes);
-        if (e == cudaSuccess)
-            e = cudaFuncSetAttribute(qmv_q4_0_tc_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     (int)kSmemBytes);
-        if (e != cudaSuccess) return e;
+        for (auto f : {qmv_q4_0_tc_kernel<1, 1>, qmv_q4_0_tc_kernel<2, 1>, qmv_q4_0_tc_kernel<1, 2>}) {
+            cudaError_t e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+            if (e != cudaSuccess) return e;
+        }
         prepared_device = dev;
     }
     cudaLaunchConfig_t cfg = {};

@@ -161,7 +161,10 @@ qbw_status qmv_gateup_q4_0(const void *w_gate, const void *w_up, const void *x, 
  *               then add their partial sums in distributed shared memory).
  *
  * Fast path: K % 256 == 0 and w, X 16-byte aligned (tcgen05 tensor cores);
- * other shapes take an exact CUDA-core path that needs no workspace.
+ * other shapes take an exact CUDA-core path that needs no workspace.  With
+ * M <= 2 and at least 15 MB of weights the call runs on the exact-code kernel
+ * of qmv_q4_0 (integer codes on the tensor cores, block scales applied in
+ * fp32: no weight is rounded), which needs no workspace either.
  */
 size_t qmm_q4_0_smallM_workspace_bytes(int64_t M, int64_t N, int64_t K);
 qbw_status qmm_q4_0_smallM(const void *w, const void *X, qbw_dtype xt, void *Y, qbw_dtype yt,

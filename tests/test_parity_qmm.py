@@ -95,6 +95,21 @@ def test_qmm_cluster_split_shapes(qbw, oracle, M, N, K, cluster):
         check_matvec(Y, Y_ref, S, rel=1e-2, out_bf16=(odt == torch.bfloat16), what=f"qmm cluster M={M} N={N} K={K}")
 
 
+@pytest.mark.parametrize("M", [1, 2])
+@pytest.mark.parametrize("N,K", [(16384, 5376), (5413, 5376), (600, 65536)])
+@pytest.mark.parametrize("odt", [torch.bfloat16, torch.float32])
+def test_qmm_one_two_tokens_exact_path(qbw, oracle, M, N, K, odt):
+    # M <= 2 with at least 15 MB of weights runs on the exact-code M = 1
+    # kernel (the two tokens take the x_hi / x_lo columns): it needs no
+    # workspace and meets the M = 1 bound, 2e-3 of sum |w x|
+    assert qbw.qmm_q4_0_smallM_workspace_bytes(M, N, K) == 0
+    w = synth.q4_0_weights(N, K, seed=N + M)
+    X = synth.activations((M, K), seed=M + 17, dtype="bf16")
+    Y = run_qmm(qbw, w, X, M, N, K, odt, calls=2)
+    Y_ref, S = oracle.qmm_q4_0(w, X, M, N, K)
+    check_matvec(Y, Y_ref, S, rel=2e-3, out_bf16=(odt == torch.bfloat16), what=f"qmm exact M={M} N={N} K={K}")
+
+
 def test_qmm_deterministic(qbw):
     M, N, K = 32, 1024, 5376
     w = dev_u8(synth.q4_0_weights(N, K, seed=9))
