@@ -92,8 +92,8 @@ def load_peaks():
 # Sources whose change voids a kernel's profiled DRAM traffic (device code and
 # the host-side launch plan).
 KERNEL_SOURCES = {
-    "qmv_q4_0": ("qbw_device.cuh", "qbw_internal.h", "qmv_stream.cuh", "qmv_stream_q4.cu", "api.cu"),
-    "qmv_gateup_q4_0": ("qbw_device.cuh", "qbw_internal.h", "qmv_stream.cuh", "qmv_stream_gateup.cu", "api.cu"),
+    "qmv_q4_0": ("qbw_device.cuh", "qbw_internal.h", "tc_common.cuh", "qmv_tc.cu", "api.cu"),
+    "qmv_gateup_q4_0": ("qbw_device.cuh", "qbw_internal.h", "tc_common.cuh", "qmv_tc.cu", "api.cu"),
 }
 TRAFFIC_SUMMARY = os.path.join(ROOT, "profiles", "qmv_sweep_layer_traffic.txt")
 

@@ -220,7 +220,10 @@ bool plan_stream(int fmt, int nmat, int64_t N, int64_t K, const DeviceInfo& di, 
 // X [M][K] bf16 row-major as a 2-D tensor; box (64, nt) with the 128-byte
 // swizzle of the tensor-core B operand.
 // Q4_0 rows as 8-byte words in 128-row tiles of one 256-element K-group
-// (144 bytes per row): the raw-weight box of the tensor-core kernels.
+// (144 bytes per row): the raw-weight box of the tensor-core kernels.  No L2
+// promotion: a row's 144-byte segment then fetches only its own sectors
+// (with 256-byte promotion the fused gate+up read 137.6 MB per 130.1 MB of
+// weights, without it 134.9 MB, and ran 1 % faster).
 bool encode_q4_tile_map(CUtensorMap* m, const void* w, int64_t N, int64_t K) {
     PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
     if (!enc) return false;
@@ -229,7 +232,7 @@ bool encode_q4_tile_map(CUtensorMap* m, const void* w, int64_t N, int64_t K) {
     cuuint32_t box[2] = {(cuuint32_t)(144 / 8), (cuuint32_t)qmm_tc_tile_rows()};
     cuuint32_t estr[2] = {1, 1};
     return enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT64, 2, const_cast<void*>(w), dims, strides, box, estr,
-               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 

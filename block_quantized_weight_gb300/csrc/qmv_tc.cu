@@ -20,8 +20,9 @@
 // product sum_i (c_i - 8) x_i in fp32, and the row's thread adds
 // d_j * (D[2j] + D[2j + 1]) for j = 0..7, in that order.
 //
-// Work split (stream-K): the units are (128-row tile, K-group) pairs in
-// tile-major order; CTA c of C takes units [c U / C, (c + 1) U / C).  A tile
+// Work split (stream-K): the units are (128-row tile, K-group, matrix) triples
+// in that order (one matrix, or gate then up); CTA c of C takes units
+// [c U / C, (c + 1) U / C).  A tile
 // that a CTA covers in full is written to y by that CTA.  A tile split between
 // CTAs is finished by the CTA that covers its first unit (it reaches the tile
 // last, at the end of its range).  Every other CTA on the tile starts its range
@@ -219,7 +220,8 @@ __device__ __forceinline__ uint32_t b_chunk(int a, int n, int c) {
 }
 
 // NMAT = 1: y = W x.  NMAT = 2: out = gelu_tanh(Wg x) * (Wu x); the units of a
-// (tile, group) are its gate and up halves, in that order.  NTOK = 2 (with
+// (tile, group) are its gate and up halves, in that order (measured faster
+// than all gate groups of a tile before its up groups, by about 1 %).  NTOK = 2 (with
 // NMAT = 1 and bf16 activations): Y[m] = W X[m] for two token rows, which take
 // the two B columns of each block that x_hi and x_lo take for one token.
 // Each row keeps NCH = NMAT * NTOK sums (channels).
