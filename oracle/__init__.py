@@ -26,7 +26,7 @@ _lock = threading.Lock()
 _lib = None
 
 F32, BF16 = 0, 1
-_FMT = {"q8_0": 0, "q4_0": 1}
+_FMT = {"q8_0": 0, "q4_0": 1, "q4_k": 2}
 
 
 def build(force: bool = False) -> str:
@@ -78,6 +78,10 @@ def _declare(L):
     L.oracle_gateup_q4_0.argtypes = [P, P, P, ctypes.c_int, i64, i64, P, P, P, P, P]
     L.oracle_qmm_q4_0.restype = ctypes.c_int
     L.oracle_qmm_q4_0.argtypes = [P, P, ctypes.c_int, i64, i64, i64, P, P]
+    L.oracle_q4k_split_scale.restype = ctypes.c_int
+    L.oracle_q4k_split_scale.argtypes = [P, P, ctypes.c_int, i64, i64, P]
+    L.oracle_q4k_scale_min.restype = None
+    L.oracle_q4k_scale_min.argtypes = [P, ctypes.c_int, P, P]
 
 
 def _ptr(a: np.ndarray):
@@ -191,3 +195,22 @@ def qmm_q4_0(w: np.ndarray, X: np.ndarray, M: int, N: int, K: int):
     S = np.empty((M, N), dtype=np.float64)
     _check(lib().oracle_qmm_q4_0(_ptr(w), _ptr(X), xt, M, N, K, _ptr(Y), _ptr(S)), "qmm")
     return Y, S
+
+
+def q4k_split_scale(w: np.ndarray, x: np.ndarray, N: int, K: int) -> np.ndarray:
+    """S2 = sum (|d_sub q| + |m_sub|) |x| per row of a Q4_K matrix (fp64): the
+    error scale of the split d_sub * sum(q x) - m_sub * sum(x)."""
+    w = _weights(w)
+    x, xt = _act(x)
+    S2 = np.empty(N, dtype=np.float64)
+    _check(lib().oracle_q4k_split_scale(_ptr(w), _ptr(x), xt, N, K, _ptr(S2)), "q4k_split_scale")
+    return S2
+
+
+def q4k_scale_min(scale_bytes, j: int):
+    """(sc, m) of sub-block j from a Q4_K super-block's 12 scale bytes."""
+    sb = np.ascontiguousarray(scale_bytes, dtype=np.uint8)
+    sc = ctypes.c_int()
+    m = ctypes.c_int()
+    lib().oracle_q4k_scale_min(_ptr(sb), j, ctypes.byref(sc), ctypes.byref(m))
+    return sc.value, m.value

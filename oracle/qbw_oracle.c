@@ -19,6 +19,15 @@
  *    18 bytes (gem architecture, "M4 Max operating assumptions").  Nibble
  *    order follows the GGUF block_q4_0 record: code j in the low nibble of
  *    byte j, code j+16 in the high nibble.
+ *  - Q4_K super-block: 256 weights in 144 bytes, w = d_sub * q - m_sub with
+ *    d_sub = d * sc_j and m_sub = dmin * m_j for sub-block j (32 weights),
+ *    q a 4-bit code (jouleclaw-loader-gguf BENCHMARKS, "Q4_K matmul --
+ *    scalar fused vs AMX-tiled" and its NEON follow-up, which computes
+ *    sum(a * (d_sub * q - m_sub)) = d_sub * sum(a * q) - m_sub * sum(a)).
+ *    The byte layout follows the GGUF block_q4_K record: fp16 d, fp16 dmin,
+ *    12 bytes of 6-bit (sc, m) pairs, 128 bytes of nibbles; each 64-weight
+ *    chunk i keeps its first 32 codes in the low nibbles of bytes
+ *    32i .. 32i + 31 and its last 32 in their high nibbles.
  *  - Matrix-vector product y = W x with W stored [out, in] row-major
  *    (SafeC Gemma 4 design notes, "Math primitives implementation status").
  *  - Gated FFN projection out = gelu_tanh(Wg x) * (Wu x) with the tanh form
@@ -35,6 +44,7 @@
 #include <string.h>
 
 #define ORACLE_QK 32
+#define ORACLE_QK_K 256
 #define ORACLE_PI 3.14159265358979323846
 
 /* ---------------------------------------------------------------- decoders */
@@ -151,12 +161,48 @@ static uint16_t read_u16le(const uint8_t *p)
     return (uint16_t)(p[0] | (p[1] << 8));
 }
 
-/* fmt: 0 = Q8_0, 1 = Q4_0 */
-static int block_size(int fmt) { return fmt == 0 ? 34 : 18; }
+/* fmt: 0 = Q8_0, 1 = Q4_0, 2 = Q4_K */
+static int block_size(int fmt) { return fmt == 0 ? 34 : (fmt == 1 ? 18 : 144); }
+static int block_elems(int fmt) { return fmt == 2 ? ORACLE_QK_K : ORACLE_QK; }
 
-/* Decode the 32 weights of one block into w[0..31]. */
+/* The 6-bit scale sc and min m of sub-block j (0..7) of a Q4_K super-block,
+ * from its 12 scale bytes s[]: sub-blocks 0..3 keep sc and m in the low six
+ * bits of s[j] and s[j + 4]; sub-blocks 4..7 keep the low four bits of sc and
+ * of m in the low and high nibble of s[j + 4], and their top two bits in the
+ * top two bits of s[j - 4] (sc) and s[j] (m). */
+void oracle_q4k_scale_min(const uint8_t *s, int j, int *sc, int *m)
+{
+    if (j < 4) {
+        *sc = s[j] & 63;
+        *m = s[j + 4] & 63;
+    } else {
+        *sc = (s[j + 4] & 0x0f) | ((s[j - 4] >> 6) << 4);
+        *m = (s[j + 4] >> 4) | ((s[j] >> 6) << 4);
+    }
+}
+
+/* The code (0..15) of weight e (0..255) of a Q4_K super-block's 128 nibble
+ * bytes: chunk e / 64, low nibble for its first 32 weights, high for the rest. */
+static int q4k_code(const uint8_t *qs, int e)
+{
+    int chunk = e / 64, l = e % 64;
+    uint8_t byte = qs[32 * chunk + (l % 32)];
+    return (l < 32) ? (byte & 0x0f) : (byte >> 4);
+}
+
+/* Decode the weights of one block into w[0 .. block_elems(fmt) - 1]. */
 static void decode_block(int fmt, const uint8_t *blk, double *w)
 {
+    if (fmt == 2) {
+        double d = oracle_fp16_to_f64(read_u16le(blk));
+        double dmin = oracle_fp16_to_f64(read_u16le(blk + 2));
+        for (int e = 0; e < ORACLE_QK_K; e++) {
+            int sc, m;
+            oracle_q4k_scale_min(blk + 4, e / 32, &sc, &m);
+            w[e] = d * (double)sc * (double)q4k_code(blk + 16, e) - dmin * (double)m;
+        }
+        return;
+    }
     double d = oracle_fp16_to_f64(read_u16le(blk));
     for (int k = 0; k < ORACLE_QK; k++) {
         if (fmt == 0) {
@@ -169,20 +215,22 @@ static void decode_block(int fmt, const uint8_t *blk, double *w)
     }
 }
 
-/* Dequantize a whole matrix to fp32.  Every d*q fits in 24 bits of
- * significand (11-bit scale times a code of at most 8 bits), so the double
- * product converts to float exactly. */
+/* Dequantize a whole matrix to fp32.  Q8_0 / Q4_0: every d*q fits in 24 bits
+ * of significand (11-bit scale times a code of at most 8 bits), so the double
+ * product converts to float exactly.  Q4_K: d*sc*q and dmin*m are exact in
+ * double, and their difference is rounded to float once (nearest even). */
 int oracle_dequant(int fmt, const uint8_t *w, int64_t N, int64_t K, float *out)
 {
-    if (K % ORACLE_QK)
+    int be = block_elems(fmt);
+    if (K % be)
         return -1;
-    int64_t nb = K / ORACLE_QK;
-    double wb[ORACLE_QK];
+    int64_t nb = K / be;
+    double wb[ORACLE_QK_K];
     for (int64_t n = 0; n < N; n++)
         for (int64_t b = 0; b < nb; b++) {
             decode_block(fmt, w + (n * nb + b) * block_size(fmt), wb);
-            for (int k = 0; k < ORACLE_QK; k++)
-                out[n * K + b * ORACLE_QK + k] = (float)wb[k];
+            for (int k = 0; k < be; k++)
+                out[n * K + b * be + k] = (float)wb[k];
         }
     return 0;
 }
@@ -193,14 +241,15 @@ int oracle_dequant(int fmt, const uint8_t *w, int64_t N, int64_t K, float *out)
 static void matvec_rows(int fmt, const uint8_t *w, const double *x,
                         int64_t n0, int64_t n1, int64_t K, double *y, double *S)
 {
-    int64_t nb = K / ORACLE_QK;
-    double wb[ORACLE_QK];
+    int be = block_elems(fmt);
+    int64_t nb = K / be;
+    double wb[ORACLE_QK_K];
     for (int64_t n = n0; n < n1; n++) {
         double acc = 0.0, sabs = 0.0;
         for (int64_t b = 0; b < nb; b++) {
             decode_block(fmt, w + (n * nb + b) * block_size(fmt), wb);
-            for (int k = 0; k < ORACLE_QK; k++) {
-                double p = wb[k] * x[b * ORACLE_QK + k];
+            for (int k = 0; k < be; k++) {
+                double p = wb[k] * x[b * be + k];
                 acc += p;
                 sabs += fabs(p);
             }
@@ -214,7 +263,7 @@ static void matvec_rows(int fmt, const uint8_t *w, const double *x,
 int oracle_qmv(int fmt, const uint8_t *w, const void *x, int xdtype,
                int64_t N, int64_t K, double *y, double *S)
 {
-    if (K % ORACLE_QK)
+    if (K % block_elems(fmt))
         return -1;
     double *xd = widen_activations(x, xdtype, K);
     if (!xd)
@@ -228,7 +277,7 @@ int oracle_qmv(int fmt, const uint8_t *w, const void *x, int xdtype,
 int oracle_qmv_rows(int fmt, const uint8_t *w, const void *x, int xdtype,
                     int64_t n0, int64_t n1, int64_t K, double *y, double *S)
 {
-    if (K % ORACLE_QK)
+    if (K % block_elems(fmt))
         return -1;
     double *xd = widen_activations(x, xdtype, K);
     if (!xd)
@@ -295,6 +344,39 @@ int oracle_qmm_q4_0(const uint8_t *w, const void *X, int xdtype,
         return -2;
     for (int64_t m = 0; m < M; m++)
         matvec_rows(1, w, xd + m * K, 0, N, K, Y + m * N, S + m * N);
+    free(xd);
+    return 0;
+}
+
+/* The error scale of the algebraic split the Q4_K kernels compute,
+ * d_sub * sum(q x) - m_sub * sum(x) per sub-block: S2[n] = sum over
+ * sub-blocks j and their weights k of (|d_sub q_k| + |m_sub|) |x_k|.  Its two
+ * sums are formed separately, so their rounding scales with this, not with
+ * sum |w x| (which is 0 where d_sub q_k = m_sub exactly). */
+int oracle_q4k_split_scale(const uint8_t *w, const void *x, int xdtype,
+                           int64_t N, int64_t K, double *S2)
+{
+    if (K % ORACLE_QK_K)
+        return -1;
+    double *xd = widen_activations(x, xdtype, K);
+    if (!xd)
+        return -2;
+    int64_t nb = K / ORACLE_QK_K;
+    for (int64_t n = 0; n < N; n++) {
+        double s2 = 0.0;
+        for (int64_t b = 0; b < nb; b++) {
+            const uint8_t *blk = w + (n * nb + b) * 144;
+            double d = oracle_fp16_to_f64(read_u16le(blk));
+            double dmin = oracle_fp16_to_f64(read_u16le(blk + 2));
+            for (int e = 0; e < ORACLE_QK_K; e++) {
+                int sc, m;
+                oracle_q4k_scale_min(blk + 4, e / 32, &sc, &m);
+                double t = fabs(d * (double)sc * (double)q4k_code(blk + 16, e)) + fabs(dmin * (double)m);
+                s2 += t * fabs(xd[b * ORACLE_QK_K + e]);
+            }
+        }
+        S2[n] = s2;
+    }
     free(xd);
     return 0;
 }

@@ -16,8 +16,14 @@ the gem architecture page, "M4 Max operating assumptions", names Q4_0 as the
   ``j`` (0..15) sits in the low nibble of ``qs[j]`` and code ``j + 16`` in its
   high nibble.
 
-A matrix with N rows and K columns (K a multiple of 32) is N rows of K/32
-consecutive blocks, rows back to back, no padding.
+* Q4_K, 144 bytes per 256 weights (the GGUF ``block_q4_K`` record): fp16 ``d``,
+  fp16 ``dmin``, 12 scale bytes (six-bit scale and min of each 32-weight
+  sub-block), 128 bytes of nibbles.  The generator draws the 12 scale bytes
+  and the 128 nibble bytes as uniform random bytes: every byte pattern is a
+  valid block, so nothing here packs or interprets the six-bit fields.
+
+A matrix with N rows and K columns (K a multiple of 32, of 256 for Q4_K) is
+N rows of consecutive blocks, rows back to back, no padding.
 
 Random streams.  Every matrix or activation owns one
 ``numpy.random.Generator(PCG64(SeedSequence([seed, stream, layer])))``.  A
@@ -27,6 +33,8 @@ of its codes.  Activations use stream 99 unless told otherwise.
 * Q8_0 scale: ``fp16(|N(0, 0.02)| / 127)``; codes uniform on -127..127.
 * Q4_0 scale: ``fp16(|N(0, 0.02)| / 8)``; codes uniform on 0..15, drawn as
   uniform bytes (each byte is two independent uniform nibbles).
+* Q4_K: ``d = fp16(|N(0, 0.02)| / 240)``, then ``dmin = fp16(|N(0, 0.02)| / 64)``
+  for every super-block, then the scale bytes, then the nibble bytes.
 * Activations: fp32 draws of N(0, 1); a bf16 activation is the fp32 draw
   rounded to nearest-even bf16.  bf16 arrays are returned as their uint16
   bit patterns.
@@ -42,21 +50,29 @@ import os
 import numpy as np
 
 QK = 32                     # weights per block
+QK_K = 256                  # weights per Q4_K super-block
 Q8_0_BLOCK_BYTES = 34       # 2 (fp16 d) + 32 (int8 q)
 Q4_0_BLOCK_BYTES = 18       # 2 (fp16 d) + 16 (packed nibbles)
+Q4_K_BLOCK_BYTES = 144      # 2 (fp16 d) + 2 (fp16 dmin) + 12 (scales) + 128 (nibbles)
 ACT_STREAM = 99
 
-_BLOCK_BYTES = {"q8_0": Q8_0_BLOCK_BYTES, "q4_0": Q4_0_BLOCK_BYTES}
+_BLOCK_BYTES = {"q8_0": Q8_0_BLOCK_BYTES, "q4_0": Q4_0_BLOCK_BYTES, "q4_k": Q4_K_BLOCK_BYTES}
+_BLOCK_ELEMS = {"q8_0": QK, "q4_0": QK, "q4_k": QK_K}
 
 
 def block_bytes(fmt: str) -> int:
     return _BLOCK_BYTES[fmt]
 
 
+def block_elems(fmt: str) -> int:
+    return _BLOCK_ELEMS[fmt]
+
+
 def row_bytes(fmt: str, K: int) -> int:
-    if K % QK:
-        raise ValueError(f"K={K} is not a multiple of {QK}")
-    return (K // QK) * _BLOCK_BYTES[fmt]
+    be = _BLOCK_ELEMS[fmt]
+    if K % be:
+        raise ValueError(f"K={K} is not a multiple of {be}")
+    return (K // be) * _BLOCK_BYTES[fmt]
 
 
 def matrix_bytes(fmt: str, N: int, K: int) -> int:
@@ -98,11 +114,39 @@ def q4_0_weights(N: int, K: int, seed: int, stream: int = 0, layer: int = 0) -> 
     return _assemble(d.view(np.uint16), qs, Q4_0_BLOCK_BYTES)
 
 
+def q4_k_weights(N: int, K: int, seed: int, stream: int = 0, layer: int = 0) -> np.ndarray:
+    """Random Q4_K matrix, returned as a flat uint8 array of N*K/256*144 bytes."""
+    if K % QK_K:
+        raise ValueError("K must be a multiple of 256")
+    nb = N * (K // QK_K)
+    g = rng(seed, stream, layer)
+    d = (np.abs(g.standard_normal(nb)) * 0.02 / 240.0).astype(np.float16)
+    dmin = (np.abs(g.standard_normal(nb)) * 0.02 / 64.0).astype(np.float16)
+    scales = g.integers(0, 256, size=nb * 12, dtype=np.uint8)
+    qs = g.integers(0, 256, size=nb * 128, dtype=np.uint8)
+    return q4_k_records(d.view(np.uint16), dmin.view(np.uint16), scales, qs)
+
+
+def q4_k_records(d_bits, dmin_bits, scales, qs) -> np.ndarray:
+    """Lay out Q4_K super-blocks from their fields: fp16 bits of d and dmin (one
+    per block), 12 scale bytes and 128 nibble bytes per block."""
+    d_bits = np.asarray(d_bits, dtype=np.uint16).reshape(-1)
+    nb = d_bits.size
+    out = np.empty((nb, Q4_K_BLOCK_BYTES), dtype=np.uint8)
+    out[:, 0:2] = d_bits.astype("<u2").view(np.uint8).reshape(nb, 2)
+    out[:, 2:4] = np.asarray(dmin_bits, dtype=np.uint16).reshape(-1).astype("<u2").view(np.uint8).reshape(nb, 2)
+    out[:, 4:16] = np.asarray(scales, dtype=np.uint8).reshape(nb, 12)
+    out[:, 16:] = np.asarray(qs, dtype=np.uint8).reshape(nb, 128)
+    return out.reshape(-1)
+
+
 def weights(fmt: str, N: int, K: int, seed: int, stream: int = 0, layer: int = 0) -> np.ndarray:
     if fmt == "q8_0":
         return q8_0_weights(N, K, seed, stream, layer)
     if fmt == "q4_0":
         return q4_0_weights(N, K, seed, stream, layer)
+    if fmt == "q4_k":
+        return q4_k_weights(N, K, seed, stream, layer)
     raise ValueError(fmt)
 
 

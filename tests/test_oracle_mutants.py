@@ -45,6 +45,21 @@ MUTANTS = {
     "qmm_operand_transposed": ("matvec_rows(1, w, xd + m * K, 0, N, K, Y + m * N, S + m * N);",
                                "matvec_rows(1, w, xd + m, 0, N, K, Y + m * N, S + m * N);"),
     "gateup_gate_on_up": ("out[n] = oracle_gelu_tanh(g[n]) * u[n];", "out[n] = oracle_gelu_tanh(u[n]) * g[n];"),
+    "q4k_scale_min_swapped": ("*sc = s[j] & 63;\n        *m = s[j + 4] & 63;", "*sc = s[j + 4] & 63;\n        *m = s[j] & 63;"),
+    "q4k_high_bits_from_wrong_byte": ("*sc = (s[j + 4] & 0x0f) | ((s[j - 4] >> 6) << 4);",
+                                      "*sc = (s[j + 4] & 0x0f) | ((s[j] >> 6) << 4);"),
+    "q4k_min_nibble_low": ("*m = (s[j + 4] >> 4) | ((s[j] >> 6) << 4);", "*m = (s[j + 4] & 0x0f) | ((s[j] >> 6) << 4);"),
+    "q4k_nibble_halves_swapped": ("return (l < 32) ? (byte & 0x0f) : (byte >> 4);",
+                                  "return (l < 32) ? (byte >> 4) : (byte & 0x0f);"),
+    "q4k_chunk_stride": ("uint8_t byte = qs[32 * chunk + (l % 32)];", "uint8_t byte = qs[16 * chunk + (l % 32)];"),
+    "q4k_min_added": ("w[e] = d * (double)sc * (double)q4k_code(blk + 16, e) - dmin * (double)m;",
+                      "w[e] = d * (double)sc * (double)q4k_code(blk + 16, e) + dmin * (double)m;"),
+    "q4k_min_unscaled": ("w[e] = d * (double)sc * (double)q4k_code(blk + 16, e) - dmin * (double)m;",
+                         "w[e] = d * (double)sc * (double)q4k_code(blk + 16, e) - (double)m;"),
+    "q4k_dmin_read_as_d": ("double dmin = oracle_fp16_to_f64(read_u16le(blk + 2));\n        for (int e = 0; e < ORACLE_QK_K; e++) {\n            int sc, m;\n            oracle_q4k_scale_min(blk + 4, e / 32, &sc, &m);\n            w[e]",
+                           "double dmin = oracle_fp16_to_f64(read_u16le(blk));\n        for (int e = 0; e < ORACLE_QK_K; e++) {\n            int sc, m;\n            oracle_q4k_scale_min(blk + 4, e / 32, &sc, &m);\n            w[e]"),
+    "q4k_subblock_of_64": ("oracle_q4k_scale_min(blk + 4, e / 32, &sc, &m);\n            w[e]",
+                           "oracle_q4k_scale_min(blk + 4, e / 64, &sc, &m);\n            w[e]"),
 }
 
 
@@ -62,6 +77,7 @@ def test_pins_catch_mutant(name, tmp_path):
     env = dict(os.environ, QBW_ORACLE_LIB=str(so))
     r = subprocess.run([sys.executable, "-m", "pytest", "-x", "-q", "-p", "no:cacheprovider",
                         os.path.join(ROOT, "tests", "test_oracle_scalars.py"),
-                        os.path.join(ROOT, "tests", "test_oracle_products.py")],
+                        os.path.join(ROOT, "tests", "test_oracle_products.py"),
+                        os.path.join(ROOT, "tests", "test_oracle_q4k.py")],
                        cwd=ROOT, env=env, capture_output=True, text=True, timeout=600)
     assert r.returncode != 0, f"mutant {name} survived the pins:\n{r.stdout[-2000:]}"
