@@ -23,8 +23,8 @@ MUTANTS = {
     "q4_offset_sign": ("w[k] = d * (double)(code - 8);", "w[k] = d * (double)(code + 8);"),
     "q8_unsigned_codes": ("w[k] = d * (double)(int)(int8_t)blk[2 + k];", "w[k] = d * (double)(int)blk[2 + k];"),
     "q4_byte_index_off": ("uint8_t byte = blk[2 + (k % 16)];", "uint8_t byte = blk[1 + (k % 16)];"),
-    "scale_read_at_end": ("double d = oracle_fp16_to_f64(read_u16le(blk));",
-                          "double d = oracle_fp16_to_f64(read_u16le(blk + 16));"),
+    "scale_read_at_end": ("double d = oracle_fp16_to_f64(read_u16le(blk));\n    for (int k = 0; k < ORACLE_QK; k++) {",
+                          "double d = oracle_fp16_to_f64(read_u16le(blk + 16));\n    for (int k = 0; k < ORACLE_QK; k++) {"),
     "fp16_subnormal_scale": ("v = ldexp((double)m, -24);", "v = ldexp((double)m, -14);"),
     "fp16_bias_off_by_one": ("v = ldexp((double)(1024 + m), e - 25);", "v = ldexp((double)(1024 + m), e - 24);"),
     "fp16_implicit_bit_dropped": ("v = ldexp((double)(1024 + m), e - 25);", "v = ldexp((double)(m), e - 25);"),
@@ -32,10 +32,10 @@ MUTANTS = {
     "round_ties_away": ("(frac == 0.5 && fmod(fl, 2.0) != 0.0)", "(frac == 0.5)"),
     "abs_dropped_from_scale": ("sabs += fabs(p);", "sabs += p;"),
     "first_block_skipped": ("for (int64_t b = 0; b < nb; b++) {\n            decode_block(fmt, w + (n * nb + b) * "
-                            "block_size(fmt), wb);\n            for (int k = 0; k < ORACLE_QK; k++) {",
+                            "block_size(fmt), wb);\n            for (int k = 0; k < be; k++) {\n                double p",
                             "for (int64_t b = 1; b < nb; b++) {\n            decode_block(fmt, w + (n * nb + b) * "
-                            "block_size(fmt), wb);\n            for (int k = 0; k < ORACLE_QK; k++) {"),
-    "dequant_block_index": ("out[n * K + b * ORACLE_QK + k] = (float)wb[k];", "out[n * K + b + k] = (float)wb[k];"),
+                            "block_size(fmt), wb);\n            for (int k = 0; k < be; k++) {\n                double p"),
+    "dequant_block_index": ("out[n * K + b * be + k] = (float)wb[k];", "out[n * K + b + k] = (float)wb[k];"),
     "gelu_cubic_constant": ("return 0.5 * v * (1.0 + tanh(c * (v + 0.044715 * v * v * v)));",
                             "return 0.5 * v * (1.0 + tanh(c * (v + 0.04715 * v * v * v)));"),
     "gelu_linear_term_dropped": ("return 0.5 * v * (1.0 + tanh(c * (v + 0.044715 * v * v * v)));",
