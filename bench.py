@@ -360,6 +360,16 @@ def supplementary_kernels(torch, qbw, hbm_peak):
     run("qmv_gateup_q4_0 2x21504x5376 bf16->f32", 2 * w.numel() + 2 * K + 4 * N, copies,
         lambda i: (lambda: qbw.qmv_gateup_q4_0(ws[i], wus[i], xb, y, 1, N, K)))
     del ws, wus, w, wu
+    # the same shape in Q4_K (256-weight super-blocks, 144 bytes each), fp32 in/out
+    N, K = 21504, 5376
+    w = torch.from_numpy(synth.q4_k_weights(N, K, seed=1)).to(dev)
+    copies = max(2, int(np.ceil(2.2 * l2 / w.numel())))
+    ws = [w.clone() for _ in range(copies)]
+    x = torch.from_numpy(synth.activations(K, seed=1)).to(dev)
+    y = torch.empty(N, device=dev)
+    run("qmv_q4_k 21504x5376 f32", w.numel() + 4 * K + 4 * N, copies,
+        lambda i: (lambda: qbw.qmv_q4_k(ws[i], x, y, 1, N, K)))
+    del ws, w
     # small-M tiles
     for (N, K) in ((5376, 5376), (5376, 21504)):
         w = torch.from_numpy(synth.q4_0_weights(N, K, seed=3)).to(dev)

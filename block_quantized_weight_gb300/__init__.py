@@ -18,7 +18,7 @@ import threading
 __all__ = [
     "QbwError", "load", "lib_path",
     "qmv_q8_0", "qmv_q4_0", "qmv_gateup_q4_0", "qmm_q4_0_smallM", "qmm_q4_0_smallM_workspace_bytes",
-    "qmm_q4_0_smallM_noalloc", "NOALLOC_SCRATCH_BYTES", "qembed_q8_0", "qdequant_q8_0", "qdequant_q4_0", "fault_read", "status_str", "version",
+    "qmm_q4_0_smallM_noalloc", "NOALLOC_SCRATCH_BYTES", "qembed_q8_0", "qdequant_q8_0", "qdequant_q4_0", "qmv_q4_k", "qdequant_q4_k", "fault_read", "status_str", "version",
     "F32", "BF16",
 ]
 
@@ -62,7 +62,7 @@ def _declare(L):
     L.qbw_status_str.argtypes = [i32]
     L.qbw_version.restype = ctypes.c_uint32
     L.qbw_version.argtypes = []
-    for name in ("qmv_q8_0", "qmv_q4_0"):
+    for name in ("qmv_q8_0", "qmv_q4_0", "qmv_q4_k"):
         getattr(L, name).restype = i32
         getattr(L, name).argtypes = [P, P, i32, P, i32, i64, i64, i64, P]
     L.qmv_gateup_q4_0.restype = i32
@@ -75,7 +75,7 @@ def _declare(L):
     L.qembed_q8_0.argtypes = [P, P, i64, P, i32, i64, i64, P]
     L.qmm_q4_0_smallM_noalloc.restype = i32
     L.qmm_q4_0_smallM_noalloc.argtypes = [P, P, i32, P, i32, i64, i64, i64, P]
-    for name in ("qdequant_q8_0", "qdequant_q4_0"):
+    for name in ("qdequant_q8_0", "qdequant_q4_0", "qdequant_q4_k"):
         getattr(L, name).restype = i32
         getattr(L, name).argtypes = [P, P, i64, i64, P]
     L.qbw_fault_read.restype = i32
@@ -132,6 +132,14 @@ def qmv_q4_0(w, x, y, M: int, N: int, K: int, stream=None):
     return y
 
 
+def qmv_q4_k(w, x, y, M: int, N: int, K: int, stream=None):
+    """y = W x for raw Q4_K super-blocks ``w`` (uint8, 144 bytes per 256 weights)."""
+    L = load()
+    _check(L.qmv_q4_k(_ptr(w), _ptr(x), _dtype_code(x), _ptr(y), _dtype_code(y), M, N, K, _stream(stream)),
+           "qmv_q4_k")
+    return y
+
+
 def qmv_gateup_q4_0(w_gate, w_up, x, out, M: int, N: int, K: int, stream=None):
     """out = gelu_tanh(Wg x) * (Wu x) for two raw Q4_0 matrices."""
     L = load()
@@ -184,6 +192,12 @@ def qdequant_q8_0(w, out, N: int, K: int, stream=None):
 def qdequant_q4_0(w, out, N: int, K: int, stream=None):
     L = load()
     _check(L.qdequant_q4_0(_ptr(w), _ptr(out), N, K, _stream(stream)), "qdequant_q4_0")
+    return out
+
+
+def qdequant_q4_k(w, out, N: int, K: int, stream=None):
+    L = load()
+    _check(L.qdequant_q4_k(_ptr(w), _ptr(out), N, K, _stream(stream)), "qdequant_q4_k")
     return out
 
 

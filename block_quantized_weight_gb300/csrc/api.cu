@@ -29,8 +29,8 @@ cudaError_t launch_qmm_tc(const CUtensorMap& tmap_w, const CUtensorMap& tmap_x, 
                           int cluster, cudaStream_t stream);
 int qmm_tc_max_active_clusters(int nt, int cluster);
 bool qmv_tc_supported(int nmat, int64_t N, int64_t K, int sm_count);
-cudaError_t launch_qmv_tc(int nmat, int ntok, const CUtensorMap* tmap_w, const void* x, int x_bf16, void* y,
-                          int y_bf16, int N, int K, int sm_count, unsigned int* fault, cudaStream_t stream);
+cudaError_t launch_qmv_tc(int fmt, int nmat, int ntok, const CUtensorMap* tmap_w, const void* x, int x_bf16,
+                          void* y, int y_bf16, int N, int K, int sm_count, unsigned int* fault, cudaStream_t stream);
 int qmm_tc_tile_rows();
 int qmm_tc_group_k();
 
@@ -374,8 +374,9 @@ qbw_status qmv_common(int fmt, int nmat, const void* w0, const void* w1, const v
     if (!valid_dtype(xt) || !valid_dtype(yt)) return QBW_EDTYPE;
     if (M != 1) return QBW_ESHAPE;
     if (N < 1 || N > INT32_MAX || K < 32 || K % 32 != 0 || K > (int64_t(1) << 24)) return QBW_ESHAPE;
+    if (fmt == kFmtQ4K && K % 256 != 0) return QBW_ESHAPE;
     if ((uintptr_t)x % dtype_size(xt) || (uintptr_t)y % dtype_size(yt)) return QBW_EALIGN;
-    const size_t wbytes = (size_t)N * (size_t)(K / 32) * block_bytes(fmt);
+    const size_t wbytes = (size_t)N * (size_t)weight_row_bytes(fmt, K);
     const size_t ybytes = (size_t)N * dtype_size(yt);
     if (overlaps(y, ybytes, x, (size_t)K * dtype_size(xt)) || overlaps(y, ybytes, w0, wbytes) ||
         (nmat == 2 && overlaps(y, ybytes, w1, wbytes)))
@@ -389,17 +390,19 @@ qbw_status qmv_common(int fmt, int nmat, const void* w0, const void* w1, const v
     // or 32 MB (gate + up); below that the streaming kernel's shorter start-up
     // wins (GB300, CUDA-graph replay: 5376 x 5376 8.3 vs 8.7 us, 4096 x 4096
     // 6.7 vs 6.1 us; gate+up 21504 x 5376 30.8 vs 34.4 us, 8192 x 2048 9.9 vs 8.3 us).
-    const bool tc_size = (double)wbytes * nmat >= (nmat == 2 ? 32e6 : 15e6);
-    if (fmt == kFmtQ4 && tc_size && K % 256 == 0 && aligned && (uintptr_t)x % 16 == 0 &&
+    // Q4_K has no streaming kernel: it takes the tensor cores whenever the
+    // alignment allows, else the exact CUDA-core kernel.
+    const bool tc_size = fmt == kFmtQ4K || (double)wbytes * nmat >= (nmat == 2 ? 32e6 : 15e6);
+    if ((fmt == kFmtQ4 || fmt == kFmtQ4K) && tc_size && K % 256 == 0 && aligned && (uintptr_t)x % 16 == 0 &&
         qmv_tc_supported(nmat, N, K, di->sm_count)) {
         CUtensorMap tw[2];
         if (encode_q4_tile_map(&tw[0], w0, N, K) && (nmat == 1 || encode_q4_tile_map(&tw[1], w1, N, K))) {
-            cudaError_t e = launch_qmv_tc(nmat, 1, tw, x, xt == QBW_BF16, y, yt == QBW_BF16, (int)N, (int)K,
+            cudaError_t e = launch_qmv_tc(fmt, nmat, 1, tw, x, xt == QBW_BF16, y, yt == QBW_BF16, (int)N, (int)K,
                                           di->sm_count, di->fault, s);
             return e == cudaSuccess ? QBW_OK : QBW_ECUDA;
         }
     }
-    if (K % 256 == 0 && aligned) {
+    if (fmt != kFmtQ4K && K % 256 == 0 && aligned) {
         StreamPlan plan;
         if (plan_stream_cached(fmt, nmat, N, K, *di, &plan) &&
             encode_weight_map(&plan.p.tmap[0], w0, N, plan.p.row_bytes, fmt, plan.R) &&
@@ -452,6 +455,11 @@ qbw_status qmv_q4_0(const void* w, const void* x, qbw_dtype xt, void* y, qbw_dty
     return qmv_common(kFmtQ4, 1, w, nullptr, x, xt, y, yt, M, N, K, stream);
 }
 
+qbw_status qmv_q4_k(const void* w, const void* x, qbw_dtype xt, void* y, qbw_dtype yt, int64_t M, int64_t N,
+                    int64_t K, void* stream) {
+    return qmv_common(kFmtQ4K, 1, w, nullptr, x, xt, y, yt, M, N, K, stream);
+}
+
 qbw_status qmv_gateup_q4_0(const void* w_gate, const void* w_up, const void* x, qbw_dtype xt, void* out,
                            qbw_dtype ot, int64_t M, int64_t N, int64_t K, void* stream) {
     return qmv_common(kFmtQ4, 2, w_gate, w_up, x, xt, out, ot, M, N, K, stream);
@@ -481,8 +489,8 @@ qbw_status qmm_q4_0_smallM(const void* w, const void* X, qbw_dtype xt, void* Y, 
     if (q.exact && (uintptr_t)w % 16 == 0 && (uintptr_t)X % 16 == 0) {
         CUtensorMap tw[2];
         if (encode_q4_tile_map(&tw[0], w, N, K)) {
-            cudaError_t e = launch_qmv_tc(1, (int)M, tw, X, 1, Y, yt == QBW_BF16, (int)N, (int)K, di->sm_count,
-                                          di->fault, s);
+            cudaError_t e = launch_qmv_tc(kFmtQ4, 1, (int)M, tw, X, 1, Y, yt == QBW_BF16, (int)N, (int)K,
+                                          di->sm_count, di->fault, s);
             return e == cudaSuccess ? QBW_OK : QBW_ECUDA;
         }
     }
@@ -511,8 +519,9 @@ qbw_status qmm_q4_0_smallM(const void* w, const void* X, qbw_dtype xt, void* Y, 
 static qbw_status dequant_common(int fmt, const void* w, float* out, int64_t N, int64_t K, void* stream) {
     if (!w || !out) return QBW_EINVAL;
     if (N < 1 || K < 32 || K % 32 != 0 || K > (int64_t(1) << 24) || N > INT32_MAX) return QBW_ESHAPE;
+    if (fmt == kFmtQ4K && K % 256 != 0) return QBW_ESHAPE;
     if ((uintptr_t)out % 4) return QBW_EALIGN;
-    if (overlaps(out, (size_t)N * K * 4, w, (size_t)N * (K / 32) * block_bytes(fmt))) return QBW_EINVAL;
+    if (overlaps(out, (size_t)N * K * 4, w, (size_t)N * (size_t)weight_row_bytes(fmt, K))) return QBW_EINVAL;
     DeviceInfo* di = nullptr;
     qbw_status st = device_info(&di);
     if (st != QBW_OK) return st;
@@ -523,6 +532,10 @@ static qbw_status dequant_common(int fmt, const void* w, float* out, int64_t N, 
 
 qbw_status qdequant_q8_0(const void* w, float* out, int64_t N, int64_t K, void* stream) {
     return dequant_common(kFmtQ8, w, out, N, K, stream);
+}
+
+qbw_status qdequant_q4_k(const void* w, float* out, int64_t N, int64_t K, void* stream) {
+    return dequant_common(kFmtQ4K, w, out, N, K, stream);
 }
 
 qbw_status qdequant_q4_0(const void* w, float* out, int64_t N, int64_t K, void* stream) {

@@ -18,7 +18,13 @@ enum FaultCode : unsigned int {
     kFaultShareWaitTimeout = 4,  // a split tile's share from another CTA never arrived
 };
 
-enum : int { kFmtQ8 = 0, kFmtQ4 = 1 };
+enum : int { kFmtQ8 = 0, kFmtQ4 = 1, kFmtQ4K = 2 };
+
+// Bytes of one row of K weights: Q8_0 34 and Q4_0 18 per 32 weights; Q4_K
+// 144 per 256-weight super-block.
+constexpr int64_t weight_row_bytes(int fmt, int64_t K) {
+    return fmt == kFmtQ4K ? (K / 256) * 144 : (K / 32) * (fmt == kFmtQ4 ? 18 : 34);
+}
 
 // Launch parameters of the streaming M = 1 kernel (qmv_stream.cuh).
 // tmap[m] views weight matrix m as a 2-D array of 8-byte elements,

@@ -1,7 +1,7 @@
 // qmv_generic.cu -- the exact-but-plain kernels: the matrix-vector fallback for
 // shapes or alignments the streaming kernel does not take (K % 256 != 0, or a
-// weight pointer not 16-byte aligned), the whole-matrix dequantizer and the
-// token-table row gather.
+// weight pointer not 16-byte aligned) and for Q4_K off the tensor-core path,
+// the whole-matrix dequantizers and the token-table row gather.
 #include <cstdint>
 
 #include "qbw_device.cuh"
@@ -61,6 +61,91 @@ __global__ void __launch_bounds__(256) qmv_generic_kernel(const uint8_t* w0, con
         if (lane == 0) {
             if (y_bf16) store_out<__nv_bfloat16>(y, n, v);
             else store_out<float>(y, n, v);
+        }
+    }
+}
+
+// ---------------------------------------------------------------- Q4_K
+// A Q4_K super-block (GGUF block_q4_K, 144 bytes, 256 weights): fp16 d at
+// byte 0, fp16 dmin at byte 2, 12 scale bytes s[] at byte 4, 128 nibble bytes
+// at byte 16.  Sub-block j (32 weights) has a six-bit scale sc_j and min m_j:
+// for j < 4 the low six bits of s[j] and s[j + 4]; for j >= 4 the low and high
+// nibble of s[j + 4], with the top two bits taken from s[j - 4] (sc) and s[j]
+// (m).  Weight e = 64 i + l (chunk i) has code (l < 32 ? low : high) nibble of
+// byte 32 i + (l % 32).  w = d sc_j q - dmin m_j (jouleclaw-loader-gguf
+// BENCHMARKS, "Q4_K matmul -- scalar fused vs AMX-tiled").
+__device__ __forceinline__ void q4k_sub_scale(const uint8_t* s, int j, int& sc, int& m) {
+    if (j < 4) {
+        sc = s[j] & 63;
+        m = s[j + 4] & 63;
+    } else {
+        sc = (s[j + 4] & 15) | ((s[j - 4] >> 6) << 4);
+        m = (s[j + 4] >> 4) | ((s[j] >> 6) << 4);
+    }
+}
+
+__device__ __forceinline__ int q4k_code_at(const uint8_t* qs, int e) {
+    const uint32_t byte = qs[32 * (e >> 6) + (e & 31)];
+    return (e & 32) ? (int)(byte >> 4) : (int)(byte & 15u);
+}
+
+// One warp per output row; lane l takes super-blocks l, l + 32, ...  Per
+// sub-block the algebraic split: d sc_j * sum(q x) - dmin m_j * sum(x).
+__global__ void __launch_bounds__(256) qmv_q4k_generic_kernel(const uint8_t* w, const void* x, int x_bf16, void* y,
+                                                              int y_bf16, int64_t N, int64_t K) {
+    const int lane = threadIdx.x & 31;
+    const int64_t nb = K / 256;
+    const int64_t row_bytes = nb * 144;
+    const int64_t warps = (int64_t)gridDim.x * (blockDim.x >> 5);
+    for (int64_t n = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); n < N; n += warps) {
+        float acc = 0.f;
+        for (int64_t b = lane; b < nb; b += 32) {
+            const uint8_t* blk = w + n * row_bytes + b * 144;
+            const float d = half_bits_to_float((uint32_t)blk[0] | ((uint32_t)blk[1] << 8));
+            const float dmin = half_bits_to_float((uint32_t)blk[2] | ((uint32_t)blk[3] << 8));
+            for (int j = 0; j < 8; ++j) {
+                int sc, m;
+                q4k_sub_scale(blk + 4, j, sc, m);
+                float s1 = 0.f, s0 = 0.f;
+                for (int t = 0; t < 32; ++t) {
+                    const int e = 32 * j + t;
+                    const int64_t i = b * 256 + e;
+                    const float xv = x_bf16 ? load_act<__nv_bfloat16>(x, i) : load_act<float>(x, i);
+                    s1 = fmaf((float)q4k_code_at(blk + 16, e), xv, s1);
+                    s0 += xv;
+                }
+                acc = fmaf(d * (float)sc, s1, acc);
+                acc = fmaf(-dmin * (float)m, s0, acc);
+            }
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+        if (lane == 0) {
+            if (y_bf16) store_out<__nv_bfloat16>(y, n, acc);
+            else store_out<float>(y, n, acc);
+        }
+    }
+}
+
+// One thread per super-block: w = (d sc) q - dmin m.  d sc, (d sc) q and
+// dmin m are exact in fp32 (at most 21 significant bits), so the single
+// rounding of the difference gives the nearest fp32 to the exact weight.
+__global__ void __launch_bounds__(256) dequant_q4k_kernel(const uint8_t* w, float* out, int64_t N, int64_t K) {
+    const int64_t nb = K / 256;
+    const int64_t total = N * nb;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
+         i += (int64_t)gridDim.x * blockDim.x) {
+        const uint8_t* blk = w + i * 144;
+        const float d = half_bits_to_float((uint32_t)blk[0] | ((uint32_t)blk[1] << 8));
+        const float dmin = half_bits_to_float((uint32_t)blk[2] | ((uint32_t)blk[3] << 8));
+        const int64_t n = i / nb, b = i - n * nb;
+        float* o = out + n * K + b * 256;
+        for (int j = 0; j < 8; ++j) {
+            int sc, m;
+            q4k_sub_scale(blk + 4, j, sc, m);
+            const float ds = __fmul_rn(d, (float)sc), dm = __fmul_rn(dmin, (float)m);
+#pragma unroll 8
+            for (int t = 0; t < 32; ++t) o[32 * j + t] = __fsub_rn(__fmul_rn(ds, (float)q4k_code_at(blk + 16, 32 * j + t)), dm);
         }
     }
 }
@@ -172,7 +257,9 @@ cudaError_t launch_qmv_generic(int fmt, int nmat, const uint8_t* w0, const uint8
     const int threads = 256;
     const int64_t want = (N + 7) / 8;
     const int ctas = (int)(want < (int64_t)sm_count * 8 ? want : (int64_t)sm_count * 8);
-    if (fmt == kFmtQ8)
+    if (fmt == kFmtQ4K)
+        qmv_q4k_generic_kernel<<<ctas, threads, 0, stream>>>(w0, x, x_bf16, y, y_bf16, N, K);
+    else if (fmt == kFmtQ8)
         qmv_generic_kernel<kFmtQ8, 1><<<ctas, threads, 0, stream>>>(w0, w1, x, x_bf16, y, y_bf16, N, K);
     else if (nmat == 1)
         qmv_generic_kernel<kFmtQ4, 1><<<ctas, threads, 0, stream>>>(w0, w1, x, x_bf16, y, y_bf16, N, K);
@@ -184,10 +271,12 @@ cudaError_t launch_qmv_generic(int fmt, int nmat, const uint8_t* w0, const uint8
 cudaError_t launch_dequant(int fmt, const uint8_t* w, float* out, int64_t N, int64_t K, int sm_count,
                            cudaStream_t stream) {
     const int threads = 256;
-    const int64_t blocks = N * (K / 32);
+    const int64_t blocks = N * (K / (fmt == kFmtQ4K ? 256 : 32));
     const int64_t want = (blocks + threads - 1) / threads;
     const int ctas = (int)(want < (int64_t)sm_count * 16 ? want : (int64_t)sm_count * 16);
-    if (fmt == kFmtQ8)
+    if (fmt == kFmtQ4K)
+        dequant_q4k_kernel<<<ctas, threads, 0, stream>>>(w, out, N, K);
+    else if (fmt == kFmtQ8)
         dequant_kernel<kFmtQ8><<<ctas, threads, 0, stream>>>(w, out, N, K);
     else
         dequant_kernel<kFmtQ4><<<ctas, threads, 0, stream>>>(w, out, N, K);

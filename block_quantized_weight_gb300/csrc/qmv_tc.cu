@@ -76,6 +76,7 @@ constexpr uint32_t kRawStageBytes = kTileRows * 144;
 constexpr uint32_t kBBytes = kN * kGroupK * 2;   // 8 KB: 4 swizzle atoms of 16 rows x 128 B
 constexpr int kMaxLocalTiles = 8;
 constexpr uint32_t kBf16Minus136 = 0xC308C308u;
+constexpr uint32_t kBf16Minus128 = 0xC300C300u;
 
 constexpr uint32_t kOffB = kStages * kRawStageBytes;                          // 1024-aligned
 constexpr uint32_t kOffPart = kOffB + kSets * kBBytes;
@@ -153,11 +154,31 @@ __device__ __forceinline__ void codes_block(const uint32_t (&v)[36], uint32_t* c
     }
 }
 
-// Block pair P (blocks 2P, 2P + 1) of the group -> 32 columns
-template <int P>
+// Q4_0: block pair P (blocks 2P, 2P + 1) of the group -> 32 columns of exact
+// c - 8.  Q4_K: 64-weight chunk P of the super-block -> 32 columns of exact
+// codes c (0..15): its 32 nibble bytes (words 4 + 8P .. 11 + 8P) hold weights
+// 64P + l in the low nibbles and 64P + 32 + l in the high nibbles, so the
+// byte pair (l, l + 1) gives columns 16 * 0 + l / 2 (low) and 16 + l / 2
+// (high) of the chunk, in K order.
+template <int FMT, int P>
 __device__ __forceinline__ void codes_pair(const uint32_t (&v)[36], uint32_t (&col)[32]) {
-    codes_block<36 * P + 2>(v, col);
-    codes_block<36 * P + 20>(v, col + 16);
+    if constexpr (FMT == kFmtQ4) {
+        codes_block<36 * P + 2>(v, col);
+        codes_block<36 * P + 20>(v, col + 16);
+    } else {
+        const uint32_t m128 = kBf16Minus128;
+#pragma unroll
+        for (int wd = 0; wd < 8; ++wd) {
+            const uint32_t w = v[4 + 8 * P + wd];
+            uint32_t lo, hi;
+            nibble_pairs<0>(w, lo, hi);                     // bytes 4wd, 4wd + 1
+            asm("add.rn.bf16x2 %0, %1, %2;" : "=r"(col[2 * wd]) : "r"(lo), "r"(m128));
+            asm("add.rn.bf16x2 %0, %1, %2;" : "=r"(col[16 + 2 * wd]) : "r"(hi), "r"(m128));
+            nibble_pairs<2>(w, lo, hi);                     // bytes 4wd + 2, 4wd + 3
+            asm("add.rn.bf16x2 %0, %1, %2;" : "=r"(col[2 * wd + 1]) : "r"(lo), "r"(m128));
+            asm("add.rn.bf16x2 %0, %1, %2;" : "=r"(col[16 + 2 * wd + 1]) : "r"(hi), "r"(m128));
+        }
+    }
 }
 
 // fp16 scales of blocks 2P (low half) and 2P + 1 (high half) of the group:
@@ -175,6 +196,32 @@ __device__ __forceinline__ float2 half2_to_float2(uint32_t h) {
         : "=f"(f.x), "=f"(f.y)
         : "r"(h));
     return f;
+}
+
+// Q4_K: the sub-block sums of one unit, r0 = sum_j d sc_j (D[2j] + D[2j + 1])
+// - dmin m_j sx_j, j = 0..7 in order: dd[] holds the super-block's first 16
+// bytes (fp16 d and dmin, then the 12 six-bit scale bytes), sx the lane's
+// sub-block sum of x (lanes 4j .. 4j + 3 hold sub-block j's).
+__device__ __forceinline__ float unit_dot_q4k(const uint32_t (&dv)[16], const uint32_t (&dd)[4], float sx) {
+    const float2 dm = half2_to_float2(dd[0]);
+    const uint32_t s03 = dd[1], s47 = dd[2], s8b = dd[3];       // scale bytes 0..3, 4..7, 8..11
+    float r = 0.f;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        uint32_t sc, m;
+        if (j < 4) {
+            sc = (s03 >> (8 * j)) & 63u;
+            m = (s47 >> (8 * j)) & 63u;
+        } else {
+            const uint32_t lo = (s8b >> (8 * (j - 4))) & 0xFFu;
+            sc = (lo & 15u) | (((s03 >> (8 * (j - 4) + 6)) & 3u) << 4);
+            m = (lo >> 4) | (((s47 >> (8 * (j - 4) + 6)) & 3u) << 4);
+        }
+        const float sxj = __shfl_sync(0xffffffffu, sx, 4 * j);
+        r = fmaf(dm.x * (float)sc, __uint_as_float(dv[2 * j]) + __uint_as_float(dv[2 * j + 1]), r);
+        r = fmaf(-dm.y * (float)m, sxj, r);
+    }
+    return r;
 }
 
 // One token (NTOK = 1): r0 = sum_j d_j (D[2j] + D[2j + 1]), the x_hi and x_lo
@@ -225,10 +272,11 @@ __device__ __forceinline__ uint32_t b_chunk(int a, int n, int c) {
 // NMAT = 1 and bf16 activations): Y[m] = W X[m] for two token rows, which take
 // the two B columns of each block that x_hi and x_lo take for one token.
 // Each row keeps NCH = NMAT * NTOK sums (channels).
-template <int NMAT, int NTOK>
-__global__ void __launch_bounds__(kThreads, 1) qmv_q4_0_tc_kernel(const __grid_constant__ QtcParams p) {
+template <int FMT, int NMAT, int NTOK>
+__device__ __forceinline__ void qmv_tc_body(const QtcParams& p) {
     constexpr int NCH = NMAT * NTOK;
     static_assert(NCH <= 2, "at most two sums per row");
+    static_assert(FMT == kFmtQ4 || (NMAT == 1 && NTOK == 1), "Q4_K: one matrix, one token");
     extern __shared__ __align__(1024) uint8_t smem[];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int ctas = (int)gridDim.x, cta = (int)blockIdx.x;
@@ -346,11 +394,19 @@ __global__ void __launch_bounds__(kThreads, 1) qmv_q4_0_tc_kernel(const __grid_c
         const uint32_t d_taddr = tmem + lanes + kDCol + 32u * (uint32_t)set;   // + 16 (k % 2)
         const uint32_t raw_row = (uint32_t)(32 * q + lane) * 144u;
         const uint32_t bbuf = sbase + kOffB + (uint32_t)set * kBBytes;
-        // B chunk of this lane (lanes 0..7): elements 64q + 8 lane .. + 7 of
-        // the group, in block j = 2q + lane / 4, rows 2j (x_hi) and 2j + 1 (x_lo)
-        const int bj = 2 * q + (lane >> 2);
-        const uint32_t b_hi = bbuf + b_chunk(q, 2 * bj, lane & 7);
-        const uint32_t b_lo = bbuf + b_chunk(q, 2 * bj + 1, lane & 7);
+        // The lane's 8-element slot xl of the group's activations: Q4_0, lanes
+        // 0..7 load slots 8q .. 8q + 7 and write them into B; Q4_K, every lane
+        // loads slot `lane` (the sub-block sums need all 256) and the lanes of
+        // slots 8q .. 8q + 7 write them.  Slot xl is elements 8 xl .. 8 xl + 7 of
+        // the group: swizzle atom xl / 8, block j = xl / 4, B rows 2j (x_hi)
+        // and 2j + 1 (x_lo), in K-half xl / 16.
+        const int xl = (FMT == kFmtQ4K) ? lane : 8 * q + lane;
+        const bool loads_x = (FMT == kFmtQ4K) || lane < 8;
+        const bool bwriter = (FMT == kFmtQ4K) ? ((lane >> 3) == q) : (lane < 8);
+        const int bj = xl >> 2;
+        const uint32_t b_hi = bbuf + b_chunk(xl >> 3, 2 * bj, xl & 7);
+        const uint32_t b_lo = bbuf + b_chunk(xl >> 3, 2 * bj + 1, xl & 7);
+        const int bhalf = xl >> 4;
         const int row = 32 * q + lane;
         bool counted = !contrib0;
         // after the three sets' shares of the first tile are in part[][0][], the
@@ -400,14 +456,15 @@ __global__ void __launch_bounds__(kThreads, 1) qmv_q4_0_tc_kernel(const __grid_c
             }
         };
         uint32_t pend_dd[4] = {0u, 0u, 0u, 0u};
+        float pend_sx = 0.f;     // Q4_K: the previous unit's sub-block sum of this lane's group of 4
         int k = 0;
         for (int i = set; i < n; i += kSets, ++k) {
             const int u = u0 + i, ug = u / NMAT, mat = u - ug * NMAT, t = ug / G, g = ug - t * G;
             const int s = i % kStages;
             // this lane's eight activations of the group, loaded before the waits
             uint4 xr0 = make_uint4(0u, 0u, 0u, 0u), xr1 = xr0;
-            if (lane < 8) {
-                const int e = g * kGroupK + 64 * q + 8 * lane;
+            if (loads_x) {
+                const int e = g * kGroupK + 8 * xl;
                 if (NTOK == 2) {
                     xr0 = __ldg(reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p.x) + e));
                     xr1 = __ldg(reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p.x) + p.K + e));
@@ -438,12 +495,30 @@ __global__ void __launch_bounds__(kThreads, 1) qmv_q4_0_tc_kernel(const __grid_c
             if (lane == 0) mbar_arrive(empty_bar(bar0, s));     // raw rows of stage s read
             uint32_t dd[4];
 #pragma unroll
-            for (int P = 0; P < 4; ++P) dd[P] = scale_pair(v, P);
+            for (int P = 0; P < 4; ++P) dd[P] = (FMT == kFmtQ4K) ? v[P] : scale_pair(v, P);
             uint32_t c0[32], c1[32];
             // B chunk of this lane (lanes 0..7): x_hi and x_lo as bf16, written
             // in the half (q / 2) the chunk belongs to
             uint4 bhi = make_uint4(0u, 0u, 0u, 0u), blo = bhi;
-            if (lane < 8) {
+            float cur_sx = 0.f;
+            if (loads_x) {
+                if (FMT == kFmtQ4K) {
+                    float f[8];
+                    if (p.x_bf16) {
+                        const uint32_t w4[4] = {xr0.x, xr0.y, xr0.z, xr0.w};
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            f[2 * e] = bf16_lo_to_float(w4[e]);
+                            f[2 * e + 1] = bf16_hi_to_float(w4[e]);
+                        }
+                    } else {
+                        f[0] = __uint_as_float(xr0.x); f[1] = __uint_as_float(xr0.y);
+                        f[2] = __uint_as_float(xr0.z); f[3] = __uint_as_float(xr0.w);
+                        f[4] = __uint_as_float(xr1.x); f[5] = __uint_as_float(xr1.y);
+                        f[6] = __uint_as_float(xr1.z); f[7] = __uint_as_float(xr1.w);
+                    }
+                    cur_sx = ((f[0] + f[1]) + (f[2] + f[3])) + ((f[4] + f[5]) + (f[6] + f[7]));
+                }
                 if (NTOK == 2) {
                     bhi = xr0;    // token 0 in the x_hi column, token 1 in the x_lo column
                     blo = xr1;
@@ -463,9 +538,14 @@ __global__ void __launch_bounds__(kThreads, 1) qmv_q4_0_tc_kernel(const __grid_c
                     blo = make_uint4(l[0], l[1], l[2], l[3]);
                 }
             }
+            if constexpr (FMT == kFmtQ4K) {
+                // sub-block sums: lanes 4j .. 4j + 3 hold sub-block j's 32 activations
+                cur_sx += __shfl_xor_sync(0xffffffffu, cur_sx, 1);
+                cur_sx += __shfl_xor_sync(0xffffffffu, cur_sx, 2);
+            }
             const uint32_t prev = (uint32_t)(k - 1) & 1u;     // completion parity of the previous unit
             // ---- half 0: K 0..127 (block pairs 0, 1; B atoms 0, 1 written by warps 0, 1)
-            codes_pair<0>(v, c0);
+            codes_pair<FMT, 0>(v, c0);
             if (k > 0) {
                 const bool free = mbar_wait_bounded(aempty_bar(bar0, set, 0), prev, p.fault, kFaultMmaWaitTimeout);
                 if (!__all_sync(0xffffffffu, free)) {
@@ -474,13 +554,13 @@ __global__ void __launch_bounds__(kThreads, 1) qmv_q4_0_tc_kernel(const __grid_c
                 }
                 tc_fence_after();
             }
-            if (q < 2 && lane < 8) {
+            if (bwriter && bhalf == 0) {
                 sts128(b_hi, bhi);
                 sts128(b_lo, blo);
                 fence_proxy_async_smem();     // B visible to the tensor core
             }
             tmem_st32(a_taddr, c0);
-            codes_pair<1>(v, c1);
+            codes_pair<FMT, 1>(v, c1);
             tmem_wait_st();
             tmem_st32(a_taddr + 32u, c1);
             tmem_wait_st();
@@ -488,7 +568,7 @@ __global__ void __launch_bounds__(kThreads, 1) qmv_q4_0_tc_kernel(const __grid_c
             __syncwarp();
             if (lane == 0) mbar_arrive(afull_bar(bar0, set, 0));
             // ---- half 1: K 128..255 (block pairs 2, 3; B atoms 2, 3 written by warps 2, 3)
-            codes_pair<2>(v, c0);
+            codes_pair<FMT, 2>(v, c0);
             if (k > 0) {
                 const bool free = mbar_wait_bounded(aempty_bar(bar0, set, 1), prev, p.fault, kFaultMmaWaitTimeout);
                 if (!__all_sync(0xffffffffu, free)) {
@@ -497,13 +577,13 @@ __global__ void __launch_bounds__(kThreads, 1) qmv_q4_0_tc_kernel(const __grid_c
                 }
                 tc_fence_after();
             }
-            if (q >= 2 && lane < 8) {
+            if (bwriter && bhalf == 1) {
                 sts128(b_hi, bhi);
                 sts128(b_lo, blo);
                 fence_proxy_async_smem();
             }
             tmem_st32(a_taddr + 64u, c0);
-            codes_pair<3>(v, c1);
+            codes_pair<FMT, 3>(v, c1);
             tmem_wait_st();
             tmem_st32(a_taddr + 96u, c1);
             tmem_wait_st();
@@ -516,12 +596,14 @@ __global__ void __launch_bounds__(kThreads, 1) qmv_q4_0_tc_kernel(const __grid_c
                 uint32_t dv[16];
                 tmem_ld16(d_taddr + 16u * prev, dv);
                 tmem_wait_ld();
-                float r0, r1;
-                unit_dot<NTOK>(dv, pend_dd, r0, r1);
+                float r0, r1 = 0.f;
+                if constexpr (FMT == kFmtQ4K) r0 = unit_dot_q4k(dv, pend_dd, pend_sx);
+                else unit_dot<NTOK>(dv, pend_dd, r0, r1);
                 add_unit(r0, r1);
             }
 #pragma unroll
             for (int P = 0; P < 4; ++P) pend_dd[P] = dd[P];
+            pend_sx = cur_sx;
             pend_tile = t;
             pend_mat = mat;
         }
@@ -534,8 +616,9 @@ __global__ void __launch_bounds__(kThreads, 1) qmv_q4_0_tc_kernel(const __grid_c
                 uint32_t dv[16];
                 tmem_ld16(d_taddr + 16u * last_par, dv);
                 tmem_wait_ld();
-                float r0, r1;
-                unit_dot<NTOK>(dv, pend_dd, r0, r1);
+                float r0, r1 = 0.f;
+                if constexpr (FMT == kFmtQ4K) r0 = unit_dot_q4k(dv, pend_dd, pend_sx);
+                else unit_dot<NTOK>(dv, pend_dd, r0, r1);
                 add_unit(r0, r1);
             }
         }
@@ -610,6 +693,15 @@ __global__ void __launch_bounds__(kThreads, 1) qmv_q4_0_tc_kernel(const __grid_c
     }
 }
 
+template <int NMAT, int NTOK>
+__global__ void __launch_bounds__(kThreads, 1) qmv_q4_0_tc_kernel(const __grid_constant__ QtcParams p) {
+    qmv_tc_body<kFmtQ4, NMAT, NTOK>(p);
+}
+
+__global__ void __launch_bounds__(kThreads, 1) qmv_q4_k_tc_kernel(const __grid_constant__ QtcParams p) {
+    qmv_tc_body<kFmtQ4K, 1, 1>(p);
+}
+
 }  // namespace
 
 // The tensor-core M = 1 path takes K % 256 == 0, at most kQtcMaxTiles tiles
@@ -630,12 +722,14 @@ bool qmv_tc_supported(int nmat, int64_t N, int64_t K, int sm_count) {
 
 size_t qmv_tc_smem_bytes() { return kSmemBytes; }
 
-// nmat = 2: gate + up (one token).  ntok = 2 (nmat = 1, bf16 X of two rows
-// of K, Y of two rows of N): two tokens.
-cudaError_t launch_qmv_tc(int nmat, int ntok, const CUtensorMap* tmap_w, const void* x, int x_bf16, void* y,
-                          int y_bf16, int N, int K, int sm_count, unsigned int* fault, cudaStream_t stream) {
+// fmt: kFmtQ4 or kFmtQ4K (one matrix, one token).  nmat = 2: gate + up (one
+// token).  ntok = 2 (nmat = 1, bf16 X of two rows of K, Y of two rows of N):
+// two tokens.
+cudaError_t launch_qmv_tc(int fmt, int nmat, int ntok, const CUtensorMap* tmap_w, const void* x, int x_bf16,
+                          void* y, int y_bf16, int N, int K, int sm_count, unsigned int* fault, cudaStream_t stream) {
     static std::atomic<unsigned int> calls{0};
     if (nmat * ntok > 2 || (ntok == 2 && !x_bf16)) return cudaErrorInvalidValue;
+    if (fmt == kFmtQ4K && nmat * ntok != 1) return cudaErrorInvalidValue;
     QtcParams p;
     p.tmap_w[0] = tmap_w[0];
     p.tmap_w[1] = tmap_w[nmat == 2 ? 1 : 0];
@@ -651,12 +745,14 @@ cudaError_t launch_qmv_tc(int nmat, int ntok, const CUtensorMap* tmap_w, const v
     p.x_bf16 = x_bf16;
     p.y_bf16 = y_bf16;
     const int ctas = p.units < sm_count ? p.units : sm_count;
-    auto kernel = nmat == 2 ? qmv_q4_0_tc_kernel<2, 1> : (ntok == 2 ? qmv_q4_0_tc_kernel<1, 2> : qmv_q4_0_tc_kernel<1, 1>);
+    auto kernel = fmt == kFmtQ4K ? qmv_q4_k_tc_kernel
+                  : (nmat == 2 ? qmv_q4_0_tc_kernel<2, 1>
+                               : (ntok == 2 ? qmv_q4_0_tc_kernel<1, 2> : qmv_q4_0_tc_kernel<1, 1>));
     static thread_local int prepared_device = -1;
     int dev = 0;
     cudaGetDevice(&dev);
     if (prepared_device != dev) {
-        for (auto f : {qmv_q4_0_tc_kernel<1, 1>, qmv_q4_0_tc_kernel<2, 1>, qmv_q4_0_tc_kernel<1, 2>}) {
+        for (auto f : {qmv_q4_0_tc_kernel<1, 1>, qmv_q4_0_tc_kernel<2, 1>, qmv_q4_0_tc_kernel<1, 2>, qmv_q4_k_tc_kernel}) {
             cudaError_t e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
             if (e != cudaSuccess) return e;
         }

@@ -210,6 +210,38 @@ qbw_status qdequant_q8_0(const void *w, float *out, int64_t N, int64_t K, void *
 qbw_status qdequant_q4_0(const void *w, float *out, int64_t N, int64_t K, void *stream);
 
 /*
+ * qmv_q4_k -- y = W x for a Q4_K weight matrix, one token (M == 1).
+ *
+ * Q4_K, the K-quant the pages benchmark beside Q8_0 (jouleclaw-loader-gguf
+ * BENCHMARKS, "Q4_K matmul -- scalar fused vs AMX-tiled" and its NEON
+ * follow-up): super-blocks of 256 weights in 144 bytes, the GGUF block_q4_K
+ * record -- fp16 d, fp16 dmin, 12 bytes of six-bit sub-block scales sc_j and
+ * mins m_j (j = 0..7, 32 weights each), 128 bytes of 4-bit codes q (each
+ * 64-weight chunk keeps its first 32 codes in the low nibbles of its 32
+ * bytes and the rest in the high nibbles).  w = d sc_j q - dmin m_j.  Each
+ * sub-block is summed by the pages' algebraic split,
+ * d sc_j * sum(q x) - dmin m_j * sum(x).
+ *
+ *   w : N rows of K/256 super-blocks (row stride K/256 * 144 bytes)
+ *   x, y, xt, yt, M, N as for qmv_q4_0;  K % 256 == 0 (else QBW_ESHAPE)
+ *
+ * Fast path: w and x 16-byte aligned (tcgen05 tensor cores, exact integer
+ * codes); otherwise an exact CUDA-core kernel.
+ */
+qbw_status qmv_q4_k(const void *w, const void *x, qbw_dtype xt, void *y, qbw_dtype yt,
+                    int64_t M, int64_t N, int64_t K, void *stream);
+
+/*
+ * qdequant_q4_k -- expand a Q4_K matrix to fp32: out[n*K + k] = w[n, k], the
+ * nearest fp32 to the exact d sc_j q - dmin m_j (d sc_j q and dmin m_j are
+ * exact in fp32; their difference is rounded once).  For testing.
+ *
+ *   w : N rows of K/256 super-blocks, any alignment;  out : N*K floats, 4-byte
+ *   aligned;  K % 256 == 0 (else QBW_ESHAPE)
+ */
+qbw_status qdequant_q4_k(const void *w, float *out, int64_t N, int64_t K, void *stream);
+
+/*
  * qembed_q8_0 -- token-table lookup: out[i, :] = W[ids[i], :], dequantized.
  *
  * The embedding side of the Q8_0 token table that the decode loop reads once

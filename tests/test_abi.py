@@ -31,7 +31,8 @@ def declared_functions():
 def test_header_declares_the_entry_points():
     names = declared_functions()
     for n in ("qmv_q8_0", "qmv_q4_0", "qmv_gateup_q4_0", "qmm_q4_0_smallM", "qmm_q4_0_smallM_workspace_bytes",
-              "qdequant_q8_0", "qdequant_q4_0", "qbw_status_str", "qbw_version", "qbw_fault_read"):
+              "qdequant_q8_0", "qdequant_q4_0", "qmv_q4_k", "qdequant_q4_k", "qbw_status_str", "qbw_version",
+              "qbw_fault_read"):
         assert n in names
 
 
@@ -69,7 +70,7 @@ def qmv(lib, name, w=ADDR, x=ADDR + (1 << 30), xt=F32, y=ADDR + (2 << 30), yt=F3
     return getattr(lib, name)(P(w) if w else None, P(x) if x else None, xt, P(y) if y else None, yt, M, N, K, None)
 
 
-@pytest.mark.parametrize("name", ["qmv_q8_0", "qmv_q4_0"])
+@pytest.mark.parametrize("name", ["qmv_q8_0", "qmv_q4_0", "qmv_q4_k"])
 def test_qmv_validation(lib, name):
     assert qmv(lib, name, w=0) == 1
     assert qmv(lib, name, x=0) == 1
@@ -88,6 +89,18 @@ def test_qmv_validation(lib, name):
     # output overlapping the activations or the weights
     assert qmv(lib, name, y=ADDR + (1 << 30) + 64) == 1
     assert qmv(lib, name, y=ADDR + 16) == 1
+
+
+def test_q4k_needs_whole_super_blocks(lib):
+    # Q4_K super-blocks hold 256 weights: K = 288 is a whole number of 32-weight
+    # blocks but not of super-blocks
+    assert qmv(lib, "qmv_q4_k", K=288) == 2
+    assert qmv(lib, "qmv_q4_k", K=512, y=ADDR + 16 * 144 - 8) == 1      # y overlaps the 16 x 512 weights
+    f = lib.qdequant_q4_k
+    assert f(None, P(ADDR + (1 << 30)), 4, 256, None) == 1
+    assert f(P(ADDR), P(ADDR + (1 << 30)), 4, 288, None) == 2
+    assert f(P(ADDR), P(ADDR + (1 << 30) + 2), 4, 256, None) == 4
+    assert f(P(ADDR), P(ADDR + 8), 4, 256, None) == 1
 
 
 def test_gateup_validation(lib):
