@@ -1,5 +1,10 @@
-// qmv_tc.cu -- the M = 1 Q4_0 matrix-vector product y = W x on the fifth-
-// generation tensor cores (tcgen05), for K a multiple of 256.
+// qmv_tc.cu -- the M = 1 (and two-token) Q4_0 matrix-vector product y = W x,
+// the fused Q4_0 gate+up, and the Q4_K product, on the fifth-generation tensor
+// cores (tcgen05), for K a multiple of 256.  A Q4_K super-block (256 weights,
+// 144 bytes) is exactly one unit's row segment; its codes enter A exactly
+// (0..15), and the read-back applies d sc_j to each sub-block's dot product
+// and subtracts dmin m_j times the sub-block's activation sum (the algebraic
+// split of jouleclaw-loader-gguf BENCHMARKS, Q4_K NEON kernel).
 //
 // Why tensor cores for one token: on CUDA cores every weight costs a code
 // extraction, an exact conversion to fp32 and a multiply-add, about 2.1
