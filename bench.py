@@ -16,7 +16,8 @@ bytes / time), tokens/s, the end-to-end rate with the token's activation
 copied in from pinned host memory and the result copied back every step, the
 roofline of the dominant kernel, SM clocks sampled during the timed region,
 the CPU oracle as a baseline, and supplementary per-kernel numbers for the
-single-matrix workloads (2048x2048 Q8_0, 21504x5376 Q4_0, gate+up, small-M).
+single-matrix workloads (2048x2048 Q8_0, 21504x5376 Q4_0 and Q4_K, gate+up,
+small-M, batched decode, the Q8_0 token table).
 
 ``--impl reference`` times the CPU oracle instead (on a bounded sample of the
 same workload per step) and prints the same line with ``"impl": "reference"``.
@@ -597,6 +598,13 @@ def profile_case(args):
         y = torch.empty(N, device=dev)
         call = lambda i: qbw.qmv_q4_0(ws[i % copies], x, y, 1, N, K)
         nbytes = ws[0].numel() + 4 * K + 4 * N
+    elif name == "q4_k":
+        N, K = 21504, 5376
+        ws = [torch.from_numpy(synth.q4_k_weights(N, K, seed=1)).to(dev) for _ in range(copies)]
+        x = torch.from_numpy(synth.activations(K, seed=1)).to(dev)
+        y = torch.empty(N, device=dev)
+        call = lambda i: qbw.qmv_q4_k(ws[i % copies], x, y, 1, N, K)
+        nbytes = ws[0].numel() + 4 * K + 4 * N
     elif name == "gateup":
         N, K = 21504, 5376
         wg = [torch.from_numpy(synth.q4_0_weights(N, K, seed=2, stream=0)).to(dev) for _ in range(2)]
@@ -691,7 +699,7 @@ def main():
     ap.add_argument("--no-kernels", action="store_true", help="skip the single-matrix supplementary numbers")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
-    ap.add_argument("--profile", choices=["q8_0", "q4_0", "gateup", "qmm", "sweep"],
+    ap.add_argument("--profile", choices=["q8_0", "q4_0", "q4_k", "gateup", "qmm", "sweep"],
                     help="run only one small case (for profiler captures): a single-matrix workload, or the "
                          "sweep's launches over 6 layers")
     args = ap.parse_args()

@@ -38,8 +38,9 @@
 //
 // Warp roles (16 warps): warps 0..11 are three sets of four dequantizing
 // warps; set s takes the CTA's units s, s + 3, ...; warp 4s + q owns rows
-// 32q .. 32q + 31 (its TMEM lane quarter) and, lanes 0..7, one eighth of the
-// group's B operand.  Warp 12 lane 0 issues the TMA copies of the raw rows
+// 32q .. 32q + 31 (its TMEM lane quarter) and one eighth of the group's B
+// operand (Q4_0: lanes 0..7; Q4_K: lanes 8q .. 8q + 7, while every lane loads
+// activations for the sub-block sums).  Warp 12 lane 0 issues the TMA copies of the raw rows
 // (128 rows x 144 bytes per unit) into a 6-stage ring.  Warp 13 + s lane 0
 // issues set s's MMAs (M = 128, N = 16, K = 16; 16 per unit) into set s's
 // accumulator.  Each set's rows read D back one unit later, while the next
@@ -502,8 +503,8 @@ __device__ __forceinline__ void qmv_tc_body(const QtcParams& p) {
 #pragma unroll
             for (int P = 0; P < 4; ++P) dd[P] = (FMT == kFmtQ4K) ? v[P] : scale_pair(v, P);
             uint32_t c0[32], c1[32];
-            // B chunk of this lane (lanes 0..7): x_hi and x_lo as bf16, written
-            // in the half (q / 2) the chunk belongs to
+            // B chunk of a B-writing lane: x_hi and x_lo as bf16, written in the
+            // K-half its slot belongs to
             uint4 bhi = make_uint4(0u, 0u, 0u, 0u), blo = bhi;
             float cur_sx = 0.f;
             if (loads_x) {
@@ -524,7 +525,9 @@ __device__ __forceinline__ void qmv_tc_body(const QtcParams& p) {
                     }
                     cur_sx = ((f[0] + f[1]) + (f[2] + f[3])) + ((f[4] + f[5]) + (f[6] + f[7]));
                 }
-                if (NTOK == 2) {
+                if (!bwriter) {
+                    // Q4_K lanes outside warp q's B slots: only the sum above
+                } else if (NTOK == 2) {
                     bhi = xr0;    // token 0 in the x_hi column, token 1 in the x_lo column
                     blo = xr1;
                 } else if (p.x_bf16) {
