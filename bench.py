@@ -82,6 +82,23 @@ def dist_env():
     return ws, rank, local
 
 
+def max_over_ranks(torch, ms: float, ws: int, device) -> float:
+    """The slowest replica's time: with N > 1 ranks the whole job is done only
+    when every rank is (all-reduce MAX over the process group)."""
+    if ws == 1:
+        return ms
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_rates(step_bytes: int, steps: int, ws: int, ms: float):
+    """Whole-job GB/s and tokens/s: every rank streams `steps` full steps
+    (weak scaling), all within the slowest rank's `ms`."""
+    sec = ms * 1e-3
+    return step_bytes * steps * ws / sec / 1e9, steps * ws / sec
+
+
 def load_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -487,10 +504,7 @@ def gpu_arm(args):
     t_start = time.time()
     ms = time_graph(torch, graph, args.steps, stream)
     t_end = time.time()
-    if ws > 1:
-        t = torch.tensor([ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(torch, ms, ws, dev)
     assert qbw.fault_read(clear=True, stream=stream) == 0, "a kernel recorded a fault"
 
     # end to end: the token's activation in from pinned host memory, the
@@ -513,8 +527,7 @@ def gpu_arm(args):
 
     wb, ab = sweep_bytes_per_layer()
     step_bytes = LAYERS * (wb + ab)
-    value = step_bytes * args.steps * ws / (ms * 1e-3) / 1e9
-    tok_s = args.steps * ws / (ms * 1e-3)
+    value, tok_s = job_rates(step_bytes, args.steps, ws, ms)
     e2e_value = step_bytes * e2e_steps * ws / e2e_s / 1e9
 
     dom = max(per_kernel, key=lambda k: per_kernel[k]["ms"])
