@@ -18,7 +18,7 @@ import threading
 __all__ = [
     "QbwError", "load", "lib_path",
     "qmv_q8_0", "qmv_q4_0", "qmv_gateup_q4_0", "qmm_q4_0_smallM", "qmm_q4_0_smallM_workspace_bytes",
-    "qmm_q4_0_smallM_noalloc", "NOALLOC_SCRATCH_BYTES", "qembed_q8_0", "qdequant_q8_0", "qdequant_q4_0", "qmv_q4_k", "qdequant_q4_k", "fault_read", "status_str", "version",
+    "qmm_q4_0_smallM_noalloc", "NOALLOC_SCRATCH_BYTES", "qembed_q8_0", "qdequant_q8_0", "qdequant_q4_0", "qmv_q4_k", "qdequant_q4_k", "selftest_wait", "fault_read", "status_str", "version",
     "F32", "BF16",
 ]
 
@@ -80,6 +80,8 @@ def _declare(L):
         getattr(L, name).argtypes = [P, P, i64, i64, P]
     L.qbw_fault_read.restype = i32
     L.qbw_fault_read.argtypes = [ctypes.POINTER(ctypes.c_uint32), i32, P]
+    L.qbw_selftest_wait.restype = i32
+    L.qbw_selftest_wait.argtypes = [i32, ctypes.c_uint32, P]
 
 
 def status_str(status: int) -> str:
@@ -199,6 +201,12 @@ def qdequant_q4_k(w, out, N: int, K: int, stream=None):
     L = load()
     _check(L.qdequant_q4_k(_ptr(w), _ptr(out), N, K, _stream(stream)), "qdequant_q4_k")
     return out
+
+
+def selftest_wait(which: int, limit_us: int, stream=None):
+    """Run a bounded wait that nothing completes (test-only; see qbw_selftest_wait)."""
+    L = load()
+    _check(L.qbw_selftest_wait(which, limit_us, _stream(stream)), "qbw_selftest_wait")
 
 
 def fault_read(clear: bool = True, stream=None) -> int:

@@ -28,6 +28,7 @@ cudaError_t launch_qmm_tc(const CUtensorMap& tmap_w, const CUtensorMap& tmap_x, 
                           unsigned int* counters, unsigned int* fault, int M, int N, int K, int splits,
                           int cluster, cudaStream_t stream);
 int qmm_tc_max_active_clusters(int nt, int cluster);
+cudaError_t launch_selftest_wait(int which, uint64_t limit_ns, unsigned int* fault, cudaStream_t stream);
 bool qmv_tc_supported(int nmat, int64_t N, int64_t K, int sm_count);
 cudaError_t launch_qmv_tc(int fmt, int nmat, int ntok, const CUtensorMap* tmap_w, const void* x, int x_bf16,
                           void* y, int y_bf16, int N, int K, int sm_count, unsigned int* fault, cudaStream_t stream);
@@ -532,6 +533,16 @@ static qbw_status dequant_common(int fmt, const void* w, float* out, int64_t N, 
 
 qbw_status qdequant_q8_0(const void* w, float* out, int64_t N, int64_t K, void* stream) {
     return dequant_common(kFmtQ8, w, out, N, K, stream);
+}
+
+qbw_status qbw_selftest_wait(int which, uint32_t limit_us, void* stream) {
+    if (which < 0 || which > 1 || limit_us < 1 || limit_us > 2000000) return QBW_EINVAL;
+    DeviceInfo* di = nullptr;
+    qbw_status st = device_info(&di);
+    if (st != QBW_OK) return st;
+    cudaError_t e = launch_selftest_wait(which, (uint64_t)limit_us * 1000ull, di->fault,
+                                         static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? QBW_OK : QBW_ECUDA;
 }
 
 qbw_status qdequant_q4_k(const void* w, float* out, int64_t N, int64_t K, void* stream) {

@@ -89,19 +89,39 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 }
 
 // Wait for phase `parity` of the barrier to complete, giving up after
-// kWaitLimitNs.  Returns false (and records `code`) on timeout.
+// limit_ns (kWaitLimitNs by default).  Returns false (and records `code`) on
+// timeout.
 __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity, unsigned int* fault,
-                                                  unsigned int code) {
+                                                  unsigned int code, uint64_t limit_ns = kWaitLimitNs) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer_ns();
     uint32_t spins = 0;
     while (!mbar_try_wait(bar, parity)) {
-        if ((++spins & 255u) == 0u && globaltimer_ns() - t0 > kWaitLimitNs) {
+        if ((++spins & 255u) == 0u && globaltimer_ns() - t0 > limit_ns) {
             record_fault(fault, code);
             return false;
         }
     }
     return true;
+}
+
+// Wait until the 64-bit word at p carries a nonzero tag (its upper half),
+// reading it with relaxed gpu-scope loads, giving up after limit_ns.  Returns
+// the last word read; on timeout records `code` (the word's tag is then 0).
+__device__ __forceinline__ unsigned long long wait_tagged_u64(const unsigned long long* p, unsigned int* fault,
+                                                              unsigned int code, uint64_t limit_ns = kWaitLimitNs) {
+    unsigned long long w;
+    asm volatile("ld.relaxed.gpu.global.b64 %0, [%1];" : "=l"(w) : "l"(p) : "memory");
+    if (w >> 32) return w;
+    const uint64_t t0 = globaltimer_ns();
+    for (;;) {
+        asm volatile("ld.relaxed.gpu.global.b64 %0, [%1];" : "=l"(w) : "l"(p) : "memory");
+        if (w >> 32) return w;
+        if (globaltimer_ns() - t0 > limit_ns) {
+            record_fault(fault, code);
+            return w;
+        }
+    }
 }
 
 // ------------------------------------------------------------------ bulk copy

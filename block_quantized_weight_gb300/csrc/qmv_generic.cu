@@ -243,6 +243,31 @@ __global__ void __launch_bounds__(256) qmm_generic_kernel(const uint8_t* w, cons
 
 }  // namespace
 
+// Self-test of the bounded waits: one thread waits, with a short limit, on
+// something nothing will complete -- which = 0: phase 0 of a fresh mbarrier
+// (the wait every pipeline stage uses; fault code 1), which = 1: the tag of a
+// global word that stays 0 (the split-tile share wait; fault code 4).  The
+// wait runs out, records its code in the fault word and the kernel returns.
+__device__ unsigned long long g_selftest_word = 0ull;
+
+__global__ void selftest_wait_kernel(int which, uint64_t limit_ns, unsigned int* fault) {
+    __shared__ __align__(8) uint64_t bar;
+    if (threadIdx.x != 0) return;
+    if (which == 0) {
+        const uint32_t b = smem_u32(&bar);
+        mbar_init(b, 1);
+        fence_mbar_init();
+        mbar_wait_bounded(b, 0u, fault, kFaultBulkWaitTimeout, limit_ns);
+    } else {
+        wait_tagged_u64(&g_selftest_word, fault, kFaultShareWaitTimeout, limit_ns);
+    }
+}
+
+cudaError_t launch_selftest_wait(int which, uint64_t limit_ns, unsigned int* fault, cudaStream_t stream) {
+    selftest_wait_kernel<<<1, 32, 0, stream>>>(which, limit_ns, fault);
+    return cudaGetLastError();
+}
+
 cudaError_t launch_qmm_generic(const uint8_t* w, const void* X, void* Y, int y_bf16, int64_t M, int64_t N,
                                int64_t K, int sm_count, cudaStream_t stream) {
     const int64_t want = (N + 7) / 8;

@@ -120,11 +120,6 @@ __device__ __forceinline__ uint32_t done_bar(uint32_t b0) { return b0 + 8u * (ui
 __device__ __forceinline__ void st_relaxed_u64(unsigned long long* p, unsigned long long v) {
     asm volatile("st.relaxed.gpu.global.b64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
 }
-__device__ __forceinline__ unsigned long long ld_relaxed_u64(const unsigned long long* p) {
-    unsigned long long v;
-    asm volatile("ld.relaxed.gpu.global.b64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
-    return v;
-}
 
 // per-set partial rows in shared memory: [set][local tile][matrix][row]
 __device__ __forceinline__ int part_at(int set, int lt, int m, int row) {
@@ -666,16 +661,7 @@ __device__ __forceinline__ void qmv_tc_body(const QtcParams& p) {
 #pragma unroll
                     for (int m = 0; m < NCH; ++m) {
                         unsigned long long* src = share + ((size_t)c * 2 + m) * kTileRows + r;
-                        unsigned long long w = ld_relaxed_u64(src);
-                        if (!(w >> 32)) {
-                            const uint64_t t0 = globaltimer_ns();
-                            while (!((w = ld_relaxed_u64(src)) >> 32)) {
-                                if (globaltimer_ns() - t0 > kWaitLimitNs) {
-                                    record_fault(p.fault, kFaultShareWaitTimeout);
-                                    break;
-                                }
-                            }
-                        }
+                        const unsigned long long w = wait_tagged_u64(src, p.fault, kFaultShareWaitTimeout);
                         v[m] += __uint_as_float((uint32_t)w);
                         st_relaxed_u64(src, 0ull);                 // consumed
                     }

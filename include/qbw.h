@@ -276,6 +276,21 @@ qbw_status qembed_q8_0(const void *w, const int32_t *ids, int64_t n_ids, void *o
  */
 qbw_status qbw_fault_read(uint32_t *code, int clear, void *stream);
 
+/*
+ * qbw_selftest_wait -- test-only: run one of the library's bounded waits on
+ * something nothing completes, with a limit of limit_us microseconds (1 ..
+ * 2,000,000), so a test can check that the wait gives up, that its code
+ * reaches the fault word and that the device stays usable.  The pages have no
+ * counterpart; it exercises this library's failure detection.
+ *   which = 0: phase 0 of a fresh shared-memory mbarrier (the wait of every
+ *              copy and MMA stage): sets fault bit 1 << 1
+ *   which = 1: the tag of a global word that stays 0 (the split-tile share
+ *              wait of qmv_q4_0 / qmv_q4_k): sets fault bit 1 << 4
+ * Enqueues one tiny kernel on `stream` and returns; QBW_EINVAL for other
+ * arguments.
+ */
+qbw_status qbw_selftest_wait(int which, uint32_t limit_us, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -103,6 +103,14 @@ def test_q4k_needs_whole_super_blocks(lib):
     assert f(P(ADDR), P(ADDR + 8), 4, 256, None) == 1
 
 
+def test_selftest_wait_validation(lib):
+    # rejected before any device work
+    assert lib.qbw_selftest_wait(2, 1000, None) == 1
+    assert lib.qbw_selftest_wait(-1, 1000, None) == 1
+    assert lib.qbw_selftest_wait(0, 0, None) == 1
+    assert lib.qbw_selftest_wait(0, 2000001, None) == 1
+
+
 def test_gateup_validation(lib):
     f = lib.qmv_gateup_q4_0
     a, b, x, y = ADDR, ADDR + (1 << 28), ADDR + (1 << 30), ADDR + (2 << 30)
