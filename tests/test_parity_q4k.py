@@ -50,7 +50,8 @@ def run(qbw, w, x, N, K, odt, offset=0):
     return to_f64(y)
 
 
-@pytest.mark.parametrize("N,K", [(1, 256), (37, 512), (300, 2304), (1000, 5376), (129, 8192), (5413, 5376)])
+@pytest.mark.parametrize("N,K", [(1, 256), (37, 512), (300, 2304), (1000, 5376), (129, 8192), (5413, 5376),
+                                 (600, 65536)])
 @pytest.mark.parametrize("xdt,odt", [("f32", "f32"), ("bf16", "bf16"), ("bf16", "f32")])
 def test_qmv_q4_k(qbw, oracle, N, K, xdt, odt):
     w = synth.q4_k_weights(N, K, seed=N + K)
