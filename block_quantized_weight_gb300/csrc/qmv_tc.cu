@@ -182,6 +182,38 @@ __device__ __forceinline__ void codes_pair(const uint32_t (&v)[36], uint32_t (&c
     }
 }
 
+// 8-bit form of block pair P (blocks 2P, 2P + 1) of a Q4_0 group -> 32 TMEM
+// columns of e4m3 bytes, 4 per column in K order.  An e4m3 byte b = 0..15 is
+// exactly b * 2^-9 (the subnormals and the first binade share one spacing), so
+// code c - 8 = (c & 7) - 8 [c < 8] splits into two exact 8-bit operands that
+// are both 0 where c = 8: block j's K-step 2j holds c & 7 and K-step 2j + 1
+// holds 8 [bit 3 of c clear] (the byte 0x08), against B columns of +x and -x.
+// Each K-step is 8 columns: the low nibbles of qs[0..15] (elements 0..15),
+// then their high nibbles (elements 16..31).  Block 2P's qs start at byte
+// 36P + 2 of the group row (two bytes into a word), block 2P + 1's at word
+// 9P + 5.
+template <int P>
+__device__ __forceinline__ void codes_pair_e4m3(const uint32_t (&v)[36], uint32_t (&col)[32]) {
+#pragma unroll
+    for (int t = 0; t < 4; ++t) {
+        const uint32_t w = __funnelshift_r(v[9 * P + t], v[9 * P + t + 1], 16);
+        const uint32_t h = __funnelshift_r(v[9 * P + t], v[9 * P + t + 1], 20);
+        col[t] = w & 0x07070707u;
+        col[4 + t] = h & 0x07070707u;
+        col[8 + t] = ~w & 0x08080808u;
+        col[12 + t] = ~h & 0x08080808u;
+    }
+#pragma unroll
+    for (int t = 0; t < 4; ++t) {
+        const uint32_t w = v[9 * P + 5 + t];
+        const uint32_t h = w >> 4;
+        col[16 + t] = w & 0x07070707u;
+        col[20 + t] = h & 0x07070707u;
+        col[24 + t] = ~w & 0x08080808u;
+        col[28 + t] = ~h & 0x08080808u;
+    }
+}
+
 // fp16 scales of blocks 2P (low half) and 2P + 1 (high half) of the group:
 // block 2P's in the low half of word 9P, block 2P + 1's in the high half of
 // word 9P + 4.
@@ -247,6 +279,38 @@ __device__ __forceinline__ void unit_dot(const uint32_t (&dv)[16], const uint32_
     }
 }
 
+// 8-bit form, one token: r0 = sum_j (d_j c_j) (D[2j] + D[2j + 1]), j = 0..7 in
+// order, where c_j = 2^9 / s_j undoes the e4m3 code scale 2^-9 and block j's
+// activation scale s_j (lanes 4j .. 4j + 3 hold c_j).
+__device__ __forceinline__ float unit_dot_e4m3(const uint32_t (&dv)[16], const uint32_t (&dd)[4], float c) {
+    float r = 0.f;
+#pragma unroll
+    for (int p = 0; p < 4; ++p) {
+        const float2 d = half2_to_float2(dd[p]);
+        const float c0 = __shfl_sync(0xffffffffu, c, 8 * p), c1 = __shfl_sync(0xffffffffu, c, 8 * p + 4);
+        r = fmaf(d.x * c0, __uint_as_float(dv[4 * p]) + __uint_as_float(dv[4 * p + 1]), r);
+        r = fmaf(d.y * c1, __uint_as_float(dv[4 * p + 2]) + __uint_as_float(dv[4 * p + 3]), r);
+    }
+    return r;
+}
+
+__device__ __forceinline__ uint32_t umax16x2(uint32_t a, uint32_t b) {
+    uint32_t r;
+    asm("max.u16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+    return r;
+}
+
+// two fp32 -> e4m3 (round to nearest, saturating), lo in the low byte
+__device__ __forceinline__ uint32_t e4m3x2(float lo, float hi) {
+    unsigned short r;
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+    return (uint32_t)r;
+}
+
+__device__ __forceinline__ void sts64(uint32_t addr, uint2 v) {
+    asm volatile("st.shared.v2.b32 [%0], {%1, %2};" ::"r"(addr), "r"(v.x), "r"(v.y) : "memory");
+}
+
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     uint32_t r;
     asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
@@ -267,17 +331,47 @@ __device__ __forceinline__ uint32_t b_chunk(int a, int n, int c) {
     return (uint32_t)(a * 2048 + (n >> 3) * 1024 + (n & 7) * 128 + ((c ^ (n & 7)) << 4));
 }
 
+// Byte offset, in the B operand, of byte `byte` of swizzle atom a, row n
+// (the 8-bit form: 128 K-elements per atom row).
+__device__ __forceinline__ uint32_t b_byte(int a, int n, uint32_t byte) {
+    return (uint32_t)(a * 2048 + (n >> 3) * 1024 + (n & 7) * 128) + ((((byte >> 4) ^ (uint32_t)(n & 7)) << 4) |
+                                                                       (byte & 15u));
+}
+
+// Eight bf16 activations (x[2e] in the low half of word e), already scaled by
+// the power of two sc, as two e4m3 pieces whose sum is exact: p0 keeps the
+// sign, exponent and top three mantissa bits (fp32 bits & 0xFFF00000), p1
+// the remaining four bits (bf16 has seven).  Both are exact in e4m3 while the
+// element is at least 2^-2 after scaling; below that e4m3's subnormal spacing
+// of 2^-9 rounds them.
+__device__ __forceinline__ void split_e4m3(uint4 xr, float sc, uint2& p0, uint2& p1) {
+    const uint32_t w[4] = {xr.x, xr.y, xr.z, xr.w};
+    uint32_t h0[4], h1[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+        const float lo = __uint_as_float(w[e] << 16) * sc, hi = __uint_as_float(w[e] & 0xFFFF0000u) * sc;
+        const float lo0 = __uint_as_float(__float_as_uint(lo) & 0xFFF00000u);
+        const float hi0 = __uint_as_float(__float_as_uint(hi) & 0xFFF00000u);
+        h0[e] = e4m3x2(lo0, hi0);
+        h1[e] = e4m3x2(lo - lo0, hi - hi0);
+    }
+    p0 = make_uint2(h0[0] | (h0[1] << 16), h0[2] | (h0[3] << 16));
+    p1 = make_uint2(h1[0] | (h1[1] << 16), h1[2] | (h1[3] << 16));
+}
+
 // NMAT = 1: y = W x.  NMAT = 2: out = gelu_tanh(Wg x) * (Wu x); the units of a
 // (tile, group) are its gate and up halves, in that order (measured faster
 // than all gate groups of a tile before its up groups, by about 1 %).  NTOK = 2 (with
 // NMAT = 1 and bf16 activations): Y[m] = W X[m] for two token rows, which take
 // the two B columns of each block that x_hi and x_lo take for one token.
-// Each row keeps NCH = NMAT * NTOK sums (channels).
-template <int FMT, int NMAT, int NTOK>
+// Each row keeps NCH = NMAT * NTOK sums (channels).  F8: the 8-bit form of
+// the operands (Q4_0, one token, bf16 activations; see codes_pair_e4m3).
+template <int FMT, int NMAT, int NTOK, bool F8>
 __device__ __forceinline__ void qmv_tc_body(const QtcParams& p) {
     constexpr int NCH = NMAT * NTOK;
     static_assert(NCH <= 2, "at most two sums per row");
     static_assert(FMT == kFmtQ4 || (NMAT == 1 && NTOK == 1), "Q4_K: one matrix, one token");
+    static_assert(!F8 || (FMT == kFmtQ4 && NTOK == 1), "8-bit form: Q4_0, one token");
     extern __shared__ __align__(1024) uint8_t smem[];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int ctas = (int)gridDim.x, cta = (int)blockIdx.x;
@@ -357,7 +451,7 @@ __device__ __forceinline__ void qmv_tc_body(const QtcParams& p) {
         const int set = warp - kMmaWarp0;
         const uint32_t tmem = *tmem_slot;
         if (lane == 0) {
-            const uint32_t idesc = idesc_bf16(kTileRows, kN);
+            const uint32_t idesc = F8 ? idesc_e4m3(kTileRows, kN) : idesc_bf16(kTileRows, kN);
             const uint32_t a_tmem = tmem + (uint32_t)set * kACols;
             const uint64_t b0 = sw128_desc(sbase + kOffB + (uint32_t)set * kBBytes);
             uint32_t phase = 0;
@@ -369,17 +463,21 @@ __device__ __forceinline__ void qmv_tc_body(const QtcParams& p) {
                 if (!ok) break;
                 tc_fence_after();
 #pragma unroll
-                for (int k = 0; k < 8; ++k)
-                    tc_mma(d_tmem, a_tmem + 8u * (uint32_t)k, b0 + (uint64_t)((k >> 2) * 128 + (k & 3) * 2), idesc,
-                           k > 0 ? 1u : 0u);
+                for (int k = 0; k < 8; ++k) {
+                    const uint64_t bd = b0 + (uint64_t)((k >> 2) * 128 + (k & 3) * 2);
+                    if constexpr (F8) tc_mma_f8(d_tmem, a_tmem + 8u * (uint32_t)k, bd, idesc, k > 0 ? 1u : 0u);
+                    else tc_mma(d_tmem, a_tmem + 8u * (uint32_t)k, bd, idesc, k > 0 ? 1u : 0u);
+                }
                 tc_commit(aempty_bar(bar0, set, 0));
                 ok = mbar_wait_bounded(afull_bar(bar0, set, 1), phase, p.fault, kFaultMmaWaitTimeout);
                 if (!ok) break;
                 tc_fence_after();
 #pragma unroll
-                for (int k = 8; k < 16; ++k)
-                    tc_mma(d_tmem, a_tmem + 8u * (uint32_t)k, b0 + (uint64_t)((k >> 2) * 128 + (k & 3) * 2), idesc,
-                           1u);
+                for (int k = 8; k < 16; ++k) {
+                    const uint64_t bd = b0 + (uint64_t)((k >> 2) * 128 + (k & 3) * 2);
+                    if constexpr (F8) tc_mma_f8(d_tmem, a_tmem + 8u * (uint32_t)k, bd, idesc, 1u);
+                    else tc_mma(d_tmem, a_tmem + 8u * (uint32_t)k, bd, idesc, 1u);
+                }
                 tc_commit(aempty_bar(bar0, set, 1));
                 phase ^= 1u;
             }
@@ -401,12 +499,21 @@ __device__ __forceinline__ void qmv_tc_body(const QtcParams& p) {
         // slots 8q .. 8q + 7 write them.  Slot xl is elements 8 xl .. 8 xl + 7 of
         // the group: swizzle atom xl / 8, block j = xl / 4, B rows 2j (x_hi)
         // and 2j + 1 (x_lo), in K-half xl / 16.
-        const int xl = (FMT == kFmtQ4K) ? lane : 8 * q + lane;
-        const bool loads_x = (FMT == kFmtQ4K) || lane < 8;
-        const bool bwriter = (FMT == kFmtQ4K) ? ((lane >> 3) == q) : (lane < 8);
+        // The 8-bit form is loaded like Q4_K: every lane loads slot `lane`, as
+        // each block's activation scale needs its maximum over 32 elements.
+        constexpr bool kAllLanesX = FMT == kFmtQ4K || F8;
+        const int xl = kAllLanesX ? lane : 8 * q + lane;
+        const bool loads_x = kAllLanesX || lane < 8;
+        const bool bwriter = kAllLanesX ? ((lane >> 3) == q) : (lane < 8);
         const int bj = xl >> 2;
         const uint32_t b_hi = bbuf + b_chunk(xl >> 3, 2 * bj, xl & 7);
         const uint32_t b_lo = bbuf + b_chunk(xl >> 3, 2 * bj + 1, xl & 7);
+        // 8-bit form: the slot's 8 bytes in K-steps 2j (+x) and 2j + 1 (-x),
+        // rows 2j (piece 0) and 2j + 1 (piece 1), atom j / 2
+        const uint32_t bo = (uint32_t)((bj & 1) * 64 + 8 * (xl & 3));
+        const uint32_t f8_p0 = bbuf + b_byte(bj >> 1, 2 * bj, bo), f8_p1 = bbuf + b_byte(bj >> 1, 2 * bj + 1, bo);
+        const uint32_t f8_n0 = bbuf + b_byte(bj >> 1, 2 * bj, bo + 32u);
+        const uint32_t f8_n1 = bbuf + b_byte(bj >> 1, 2 * bj + 1, bo + 32u);
         const int bhalf = xl >> 4;
         const int row = 32 * q + lane;
         bool counted = !contrib0;
@@ -458,6 +565,7 @@ __device__ __forceinline__ void qmv_tc_body(const QtcParams& p) {
         };
         uint32_t pend_dd[4] = {0u, 0u, 0u, 0u};
         float pend_sx = 0.f;     // Q4_K: the previous unit's sub-block sum of this lane's group of 4
+        float pend_c = 0.f;      // 8-bit form: the previous unit's c_j of this lane's block
         int k = 0;
         for (int i = set; i < n; i += kSets, ++k) {
             const int u = u0 + i, ug = u / NMAT, mat = u - ug * NMAT, t = ug / G, g = ug - t * G;
@@ -546,9 +654,27 @@ __device__ __forceinline__ void qmv_tc_body(const QtcParams& p) {
                 cur_sx += __shfl_xor_sync(0xffffffffu, cur_sx, 1);
                 cur_sx += __shfl_xor_sync(0xffffffffu, cur_sx, 2);
             }
+            // 8-bit form: block j's scale s_j = 2^(es - 127) takes its largest
+            // |x| into [2^7, 2^8) (e4m3 reaches 448); lanes 4j .. 4j + 3 hold
+            // block j's 32 activations
+            float cur_c = 0.f;
+            uint2 bp0 = make_uint2(0u, 0u), bp1 = bp0;
+            if constexpr (F8) {
+                const uint32_t m2 = umax16x2(umax16x2(xr0.x & 0x7FFF7FFFu, xr0.y & 0x7FFF7FFFu),
+                                             umax16x2(xr0.z & 0x7FFF7FFFu, xr0.w & 0x7FFF7FFFu));
+                uint32_t mx = max(m2 & 0xFFFFu, m2 >> 16);
+                mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+                mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+                // bf16 biased exponent E of the maximum: es = 261 - E, kept where
+                // both 2^(es - 127) and 2^9 / that are normal fp32
+                const int es = min(max(261 - (int)(mx >> 7), 9), 253);
+                cur_c = __uint_as_float((uint32_t)(263 - es) << 23);
+                split_e4m3(xr0, __uint_as_float((uint32_t)es << 23), bp0, bp1);
+            }
             const uint32_t prev = (uint32_t)(k - 1) & 1u;     // completion parity of the previous unit
             // ---- half 0: K 0..127 (block pairs 0, 1; B atoms 0, 1 written by warps 0, 1)
-            codes_pair<FMT, 0>(v, c0);
+            if constexpr (F8) codes_pair_e4m3<0>(v, c0);
+            else codes_pair<FMT, 0>(v, c0);
             if (k > 0) {
                 const bool free = mbar_wait_bounded(aempty_bar(bar0, set, 0), prev, p.fault, kFaultMmaWaitTimeout);
                 if (!__all_sync(0xffffffffu, free)) {
@@ -558,12 +684,20 @@ __device__ __forceinline__ void qmv_tc_body(const QtcParams& p) {
                 tc_fence_after();
             }
             if (bwriter && bhalf == 0) {
-                sts128(b_hi, bhi);
-                sts128(b_lo, blo);
+                if constexpr (F8) {
+                    sts64(f8_p0, bp0);
+                    sts64(f8_p1, bp1);
+                    sts64(f8_n0, make_uint2(bp0.x ^ 0x80808080u, bp0.y ^ 0x80808080u));
+                    sts64(f8_n1, make_uint2(bp1.x ^ 0x80808080u, bp1.y ^ 0x80808080u));
+                } else {
+                    sts128(b_hi, bhi);
+                    sts128(b_lo, blo);
+                }
                 fence_proxy_async_smem();     // B visible to the tensor core
             }
             tmem_st32(a_taddr, c0);
-            codes_pair<FMT, 1>(v, c1);
+            if constexpr (F8) codes_pair_e4m3<1>(v, c1);
+            else codes_pair<FMT, 1>(v, c1);
             tmem_wait_st();
             tmem_st32(a_taddr + 32u, c1);
             tmem_wait_st();
@@ -571,7 +705,8 @@ __device__ __forceinline__ void qmv_tc_body(const QtcParams& p) {
             __syncwarp();
             if (lane == 0) mbar_arrive(afull_bar(bar0, set, 0));
             // ---- half 1: K 128..255 (block pairs 2, 3; B atoms 2, 3 written by warps 2, 3)
-            codes_pair<FMT, 2>(v, c0);
+            if constexpr (F8) codes_pair_e4m3<2>(v, c0);
+            else codes_pair<FMT, 2>(v, c0);
             if (k > 0) {
                 const bool free = mbar_wait_bounded(aempty_bar(bar0, set, 1), prev, p.fault, kFaultMmaWaitTimeout);
                 if (!__all_sync(0xffffffffu, free)) {
@@ -581,12 +716,20 @@ __device__ __forceinline__ void qmv_tc_body(const QtcParams& p) {
                 tc_fence_after();
             }
             if (bwriter && bhalf == 1) {
-                sts128(b_hi, bhi);
-                sts128(b_lo, blo);
+                if constexpr (F8) {
+                    sts64(f8_p0, bp0);
+                    sts64(f8_p1, bp1);
+                    sts64(f8_n0, make_uint2(bp0.x ^ 0x80808080u, bp0.y ^ 0x80808080u));
+                    sts64(f8_n1, make_uint2(bp1.x ^ 0x80808080u, bp1.y ^ 0x80808080u));
+                } else {
+                    sts128(b_hi, bhi);
+                    sts128(b_lo, blo);
+                }
                 fence_proxy_async_smem();
             }
             tmem_st32(a_taddr + 64u, c0);
-            codes_pair<FMT, 3>(v, c1);
+            if constexpr (F8) codes_pair_e4m3<3>(v, c1);
+            else codes_pair<FMT, 3>(v, c1);
             tmem_wait_st();
             tmem_st32(a_taddr + 96u, c1);
             tmem_wait_st();
@@ -601,12 +744,14 @@ __device__ __forceinline__ void qmv_tc_body(const QtcParams& p) {
                 tmem_wait_ld();
                 float r0, r1 = 0.f;
                 if constexpr (FMT == kFmtQ4K) r0 = unit_dot_q4k(dv, pend_dd, pend_sx);
+                else if constexpr (F8) r0 = unit_dot_e4m3(dv, pend_dd, pend_c);
                 else unit_dot<NTOK>(dv, pend_dd, r0, r1);
                 add_unit(r0, r1);
             }
 #pragma unroll
             for (int P = 0; P < 4; ++P) pend_dd[P] = dd[P];
             pend_sx = cur_sx;
+            pend_c = cur_c;
             pend_tile = t;
             pend_mat = mat;
         }
@@ -621,6 +766,7 @@ __device__ __forceinline__ void qmv_tc_body(const QtcParams& p) {
                 tmem_wait_ld();
                 float r0, r1 = 0.f;
                 if constexpr (FMT == kFmtQ4K) r0 = unit_dot_q4k(dv, pend_dd, pend_sx);
+                else if constexpr (F8) r0 = unit_dot_e4m3(dv, pend_dd, pend_c);
                 else unit_dot<NTOK>(dv, pend_dd, r0, r1);
                 add_unit(r0, r1);
             }
@@ -689,11 +835,17 @@ __device__ __forceinline__ void qmv_tc_body(const QtcParams& p) {
 
 template <int NMAT, int NTOK>
 __global__ void __launch_bounds__(kThreads, 1) qmv_q4_0_tc_kernel(const __grid_constant__ QtcParams p) {
-    qmv_tc_body<kFmtQ4, NMAT, NTOK>(p);
+    qmv_tc_body<kFmtQ4, NMAT, NTOK, false>(p);
+}
+
+// bf16 activations, one token: the 8-bit operand form
+template <int NMAT>
+__global__ void __launch_bounds__(kThreads, 1) qmv_q4_0_tc_e4m3_kernel(const __grid_constant__ QtcParams p) {
+    qmv_tc_body<kFmtQ4, NMAT, 1, true>(p);
 }
 
 __global__ void __launch_bounds__(kThreads, 1) qmv_q4_k_tc_kernel(const __grid_constant__ QtcParams p) {
-    qmv_tc_body<kFmtQ4K, 1, 1>(p);
+    qmv_tc_body<kFmtQ4K, 1, 1, false>(p);
 }
 
 }  // namespace
@@ -739,14 +891,17 @@ cudaError_t launch_qmv_tc(int fmt, int nmat, int ntok, const CUtensorMap* tmap_w
     p.x_bf16 = x_bf16;
     p.y_bf16 = y_bf16;
     const int ctas = p.units < sm_count ? p.units : sm_count;
+    const bool f8 = fmt == kFmtQ4 && ntok == 1 && x_bf16;
     auto kernel = fmt == kFmtQ4K ? qmv_q4_k_tc_kernel
+                  : f8           ? (nmat == 2 ? qmv_q4_0_tc_e4m3_kernel<2> : qmv_q4_0_tc_e4m3_kernel<1>)
                   : (nmat == 2 ? qmv_q4_0_tc_kernel<2, 1>
                                : (ntok == 2 ? qmv_q4_0_tc_kernel<1, 2> : qmv_q4_0_tc_kernel<1, 1>));
     static thread_local int prepared_device = -1;
     int dev = 0;
     cudaGetDevice(&dev);
     if (prepared_device != dev) {
-        for (auto f : {qmv_q4_0_tc_kernel<1, 1>, qmv_q4_0_tc_kernel<2, 1>, qmv_q4_0_tc_kernel<1, 2>, qmv_q4_k_tc_kernel}) {
+        for (auto f : {qmv_q4_0_tc_kernel<1, 1>, qmv_q4_0_tc_kernel<2, 1>, qmv_q4_0_tc_kernel<1, 2>,
+                       qmv_q4_0_tc_e4m3_kernel<1>, qmv_q4_0_tc_e4m3_kernel<2>, qmv_q4_k_tc_kernel}) {
             cudaError_t e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
             if (e != cudaSuccess) return e;
         }
