@@ -371,6 +371,10 @@ def supplementary_kernels(torch, qbw, hbm_peak):
     y = torch.empty(N, device=dev)
     run("qmv_q4_0 21504x5376 f32", w.numel() + 4 * K + 4 * N, copies,
         lambda i: (lambda: qbw.qmv_q4_0(ws[i], x, y, 1, N, K)))
+    # the same matrix with bf16 activations (the sweep's case), fp32 out
+    xb1 = bf16(synth.activations(K, seed=1, dtype="bf16"))
+    run("qmv_q4_0 21504x5376 bf16->f32", w.numel() + 2 * K + 4 * N, copies,
+        lambda i: (lambda: qbw.qmv_q4_0(ws[i], xb1, y, 1, N, K)))
     # gate+up on two such matrices, bf16 in, fp32 out
     wu = torch.from_numpy(synth.q4_0_weights(N, K, seed=2, stream=1)).to(dev)
     wus = [wu.clone() for _ in range(copies)]
@@ -611,6 +615,15 @@ def profile_case(args):
         y = torch.empty(N, device=dev)
         call = lambda i: qbw.qmv_q4_0(ws[i % copies], x, y, 1, N, K)
         nbytes = ws[0].numel() + 4 * K + 4 * N
+    elif name == "q4_0_bf16":
+        # the same matrix with bf16 activations: the tensor-core kernel's 8-bit operand form
+        N, K = 21504, 5376
+        ws = [torch.from_numpy(synth.q4_0_weights(N, K, seed=1)).to(dev) for _ in range(copies)]
+        xb = torch.from_numpy(synth.activations(K, seed=1, dtype="bf16").view(np.int16).copy()).view(
+            torch.bfloat16).to(dev)
+        y = torch.empty(N, device=dev)
+        call = lambda i: qbw.qmv_q4_0(ws[i % copies], xb, y, 1, N, K)
+        nbytes = ws[0].numel() + 2 * K + 4 * N
     elif name == "q4_k":
         N, K = 21504, 5376
         ws = [torch.from_numpy(synth.q4_k_weights(N, K, seed=1)).to(dev) for _ in range(copies)]
@@ -712,7 +725,7 @@ def main():
     ap.add_argument("--no-kernels", action="store_true", help="skip the single-matrix supplementary numbers")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
-    ap.add_argument("--profile", choices=["q8_0", "q4_0", "q4_k", "gateup", "qmm", "sweep"],
+    ap.add_argument("--profile", choices=["q8_0", "q4_0", "q4_0_bf16", "q4_k", "gateup", "qmm", "sweep"],
                     help="run only one small case (for profiler captures): a single-matrix workload, or the "
                          "sweep's launches over 6 layers")
     args = ap.parse_args()

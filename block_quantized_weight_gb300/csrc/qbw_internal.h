@@ -16,6 +16,7 @@ enum FaultCode : unsigned int {
     kFaultMmaWaitTimeout = 2,    // an mbarrier guarding tensor-core work never completed
     kFaultBadIndex = 3,          // a token-table row index outside [0, N)
     kFaultShareWaitTimeout = 4,  // a split tile's share from another CTA never arrived
+    kFaultPlan = 5,              // a launch plan exceeded a kernel's fixed capacity (internal)
 };
 
 enum : int { kFmtQ8 = 0, kFmtQ4 = 1, kFmtQ4K = 2 };

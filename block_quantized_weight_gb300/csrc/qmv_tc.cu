@@ -45,6 +45,7 @@
 // issues set s's MMAs (M = 128, N = 16, K = 16; 16 per unit) into set s's
 // accumulator.  Each set's rows read D back one unit later, while the next
 // unit's codes are already decoded in registers.
+#include <algorithm>
 #include <atomic>
 #include <cstdint>
 
@@ -89,7 +90,13 @@ constexpr uint32_t kOffPart = kOffB + kSets * kBBytes;
 constexpr uint32_t kOffBar = kOffPart + kSets * kMaxLocalTiles * 2 * kTileRows * 4;
 constexpr int kBars = 2 * kStages + 4 * kSets + 1;
 constexpr uint32_t kOffSlot = kOffBar + 8 * kBars;
-constexpr uint32_t kSmemBytes = kOffSlot + 16;
+// 8-bit form: the activations of up to kXtGroups K-groups, built once per CTA:
+// per group 32 chunks of 8 elements as {piece 0, piece 1} (16 bytes each),
+// and per group the 8 blocks' read-back factors c_j (fp32)
+constexpr int kXtGroups = 64;
+constexpr uint32_t kOffXt = (kOffSlot + 16 + 15) & ~15u;
+constexpr uint32_t kOffXc = kOffXt + kXtGroups * 32 * 16;
+constexpr uint32_t kSmemBytes = kOffXc + kXtGroups * 8 * 4;
 
 static_assert(kStages % kSets == 0, "stage s must serve set s % 3");
 static_assert(kOffB % 1024 == 0, "B operand needs 1024-byte alignment");
@@ -281,15 +288,14 @@ __device__ __forceinline__ void unit_dot(const uint32_t (&dv)[16], const uint32_
 
 // 8-bit form, one token: r0 = sum_j (d_j c_j) (D[2j] + D[2j + 1]), j = 0..7 in
 // order, where c_j = 2^9 / s_j undoes the e4m3 code scale 2^-9 and block j's
-// activation scale s_j (lanes 4j .. 4j + 3 hold c_j).
-__device__ __forceinline__ float unit_dot_e4m3(const uint32_t (&dv)[16], const uint32_t (&dd)[4], float c) {
+// activation scale s_j (c[0..7] = c_j).
+__device__ __forceinline__ float unit_dot_e4m3(const uint32_t (&dv)[16], const uint32_t (&dd)[4], const float (&c)[8]) {
     float r = 0.f;
 #pragma unroll
     for (int p = 0; p < 4; ++p) {
         const float2 d = half2_to_float2(dd[p]);
-        const float c0 = __shfl_sync(0xffffffffu, c, 8 * p), c1 = __shfl_sync(0xffffffffu, c, 8 * p + 4);
-        r = fmaf(d.x * c0, __uint_as_float(dv[4 * p]) + __uint_as_float(dv[4 * p + 1]), r);
-        r = fmaf(d.y * c1, __uint_as_float(dv[4 * p + 2]) + __uint_as_float(dv[4 * p + 3]), r);
+        r = fmaf(d.x * c[2 * p], __uint_as_float(dv[4 * p]) + __uint_as_float(dv[4 * p + 1]), r);
+        r = fmaf(d.y * c[2 * p + 1], __uint_as_float(dv[4 * p + 2]) + __uint_as_float(dv[4 * p + 3]), r);
     }
     return r;
 }
@@ -329,6 +335,19 @@ __device__ __forceinline__ void sts128(uint32_t addr, uint4 v) {
 // 16-byte chunk holding elements 8c .. 8c + 7 of swizzle atom a, row n.
 __device__ __forceinline__ uint32_t b_chunk(int a, int n, int c) {
     return (uint32_t)(a * 2048 + (n >> 3) * 1024 + (n & 7) * 128 + ((c ^ (n & 7)) << 4));
+}
+
+// 8-bit form: the read-back factors c_j of the group in table slot sl
+__device__ __forceinline__ void table_c(uint32_t sbase, int sl, float (&c)[8]) {
+    const uint4 a = lds128(sbase + kOffXc + (uint32_t)sl * 32u), b = lds128(sbase + kOffXc + (uint32_t)sl * 32u + 16u);
+    c[0] = __uint_as_float(a.x);
+    c[1] = __uint_as_float(a.y);
+    c[2] = __uint_as_float(a.z);
+    c[3] = __uint_as_float(a.w);
+    c[4] = __uint_as_float(b.x);
+    c[5] = __uint_as_float(b.y);
+    c[6] = __uint_as_float(b.z);
+    c[7] = __uint_as_float(b.w);
 }
 
 // Byte offset, in the B operand, of byte `byte` of swizzle atom a, row n
@@ -499,11 +518,10 @@ __device__ __forceinline__ void qmv_tc_body(const QtcParams& p) {
         // slots 8q .. 8q + 7 write them.  Slot xl is elements 8 xl .. 8 xl + 7 of
         // the group: swizzle atom xl / 8, block j = xl / 4, B rows 2j (x_hi)
         // and 2j + 1 (x_lo), in K-half xl / 16.
-        // The 8-bit form is loaded like Q4_K: every lane loads slot `lane`, as
-        // each block's activation scale needs its maximum over 32 elements.
-        constexpr bool kAllLanesX = FMT == kFmtQ4K || F8;
+        // (the 8-bit form's B-writing lanes read their slot from the table)
+        constexpr bool kAllLanesX = FMT == kFmtQ4K;
         const int xl = kAllLanesX ? lane : 8 * q + lane;
-        const bool loads_x = kAllLanesX || lane < 8;
+        const bool loads_x = !F8 && (kAllLanesX || lane < 8);
         const bool bwriter = kAllLanesX ? ((lane >> 3) == q) : (lane < 8);
         const int bj = xl >> 2;
         const uint32_t b_hi = bbuf + b_chunk(xl >> 3, 2 * bj, xl & 7);
@@ -516,6 +534,40 @@ __device__ __forceinline__ void qmv_tc_body(const QtcParams& p) {
         const uint32_t f8_n1 = bbuf + b_byte(bj >> 1, 2 * bj + 1, bo + 32u);
         const int bhalf = xl >> 4;
         const int row = 32 * q + lane;
+        // 8-bit form: the table of the K-groups g of this CTA's units, group g
+        // in slot (g - xg0) mod G.  Each chunk of 8 elements is scaled by its
+        // block's s_j = 2^(es - 127), which takes the block's largest |x| into
+        // [2^7, 2^8) (e4m3 reaches 448); es = 261 - E for the bf16 biased
+        // exponent E of that maximum, kept where s_j and c_j = 2^9 / s_j are
+        // normal fp32.  Built by the twelve dequantizing warps; the host
+        // launches this form only where the table holds every group needed.
+        const int xg0 = (u0 / NMAT) % G;
+        if constexpr (F8) {
+            const int cnt = n > 0 ? min(G, (u1 - 1) / NMAT - u0 / NMAT + 1) : 0;
+            if (cnt > kXtGroups) record_fault(p.fault, kFaultPlan);
+            const int nch = min(cnt, kXtGroups) * 32;
+            for (int c0 = warp * 32; c0 < nch; c0 += kProducerWarp * 32) {
+                const int c = c0 + lane, sl = c >> 5;
+                int g = xg0 + sl;
+                if (g >= G) g -= G;
+                const uint4 xr = __ldg(reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p.x) +
+                                                                      (size_t)g * kGroupK + 8 * (c & 31)));
+                const uint32_t m2 = umax16x2(umax16x2(xr.x & 0x7FFF7FFFu, xr.y & 0x7FFF7FFFu),
+                                             umax16x2(xr.z & 0x7FFF7FFFu, xr.w & 0x7FFF7FFFu));
+                uint32_t mx = max(m2 & 0xFFFFu, m2 >> 16);
+                mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+                mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+                const int es = min(max(261 - (int)(mx >> 7), 9), 253);
+                uint2 q0, q1;
+                split_e4m3(xr, __uint_as_float((uint32_t)es << 23), q0, q1);
+                sts128(sbase + kOffXt + (uint32_t)c * 16u, make_uint4(q0.x, q0.y, q1.x, q1.y));
+                if ((lane & 3) == 0)
+                    asm volatile("st.shared.b32 [%0], %1;" ::"r"(sbase + kOffXc + (uint32_t)(c >> 2) * 4u),
+                                 "r"((uint32_t)(263 - es) << 23)
+                                 : "memory");
+            }
+            asm volatile("bar.sync 2, %0;" ::"n"(kProducerWarp * 32) : "memory");
+        }
         bool counted = !contrib0;
         // after the three sets' shares of the first tile are in part[][0][], the
         // last of a quarter's three warps publishes the quarter's rows
@@ -565,7 +617,7 @@ __device__ __forceinline__ void qmv_tc_body(const QtcParams& p) {
         };
         uint32_t pend_dd[4] = {0u, 0u, 0u, 0u};
         float pend_sx = 0.f;     // Q4_K: the previous unit's sub-block sum of this lane's group of 4
-        float pend_c = 0.f;      // 8-bit form: the previous unit's c_j of this lane's block
+        int pend_sl = 0;         // 8-bit form: the previous unit's table slot
         int k = 0;
         for (int i = set; i < n; i += kSets, ++k) {
             const int u = u0 + i, ug = u / NMAT, mat = u - ug * NMAT, t = ug / G, g = ug - t * G;
@@ -654,22 +706,19 @@ __device__ __forceinline__ void qmv_tc_body(const QtcParams& p) {
                 cur_sx += __shfl_xor_sync(0xffffffffu, cur_sx, 1);
                 cur_sx += __shfl_xor_sync(0xffffffffu, cur_sx, 2);
             }
-            // 8-bit form: block j's scale s_j = 2^(es - 127) takes its largest
-            // |x| into [2^7, 2^8) (e4m3 reaches 448); lanes 4j .. 4j + 3 hold
-            // block j's 32 activations
-            float cur_c = 0.f;
+            // 8-bit form: this unit's group in the table; the B-writing lanes'
+            // two pieces of their slot
+            int cur_sl = 0;
             uint2 bp0 = make_uint2(0u, 0u), bp1 = bp0;
             if constexpr (F8) {
-                const uint32_t m2 = umax16x2(umax16x2(xr0.x & 0x7FFF7FFFu, xr0.y & 0x7FFF7FFFu),
-                                             umax16x2(xr0.z & 0x7FFF7FFFu, xr0.w & 0x7FFF7FFFu));
-                uint32_t mx = max(m2 & 0xFFFFu, m2 >> 16);
-                mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
-                mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-                // bf16 biased exponent E of the maximum: es = 261 - E, kept where
-                // both 2^(es - 127) and 2^9 / that are normal fp32
-                const int es = min(max(261 - (int)(mx >> 7), 9), 253);
-                cur_c = __uint_as_float((uint32_t)(263 - es) << 23);
-                split_e4m3(xr0, __uint_as_float((uint32_t)es << 23), bp0, bp1);
+                cur_sl = g - xg0;
+                if (cur_sl < 0) cur_sl += G;
+                if (cur_sl >= kXtGroups) cur_sl = 0;       // never: the host checks the table size
+                if (bwriter) {
+                    const uint4 tq = lds128(sbase + kOffXt + (uint32_t)(cur_sl * 32 + xl) * 16u);
+                    bp0 = make_uint2(tq.x, tq.y);
+                    bp1 = make_uint2(tq.z, tq.w);
+                }
             }
             const uint32_t prev = (uint32_t)(k - 1) & 1u;     // completion parity of the previous unit
             // ---- half 0: K 0..127 (block pairs 0, 1; B atoms 0, 1 written by warps 0, 1)
@@ -744,14 +793,18 @@ __device__ __forceinline__ void qmv_tc_body(const QtcParams& p) {
                 tmem_wait_ld();
                 float r0, r1 = 0.f;
                 if constexpr (FMT == kFmtQ4K) r0 = unit_dot_q4k(dv, pend_dd, pend_sx);
-                else if constexpr (F8) r0 = unit_dot_e4m3(dv, pend_dd, pend_c);
+                else if constexpr (F8) {
+                    float c[8];
+                    table_c(sbase, pend_sl, c);
+                    r0 = unit_dot_e4m3(dv, pend_dd, c);
+                }
                 else unit_dot<NTOK>(dv, pend_dd, r0, r1);
                 add_unit(r0, r1);
             }
 #pragma unroll
             for (int P = 0; P < 4; ++P) pend_dd[P] = dd[P];
             pend_sx = cur_sx;
-            pend_c = cur_c;
+            pend_sl = cur_sl;
             pend_tile = t;
             pend_mat = mat;
         }
@@ -766,7 +819,11 @@ __device__ __forceinline__ void qmv_tc_body(const QtcParams& p) {
                 tmem_wait_ld();
                 float r0, r1 = 0.f;
                 if constexpr (FMT == kFmtQ4K) r0 = unit_dot_q4k(dv, pend_dd, pend_sx);
-                else if constexpr (F8) r0 = unit_dot_e4m3(dv, pend_dd, pend_c);
+                else if constexpr (F8) {
+                    float c[8];
+                    table_c(sbase, pend_sl, c);
+                    r0 = unit_dot_e4m3(dv, pend_dd, c);
+                }
                 else unit_dot<NTOK>(dv, pend_dd, r0, r1);
                 add_unit(r0, r1);
             }
@@ -891,7 +948,10 @@ cudaError_t launch_qmv_tc(int fmt, int nmat, int ntok, const CUtensorMap* tmap_w
     p.x_bf16 = x_bf16;
     p.y_bf16 = y_bf16;
     const int ctas = p.units < sm_count ? p.units : sm_count;
-    const bool f8 = fmt == kFmtQ4 && ntok == 1 && x_bf16;
+    // the 8-bit form needs every K-group of a CTA's unit range in its table
+    const int per_cta = (p.units + ctas - 1) / ctas;
+    const bool f8 = fmt == kFmtQ4 && ntok == 1 && x_bf16 &&
+                    std::min(p.groups, (per_cta - 1) / nmat + 2) <= kXtGroups;
     auto kernel = fmt == kFmtQ4K ? qmv_q4_k_tc_kernel
                   : f8           ? (nmat == 2 ? qmv_q4_0_tc_e4m3_kernel<2> : qmv_q4_0_tc_e4m3_kernel<1>)
                   : (nmat == 2 ? qmv_q4_0_tc_kernel<2, 1>

@@ -271,6 +271,8 @@ qbw_status qembed_q8_0(const void *w, const int32_t *ids, int64_t n_ids, void *o
  *   c = 3  qembed_q8_0 met a row index outside [0, N)
  *   c = 4  qmv_q4_0 waited in vain (about two seconds) for another CTA's share
  *          of a 128-row tile split between CTAs
+ *   c = 5  internal: a launch plan exceeded a kernel's fixed capacity (the
+ *          host-side planning never allows it; seen only after a library bug)
  * Synchronizes `stream`, stores the word in *code and, if clear != 0, resets
  * it to zero.
  */
