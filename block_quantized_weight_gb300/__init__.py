@@ -18,7 +18,7 @@ import threading
 __all__ = [
     "QbwError", "load", "lib_path",
     "qmv_q8_0", "qmv_q4_0", "qmv_gateup_q4_0", "qmm_q4_0_smallM", "qmm_q4_0_smallM_workspace_bytes",
-    "qmm_q4_0_smallM_noalloc", "NOALLOC_SCRATCH_BYTES", "qembed_q8_0", "qdequant_q8_0", "qdequant_q4_0", "qmv_q4_k", "qdequant_q4_k", "selftest_wait", "fault_read", "status_str", "version",
+    "qmm_q4_0_smallM_noalloc", "NOALLOC_SCRATCH_BYTES", "qembed_q8_0", "qdequant_q8_0", "qdequant_q4_0", "qmv_q4_k", "qdequant_q4_k", "selftest_wait", "Chain", "fault_read", "status_str", "version",
     "F32", "BF16",
 ]
 
@@ -82,6 +82,18 @@ def _declare(L):
     L.qbw_fault_read.argtypes = [ctypes.POINTER(ctypes.c_uint32), i32, P]
     L.qbw_selftest_wait.restype = i32
     L.qbw_selftest_wait.argtypes = [i32, ctypes.c_uint32, P]
+    L.qbw_chain_create.restype = i32
+    L.qbw_chain_create.argtypes = [ctypes.POINTER(_ChainStep), i32, ctypes.POINTER(P)]
+    L.qbw_chain_run.restype = i32
+    L.qbw_chain_run.argtypes = [P, P]
+    L.qbw_chain_destroy.restype = i32
+    L.qbw_chain_destroy.argtypes = [P]
+
+
+class _ChainStep(ctypes.Structure):
+    """qbw_chain_step of include/qbw.h."""
+    _fields_ = [("w", ctypes.c_void_p), ("w_up", ctypes.c_void_p), ("x", ctypes.c_void_p), ("y", ctypes.c_void_p),
+                ("yt", ctypes.c_int), ("N", ctypes.c_int64), ("K", ctypes.c_int64)]
 
 
 def status_str(status: int) -> str:
@@ -207,6 +219,40 @@ def selftest_wait(which: int, limit_us: int, stream=None):
     """Run a bounded wait that nothing completes (test-only; see qbw_selftest_wait)."""
     L = load()
     _check(L.qbw_selftest_wait(which, limit_us, _stream(stream)), "qbw_selftest_wait")
+
+
+class Chain:
+    """A chain of dependent Q4_0 products run as one launch (qbw_chain_create /
+    qbw_chain_run / qbw_chain_destroy).  ``steps`` is a sequence of
+    ``(w, w_up, x, y, N, K)``: ``w_up`` None for ``y = W x``, else the up
+    matrix of a fused gate+up step; ``x`` bf16 [K]; ``y`` bf16 or fp32 [N].
+    The tensors must stay alive and in place while the chain exists."""
+
+    def __init__(self, steps):
+        L = load()
+        arr = (_ChainStep * len(steps))()
+        self._keep = []
+        for i, (w, w_up, x, y, N, K) in enumerate(steps):
+            self._keep += [w, w_up, x, y]
+            arr[i] = _ChainStep(w.data_ptr(), None if w_up is None else w_up.data_ptr(), x.data_ptr(),
+                                y.data_ptr(), _dtype_code(y), int(N), int(K))
+        h = ctypes.c_void_p()
+        _check(L.qbw_chain_create(arr, len(steps), ctypes.byref(h)), "qbw_chain_create")
+        self._h = h
+
+    def run(self, stream=None):
+        _check(load().qbw_chain_run(self._h, _stream(stream)), "qbw_chain_run")
+
+    def close(self):
+        if getattr(self, "_h", None):
+            _check(load().qbw_chain_destroy(self._h), "qbw_chain_destroy")
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
 
 
 def fault_read(clear: bool = True, stream=None) -> int:

@@ -6,6 +6,7 @@
 #include <cstdint>
 #include <cstring>
 #include <mutex>
+#include <vector>
 
 #include <cuda.h>
 #include <cudaTypedefs.h>
@@ -33,6 +34,12 @@ bool qmv_tc_supported(int nmat, int64_t N, int64_t K, int sm_count);
 cudaError_t launch_qmv_tc(int fmt, int nmat, int ntok, const CUtensorMap* tmap_w, const void* x, int x_bf16,
                           void* y, int y_bf16, int N, int K, int sm_count, unsigned int* fault, cudaStream_t stream);
 int qmm_tc_tile_rows();
+bool qmv_chain_step_supported(int nmat, int64_t N, int64_t K, int ctas);
+void qmv_chain_fill_step(ChainStepDesc* d, int nmat, int64_t N, int64_t K);
+int qmv_chain_ctas(int sm_count);
+size_t qmv_chain_share_bytes(int ctas);
+cudaError_t launch_qmv_chain(const ChainStepDesc* steps, int nsteps, int ctas, unsigned int* bar_count,
+                             unsigned long long* share, unsigned int* fault, cudaStream_t stream);
 int qmm_tc_group_k();
 
 namespace {
@@ -426,6 +433,18 @@ qbw_status qmv_common(int fmt, int nmat, const void* w0, const void* w1, const v
 }  // namespace
 }  // namespace qbw
 
+// A built chain: its step descriptors, grid-barrier counter and split-tile
+// scratch in device memory, on the device that was current at creation.
+struct qbw_chain_s {
+    int device = -1;
+    int nsteps = 0;
+    int ctas = 0;
+    qbw::ChainStepDesc* steps = nullptr;
+    unsigned int* bar = nullptr;          // [0] grid barrier counter, [1] abort flag
+    unsigned long long* share = nullptr;
+    unsigned int* fault = nullptr;
+};
+
 using namespace qbw;
 
 extern "C" {
@@ -570,6 +589,87 @@ qbw_status qembed_q8_0(const void* w, const int32_t* ids, int64_t n_ids, void* o
     if (st != QBW_OK) return st;
     cudaError_t e = launch_embed(kFmtQ8, static_cast<const uint8_t*>(w), ids, n_ids, N, K, out, ot == QBW_BF16,
                                  di->fault, di->sm_count, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? QBW_OK : QBW_ECUDA;
+}
+
+qbw_status qbw_chain_destroy(qbw_chain chain) {
+    if (!chain) return QBW_EINVAL;
+    int prev = -1;
+    cudaGetDevice(&prev);
+    bool ok = cudaSetDevice(chain->device) == cudaSuccess;
+    ok = (!chain->steps || cudaFree(chain->steps) == cudaSuccess) && ok;
+    ok = (!chain->bar || cudaFree(chain->bar) == cudaSuccess) && ok;
+    ok = (!chain->share || cudaFree(chain->share) == cudaSuccess) && ok;
+    if (prev >= 0) cudaSetDevice(prev);
+    delete chain;
+    return ok ? QBW_OK : QBW_ECUDA;
+}
+
+qbw_status qbw_chain_create(const qbw_chain_step* steps, int nsteps, qbw_chain* out) {
+    if (!out) return QBW_EINVAL;
+    *out = nullptr;
+    if (!steps || nsteps < 1 || nsteps > (1 << 20)) return QBW_EINVAL;
+    DeviceInfo* di = nullptr;
+    qbw_status st = device_info(&di);
+    if (st != QBW_OK) return st;
+    const int ctas = qmv_chain_ctas(di->sm_count);
+    if (ctas < 1) return QBW_ECUDA;
+    std::vector<ChainStepDesc> host((size_t)nsteps);
+    for (int i = 0; i < nsteps; ++i) {
+        const qbw_chain_step& c = steps[i];
+        if (!c.w || !c.x || !c.y) return QBW_EINVAL;
+        if (!valid_dtype(c.yt)) return QBW_EDTYPE;
+        const int nmat = c.w_up ? 2 : 1;
+        if (c.N < 1 || c.N > INT32_MAX || c.K < 256 || c.K % 256 != 0 || c.K > (int64_t(1) << 24) ||
+            !qmv_chain_step_supported(nmat, c.N, c.K, ctas))
+            return QBW_ESHAPE;
+        if ((uintptr_t)c.w % 16 || (uintptr_t)c.w_up % 16 || (uintptr_t)c.x % 16 || (uintptr_t)c.y % dtype_size(c.yt))
+            return QBW_EALIGN;
+        const size_t wbytes = (size_t)c.N * (size_t)weight_row_bytes(kFmtQ4, c.K);
+        const size_t ybytes = (size_t)c.N * dtype_size(c.yt);
+        if (overlaps(c.y, ybytes, c.x, (size_t)c.K * 2)) return QBW_EINVAL;
+        for (int j = 0; j < nsteps; ++j) {     // no step writes weights
+            const size_t wb = (size_t)steps[j].N * (size_t)weight_row_bytes(kFmtQ4, steps[j].K);
+            if ((steps[j].w && overlaps(c.y, ybytes, steps[j].w, wb)) ||
+                (steps[j].w_up && overlaps(c.y, ybytes, steps[j].w_up, wb)))
+                return QBW_EINVAL;
+        }
+        ChainStepDesc& d = host[(size_t)i];
+        std::memset(&d, 0, sizeof(d));
+        if (!encode_q4_tile_map(&d.tmap[0], c.w, c.N, c.K) ||
+            !encode_q4_tile_map(&d.tmap[1], nmat == 2 ? c.w_up : c.w, c.N, c.K))
+            return QBW_ECUDA;
+        qmv_chain_fill_step(&d, nmat, c.N, c.K);
+        d.x = c.x;
+        d.y = c.y;
+        d.y_bf16 = c.yt == QBW_BF16;
+    }
+    qbw_chain_s* ch = new qbw_chain_s;
+    cudaGetDevice(&ch->device);
+    ch->nsteps = nsteps;
+    ch->ctas = ctas;
+    ch->fault = di->fault;
+    const size_t share_bytes = qmv_chain_share_bytes(ctas);
+    if (cudaMalloc(&ch->steps, sizeof(ChainStepDesc) * (size_t)nsteps) != cudaSuccess ||
+        cudaMalloc(&ch->bar, 2 * sizeof(unsigned int)) != cudaSuccess ||
+        cudaMalloc(&ch->share, share_bytes) != cudaSuccess ||
+        cudaMemcpy(ch->steps, host.data(), sizeof(ChainStepDesc) * (size_t)nsteps, cudaMemcpyHostToDevice) !=
+            cudaSuccess ||
+        cudaMemset(ch->share, 0, share_bytes) != cudaSuccess || cudaMemset(ch->bar, 0, 2 * sizeof(unsigned int)) != cudaSuccess) {
+        qbw_chain_destroy(ch);
+        return QBW_ECUDA;
+    }
+    *out = ch;
+    return QBW_OK;
+}
+
+qbw_status qbw_chain_run(qbw_chain chain, void* stream) {
+    if (!chain) return QBW_EINVAL;
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess) return QBW_ECUDA;
+    if (dev != chain->device) return QBW_EINVAL;
+    cudaError_t e = launch_qmv_chain(chain->steps, chain->nsteps, chain->ctas, chain->bar, chain->share,
+                                     chain->fault, static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? QBW_OK : QBW_ECUDA;
 }
 

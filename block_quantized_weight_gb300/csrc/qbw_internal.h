@@ -17,6 +17,7 @@ enum FaultCode : unsigned int {
     kFaultBadIndex = 3,          // a token-table row index outside [0, N)
     kFaultShareWaitTimeout = 4,  // a split tile's share from another CTA never arrived
     kFaultPlan = 5,              // a launch plan exceeded a kernel's fixed capacity (internal)
+    kFaultGridWait = 6,          // a chain's CTAs waited in vain for the others between steps
 };
 
 enum : int { kFmtQ8 = 0, kFmtQ4 = 1, kFmtQ4K = 2 };
@@ -86,5 +87,16 @@ cudaError_t launch_embed(int fmt, const uint8_t* w, const int32_t* ids, int64_t 
 
 // Largest dynamic shared memory the streaming kernels may request.
 cudaError_t prepare_qmv_stream(int fmt, int nmat, int R, size_t smem);
+
+// One step of a chained product (qmv_chain.cu), in device memory (aligned as
+// its tensor maps require): y = W x (nmat = 1) or gelu_tanh(Wg x) * (Wu x)
+// (nmat = 2), Q4_0 weights, bf16 x.
+struct ChainStepDesc {
+    CUtensorMap tmap[2];      // the (gate) matrix and, for nmat = 2, the up matrix
+    const void* x;            // bf16 [K]
+    void* y;                  // [N], bf16 (y_bf16) or fp32
+    int32_t N, K, nmat, y_bf16;
+    int32_t tiles, groups, units, reserved;
+};
 
 }  // namespace qbw

@@ -52,6 +52,7 @@
 #include "qbw_device.cuh"
 #include "qbw_internal.h"
 #include "tc_common.cuh"
+#include "qmv_tc_common.cuh"
 
 namespace qbw {
 
@@ -65,318 +66,7 @@ __device__ unsigned long long g_qtc_share[kQtcSlots][kQtcMaxCtas][2][128];
 
 namespace {
 
-using namespace tc;
-
-constexpr int kTileRows = 128;
-constexpr int kGroupK = 256;
-constexpr int kGroupWords = 18;                  // 144 raw bytes per row per group, as 8-byte TMA words
-constexpr int kSets = 3;
-constexpr int kProducerWarp = 12;
-constexpr int kMmaWarp0 = 13;                    // set s's issuer: warp 13 + s
-constexpr int kThreads = 16 * 32;
-constexpr int kStages = 6;                       // a multiple of kSets: stage s always serves set s % 3
-constexpr int kN = 16;
-constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kACols = kGroupK / 2;         // 128 TMEM columns of A per set
-constexpr uint32_t kDCol = kSets * kACols;       // set s's two D buffers at columns 384 + 32 s (+ 16)
-constexpr uint32_t kRawStageBytes = kTileRows * 144;
-constexpr uint32_t kBBytes = kN * kGroupK * 2;   // 8 KB: 4 swizzle atoms of 16 rows x 128 B
-constexpr int kMaxLocalTiles = 8;
-constexpr uint32_t kBf16Minus136 = 0xC308C308u;
-constexpr uint32_t kBf16Minus128 = 0xC300C300u;
-
-constexpr uint32_t kOffB = kStages * kRawStageBytes;                          // 1024-aligned
-constexpr uint32_t kOffPart = kOffB + kSets * kBBytes;
-constexpr uint32_t kOffBar = kOffPart + kSets * kMaxLocalTiles * 2 * kTileRows * 4;
-constexpr int kBars = 2 * kStages + 4 * kSets + 1;
-constexpr uint32_t kOffSlot = kOffBar + 8 * kBars;
-// 8-bit form: the activations of up to kXtGroups K-groups, built once per CTA:
-// per group 32 chunks of 8 elements as {piece 0, piece 1} (16 bytes each),
-// and per group the 8 blocks' read-back factors c_j (fp32)
-constexpr int kXtGroups = 64;
-constexpr uint32_t kOffXt = (kOffSlot + 16 + 15) & ~15u;
-constexpr uint32_t kOffXc = kOffXt + kXtGroups * 32 * 16;
-constexpr uint32_t kSmemBytes = kOffXc + kXtGroups * 8 * 4;
-
-static_assert(kStages % kSets == 0, "stage s must serve set s % 3");
-static_assert(kOffB % 1024 == 0, "B operand needs 1024-byte alignment");
-
-struct QtcParams {
-    CUtensorMap tmap_w[2];   // Q4_0 rows as 8-byte words, box (18, 128); [1]: the up matrix of gate+up
-    const void* x;
-    void* y;
-    unsigned int* fault;
-    int32_t N, K;
-    int32_t tiles, groups, units;     // units = tiles x groups x matrices
-    int32_t slot;
-    int32_t x_bf16, y_bf16;
-};
-
-__device__ __forceinline__ uint32_t full_bar(uint32_t b0, int s) { return b0 + 8u * (uint32_t)s; }
-__device__ __forceinline__ uint32_t empty_bar(uint32_t b0, int s) { return b0 + 8u * (uint32_t)(kStages + s); }
-// afull(a, h): half h (K 128h .. 128h + 127) of set a's A and B operands is
-// written; aempty(a, h): the MMAs reading that half have completed.
-__device__ __forceinline__ uint32_t afull_bar(uint32_t b0, int a, int h) {
-    return b0 + 8u * (uint32_t)(2 * kStages + 2 * a + h);
-}
-__device__ __forceinline__ uint32_t aempty_bar(uint32_t b0, int a, int h) {
-    return b0 + 8u * (uint32_t)(2 * kStages + 2 * kSets + 2 * a + h);
-}
-__device__ __forceinline__ uint32_t done_bar(uint32_t b0) { return b0 + 8u * (uint32_t)(2 * kStages + 4 * kSets); }
-
-__device__ __forceinline__ void st_relaxed_u64(unsigned long long* p, unsigned long long v) {
-    asm volatile("st.relaxed.gpu.global.b64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
-}
-
-// per-set partial rows in shared memory: [set][local tile][matrix][row]
-__device__ __forceinline__ int part_at(int set, int lt, int m, int row) {
-    return ((set * kMaxLocalTiles + lt) * 2 + m) * kTileRows + row;
-}
-
-__device__ __forceinline__ int unit_begin(int c, int units, int ctas) {
-    return (int)(((int64_t)units * c) / ctas);
-}
-
-// the CTA whose unit range holds unit u
-__device__ __forceinline__ int owner_of(int u, int units, int ctas) {
-    int c = (int)(((int64_t)u * ctas) / units);
-    while (c + 1 < ctas && unit_begin(c + 1, units, ctas) <= u) ++c;
-    while (c > 0 && unit_begin(c, units, ctas) > u) --c;
-    return c;
-}
-
-// One Q4_0 block of the row's group (qs[0] at byte OFF of the words v[]) ->
-// 16 bf16x2 columns of exact codes c - 8 in K order: column t holds elements
-// 2t and 2t + 1 (t < 8) or 16 + 2(t - 8) and 17 + 2(t - 8).
-template <int OFF>
-__device__ __forceinline__ void codes_block(const uint32_t (&v)[36], uint32_t* col) {
-    const uint32_t m136 = kBf16Minus136;
-#pragma unroll
-    for (int j = 0; j < 16; j += 2) {
-        const int byte = OFF + j;
-        uint32_t lo, hi;
-        if ((byte & 3) == 0) nibble_pairs<0>(v[byte >> 2], lo, hi);
-        else nibble_pairs<2>(v[byte >> 2], lo, hi);
-        asm("add.rn.bf16x2 %0, %1, %2;" : "=r"(col[j >> 1]) : "r"(lo), "r"(m136));
-        asm("add.rn.bf16x2 %0, %1, %2;" : "=r"(col[8 + (j >> 1)]) : "r"(hi), "r"(m136));
-    }
-}
-
-// Q4_0: block pair P (blocks 2P, 2P + 1) of the group -> 32 columns of exact
-// c - 8.  Q4_K: 64-weight chunk P of the super-block -> 32 columns of exact
-// codes c (0..15): its 32 nibble bytes (words 4 + 8P .. 11 + 8P) hold weights
-// 64P + l in the low nibbles and 64P + 32 + l in the high nibbles, so the
-// byte pair (l, l + 1) gives columns 16 * 0 + l / 2 (low) and 16 + l / 2
-// (high) of the chunk, in K order.
-template <int FMT, int P>
-__device__ __forceinline__ void codes_pair(const uint32_t (&v)[36], uint32_t (&col)[32]) {
-    if constexpr (FMT == kFmtQ4) {
-        codes_block<36 * P + 2>(v, col);
-        codes_block<36 * P + 20>(v, col + 16);
-    } else {
-        const uint32_t m128 = kBf16Minus128;
-#pragma unroll
-        for (int wd = 0; wd < 8; ++wd) {
-            const uint32_t w = v[4 + 8 * P + wd];
-            uint32_t lo, hi;
-            nibble_pairs<0>(w, lo, hi);                     // bytes 4wd, 4wd + 1
-            asm("add.rn.bf16x2 %0, %1, %2;" : "=r"(col[2 * wd]) : "r"(lo), "r"(m128));
-            asm("add.rn.bf16x2 %0, %1, %2;" : "=r"(col[16 + 2 * wd]) : "r"(hi), "r"(m128));
-            nibble_pairs<2>(w, lo, hi);                     // bytes 4wd + 2, 4wd + 3
-            asm("add.rn.bf16x2 %0, %1, %2;" : "=r"(col[2 * wd + 1]) : "r"(lo), "r"(m128));
-            asm("add.rn.bf16x2 %0, %1, %2;" : "=r"(col[16 + 2 * wd + 1]) : "r"(hi), "r"(m128));
-        }
-    }
-}
-
-// 8-bit form of block pair P (blocks 2P, 2P + 1) of a Q4_0 group -> 32 TMEM
-// columns of e4m3 bytes, 4 per column in K order.  An e4m3 byte b = 0..15 is
-// exactly b * 2^-9 (the subnormals and the first binade share one spacing), so
-// code c - 8 = (c & 7) - 8 [c < 8] splits into two exact 8-bit operands that
-// are both 0 where c = 8: block j's K-step 2j holds c & 7 and K-step 2j + 1
-// holds 8 [bit 3 of c clear] (the byte 0x08), against B columns of +x and -x.
-// Each K-step is 8 columns: the low nibbles of qs[0..15] (elements 0..15),
-// then their high nibbles (elements 16..31).  Block 2P's qs start at byte
-// 36P + 2 of the group row (two bytes into a word), block 2P + 1's at word
-// 9P + 5.
-template <int P>
-__device__ __forceinline__ void codes_pair_e4m3(const uint32_t (&v)[36], uint32_t (&col)[32]) {
-#pragma unroll
-    for (int t = 0; t < 4; ++t) {
-        const uint32_t w = __funnelshift_r(v[9 * P + t], v[9 * P + t + 1], 16);
-        const uint32_t h = __funnelshift_r(v[9 * P + t], v[9 * P + t + 1], 20);
-        col[t] = w & 0x07070707u;
-        col[4 + t] = h & 0x07070707u;
-        col[8 + t] = ~w & 0x08080808u;
-        col[12 + t] = ~h & 0x08080808u;
-    }
-#pragma unroll
-    for (int t = 0; t < 4; ++t) {
-        const uint32_t w = v[9 * P + 5 + t];
-        const uint32_t h = w >> 4;
-        col[16 + t] = w & 0x07070707u;
-        col[20 + t] = h & 0x07070707u;
-        col[24 + t] = ~w & 0x08080808u;
-        col[28 + t] = ~h & 0x08080808u;
-    }
-}
-
-// fp16 scales of blocks 2P (low half) and 2P + 1 (high half) of the group:
-// block 2P's in the low half of word 9P, block 2P + 1's in the high half of
-// word 9P + 4.
-__device__ __forceinline__ uint32_t scale_pair(const uint32_t (&v)[36], int P) {
-    uint32_t r;
-    asm("prmt.b32 %0, %1, %2, 0x7610;" : "=r"(r) : "r"(v[9 * P]), "r"(v[9 * P + 4]));
-    return r;
-}
-
-__device__ __forceinline__ float2 half2_to_float2(uint32_t h) {
-    float2 f;
-    asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %2;\n\tcvt.f32.f16 %0, lo;\n\tcvt.f32.f16 %1, hi;\n\t}"
-        : "=f"(f.x), "=f"(f.y)
-        : "r"(h));
-    return f;
-}
-
-// Q4_K: the sub-block sums of one unit, r0 = sum_j d sc_j (D[2j] + D[2j + 1])
-// - dmin m_j sx_j, j = 0..7 in order: dd[] holds the super-block's first 16
-// bytes (fp16 d and dmin, then the 12 six-bit scale bytes), sx the lane's
-// sub-block sum of x (lanes 4j .. 4j + 3 hold sub-block j's).
-__device__ __forceinline__ float unit_dot_q4k(const uint32_t (&dv)[16], const uint32_t (&dd)[4], float sx) {
-    const float2 dm = half2_to_float2(dd[0]);
-    const uint32_t s03 = dd[1], s47 = dd[2], s8b = dd[3];       // scale bytes 0..3, 4..7, 8..11
-    float r = 0.f;
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-        uint32_t sc, m;
-        if (j < 4) {
-            sc = (s03 >> (8 * j)) & 63u;
-            m = (s47 >> (8 * j)) & 63u;
-        } else {
-            const uint32_t lo = (s8b >> (8 * (j - 4))) & 0xFFu;
-            sc = (lo & 15u) | (((s03 >> (8 * (j - 4) + 6)) & 3u) << 4);
-            m = (lo >> 4) | (((s47 >> (8 * (j - 4) + 6)) & 3u) << 4);
-        }
-        const float sxj = __shfl_sync(0xffffffffu, sx, 4 * j);
-        r = fmaf(dm.x * (float)sc, __uint_as_float(dv[2 * j]) + __uint_as_float(dv[2 * j + 1]), r);
-        r = fmaf(-dm.y * (float)m, sxj, r);
-    }
-    return r;
-}
-
-// One token (NTOK = 1): r0 = sum_j d_j (D[2j] + D[2j + 1]), the x_hi and x_lo
-// columns of block j.  Two tokens: r0 = sum_j d_j D[2j], r1 = sum_j d_j
-// D[2j + 1].  j = 0..7 in order.
-template <int NTOK>
-__device__ __forceinline__ void unit_dot(const uint32_t (&dv)[16], const uint32_t (&dd)[4], float& r0, float& r1) {
-    r0 = 0.f;
-    r1 = 0.f;
-#pragma unroll
-    for (int p = 0; p < 4; ++p) {
-        const float2 d = half2_to_float2(dd[p]);
-        if constexpr (NTOK == 1) {
-            r0 = fmaf(d.x, __uint_as_float(dv[4 * p]) + __uint_as_float(dv[4 * p + 1]), r0);
-            r0 = fmaf(d.y, __uint_as_float(dv[4 * p + 2]) + __uint_as_float(dv[4 * p + 3]), r0);
-        } else {
-            r0 = fmaf(d.x, __uint_as_float(dv[4 * p]), r0);
-            r1 = fmaf(d.x, __uint_as_float(dv[4 * p + 1]), r1);
-            r0 = fmaf(d.y, __uint_as_float(dv[4 * p + 2]), r0);
-            r1 = fmaf(d.y, __uint_as_float(dv[4 * p + 3]), r1);
-        }
-    }
-}
-
-// 8-bit form, one token: r0 = sum_j (d_j c_j) (D[2j] + D[2j + 1]), j = 0..7 in
-// order, where c_j = 2^9 / s_j undoes the e4m3 code scale 2^-9 and block j's
-// activation scale s_j (c[0..7] = c_j).
-__device__ __forceinline__ float unit_dot_e4m3(const uint32_t (&dv)[16], const uint32_t (&dd)[4], const float (&c)[8]) {
-    float r = 0.f;
-#pragma unroll
-    for (int p = 0; p < 4; ++p) {
-        const float2 d = half2_to_float2(dd[p]);
-        r = fmaf(d.x * c[2 * p], __uint_as_float(dv[4 * p]) + __uint_as_float(dv[4 * p + 1]), r);
-        r = fmaf(d.y * c[2 * p + 1], __uint_as_float(dv[4 * p + 2]) + __uint_as_float(dv[4 * p + 3]), r);
-    }
-    return r;
-}
-
-__device__ __forceinline__ uint32_t umax16x2(uint32_t a, uint32_t b) {
-    uint32_t r;
-    asm("max.u16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
-    return r;
-}
-
-// two fp32 -> e4m3 (round to nearest, saturating), lo in the low byte
-__device__ __forceinline__ uint32_t e4m3x2(float lo, float hi) {
-    unsigned short r;
-    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
-    return (uint32_t)r;
-}
-
-__device__ __forceinline__ void sts64(uint32_t addr, uint2 v) {
-    asm volatile("st.shared.v2.b32 [%0], {%1, %2};" ::"r"(addr), "r"(v.x), "r"(v.y) : "memory");
-}
-
-__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
-    uint32_t r;
-    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
-    return r;
-}
-
-__device__ __forceinline__ float bf16_lo_to_float(uint32_t w) { return __uint_as_float(w << 16); }
-__device__ __forceinline__ float bf16_hi_to_float(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
-
-__device__ __forceinline__ void sts128(uint32_t addr, uint4 v) {
-    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
-                 : "memory");
-}
-
-// Byte offset, in the B operand (K-major, 128-byte swizzle, 16 rows), of the
-// 16-byte chunk holding elements 8c .. 8c + 7 of swizzle atom a, row n.
-__device__ __forceinline__ uint32_t b_chunk(int a, int n, int c) {
-    return (uint32_t)(a * 2048 + (n >> 3) * 1024 + (n & 7) * 128 + ((c ^ (n & 7)) << 4));
-}
-
-// 8-bit form: the read-back factors c_j of the group in table slot sl
-__device__ __forceinline__ void table_c(uint32_t sbase, int sl, float (&c)[8]) {
-    const uint4 a = lds128(sbase + kOffXc + (uint32_t)sl * 32u), b = lds128(sbase + kOffXc + (uint32_t)sl * 32u + 16u);
-    c[0] = __uint_as_float(a.x);
-    c[1] = __uint_as_float(a.y);
-    c[2] = __uint_as_float(a.z);
-    c[3] = __uint_as_float(a.w);
-    c[4] = __uint_as_float(b.x);
-    c[5] = __uint_as_float(b.y);
-    c[6] = __uint_as_float(b.z);
-    c[7] = __uint_as_float(b.w);
-}
-
-// Byte offset, in the B operand, of byte `byte` of swizzle atom a, row n
-// (the 8-bit form: 128 K-elements per atom row).
-__device__ __forceinline__ uint32_t b_byte(int a, int n, uint32_t byte) {
-    return (uint32_t)(a * 2048 + (n >> 3) * 1024 + (n & 7) * 128) + ((((byte >> 4) ^ (uint32_t)(n & 7)) << 4) |
-                                                                       (byte & 15u));
-}
-
-// Eight bf16 activations (x[2e] in the low half of word e), already scaled by
-// the power of two sc, as two e4m3 pieces whose sum is exact: p0 keeps the
-// sign, exponent and top three mantissa bits (fp32 bits & 0xFFF00000), p1
-// the remaining four bits (bf16 has seven).  Both are exact in e4m3 while the
-// element is at least 2^-2 after scaling; below that e4m3's subnormal spacing
-// of 2^-9 rounds them.
-__device__ __forceinline__ void split_e4m3(uint4 xr, float sc, uint2& p0, uint2& p1) {
-    const uint32_t w[4] = {xr.x, xr.y, xr.z, xr.w};
-    uint32_t h0[4], h1[4];
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-        const float lo = __uint_as_float(w[e] << 16) * sc, hi = __uint_as_float(w[e] & 0xFFFF0000u) * sc;
-        const float lo0 = __uint_as_float(__float_as_uint(lo) & 0xFFF00000u);
-        const float hi0 = __uint_as_float(__float_as_uint(hi) & 0xFFF00000u);
-        h0[e] = e4m3x2(lo0, hi0);
-        h1[e] = e4m3x2(lo - lo0, hi - hi0);
-    }
-    p0 = make_uint2(h0[0] | (h0[1] << 16), h0[2] | (h0[3] << 16));
-    p1 = make_uint2(h1[0] | (h1[1] << 16), h1[2] | (h1[3] << 16));
-}
+using namespace qtc;
 
 // NMAT = 1: y = W x.  NMAT = 2: out = gelu_tanh(Wg x) * (Wu x); the units of a
 // (tile, group) are its gate and up halves, in that order (measured faster
@@ -534,38 +224,15 @@ __device__ __forceinline__ void qmv_tc_body(const QtcParams& p) {
         const uint32_t f8_n1 = bbuf + b_byte(bj >> 1, 2 * bj + 1, bo + 32u);
         const int bhalf = xl >> 4;
         const int row = 32 * q + lane;
-        // 8-bit form: the table of the K-groups g of this CTA's units, group g
-        // in slot (g - xg0) mod G.  Each chunk of 8 elements is scaled by its
-        // block's s_j = 2^(es - 127), which takes the block's largest |x| into
-        // [2^7, 2^8) (e4m3 reaches 448); es = 261 - E for the bf16 biased
-        // exponent E of that maximum, kept where s_j and c_j = 2^9 / s_j are
-        // normal fp32.  Built by the twelve dequantizing warps; the host
-        // launches this form only where the table holds every group needed.
+        // 8-bit form: the activation table of the K-groups g of this CTA's
+        // units, group g in slot (g - xg0) mod G, built by the twelve
+        // dequantizing warps; the host launches this form only where the table
+        // holds every group needed.
         const int xg0 = (u0 / NMAT) % G;
         if constexpr (F8) {
             const int cnt = n > 0 ? min(G, (u1 - 1) / NMAT - u0 / NMAT + 1) : 0;
             if (cnt > kXtGroups) record_fault(p.fault, kFaultPlan);
-            const int nch = min(cnt, kXtGroups) * 32;
-            for (int c0 = warp * 32; c0 < nch; c0 += kProducerWarp * 32) {
-                const int c = c0 + lane, sl = c >> 5;
-                int g = xg0 + sl;
-                if (g >= G) g -= G;
-                const uint4 xr = __ldg(reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p.x) +
-                                                                      (size_t)g * kGroupK + 8 * (c & 31)));
-                const uint32_t m2 = umax16x2(umax16x2(xr.x & 0x7FFF7FFFu, xr.y & 0x7FFF7FFFu),
-                                             umax16x2(xr.z & 0x7FFF7FFFu, xr.w & 0x7FFF7FFFu));
-                uint32_t mx = max(m2 & 0xFFFFu, m2 >> 16);
-                mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
-                mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-                const int es = min(max(261 - (int)(mx >> 7), 9), 253);
-                uint2 q0, q1;
-                split_e4m3(xr, __uint_as_float((uint32_t)es << 23), q0, q1);
-                sts128(sbase + kOffXt + (uint32_t)c * 16u, make_uint4(q0.x, q0.y, q1.x, q1.y));
-                if ((lane & 3) == 0)
-                    asm volatile("st.shared.b32 [%0], %1;" ::"r"(sbase + kOffXc + (uint32_t)(c >> 2) * 4u),
-                                 "r"((uint32_t)(263 - es) << 23)
-                                 : "memory");
-            }
+            build_x_table<false>(sbase, p.x, xg0, G, min(cnt, kXtGroups), warp, lane, kProducerWarp);
             asm volatile("bar.sync 2, %0;" ::"n"(kProducerWarp * 32) : "memory");
         }
         bool counted = !contrib0;

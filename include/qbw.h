@@ -262,6 +262,63 @@ qbw_status qembed_q8_0(const void *w, const int32_t *ids, int64_t n_ids, void *o
                        int64_t K, void *stream);
 
 /*
+ * Chained products -- a sequence of dependent Q4_0 matrix-vector products in
+ * one launch, such as one token's decode weight sweep (per layer q|k|v, o,
+ * gate+up, down, each step's activations the previous step's output).  The
+ * pages count the GPU round trips per token and chain the FFN's dispatches
+ * on the GPU to cut them, against one command buffer per token as the
+ * reference point (SafeC Gemma 4 design notes, "Further optimization: QKV
+ * projection fusion, fully GPU-chained FFN").
+ *
+ * Defined by the same arithmetic as qmv_q4_0 / qmv_gateup_q4_0 with M = 1 and
+ * bf16 activations: step s computes y_s = W_s x_s, or, when w_up is given,
+ * y_s = gelu_tanh(W_s x_s) * (W_up,s x_s), with the weights of the Q4_0
+ * layout above.  Steps run in order and step s sees
+ * the outputs of every earlier step, so x_s may be (part of) an earlier y.
+ * The results match the separate calls within the same bound (2e-3 of the
+ * row's sum |w x|, plus the bf16 output rounding).
+ *
+ * qbw_chain_step (one step; the caller keeps every buffer alive and in place
+ * while the chain exists):
+ *   w    : Q4_0 matrix, N rows of K/32 blocks, 16-byte aligned (QBW_EALIGN)
+ *   w_up : NULL for y = W x; else the up matrix, same shape and alignment
+ *   x    : bf16 [K], 16-byte aligned; may not overlap this step's y (QBW_EINVAL)
+ *   y    : [N] of yt (QBW_BF16 or QBW_F32, else QBW_EDTYPE), aligned to yt;
+ *          may not overlap any step's weights (QBW_EINVAL)
+ *   N    : 1 .. 2^31-1;  K: 256 .. 2^24, K % 256 == 0 (else QBW_ESHAPE); a
+ *          step whose unit split exceeds the kernel's per-CTA capacity (far
+ *          beyond the model shapes) also gives QBW_ESHAPE
+ *
+ * qbw_chain_create -- validate nsteps >= 1 steps (QBW_EINVAL for a null or
+ *   empty list), encode their weight descriptors and copy them, with a
+ *   barrier counter and split-tile scratch, to memory it allocates on the
+ *   current device (QBW_ECUDA if that fails).  *out receives the chain,
+ *   owned by the caller until qbw_chain_destroy.
+ * qbw_chain_run -- enqueue the whole chain on `stream` (a CUDA stream of the
+ *   chain's device, else QBW_EINVAL): a counter reset and one cooperative
+ *   launch with one CTA per SM, so it may be captured in a CUDA graph.  Runs
+ *   of one chain must not overlap in time (they share its counter and
+ *   scratch).  Device-side problems set fault-word bits (see qbw_fault_read).
+ * qbw_chain_destroy -- free the chain's device memory (after its last run has
+ *   completed) and the chain.
+ */
+typedef struct qbw_chain_step {
+    const void *w;
+    const void *w_up;
+    const void *x;
+    void *y;
+    qbw_dtype yt;
+    int64_t N;
+    int64_t K;
+} qbw_chain_step;
+
+typedef struct qbw_chain_s *qbw_chain;
+
+qbw_status qbw_chain_create(const qbw_chain_step *steps, int nsteps, qbw_chain *out);
+qbw_status qbw_chain_run(qbw_chain chain, void *stream);
+qbw_status qbw_chain_destroy(qbw_chain chain);
+
+/*
  * qbw_fault_read -- read the library's device fault word for the current
  * device.  Kernels report problems found while they run by setting bit
  * (1 << c) of this word, then return early (outputs of that call are then
@@ -273,6 +330,8 @@ qbw_status qembed_q8_0(const void *w, const int32_t *ids, int64_t n_ids, void *o
  *          of a 128-row tile split between CTAs
  *   c = 5  internal: a launch plan exceeded a kernel's fixed capacity (the
  *          host-side planning never allows it; seen only after a library bug)
+ *   c = 6  qbw_chain_run: a CTA waited in vain (about two seconds) for the
+ *          other CTAs at the barrier between two steps
  * Synchronizes `stream`, stores the word in *code and, if clear != 0, resets
  * it to zero.
  */

@@ -137,3 +137,16 @@ def test_dequant_validation(lib):
         assert f(P(ADDR), P(ADDR + (1 << 30)), 4, 40, None) == 2
         assert f(P(ADDR), P(ADDR + (1 << 30) + 2), 4, 64, None) == 4
         assert f(P(ADDR), P(ADDR + 8), 4, 64, None) == 1
+
+
+def test_chain_calls_reject_null_arguments_before_touching_a_device(lib):
+    import ctypes
+    import block_quantized_weight_gb300 as qbw
+    L = qbw.load()
+    h = ctypes.c_void_p()
+    assert L.qbw_chain_create(None, 1, ctypes.byref(h)) == 1          # QBW_EINVAL
+    assert L.qbw_chain_create(None, 0, ctypes.byref(h)) == 1
+    assert not h.value
+    assert L.qbw_chain_create(None, 1, None) == 1
+    assert L.qbw_chain_run(None, None) == 1
+    assert L.qbw_chain_destroy(None) == 1
