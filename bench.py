@@ -110,8 +110,9 @@ def load_peaks():
 # Sources whose change voids a kernel's profiled DRAM traffic (device code and
 # the host-side launch plan).
 KERNEL_SOURCES = {
-    "qmv_q4_0": ("qbw_device.cuh", "qbw_internal.h", "tc_common.cuh", "qmv_tc.cu", "api.cu"),
-    "qmv_gateup_q4_0": ("qbw_device.cuh", "qbw_internal.h", "tc_common.cuh", "qmv_tc.cu", "api.cu"),
+    "qmv_q4_0": ("qbw_device.cuh", "qbw_internal.h", "tc_common.cuh", "qmv_tc_common.cuh", "qmv_tc.cu", "api.cu"),
+    "qmv_gateup_q4_0": ("qbw_device.cuh", "qbw_internal.h", "tc_common.cuh", "qmv_tc_common.cuh", "qmv_tc.cu",
+                        "api.cu"),
 }
 TRAFFIC_SUMMARY = os.path.join(ROOT, "profiles", "qmv_sweep_layer_traffic.txt")
 
@@ -554,6 +555,7 @@ def gpu_arm(args):
         return
 
     supp = {} if args.no_kernels else supplementary_kernels(torch, qbw, hbm_peak)
+    chained = None if args.no_kernels else sweep_as_one_launch(torch, qbw, sweep, x0_dev, stream, graph, step_bytes)
     cpu = None
     if not args.no_cpu and ws == 1:
         v, dt, nbytes, rows = cpu_baseline(sweep.layer0_host, x0, args.cpu_seconds)
@@ -579,6 +581,7 @@ def gpu_arm(args):
         "clocks": clocks.summary(t_start - 0.05, t_end + 0.05),
         "cpu_baseline": cpu,
         "kernels": supp,
+        "sweep_as_one_launch": chained,
         "per_kernel_in_sweep": {k: {"launches": v["launches"], "ms": round(v["ms"], 4),
                                     "GB_per_s": round(v["bytes"] / (v["ms"] * 1e-3) / 1e9, 1)}
                                 for k, v in per_kernel.items()},
@@ -587,6 +590,38 @@ def gpu_arm(args):
     print(json.dumps(line), flush=True)
     if ws > 1:
         torch.distributed.destroy_process_group()
+
+
+def sweep_as_one_launch(torch, qbw, sweep, x0_dev, stream, graph, step_bytes, replays=50):
+    """The same token as one chained launch (qbw_chain_run over the sweep's
+    240 steps and buffers), against the graph of 240 launches: its time and
+    whether its final activation equals the graph's bit for bit."""
+    steps = []
+    for L in range(sweep.layers):
+        steps += [(sweep.qkv_view(L), None, sweep.h, sweep.qkv, QDIM + 2 * KVDIM, HIDDEN),
+                  (sweep.view(L, "o"), None, sweep.q, sweep.o, HIDDEN, QDIM),
+                  (sweep.view(L, "gate"), sweep.view(L, "up"), sweep.o, sweep.a, FFN, HIDDEN),
+                  (sweep.view(L, "down"), None, sweep.a, sweep.h, HIDDEN, FFN)]
+    chain = qbw.Chain(steps)
+    try:
+        with torch.cuda.stream(stream):
+            sweep.h.copy_(x0_dev)
+            graph.replay()
+            h_graph = sweep.h.clone()
+            sweep.h.copy_(x0_dev)
+            chain.run(stream)
+        torch.cuda.synchronize()
+        same = bool(torch.equal(h_graph.view(torch.int16), sweep.h.view(torch.int16)))
+        g = capture(torch, lambda: chain.run(torch.cuda.current_stream()), stream)
+        time_graph(torch, g, 3, stream)
+        ms = time_graph(torch, g, replays, stream) / replays
+        assert qbw.fault_read(clear=True, stream=stream) == 0, "the chained launch recorded a fault"
+    finally:
+        chain.close()
+    return {"ms_per_step": round(ms, 4), "GB_per_s": round(step_bytes / (ms * 1e-3) / 1e9, 1),
+            "tok_per_s": round(1e3 / ms, 2), "final_activation_bit_identical_to_graph": same,
+            "launches_per_step": 1,
+            "what": "qbw_chain_run: the 240 steps as one cooperative launch with a grid barrier between steps"}
 
 
 def profile_case(args):
