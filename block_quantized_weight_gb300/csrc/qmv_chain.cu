@@ -262,7 +262,7 @@ __global__ void __launch_bounds__(kThreads, 1) qmv_chain_kernel(const __grid_con
             {
                 const int cnt = n > 0 ? min(G, (r.u1 - 1) / nmat - u0 / nmat + 1) : 0;
                 if (cnt > kXtGroups) record_fault(p.fault, kFaultPlan);
-                build_x_table<true>(sbase, st.x, xg0, G, min(cnt, kXtGroups), warp, lane, kProducerWarp);
+                build_x_table<true, 2>(sbase, st.x, xg0, G, min(cnt, kXtGroups), warp, lane, kProducerWarp);
             }
             dequant_sync();     // table written; part[] and qcount clear
             bool counted = !r.contrib0;

@@ -74,13 +74,16 @@ using namespace qtc;
 // NMAT = 1 and bf16 activations): Y[m] = W X[m] for two token rows, which take
 // the two B columns of each block that x_hi and x_lo take for one token.
 // Each row keeps NCH = NMAT * NTOK sums (channels).  F8: the 8-bit form of
-// the operands (Q4_0, one token, bf16 activations; see codes_pair_e4m3).
-template <int FMT, int NMAT, int NTOK, bool F8>
+// the operands (Q4_0, one token; see codes_pair_e4m3), with F8 e4m3 pieces
+// per activation: 2 for bf16 x, 3 for fp32 x (the third pieces in a second B,
+// one more MMA per K-step on the same A, into the D column of the second
+// piece).  F8 = 0: the bf16-code form.
+template <int FMT, int NMAT, int NTOK, int F8>
 __device__ __forceinline__ void qmv_tc_body(const QtcParams& p) {
     constexpr int NCH = NMAT * NTOK;
     static_assert(NCH <= 2, "at most two sums per row");
     static_assert(FMT == kFmtQ4 || (NMAT == 1 && NTOK == 1), "Q4_K: one matrix, one token");
-    static_assert(!F8 || (FMT == kFmtQ4 && NTOK == 1), "8-bit form: Q4_0, one token");
+    static_assert(F8 == 0 || ((F8 == 2 || F8 == 3) && FMT == kFmtQ4 && NTOK == 1), "8-bit form: Q4_0, one token");
     extern __shared__ __align__(1024) uint8_t smem[];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int ctas = (int)gridDim.x, cta = (int)blockIdx.x;
@@ -102,7 +105,7 @@ __device__ __forceinline__ void qmv_tc_body(const QtcParams& p) {
 
     // zero B operands (only their fixed activation positions are ever written
     // again) and the per-set partial rows
-    for (int i = threadIdx.x; i < (int)(kSets * kBBytes / 16); i += kThreads)
+    for (int i = threadIdx.x; i < (int)(2 * kSets * kBBytes / 16); i += kThreads)     // B and B2
         sts128(sbase + kOffB + 16u * (uint32_t)i, make_uint4(0u, 0u, 0u, 0u));
     for (int i = threadIdx.x; i < kSets * kMaxLocalTiles * 2 * kTileRows; i += kThreads) part[i] = 0.f;
 
@@ -163,6 +166,7 @@ __device__ __forceinline__ void qmv_tc_body(const QtcParams& p) {
             const uint32_t idesc = F8 ? idesc_e4m3(kTileRows, kN) : idesc_bf16(kTileRows, kN);
             const uint32_t a_tmem = tmem + (uint32_t)set * kACols;
             const uint64_t b0 = sw128_desc(sbase + kOffB + (uint32_t)set * kBBytes);
+            const uint64_t b20 = sw128_desc(sbase + kOffB2 + (uint32_t)set * kBBytes);
             uint32_t phase = 0;
             for (int i = set; i < n; i += kSets) {
                 // the set's k-th unit accumulates into D buffer k % 2
@@ -173,9 +177,13 @@ __device__ __forceinline__ void qmv_tc_body(const QtcParams& p) {
                 tc_fence_after();
 #pragma unroll
                 for (int k = 0; k < 8; ++k) {
-                    const uint64_t bd = b0 + (uint64_t)((k >> 2) * 128 + (k & 3) * 2);
-                    if constexpr (F8) tc_mma_f8(d_tmem, a_tmem + 8u * (uint32_t)k, bd, idesc, k > 0 ? 1u : 0u);
-                    else tc_mma(d_tmem, a_tmem + 8u * (uint32_t)k, bd, idesc, k > 0 ? 1u : 0u);
+                    const uint64_t bo = (uint64_t)((k >> 2) * 128 + (k & 3) * 2);
+                    if constexpr (F8) {
+                        tc_mma_f8(d_tmem, a_tmem + 8u * (uint32_t)k, b0 + bo, idesc, k > 0 ? 1u : 0u);
+                        if constexpr (F8 == 3) tc_mma_f8(d_tmem, a_tmem + 8u * (uint32_t)k, b20 + bo, idesc, 1u);
+                    } else {
+                        tc_mma(d_tmem, a_tmem + 8u * (uint32_t)k, b0 + bo, idesc, k > 0 ? 1u : 0u);
+                    }
                 }
                 tc_commit(aempty_bar(bar0, set, 0));
                 ok = mbar_wait_bounded(afull_bar(bar0, set, 1), phase, p.fault, kFaultMmaWaitTimeout);
@@ -183,9 +191,13 @@ __device__ __forceinline__ void qmv_tc_body(const QtcParams& p) {
                 tc_fence_after();
 #pragma unroll
                 for (int k = 8; k < 16; ++k) {
-                    const uint64_t bd = b0 + (uint64_t)((k >> 2) * 128 + (k & 3) * 2);
-                    if constexpr (F8) tc_mma_f8(d_tmem, a_tmem + 8u * (uint32_t)k, bd, idesc, 1u);
-                    else tc_mma(d_tmem, a_tmem + 8u * (uint32_t)k, bd, idesc, 1u);
+                    const uint64_t bo = (uint64_t)((k >> 2) * 128 + (k & 3) * 2);
+                    if constexpr (F8) {
+                        tc_mma_f8(d_tmem, a_tmem + 8u * (uint32_t)k, b0 + bo, idesc, 1u);
+                        if constexpr (F8 == 3) tc_mma_f8(d_tmem, a_tmem + 8u * (uint32_t)k, b20 + bo, idesc, 1u);
+                    } else {
+                        tc_mma(d_tmem, a_tmem + 8u * (uint32_t)k, b0 + bo, idesc, 1u);
+                    }
                 }
                 tc_commit(aempty_bar(bar0, set, 1));
                 phase ^= 1u;
@@ -232,7 +244,7 @@ __device__ __forceinline__ void qmv_tc_body(const QtcParams& p) {
         if constexpr (F8) {
             const int cnt = n > 0 ? min(G, (u1 - 1) / NMAT - u0 / NMAT + 1) : 0;
             if (cnt > kXtGroups) record_fault(p.fault, kFaultPlan);
-            build_x_table<false>(sbase, p.x, xg0, G, min(cnt, kXtGroups), warp, lane, kProducerWarp);
+            build_x_table<false, F8>(sbase, p.x, xg0, G, min(cnt, kXtGroups), warp, lane, kProducerWarp);
             asm volatile("bar.sync 2, %0;" ::"n"(kProducerWarp * 32) : "memory");
         }
         bool counted = !contrib0;
@@ -374,17 +386,22 @@ __device__ __forceinline__ void qmv_tc_body(const QtcParams& p) {
                 cur_sx += __shfl_xor_sync(0xffffffffu, cur_sx, 2);
             }
             // 8-bit form: this unit's group in the table; the B-writing lanes'
-            // two pieces of their slot
+            // pieces of their slot
             int cur_sl = 0;
-            uint2 bp0 = make_uint2(0u, 0u), bp1 = bp0;
+            uint2 bp0 = make_uint2(0u, 0u), bp1 = bp0, bp2 = bp0;
             if constexpr (F8) {
                 cur_sl = g - xg0;
                 if (cur_sl < 0) cur_sl += G;
                 if (cur_sl >= kXtGroups) cur_sl = 0;       // never: the host checks the table size
                 if (bwriter) {
-                    const uint4 tq = lds128(sbase + kOffXt + (uint32_t)(cur_sl * 32 + xl) * 16u);
+                    const uint32_t ch = (uint32_t)(cur_sl * 32 + xl);
+                    const uint4 tq = lds128(sbase + kOffXt + ch * 16u);
                     bp0 = make_uint2(tq.x, tq.y);
                     bp1 = make_uint2(tq.z, tq.w);
+                    if constexpr (F8 == 3)
+                        asm volatile("ld.shared.v2.b32 {%0, %1}, [%2];"
+                                     : "=r"(bp2.x), "=r"(bp2.y)
+                                     : "r"(sbase + kOffXt2 + ch * 8u));
                 }
             }
             const uint32_t prev = (uint32_t)(k - 1) & 1u;     // completion parity of the previous unit
@@ -405,6 +422,10 @@ __device__ __forceinline__ void qmv_tc_body(const QtcParams& p) {
                     sts64(f8_p1, bp1);
                     sts64(f8_n0, make_uint2(bp0.x ^ 0x80808080u, bp0.y ^ 0x80808080u));
                     sts64(f8_n1, make_uint2(bp1.x ^ 0x80808080u, bp1.y ^ 0x80808080u));
+                    if constexpr (F8 == 3) {     // third pieces: B2, the second piece's rows
+                        sts64(f8_p1 + (kOffB2 - kOffB), bp2);
+                        sts64(f8_n1 + (kOffB2 - kOffB), make_uint2(bp2.x ^ 0x80808080u, bp2.y ^ 0x80808080u));
+                    }
                 } else {
                     sts128(b_hi, bhi);
                     sts128(b_lo, blo);
@@ -437,6 +458,10 @@ __device__ __forceinline__ void qmv_tc_body(const QtcParams& p) {
                     sts64(f8_p1, bp1);
                     sts64(f8_n0, make_uint2(bp0.x ^ 0x80808080u, bp0.y ^ 0x80808080u));
                     sts64(f8_n1, make_uint2(bp1.x ^ 0x80808080u, bp1.y ^ 0x80808080u));
+                    if constexpr (F8 == 3) {     // third pieces: B2, the second piece's rows
+                        sts64(f8_p1 + (kOffB2 - kOffB), bp2);
+                        sts64(f8_n1 + (kOffB2 - kOffB), make_uint2(bp2.x ^ 0x80808080u, bp2.y ^ 0x80808080u));
+                    }
                 } else {
                     sts128(b_hi, bhi);
                     sts128(b_lo, blo);
@@ -559,17 +584,17 @@ __device__ __forceinline__ void qmv_tc_body(const QtcParams& p) {
 
 template <int NMAT, int NTOK>
 __global__ void __launch_bounds__(kThreads, 1) qmv_q4_0_tc_kernel(const __grid_constant__ QtcParams p) {
-    qmv_tc_body<kFmtQ4, NMAT, NTOK, false>(p);
+    qmv_tc_body<kFmtQ4, NMAT, NTOK, 0>(p);
 }
 
-// bf16 activations, one token: the 8-bit operand form
-template <int NMAT>
+// one token: the 8-bit operand form, XP pieces per activation (2: bf16, 3: fp32)
+template <int NMAT, int XP>
 __global__ void __launch_bounds__(kThreads, 1) qmv_q4_0_tc_e4m3_kernel(const __grid_constant__ QtcParams p) {
-    qmv_tc_body<kFmtQ4, NMAT, 1, true>(p);
+    qmv_tc_body<kFmtQ4, NMAT, 1, XP>(p);
 }
 
 __global__ void __launch_bounds__(kThreads, 1) qmv_q4_k_tc_kernel(const __grid_constant__ QtcParams p) {
-    qmv_tc_body<kFmtQ4K, 1, 1, false>(p);
+    qmv_tc_body<kFmtQ4K, 1, 1, 0>(p);
 }
 
 }  // namespace
@@ -617,10 +642,10 @@ cudaError_t launch_qmv_tc(int fmt, int nmat, int ntok, const CUtensorMap* tmap_w
     const int ctas = p.units < sm_count ? p.units : sm_count;
     // the 8-bit form needs every K-group of a CTA's unit range in its table
     const int per_cta = (p.units + ctas - 1) / ctas;
-    const bool f8 = fmt == kFmtQ4 && ntok == 1 && x_bf16 &&
-                    std::min(p.groups, (per_cta - 1) / nmat + 2) <= kXtGroups;
+    const bool f8 = fmt == kFmtQ4 && ntok == 1 && std::min(p.groups, (per_cta - 1) / nmat + 2) <= kXtGroups;
     auto kernel = fmt == kFmtQ4K ? qmv_q4_k_tc_kernel
-                  : f8           ? (nmat == 2 ? qmv_q4_0_tc_e4m3_kernel<2> : qmv_q4_0_tc_e4m3_kernel<1>)
+                  : f8 ? (x_bf16 ? (nmat == 2 ? qmv_q4_0_tc_e4m3_kernel<2, 2> : qmv_q4_0_tc_e4m3_kernel<1, 2>)
+                                 : (nmat == 2 ? qmv_q4_0_tc_e4m3_kernel<2, 3> : qmv_q4_0_tc_e4m3_kernel<1, 3>))
                   : (nmat == 2 ? qmv_q4_0_tc_kernel<2, 1>
                                : (ntok == 2 ? qmv_q4_0_tc_kernel<1, 2> : qmv_q4_0_tc_kernel<1, 1>));
     static thread_local int prepared_device = -1;
@@ -628,7 +653,8 @@ cudaError_t launch_qmv_tc(int fmt, int nmat, int ntok, const CUtensorMap* tmap_w
     cudaGetDevice(&dev);
     if (prepared_device != dev) {
         for (auto f : {qmv_q4_0_tc_kernel<1, 1>, qmv_q4_0_tc_kernel<2, 1>, qmv_q4_0_tc_kernel<1, 2>,
-                       qmv_q4_0_tc_e4m3_kernel<1>, qmv_q4_0_tc_e4m3_kernel<2>, qmv_q4_k_tc_kernel}) {
+                       qmv_q4_0_tc_e4m3_kernel<1, 2>, qmv_q4_0_tc_e4m3_kernel<2, 2>, qmv_q4_0_tc_e4m3_kernel<1, 3>,
+                       qmv_q4_0_tc_e4m3_kernel<2, 3>, qmv_q4_k_tc_kernel}) {
             cudaError_t e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
             if (e != cudaSuccess) return e;
         }

@@ -34,17 +34,22 @@ constexpr uint32_t kBf16Minus136 = 0xC308C308u;
 constexpr uint32_t kBf16Minus128 = 0xC300C300u;
 
 constexpr uint32_t kOffB = kStages * kRawStageBytes;                          // 1024-aligned
-constexpr uint32_t kOffPart = kOffB + kSets * kBBytes;
+// 8-bit form with fp32 activations: a second B per set, the third pieces
+constexpr uint32_t kOffB2 = kOffB + kSets * kBBytes;
+constexpr uint32_t kOffPart = kOffB2 + kSets * kBBytes;
 constexpr uint32_t kOffBar = kOffPart + kSets * kMaxLocalTiles * 2 * kTileRows * 4;
 constexpr int kBars = 2 * kStages + 4 * kSets + 1;
 constexpr uint32_t kOffSlot = kOffBar + 8 * kBars;
 // 8-bit form: the activations of up to kXtGroups K-groups, built once per CTA:
 // per group 32 chunks of 8 elements as {piece 0, piece 1} (16 bytes each),
-// and per group the 8 blocks' read-back factors c_j (fp32)
-constexpr int kXtGroups = 64;
+// with fp32 activations a third piece (8 bytes each), and per group the 8
+// blocks' read-back factors c_j (fp32)
+constexpr int kXtGroups = 48;
 constexpr uint32_t kOffXt = (kOffSlot + 16 + 15) & ~15u;
-constexpr uint32_t kOffXc = kOffXt + kXtGroups * 32 * 16;
+constexpr uint32_t kOffXt2 = kOffXt + kXtGroups * 32 * 16;
+constexpr uint32_t kOffXc = kOffXt2 + kXtGroups * 32 * 8;
 constexpr uint32_t kSmemBytes = kOffXc + kXtGroups * 8 * 4;
+static_assert(kSmemBytes <= 227 * 1024, "one CTA per SM");
 
 static_assert(kStages % kSets == 0, "stage s must serve set s % 3");
 static_assert(kOffB % 1024 == 0, "B operand needs 1024-byte alignment");
@@ -326,39 +331,95 @@ __device__ __forceinline__ void split_e4m3(uint4 xr, float sc, uint2& p0, uint2&
     p1 = make_uint2(h1[0] | (h1[1] << 16), h1[2] | (h1[3] << 16));
 }
 
+// v rounded to four significant bits (sign, exponent, top three mantissa
+// bits; half-way cases away from zero): exact in e4m3 in its normal range
+__device__ __forceinline__ float round4(float v) { return __uint_as_float((__float_as_uint(v) + 0x00080000u) & 0xFFF00000u); }
+
+// Eight fp32 activations (xa, xb in element order), already scaled by the
+// power of two sc, as three e4m3 pieces: p0 = round4(x), p1 = round4(x - p0),
+// p2 = e4m3(x - p0 - p1).  |x - p0| <= 2^-4 |x| and |x - p0 - p1| <= 2^-8 |x|
+// (each round4 halves an ulp of four bits), so p0 + p1 + p2 carries x to
+// 2^-12 relative while the pieces stay in e4m3's normal range.
+__device__ __forceinline__ void split3_e4m3(uint4 xa, uint4 xb, float sc, uint2& p0, uint2& p1, uint2& p2) {
+    const uint32_t w[8] = {xa.x, xa.y, xa.z, xa.w, xb.x, xb.y, xb.z, xb.w};
+    uint32_t h0[4], h1[4], h2[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+        const float a = __uint_as_float(w[2 * e]) * sc, b = __uint_as_float(w[2 * e + 1]) * sc;
+        const float a0 = round4(a), b0 = round4(b);
+        const float ar = a - a0, br = b - b0;
+        const float a1 = round4(ar), b1 = round4(br);
+        h0[e] = e4m3x2(a0, b0);
+        h1[e] = e4m3x2(a1, b1);
+        h2[e] = e4m3x2(ar - a1, br - b1);
+    }
+    p0 = make_uint2(h0[0] | (h0[1] << 16), h0[2] | (h0[3] << 16));
+    p1 = make_uint2(h1[0] | (h1[1] << 16), h1[2] | (h1[3] << 16));
+    p2 = make_uint2(h2[0] | (h2[1] << 16), h2[2] | (h2[3] << 16));
+}
+
 // 8-bit form: the activation table of cnt K-groups, group xg0 + sl (mod G) in
-// slot sl, from bf16 x, built by warps w = 0 .. nwarps - 1 of the calling
+// slot sl, from bf16 (XP = 2) or fp32 (XP = 3) x, built by warps w = 0 .. nwarps - 1 of the calling
 // group (every lane of each).  Each chunk of 8 elements is scaled by its
 // block's s_j = 2^(es - 127), which takes the block's largest |x| into
-// [2^7, 2^8) (e4m3 reaches 448); es = 261 - E for the bf16 biased exponent E
-// of that maximum, kept where s_j and c_j = 2^9 / s_j are normal fp32.
+// [2^7, 2^8) (e4m3 reaches 448); es = 261 - E for the biased exponent E of
+// that maximum, kept where s_j and c_j = 2^9 / s_j are normal fp32.
 // kCoherent: x may have been written earlier in the same launch by other CTAs
 // (loads through L2 only).
 template <bool kCoherent>
-__device__ __forceinline__ uint4 load_x_chunk(const void* x, int xg0, int G, int c) {
-    int g = xg0 + (c >> 5);
-    if (g >= G) g -= G;
-    const uint16_t* src = static_cast<const uint16_t*>(x) + (size_t)g * kGroupK + 8 * (c & 31);
-    uint4 xr;
+__device__ __forceinline__ uint4 ld_x16(const void* p) {
+    uint4 v;
     if constexpr (kCoherent)
         asm volatile("ld.global.cg.v4.u32 {%0, %1, %2, %3}, [%4];"
-                     : "=r"(xr.x), "=r"(xr.y), "=r"(xr.z), "=r"(xr.w)
-                     : "l"(src)
+                     : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                     : "l"(p)
                      : "memory");
     else
-        xr = __ldg(reinterpret_cast<const uint4*>(src));
-    return xr;
+        v = __ldg(reinterpret_cast<const uint4*>(p));
+    return v;
 }
 
-__device__ __forceinline__ void table_chunk(uint32_t sbase, int c, int lane, uint4 xr) {
-    const uint32_t m2 = umax16x2(umax16x2(xr.x & 0x7FFF7FFFu, xr.y & 0x7FFF7FFFu),
-                                 umax16x2(xr.z & 0x7FFF7FFFu, xr.w & 0x7FFF7FFFu));
-    uint32_t mx = max(m2 & 0xFFFFu, m2 >> 16);
+// chunk c of the table (8 elements): bf16 (XP = 2, one 16-byte load) or fp32
+// (XP = 3, two)
+template <bool kCoherent, int XP>
+__device__ __forceinline__ void load_x_chunk(const void* x, int xg0, int G, int c, uint4& xa, uint4& xb) {
+    int g = xg0 + (c >> 5);
+    if (g >= G) g -= G;
+    const size_t e = (size_t)g * kGroupK + 8 * (c & 31);
+    if constexpr (XP == 2) {
+        xa = ld_x16<kCoherent>(static_cast<const uint16_t*>(x) + e);
+    } else {
+        xa = ld_x16<kCoherent>(static_cast<const float*>(x) + e);
+        xb = ld_x16<kCoherent>(static_cast<const float*>(x) + e + 4);
+    }
+}
+
+template <int XP>
+__device__ __forceinline__ void table_chunk(uint32_t sbase, int c, int lane, uint4 xa, uint4 xb) {
+    // the block's largest |x|, as bits: bf16 exponent at bit 7, fp32 at bit 23
+    uint32_t mx;
+    if constexpr (XP == 2) {
+        const uint32_t m2 = umax16x2(umax16x2(xa.x & 0x7FFF7FFFu, xa.y & 0x7FFF7FFFu),
+                                     umax16x2(xa.z & 0x7FFF7FFFu, xa.w & 0x7FFF7FFFu));
+        mx = max(m2 & 0xFFFFu, m2 >> 16) >> 7;
+    } else {
+        const uint32_t m = max(max(max(xa.x & 0x7FFFFFFFu, xa.y & 0x7FFFFFFFu), max(xa.z & 0x7FFFFFFFu, xa.w & 0x7FFFFFFFu)),
+                               max(max(xb.x & 0x7FFFFFFFu, xb.y & 0x7FFFFFFFu), max(xb.z & 0x7FFFFFFFu, xb.w & 0x7FFFFFFFu)));
+        mx = m >> 23;
+    }
     mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
     mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-    const int es = min(max(261 - (int)(mx >> 7), 9), 253);
-    uint2 q0, q1;
-    split_e4m3(xr, __uint_as_float((uint32_t)es << 23), q0, q1);
+    const int es = min(max(261 - (int)mx, 9), 253);
+    const float sc = __uint_as_float((uint32_t)es << 23);
+    uint2 q0, q1, q2;
+    if constexpr (XP == 2) {
+        split_e4m3(xa, sc, q0, q1);
+    } else {
+        split3_e4m3(xa, xb, sc, q0, q1, q2);
+        asm volatile("st.shared.v2.b32 [%0], {%1, %2};" ::"r"(sbase + kOffXt2 + (uint32_t)c * 8u), "r"(q2.x),
+                     "r"(q2.y)
+                     : "memory");
+    }
     sts128(sbase + kOffXt + (uint32_t)c * 16u, make_uint4(q0.x, q0.y, q1.x, q1.y));
     if ((lane & 3) == 0)
         asm volatile("st.shared.b32 [%0], %1;" ::"r"(sbase + kOffXc + (uint32_t)(c >> 2) * 4u),
@@ -366,7 +427,7 @@ __device__ __forceinline__ void table_chunk(uint32_t sbase, int c, int lane, uin
                      : "memory");
 }
 
-template <bool kCoherent>
+template <bool kCoherent, int XP>
 __device__ __forceinline__ void build_x_table(uint32_t sbase, const void* x, int xg0, int G, int cnt, int w,
                                               int lane, int nwarps) {
     // a warp's chunks are 32 consecutive ones (block j = lanes 4j .. 4j + 3);
@@ -375,13 +436,13 @@ __device__ __forceinline__ void build_x_table(uint32_t sbase, const void* x, int
     const int nch = cnt * 32;
     const int stride = nwarps * 32;
     for (int c0 = w * 32; c0 < nch; c0 += 4 * stride) {
-        uint4 xr[4];
+        uint4 xa[4], xb[4];
 #pragma unroll
         for (int j = 0; j < 4; ++j)
-            if (c0 + j * stride < nch) xr[j] = load_x_chunk<kCoherent>(x, xg0, G, c0 + j * stride + lane);
+            if (c0 + j * stride < nch) load_x_chunk<kCoherent, XP>(x, xg0, G, c0 + j * stride + lane, xa[j], xb[j]);
 #pragma unroll
         for (int j = 0; j < 4; ++j)
-            if (c0 + j * stride < nch) table_chunk(sbase, c0 + j * stride + lane, lane, xr[j]);
+            if (c0 + j * stride < nch) table_chunk<XP>(sbase, c0 + j * stride + lane, lane, xa[j], xb[j]);
     }
 }
 

@@ -111,27 +111,29 @@ def test_qmv_q4_0_tensor_core_shapes(qbw, oracle, N, K, xdt, odt):
     assert qbw.fault_read(clear=True) == 0
 
 
-# bf16 activations on the tensor-core path take the 8-bit operand form: codes
-# c & 7 and the bit-3 indicator as e4m3 bytes (both 0 where c = 8), each
-# activation as two e4m3 pieces under a power-of-two scale per 32-element
-# block.  15.1 MB of weights (the tensor-core path), a last tile of 8 rows.
+# The tensor-core path's one-token Q4_0 products take the 8-bit operand form:
+# codes c & 7 and the bit-3 indicator as e4m3 bytes (both 0 where c = 8), each
+# activation as e4m3 pieces under a power-of-two scale per 32-element block
+# (two pieces for bf16 activations, three for fp32).  15.1 MB of weights (the
+# tensor-core path), a last tile of 8 rows.
 F8_N, F8_K = 5000, 5376
 
 
+@pytest.mark.parametrize("xdt", ["bf16", "f32"])
 @pytest.mark.parametrize("code", [0, 7, 8, 9, 15])
-def test_tc_bf16_constant_blocks(qbw, oracle, code):
+def test_tc_8bit_constant_blocks(qbw, oracle, code, xdt):
     # code 8 is weight 0 everywhere: S = 0 and the output must be exactly 0
     w = synth.constant_blocks("q4_0", F8_N, F8_K, 0x3555, code)
-    x = synth.activations(F8_K, seed=6, dtype="bf16")
+    x = synth.activations(F8_K, seed=6, dtype=xdt)
     y = run_qmv(qbw, "q4_0", w, x, F8_N, F8_K, "f32")
     y_ref, S = oracle.qmv("q4_0", w, x, F8_N, F8_K)
-    check_matvec(y, y_ref, S, what=f"tc bf16 constant code {code}")
+    check_matvec(y, y_ref, S, what=f"tc 8-bit {xdt} constant code {code}")
     if code == 8:
         assert np.all(y == 0.0)
 
 
-@pytest.mark.parametrize("odt", ["f32", "bf16"])
-def test_tc_bf16_activation_ranges(qbw, oracle, odt):
+@pytest.mark.parametrize("xdt,odt", [("bf16", "f32"), ("bf16", "bf16"), ("f32", "f32")])
+def test_tc_8bit_activation_ranges(qbw, oracle, xdt, odt):
     # Each 32-element block of x gets its own factor 10^-30 .. 10^30, a tenth
     # of the blocks are all zero, and a quarter carry one element 1000 times
     # the rest (an outlier channel): the per-block scale must place every
@@ -144,21 +146,35 @@ def test_tc_bf16_activation_ranges(qbw, oracle, odt):
     x.reshape(nb, 32)[g.random(nb) < 0.1] = 0.0
     out_blocks = np.flatnonzero(g.random(nb) < 0.25)
     x.reshape(nb, 32)[out_blocks, g.integers(0, 32, size=out_blocks.size)] *= 1000.0
-    xb = synth.f32_to_bf16_bits(x)
+    xin = synth.f32_to_bf16_bits(x) if xdt == "bf16" else x
     w = synth.q4_0_weights(N, K, seed=61)
-    y_ref, S = oracle.qmv("q4_0", w, xb, N, K)
-    y = run_qmv(qbw, "q4_0", w, xb, N, K, odt)
-    check_matvec(y, y_ref, S, out_bf16=(odt == "bf16"), what="tc bf16 activation ranges")
+    y_ref, S = oracle.qmv("q4_0", w, xin, N, K)
+    y = run_qmv(qbw, "q4_0", w, xin, N, K, odt)
+    worst = check_matvec(y, y_ref, S, out_bf16=(odt == "bf16"), what=f"tc 8-bit {xdt} activation ranges")
+    if xdt == "f32" and odt == "f32":
+        assert worst < 5e-4      # three pieces carry fp32 x to about 2^-12
 
 
-def test_tc_bf16_edge_scales(qbw, oracle):
+@pytest.mark.parametrize("xdt", ["bf16", "f32"])
+def test_tc_8bit_edge_scales(qbw, oracle, xdt):
     pool = np.array([0x0000, 0x8000, 0x0001, 0x03FF, 0x0400, 0x7BFF, 0xFBFF, 0x3C00, 0x2E66, 0xA123],
                     dtype=np.uint16)
     w = synth.random_with_scale_bits("q4_0", F8_N, F8_K, 18, pool)
-    x = synth.activations(F8_K, seed=18, dtype="bf16")
+    x = synth.activations(F8_K, seed=18, dtype=xdt)
     y = run_qmv(qbw, "q4_0", w, x, F8_N, F8_K, "f32")
     y_ref, S = oracle.qmv("q4_0", w, x, F8_N, F8_K)
-    check_matvec(y, y_ref, S, what="tc bf16 edge scales")
+    check_matvec(y, y_ref, S, what=f"tc 8-bit {xdt} edge scales")
+
+
+def test_tc_fp32_gateup(qbw, oracle):
+    # gate+up with fp32 activations: the 8-bit form with three pieces
+    N, K = 5413, 5376
+    wg = synth.q4_0_weights(N, K, seed=52, stream=0)
+    wu = synth.q4_0_weights(N, K, seed=52, stream=1)
+    x = synth.activations(K, seed=52, dtype="f32")
+    o = run_gateup(qbw, wg, wu, x, N, K, "f32")
+    ref = oracle.gateup_q4_0(wg, wu, x, N, K)
+    check_gateup(o, ref, oracle, what="gateup fp32 x")
 
 
 def run_gateup(qbw, wg, wu, x, N, K, odt):
