@@ -392,6 +392,9 @@ def supplementary_kernels(torch, qbw, hbm_peak):
     y = torch.empty(N, device=dev)
     run("qmv_q4_k 21504x5376 f32", w.numel() + 4 * K + 4 * N, copies,
         lambda i: (lambda: qbw.qmv_q4_k(ws[i], x, y, 1, N, K)))
+    xk = bf16(synth.activations(K, seed=1, dtype="bf16"))
+    run("qmv_q4_k 21504x5376 bf16->f32", w.numel() + 2 * K + 4 * N, copies,
+        lambda i: (lambda: qbw.qmv_q4_k(ws[i], xk, y, 1, N, K)))
     del ws, w
     # small-M tiles
     for (N, K) in ((5376, 5376), (5376, 21504)):

@@ -313,7 +313,7 @@ __global__ void __launch_bounds__(kThreads, 1) qmv_chain_kernel(const __grid_con
                 tmem_ld16(d_taddr + 16u * buf, dv);
                 tmem_wait_ld();
                 float c[8];
-                table_c(sbase, pend_sl, c);
+                table_f8(sbase, kOffXc, pend_sl, c);
                 add_unit(unit_dot_e4m3(dv, pend_dd, c));
             };
             // this set's units of the step: I = I_base + i = set (mod 3)

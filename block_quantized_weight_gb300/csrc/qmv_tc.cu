@@ -83,7 +83,10 @@ __device__ __forceinline__ void qmv_tc_body(const QtcParams& p) {
     constexpr int NCH = NMAT * NTOK;
     static_assert(NCH <= 2, "at most two sums per row");
     static_assert(FMT == kFmtQ4 || (NMAT == 1 && NTOK == 1), "Q4_K: one matrix, one token");
-    static_assert(F8 == 0 || ((F8 == 2 || F8 == 3) && FMT == kFmtQ4 && NTOK == 1), "8-bit form: Q4_0, one token");
+    static_assert(F8 == 0 || ((F8 == 2 || F8 == 3) && NTOK == 1), "8-bit form: one token");
+    // the 8-bit form of Q4_K: one A operand (codes 0..15), 8 K-steps per unit
+    constexpr bool Q4K8 = F8 != 0 && FMT == kFmtQ4K;
+    constexpr int kSteps = Q4K8 ? 8 : 16;
     extern __shared__ __align__(1024) uint8_t smem[];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int ctas = (int)gridDim.x, cta = (int)blockIdx.x;
@@ -176,7 +179,7 @@ __device__ __forceinline__ void qmv_tc_body(const QtcParams& p) {
                 if (!ok) break;
                 tc_fence_after();
 #pragma unroll
-                for (int k = 0; k < 8; ++k) {
+                for (int k = 0; k < kSteps / 2; ++k) {
                     const uint64_t bo = (uint64_t)((k >> 2) * 128 + (k & 3) * 2);
                     if constexpr (F8) {
                         tc_mma_f8(d_tmem, a_tmem + 8u * (uint32_t)k, b0 + bo, idesc, k > 0 ? 1u : 0u);
@@ -190,7 +193,7 @@ __device__ __forceinline__ void qmv_tc_body(const QtcParams& p) {
                 if (!ok) break;
                 tc_fence_after();
 #pragma unroll
-                for (int k = 8; k < 16; ++k) {
+                for (int k = kSteps / 2; k < kSteps; ++k) {
                     const uint64_t bo = (uint64_t)((k >> 2) * 128 + (k & 3) * 2);
                     if constexpr (F8) {
                         tc_mma_f8(d_tmem, a_tmem + 8u * (uint32_t)k, b0 + bo, idesc, 1u);
@@ -221,7 +224,7 @@ __device__ __forceinline__ void qmv_tc_body(const QtcParams& p) {
         // the group: swizzle atom xl / 8, block j = xl / 4, B rows 2j (x_hi)
         // and 2j + 1 (x_lo), in K-half xl / 16.
         // (the 8-bit form's B-writing lanes read their slot from the table)
-        constexpr bool kAllLanesX = FMT == kFmtQ4K;
+        constexpr bool kAllLanesX = FMT == kFmtQ4K && !Q4K8;
         const int xl = kAllLanesX ? lane : 8 * q + lane;
         const bool loads_x = !F8 && (kAllLanesX || lane < 8);
         const bool bwriter = kAllLanesX ? ((lane >> 3) == q) : (lane < 8);
@@ -234,6 +237,9 @@ __device__ __forceinline__ void qmv_tc_body(const QtcParams& p) {
         const uint32_t f8_p0 = bbuf + b_byte(bj >> 1, 2 * bj, bo), f8_p1 = bbuf + b_byte(bj >> 1, 2 * bj + 1, bo);
         const uint32_t f8_n0 = bbuf + b_byte(bj >> 1, 2 * bj, bo + 32u);
         const uint32_t f8_n1 = bbuf + b_byte(bj >> 1, 2 * bj + 1, bo + 32u);
+        // 8-bit Q4_K: sub-block bj at K-step bj, rows 2bj (piece 0) and 2bj + 1
+        const uint32_t kb = (uint32_t)((bj & 3) * 32 + 8 * (xl & 3));
+        const uint32_t k8_p0 = bbuf + b_byte(bj >> 2, 2 * bj, kb), k8_p1 = bbuf + b_byte(bj >> 2, 2 * bj + 1, kb);
         const int bhalf = xl >> 4;
         const int row = 32 * q + lane;
         // 8-bit form: the activation table of the K-groups g of this CTA's
@@ -244,7 +250,7 @@ __device__ __forceinline__ void qmv_tc_body(const QtcParams& p) {
         if constexpr (F8) {
             const int cnt = n > 0 ? min(G, (u1 - 1) / NMAT - u0 / NMAT + 1) : 0;
             if (cnt > kXtGroups) record_fault(p.fault, kFaultPlan);
-            build_x_table<false, F8>(sbase, p.x, xg0, G, min(cnt, kXtGroups), warp, lane, kProducerWarp);
+            build_x_table<false, F8, Q4K8>(sbase, p.x, xg0, G, min(cnt, kXtGroups), warp, lane, kProducerWarp);
             asm volatile("bar.sync 2, %0;" ::"n"(kProducerWarp * 32) : "memory");
         }
         bool counted = !contrib0;
@@ -406,7 +412,8 @@ __device__ __forceinline__ void qmv_tc_body(const QtcParams& p) {
             }
             const uint32_t prev = (uint32_t)(k - 1) & 1u;     // completion parity of the previous unit
             // ---- half 0: K 0..127 (block pairs 0, 1; B atoms 0, 1 written by warps 0, 1)
-            if constexpr (F8) codes_pair_e4m3<0>(v, c0);
+            if constexpr (Q4K8) codes_q4k_e4m3<0>(v, c0);
+            else if constexpr (F8) codes_pair_e4m3<0>(v, c0);
             else codes_pair<FMT, 0>(v, c0);
             if (k > 0) {
                 const bool free = mbar_wait_bounded(aempty_bar(bar0, set, 0), prev, p.fault, kFaultMmaWaitTimeout);
@@ -417,7 +424,11 @@ __device__ __forceinline__ void qmv_tc_body(const QtcParams& p) {
                 tc_fence_after();
             }
             if (bwriter && bhalf == 0) {
-                if constexpr (F8) {
+                if constexpr (Q4K8) {
+                    sts64(k8_p0, bp0);
+                    sts64(k8_p1, bp1);
+                    if constexpr (F8 == 3) sts64(k8_p1 + (kOffB2 - kOffB), bp2);
+                } else if constexpr (F8) {
                     sts64(f8_p0, bp0);
                     sts64(f8_p1, bp1);
                     sts64(f8_n0, make_uint2(bp0.x ^ 0x80808080u, bp0.y ^ 0x80808080u));
@@ -433,16 +444,19 @@ __device__ __forceinline__ void qmv_tc_body(const QtcParams& p) {
                 fence_proxy_async_smem();     // B visible to the tensor core
             }
             tmem_st32(a_taddr, c0);
-            if constexpr (F8) codes_pair_e4m3<1>(v, c1);
-            else codes_pair<FMT, 1>(v, c1);
-            tmem_wait_st();
-            tmem_st32(a_taddr + 32u, c1);
+            if constexpr (!Q4K8) {
+                if constexpr (F8) codes_pair_e4m3<1>(v, c1);
+                else codes_pair<FMT, 1>(v, c1);
+                tmem_wait_st();
+                tmem_st32(a_taddr + 32u, c1);
+            }
             tmem_wait_st();
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(afull_bar(bar0, set, 0));
             // ---- half 1: K 128..255 (block pairs 2, 3; B atoms 2, 3 written by warps 2, 3)
-            if constexpr (F8) codes_pair_e4m3<2>(v, c0);
+            if constexpr (Q4K8) codes_q4k_e4m3<1>(v, c0);
+            else if constexpr (F8) codes_pair_e4m3<2>(v, c0);
             else codes_pair<FMT, 2>(v, c0);
             if (k > 0) {
                 const bool free = mbar_wait_bounded(aempty_bar(bar0, set, 1), prev, p.fault, kFaultMmaWaitTimeout);
@@ -453,7 +467,11 @@ __device__ __forceinline__ void qmv_tc_body(const QtcParams& p) {
                 tc_fence_after();
             }
             if (bwriter && bhalf == 1) {
-                if constexpr (F8) {
+                if constexpr (Q4K8) {
+                    sts64(k8_p0, bp0);
+                    sts64(k8_p1, bp1);
+                    if constexpr (F8 == 3) sts64(k8_p1 + (kOffB2 - kOffB), bp2);
+                } else if constexpr (F8) {
                     sts64(f8_p0, bp0);
                     sts64(f8_p1, bp1);
                     sts64(f8_n0, make_uint2(bp0.x ^ 0x80808080u, bp0.y ^ 0x80808080u));
@@ -468,11 +486,15 @@ __device__ __forceinline__ void qmv_tc_body(const QtcParams& p) {
                 }
                 fence_proxy_async_smem();
             }
-            tmem_st32(a_taddr + 64u, c0);
-            if constexpr (F8) codes_pair_e4m3<3>(v, c1);
-            else codes_pair<FMT, 3>(v, c1);
-            tmem_wait_st();
-            tmem_st32(a_taddr + 96u, c1);
+            if constexpr (Q4K8) {
+                tmem_st32(a_taddr + 32u, c0);
+            } else {
+                tmem_st32(a_taddr + 64u, c0);
+                if constexpr (F8) codes_pair_e4m3<3>(v, c1);
+                else codes_pair<FMT, 3>(v, c1);
+                tmem_wait_st();
+                tmem_st32(a_taddr + 96u, c1);
+            }
             tmem_wait_st();
             tc_fence_before();
             __syncwarp();
@@ -484,10 +506,15 @@ __device__ __forceinline__ void qmv_tc_body(const QtcParams& p) {
                 tmem_ld16(d_taddr + 16u * prev, dv);
                 tmem_wait_ld();
                 float r0, r1 = 0.f;
-                if constexpr (FMT == kFmtQ4K) r0 = unit_dot_q4k(dv, pend_dd, pend_sx);
+                if constexpr (Q4K8) {
+                    float c[8], sx[8];
+                    table_f8(sbase, kOffXc, pend_sl, c);
+                    table_f8(sbase, kOffXs, pend_sl, sx);
+                    r0 = unit_dot_q4k_e4m3(dv, pend_dd, c, sx);
+                } else if constexpr (FMT == kFmtQ4K) r0 = unit_dot_q4k(dv, pend_dd, pend_sx);
                 else if constexpr (F8) {
                     float c[8];
-                    table_c(sbase, pend_sl, c);
+                    table_f8(sbase, kOffXc, pend_sl, c);
                     r0 = unit_dot_e4m3(dv, pend_dd, c);
                 }
                 else unit_dot<NTOK>(dv, pend_dd, r0, r1);
@@ -510,10 +537,15 @@ __device__ __forceinline__ void qmv_tc_body(const QtcParams& p) {
                 tmem_ld16(d_taddr + 16u * last_par, dv);
                 tmem_wait_ld();
                 float r0, r1 = 0.f;
-                if constexpr (FMT == kFmtQ4K) r0 = unit_dot_q4k(dv, pend_dd, pend_sx);
+                if constexpr (Q4K8) {
+                    float c[8], sx[8];
+                    table_f8(sbase, kOffXc, pend_sl, c);
+                    table_f8(sbase, kOffXs, pend_sl, sx);
+                    r0 = unit_dot_q4k_e4m3(dv, pend_dd, c, sx);
+                } else if constexpr (FMT == kFmtQ4K) r0 = unit_dot_q4k(dv, pend_dd, pend_sx);
                 else if constexpr (F8) {
                     float c[8];
-                    table_c(sbase, pend_sl, c);
+                    table_f8(sbase, kOffXc, pend_sl, c);
                     r0 = unit_dot_e4m3(dv, pend_dd, c);
                 }
                 else unit_dot<NTOK>(dv, pend_dd, r0, r1);
@@ -597,6 +629,12 @@ __global__ void __launch_bounds__(kThreads, 1) qmv_q4_k_tc_kernel(const __grid_c
     qmv_tc_body<kFmtQ4K, 1, 1, 0>(p);
 }
 
+// Q4_K in the 8-bit operand form, XP pieces per activation
+template <int XP>
+__global__ void __launch_bounds__(kThreads, 1) qmv_q4_k_tc_e4m3_kernel(const __grid_constant__ QtcParams p) {
+    qmv_tc_body<kFmtQ4K, 1, 1, XP>(p);
+}
+
 }  // namespace
 
 // The tensor-core M = 1 path takes K % 256 == 0, at most kQtcMaxTiles tiles
@@ -642,8 +680,9 @@ cudaError_t launch_qmv_tc(int fmt, int nmat, int ntok, const CUtensorMap* tmap_w
     const int ctas = p.units < sm_count ? p.units : sm_count;
     // the 8-bit form needs every K-group of a CTA's unit range in its table
     const int per_cta = (p.units + ctas - 1) / ctas;
-    const bool f8 = fmt == kFmtQ4 && ntok == 1 && std::min(p.groups, (per_cta - 1) / nmat + 2) <= kXtGroups;
-    auto kernel = fmt == kFmtQ4K ? qmv_q4_k_tc_kernel
+    const bool f8 = ntok == 1 && std::min(p.groups, (per_cta - 1) / nmat + 2) <= kXtGroups;
+    auto kernel = fmt == kFmtQ4K ? (f8 ? (x_bf16 ? qmv_q4_k_tc_e4m3_kernel<2> : qmv_q4_k_tc_e4m3_kernel<3>)
+                                       : qmv_q4_k_tc_kernel)
                   : f8 ? (x_bf16 ? (nmat == 2 ? qmv_q4_0_tc_e4m3_kernel<2, 2> : qmv_q4_0_tc_e4m3_kernel<1, 2>)
                                  : (nmat == 2 ? qmv_q4_0_tc_e4m3_kernel<2, 3> : qmv_q4_0_tc_e4m3_kernel<1, 3>))
                   : (nmat == 2 ? qmv_q4_0_tc_kernel<2, 1>
@@ -654,7 +693,8 @@ cudaError_t launch_qmv_tc(int fmt, int nmat, int ntok, const CUtensorMap* tmap_w
     if (prepared_device != dev) {
         for (auto f : {qmv_q4_0_tc_kernel<1, 1>, qmv_q4_0_tc_kernel<2, 1>, qmv_q4_0_tc_kernel<1, 2>,
                        qmv_q4_0_tc_e4m3_kernel<1, 2>, qmv_q4_0_tc_e4m3_kernel<2, 2>, qmv_q4_0_tc_e4m3_kernel<1, 3>,
-                       qmv_q4_0_tc_e4m3_kernel<2, 3>, qmv_q4_k_tc_kernel}) {
+                       qmv_q4_0_tc_e4m3_kernel<2, 3>, qmv_q4_k_tc_kernel, qmv_q4_k_tc_e4m3_kernel<2>,
+                       qmv_q4_k_tc_e4m3_kernel<3>}) {
             cudaError_t e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
             if (e != cudaSuccess) return e;
         }

@@ -48,7 +48,8 @@ constexpr int kXtGroups = 48;
 constexpr uint32_t kOffXt = (kOffSlot + 16 + 15) & ~15u;
 constexpr uint32_t kOffXt2 = kOffXt + kXtGroups * 32 * 16;
 constexpr uint32_t kOffXc = kOffXt2 + kXtGroups * 32 * 8;
-constexpr uint32_t kSmemBytes = kOffXc + kXtGroups * 8 * 4;
+constexpr uint32_t kOffXs = kOffXc + kXtGroups * 8 * 4;        // Q4_K: per block sum of x (fp32)
+constexpr uint32_t kSmemBytes = kOffXs + kXtGroups * 8 * 4;
 static_assert(kSmemBytes <= 227 * 1024, "one CTA per SM");
 
 static_assert(kStages % kSets == 0, "stage s must serve set s % 3");
@@ -174,6 +175,24 @@ __device__ __forceinline__ void codes_pair_e4m3(const uint32_t (&v)[36], uint32_
     }
 }
 
+// 8-bit form of Q4_K: half H of a super-block (sub-blocks 4H .. 4H + 3) -> 32
+// TMEM columns of e4m3 codes 0..15 (exact, b * 2^-9), one K-step of 8
+// columns per sub-block.  Sub-block j is the low (j even) or high (j odd)
+// nibbles of 64-weight chunk j / 2, whose 32 bytes are words 4 + 8 (j / 2) ..
+// 11 + 8 (j / 2) of the row: byte l holds weight l of the sub-block.
+template <int H>
+__device__ __forceinline__ void codes_q4k_e4m3(const uint32_t (&v)[36], uint32_t (&col)[32]) {
+#pragma unroll
+    for (int s = 0; s < 4; ++s) {
+        const int j = 4 * H + s;
+#pragma unroll
+        for (int t = 0; t < 8; ++t) {
+            const uint32_t w = v[4 + 8 * (j >> 1) + t];
+            col[8 * s + t] = ((j & 1) ? (w >> 4) : w) & 0x0F0F0F0Fu;
+        }
+    }
+}
+
 // fp16 scales of blocks 2P (low half) and 2P + 1 (high half) of the group:
 // block 2P's in the low half of word 9P, block 2P + 1's in the high half of
 // word 9P + 4.
@@ -253,6 +272,32 @@ __device__ __forceinline__ float unit_dot_e4m3(const uint32_t (&dv)[16], const u
     return r;
 }
 
+// 8-bit form of Q4_K: r0 = sum_j (d sc_j c_j) (D[2j] + D[2j + 1]) - dmin m_j sx_j,
+// j = 0..7 in order; dd[] holds the super-block's first 16 bytes (fp16 d and
+// dmin, then the 12 six-bit scale bytes), c[j] the read-back factors and sx[j]
+// the sub-blocks' activation sums.
+__device__ __forceinline__ float unit_dot_q4k_e4m3(const uint32_t (&dv)[16], const uint32_t (&dd)[4],
+                                                   const float (&c)[8], const float (&sx)[8]) {
+    const float2 dm = half2_to_float2(dd[0]);
+    const uint32_t s03 = dd[1], s47 = dd[2], s8b = dd[3];
+    float r = 0.f;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        uint32_t sc, m;
+        if (j < 4) {
+            sc = (s03 >> (8 * j)) & 63u;
+            m = (s47 >> (8 * j)) & 63u;
+        } else {
+            const uint32_t lo = (s8b >> (8 * (j - 4))) & 0xFFu;
+            sc = (lo & 15u) | (((s03 >> (8 * (j - 4) + 6)) & 3u) << 4);
+            m = (lo >> 4) | (((s47 >> (8 * (j - 4) + 6)) & 3u) << 4);
+        }
+        r = fmaf(dm.x * (float)sc * c[j], __uint_as_float(dv[2 * j]) + __uint_as_float(dv[2 * j + 1]), r);
+        r = fmaf(-dm.y * (float)m, sx[j], r);
+    }
+    return r;
+}
+
 __device__ __forceinline__ uint32_t umax16x2(uint32_t a, uint32_t b) {
     uint32_t r;
     asm("max.u16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
@@ -290,9 +335,10 @@ __device__ __forceinline__ uint32_t b_chunk(int a, int n, int c) {
     return (uint32_t)(a * 2048 + (n >> 3) * 1024 + (n & 7) * 128 + ((c ^ (n & 7)) << 4));
 }
 
-// 8-bit form: the read-back factors c_j of the group in table slot sl
-__device__ __forceinline__ void table_c(uint32_t sbase, int sl, float (&c)[8]) {
-    const uint4 a = lds128(sbase + kOffXc + (uint32_t)sl * 32u), b = lds128(sbase + kOffXc + (uint32_t)sl * 32u + 16u);
+// 8-bit form: eight fp32 values of table slot sl at offset off (the read-back
+// factors c_j at kOffXc, Q4_K's sub-block sums at kOffXs)
+__device__ __forceinline__ void table_f8(uint32_t sbase, uint32_t off, int sl, float (&c)[8]) {
+    const uint4 a = lds128(sbase + off + (uint32_t)sl * 32u), b = lds128(sbase + off + (uint32_t)sl * 32u + 16u);
     c[0] = __uint_as_float(a.x);
     c[1] = __uint_as_float(a.y);
     c[2] = __uint_as_float(a.z);
@@ -394,8 +440,29 @@ __device__ __forceinline__ void load_x_chunk(const void* x, int xg0, int G, int 
     }
 }
 
-template <int XP>
+template <int XP, bool kSums>
 __device__ __forceinline__ void table_chunk(uint32_t sbase, int c, int lane, uint4 xa, uint4 xb) {
+    if constexpr (kSums) {
+        // the block's sum of x (Q4_K's min term): 8 elements per lane, 4 lanes
+        float f[8];
+        if constexpr (XP == 2) {
+            const uint32_t w4[4] = {xa.x, xa.y, xa.z, xa.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                f[2 * e] = __uint_as_float(w4[e] << 16);
+                f[2 * e + 1] = __uint_as_float(w4[e] & 0xFFFF0000u);
+            }
+        } else {
+            const uint32_t w8[8] = {xa.x, xa.y, xa.z, xa.w, xb.x, xb.y, xb.z, xb.w};
+#pragma unroll
+            for (int e = 0; e < 8; ++e) f[e] = __uint_as_float(w8[e]);
+        }
+        float sx = ((f[0] + f[1]) + (f[2] + f[3])) + ((f[4] + f[5]) + (f[6] + f[7]));
+        sx += __shfl_xor_sync(0xffffffffu, sx, 1);
+        sx += __shfl_xor_sync(0xffffffffu, sx, 2);
+        if ((lane & 3) == 0)
+            asm volatile("st.shared.f32 [%0], %1;" ::"r"(sbase + kOffXs + (uint32_t)(c >> 2) * 4u), "f"(sx) : "memory");
+    }
     // the block's largest |x|, as bits: bf16 exponent at bit 7, fp32 at bit 23
     uint32_t mx;
     if constexpr (XP == 2) {
@@ -427,7 +494,7 @@ __device__ __forceinline__ void table_chunk(uint32_t sbase, int c, int lane, uin
                      : "memory");
 }
 
-template <bool kCoherent, int XP>
+template <bool kCoherent, int XP, bool kSums = false>
 __device__ __forceinline__ void build_x_table(uint32_t sbase, const void* x, int xg0, int G, int cnt, int w,
                                               int lane, int nwarps) {
     // a warp's chunks are 32 consecutive ones (block j = lanes 4j .. 4j + 3);
@@ -442,7 +509,7 @@ __device__ __forceinline__ void build_x_table(uint32_t sbase, const void* x, int
             if (c0 + j * stride < nch) load_x_chunk<kCoherent, XP>(x, xg0, G, c0 + j * stride + lane, xa[j], xb[j]);
 #pragma unroll
         for (int j = 0; j < 4; ++j)
-            if (c0 + j * stride < nch) table_chunk<XP>(sbase, c0 + j * stride + lane, lane, xa[j], xb[j]);
+            if (c0 + j * stride < nch) table_chunk<XP, kSums>(sbase, c0 + j * stride + lane, lane, xa[j], xb[j]);
     }
 }
 
