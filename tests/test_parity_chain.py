@@ -160,3 +160,24 @@ def test_chain_rejects_bad_steps(qbw):
         qbw.Chain([(wy, None, x, y, N, K), (w, None, y, wy.view(torch.bfloat16)[:N], N, K)])   # y over weights
     with pytest.raises(qbw.QbwError, match="QBW_EDTYPE"):
         qbw.Chain([(w, None, x, torch.zeros(N, dtype=torch.float16, device="cuda"), N, K)])
+
+
+def test_chain_one_group_steps_and_fp32_gateup(qbw, oracle):
+    # K = 256: one K-group per tile, so every unit is a whole tile; the last
+    # step is a gate+up with fp32 output
+    x0 = synth.activations(256, seed=95, dtype="bf16")
+    w0 = synth.q4_0_weights(256, 256, seed=96)
+    wg = synth.q4_0_weights(300, 256, seed=97, stream=0)
+    wu = synth.q4_0_weights(300, 256, seed=97, stream=1)
+    y0 = torch.empty(256, dtype=torch.bfloat16, device="cuda")
+    y1 = torch.empty(300, dtype=torch.float32, device="cuda")
+    chain = qbw.Chain([(dev_u8(w0), None, bf16_dev(x0), y0, 256, 256),
+                       (dev_u8(wg), dev_u8(wu), y0, y1, 300, 256)])
+    try:
+        chain.run()
+        torch.cuda.synchronize()
+        assert qbw.fault_read(clear=True) == 0
+        check_step(oracle, w0, None, x0, y0, 256, 256, "chain K=256 step 0")
+        check_step(oracle, wg, wu, bits(y0), y1, 300, 256, "chain K=256 gate+up")
+    finally:
+        chain.close()

@@ -166,6 +166,18 @@ def test_tc_8bit_edge_scales(qbw, oracle, xdt):
     check_matvec(y, y_ref, S, what=f"tc 8-bit {xdt} edge scales")
 
 
+@pytest.mark.parametrize("xdt", ["bf16", "f32"])
+def test_tc_8bit_one_group_per_tile(qbw, oracle, xdt):
+    # K = 256 with 15.8 MB of weights: every 128-row tile is a single unit,
+    # so no tile is split and the activation table holds one group
+    N, K = 110000, 256
+    w = synth.q4_0_weights(N, K, seed=63)
+    x = synth.activations(K, seed=63, dtype=xdt)
+    y = run_qmv(qbw, "q4_0", w, x, N, K, "f32")
+    y_ref, S = oracle.qmv("q4_0", w, x, N, K)
+    check_matvec(y, y_ref, S, what=f"tc 8-bit K=256 {xdt}")
+
+
 def test_tc_fp32_gateup(qbw, oracle):
     # gate+up with fp32 activations: the 8-bit form with three pieces
     N, K = 5413, 5376
