@@ -300,17 +300,18 @@ __global__ void __launch_bounds__(kThreads, 1) qmm_q4_0_tc_kernel(const __grid_c
     bool ok = true;
 
     // K-group i of this CTA -> stage i % kStages: raw W box and the 4 X boxes
-    auto issue = [&](int i) {
+    auto issue_w = [&](int i) {
         const int s = i % kStages;
-        const int g = g_begin + i;
-        const uint32_t st = sbase + (uint32_t)s * stage_bytes;
         mbar_arrive_expect_tx(full_bar_at(bar0, s), kRawStageBytes + xbytes);
-        tma_load_2d(st, &p.tmap_w, g * (kGroupBytes / 8), tile * kTileRows, full_bar_at(bar0, s),
-                    policy_evict_first());
+        tma_load_2d(sbase + (uint32_t)s * stage_bytes, &p.tmap_w, (g_begin + i) * (kGroupBytes / 8), tile * kTileRows,
+                    full_bar_at(bar0, s), policy_evict_first());
+    };
+    auto issue_x = [&](int i) {
+        const uint32_t st = sbase + (uint32_t)(i % kStages) * stage_bytes;
 #pragma unroll
         for (int a = 0; a < 4; ++a)
-            tma_load_2d(st + kRawStageBytes + (uint32_t)a * (uint32_t)p.NT * 128u, &p.tmap_x, g * kGroupK + a * 64, 0,
-                        full_bar_at(bar0, s), 0ull);
+            tma_load_2d(st + kRawStageBytes + (uint32_t)a * (uint32_t)p.NT * 128u, &p.tmap_x,
+                        (g_begin + i) * kGroupK + a * 64, 0, full_bar_at(bar0, i % kStages), 0ull);
     };
 
     // The producer initialises the barriers, releases everyone else through
@@ -334,12 +335,20 @@ __global__ void __launch_bounds__(kThreads, 1) qmm_q4_0_tc_kernel(const __grid_c
         if (lane == 0) {
             prefetch_tmap(&p.tmap_w);
             prefetch_tmap(&p.tmap_x);
-            for (int i = 0; i < ng && ok; ++i) {
+            // the weights do not depend on the preceding grid: the first stages'
+            // weight boxes go out before its completion, X after
+            const int pre = ng < kStages ? ng : kStages;
+            for (int i = 0; i < pre; ++i) issue_w(i);
+            grid_dependency_wait();
+            for (int i = 0; i < pre; ++i) issue_x(i);
+            for (int i = pre; i < ng && ok; ++i) {
                 const int s = i % kStages;
-                if (i >= kStages)
-                    ok = mbar_wait_bounded(empty_bar_at(bar0, s), (uint32_t)((i / kStages) - 1) & 1u, p.fault,
-                                           kFaultBulkWaitTimeout);
-                if (ok) issue(i);
+                ok = mbar_wait_bounded(empty_bar_at(bar0, s), (uint32_t)((i / kStages) - 1) & 1u, p.fault,
+                                       kFaultBulkWaitTimeout);
+                if (ok) {
+                    issue_w(i);
+                    issue_x(i);
+                }
             }
         }
     } else {
@@ -353,6 +362,9 @@ __global__ void __launch_bounds__(kThreads, 1) qmm_q4_0_tc_kernel(const __grid_c
         asm volatile("bar.sync 1, %0;" ::"n"(kThreads) : "memory");
         tc_fence_after();
     }
+    // X, Y and the workspace belong to the preceding grid's stream order
+    grid_dependency_wait();
+    grid_launch_dependents();
 
     if (warp >= kMmaWarp0) {
         // ---------------- MMA issuers: issuer j takes K-steps j, j + 2, ... of every group
@@ -575,22 +587,22 @@ cudaError_t launch_qmm_tc(const CUtensorMap& tmap_w, const CUtensorMap& tmap_x, 
         if (e != cudaSuccess) return e;
         prepared_device = dev;
     }
-    if (!cluster) {
-        qmm_q4_0_tc_kernel<<<p.tiles * splits, kThreads, smem, stream>>>(p);
-        return cudaGetLastError();
-    }
+    // programmatic dependent launch: the prologue and the first weight copies
+    // overlap the preceding kernel's tail
     cudaLaunchConfig_t cfg = {};
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = (unsigned)splits;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = (unsigned)splits;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
     cfg.gridDim = dim3((unsigned)(p.tiles * splits));
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = cluster ? 2 : 1;
     return cudaLaunchKernelEx(&cfg, qmm_q4_0_tc_kernel, p);
 }
 
