@@ -83,6 +83,17 @@ def test_qmv_q4_k_full_21504x5376(qbw, oracle):
     assert worst < 1e-4
 
 
+def test_qmv_q4_k_table_too_small_takes_bf16_code_form(qbw, oracle):
+    # each CTA's units touch up to 55 super-block columns, more than the 8-bit form's
+    # activation table holds (48): the bf16-code instantiation runs
+    N, K = 4000, 65536
+    w = synth.q4_k_weights(N, K, seed=65)
+    x = synth.activations(K, seed=65)
+    y = run(qbw, w, x, N, K, "f32")
+    y_ref, _ = oracle.qmv("q4_k", w, x, N, K)
+    check_matvec(y, y_ref, oracle.q4k_split_scale(w, x, N, K), what="q4_k K=65536 bf16-code form")
+
+
 def test_qmv_q4_k_cancelling_weights(qbw, oracle):
     # d sc q = dmin m in every sub-block: every weight is exactly 0, while the
     # two split sums are not; the result must stay within 2e-3 of S2

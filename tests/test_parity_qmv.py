@@ -178,6 +178,18 @@ def test_tc_8bit_one_group_per_tile(qbw, oracle, xdt):
     check_matvec(y, y_ref, S, what=f"tc 8-bit K=256 {xdt}")
 
 
+@pytest.mark.parametrize("xdt", ["bf16", "f32"])
+def test_tc_table_too_small_takes_bf16_code_form(qbw, oracle, xdt):
+    # K = 65536 over 32 tiles: each CTA's units touch up to 55 K-groups, more than
+    # the 8-bit form's activation table holds (48), so the bf16-code form runs
+    N, K = 4000, 65536
+    w = synth.q4_0_weights(N, K, seed=64)
+    x = synth.activations(K, seed=64, dtype=xdt)
+    y = run_qmv(qbw, "q4_0", w, x, N, K, "f32")
+    y_ref, S = oracle.qmv("q4_0", w, x, N, K)
+    check_matvec(y, y_ref, S, what=f"tc bf16-code form K=65536 {xdt}")
+
+
 def test_tc_fp32_gateup(qbw, oracle):
     # gate+up with fp32 activations: the 8-bit form with three pieces
     N, K = 5413, 5376
