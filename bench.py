@@ -26,6 +26,7 @@ from __future__ import annotations
 
 import argparse
 import hashlib
+import re
 import json
 import os
 import statistics
@@ -117,12 +118,21 @@ KERNEL_SOURCES = {
 TRAFFIC_SUMMARY = os.path.join(ROOT, "profiles", "qmv_sweep_layer_traffic.txt")
 
 
+def _code_only(text: str) -> str:
+    """Source text without comments and with whitespace collapsed: a change of
+    comments or layout leaves the compiled kernel, and so its profiled
+    traffic, unchanged."""
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", "", text)
+    return " ".join(text.split())
+
+
 def kernel_source_hash(kernel: str):
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "block_quantized_weight_gb300", "csrc")
     for f in KERNEL_SOURCES[kernel]:
         h.update(f.encode())
-        h.update(open(os.path.join(csrc, f), "rb").read())
+        h.update(_code_only(open(os.path.join(csrc, f)).read()).encode())
     return h.hexdigest()[:16]
 
 

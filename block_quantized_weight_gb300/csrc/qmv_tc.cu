@@ -9,21 +9,26 @@
 // Why tensor cores for one token: on CUDA cores every weight costs a code
 // extraction, an exact conversion to fp32 and a multiply-add, about 2.1
 // instructions, and that instruction stream, not HBM, bounds the CUDA-core
-// kernel.  Here a weight costs about 1.6 instructions: two codes become one
-// exact bf16x2 pair (byte permute, LOP3 with the exponent of 128, one packed
-// add of -136 that leaves c - 8 exactly), and the products and sums run on the
-// tensor core.
+// kernel.  On the tensor core the products and sums leave the decode warps,
+// which only turn codes into an exact operand.
 //
-// Exact block scales.  A = the integer codes c - 8 (exact in bf16); the scale
-// d of each block is applied after the MMA, in fp32, so no weight is rounded.
-// The MMA's N dimension carries one column pair per block instead of one per
-// token: for a K-group of 256 (8 blocks), B is 16 columns x 256 K where column
-// 2j holds x_hi and column 2j + 1 holds x_lo over block j's 32 elements and
-// zeros elsewhere.  x_hi = bf16(x), x_lo = bf16(x - x_hi): their sum is x to
-// 2^-17 relative (bf16 activations are exact: x_lo = 0).  So after the 16 MMAs
-// of a group, D[row][2j] + D[row][2j + 1] is the block's exact-code dot
-// product sum_i (c_i - 8) x_i in fp32, and the row's thread adds
-// d_j * (D[2j] + D[2j + 1]) for j = 0..7, in that order.
+// Exact block scales.  A holds exact integer codes; the scale d of each block
+// is applied after the MMA, in fp32, so no weight is rounded.  The MMA's N
+// dimension carries one column pair per block instead of one per token: for a
+// K-group of 256 (8 blocks), B is 16 columns where columns 2j and 2j + 1 hold
+// two pieces of block j's activations (zeros elsewhere), and the row's thread
+// adds d_j (D[2j] + D[2j + 1]) for j = 0..7, in that order.  Two forms
+// (qmv_tc_common.cuh):
+// * 8-bit (kind::f8f6f4, one token): Q4_0's c - 8 as two e4m3 operands,
+//   c & 7 and 8 [bit 3 clear] (both 0 where c = 8), about 5.5 instructions
+//   per 8 codes; Q4_K's codes 0..15 as one.  Activations are e4m3 pieces under
+//   a power-of-two scale per block: two for bf16 x (exact), three for fp32
+//   (about 12 bits; the third in a second B, one more MMA per K-step).  The
+//   pieces and factors come from a table each CTA builds once.
+// * bf16-code (kind::f16): c - 8 exact in bf16 (byte permute, LOP3 with the
+//   exponent of 128, a packed add of -136), x as x_hi = bf16(x) and x_lo =
+//   bf16(x - x_hi), 2^-17 relative; two bf16 tokens take those two columns.
+//   It serves two tokens and shapes whose table would not fit.
 //
 // Work split (stream-K): the units are (128-row tile, K-group, matrix) triples
 // in that order (one matrix, or gate then up); CTA c of C takes units
@@ -39,12 +44,13 @@
 // Warp roles (16 warps): warps 0..11 are three sets of four dequantizing
 // warps; set s takes the CTA's units s, s + 3, ...; warp 4s + q owns rows
 // 32q .. 32q + 31 (its TMEM lane quarter) and one eighth of the group's B
-// operand (Q4_0: lanes 0..7; Q4_K: lanes 8q .. 8q + 7, while every lane loads
-// activations for the sub-block sums).  Warp 12 lane 0 issues the TMA copies of the raw rows
-// (128 rows x 144 bytes per unit) into a 6-stage ring.  Warp 13 + s lane 0
-// issues set s's MMAs (M = 128, N = 16, K = 16; 16 per unit) into set s's
-// accumulator.  Each set's rows read D back one unit later, while the next
-// unit's codes are already decoded in registers.
+// operand (lanes 0..7; the bf16-code Q4_K form: lanes 8q .. 8q + 7, while
+// every lane loads activations for the sub-block sums).  Warp 12 lane 0
+// issues the TMA copies of the raw rows (128 rows x 144 bytes per unit) into a
+// 6-stage ring.  Warp 13 + s lane 0 issues set s's MMAs (M = 128, N = 16; 16
+// K-steps per unit, 8 for 8-bit Q4_K) into one of set s's two D buffers.
+// Each set's rows read D back one unit later, while the next unit's codes are
+// already decoded in registers.
 #include <algorithm>
 #include <atomic>
 #include <cstdint>
