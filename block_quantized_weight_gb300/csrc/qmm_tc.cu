@@ -18,10 +18,11 @@
 // takes the CTA's K-groups g, g + 3, g + 6, ... and owns TMEM A stage g;
 // warp 4g + q of the set handles rows 32q .. 32q + 31 (the TMEM lanes of its
 // quarter) over the whole group.  Warp 12 lane 0 issues the TMA copies.
-// Warps 13 and 14 (lane 0) issue the MMAs: issuer j takes K-steps j, j + 2,
-// ... of every group into its own accumulator D_j, because one thread issues
-// a narrow (N <= 32) MMA only about every 50 cycles, well below what the
-// tensor core retires.  Warps 0..3 read D_0 + D_1 back.
+// Warps 13, 14 and 15 (lane 0) issue the MMAs: issuer j takes set j's groups
+// (all 16 K-steps of each) into its own accumulator D_j.  One thread issues a
+// narrow (N <= 32) MMA only about every 50 cycles, well below what the tensor
+// core retires, and issuing threads overlap, so three issuers keep up with
+// three sets.  Warps 0..3 read D_0 + D_1 + D_2 back.
 //
 // Dequantization to bf16, two adjacent weights j, j + 1 of a block at a time:
 // a byte permute puts qs[j] and qs[j + 1] in bytes 0 and 2 of a word; a LOP3
@@ -60,8 +61,8 @@ constexpr int kGroupBytes = 144;              // raw bytes per row per K-group
 constexpr int kSets = 3;                      // dequantizing warp sets = TMEM A stages
 constexpr int kDequantWarps = 4 * kSets;
 constexpr int kProducerWarp = kDequantWarps;
-constexpr int kMmaWarp0 = kDequantWarps + 1;  // and kMmaWarp0 + 1
-constexpr int kIssuers = 2;
+constexpr int kMmaWarp0 = kDequantWarps + 1;  // issuer j: warp kMmaWarp0 + j
+constexpr int kIssuers = kSets;               // one per set
 constexpr int kThreads = (kDequantWarps + 1 + kIssuers) * 32;
 constexpr int kStages = 6;                    // shared-memory stages (raw W + X)
 constexpr int kAStages = kSets;
@@ -186,59 +187,46 @@ __device__ __forceinline__ bool dequant_warp(int g, uint32_t raw_row, uint32_t a
     return true;
 }
 
-// One MMA issuer (lane 0 of its warp): K-steps J, J + 2, ... of each of the
-// CTA's ng K-groups into accumulator D_J.  Every operand of a group's eight
-// MMAs is formed before its barrier waits, and stage and phase are carried
-// incrementally, so that once the A stage is published the eight MMAs go out
-// back to back: this thread shares its SM sub-partition with three busy
-// dequantizing warps, and every instruction between two MMAs costs issue slots.
+// One MMA issuer (lane 0 of its warp): all 16 K-steps of set J's groups J,
+// J + 3, ... of the CTA's ng K-groups, into accumulator D_J.  Every operand
+// of a group's MMAs is formed before its barrier waits, and stage and phase
+// are carried incrementally, so that once the A stage is published the MMAs
+// go out back to back: this thread shares its SM sub-partition with three
+// busy dequantizing warps, and every instruction between two MMAs costs
+// issue slots.
 template <int J>
 __device__ __forceinline__ bool issue_mmas(uint32_t tmem, uint32_t sbase, uint32_t stage_bytes, uint32_t bar0, int nt,
                                            int ng, unsigned int* fault) {
-    constexpr int kSteps = kGroupK / 16 / kIssuers;          // 8 MMAs per group per issuer
+    constexpr int kSteps = kGroupK / 16;                     // 16 MMAs per group
     const uint32_t idesc = idesc_bf16(kTileRows, nt);
     const uint32_t d_tmem = tmem + kDCol + 32u * (uint32_t)J;
+    const uint32_t a_tmem = tmem + (uint32_t)J * kAColsPerStage;   // set J's A stage
     // X of stage s, atom t, 16-element slice c: descriptor start field advances
     // by stage_bytes / 16, nt * 128 / 16 and 32 / 16 respectively
     const uint64_t atom_step = (uint64_t)((uint32_t)nt * 8u);
     const uint64_t stage_step = (uint64_t)(stage_bytes >> 4);
     uint64_t koff[kSteps];
 #pragma unroll
-    for (int kk = 0; kk < kSteps; ++kk) {
-        const int k = kIssuers * kk + J;
-        koff[kk] = (uint64_t)(k >> 2) * atom_step + (uint64_t)((k & 3) * 2);
-    }
-    uint64_t ds = sw128_desc(sbase + kRawStageBytes);
-    int s = 0, a = 0;
-    uint32_t sphase = 0, aphase = 0;
+    for (int k = 0; k < kSteps; ++k) koff[k] = (uint64_t)(k >> 2) * atom_step + (uint64_t)((k & 3) * 2);
+    // group i = J + 3 t sits in stage i % 6, pass i / 6, and uses A stage J for
+    // the t-th time
+    const uint64_t ds0 = sw128_desc(sbase + kRawStageBytes);
+    uint32_t aphase = 0;
     bool ok = true;
-    for (int i = 0; i < ng; ++i) {
-        uint64_t dk[kSteps];
-#pragma unroll
-        for (int kk = 0; kk < kSteps; ++kk) dk[kk] = ds + koff[kk];
-        const uint32_t a_tmem = tmem + (uint32_t)a * kAColsPerStage + (uint32_t)J * 8u;
+    for (int i = J; i < ng; i += kSets) {
+        const int s = i % kStages;
+        const uint32_t sphase = (uint32_t)(i / kStages) & 1u;
+        const uint64_t ds = ds0 + (uint64_t)s * stage_step;
         ok = mbar_wait_bounded(full_bar_at(bar0, s), sphase, fault, kFaultMmaWaitTimeout) &&
-             mbar_wait_bounded(afull_bar_at(bar0, a), aphase, fault, kFaultMmaWaitTimeout);
+             mbar_wait_bounded(afull_bar_at(bar0, J), aphase, fault, kFaultMmaWaitTimeout);
         if (!ok) break;
         tc_fence_after();
-        const uint32_t acc0 = (i > 0) ? 1u : 0u;
-        tc_mma(d_tmem, a_tmem, dk[0], idesc, acc0);
+        tc_mma(d_tmem, a_tmem, ds + koff[0], idesc, (i > J) ? 1u : 0u);
 #pragma unroll
-        for (int kk = 1; kk < kSteps; ++kk)
-            tc_mma(d_tmem, a_tmem + (uint32_t)(kIssuers * kk) * 8u, dk[kk], idesc, 1u);
+        for (int k = 1; k < kSteps; ++k) tc_mma(d_tmem, a_tmem + 8u * (uint32_t)k, ds + koff[k], idesc, 1u);
         tc_commit(empty_bar_at(bar0, s));     // X tile of stage s consumed
-        tc_commit(aempty_bar_at(bar0, a));    // TMEM A stage a consumed
-        if (++s == kStages) {
-            s = 0;
-            sphase ^= 1u;
-            ds -= (uint64_t)(kStages - 1) * stage_step;
-        } else {
-            ds += stage_step;
-        }
-        if (++a == kAStages) {
-            a = 0;
-            aphase ^= 1u;
-        }
+        tc_commit(aempty_bar_at(bar0, J));    // TMEM A stage J consumed
+        aphase ^= 1u;
     }
     // completes when every MMA issued above has finished, even after a
     // timeout (the accumulator is then not read, only TMEM released)
@@ -321,11 +309,11 @@ __global__ void __launch_bounds__(kThreads, 1) qmm_q4_0_tc_kernel(const __grid_c
         if (lane == 0) {
             for (int s = 0; s < kStages; ++s) {
                 mbar_init(full_bar_at(bar0, s), 1);
-                mbar_init(empty_bar_at(bar0, s), 4 + kIssuers);   // the group's 4 dequantizing warps + the MMA commits
+                mbar_init(empty_bar_at(bar0, s), 4 + 1);   // the group's 4 dequantizing warps + its issuer's commit
             }
             for (int a = 0; a < kAStages; ++a) {
                 mbar_init(afull_bar_at(bar0, a), 4);
-                mbar_init(aempty_bar_at(bar0, a), kIssuers);
+                mbar_init(aempty_bar_at(bar0, a), 1);
             }
             mbar_init(dfull_bar, kIssuers);
             fence_mbar_init();
@@ -367,11 +355,12 @@ __global__ void __launch_bounds__(kThreads, 1) qmm_q4_0_tc_kernel(const __grid_c
     grid_launch_dependents();
 
     if (warp >= kMmaWarp0) {
-        // ---------------- MMA issuers: issuer j takes K-steps j, j + 2, ... of every group
+        // ---------------- MMA issuers: issuer j takes set j's groups
         const uint32_t tmem = *tmem_slot;
         if (lane == 0) {
             if (warp == kMmaWarp0) ok = issue_mmas<0>(tmem, sbase, stage_bytes, bar0, p.NT, ng, p.fault);
-            else ok = issue_mmas<1>(tmem, sbase, stage_bytes, bar0, p.NT, ng, p.fault);
+            else if (warp == kMmaWarp0 + 1) ok = issue_mmas<1>(tmem, sbase, stage_bytes, bar0, p.NT, ng, p.fault);
+            else ok = issue_mmas<2>(tmem, sbase, stage_bytes, bar0, p.NT, ng, p.fault);
         }
     } else if (warp < kDequantWarps) {
         // ---------------- dequantizing warps
@@ -381,7 +370,7 @@ __global__ void __launch_bounds__(kThreads, 1) qmm_q4_0_tc_kernel(const __grid_c
         ok = dequant_warp(set, (uint32_t)row * kGroupBytes,
                           tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)set * kAColsPerStage, sbase,
                           stage_bytes, bar0, lane, ng, p.fault);
-        // ---------------- epilogue: warps 0..3 read D_0 + D_1 (128 rows x NT) and emit
+        // ---------------- epilogue: warps 0..3 read D_0 + D_1 + D_2 (128 rows x NT) and emit
         if (warp < 4) {
             const bool got = ok && mbar_wait_bounded(dfull_bar, 0u, p.fault, kFaultMmaWaitTimeout);
             if (__all_sync(0xffffffffu, got)) {
@@ -390,14 +379,18 @@ __global__ void __launch_bounds__(kThreads, 1) qmm_q4_0_tc_kernel(const __grid_c
                 const int mp = (p.M + 3) & ~3;
                 float* part = p.partials + ((size_t)(split * p.tiles + tile) * kTileRows + row) * (size_t)mp;
                 for (int c0 = 0; c0 < p.NT; c0 += 16) {
-                    uint32_t d0[16], d1[16];
+                    uint32_t d0[16], d1[16], d2[16];
                     const uint32_t lane_base = tmem + ((uint32_t)(quarter * 32) << 16) + kDCol + (uint32_t)c0;
                     tmem_ld16(lane_base, d0);
                     tmem_ld16(lane_base + 32u, d1);
+                    tmem_ld16(lane_base + 64u, d2);
                     tmem_wait_ld();
                     float v[16];
+                    // D_j holds nothing when the CTA has no group j (ng <= j)
 #pragma unroll
-                    for (int q = 0; q < 16; ++q) v[q] = __uint_as_float(d0[q]) + __uint_as_float(d1[q]);
+                    for (int q = 0; q < 16; ++q)
+                        v[q] = (__uint_as_float(d0[q]) + (ng > 1 ? __uint_as_float(d1[q]) : 0.f)) +
+                               (ng > 2 ? __uint_as_float(d2[q]) : 0.f);
                     if (p.splits == 1) {
                         if (n < p.N) {
 #pragma unroll
