@@ -26,8 +26,8 @@ cudaError_t prepare_stream_gateup(int R, size_t smem);
 cudaError_t launch_qmm_generic(const uint8_t* w, const void* X, void* Y, int y_bf16, int64_t M, int64_t N,
                                int64_t K, int sm_count, cudaStream_t stream);
 cudaError_t launch_qmm_tc(const CUtensorMap& tmap_w, const CUtensorMap& tmap_x, void* y, int y_bf16, float* partials,
-                          unsigned int* counters, unsigned int* fault, int M, int N, int K, int splits,
-                          int cluster, cudaStream_t stream);
+                          unsigned int* counters, unsigned long long* share, unsigned int* fault, int M, int N, int K,
+                          int splits, int cluster, int streamk_ctas, cudaStream_t stream);
 int qmm_tc_max_active_clusters(int nt, int cluster);
 cudaError_t launch_selftest_wait(int which, uint64_t limit_ns, unsigned int* fault, cudaStream_t stream);
 bool qmv_tc_supported(int nmat, int64_t N, int64_t K, int sm_count);
@@ -261,8 +261,10 @@ bool encode_x_map(CUtensorMap* m, const void* X, int64_t M, int64_t K, int nt) {
 //
 // Workspace layout, the same for every shape so that one workspace can serve
 // calls of different shapes: the tile arrival counters first, in a fixed
-// region of kQmmCounterBytes, then the partial sums.  Each call returns its
-// counters to zero, and no call's partial sums ever land on a counter.
+// region of kQmmCounterBytes, then the partial sums (or, for a stream-K plan,
+// the CTAs' tagged shares).  Each call leaves the whole workspace zero again:
+// counters reset, partial sums cleared, shares' tags cleared by the finishing
+// CTA.
 constexpr size_t kQmmCounterBytes = 4096;
 //
 // With 2 .. 8 splits per tile, and room on the device for all tiles' clusters
@@ -273,7 +275,8 @@ struct QmmPlan {
     bool tc = false, cluster = false;
     bool exact = false;    // one or two token rows on the exact-code M = 1 kernel (qmv_tc.cu)
     int tiles = 0, splits = 1;
-    size_t partial_off = 0, workspace = 0;
+    int streamk_ctas = 0;  // > 0: stream-K over this many CTAs (one per SM), shares at share_off
+    size_t partial_off = 0, share_off = 0, workspace = 0;
 };
 
 int qmm_clusters_fit(DeviceInfo& di, int nt, int cluster) {
@@ -299,6 +302,24 @@ QmmPlan plan_qmm(int64_t M, int64_t N, int64_t K, DeviceInfo& di) {
     int splits = di.sm_count / q.tiles;
     if (splits < 1) splits = 1;
     if (splits > groups) splits = groups;
+    // Stream-K (M <= 16, so that two segments' accumulators fit TMEM): one CTA
+    // per SM over equal ranges of the (tile, K-group) units.  It pays for its
+    // tagged-share finish (measured at 2 to 4 us) only on long ranges (at least
+    // 16 groups a CTA), where whole-tile splits add partial sums anyway (two
+    // or more splits) and the busiest CTA then runs at least two and an eighth
+    // fewer groups.  With fewer tiles than SMs no range is longer than a tile.
+    const int64_t units = (int64_t)q.tiles * groups;
+    const int ctas = di.sm_count;
+    const int64_t busiest_split = (groups + splits - 1) / splits, busiest_streamk = (units + ctas - 1) / ctas;
+    if (M <= 16 && splits >= 2 && q.tiles < ctas && units >= 16 * (int64_t)ctas &&
+        busiest_split - busiest_streamk >= 2 && 8 * busiest_streamk <= 7 * busiest_split) {
+        q.streamk_ctas = ctas;
+        q.share_off = kQmmCounterBytes;
+        // shares [ctas][M rounded up to 4][128 rows] of 64-bit tagged words
+        const size_t mp = (size_t)((M + 3) / 4 * 4);
+        q.workspace = kQmmCounterBytes + align_up((size_t)ctas * mp * (size_t)qmm_tc_tile_rows() * 8, 256);
+        return q;
+    }
     if (splits >= 2 && splits <= kQmmMaxCluster &&
         qmm_clusters_fit(di, (int)((M + 15) / 16 * 16), splits) >= q.tiles) {
         q.splits = splits;
@@ -525,10 +546,12 @@ qbw_status qmm_q4_0_smallM(const void* w, const void* X, qbw_dtype xt, void* Y, 
         const int nt = (int)((M + 15) / 16 * 16);
         if (encode_q4_tile_map(&tw, w, N, K) && encode_x_map(&tx, X, M, K, nt)) {
             uint8_t* ws = static_cast<uint8_t*>(workspace);
-            cudaError_t e = launch_qmm_tc(tw, tx, Y, yt == QBW_BF16,
-                                          q.workspace ? reinterpret_cast<float*>(ws + q.partial_off) : nullptr,
-                                          q.workspace ? reinterpret_cast<unsigned int*>(ws) : nullptr,
-                                          di->fault, (int)M, (int)N, (int)K, q.splits, q.cluster ? 1 : 0, s);
+            const bool sk = q.streamk_ctas > 0;
+            cudaError_t e = launch_qmm_tc(
+                tw, tx, Y, yt == QBW_BF16, q.workspace && !sk ? reinterpret_cast<float*>(ws + q.partial_off) : nullptr,
+                q.workspace && !sk ? reinterpret_cast<unsigned int*>(ws) : nullptr,
+                sk ? reinterpret_cast<unsigned long long*>(ws + q.share_off) : nullptr, di->fault, (int)M, (int)N,
+                (int)K, q.splits, q.cluster ? 1 : 0, q.streamk_ctas, s);
             return e == cudaSuccess ? QBW_OK : QBW_ECUDA;
         }
     }

@@ -105,6 +105,12 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
     return true;
 }
 
+// Publish or clear a tagged 64-bit word (value in the lower half, tag in the
+// upper): one store, so a reader sees the old word or the new one whole.
+__device__ __forceinline__ void st_relaxed_u64(unsigned long long* p, unsigned long long v) {
+    asm volatile("st.relaxed.gpu.global.b64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+
 // Wait until the 64-bit word at p carries a nonzero tag (its upper half),
 // reading it with relaxed gpu-scope loads, giving up after limit_ns.  Returns
 // the last word read; on timeout records `code` (the word's tag is then 0).

@@ -43,7 +43,22 @@
 // CTA's shared memory alive until its peers have read it.  With more splits,
 // each CTA writes its partial tile to the workspace; the last CTA of a tile
 // (counted with an atomic) adds the partials in split order and writes Y,
-// then resets the counter so the workspace stays zero-filled.
+// then resets the counter and clears the partials, so the workspace is all
+// zero again after every call.
+//
+// Stream-K (M <= 16).  When whole-tile splits would leave SMs idle (42 tiles
+// of 3 splits use 126 of 152), one CTA per SM takes an equal range of the
+// (tile, K-group) units in tile-major order instead.  A range meets at most
+// two tiles (it is never longer than a tile), so a CTA has one or two
+// segments, each with its own three accumulators (TMEM 384 + 2 x 3 x 16
+// columns).  A segment that starts inside a tile is a share: the CTA
+// publishes it as one tagged 64-bit word (fp32 bits, tag 1) per row and token
+// column; the first of two segments is published mid-range by the set that
+// ran its last group, as soon as its MMAs have completed.  The CTA that covers
+// a tile's first group finishes the tile at the end of its range: it adds the
+// later CTAs' shares after its own, in CTA order, clears their tags and writes
+// Y.  A range covering a whole tile writes Y directly.  Results depend only on
+// the plan, so they are bit-reproducible.
 #include <cstdint>
 
 #include "qbw_device.cuh"
@@ -68,7 +83,7 @@ constexpr int kStages = 6;                    // shared-memory stages (raw W + X
 constexpr int kAStages = kSets;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kAColsPerStage = kGroupK / 2;          // 2 bf16 per 32-bit column
-constexpr uint32_t kDCol = kAStages * kAColsPerStage;     // accumulator D_j at kDCol + 32 j
+constexpr uint32_t kDCol = kAStages * kAColsPerStage;     // accumulator D_j of segment s at kDCol + NT (3 s + j)
 constexpr uint32_t kRawStageBytes = kTileRows * kGroupBytes;   // 18432
 constexpr int kReduceItems = 3;               // row x 4-column items per thread in the split-K sum: 480 x 3 >= 128 x 8
 
@@ -118,8 +133,29 @@ __device__ __forceinline__ void dequant_pair(const uint32_t (&v)[36], uint32_t (
     dequant_block<36 * P + 20, 9 * P + 4, 1>(v, col + 16);
 }
 
+struct QmmParams {
+    CUtensorMap tmap_w;     // Q4_0 rows as 8-byte words, box (18, 128)
+    CUtensorMap tmap_x;     // X [M][K] bf16, box (64, NT), 128-byte swizzle
+    void* y;
+    float* partials;        // [splits][tiles][128][M rounded up to 4] fp32 (splits > 1)
+    unsigned int* counters; // [tiles] (splits > 1)
+    unsigned long long* share;   // stream-K: [ctas][M rounded up to 4][128] tagged words
+    unsigned int* fault;
+    int32_t M, N, K;
+    int32_t NT;             // MMA N: M rounded up to 16
+    int32_t groups;         // K / 256
+    int32_t splits;
+    int32_t tiles;          // ceil(N / 128)
+    int32_t y_bf16;
+    int32_t cluster;        // 1: the splits of a tile are one cluster (no workspace)
+    int32_t streamk;        // 1: ctas CTAs over `units` (tile, group) units (NT = 16)
+    int32_t ctas;
+    int32_t units;          // tiles * groups
+};
+
 // Barrier layout shared by every role: full[kStages], empty[kStages],
-// afull[kAStages], aempty[kAStages], dfull, 8 bytes each from bar0.
+// afull[kAStages], aempty[kAStages], dfull, dmid, 8 bytes each from bar0.
+constexpr int kBarriers = 2 * kStages + 2 * kAStages + 2;
 __device__ __forceinline__ uint32_t full_bar_at(uint32_t bar0, int s) { return bar0 + 8u * (uint32_t)s; }
 __device__ __forceinline__ uint32_t empty_bar_at(uint32_t bar0, int s) { return bar0 + 8u * (uint32_t)(kStages + s); }
 __device__ __forceinline__ uint32_t afull_bar_at(uint32_t bar0, int a) {
@@ -131,6 +167,70 @@ __device__ __forceinline__ uint32_t aempty_bar_at(uint32_t bar0, int a) {
 __device__ __forceinline__ uint32_t dfull_bar_at(uint32_t bar0) {
     return bar0 + 8u * (uint32_t)(2 * kStages + 2 * kAStages);
 }
+// dmid: every MMA of the first of two stream-K segments has completed
+__device__ __forceinline__ uint32_t dmid_bar_at(uint32_t bar0) {
+    return bar0 + 8u * (uint32_t)(2 * kStages + 2 * kAStages + 1);
+}
+
+// v[q] = sum of the included accumulators' column q (16 columns from taddr;
+// D_1 and D_2 at nt and 2 nt columns further), added in issuer order.
+__device__ __forceinline__ void read_d(uint32_t taddr, uint32_t nt, bool i0, bool i1, bool i2, float (&v)[16]) {
+    uint32_t d0[16], d1[16], d2[16];
+    tmem_ld16(taddr, d0);
+    tmem_ld16(taddr + nt, d1);
+    tmem_ld16(taddr + 2u * nt, d2);
+    tmem_wait_ld();
+#pragma unroll
+    for (int q = 0; q < 16; ++q)
+        v[q] = ((i0 ? __uint_as_float(d0[q]) : 0.f) + (i1 ? __uint_as_float(d1[q]) : 0.f)) +
+               (i2 ? __uint_as_float(d2[q]) : 0.f);
+}
+
+// The same one accumulator at a time, for the mid-range publish, which runs
+// while a group's codes are held in registers.
+__device__ __forceinline__ void read_d_lean(uint32_t taddr, uint32_t nt, bool i1, bool i2, float (&v)[16]) {
+    uint32_t d[16];
+    tmem_ld16(taddr, d);
+    tmem_wait_ld();
+#pragma unroll
+    for (int q = 0; q < 16; ++q) v[q] = __uint_as_float(d[q]);
+    tmem_ld16(taddr + nt, d);
+    tmem_wait_ld();
+#pragma unroll
+    for (int q = 0; q < 16; ++q) v[q] += i1 ? __uint_as_float(d[q]) : 0.f;
+    tmem_ld16(taddr + 2u * nt, d);
+    tmem_wait_ld();
+#pragma unroll
+    for (int q = 0; q < 16; ++q) v[q] += i2 ? __uint_as_float(d[q]) : 0.f;
+}
+
+__device__ __forceinline__ unsigned long long ld_relaxed_u64(const unsigned long long* p) {
+    unsigned long long w;
+    asm volatile("ld.relaxed.gpu.global.b64 %0, [%1];" : "=l"(w) : "l"(p) : "memory");
+    return w;
+}
+
+// A row's share: token column q at dst[128 q], as (fp32 bits, tag 1).
+__device__ __forceinline__ void store_share(unsigned long long* dst, const float (&v)[16], int mp) {
+#pragma unroll
+    for (int q = 0; q < 16; ++q)
+        if (q < mp) st_relaxed_u64(dst + (size_t)q * kTileRows, (1ull << 32) | (unsigned long long)__float_as_uint(v[q]));
+}
+
+// The first of a stream-K CTA's two segments (its groups 0 .. last_group),
+// published by the set that ran its last group once the segment's MMAs have
+// completed.  d_taddr: the quarter's TMEM lanes at the segment's D_0.
+__device__ __forceinline__ bool publish_mid(const QmmParams& p, int last_group, uint32_t d_taddr, uint32_t bar0) {
+    const bool got = mbar_wait_bounded(dmid_bar_at(bar0), 0u, p.fault, kFaultMmaWaitTimeout);
+    if (!__all_sync(0xffffffffu, got)) return false;
+    tc_fence_after();
+    float v[16];
+    read_d_lean(d_taddr, 16u, last_group >= 1, last_group >= 2, v);
+    const int mp = (p.M + 3) & ~3;
+    const int row = (int)(threadIdx.x & 127u);   // warp 4g + q, lane l: row 32 q + l
+    store_share(p.share + (size_t)blockIdx.x * mp * kTileRows + row, v, mp);
+    return true;
+}
 
 // One dequantizing warp of set g over the CTA's K-groups g, g + 3, ...
 // Per group: wait for the raw stage; read the lane's 144 bytes with nine
@@ -139,10 +239,16 @@ __device__ __forceinline__ uint32_t dfull_bar_at(uint32_t bar0) {
 // block pairs into two alternating register buffers and store each into TMEM
 // A stage g.  A buffer is rewritten only after a tcgen05.wait::st covering
 // its previous store.  raw_row: the row's byte offset within a stage;
-// a_taddr: TMEM address of the quarter's lanes, A stage g, column 0.
+// a_taddr: TMEM address of the quarter's lanes, A stage g, column 0.  With
+// two stream-K segments (mid >= 0: the first one's last group), the set that
+// runs group mid publishes the first segment's share, right after its next
+// A-stage wait (which follows the same MMAs) or after its last group.
+template <bool SK>
 __device__ __forceinline__ bool dequant_warp(int g, uint32_t raw_row, uint32_t a_taddr, uint32_t sbase,
-                                             uint32_t stage_bytes, uint32_t bar0, int lane, int ng,
-                                             unsigned int* fault) {
+                                             uint32_t stage_bytes, uint32_t bar0, int lane, int ng, int mid,
+                                             const QmmParams& p) {
+    unsigned int* const fault = p.fault;
+    const uint32_t d_taddr = a_taddr - (uint32_t)g * kAColsPerStage + kDCol;
     for (int i = g; i < ng; i += kSets) {
         const int s = i % kStages;
         const bool got = mbar_wait_bounded(full_bar_at(bar0, s), (uint32_t)(i / kStages) & 1u, fault,
@@ -168,6 +274,8 @@ __device__ __forceinline__ bool dequant_warp(int g, uint32_t raw_row, uint32_t a
                                                 kFaultMmaWaitTimeout);
             if (!__all_sync(0xffffffffu, free)) return false;
             tc_fence_after();
+            if constexpr (SK)
+                if (i - kSets == mid && !publish_mid(p, mid, d_taddr, bar0)) return false;
         }
         tmem_st32(a_taddr, c0);
         dequant_pair<1>(v, c1);
@@ -184,22 +292,26 @@ __device__ __forceinline__ bool dequant_warp(int g, uint32_t raw_row, uint32_t a
         __syncwarp();
         if (lane == 0) mbar_arrive(afull_bar_at(bar0, g));
     }
+    if constexpr (SK)
+        if (mid >= 0 && mid % kSets == g && mid + kSets >= ng) return publish_mid(p, mid, d_taddr, bar0);
     return true;
 }
 
 // One MMA issuer (lane 0 of its warp): all 16 K-steps of set J's groups J,
-// J + 3, ... of the CTA's ng K-groups, into accumulator D_J.  Every operand
+// J + 3, ... of the CTA's ng K-groups, into accumulator D_J of the group's
+// segment (groups below nA: the first; the rest: the second).  Every operand
 // of a group's MMAs is formed before its barrier waits, and stage and phase
 // are carried incrementally, so that once the A stage is published the MMAs
 // go out back to back: this thread shares its SM sub-partition with three
 // busy dequantizing warps, and every instruction between two MMAs costs
 // issue slots.
-template <int J>
+template <int J, bool SK>
 __device__ __forceinline__ bool issue_mmas(uint32_t tmem, uint32_t sbase, uint32_t stage_bytes, uint32_t bar0, int nt,
-                                           int ng, unsigned int* fault) {
+                                           int ng, int nA, unsigned int* fault) {
     constexpr int kSteps = kGroupK / 16;                     // 16 MMAs per group
     const uint32_t idesc = idesc_bf16(kTileRows, nt);
-    const uint32_t d_tmem = tmem + kDCol + 32u * (uint32_t)J;
+    const uint32_t d_seg0 = tmem + kDCol + (uint32_t)nt * (uint32_t)J;
+    const uint32_t d_seg1 = d_seg0 + 3u * (uint32_t)nt;
     const uint32_t a_tmem = tmem + (uint32_t)J * kAColsPerStage;   // set J's A stage
     // X of stage s, atom t, 16-element slice c: descriptor start field advances
     // by stage_bytes / 16, nt * 128 / 16 and 32 / 16 respectively
@@ -213,42 +325,36 @@ __device__ __forceinline__ bool issue_mmas(uint32_t tmem, uint32_t sbase, uint32
     const uint64_t ds0 = sw128_desc(sbase + kRawStageBytes);
     uint32_t aphase = 0;
     bool ok = true;
+    bool owe_mid = SK && nA < ng;     // two segments: dmid marks the end of the first
     for (int i = J; i < ng; i += kSets) {
         const int s = i % kStages;
         const uint32_t sphase = (uint32_t)(i / kStages) & 1u;
         const uint64_t ds = ds0 + (uint64_t)s * stage_step;
+        const bool seg1 = SK && i >= nA;
+        const uint32_t d_tmem = seg1 ? d_seg1 : d_seg0;
+        const uint32_t acc0 = (seg1 ? i - kSets >= nA : i > J) ? 1u : 0u;
+        if (owe_mid && seg1) {
+            tc_commit(dmid_bar_at(bar0));     // this issuer's first-segment MMAs
+            owe_mid = false;
+        }
         ok = mbar_wait_bounded(full_bar_at(bar0, s), sphase, fault, kFaultMmaWaitTimeout) &&
              mbar_wait_bounded(afull_bar_at(bar0, J), aphase, fault, kFaultMmaWaitTimeout);
         if (!ok) break;
         tc_fence_after();
-        tc_mma(d_tmem, a_tmem, ds + koff[0], idesc, (i > J) ? 1u : 0u);
+        tc_mma(d_tmem, a_tmem, ds + koff[0], idesc, acc0);
 #pragma unroll
         for (int k = 1; k < kSteps; ++k) tc_mma(d_tmem, a_tmem + 8u * (uint32_t)k, ds + koff[k], idesc, 1u);
         tc_commit(empty_bar_at(bar0, s));     // X tile of stage s consumed
         tc_commit(aempty_bar_at(bar0, J));    // TMEM A stage J consumed
         aphase ^= 1u;
     }
+    if (owe_mid) tc_commit(dmid_bar_at(bar0));
     // completes when every MMA issued above has finished, even after a
     // timeout (the accumulator is then not read, only TMEM released)
     tc_commit(dfull_bar_at(bar0));
     return ok;
 }
 
-struct QmmParams {
-    CUtensorMap tmap_w;     // Q4_0 rows as 8-byte words, box (18, 128)
-    CUtensorMap tmap_x;     // X [M][K] bf16, box (64, NT), 128-byte swizzle
-    void* y;
-    float* partials;        // [splits][tiles][128][M rounded up to 4] fp32 (splits > 1)
-    unsigned int* counters; // [tiles] (splits > 1)
-    unsigned int* fault;
-    int32_t M, N, K;
-    int32_t NT;             // MMA N: M rounded up to 16
-    int32_t groups;         // K / 256
-    int32_t splits;
-    int32_t tiles;          // ceil(N / 128)
-    int32_t y_bf16;
-    int32_t cluster;        // 1: the splits of a tile are one cluster (no workspace)
-};
 
 __device__ __forceinline__ void cluster_sync_all() {
     asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
@@ -269,13 +375,42 @@ __device__ __forceinline__ float4 ld_dsmem_f4(uint32_t a, uint32_t rank) {
     return v;
 }
 
+// SK: a stream-K plan (p.streamk = 1); the split-K plans compile without its code.
+template <bool SK>
 __global__ void __launch_bounds__(kThreads, 1) qmm_q4_0_tc_kernel(const __grid_constant__ QmmParams p) {
     extern __shared__ __align__(1024) uint8_t smem[];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int tile = blockIdx.x / p.splits, split = blockIdx.x - tile * p.splits;
-    const int g_begin = (int)((int64_t)p.groups * split / p.splits);
-    const int g_end = (int)((int64_t)p.groups * (split + 1) / p.splits);
-    const int ng = g_end - g_begin;
+    // The CTA's ng K-groups: groups g_begin .. g_begin + nA - 1 of `tile`, then
+    // (stream-K only) groups 0 .. ng - nA - 1 of tile + 1.
+    int tile, split, g_begin, ng, nA;
+    if constexpr (SK) {
+        const int u0 = (int)((int64_t)p.units * blockIdx.x / p.ctas);
+        const int u1 = (int)((int64_t)p.units * (blockIdx.x + 1) / p.ctas);
+        tile = u0 / p.groups;
+        g_begin = u0 - tile * p.groups;
+        split = 0;
+        ng = u1 - u0;
+        nA = min(ng, p.groups - g_begin);
+        // the plan keeps NT = 16 (the two segments' accumulators fit TMEM) and
+        // every range non-empty and no longer than a tile
+        if (p.NT != 16 || ng < 1 || ng > p.groups) {
+            if (threadIdx.x == 0) record_fault(p.fault, kFaultPlan);
+            return;
+        }
+    } else {
+        tile = blockIdx.x / p.splits;
+        split = blockIdx.x - tile * p.splits;
+        g_begin = (int)((int64_t)p.groups * split / p.splits);
+        ng = (int)((int64_t)p.groups * (split + 1) / p.splits) - g_begin;
+        nA = ng;
+    }
+    const bool two = SK && nA < ng;
+    // the last segment: its tile, first group there and length; a stream-K
+    // CTA that covers a tile's first group but not all of it finishes the tile
+    const int tile_e = two ? tile + 1 : tile;
+    const int start_e = two ? 0 : g_begin;
+    const int len_e = ng - (two ? nA : 0);
+    const bool finisher = SK && start_e == 0 && len_e < p.groups;
 
     // shared memory: [stages][raw W 18432 B | X NT x 256 bf16] (1024-aligned), barriers, TMEM slot
     const uint32_t xbytes = (uint32_t)p.NT * kGroupK * 2;            // 4 swizzle atoms of NT x 128 B
@@ -283,23 +418,24 @@ __global__ void __launch_bounds__(kThreads, 1) qmm_q4_0_tc_kernel(const __grid_c
     const uint32_t sbase = smem_u32(smem);
     const uint32_t bar0 = sbase + kStages * stage_bytes;
     const uint32_t dfull_bar = dfull_bar_at(bar0);
-    uint32_t* tmem_slot =
-        reinterpret_cast<uint32_t*>(smem + kStages * stage_bytes + 8 * (2 * kStages + 2 * kAStages + 1));
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kStages * stage_bytes + 8 * kBarriers);
     bool ok = true;
 
     // K-group i of this CTA -> stage i % kStages: raw W box and the 4 X boxes
     auto issue_w = [&](int i) {
         const int s = i % kStages;
         mbar_arrive_expect_tx(full_bar_at(bar0, s), kRawStageBytes + xbytes);
-        tma_load_2d(sbase + (uint32_t)s * stage_bytes, &p.tmap_w, (g_begin + i) * (kGroupBytes / 8), tile * kTileRows,
-                    full_bar_at(bar0, s), policy_evict_first());
+        const bool seg1 = SK && i >= nA;
+        tma_load_2d(sbase + (uint32_t)s * stage_bytes, &p.tmap_w, (seg1 ? i - nA : g_begin + i) * (kGroupBytes / 8),
+                    (seg1 ? tile + 1 : tile) * kTileRows, full_bar_at(bar0, s), policy_evict_first());
     };
     auto issue_x = [&](int i) {
         const uint32_t st = sbase + (uint32_t)(i % kStages) * stage_bytes;
 #pragma unroll
         for (int a = 0; a < 4; ++a)
             tma_load_2d(st + kRawStageBytes + (uint32_t)a * (uint32_t)p.NT * 128u, &p.tmap_x,
-                        (g_begin + i) * kGroupK + a * 64, 0, full_bar_at(bar0, i % kStages), 0ull);
+                        ((SK && i >= nA) ? i - nA : g_begin + i) * kGroupK + a * 64, 0, full_bar_at(bar0, i % kStages),
+                        0ull);
     };
 
     // The producer initialises the barriers, releases everyone else through
@@ -316,6 +452,7 @@ __global__ void __launch_bounds__(kThreads, 1) qmm_q4_0_tc_kernel(const __grid_c
                 mbar_init(aempty_bar_at(bar0, a), 1);
             }
             mbar_init(dfull_bar, kIssuers);
+            if constexpr (SK) mbar_init(dmid_bar_at(bar0), kIssuers);
             fence_mbar_init();
         }
         __syncwarp();
@@ -358,40 +495,53 @@ __global__ void __launch_bounds__(kThreads, 1) qmm_q4_0_tc_kernel(const __grid_c
         // ---------------- MMA issuers: issuer j takes set j's groups
         const uint32_t tmem = *tmem_slot;
         if (lane == 0) {
-            if (warp == kMmaWarp0) ok = issue_mmas<0>(tmem, sbase, stage_bytes, bar0, p.NT, ng, p.fault);
-            else if (warp == kMmaWarp0 + 1) ok = issue_mmas<1>(tmem, sbase, stage_bytes, bar0, p.NT, ng, p.fault);
-            else ok = issue_mmas<2>(tmem, sbase, stage_bytes, bar0, p.NT, ng, p.fault);
+            if (warp == kMmaWarp0) ok = issue_mmas<0, SK>(tmem, sbase, stage_bytes, bar0, p.NT, ng, nA, p.fault);
+            else if (warp == kMmaWarp0 + 1) ok = issue_mmas<1, SK>(tmem, sbase, stage_bytes, bar0, p.NT, ng, nA, p.fault);
+            else ok = issue_mmas<2, SK>(tmem, sbase, stage_bytes, bar0, p.NT, ng, nA, p.fault);
         }
     } else if (warp < kDequantWarps) {
         // ---------------- dequantizing warps
         const uint32_t tmem = *tmem_slot;
         const int set = warp >> 2, quarter = warp & 3;   // TMEM lanes 32 quarter .. +31
         const int row = quarter * 32 + lane;             // weight row within the tile
-        ok = dequant_warp(set, (uint32_t)row * kGroupBytes,
+        ok = dequant_warp<SK>(set, (uint32_t)row * kGroupBytes,
                           tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)set * kAColsPerStage, sbase,
-                          stage_bytes, bar0, lane, ng, p.fault);
-        // ---------------- epilogue: warps 0..3 read D_0 + D_1 + D_2 (128 rows x NT) and emit
+                          stage_bytes, bar0, lane, ng, two ? nA - 1 : -1, p);
+        // ---------------- epilogue: warps 0..3 read the last segment's D_0 + D_1 + D_2
+        // (128 rows x NT) and emit
         if (warp < 4) {
             const bool got = ok && mbar_wait_bounded(dfull_bar, 0u, p.fault, kFaultMmaWaitTimeout);
             if (__all_sync(0xffffffffu, got)) {
                 tc_fence_after();
-                const int n = tile * kTileRows + row;
+                const int n = tile_e * kTileRows + row;
+                // issuer j has groups in the last segment (D_j holds nothing otherwise)
+                bool inc[kSets];
+#pragma unroll
+                for (int j = 0; j < kSets; ++j) inc[j] = two ? (j - nA % kSets + kSets) % kSets < len_e : j < ng;
                 const int mp = (p.M + 3) & ~3;
                 float* part = p.partials + ((size_t)(split * p.tiles + tile) * kTileRows + row) * (size_t)mp;
+                const uint32_t lane_base = tmem + ((uint32_t)(quarter * 32) << 16) + kDCol + (two ? 3u * p.NT : 0u);
                 for (int c0 = 0; c0 < p.NT; c0 += 16) {
-                    uint32_t d0[16], d1[16], d2[16];
-                    const uint32_t lane_base = tmem + ((uint32_t)(quarter * 32) << 16) + kDCol + (uint32_t)c0;
-                    tmem_ld16(lane_base, d0);
-                    tmem_ld16(lane_base + 32u, d1);
-                    tmem_ld16(lane_base + 64u, d2);
-                    tmem_wait_ld();
                     float v[16];
-                    // D_j holds nothing when the CTA has no group j (ng <= j)
+                    read_d(lane_base + (uint32_t)c0, (uint32_t)p.NT, inc[0], inc[1], inc[2], v);
+                    bool to_y = p.splits == 1;
+                    if constexpr (SK) {
+                        if (start_e > 0) {
+                            // a share of a tile that an earlier CTA finishes
+                            store_share(p.share + (size_t)blockIdx.x * mp * kTileRows + row, v, mp);
+                            to_y = false;
+                        } else if (finisher) {
+                            // the CTA's own part, [column][row] in shared memory (the
+                            // pipeline's stages are idle once every MMA has completed);
+                            // all warps finish the tile below
+                            float* own = reinterpret_cast<float*>(smem);
 #pragma unroll
-                    for (int q = 0; q < 16; ++q)
-                        v[q] = (__uint_as_float(d0[q]) + (ng > 1 ? __uint_as_float(d1[q]) : 0.f)) +
-                               (ng > 2 ? __uint_as_float(d2[q]) : 0.f);
-                    if (p.splits == 1) {
+                            for (int q = 0; q < 16; ++q)
+                                if (q < mp) own[q * kTileRows + row] = v[q];
+                            to_y = false;
+                        }
+                    }
+                    if (to_y) {
                         if (n < p.N) {
 #pragma unroll
                             for (int q = 0; q < 16; ++q) {
@@ -402,6 +552,8 @@ __global__ void __launch_bounds__(kThreads, 1) qmm_q4_0_tc_kernel(const __grid_c
                                 }
                             }
                         }
+                    } else if (SK) {
+                        // published or left for the finish above
                     } else if (p.cluster) {
                         // column quad u of this row at byte (u * 128 + row) * 16 of
                         // the CTA's shared memory: a warp stores 512 contiguous bytes
@@ -418,7 +570,7 @@ __global__ void __launch_bounds__(kThreads, 1) qmm_q4_0_tc_kernel(const __grid_c
                                 *reinterpret_cast<float4*>(part + c0 + q) = make_float4(v[q], v[q + 1], v[q + 2], v[q + 3]);
                     }
                 }
-                if (!p.cluster) __threadfence();   // partials visible before the split counter moves
+                if (p.splits > 1 && !p.cluster) __threadfence();   // partials visible before the split counter moves
             } else {
                 ok = false;
             }
@@ -433,6 +585,68 @@ __global__ void __launch_bounds__(kThreads, 1) qmm_q4_0_tc_kernel(const __grid_c
         mbar_wait_bounded(dfull_bar, 0u, p.fault, kFaultMmaWaitTimeout);
         tc_fence_after();
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "n"(kTmemCols));
+    }
+
+    if constexpr (SK) {
+        if (finisher) {
+            // Finish the tile: word t = column t / 128, row t % 128 of the CTA's own
+            // part plus, in CTA order, the shares of the later CTAs whose ranges
+            // start inside the tile.  Up to four shares' words are loaded at once;
+            // a word not yet tagged is waited for (after one timeout, no longer),
+            // and every word read is cleared.
+            const int mp = (p.M + 3) & ~3;
+            const int words = kTileRows * mp;
+            const int tile_end_unit = (tile_e + 1) * p.groups;
+            int c_end = (int)blockIdx.x + 1;
+            while (c_end < p.ctas && (int)((int64_t)p.units * c_end / p.ctas) < tile_end_unit) ++c_end;
+            const float* own = reinterpret_cast<const float*>(smem);
+            constexpr int kWordsPerThread = 16 * kTileRows / kThreads;   // mp <= 16
+            float acc[kWordsPerThread];
+#pragma unroll
+            for (int k = 0; k < kWordsPerThread; ++k) {
+                const int t = (int)threadIdx.x + k * kThreads;
+                acc[k] = t < words ? own[t] : 0.f;
+            }
+            bool live = true;
+            for (int c0 = (int)blockIdx.x + 1; c0 < c_end; c0 += 4) {
+                unsigned long long w[4][kWordsPerThread];
+#pragma unroll
+                for (int u = 0; u < 4; ++u)
+#pragma unroll
+                    for (int k = 0; k < kWordsPerThread; ++k) {
+                        const int t = (int)threadIdx.x + k * kThreads;
+                        w[u][k] = (c0 + u < c_end && t < words)
+                                      ? ld_relaxed_u64(p.share + (size_t)(c0 + u) * words + t)
+                                      : 0ull;
+                    }
+#pragma unroll
+                for (int u = 0; u < 4; ++u)
+#pragma unroll
+                    for (int k = 0; k < kWordsPerThread; ++k) {
+                        const int t = (int)threadIdx.x + k * kThreads;
+                        if (c0 + u < c_end && t < words) {
+                            unsigned long long* src = p.share + (size_t)(c0 + u) * words + t;
+                            unsigned long long wk = w[u][k];
+                            if ((wk >> 32) == 0) {
+                                wk = wait_tagged_u64(src, p.fault, kFaultShareWaitTimeout, live ? kWaitLimitNs : 0);
+                                live = live && (wk >> 32) != 0;
+                            }
+                            acc[k] += __uint_as_float((uint32_t)wk);
+                            st_relaxed_u64(src, 0ull);
+                        }
+                    }
+            }
+#pragma unroll
+            for (int k = 0; k < kWordsPerThread; ++k) {
+                const int t = (int)threadIdx.x + k * kThreads;
+                const int m = t / kTileRows, n = tile_e * kTileRows + (t & (kTileRows - 1));
+                if (t < words && m < p.M && n < p.N) {
+                    if (p.y_bf16) store_out<__nv_bfloat16>(p.y, (int64_t)m * p.N + n, acc[k]);
+                    else store_out<float>(p.y, (int64_t)m * p.N + n, acc[k]);
+                }
+            }
+        }
+        return;
     }
 
     if (p.splits > 1 && p.cluster) {
@@ -473,7 +687,8 @@ __global__ void __launch_bounds__(kThreads, 1) qmm_q4_0_tc_kernel(const __grid_c
         return;
     }
 
-    // split K: the last CTA of this tile adds the partials in split order
+    // split K: the last CTA of this tile adds the partials in split order and
+    // clears them
     if (p.splits > 1) {
         __shared__ unsigned int last;
         if (threadIdx.x == 0) {
@@ -504,6 +719,19 @@ __global__ void __launch_bounds__(kThreads, 1) qmm_q4_0_tc_kernel(const __grid_c
                         const int r = t & (kTileRows - 1), q = t / kTileRows;
                         val[u][e] = (s0 + u < p.splits && t < items) ? __ldcg(src + (size_t)r * quads + q)
                                                                      : make_float4(0.f, 0.f, 0.f, 0.f);
+                    }
+                }
+                // every call leaves the workspace all zero, so that any later
+                // call (a stream-K plan reads it as tagged words) finds it clean
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    float4* dst = reinterpret_cast<float4*>(
+                        p.partials + (size_t)((s0 + u) * p.tiles + tile) * kTileRows * (size_t)mp);
+#pragma unroll
+                    for (int e = 0; e < kReduceItems; ++e) {
+                        const int t = (int)threadIdx.x + e * kThreads;
+                        const int r = t & (kTileRows - 1), q = t / kTileRows;
+                        if (s0 + u < p.splits && t < items) __stcg(dst + (size_t)r * quads + q, make_float4(0.f, 0.f, 0.f, 0.f));
                     }
                 }
 #pragma unroll
@@ -544,7 +772,7 @@ __global__ void __launch_bounds__(kThreads, 1) qmm_q4_0_tc_kernel(const __grid_c
 // that a single CTA fits per SM (its 512 TMEM columns are then always free).
 size_t qmm_tc_smem_bytes(int nt) {
     const size_t stage = (size_t)kRawStageBytes + (size_t)nt * kGroupK * 2;
-    const size_t need = kStages * stage + 8 * (2 * kStages + 2 * kAStages + 1) + 16;
+    const size_t need = kStages * stage + 8 * kBarriers + 16;
     return need < 116 * 1024 ? 116 * 1024 : need;
 }
 
@@ -552,14 +780,15 @@ int qmm_tc_tile_rows() { return kTileRows; }
 int qmm_tc_group_k() { return kGroupK; }
 
 cudaError_t launch_qmm_tc(const CUtensorMap& tmap_w, const CUtensorMap& tmap_x, void* y, int y_bf16, float* partials,
-                          unsigned int* counters, unsigned int* fault, int M, int N, int K, int splits,
-                          int cluster, cudaStream_t stream) {
+                          unsigned int* counters, unsigned long long* share, unsigned int* fault, int M, int N, int K,
+                          int splits, int cluster, int streamk_ctas, cudaStream_t stream) {
     QmmParams p;
     p.tmap_w = tmap_w;
     p.tmap_x = tmap_x;
     p.y = y;
     p.partials = partials;
     p.counters = counters;
+    p.share = share;
     p.fault = fault;
     p.M = M;
     p.N = N;
@@ -570,14 +799,20 @@ cudaError_t launch_qmm_tc(const CUtensorMap& tmap_w, const CUtensorMap& tmap_x, 
     p.tiles = (N + kTileRows - 1) / kTileRows;
     p.y_bf16 = y_bf16;
     p.cluster = cluster;
+    p.streamk = streamk_ctas > 0 ? 1 : 0;
+    p.ctas = streamk_ctas;
+    p.units = p.tiles * p.groups;
+    if (p.streamk) p.splits = 1;
     const size_t smem = qmm_tc_smem_bytes(p.NT);
     static thread_local int prepared_device = -1;
     int dev = 0;
     cudaGetDevice(&dev);
     if (prepared_device != dev) {
-        cudaError_t e = cudaFuncSetAttribute(qmm_q4_0_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             (int)qmm_tc_smem_bytes(32));
-        if (e != cudaSuccess) return e;
+        for (auto k : {qmm_q4_0_tc_kernel<false>, qmm_q4_0_tc_kernel<true>}) {
+            cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                 (int)qmm_tc_smem_bytes(32));
+            if (e != cudaSuccess) return e;
+        }
         prepared_device = dev;
     }
     // programmatic dependent launch: the prologue and the first weight copies
@@ -590,19 +825,20 @@ cudaError_t launch_qmm_tc(const CUtensorMap& tmap_w, const CUtensorMap& tmap_x, 
     attr[1].val.clusterDim.x = (unsigned)splits;
     attr[1].val.clusterDim.y = 1;
     attr[1].val.clusterDim.z = 1;
-    cfg.gridDim = dim3((unsigned)(p.tiles * splits));
+    cfg.gridDim = dim3((unsigned)(p.streamk ? streamk_ctas : p.tiles * splits));
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
     cfg.attrs = attr;
-    cfg.numAttrs = cluster ? 2 : 1;
-    return cudaLaunchKernelEx(&cfg, qmm_q4_0_tc_kernel, p);
+    cfg.numAttrs = (cluster && !p.streamk) ? 2 : 1;
+    return p.streamk ? cudaLaunchKernelEx(&cfg, qmm_q4_0_tc_kernel<true>, p)
+                     : cudaLaunchKernelEx(&cfg, qmm_q4_0_tc_kernel<false>, p);
 }
 
 // Clusters of `cluster` CTAs (MMA width nt) that the device holds at once; 0
 // when such a launch is not possible.
 int qmm_tc_max_active_clusters(int nt, int cluster) {
-    if (cudaFuncSetAttribute(qmm_q4_0_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if (cudaFuncSetAttribute(qmm_q4_0_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)qmm_tc_smem_bytes(32)) != cudaSuccess)
         return 0;
     cudaLaunchConfig_t cfg = {};
@@ -617,7 +853,7 @@ int qmm_tc_max_active_clusters(int nt, int cluster) {
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, qmm_q4_0_tc_kernel, &cfg) != cudaSuccess) {
+    if (cudaOccupancyMaxActiveClusters(&n, qmm_q4_0_tc_kernel<false>, &cfg) != cudaSuccess) {
         cudaGetLastError();
         return 0;
     }

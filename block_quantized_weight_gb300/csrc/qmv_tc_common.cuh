@@ -78,10 +78,6 @@ __device__ __forceinline__ uint32_t aempty_bar(uint32_t b0, int a, int h) {
 }
 __device__ __forceinline__ uint32_t done_bar(uint32_t b0) { return b0 + 8u * (uint32_t)(2 * kStages + 4 * kSets); }
 
-__device__ __forceinline__ void st_relaxed_u64(unsigned long long* p, unsigned long long v) {
-    asm volatile("st.relaxed.gpu.global.b64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
-}
-
 // per-set partial rows in shared memory: [set][local tile][matrix][row]
 __device__ __forceinline__ int part_at(int set, int lt, int m, int row) {
     return ((set * kMaxLocalTiles + lt) * 2 + m) * kTileRows + row;

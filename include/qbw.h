@@ -150,11 +150,16 @@ qbw_status qmv_gateup_q4_0(const void *w_gate, const void *w_up, const void *x, 
  *               qmm_q4_0_smallM_workspace_bytes(M, N, K) bytes (size for the
  *               current device), 256-byte aligned, ZERO-FILLED once before
  *               its first use.  It holds one arrival counter per 128-row
- *               tile in a fixed 4096-byte region at its start, then the
- *               split-K partial sums.  Every call returns the counters to
- *               zero, so the single zero-fill at allocation is enough, also
- *               when one workspace serves calls of different shapes.  Calls
- *               that share one workspace must not run concurrently.  May be
+ *               tile in a fixed 4096-byte region at its start, then either
+ *               the split-K partial sums or, for M <= 16 when whole-tile
+ *               splits would leave SMs idle (a stream-K plan: one CTA per SM
+ *               over equal ranges of the tiles' K-groups), one tagged 64-bit
+ *               word per CTA, row and token column.  Every call leaves the
+ *               whole workspace zero again, so the single zero-fill at
+ *               allocation is enough, also when one workspace serves calls of
+ *               different shapes; after a call that reported a device fault
+ *               (qbw_fault_read), zero-fill it again.  Calls that share one
+ *               workspace must not run concurrently.  May be
  *               NULL when the size query returns 0: so it does for one K-split
  *               per tile, and for 2 .. 8 splits when the device holds all the
  *               tiles' thread-block clusters at once (the splits of a tile

@@ -95,6 +95,31 @@ def test_qmm_cluster_split_shapes(qbw, oracle, M, N, K, cluster):
         check_matvec(Y, Y_ref, S, rel=1e-2, out_bf16=(odt == torch.bfloat16), what=f"qmm cluster M={M} N={N} K={K}")
 
 
+# Stream-K shapes (M <= 16): whole-tile splits would leave SMs idle, so one CTA
+# per SM takes an equal range of (tile, K-group) units; ranges cross tile
+# boundaries and the tiles are finished from the other CTAs' published shares.
+# (M, N, K): 42 tiles x 84 groups (ranges of 23..24 units, 3..4 CTAs per
+# tile); 32 tiles with a 32-row tail; 3 and 4 tokens (column padding); 60
+# tiles x 64 groups.
+STREAMK_CASES = [(8, 5376, 21504), (16, 4000, 21504), (3, 5376, 21504), (4, 4000, 21504), (13, 7680, 16384)]
+
+
+@pytest.mark.parametrize("M,N,K", STREAMK_CASES)
+def test_qmm_streamk_shapes(qbw, oracle, M, N, K):
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    if sms == 152:
+        # the shares' layout: a 4096-byte counter region, then [152][M rounded
+        # up to 4][128] 64-bit words
+        mp = (M + 3) // 4 * 4
+        assert qbw.qmm_q4_0_smallM_workspace_bytes(M, N, K) == 4096 + (152 * mp * 128 * 8 + 255) // 256 * 256
+    w = synth.q4_0_weights(N, K, seed=N + 3 * M)
+    X = synth.activations((M, K), seed=M + 29, dtype="bf16")
+    Y_ref, S = oracle.qmm_q4_0(w, X, M, N, K)
+    for odt in (torch.float32, torch.bfloat16):
+        Y = run_qmm(qbw, w, X, M, N, K, odt, calls=3)
+        check_matvec(Y, Y_ref, S, rel=1e-2, out_bf16=(odt == torch.bfloat16), what=f"qmm stream-K M={M} N={N} K={K}")
+
+
 @pytest.mark.parametrize("M", [1, 2])
 @pytest.mark.parametrize("N,K", [(16384, 5376), (5413, 5376), (600, 65536)])
 @pytest.mark.parametrize("odt", [torch.bfloat16, torch.float32])
@@ -153,10 +178,11 @@ def test_qmm_workspace_too_small_is_rejected(qbw):
 
 def test_qmm_workspace_shared_across_shapes(qbw):
     # One workspace, zero-filled once, serves calls of different shapes in turn:
-    # every call must find its arrival counters at zero, whatever the partial
-    # sums of an earlier shape left behind.
+    # every call must find its arrival counters at zero and, for a stream-K
+    # plan, its share words untagged, whatever an earlier shape left behind
+    # (the last shape is a stream-K plan, run after workspace-path ones).
     shapes = [(16, 5376, 5376), (17, 256, 2048), (32, 128, 21504), (8, 640, 4096), (32, 1024, 5376),
-              (16, 5376, 5376)]
+              (8, 4000, 21504)]
     size = max(qbw.qmm_q4_0_smallM_workspace_bytes(M, N, K) for M, N, K in shapes)
     if size == 0:
         pytest.skip("this device plans no split for these shapes")

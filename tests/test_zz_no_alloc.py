@@ -51,11 +51,12 @@ def compare_with_workspace_path(qbw, M, N, K, odt, seed):
 
 
 @pytest.mark.parametrize("M,N,K", [(8, 5376, 5376), (16, 5376, 5376), (32, 5376, 5376),
-                                   (17, 256, 2048), (32, 128, 21504)])
+                                   (17, 256, 2048), (32, 128, 21504), (8, 4000, 21504)])
 @pytest.mark.parametrize("odt", [torch.bfloat16, torch.float32])
 def test_noalloc_matches_workspace_entry(qbw, M, N, K, odt):
-    # the 5376-row shapes split K inside one cluster (no scratch) on a 152-SM
-    # part; the other two take the workspace path
+    # on a 152-SM part the 5376-row shapes split K inside one cluster (no
+    # scratch), the next two take the workspace path and the last one is a
+    # stream-K plan (its shares in the scratch)
     _, _, _, need = compare_with_workspace_path(qbw, M, N, K, odt, seed=M + N + K)
     assert need <= qbw.NOALLOC_SCRATCH_BYTES
 
