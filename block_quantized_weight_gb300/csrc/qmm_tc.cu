@@ -52,9 +52,8 @@
 // two tiles (it is never longer than a tile), so a CTA has one or two
 // segments, each with its own three accumulators (TMEM 384 + 2 x 3 x 16
 // columns).  A segment that starts inside a tile is a share: the CTA
-// publishes it as one tagged 64-bit word (fp32 bits, tag 1) per row and token
-// column; the first of two segments is published mid-range by the set that
-// ran its last group, as soon as its MMAs have completed.  The CTA that covers
+// publishes it at the end of its range as one tagged 64-bit word (fp32 bits,
+// tag 1) per row and token column.  The CTA that covers
 // a tile's first group finishes the tile at the end of its range: it adds the
 // later CTAs' shares after its own, in CTA order, clears their tags and writes
 // Y.  A range covering a whole tile writes Y directly.  Results depend only on
@@ -154,8 +153,8 @@ struct QmmParams {
 };
 
 // Barrier layout shared by every role: full[kStages], empty[kStages],
-// afull[kAStages], aempty[kAStages], dfull, dmid, 8 bytes each from bar0.
-constexpr int kBarriers = 2 * kStages + 2 * kAStages + 2;
+// afull[kAStages], aempty[kAStages], dfull, 8 bytes each from bar0.
+constexpr int kBarriers = 2 * kStages + 2 * kAStages + 1;
 __device__ __forceinline__ uint32_t full_bar_at(uint32_t bar0, int s) { return bar0 + 8u * (uint32_t)s; }
 __device__ __forceinline__ uint32_t empty_bar_at(uint32_t bar0, int s) { return bar0 + 8u * (uint32_t)(kStages + s); }
 __device__ __forceinline__ uint32_t afull_bar_at(uint32_t bar0, int a) {
@@ -166,10 +165,6 @@ __device__ __forceinline__ uint32_t aempty_bar_at(uint32_t bar0, int a) {
 }
 __device__ __forceinline__ uint32_t dfull_bar_at(uint32_t bar0) {
     return bar0 + 8u * (uint32_t)(2 * kStages + 2 * kAStages);
-}
-// dmid: every MMA of the first of two stream-K segments has completed
-__device__ __forceinline__ uint32_t dmid_bar_at(uint32_t bar0) {
-    return bar0 + 8u * (uint32_t)(2 * kStages + 2 * kAStages + 1);
 }
 
 // v[q] = sum of the included accumulators' column q (16 columns from taddr;
@@ -186,24 +181,6 @@ __device__ __forceinline__ void read_d(uint32_t taddr, uint32_t nt, bool i0, boo
                (i2 ? __uint_as_float(d2[q]) : 0.f);
 }
 
-// The same one accumulator at a time, for the mid-range publish, which runs
-// while a group's codes are held in registers.
-__device__ __forceinline__ void read_d_lean(uint32_t taddr, uint32_t nt, bool i1, bool i2, float (&v)[16]) {
-    uint32_t d[16];
-    tmem_ld16(taddr, d);
-    tmem_wait_ld();
-#pragma unroll
-    for (int q = 0; q < 16; ++q) v[q] = __uint_as_float(d[q]);
-    tmem_ld16(taddr + nt, d);
-    tmem_wait_ld();
-#pragma unroll
-    for (int q = 0; q < 16; ++q) v[q] += i1 ? __uint_as_float(d[q]) : 0.f;
-    tmem_ld16(taddr + 2u * nt, d);
-    tmem_wait_ld();
-#pragma unroll
-    for (int q = 0; q < 16; ++q) v[q] += i2 ? __uint_as_float(d[q]) : 0.f;
-}
-
 __device__ __forceinline__ unsigned long long ld_relaxed_u64(const unsigned long long* p) {
     unsigned long long w;
     asm volatile("ld.relaxed.gpu.global.b64 %0, [%1];" : "=l"(w) : "l"(p) : "memory");
@@ -217,21 +194,6 @@ __device__ __forceinline__ void store_share(unsigned long long* dst, const float
         if (q < mp) st_relaxed_u64(dst + (size_t)q * kTileRows, (1ull << 32) | (unsigned long long)__float_as_uint(v[q]));
 }
 
-// The first of a stream-K CTA's two segments (its groups 0 .. last_group),
-// published by the set that ran its last group once the segment's MMAs have
-// completed.  d_taddr: the quarter's TMEM lanes at the segment's D_0.
-__device__ __forceinline__ bool publish_mid(const QmmParams& p, int last_group, uint32_t d_taddr, uint32_t bar0) {
-    const bool got = mbar_wait_bounded(dmid_bar_at(bar0), 0u, p.fault, kFaultMmaWaitTimeout);
-    if (!__all_sync(0xffffffffu, got)) return false;
-    tc_fence_after();
-    float v[16];
-    read_d_lean(d_taddr, 16u, last_group >= 1, last_group >= 2, v);
-    const int mp = (p.M + 3) & ~3;
-    const int row = (int)(threadIdx.x & 127u);   // warp 4g + q, lane l: row 32 q + l
-    store_share(p.share + (size_t)blockIdx.x * mp * kTileRows + row, v, mp);
-    return true;
-}
-
 // One dequantizing warp of set g over the CTA's K-groups g, g + 3, ...
 // Per group: wait for the raw stage; read the lane's 144 bytes with nine
 // 16-byte loads (8 consecutive lanes = 8 rows 144 bytes apart hit 8 distinct
@@ -239,16 +201,10 @@ __device__ __forceinline__ bool publish_mid(const QmmParams& p, int last_group, 
 // block pairs into two alternating register buffers and store each into TMEM
 // A stage g.  A buffer is rewritten only after a tcgen05.wait::st covering
 // its previous store.  raw_row: the row's byte offset within a stage;
-// a_taddr: TMEM address of the quarter's lanes, A stage g, column 0.  With
-// two stream-K segments (mid >= 0: the first one's last group), the set that
-// runs group mid publishes the first segment's share, right after its next
-// A-stage wait (which follows the same MMAs) or after its last group.
-template <bool SK>
+// a_taddr: TMEM address of the quarter's lanes, A stage g, column 0.
 __device__ __forceinline__ bool dequant_warp(int g, uint32_t raw_row, uint32_t a_taddr, uint32_t sbase,
-                                             uint32_t stage_bytes, uint32_t bar0, int lane, int ng, int mid,
-                                             const QmmParams& p) {
-    unsigned int* const fault = p.fault;
-    const uint32_t d_taddr = a_taddr - (uint32_t)g * kAColsPerStage + kDCol;
+                                             uint32_t stage_bytes, uint32_t bar0, int lane, int ng,
+                                             unsigned int* fault) {
     for (int i = g; i < ng; i += kSets) {
         const int s = i % kStages;
         const bool got = mbar_wait_bounded(full_bar_at(bar0, s), (uint32_t)(i / kStages) & 1u, fault,
@@ -274,8 +230,6 @@ __device__ __forceinline__ bool dequant_warp(int g, uint32_t raw_row, uint32_t a
                                                 kFaultMmaWaitTimeout);
             if (!__all_sync(0xffffffffu, free)) return false;
             tc_fence_after();
-            if constexpr (SK)
-                if (i - kSets == mid && !publish_mid(p, mid, d_taddr, bar0)) return false;
         }
         tmem_st32(a_taddr, c0);
         dequant_pair<1>(v, c1);
@@ -292,8 +246,6 @@ __device__ __forceinline__ bool dequant_warp(int g, uint32_t raw_row, uint32_t a
         __syncwarp();
         if (lane == 0) mbar_arrive(afull_bar_at(bar0, g));
     }
-    if constexpr (SK)
-        if (mid >= 0 && mid % kSets == g && mid + kSets >= ng) return publish_mid(p, mid, d_taddr, bar0);
     return true;
 }
 
@@ -325,7 +277,6 @@ __device__ __forceinline__ bool issue_mmas(uint32_t tmem, uint32_t sbase, uint32
     const uint64_t ds0 = sw128_desc(sbase + kRawStageBytes);
     uint32_t aphase = 0;
     bool ok = true;
-    bool owe_mid = SK && nA < ng;     // two segments: dmid marks the end of the first
     for (int i = J; i < ng; i += kSets) {
         const int s = i % kStages;
         const uint32_t sphase = (uint32_t)(i / kStages) & 1u;
@@ -333,10 +284,6 @@ __device__ __forceinline__ bool issue_mmas(uint32_t tmem, uint32_t sbase, uint32
         const bool seg1 = SK && i >= nA;
         const uint32_t d_tmem = seg1 ? d_seg1 : d_seg0;
         const uint32_t acc0 = (seg1 ? i - kSets >= nA : i > J) ? 1u : 0u;
-        if (owe_mid && seg1) {
-            tc_commit(dmid_bar_at(bar0));     // this issuer's first-segment MMAs
-            owe_mid = false;
-        }
         ok = mbar_wait_bounded(full_bar_at(bar0, s), sphase, fault, kFaultMmaWaitTimeout) &&
              mbar_wait_bounded(afull_bar_at(bar0, J), aphase, fault, kFaultMmaWaitTimeout);
         if (!ok) break;
@@ -348,7 +295,6 @@ __device__ __forceinline__ bool issue_mmas(uint32_t tmem, uint32_t sbase, uint32
         tc_commit(aempty_bar_at(bar0, J));    // TMEM A stage J consumed
         aphase ^= 1u;
     }
-    if (owe_mid) tc_commit(dmid_bar_at(bar0));
     // completes when every MMA issued above has finished, even after a
     // timeout (the accumulator is then not read, only TMEM released)
     tc_commit(dfull_bar_at(bar0));
@@ -452,7 +398,6 @@ __global__ void __launch_bounds__(kThreads, 1) qmm_q4_0_tc_kernel(const __grid_c
                 mbar_init(aempty_bar_at(bar0, a), 1);
             }
             mbar_init(dfull_bar, kIssuers);
-            if constexpr (SK) mbar_init(dmid_bar_at(bar0), kIssuers);
             fence_mbar_init();
         }
         __syncwarp();
@@ -504,9 +449,9 @@ __global__ void __launch_bounds__(kThreads, 1) qmm_q4_0_tc_kernel(const __grid_c
         const uint32_t tmem = *tmem_slot;
         const int set = warp >> 2, quarter = warp & 3;   // TMEM lanes 32 quarter .. +31
         const int row = quarter * 32 + lane;             // weight row within the tile
-        ok = dequant_warp<SK>(set, (uint32_t)row * kGroupBytes,
+        ok = dequant_warp(set, (uint32_t)row * kGroupBytes,
                           tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)set * kAColsPerStage, sbase,
-                          stage_bytes, bar0, lane, ng, two ? nA - 1 : -1, p);
+                          stage_bytes, bar0, lane, ng, p.fault);
         // ---------------- epilogue: warps 0..3 read the last segment's D_0 + D_1 + D_2
         // (128 rows x NT) and emit
         if (warp < 4) {
@@ -520,6 +465,15 @@ __global__ void __launch_bounds__(kThreads, 1) qmm_q4_0_tc_kernel(const __grid_c
                 for (int j = 0; j < kSets; ++j) inc[j] = two ? (j - nA % kSets + kSets) % kSets < len_e : j < ng;
                 const int mp = (p.M + 3) & ~3;
                 float* part = p.partials + ((size_t)(split * p.tiles + tile) * kTileRows + row) * (size_t)mp;
+                if constexpr (SK)
+                    if (two) {
+                        // the first segment is a share of a tile that an earlier CTA
+                        // finishes; published here, at the end of the range (a
+                        // mid-range publish held up the decode and measured slower)
+                        float v0[16];
+                        read_d(tmem + ((uint32_t)(quarter * 32) << 16) + kDCol, 16u, true, nA > 1, nA > 2, v0);
+                        store_share(p.share + (size_t)blockIdx.x * mp * kTileRows + row, v0, mp);
+                    }
                 const uint32_t lane_base = tmem + ((uint32_t)(quarter * 32) << 16) + kDCol + (two ? 3u * p.NT : 0u);
                 for (int c0 = 0; c0 < p.NT; c0 += 16) {
                     float v[16];
