@@ -46,18 +46,18 @@
 // then resets the counter and clears the partials, so the workspace is all
 // zero again after every call.
 //
-// Stream-K (M <= 16).  When whole-tile splits would leave SMs idle (42 tiles
-// of 3 splits use 126 of 152), one CTA per SM takes an equal range of the
-// (tile, K-group) units in tile-major order instead.  A range meets at most
-// two tiles (it is never longer than a tile), so a CTA has one or two
-// segments, each with its own three accumulators (TMEM 384 + 2 x 3 x 16
-// columns).  A segment that starts inside a tile is a share: the CTA
-// publishes it at the end of its range as one tagged 64-bit word (fp32 bits,
-// tag 1) per row and token column.  The CTA that covers
-// a tile's first group finishes the tile at the end of its range: it adds the
-// later CTAs' shares after its own, in CTA order, clears their tags and writes
-// Y.  A range covering a whole tile writes Y directly.  Results depend only on
-// the plan, so they are bit-reproducible.
+// Stream-K (M <= 16).  Where whole-tile splits leave SMs idle (42 tiles of 3
+// splits use 126 of 152) and K is long (16 groups or more a CTA), one CTA per
+// SM takes an equal range of the (tile, K-group) units in tile-major order
+// instead.  A range meets at most two tiles (it is never longer than a tile),
+// so a CTA has one or two segments, each with its own three accumulators
+// (TMEM 384 + 2 x 3 x 16 columns).  A segment that starts inside a tile is a
+// share: the CTA publishes it at the end of its range as one tagged 64-bit
+// word (fp32 bits, tag 1) per row and token column.  The CTA that covers a
+// tile's first group finishes the tile at the end of its range: it adds the
+// later CTAs' shares after its own, in CTA order, clears their tags and
+// writes Y.  A range covering a whole tile writes Y directly.  Results depend
+// only on the plan, so they are bit-reproducible.
 #include <cstdint>
 
 #include "qbw_device.cuh"
