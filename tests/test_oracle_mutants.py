@@ -60,6 +60,9 @@ MUTANTS = {
                            "double dmin = oracle_fp16_to_f64(read_u16le(blk));\n        for (int e = 0; e < ORACLE_QK_K; e++) {\n            int sc, m;\n            oracle_q4k_scale_min(blk + 4, e / 32, &sc, &m);\n            w[e]"),
     "q4k_subblock_of_64": ("oracle_q4k_scale_min(blk + 4, e / 32, &sc, &m);\n            w[e]",
                            "oracle_q4k_scale_min(blk + 4, e / 64, &sc, &m);\n            w[e]"),
+    "q4k_split_min_doubled": ("fabs(dmin * (double)m);\n                s2 +=", "fabs(2.0 * dmin * (double)m);\n                s2 +="),
+    "q4k_split_min_dropped": ("double t = fabs(d * (double)sc * (double)q4k_code(blk + 16, e)) + fabs(dmin * (double)m);",
+                              "double t = fabs(d * (double)sc * (double)q4k_code(blk + 16, e));"),
 }
 
 

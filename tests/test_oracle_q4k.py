@@ -157,3 +157,37 @@ def test_rejects_k_not_multiple_of_256(oracle):
     w = synth.q4_k_weights(1, 256, seed=1)
     with pytest.raises(ValueError):
         oracle.qmv("q4_k", w, synth.activations(288, seed=1), 1, 288)
+
+
+def test_split_scale_handworked(oracle):
+    """S2 of a hand-built super-block, worked out here by hand.
+
+    The split forms d sc_j * sum(q x) and dmin m_j * sum(x) separately
+    (jouleclaw-loader-gguf BENCHMARKS, "Q4_K matmul -- scalar fused vs
+    AMX-tiled"), so its error scale takes |d sc_j q_k| and |dmin m_j| apart:
+    S2 = sum_j sum_k (|d sc_j q_k| + |dmin m_j|) |x_k|.
+
+    Fields: d = 1/2, dmin = 1/4, sc_j = j + 1, m_j = 2 j, every code of
+    sub-block j equal to j, and x_k = +-1 (sign alternating), so |x_k| = 1.
+    Sub-block j then adds 32 * (j (j + 1) / 2 + j / 2) = 16 j^2 + 32 j, and
+    over j = 0..7: 16 * 140 + 32 * 28 = 2240 + 896 = 3136.  The plain scale
+    sum |w x| differs: weight d sc_j q - dmin m_j = j (j + 1) / 2 - j / 2
+    = j^2 / 2, so S = 32 * sum_j j^2 / 2 = 16 * 140 = 2240.
+
+    A second row sets every code to 8 and sc_j = 1, m_j = 8 with d = dmin =
+    1/4: each weight is 1/4 * 8 - 1/4 * 8 = 0, so S = 0, but S2 = 256 *
+    (2 + 2) = 1024 (both terms of the split are nonzero and cancel).
+    """
+    rows = []
+    sc = [j + 1 for j in range(8)]
+    m = [2 * j for j in range(8)]
+    q = [e // 32 for e in range(256)]
+    rows.append(synth.q4_k_records([f16_bits(0.5)], [f16_bits(0.25)], pack_scales(sc, m), pack_codes(q)))
+    rows.append(synth.q4_k_records([f16_bits(0.25)], [f16_bits(0.25)], pack_scales([1] * 8, [8] * 8),
+                                   pack_codes([8] * 256)))
+    w = np.concatenate(rows)
+    x = np.array([1.0 if k % 2 == 0 else -1.0 for k in range(256)], dtype=np.float32)
+    S2 = oracle.q4k_split_scale(w, x, 2, 256)
+    assert S2[0] == 3136.0 and S2[1] == 1024.0, S2
+    y, S = oracle.qmv("q4_k", w, x, 2, 256)
+    assert S[0] == 2240.0 and S[1] == 0.0 and y[1] == 0.0, (S, y)
