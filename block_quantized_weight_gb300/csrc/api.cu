@@ -706,6 +706,12 @@ qbw_status qbw_fault_read(uint32_t* code, int clear, void* stream) {
     if (cudaMemcpyAsync(&v, di->fault, sizeof(v), cudaMemcpyDeviceToHost, s) != cudaSuccess) return QBW_ECUDA;
     if (clear && cudaMemsetAsync(di->fault, 0, sizeof(unsigned int), s) != cudaSuccess) return QBW_ECUDA;
     if (cudaStreamSynchronize(s) != cudaSuccess) return QBW_ECUDA;
+    // a fault can leave split-K counters of the allocation-free entry point's
+    // static scratch nonzero: its next call zero-fills the scratch again
+    if (v != 0) {
+        int dev = 0;
+        if (cudaGetDevice(&dev) == cudaSuccess) noalloc_scratch_mark_dirty(dev);
+    }
     *code = v;
     return QBW_OK;
 }

@@ -111,18 +111,33 @@ __device__ __forceinline__ void st_relaxed_u64(unsigned long long* p, unsigned l
     asm volatile("st.relaxed.gpu.global.b64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
 }
 
-// Wait until the 64-bit word at p carries a nonzero tag (its upper half),
-// reading it with relaxed gpu-scope loads, giving up after limit_ns.  Returns
-// the last word read; on timeout records `code` (the word's tag is then 0).
-__device__ __forceinline__ unsigned long long wait_tagged_u64(const unsigned long long* p, unsigned int* fault,
-                                                              unsigned int code, uint64_t limit_ns = kWaitLimitNs) {
+// The launch's grid identifier (PTX %gridid): the same in every CTA of one
+// grid, and different for grids launched at different times in this context.
+__device__ __forceinline__ uint64_t grid_id() {
+    uint64_t g;
+    asm volatile("mov.u64 %0, %%gridid;" : "=l"(g));
+    return g;
+}
+
+// Tag that marks a word published by this launch: 1 .. 2^32 - 1, different
+// for any two grids fewer than 2^32 - 1 launches apart (0 means "no share").
+__device__ __forceinline__ uint32_t launch_tag() { return (uint32_t)(grid_id() % 0xFFFFFFFFull) + 1u; }
+
+// Wait until the 64-bit word at p carries `tag` in its upper half, reading it
+// with relaxed gpu-scope loads, giving up after limit_ns.  A word with any
+// other tag (consumed, stale, or another launch's) is not accepted.  Returns
+// the last word read; on timeout records `code` (the word's tag is then not
+// `tag`).
+__device__ __forceinline__ unsigned long long wait_tag_u64(const unsigned long long* p, uint32_t tag,
+                                                           unsigned int* fault, unsigned int code,
+                                                           uint64_t limit_ns = kWaitLimitNs) {
     unsigned long long w;
     asm volatile("ld.relaxed.gpu.global.b64 %0, [%1];" : "=l"(w) : "l"(p) : "memory");
-    if (w >> 32) return w;
+    if ((uint32_t)(w >> 32) == tag) return w;
     const uint64_t t0 = globaltimer_ns();
     for (;;) {
         asm volatile("ld.relaxed.gpu.global.b64 %0, [%1];" : "=l"(w) : "l"(p) : "memory");
-        if (w >> 32) return w;
+        if ((uint32_t)(w >> 32) == tag) return w;
         if (globaltimer_ns() - t0 > limit_ns) {
             record_fault(fault, code);
             return w;

@@ -85,6 +85,10 @@ cudaError_t launch_dequant(int fmt, const uint8_t* w, float* out, int64_t N, int
 cudaError_t launch_embed(int fmt, const uint8_t* w, const int32_t* ids, int64_t n_ids, int64_t N, int64_t K, void* out,
                          int out_bf16, unsigned int* fault, int sm_count, cudaStream_t stream);
 
+// qmm_noalloc.cu: the next qmm_q4_0_smallM_noalloc call on `device` zero-fills
+// its static scratch again (called when qbw_fault_read finds a fault).
+void noalloc_scratch_mark_dirty(int device);
+
 // Largest dynamic shared memory the streaming kernels may request.
 cudaError_t prepare_qmv_stream(int fmt, int nmat, int R, size_t smem);
 

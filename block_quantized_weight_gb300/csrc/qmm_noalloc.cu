@@ -8,7 +8,7 @@
 // ABI with no memory pool of its own, or a loop where a cudaMalloc (which can
 // synchronize the whole device) would stall the pipeline.  For them this entry
 // point takes no workspace argument and allocates nothing: the scratch is one
-// module-level array, located once per device with cudaGetSymbolAddress.
+// module-level array, located on the current device with cudaGetSymbolAddress.
 //
 // The arithmetic, the split-K plan and the kernel are exactly those of
 // qmm_q4_0_smallM: this file only supplies the scratch and forwards the call.
@@ -18,6 +18,7 @@
 #include <mutex>
 
 #include "qbw.h"
+#include "qbw_internal.h"
 
 namespace {
 
@@ -31,24 +32,39 @@ static __device__ __align__(256) unsigned char g_qmm_scratch[kScratchBytes];
 
 std::mutex g_scratch_mu;
 void* g_scratch_addr[kMaxDevices] = {};
+bool g_scratch_dirty[kMaxDevices] = {};
 
-// First call on a device: look up the array's address there and zero it on the
-// caller's stream, so the kernel that follows sees zero counters.
+// The array's address on the current device, looked up on every call (cheap;
+// a device reset or a new context moves it).  When the address is new, or a
+// fault was reported since the last call (a call that gave up may have left
+// counters nonzero), the array is zero-filled on the caller's stream first,
+// so the kernel that follows sees zero counters.
 qbw_status scratch_for_current_device(cudaStream_t s, void** out) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return QBW_ECUDA;
+    void* addr = nullptr;
+    if (cudaGetSymbolAddress(&addr, g_qmm_scratch) != cudaSuccess || !addr) return QBW_ECUDA;
     std::lock_guard<std::mutex> lk(g_scratch_mu);
-    if (!g_scratch_addr[dev]) {
-        void* addr = nullptr;
-        if (cudaGetSymbolAddress(&addr, g_qmm_scratch) != cudaSuccess || !addr) return QBW_ECUDA;
+    if (g_scratch_addr[dev] != addr || g_scratch_dirty[dev]) {
         if (cudaMemsetAsync(addr, 0, kScratchBytes, s) != cudaSuccess) return QBW_ECUDA;
         g_scratch_addr[dev] = addr;
+        g_scratch_dirty[dev] = false;
     }
-    *out = g_scratch_addr[dev];
+    *out = addr;
     return QBW_OK;
 }
 
 }  // namespace
+
+namespace qbw {
+
+void noalloc_scratch_mark_dirty(int device) {
+    if (device < 0 || device >= kMaxDevices) return;
+    std::lock_guard<std::mutex> lk(g_scratch_mu);
+    g_scratch_dirty[device] = true;
+}
+
+}  // namespace qbw
 
 extern "C" {
 

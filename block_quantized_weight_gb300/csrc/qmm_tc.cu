@@ -53,10 +53,11 @@
 // so a CTA has one or two segments, each with its own three accumulators
 // (TMEM 384 + 2 x 3 x 16 columns).  A segment that starts inside a tile is a
 // share: the CTA publishes it at the end of its range as one tagged 64-bit
-// word (fp32 bits, tag 1) per row and token column.  The CTA that covers a
-// tile's first group finishes the tile at the end of its range: it adds the
-// later CTAs' shares after its own, in CTA order, clears their tags and
-// writes Y.  A range covering a whole tile writes Y directly.  Results depend
+// word (fp32 bits, tag) per row and token column, the tag being the launch's
+// own (launch_tag: derived from the grid id), so a word left by another call
+// is never taken.  The CTA that covers a tile's first group finishes the tile
+// at the end of its range: it adds the later CTAs' shares after its own, in
+// CTA order, clears them and writes Y.  A range covering a whole tile writes Y directly.  Results depend
 // only on the plan, so they are bit-reproducible.
 #include <cstdint>
 
@@ -187,11 +188,13 @@ __device__ __forceinline__ unsigned long long ld_relaxed_u64(const unsigned long
     return w;
 }
 
-// A row's share: token column q at dst[128 q], as (fp32 bits, tag 1).
+// A row's share: token column q at dst[128 q], as (fp32 bits, this launch's
+// tag), so that a finisher never takes a word left by another call.
 __device__ __forceinline__ void store_share(unsigned long long* dst, const float (&v)[16], int mp) {
+    const unsigned long long tag = (unsigned long long)launch_tag() << 32;
 #pragma unroll
     for (int q = 0; q < 16; ++q)
-        if (q < mp) st_relaxed_u64(dst + (size_t)q * kTileRows, (1ull << 32) | (unsigned long long)__float_as_uint(v[q]));
+        if (q < mp) st_relaxed_u64(dst + (size_t)q * kTileRows, tag | (unsigned long long)__float_as_uint(v[q]));
 }
 
 // One dequantizing warp of set g over the CTA's K-groups g, g + 3, ...
@@ -550,6 +553,7 @@ __global__ void __launch_bounds__(kThreads, 1) qmm_q4_0_tc_kernel(const __grid_c
             // and every word read is cleared.
             const int mp = (p.M + 3) & ~3;
             const int words = kTileRows * mp;
+            const uint32_t tag = launch_tag();
             const int tile_end_unit = (tile_e + 1) * p.groups;
             int c_end = (int)blockIdx.x + 1;
             while (c_end < p.ctas && (int)((int64_t)p.units * c_end / p.ctas) < tile_end_unit) ++c_end;
@@ -581,9 +585,9 @@ __global__ void __launch_bounds__(kThreads, 1) qmm_q4_0_tc_kernel(const __grid_c
                         if (c0 + u < c_end && t < words) {
                             unsigned long long* src = p.share + (size_t)(c0 + u) * words + t;
                             unsigned long long wk = w[u][k];
-                            if ((wk >> 32) == 0) {
-                                wk = wait_tagged_u64(src, p.fault, kFaultShareWaitTimeout, live ? kWaitLimitNs : 0);
-                                live = live && (wk >> 32) != 0;
+                            if ((uint32_t)(wk >> 32) != tag) {
+                                wk = wait_tag_u64(src, tag, p.fault, kFaultShareWaitTimeout, live ? kWaitLimitNs : 0);
+                                live = live && (uint32_t)(wk >> 32) == tag;
                             }
                             acc[k] += __uint_as_float((uint32_t)wk);
                             st_relaxed_u64(src, 0ull);

@@ -74,16 +74,18 @@ __device__ __forceinline__ bool grid_barrier(unsigned int* count, unsigned int t
     }
 }
 
-// a split tile's share from another CTA, unless the run has been aborted
-__device__ __forceinline__ unsigned long long wait_share(const unsigned long long* src, unsigned int* fault,
-                                                         unsigned int* abort_flag) {
+// a split tile's share from another CTA (a word carrying this run's launch
+// tag; a stale word from a run that faulted is never taken), unless the run
+// has been aborted
+__device__ __forceinline__ unsigned long long wait_share(const unsigned long long* src, uint32_t tag,
+                                                         unsigned int* fault, unsigned int* abort_flag) {
     unsigned long long w;
     asm volatile("ld.relaxed.gpu.global.b64 %0, [%1];" : "=l"(w) : "l"(src) : "memory");
-    if (w >> 32) return w;
+    if ((uint32_t)(w >> 32) == tag) return w;
     const uint64_t t0 = globaltimer_ns();
     for (;;) {
         asm volatile("ld.relaxed.gpu.global.b64 %0, [%1];" : "=l"(w) : "l"(src) : "memory");
-        if (w >> 32) return w;
+        if ((uint32_t)(w >> 32) == tag) return w;
         if (aborted(abort_flag)) return w;
         if (globaltimer_ns() - t0 > kWaitLimitNs) {
             record_fault(fault, kFaultShareWaitTimeout);
@@ -115,6 +117,7 @@ __global__ void __launch_bounds__(kThreads, 1) qmv_chain_kernel(const __grid_con
     extern __shared__ __align__(1024) uint8_t smem[];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int ctas = (int)gridDim.x, cta = (int)blockIdx.x;
+    const uint32_t tag = launch_tag();     // marks this run's split-tile shares
     __shared__ unsigned int qcount[4];
     if (threadIdx.x < 4) qcount[threadIdx.x] = 0u;
 
@@ -284,7 +287,7 @@ __global__ void __launch_bounds__(kThreads, 1) qmv_chain_kernel(const __grid_con
                         const float v = part[part_at(0, 0, m, row)] + part[part_at(1, 0, m, row)] +
                                         part[part_at(2, 0, m, row)];
                         st_relaxed_u64(p.share + ((size_t)cta * 2 + m) * kTileRows + row,
-                                       (unsigned long long)__float_as_uint(v) | (1ull << 32));
+                                       (unsigned long long)__float_as_uint(v) | ((unsigned long long)tag << 32));
                     }
                 }
                 counted = true;
@@ -457,7 +460,7 @@ __global__ void __launch_bounds__(kThreads, 1) qmv_chain_kernel(const __grid_con
                             for (int m = 0; m < 2; ++m) {
                                 if (m >= nmat) break;
                                 unsigned long long* src = p.share + ((size_t)c * 2 + m) * kTileRows + rr;
-                                const unsigned long long w = wait_share(src, p.fault, p.bar_count + 1);
+                                const unsigned long long w = wait_share(src, tag, p.fault, p.bar_count + 1);
                                 v[m] += __uint_as_float((uint32_t)w);
                                 st_relaxed_u64(src, 0ull);                 // consumed
                             }

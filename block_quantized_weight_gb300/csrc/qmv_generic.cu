@@ -259,7 +259,7 @@ __global__ void selftest_wait_kernel(int which, uint64_t limit_ns, unsigned int*
         fence_mbar_init();
         mbar_wait_bounded(b, 0u, fault, kFaultBulkWaitTimeout, limit_ns);
     } else {
-        wait_tagged_u64(&g_selftest_word, fault, kFaultShareWaitTimeout, limit_ns);
+        wait_tag_u64(&g_selftest_word, launch_tag(), fault, kFaultShareWaitTimeout, limit_ns);   // stays 0
     }
 }
 

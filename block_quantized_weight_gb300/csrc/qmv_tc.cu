@@ -37,9 +37,10 @@
 // CTAs is finished by the CTA that covers its first unit (it reaches the tile
 // last, at the end of its range).  Every other CTA on the tile starts its range
 // inside it, completes its share early and publishes it then: one 64-bit word
-// per row, (value, 1).  The finisher waits for those words (bounded), adds
-// them after its own share in CTA order, writes y and marks them consumed
-// (tag 0).  Results are therefore bit-reproducible.
+// per row, (value, the launch's tag), in a scratch slot chosen from the grid
+// id.  The finisher waits for words with its own tag (bounded), adds them
+// after its own share in CTA order, writes y and marks them consumed (tag 0).
+// Results are therefore bit-reproducible.
 //
 // Warp roles (16 warps): warps 0..11 are three sets of four dequantizing
 // warps; set s takes the CTA's units s, s + 3, ...; warp 4s + q owns rows
@@ -52,7 +53,6 @@
 // Each set's rows read D back one unit later, while the next unit's codes are
 // already decoded in registers.
 #include <algorithm>
-#include <atomic>
 #include <cstdint>
 
 #include "qbw_device.cuh"
@@ -62,10 +62,17 @@
 
 namespace qbw {
 
-// Split-tile scratch, one slot per call in flight: each CTA's published
-// share of its first tile, per row (fp32 bits, tag) with tag 1 = published,
-// 0 = consumed (all zero at load).
-constexpr int kQtcSlots = 16;
+// Split-tile scratch: each CTA's published share of its first tile, per row,
+// as (fp32 bits, tag) with tag = the publishing launch's launch_tag() and 0 =
+// consumed (all zero at load).  A launch uses slot (grid id mod kQtcSlots),
+// chosen on the device, so launches close together in launch order (the
+// launches of a captured graph, calls on several streams) take different
+// slots, and a word is accepted only with the finisher's own launch tag: a
+// stale word (left by a launch that faulted) or another launch's is never
+// added.  Two launches kQtcSlots apart in launch order that run at the same
+// time share a slot; the finisher then waits in vain and reports fault 4
+// instead of adding a foreign value.
+constexpr int kQtcSlots = 32;
 constexpr int kQtcMaxCtas = 160;
 constexpr int kQtcMaxTiles = 4096;
 __device__ unsigned long long g_qtc_share[kQtcSlots][kQtcMaxCtas][2][128];
@@ -104,7 +111,9 @@ __device__ __forceinline__ void qmv_tc_body(const QtcParams& p) {
     const bool contrib0 = n > 0 && tile0 * GU < u0;
     __shared__ unsigned int qcount[4];
     if (threadIdx.x < 4) qcount[threadIdx.x] = 0u;
-    unsigned long long* share = &g_qtc_share[p.slot][0][0][0];   // [cta][matrix][row]
+    const uint64_t gid = grid_id();
+    const uint32_t tag = launch_tag();
+    unsigned long long* share = &g_qtc_share[gid % kQtcSlots][0][0][0];   // [cta][matrix][row]
 
     const uint32_t sbase = smem_u32(smem);
     const uint32_t bar0 = sbase + kOffBar;
@@ -277,7 +286,7 @@ __device__ __forceinline__ void qmv_tc_body(const QtcParams& p) {
                     const float v = part[part_at(0, 0, m, row)] + part[part_at(1, 0, m, row)] +
                                     part[part_at(2, 0, m, row)];
                     st_relaxed_u64(share + ((size_t)cta * 2 + m) * kTileRows + row,
-                                   (unsigned long long)__float_as_uint(v) | (1ull << 32));
+                                   (unsigned long long)__float_as_uint(v) | ((unsigned long long)tag << 32));
                 }
             }
             counted = true;
@@ -594,7 +603,7 @@ __device__ __forceinline__ void qmv_tc_body(const QtcParams& p) {
 #pragma unroll
                     for (int m = 0; m < NCH; ++m) {
                         unsigned long long* src = share + ((size_t)c * 2 + m) * kTileRows + r;
-                        const unsigned long long w = wait_tagged_u64(src, p.fault, kFaultShareWaitTimeout);
+                        const unsigned long long w = wait_tag_u64(src, tag, p.fault, kFaultShareWaitTimeout);
                         v[m] += __uint_as_float((uint32_t)w);
                         st_relaxed_u64(src, 0ull);                 // consumed
                     }
@@ -666,7 +675,6 @@ size_t qmv_tc_smem_bytes() { return kSmemBytes; }
 // two tokens.
 cudaError_t launch_qmv_tc(int fmt, int nmat, int ntok, const CUtensorMap* tmap_w, const void* x, int x_bf16,
                           void* y, int y_bf16, int N, int K, int sm_count, unsigned int* fault, cudaStream_t stream) {
-    static std::atomic<unsigned int> calls{0};
     if (nmat * ntok > 2 || (ntok == 2 && !x_bf16)) return cudaErrorInvalidValue;
     if (fmt == kFmtQ4K && nmat * ntok != 1) return cudaErrorInvalidValue;
     QtcParams p;
@@ -680,7 +688,6 @@ cudaError_t launch_qmv_tc(int fmt, int nmat, int ntok, const CUtensorMap* tmap_w
     p.tiles = (N + kTileRows - 1) / kTileRows;
     p.groups = K / kGroupK;
     p.units = p.tiles * p.groups * nmat;
-    p.slot = (int)(calls.fetch_add(1u) % kQtcSlots);
     p.x_bf16 = x_bf16;
     p.y_bf16 = y_bf16;
     const int ctas = p.units < sm_count ? p.units : sm_count;

@@ -62,7 +62,6 @@ struct QtcParams {
     unsigned int* fault;
     int32_t N, K;
     int32_t tiles, groups, units;     // units = tiles x groups x matrices
-    int32_t slot;
     int32_t x_bf16, y_bf16;
 };
 

@@ -24,8 +24,32 @@
  *
  * Pointers.  Every w, x, y, out, X, Y, workspace pointer is a DEVICE pointer
  * (or managed memory) on the current CUDA device.  The caller owns every
- * buffer: the library allocates nothing, frees nothing and keeps no pointer
- * after a call returns.  Outputs must not overlap inputs.
+ * buffer: the calls allocate nothing, free nothing and keep no pointer after
+ * they return (qbw_chain_create is the one call that allocates).  Outputs
+ * must not overlap inputs.
+ *
+ * Library state.  Loading the library on a device reserves, as static device
+ * arrays of the library's module, besides a 4-byte fault word
+ * (qbw_fault_read):
+ *   - the split-tile scratch of the tensor-core M = 1 kernels (qmv_q4_0,
+ *     qmv_gateup_q4_0 and qmv_q4_k at the sizes that take them, and
+ *     qmm_q4_0_smallM with M <= 2): 32 slots of 160 CTAs x 2 x 128 tagged
+ *     64-bit words, 10,485,760 bytes.  When a 128-row output tile is split
+ *     between two CTAs, the CTA that does not write it publishes its partial
+ *     sums there, each word tagged with its launch's grid identifier, and the
+ *     CTA that writes the tile takes only words carrying its own launch's tag,
+ *     then clears them.  The slot is chosen on the device from the launch's
+ *     grid identifier (it is not fixed when a call is captured in a CUDA
+ *     graph), so launches near each other in launch order never share a slot.
+ *     Two launches 32 apart in the device's launch order that run at the same
+ *     time (for example on two streams, one of them issuing 32 launches while
+ *     a call on the other is still running) share a slot: the writing CTA then
+ *     waits in vain and reports fault bit 1 << 4 instead of adding a value from
+ *     another call.  No word left by a call that faulted is ever taken by a
+ *     later call.
+ *   - the scratch of qmm_q4_0_smallM_noalloc (see there), 4 MiB.
+ * Both stay reserved on every device that loads the library until the process
+ * exits.
  *
  * Streams.  `stream` is a cudaStream_t passed as void* (NULL = legacy default
  * stream).  Work is enqueued asynchronously; a call never synchronizes.
@@ -158,7 +182,10 @@ qbw_status qmv_gateup_q4_0(const void *w_gate, const void *w_up, const void *x, 
  *               whole workspace zero again, so the single zero-fill at
  *               allocation is enough, also when one workspace serves calls of
  *               different shapes; after a call that reported a device fault
- *               (qbw_fault_read), zero-fill it again.  Calls that share one
+ *               (qbw_fault_read), zero-fill it again (a call that gave up may
+ *               leave arrival counters nonzero; tagged words carry their
+ *               launch's grid identifier, so no later call takes a stale
+ *               one).  Calls that share one
  *               workspace must not run concurrently.  May be
  *               NULL when the size query returns 0: so it does for one K-split
  *               per tile, and for 2 .. 8 splits when the device holds all the
@@ -190,10 +217,13 @@ qbw_status qmm_q4_0_smallM(const void *w, const void *X, qbw_dtype xt, void *Y, 
  * shape needs at most 2,494,464 bytes, so the limit is only reached on parts
  * with more SMs.
  *
- * The first call on each device that needs scratch does a one-time set-up: it
- * looks up the array's address on that device and zero-fills it on `stream`
- * (the arrival counters must start at zero; every completed call leaves them at
- * zero).  Make that first call before any stream capture.
+ * Every call that needs scratch looks up the array's address on the current
+ * device (cudaGetSymbolAddress; no allocation).  The first such call on a
+ * device, and the first one after qbw_fault_read has reported a nonzero fault
+ * word, first zero-fills the array on `stream` (cudaMemsetAsync): the arrival
+ * counters must start at zero, every completed call leaves them at zero, but a
+ * call that gave up on a bounded wait may leave them nonzero.  Make the first
+ * call before any stream capture, and read the fault word outside a capture.
  *
  * All calls on one device share the one array: calls that may overlap in time
  * (different streams without ordering, several host threads) race on it and
@@ -331,8 +361,10 @@ qbw_status qbw_chain_destroy(qbw_chain chain);
  *   c = 1  a bounded wait for an asynchronous copy ran out (about two seconds)
  *   c = 2  a bounded wait for tensor-core work ran out
  *   c = 3  qembed_q8_0 met a row index outside [0, N)
- *   c = 4  qmv_q4_0 waited in vain (about two seconds) for another CTA's share
- *          of a 128-row tile split between CTAs
+ *   c = 4  a kernel waited in vain (about two seconds) for another CTA's share
+ *          of a 128-row tile split between CTAs (qmv_q4_0, qmv_gateup_q4_0,
+ *          qmv_q4_k, qmm_q4_0_smallM; see "Library state" for the one case
+ *          of concurrent launches that causes it)
  *   c = 5  internal: a launch plan exceeded a kernel's fixed capacity (the
  *          host-side planning never allows it; seen only after a library bug)
  *   c = 6  qbw_chain_run: a CTA waited in vain (about two seconds) for the
