@@ -31,8 +31,9 @@ cudaError_t launch_qmm_tc(const CUtensorMap& tmap_w, const CUtensorMap& tmap_x, 
 int qmm_tc_max_active_clusters(int nt, int cluster);
 cudaError_t launch_selftest_wait(int which, uint64_t limit_ns, unsigned int* fault, cudaStream_t stream);
 bool qmv_tc_supported(int nmat, int64_t N, int64_t K, int sm_count);
-cudaError_t launch_qmv_tc(int fmt, int nmat, int ntok, const CUtensorMap* tmap_w, const void* x, int x_bf16,
-                          void* y, int y_bf16, int N, int K, int sm_count, unsigned int* fault, cudaStream_t stream);
+cudaError_t launch_qmv_tc(int fmt, int nmat, int ntok, const CUtensorMap* tmap_w, const void* const* w,
+                          const void* x, int x_bf16, void* y, int y_bf16, int N, int K, int sm_count,
+                          unsigned int* fault, cudaStream_t stream);
 int qmm_tc_tile_rows();
 bool qmv_chain_step_supported(int nmat, int64_t N, int64_t K, int ctas);
 void qmv_chain_fill_step(ChainStepDesc* d, int nmat, int64_t N, int64_t K);
@@ -426,8 +427,9 @@ qbw_status qmv_common(int fmt, int nmat, const void* w0, const void* w1, const v
         qmv_tc_supported(nmat, N, K, di->sm_count)) {
         CUtensorMap tw[2];
         if (encode_q4_tile_map(&tw[0], w0, N, K) && (nmat == 1 || encode_q4_tile_map(&tw[1], w1, N, K))) {
-            cudaError_t e = launch_qmv_tc(fmt, nmat, 1, tw, x, xt == QBW_BF16, y, yt == QBW_BF16, (int)N, (int)K,
-                                          di->sm_count, di->fault, s);
+            const void* wp[2] = {w0, nmat == 2 ? w1 : w0};
+            cudaError_t e = launch_qmv_tc(fmt, nmat, 1, tw, wp, x, xt == QBW_BF16, y, yt == QBW_BF16, (int)N,
+                                          (int)K, di->sm_count, di->fault, s);
             return e == cudaSuccess ? QBW_OK : QBW_ECUDA;
         }
     }
@@ -530,7 +532,8 @@ qbw_status qmm_q4_0_smallM(const void* w, const void* X, qbw_dtype xt, void* Y, 
     if (q.exact && (uintptr_t)w % 16 == 0 && (uintptr_t)X % 16 == 0) {
         CUtensorMap tw[2];
         if (encode_q4_tile_map(&tw[0], w, N, K)) {
-            cudaError_t e = launch_qmv_tc(kFmtQ4, 1, (int)M, tw, X, 1, Y, yt == QBW_BF16, (int)N, (int)K,
+            const void* wp[2] = {w, w};
+            cudaError_t e = launch_qmv_tc(kFmtQ4, 1, (int)M, tw, wp, X, 1, Y, yt == QBW_BF16, (int)N, (int)K,
                                           di->sm_count, di->fault, s);
             return e == cudaSuccess ? QBW_OK : QBW_ECUDA;
         }
@@ -663,6 +666,8 @@ qbw_status qbw_chain_create(const qbw_chain_step* steps, int nsteps, qbw_chain* 
             !encode_q4_tile_map(&d.tmap[1], nmat == 2 ? c.w_up : c.w, c.N, c.K))
             return QBW_ECUDA;
         qmv_chain_fill_step(&d, nmat, c.N, c.K);
+        d.w[0] = static_cast<const uint8_t*>(c.w);
+        d.w[1] = static_cast<const uint8_t*>(nmat == 2 ? c.w_up : c.w);
         d.x = c.x;
         d.y = c.y;
         d.y_bf16 = c.yt == QBW_BF16;

@@ -99,6 +99,7 @@ struct ChainStepDesc {
     CUtensorMap tmap[2];      // the (gate) matrix and, for nmat = 2, the up matrix
     const void* x;            // bf16 [K]
     void* y;                  // [N], bf16 (y_bf16) or fp32
+    const uint8_t* w[2];      // the raw weights of tmap[0], tmap[1] (the read-back correction reads a row)
     int32_t N, K, nmat, y_bf16;
     int32_t tiles, groups, units, reserved;
 };

@@ -130,6 +130,8 @@ __global__ void __launch_bounds__(kThreads, 1) qmv_chain_kernel(const __grid_con
     for (int i = threadIdx.x; i < (int)(kSets * kBBytes / 16); i += kThreads)
         sts128(sbase + kOffB + 16u * (uint32_t)i, make_uint4(0u, 0u, 0u, 0u));
     for (int i = threadIdx.x; i < kSets * kMaxLocalTiles * 2 * kTileRows; i += kThreads) part[i] = 0.f;
+    for (int i = threadIdx.x; i < kProducerWarp * 32 * 3; i += kThreads)       // acc_q and fixups
+        reinterpret_cast<uint32_t*>(smem + kOffQ)[i] = 0u;
 
     // this CTA's units over all steps (the ring and set sequence runs on across steps)
     int n_total = 0;
@@ -292,20 +294,58 @@ __global__ void __launch_bounds__(kThreads, 1) qmv_chain_kernel(const __grid_con
                 }
                 counted = true;
             };
+            // the row's sums of the tile being accumulated, one per matrix, and
+            // the error-check terms of its flagged units
             float acc[2] = {0.f, 0.f};
+            float* acc_q = reinterpret_cast<float*>(smem + kOffQ) + 2 * threadIdx.x;
+            uint32_t* fixups = reinterpret_cast<uint32_t*>(smem + kOffFix) + threadIdx.x;
             int acc_tile = -1, pend_tile = -1, pend_mat = 0, pend_sl = 0;
             uint32_t pend_dd[4] = {0u, 0u, 0u, 0u};
             bool pend = false;
+            // the exact sum of w r over this set's units of tile T, matrix m (r:
+            // what the pieces miss), for a segment the check flags
+            auto segment_correction = [&](int T, int m) -> float {
+                const int64_t nrow = (int64_t)T * kTileRows + row;
+                float corr = 0.f;
+                if (nrow >= st.N) return corr;
+                const int64_t rb = weight_row_bytes(kFmtQ4, st.K);
+                for (int i = ((set - I_base) % kSets + kSets) % kSets; i < n; i += kSets) {
+                    const int u = u0 + i, ug = u / nmat, mat = u - ug * nmat, t = ug / G, g = ug - t * G;
+                    if (t > T) break;
+                    if (t < T || mat != m) continue;
+                    int sl = g - xg0;
+                    if (sl < 0) sl += G;
+                    if (sl >= kXtGroups) sl = 0;
+                    if (!group_flagged(sbase, sl)) continue;     // no residuals
+                    corr += unit_correction<kFmtQ4, 2, true>(st.w[m] + nrow * rb + (int64_t)g * 144, st.x, g, sbase, sl);
+                }
+                return corr;
+            };
+            // the set's partial rows of acc_tile -> part[]; a segment that fails
+            // the error check (its units' terms, summed in acc_q) gets bit
+            // 2 (acc_tile - tile0) + m in fixups, and its exact correction is
+            // added after the step's unit loop
+            auto flush = [&]() {
+                if (acc_tile < 0) return;
+#pragma unroll
+                for (int m = 0; m < 2; ++m) {
+                    const float q = acc_q[m];
+                    if (q != 0.f) {
+                        acc_q[m] = 0.f;
+                        if (segment_needs_correction(q)) *fixups |= 1u << (2 * (acc_tile - tile0) + m);
+                    }
+                    part[part_at(set, acc_tile - tile0, m, row)] = acc[m];
+                }
+            };
             auto add_unit = [&](float r0) {
                 if (pend_tile != acc_tile) {
-                    if (acc_tile >= 0) {
-                        part[part_at(set, acc_tile - tile0, 0, row)] = acc[0];
-                        part[part_at(set, acc_tile - tile0, 1, row)] = acc[1];
-                    }
+                    flush();
                     acc[0] = 0.f;
                     acc[1] = 0.f;
                     acc_tile = pend_tile;
-                    if (!counted && pend_tile > tile0) count_in();
+                    // a first-tile share that needs its correction is published
+                    // after the unit loop instead
+                    if (!counted && pend_tile > tile0 && !__any_sync(0xffffffffu, (*fixups & 3u) != 0u)) count_in();
                 }
                 if (pend_mat == 0) acc[0] += r0;
                 else acc[1] += r0;
@@ -317,13 +357,24 @@ __global__ void __launch_bounds__(kThreads, 1) qmv_chain_kernel(const __grid_con
                 tmem_wait_ld();
                 float c[8];
                 table_f8(sbase, kOffXc, pend_sl, c);
-                add_unit(unit_dot_e4m3(dv, pend_dd, c));
+                const float r0 = unit_dot_e4m3(dv, pend_dd, c);
+                add_unit(r0);
+                if (__builtin_expect(__float_as_uint(c[0]) >> 31, 0)) {     // a flagged group
+                    // the unit's error-check term into its segment's sum
+                    float a[8];
+                    table_f8(sbase, kOffXr, pend_sl, a);
+                    acc_q[pend_mat] += unit_check_term<kFmtQ4>(dv, pend_dd, c, a);
+                }
             };
             // this set's units of the step: I = I_base + i = set (mod 3)
             for (int i = ((set - I_base) % kSets + kSets) % kSets; i < n && ok; i += kSets, ++k) {
                 const int I = I_base + i;
                 const int u = u0 + i, ug = u / nmat, mat = u - ug * nmat, t = ug / G, g = ug - t * G;
                 const int stg = I % kStages;
+                // this unit's group in the table
+                int cur_sl = g - xg0;
+                if (cur_sl < 0) cur_sl += G;
+                if (cur_sl >= kXtGroups) cur_sl = 0;       // never: the host checks the table size
                 const bool got = mbar_wait_bounded(full_bar(bar0, stg), (uint32_t)(I / kStages) & 1u, p.fault,
                                                    kFaultBulkWaitTimeout);
                 if (!__all_sync(0xffffffffu, got)) {
@@ -346,9 +397,6 @@ __global__ void __launch_bounds__(kThreads, 1) qmv_chain_kernel(const __grid_con
                 uint32_t dd[4];
 #pragma unroll
                 for (int P = 0; P < 4; ++P) dd[P] = scale_pair(v, P);
-                int cur_sl = g - xg0;
-                if (cur_sl < 0) cur_sl += G;
-                if (cur_sl >= kXtGroups) cur_sl = 0;       // never: the host checks the table size
                 uint2 bp0 = make_uint2(0u, 0u), bp1 = bp0;
                 if (bwriter) {
                     const uint4 tq = lds128(sbase + kOffXt + (uint32_t)(cur_sl * 32 + xl) * 16u);
@@ -433,9 +481,15 @@ __global__ void __launch_bounds__(kThreads, 1) qmv_chain_kernel(const __grid_con
                     if (lane == 0) set_abort(p.bar_count + 1);
                 }
             }
-            if (acc_tile >= 0) {
-                part[part_at(set, acc_tile - tile0, 0, row)] = acc[0];
-                part[part_at(set, acc_tile - tile0, 1, row)] = acc[1];
+            flush();
+            // the flagged segments' exact corrections (rare: activations whose
+            // elements far below their block's largest carry the row's sum)
+            uint32_t fx = *fixups;
+            *fixups = 0u;
+            while (fx != 0u) {
+                const int b = __ffs(fx) - 1;
+                fx &= fx - 1u;
+                part[part_at(set, b >> 1, b & 1, row)] += segment_correction(tile0 + (b >> 1), b & 1);
             }
             if (!counted) count_in();
             dequant_sync();     // every set's partial rows are in part[]

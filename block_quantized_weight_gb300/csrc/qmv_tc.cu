@@ -54,6 +54,7 @@
 // already decoded in registers.
 #include <algorithm>
 #include <cstdint>
+#include <type_traits>
 
 #include "qbw_device.cuh"
 #include "qbw_internal.h"
@@ -111,6 +112,7 @@ __device__ __forceinline__ void qmv_tc_body(const QtcParams& p) {
     const bool contrib0 = n > 0 && tile0 * GU < u0;
     __shared__ unsigned int qcount[4];
     if (threadIdx.x < 4) qcount[threadIdx.x] = 0u;
+    if (threadIdx.x == 0) *reinterpret_cast<uint32_t*>(smem + kOffXflag) = 0u;     // set by the table build
     const uint64_t gid = grid_id();
     const uint32_t tag = launch_tag();
     unsigned long long* share = &g_qtc_share[gid % kQtcSlots][0][0][0];   // [cta][matrix][row]
@@ -126,6 +128,8 @@ __device__ __forceinline__ void qmv_tc_body(const QtcParams& p) {
     for (int i = threadIdx.x; i < (int)(2 * kSets * kBBytes / 16); i += kThreads)     // B and B2
         sts128(sbase + kOffB + 16u * (uint32_t)i, make_uint4(0u, 0u, 0u, 0u));
     for (int i = threadIdx.x; i < kSets * kMaxLocalTiles * 2 * kTileRows; i += kThreads) part[i] = 0.f;
+    for (int i = threadIdx.x; i < kProducerWarp * 32 * 3; i += kThreads)       // acc_q and fixups
+        reinterpret_cast<uint32_t*>(smem + kOffQ)[i] = 0u;
 
     if (warp == kProducerWarp) {
         if (lane == 0) {
@@ -291,286 +295,377 @@ __device__ __forceinline__ void qmv_tc_body(const QtcParams& p) {
             }
             counted = true;
         };
-        // the row's sums of the tile being accumulated, one per matrix
-        float acc[NCH];
-#pragma unroll
-        for (int m = 0; m < NCH; ++m) acc[m] = 0.f;
-        int acc_tile = -1, pend_tile = -1, pend_mat = 0;
-        auto add_unit = [&](float r0, float r1) {
-            if (pend_tile != acc_tile) {
-                if (acc_tile >= 0)
-#pragma unroll
-                    for (int m = 0; m < NCH; ++m) part[part_at(set, acc_tile - tile0, m, row)] = acc[m];
-#pragma unroll
-                for (int m = 0; m < NCH; ++m) acc[m] = 0.f;
-                acc_tile = pend_tile;
-                if (!counted && pend_tile > tile0) count_in();
-            }
-            if constexpr (NTOK == 2) {
-                acc[0] += r0;
-                acc[1] += r1;
-            } else {
-#pragma unroll
-                for (int m = 0; m < NMAT; ++m)
-                    if (m == pend_mat) acc[m] += r0;
-            }
-        };
-        uint32_t pend_dd[4] = {0u, 0u, 0u, 0u};
-        float pend_sx = 0.f;     // Q4_K: the previous unit's sub-block sum of this lane's group of 4
-        int pend_sl = 0;         // 8-bit form: the previous unit's table slot
-        int k = 0;
-        for (int i = set; i < n; i += kSets, ++k) {
-            const int u = u0 + i, ug = u / NMAT, mat = u - ug * NMAT, t = ug / G, g = ug - t * G;
-            const int s = i % kStages;
-            // this lane's eight activations of the group, loaded before the waits
-            uint4 xr0 = make_uint4(0u, 0u, 0u, 0u), xr1 = xr0;
-            if (loads_x) {
-                const int e = g * kGroupK + 8 * xl;
-                if (NTOK == 2) {
-                    xr0 = __ldg(reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p.x) + e));
-                    xr1 = __ldg(reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p.x) + p.K + e));
-                } else if (p.x_bf16) {
-                    xr0 = __ldg(reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p.x) + e));
-                } else {
-                    xr0 = __ldg(reinterpret_cast<const uint4*>(static_cast<const float*>(p.x) + e));
-                    xr1 = __ldg(reinterpret_cast<const uint4*>(static_cast<const float*>(p.x) + e + 4));
+        // The unit loop, in two compiled forms: kGuard (the 8-bit form, when
+        // some group of this CTA's table is flagged) adds each flagged unit's
+        // error-check term and the flagged segments' exact corrections; the
+        // other form carries none of that code.
+        auto run = [&](auto guard_tag) {
+            constexpr bool kGuard = decltype(guard_tag)::value;
+            // the row's sums of the tile being accumulated, one per matrix; in the
+            // 8-bit form also the error-check terms of its flagged units
+            float acc[NCH];
+    #pragma unroll
+            for (int m = 0; m < NCH; ++m) acc[m] = 0.f;
+            float* acc_q = reinterpret_cast<float*>(smem + kOffQ) + 2 * threadIdx.x;
+            uint32_t* fixups = reinterpret_cast<uint32_t*>(smem + kOffFix) + threadIdx.x;
+            int acc_tile = -1, pend_tile = -1, pend_mat = 0;
+            // 8-bit form: the exact sum of w r over this set's units of tile T,
+            // matrix m (r: what the pieces miss), for a segment the check flags
+            auto segment_correction = [&](int T, int m) -> float {
+                const int64_t nrow = (int64_t)T * kTileRows + row;
+                float corr = 0.f;
+                if (nrow >= p.N) return corr;
+                for (int i = set; i < n; i += kSets) {
+                    const int u = u0 + i, ug = u / NMAT, mat = u - ug * NMAT, t = ug / G, g = ug - t * G;
+                    if (t > T) break;
+                    if (t < T || mat != m) continue;
+                    int sl = g - xg0;
+                    if (sl < 0) sl += G;
+                    if (sl >= kXtGroups) sl = 0;
+                    if (!group_flagged(sbase, sl)) continue;     // no residuals
+                    corr += unit_correction<FMT, F8 ? F8 : 2, false>(p.w[m] + nrow * p.row_bytes + (int64_t)g * 144,
+                                                                      p.x, g, sbase, sl);
                 }
-            }
-            const bool got = mbar_wait_bounded(full_bar(bar0, s), (uint32_t)(i / kStages) & 1u, p.fault,
-                                               kFaultBulkWaitTimeout);
-            if (!__all_sync(0xffffffffu, got)) {
-                ok = false;
-                break;
-            }
-            const uint32_t src = sbase + (uint32_t)s * kRawStageBytes + raw_row;
-            uint32_t v[36];
-#pragma unroll
-            for (int j = 0; j < 9; ++j) {
-                const uint4 w = lds128(src + 16u * (uint32_t)j);
-                v[4 * j] = w.x;
-                v[4 * j + 1] = w.y;
-                v[4 * j + 2] = w.z;
-                v[4 * j + 3] = w.w;
-            }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(empty_bar(bar0, s));     // raw rows of stage s read
-            uint32_t dd[4];
-#pragma unroll
-            for (int P = 0; P < 4; ++P) dd[P] = (FMT == kFmtQ4K) ? v[P] : scale_pair(v, P);
-            uint32_t c0[32], c1[32];
-            // B chunk of a B-writing lane: x_hi and x_lo as bf16, written in the
-            // K-half its slot belongs to
-            uint4 bhi = make_uint4(0u, 0u, 0u, 0u), blo = bhi;
-            float cur_sx = 0.f;
-            if (loads_x) {
-                if (FMT == kFmtQ4K) {
-                    float f[8];
-                    if (p.x_bf16) {
-                        const uint32_t w4[4] = {xr0.x, xr0.y, xr0.z, xr0.w};
-#pragma unroll
+                return corr;
+            };
+            // the set's partial rows of acc_tile -> part[]; in the 8-bit form a
+            // segment that fails the error check (its units' terms, summed in
+            // acc_q) gets bit 2 (acc_tile - tile0) + m in fixups, and its exact
+            // correction is added after the unit loop
+            auto flush = [&]() {
+                if (acc_tile < 0) return;
+    #pragma unroll
+                for (int m = 0; m < NCH; ++m) {
+                    if constexpr (kGuard) {
+                        const float q = acc_q[m];
+                        if (q != 0.f) {
+                            acc_q[m] = 0.f;
+                            if (segment_needs_correction(q)) *fixups |= 1u << (2 * (acc_tile - tile0) + m);
+                        }
+                    }
+                    part[part_at(set, acc_tile - tile0, m, row)] = acc[m];
+                }
+            };
+            auto add_unit = [&](float r0, float r1) {
+                if (pend_tile != acc_tile) {
+                    flush();
+    #pragma unroll
+                    for (int m = 0; m < NCH; ++m) acc[m] = 0.f;
+                    acc_tile = pend_tile;
+                    // a first-tile share that needs its correction is published
+                    // after the unit loop instead
+                    if (!counted && pend_tile > tile0 && !__any_sync(0xffffffffu, kGuard && (*fixups & 3u) != 0u))
+                        count_in();
+                }
+                if constexpr (NTOK == 2) {
+                    acc[0] += r0;
+                    acc[1] += r1;
+                } else {
+    #pragma unroll
+                    for (int m = 0; m < NMAT; ++m)
+                        if (m == pend_mat) acc[m] += r0;
+                }
+            };
+            uint32_t pend_dd[4] = {0u, 0u, 0u, 0u};
+            float pend_sx = 0.f;     // Q4_K: the previous unit's sub-block sum of this lane's group of 4
+            int pend_sl = 0;         // 8-bit form: the previous unit's table slot
+            // 8-bit form, a unit of a flagged group (the sign of its c_0; after
+            // add_unit has moved acc_tile to it): its error-check term into the
+            // segment's sum
+            auto check_unit = [&](const uint32_t (&dv)[16], const float (&c)[8]) {
+                float a[8];
+                table_f8(sbase, kOffXr, pend_sl, a);
+                acc_q[pend_mat] += unit_check_term<FMT>(dv, pend_dd, c, a);
+            };
+            int k = 0;
+            for (int i = set; i < n; i += kSets, ++k) {
+                const int u = u0 + i, ug = u / NMAT, mat = u - ug * NMAT, t = ug / G, g = ug - t * G;
+                const int s = i % kStages;
+                // this lane's eight activations of the group, loaded before the waits
+                uint4 xr0 = make_uint4(0u, 0u, 0u, 0u), xr1 = xr0;
+                if (loads_x) {
+                    const int e = g * kGroupK + 8 * xl;
+                    if (NTOK == 2) {
+                        xr0 = __ldg(reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p.x) + e));
+                        xr1 = __ldg(reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p.x) + p.K + e));
+                    } else if (p.x_bf16) {
+                        xr0 = __ldg(reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p.x) + e));
+                    } else {
+                        xr0 = __ldg(reinterpret_cast<const uint4*>(static_cast<const float*>(p.x) + e));
+                        xr1 = __ldg(reinterpret_cast<const uint4*>(static_cast<const float*>(p.x) + e + 4));
+                    }
+                }
+                const bool got = mbar_wait_bounded(full_bar(bar0, s), (uint32_t)(i / kStages) & 1u, p.fault,
+                                                   kFaultBulkWaitTimeout);
+                if (!__all_sync(0xffffffffu, got)) {
+                    ok = false;
+                    break;
+                }
+                const uint32_t src = sbase + (uint32_t)s * kRawStageBytes + raw_row;
+                uint32_t v[36];
+    #pragma unroll
+                for (int j = 0; j < 9; ++j) {
+                    const uint4 w = lds128(src + 16u * (uint32_t)j);
+                    v[4 * j] = w.x;
+                    v[4 * j + 1] = w.y;
+                    v[4 * j + 2] = w.z;
+                    v[4 * j + 3] = w.w;
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(empty_bar(bar0, s));     // raw rows of stage s read
+                uint32_t dd[4];
+    #pragma unroll
+                for (int P = 0; P < 4; ++P) dd[P] = (FMT == kFmtQ4K) ? v[P] : scale_pair(v, P);
+                uint32_t c0[32], c1[32];
+                // B chunk of a B-writing lane: x_hi and x_lo as bf16, written in the
+                // K-half its slot belongs to
+                uint4 bhi = make_uint4(0u, 0u, 0u, 0u), blo = bhi;
+                float cur_sx = 0.f;
+                if (loads_x) {
+                    if (FMT == kFmtQ4K) {
+                        float f[8];
+                        if (p.x_bf16) {
+                            const uint32_t w4[4] = {xr0.x, xr0.y, xr0.z, xr0.w};
+    #pragma unroll
+                            for (int e = 0; e < 4; ++e) {
+                                f[2 * e] = bf16_lo_to_float(w4[e]);
+                                f[2 * e + 1] = bf16_hi_to_float(w4[e]);
+                            }
+                        } else {
+                            f[0] = __uint_as_float(xr0.x); f[1] = __uint_as_float(xr0.y);
+                            f[2] = __uint_as_float(xr0.z); f[3] = __uint_as_float(xr0.w);
+                            f[4] = __uint_as_float(xr1.x); f[5] = __uint_as_float(xr1.y);
+                            f[6] = __uint_as_float(xr1.z); f[7] = __uint_as_float(xr1.w);
+                        }
+                        cur_sx = ((f[0] + f[1]) + (f[2] + f[3])) + ((f[4] + f[5]) + (f[6] + f[7]));
+                    }
+                    if (!bwriter) {
+                        // Q4_K lanes outside warp q's B slots: only the sum above
+                    } else if (NTOK == 2) {
+                        bhi = xr0;    // token 0 in the x_hi column, token 1 in the x_lo column
+                        blo = xr1;
+                    } else if (p.x_bf16) {
+                        bhi = xr0;
+                    } else {
+                        const float f[8] = {__uint_as_float(xr0.x), __uint_as_float(xr0.y), __uint_as_float(xr0.z),
+                                            __uint_as_float(xr0.w), __uint_as_float(xr1.x), __uint_as_float(xr1.y),
+                                            __uint_as_float(xr1.z), __uint_as_float(xr1.w)};
+                        uint32_t h[4], l[4];
+    #pragma unroll
                         for (int e = 0; e < 4; ++e) {
-                            f[2 * e] = bf16_lo_to_float(w4[e]);
-                            f[2 * e + 1] = bf16_hi_to_float(w4[e]);
+                            h[e] = pack_bf16x2(f[2 * e], f[2 * e + 1]);
+                            l[e] = pack_bf16x2(f[2 * e] - bf16_lo_to_float(h[e]), f[2 * e + 1] - bf16_hi_to_float(h[e]));
+                        }
+                        bhi = make_uint4(h[0], h[1], h[2], h[3]);
+                        blo = make_uint4(l[0], l[1], l[2], l[3]);
+                    }
+                }
+                if constexpr (FMT == kFmtQ4K) {
+                    // sub-block sums: lanes 4j .. 4j + 3 hold sub-block j's 32 activations
+                    cur_sx += __shfl_xor_sync(0xffffffffu, cur_sx, 1);
+                    cur_sx += __shfl_xor_sync(0xffffffffu, cur_sx, 2);
+                }
+                // 8-bit form: this unit's group in the table; the B-writing lanes'
+                // pieces of their slot
+                int cur_sl = 0;
+                uint2 bp0 = make_uint2(0u, 0u), bp1 = bp0, bp2 = bp0;
+                if constexpr (F8) {
+                    cur_sl = g - xg0;
+                    if (cur_sl < 0) cur_sl += G;
+                    if (cur_sl >= kXtGroups) cur_sl = 0;       // never: the host checks the table size
+                    if (bwriter) {
+                        const uint32_t ch = (uint32_t)(cur_sl * 32 + xl);
+                        const uint4 tq = lds128(sbase + kOffXt + ch * 16u);
+                        bp0 = make_uint2(tq.x, tq.y);
+                        bp1 = make_uint2(tq.z, tq.w);
+                        if constexpr (F8 == 3)
+                            asm volatile("ld.shared.v2.b32 {%0, %1}, [%2];"
+                                         : "=r"(bp2.x), "=r"(bp2.y)
+                                         : "r"(sbase + kOffXt2 + ch * 8u));
+                    }
+                }
+                const uint32_t prev = (uint32_t)(k - 1) & 1u;     // completion parity of the previous unit
+                // ---- half 0: K 0..127 (block pairs 0, 1; B atoms 0, 1 written by warps 0, 1)
+                if constexpr (Q4K8) codes_q4k_e4m3<0>(v, c0);
+                else if constexpr (F8) codes_pair_e4m3<0>(v, c0);
+                else codes_pair<FMT, 0>(v, c0);
+                if (k > 0) {
+                    const bool free = mbar_wait_bounded(aempty_bar(bar0, set, 0), prev, p.fault, kFaultMmaWaitTimeout);
+                    if (!__all_sync(0xffffffffu, free)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                }
+                if (bwriter && bhalf == 0) {
+                    if constexpr (Q4K8) {
+                        sts64(k8_p0, bp0);
+                        sts64(k8_p1, bp1);
+                        if constexpr (F8 == 3) sts64(k8_p1 + (kOffB2 - kOffB), bp2);
+                    } else if constexpr (F8) {
+                        sts64(f8_p0, bp0);
+                        sts64(f8_p1, bp1);
+                        sts64(f8_n0, make_uint2(bp0.x ^ 0x80808080u, bp0.y ^ 0x80808080u));
+                        sts64(f8_n1, make_uint2(bp1.x ^ 0x80808080u, bp1.y ^ 0x80808080u));
+                        if constexpr (F8 == 3) {     // third pieces: B2, the second piece's rows
+                            sts64(f8_p1 + (kOffB2 - kOffB), bp2);
+                            sts64(f8_n1 + (kOffB2 - kOffB), make_uint2(bp2.x ^ 0x80808080u, bp2.y ^ 0x80808080u));
                         }
                     } else {
-                        f[0] = __uint_as_float(xr0.x); f[1] = __uint_as_float(xr0.y);
-                        f[2] = __uint_as_float(xr0.z); f[3] = __uint_as_float(xr0.w);
-                        f[4] = __uint_as_float(xr1.x); f[5] = __uint_as_float(xr1.y);
-                        f[6] = __uint_as_float(xr1.z); f[7] = __uint_as_float(xr1.w);
+                        sts128(b_hi, bhi);
+                        sts128(b_lo, blo);
                     }
-                    cur_sx = ((f[0] + f[1]) + (f[2] + f[3])) + ((f[4] + f[5]) + (f[6] + f[7]));
+                    fence_proxy_async_smem();     // B visible to the tensor core
                 }
-                if (!bwriter) {
-                    // Q4_K lanes outside warp q's B slots: only the sum above
-                } else if (NTOK == 2) {
-                    bhi = xr0;    // token 0 in the x_hi column, token 1 in the x_lo column
-                    blo = xr1;
-                } else if (p.x_bf16) {
-                    bhi = xr0;
-                } else {
-                    const float f[8] = {__uint_as_float(xr0.x), __uint_as_float(xr0.y), __uint_as_float(xr0.z),
-                                        __uint_as_float(xr0.w), __uint_as_float(xr1.x), __uint_as_float(xr1.y),
-                                        __uint_as_float(xr1.z), __uint_as_float(xr1.w)};
-                    uint32_t h[4], l[4];
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        h[e] = pack_bf16x2(f[2 * e], f[2 * e + 1]);
-                        l[e] = pack_bf16x2(f[2 * e] - bf16_lo_to_float(h[e]), f[2 * e + 1] - bf16_hi_to_float(h[e]));
-                    }
-                    bhi = make_uint4(h[0], h[1], h[2], h[3]);
-                    blo = make_uint4(l[0], l[1], l[2], l[3]);
+                tmem_st32(a_taddr, c0);
+                if constexpr (!Q4K8) {
+                    if constexpr (F8) codes_pair_e4m3<1>(v, c1);
+                    else codes_pair<FMT, 1>(v, c1);
+                    tmem_wait_st();
+                    tmem_st32(a_taddr + 32u, c1);
                 }
-            }
-            if constexpr (FMT == kFmtQ4K) {
-                // sub-block sums: lanes 4j .. 4j + 3 hold sub-block j's 32 activations
-                cur_sx += __shfl_xor_sync(0xffffffffu, cur_sx, 1);
-                cur_sx += __shfl_xor_sync(0xffffffffu, cur_sx, 2);
-            }
-            // 8-bit form: this unit's group in the table; the B-writing lanes'
-            // pieces of their slot
-            int cur_sl = 0;
-            uint2 bp0 = make_uint2(0u, 0u), bp1 = bp0, bp2 = bp0;
-            if constexpr (F8) {
-                cur_sl = g - xg0;
-                if (cur_sl < 0) cur_sl += G;
-                if (cur_sl >= kXtGroups) cur_sl = 0;       // never: the host checks the table size
-                if (bwriter) {
-                    const uint32_t ch = (uint32_t)(cur_sl * 32 + xl);
-                    const uint4 tq = lds128(sbase + kOffXt + ch * 16u);
-                    bp0 = make_uint2(tq.x, tq.y);
-                    bp1 = make_uint2(tq.z, tq.w);
-                    if constexpr (F8 == 3)
-                        asm volatile("ld.shared.v2.b32 {%0, %1}, [%2];"
-                                     : "=r"(bp2.x), "=r"(bp2.y)
-                                     : "r"(sbase + kOffXt2 + ch * 8u));
-                }
-            }
-            const uint32_t prev = (uint32_t)(k - 1) & 1u;     // completion parity of the previous unit
-            // ---- half 0: K 0..127 (block pairs 0, 1; B atoms 0, 1 written by warps 0, 1)
-            if constexpr (Q4K8) codes_q4k_e4m3<0>(v, c0);
-            else if constexpr (F8) codes_pair_e4m3<0>(v, c0);
-            else codes_pair<FMT, 0>(v, c0);
-            if (k > 0) {
-                const bool free = mbar_wait_bounded(aempty_bar(bar0, set, 0), prev, p.fault, kFaultMmaWaitTimeout);
-                if (!__all_sync(0xffffffffu, free)) {
-                    ok = false;
-                    break;
-                }
-                tc_fence_after();
-            }
-            if (bwriter && bhalf == 0) {
-                if constexpr (Q4K8) {
-                    sts64(k8_p0, bp0);
-                    sts64(k8_p1, bp1);
-                    if constexpr (F8 == 3) sts64(k8_p1 + (kOffB2 - kOffB), bp2);
-                } else if constexpr (F8) {
-                    sts64(f8_p0, bp0);
-                    sts64(f8_p1, bp1);
-                    sts64(f8_n0, make_uint2(bp0.x ^ 0x80808080u, bp0.y ^ 0x80808080u));
-                    sts64(f8_n1, make_uint2(bp1.x ^ 0x80808080u, bp1.y ^ 0x80808080u));
-                    if constexpr (F8 == 3) {     // third pieces: B2, the second piece's rows
-                        sts64(f8_p1 + (kOffB2 - kOffB), bp2);
-                        sts64(f8_n1 + (kOffB2 - kOffB), make_uint2(bp2.x ^ 0x80808080u, bp2.y ^ 0x80808080u));
-                    }
-                } else {
-                    sts128(b_hi, bhi);
-                    sts128(b_lo, blo);
-                }
-                fence_proxy_async_smem();     // B visible to the tensor core
-            }
-            tmem_st32(a_taddr, c0);
-            if constexpr (!Q4K8) {
-                if constexpr (F8) codes_pair_e4m3<1>(v, c1);
-                else codes_pair<FMT, 1>(v, c1);
                 tmem_wait_st();
-                tmem_st32(a_taddr + 32u, c1);
-            }
-            tmem_wait_st();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(afull_bar(bar0, set, 0));
-            // ---- half 1: K 128..255 (block pairs 2, 3; B atoms 2, 3 written by warps 2, 3)
-            if constexpr (Q4K8) codes_q4k_e4m3<1>(v, c0);
-            else if constexpr (F8) codes_pair_e4m3<2>(v, c0);
-            else codes_pair<FMT, 2>(v, c0);
-            if (k > 0) {
-                const bool free = mbar_wait_bounded(aempty_bar(bar0, set, 1), prev, p.fault, kFaultMmaWaitTimeout);
-                if (!__all_sync(0xffffffffu, free)) {
-                    ok = false;
-                    break;
-                }
-                tc_fence_after();
-            }
-            if (bwriter && bhalf == 1) {
-                if constexpr (Q4K8) {
-                    sts64(k8_p0, bp0);
-                    sts64(k8_p1, bp1);
-                    if constexpr (F8 == 3) sts64(k8_p1 + (kOffB2 - kOffB), bp2);
-                } else if constexpr (F8) {
-                    sts64(f8_p0, bp0);
-                    sts64(f8_p1, bp1);
-                    sts64(f8_n0, make_uint2(bp0.x ^ 0x80808080u, bp0.y ^ 0x80808080u));
-                    sts64(f8_n1, make_uint2(bp1.x ^ 0x80808080u, bp1.y ^ 0x80808080u));
-                    if constexpr (F8 == 3) {     // third pieces: B2, the second piece's rows
-                        sts64(f8_p1 + (kOffB2 - kOffB), bp2);
-                        sts64(f8_n1 + (kOffB2 - kOffB), make_uint2(bp2.x ^ 0x80808080u, bp2.y ^ 0x80808080u));
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(afull_bar(bar0, set, 0));
+                // ---- half 1: K 128..255 (block pairs 2, 3; B atoms 2, 3 written by warps 2, 3)
+                if constexpr (Q4K8) codes_q4k_e4m3<1>(v, c0);
+                else if constexpr (F8) codes_pair_e4m3<2>(v, c0);
+                else codes_pair<FMT, 2>(v, c0);
+                if (k > 0) {
+                    const bool free = mbar_wait_bounded(aempty_bar(bar0, set, 1), prev, p.fault, kFaultMmaWaitTimeout);
+                    if (!__all_sync(0xffffffffu, free)) {
+                        ok = false;
+                        break;
                     }
+                    tc_fence_after();
+                }
+                if (bwriter && bhalf == 1) {
+                    if constexpr (Q4K8) {
+                        sts64(k8_p0, bp0);
+                        sts64(k8_p1, bp1);
+                        if constexpr (F8 == 3) sts64(k8_p1 + (kOffB2 - kOffB), bp2);
+                    } else if constexpr (F8) {
+                        sts64(f8_p0, bp0);
+                        sts64(f8_p1, bp1);
+                        sts64(f8_n0, make_uint2(bp0.x ^ 0x80808080u, bp0.y ^ 0x80808080u));
+                        sts64(f8_n1, make_uint2(bp1.x ^ 0x80808080u, bp1.y ^ 0x80808080u));
+                        if constexpr (F8 == 3) {     // third pieces: B2, the second piece's rows
+                            sts64(f8_p1 + (kOffB2 - kOffB), bp2);
+                            sts64(f8_n1 + (kOffB2 - kOffB), make_uint2(bp2.x ^ 0x80808080u, bp2.y ^ 0x80808080u));
+                        }
+                    } else {
+                        sts128(b_hi, bhi);
+                        sts128(b_lo, blo);
+                    }
+                    fence_proxy_async_smem();
+                }
+                if constexpr (Q4K8) {
+                    tmem_st32(a_taddr + 32u, c0);
                 } else {
-                    sts128(b_hi, bhi);
-                    sts128(b_lo, blo);
+                    tmem_st32(a_taddr + 64u, c0);
+                    if constexpr (F8) codes_pair_e4m3<3>(v, c1);
+                    else codes_pair<FMT, 3>(v, c1);
+                    tmem_wait_st();
+                    tmem_st32(a_taddr + 96u, c1);
                 }
-                fence_proxy_async_smem();
-            }
-            if constexpr (Q4K8) {
-                tmem_st32(a_taddr + 32u, c0);
-            } else {
-                tmem_st32(a_taddr + 64u, c0);
-                if constexpr (F8) codes_pair_e4m3<3>(v, c1);
-                else codes_pair<FMT, 3>(v, c1);
                 tmem_wait_st();
-                tmem_st32(a_taddr + 96u, c1);
-            }
-            tmem_wait_st();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(afull_bar(bar0, set, 1));
-            if (k > 0) {
-                // the previous unit's D (buffer (k - 1) % 2; complete since its
-                // second half's MMAs are), while this unit's MMAs use the other
-                uint32_t dv[16];
-                tmem_ld16(d_taddr + 16u * prev, dv);
-                tmem_wait_ld();
-                float r0, r1 = 0.f;
-                if constexpr (Q4K8) {
-                    float c[8], sx[8];
-                    table_f8(sbase, kOffXc, pend_sl, c);
-                    table_f8(sbase, kOffXs, pend_sl, sx);
-                    r0 = unit_dot_q4k_e4m3(dv, pend_dd, c, sx);
-                } else if constexpr (FMT == kFmtQ4K) r0 = unit_dot_q4k(dv, pend_dd, pend_sx);
-                else if constexpr (F8) {
-                    float c[8];
-                    table_f8(sbase, kOffXc, pend_sl, c);
-                    r0 = unit_dot_e4m3(dv, pend_dd, c);
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(afull_bar(bar0, set, 1));
+                if (k > 0) {
+                    // the previous unit's D (buffer (k - 1) % 2; complete since its
+                    // second half's MMAs are), while this unit's MMAs use the other
+                    uint32_t dv[16];
+                    tmem_ld16(d_taddr + 16u * prev, dv);
+                    tmem_wait_ld();
+                    float r0, r1 = 0.f;
+                    if constexpr (Q4K8) {
+                        float c[8], sx[8];
+                        table_f8(sbase, kOffXc, pend_sl, c);
+                        table_f8(sbase, kOffXs, pend_sl, sx);
+                        r0 = unit_dot_q4k_e4m3(dv, pend_dd, c, sx);
+                        add_unit(r0, r1);
+                        if constexpr (kGuard)
+                            if (__float_as_uint(c[0]) >> 31) check_unit(dv, c);
+                    } else if constexpr (FMT == kFmtQ4K) {
+                        r0 = unit_dot_q4k(dv, pend_dd, pend_sx);
+                        add_unit(r0, r1);
+                    } else if constexpr (F8) {
+                        float c[8];
+                        table_f8(sbase, kOffXc, pend_sl, c);
+                        r0 = unit_dot_e4m3(dv, pend_dd, c);
+                        add_unit(r0, r1);
+                        if constexpr (kGuard)
+                            if (__float_as_uint(c[0]) >> 31) check_unit(dv, c);
+                    } else {
+                        unit_dot<NTOK>(dv, pend_dd, r0, r1);
+                        add_unit(r0, r1);
+                    }
                 }
-                else unit_dot<NTOK>(dv, pend_dd, r0, r1);
-                add_unit(r0, r1);
+    #pragma unroll
+                for (int P = 0; P < 4; ++P) pend_dd[P] = dd[P];
+                pend_sx = cur_sx;
+                pend_sl = cur_sl;
+                pend_tile = t;
+                pend_mat = mat;
             }
-#pragma unroll
-            for (int P = 0; P < 4; ++P) pend_dd[P] = dd[P];
-            pend_sx = cur_sx;
-            pend_sl = cur_sl;
-            pend_tile = t;
-            pend_mat = mat;
-        }
-        if (ok && k > 0) {
-            // the set's last unit (k - 1)
-            const uint32_t last_par = (uint32_t)(k - 1) & 1u;
-            const bool fin = mbar_wait_bounded(aempty_bar(bar0, set, 1), last_par, p.fault, kFaultMmaWaitTimeout);
-            if (__all_sync(0xffffffffu, fin)) {
-                tc_fence_after();
-                uint32_t dv[16];
-                tmem_ld16(d_taddr + 16u * last_par, dv);
-                tmem_wait_ld();
-                float r0, r1 = 0.f;
-                if constexpr (Q4K8) {
-                    float c[8], sx[8];
-                    table_f8(sbase, kOffXc, pend_sl, c);
-                    table_f8(sbase, kOffXs, pend_sl, sx);
-                    r0 = unit_dot_q4k_e4m3(dv, pend_dd, c, sx);
-                } else if constexpr (FMT == kFmtQ4K) r0 = unit_dot_q4k(dv, pend_dd, pend_sx);
-                else if constexpr (F8) {
-                    float c[8];
-                    table_f8(sbase, kOffXc, pend_sl, c);
-                    r0 = unit_dot_e4m3(dv, pend_dd, c);
+            if (ok && k > 0) {
+                // the set's last unit (k - 1)
+                const uint32_t last_par = (uint32_t)(k - 1) & 1u;
+                const bool fin = mbar_wait_bounded(aempty_bar(bar0, set, 1), last_par, p.fault, kFaultMmaWaitTimeout);
+                if (__all_sync(0xffffffffu, fin)) {
+                    tc_fence_after();
+                    uint32_t dv[16];
+                    tmem_ld16(d_taddr + 16u * last_par, dv);
+                    tmem_wait_ld();
+                    float r0, r1 = 0.f;
+                    if constexpr (Q4K8) {
+                        float c[8], sx[8];
+                        table_f8(sbase, kOffXc, pend_sl, c);
+                        table_f8(sbase, kOffXs, pend_sl, sx);
+                        r0 = unit_dot_q4k_e4m3(dv, pend_dd, c, sx);
+                        add_unit(r0, r1);
+                        if constexpr (kGuard)
+                            if (__float_as_uint(c[0]) >> 31) check_unit(dv, c);
+                    } else if constexpr (FMT == kFmtQ4K) {
+                        r0 = unit_dot_q4k(dv, pend_dd, pend_sx);
+                        add_unit(r0, r1);
+                    } else if constexpr (F8) {
+                        float c[8];
+                        table_f8(sbase, kOffXc, pend_sl, c);
+                        r0 = unit_dot_e4m3(dv, pend_dd, c);
+                        add_unit(r0, r1);
+                        if constexpr (kGuard)
+                            if (__float_as_uint(c[0]) >> 31) check_unit(dv, c);
+                    } else {
+                        unit_dot<NTOK>(dv, pend_dd, r0, r1);
+                        add_unit(r0, r1);
+                    }
                 }
-                else unit_dot<NTOK>(dv, pend_dd, r0, r1);
-                add_unit(r0, r1);
             }
+            flush();
+            if constexpr (kGuard) {
+                // the flagged segments' exact corrections (rare: activations whose
+                // elements far below their block's largest carry the row's sum)
+                uint32_t fx = *fixups;
+                *fixups = 0u;
+                while (fx != 0u) {
+                    const int b = __ffs(fx) - 1;
+                    fx &= fx - 1u;
+                    part[part_at(set, b >> 1, b & 1, row)] += segment_correction(tile0 + (b >> 1), b & 1);
+                }
+            }
+            if (!counted) count_in();
+        };
+        bool guard = false;
+        if constexpr (F8 != 0) guard = lds32(sbase + kOffXflag) != 0u;
+        if constexpr (F8 != 0) {
+            if (guard) run(std::true_type{});
+            else run(std::false_type{});
+        } else {
+            run(std::false_type{});
         }
-        if (acc_tile >= 0)
-#pragma unroll
-            for (int m = 0; m < NCH; ++m) part[part_at(set, acc_tile - tile0, m, row)] = acc[m];
-        if (!counted) count_in();
     }
 
     tc_fence_before();
@@ -673,13 +768,17 @@ size_t qmv_tc_smem_bytes() { return kSmemBytes; }
 // fmt: kFmtQ4 or kFmtQ4K (one matrix, one token).  nmat = 2: gate + up (one
 // token).  ntok = 2 (nmat = 1, bf16 X of two rows of K, Y of two rows of N):
 // two tokens.
-cudaError_t launch_qmv_tc(int fmt, int nmat, int ntok, const CUtensorMap* tmap_w, const void* x, int x_bf16,
-                          void* y, int y_bf16, int N, int K, int sm_count, unsigned int* fault, cudaStream_t stream) {
+cudaError_t launch_qmv_tc(int fmt, int nmat, int ntok, const CUtensorMap* tmap_w, const void* const* w,
+                          const void* x, int x_bf16, void* y, int y_bf16, int N, int K, int sm_count,
+                          unsigned int* fault, cudaStream_t stream) {
     if (nmat * ntok > 2 || (ntok == 2 && !x_bf16)) return cudaErrorInvalidValue;
     if (fmt == kFmtQ4K && nmat * ntok != 1) return cudaErrorInvalidValue;
     QtcParams p;
     p.tmap_w[0] = tmap_w[0];
     p.tmap_w[1] = tmap_w[nmat == 2 ? 1 : 0];
+    p.w[0] = static_cast<const uint8_t*>(w[0]);
+    p.w[1] = static_cast<const uint8_t*>(w[nmat == 2 ? 1 : 0]);
+    p.row_bytes = weight_row_bytes(fmt, K);
     p.x = x;
     p.y = y;
     p.fault = fault;

@@ -40,6 +40,8 @@ constexpr uint32_t kOffPart = kOffB2 + kSets * kBBytes;
 constexpr uint32_t kOffBar = kOffPart + kSets * kMaxLocalTiles * 2 * kTileRows * 4;
 constexpr int kBars = 2 * kStages + 4 * kSets + 1;
 constexpr uint32_t kOffSlot = kOffBar + 8 * kBars;
+// a word set to 1 by the table build when some group of the table is flagged
+constexpr uint32_t kOffXflag = kOffSlot + 8;
 // 8-bit form: the activations of up to kXtGroups K-groups, built once per CTA:
 // per group 32 chunks of 8 elements as {piece 0, piece 1} (16 bytes each),
 // with fp32 activations a third piece (8 bytes each), and per group the 8
@@ -49,7 +51,25 @@ constexpr uint32_t kOffXt = (kOffSlot + 16 + 15) & ~15u;
 constexpr uint32_t kOffXt2 = kOffXt + kXtGroups * 32 * 16;
 constexpr uint32_t kOffXc = kOffXt2 + kXtGroups * 32 * 8;
 constexpr uint32_t kOffXs = kOffXc + kXtGroups * 8 * 4;        // Q4_K: per block sum of x (fp32)
-constexpr uint32_t kSmemBytes = kOffXs + kXtGroups * 8 * 4;
+// Per block a_j = Wmax (1 + eps) sum |x_k - pieces_k| over its elements
+// (unscaled, fp32; Wmax = 8 for Q4_0 codes, 15 for Q4_K's): the read-back's
+// bound on what the pieces miss, per unit of the block scale (see
+// unit_check_term); valid for a group whose flag is set.  The flag (some
+// element not carried exactly by its pieces) is the sign bit of the group's
+// first read-back factor c_0 at kOffXc, which is otherwise positive.
+constexpr uint32_t kOffXr = kOffXs + kXtGroups * 8 * 4;
+// Per dequantizing thread (a row of a set): the error-check term of the
+// segment being accumulated, per matrix (fp32), and the bits of its flagged
+// segments (see the read-back of the 8-bit form); zero at the start.
+constexpr uint32_t kOffQ = kOffXr + kXtGroups * 8 * 4;
+constexpr uint32_t kOffFix = kOffQ + kProducerWarp * 32 * 2 * 4;
+constexpr uint32_t kSmemBytes = kOffFix + kProducerWarp * 32 * 4;
+// The pieces' error over a segment of a row's units is accepted while it is
+// at most kPieceEps of a lower bound of the row's sum |w x| over the segment;
+// otherwise the segment's residuals are added exactly.  Elements whose
+// residual is not formed (the fp32 form's, within 2^-12) add at most 2^-12
+// more.
+constexpr float kPieceEps = 0x1p-11f;
 static_assert(kSmemBytes <= 227 * 1024, "one CTA per SM");
 
 static_assert(kStages % kSets == 0, "stage s must serve set s % 3");
@@ -63,6 +83,8 @@ struct QtcParams {
     int32_t N, K;
     int32_t tiles, groups, units;     // units = tiles x groups x matrices
     int32_t x_bf16, y_bf16;
+    const uint8_t* w[2];              // the raw weights (w[1]: the up matrix), for the read-back correction
+    int64_t row_bytes;
 };
 
 __device__ __forceinline__ uint32_t full_bar(uint32_t b0, int s) { return b0 + 8u * (uint32_t)s; }
@@ -253,21 +275,22 @@ __device__ __forceinline__ void unit_dot(const uint32_t (&dv)[16], const uint32_
     }
 }
 
-// 8-bit form, one token: r0 = sum_j (d_j c_j) (D[2j] + D[2j + 1]), j = 0..7 in
-// order, where c_j = 2^9 / s_j undoes the e4m3 code scale 2^-9 and block j's
-// activation scale s_j (c[0..7] = c_j).
+// 8-bit form, one token: r0 = sum_j (d_j c_j) (D[2j] + D[2j + 1] / 16), j =
+// 0..7 in order, where c_j = 2^9 / s_j undoes the e4m3 code scale 2^-9 and
+// block j's activation scale s_j (c[0..7] = c_j), and 1/16 the scale of the
+// second pieces.
 __device__ __forceinline__ float unit_dot_e4m3(const uint32_t (&dv)[16], const uint32_t (&dd)[4], const float (&c)[8]) {
     float r = 0.f;
 #pragma unroll
     for (int p = 0; p < 4; ++p) {
         const float2 d = half2_to_float2(dd[p]);
-        r = fmaf(d.x * c[2 * p], __uint_as_float(dv[4 * p]) + __uint_as_float(dv[4 * p + 1]), r);
-        r = fmaf(d.y * c[2 * p + 1], __uint_as_float(dv[4 * p + 2]) + __uint_as_float(dv[4 * p + 3]), r);
+        r = fmaf(d.x * fabsf(c[2 * p]), fmaf(__uint_as_float(dv[4 * p + 1]), 0.0625f, __uint_as_float(dv[4 * p])), r);
+        r = fmaf(d.y * c[2 * p + 1], fmaf(__uint_as_float(dv[4 * p + 3]), 0.0625f, __uint_as_float(dv[4 * p + 2])), r);
     }
     return r;
 }
 
-// 8-bit form of Q4_K: r0 = sum_j (d sc_j c_j) (D[2j] + D[2j + 1]) - dmin m_j sx_j,
+// 8-bit form of Q4_K: r0 = sum_j (d sc_j c_j) (D[2j] + D[2j + 1] / 16) - dmin m_j sx_j,
 // j = 0..7 in order; dd[] holds the super-block's first 16 bytes (fp16 d and
 // dmin, then the 12 six-bit scale bytes), c[j] the read-back factors and sx[j]
 // the sub-blocks' activation sums.
@@ -287,7 +310,7 @@ __device__ __forceinline__ float unit_dot_q4k_e4m3(const uint32_t (&dv)[16], con
             sc = (lo & 15u) | (((s03 >> (8 * (j - 4) + 6)) & 3u) << 4);
             m = (lo >> 4) | (((s47 >> (8 * (j - 4) + 6)) & 3u) << 4);
         }
-        r = fmaf(dm.x * (float)sc * c[j], __uint_as_float(dv[2 * j]) + __uint_as_float(dv[2 * j + 1]), r);
+        r = fmaf(dm.x * (float)sc * fabsf(c[j]), fmaf(__uint_as_float(dv[2 * j + 1]), 0.0625f, __uint_as_float(dv[2 * j])), r);
         r = fmaf(-dm.y * (float)m, sx[j], r);
     }
     return r;
@@ -352,10 +375,11 @@ __device__ __forceinline__ uint32_t b_byte(int a, int n, uint32_t byte) {
 }
 
 // Eight bf16 activations (x[2e] in the low half of word e), already scaled by
-// the power of two sc, as two e4m3 pieces whose sum is exact: p0 keeps the
-// sign, exponent and top three mantissa bits (fp32 bits & 0xFFF00000), p1
-// the remaining four bits (bf16 has seven).  Both are exact in e4m3 while the
-// element is at least 2^-2 after scaling; below that e4m3's subnormal spacing
+// the power of two sc, as two e4m3 pieces: p0 keeps the sign, exponent and top
+// three mantissa bits (fp32 bits & 0xFFF00000), p1 the remaining four bits
+// (bf16 has seven) times 16 (below 2^8 for |x| < 2^8, so within e4m3's 448;
+// the read-back divides its column by 16).  Both are exact in e4m3 while the
+// element is at least 2^-6 after scaling; below that e4m3's subnormal spacing
 // of 2^-9 rounds them.
 __device__ __forceinline__ void split_e4m3(uint4 xr, float sc, uint2& p0, uint2& p1) {
     const uint32_t w[4] = {xr.x, xr.y, xr.z, xr.w};
@@ -366,7 +390,7 @@ __device__ __forceinline__ void split_e4m3(uint4 xr, float sc, uint2& p0, uint2&
         const float lo0 = __uint_as_float(__float_as_uint(lo) & 0xFFF00000u);
         const float hi0 = __uint_as_float(__float_as_uint(hi) & 0xFFF00000u);
         h0[e] = e4m3x2(lo0, hi0);
-        h1[e] = e4m3x2(lo - lo0, hi - hi0);
+        h1[e] = e4m3x2((lo - lo0) * 16.f, (hi - hi0) * 16.f);
     }
     p0 = make_uint2(h0[0] | (h0[1] << 16), h0[2] | (h0[3] << 16));
     p1 = make_uint2(h1[0] | (h1[1] << 16), h1[2] | (h1[3] << 16));
@@ -377,10 +401,12 @@ __device__ __forceinline__ void split_e4m3(uint4 xr, float sc, uint2& p0, uint2&
 __device__ __forceinline__ float round4(float v) { return __uint_as_float((__float_as_uint(v) + 0x00080000u) & 0xFFF00000u); }
 
 // Eight fp32 activations (xa, xb in element order), already scaled by the
-// power of two sc, as three e4m3 pieces: p0 = round4(x), p1 = round4(x - p0),
-// p2 = e4m3(x - p0 - p1).  |x - p0| <= 2^-4 |x| and |x - p0 - p1| <= 2^-8 |x|
-// (each round4 halves an ulp of four bits), so p0 + p1 + p2 carries x to
-// 2^-12 relative while the pieces stay in e4m3's normal range.
+// power of two sc, as three e4m3 pieces: p0 = round4(x), p1 = 16 round4(x -
+// p0), p2 = e4m3(16 (x - p0 - round4(x - p0))); p1 and p2 share the second
+// column, which the read-back divides by 16.  |x - p0| <= 2^-4 |x| and the
+// remainder after the second piece is at most 2^-8 |x| (each round4 halves an
+// ulp of four bits), so the pieces carry x to 2^-12 relative while the third
+// stays in e4m3's normal range (the element at least 2^-2 after scaling).
 __device__ __forceinline__ void split3_e4m3(uint4 xa, uint4 xb, float sc, uint2& p0, uint2& p1, uint2& p2) {
     const uint32_t w[8] = {xa.x, xa.y, xa.z, xa.w, xb.x, xb.y, xb.z, xb.w};
     uint32_t h0[4], h1[4], h2[4];
@@ -391,13 +417,53 @@ __device__ __forceinline__ void split3_e4m3(uint4 xa, uint4 xb, float sc, uint2&
         const float ar = a - a0, br = b - b0;
         const float a1 = round4(ar), b1 = round4(br);
         h0[e] = e4m3x2(a0, b0);
-        h1[e] = e4m3x2(a1, b1);
-        h2[e] = e4m3x2(ar - a1, br - b1);
+        h1[e] = e4m3x2(a1 * 16.f, b1 * 16.f);
+        h2[e] = e4m3x2((ar - a1) * 16.f, (br - b1) * 16.f);
     }
     p0 = make_uint2(h0[0] | (h0[1] << 16), h0[2] | (h0[3] << 16));
     p1 = make_uint2(h1[0] | (h1[1] << 16), h1[2] | (h1[3] << 16));
     p2 = make_uint2(h2[0] | (h2[1] << 16), h2[2] | (h2[3] << 16));
 }
+
+__device__ __forceinline__ uint32_t umin16x2(uint32_t a, uint32_t b) {
+    uint32_t r;
+    asm("min.u16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+    return r;
+}
+
+// two e4m3 bytes (the first element in the low byte) -> two floats
+__device__ __forceinline__ float2 e4m3x2_to_float2(uint32_t b2) {
+    uint32_t h;
+    asm("{\n\t.reg .b16 t;\n\tcvt.u16.u32 t, %1;\n\tcvt.rn.f16x2.e4m3x2 %0, t;\n\t}" : "=r"(h) : "r"(b2));
+    return half2_to_float2(h);
+}
+
+// What the e4m3 pieces of one scaled activation v = x s_j leave out: v minus
+// the sum of the pieces' values, formed exactly as split_e4m3 (XP = 2) or
+// split3_e4m3 (XP = 3) forms the pieces.  Every step is exact in fp32 for bf16
+// x; for fp32 x it is within fp32 rounding of the exact residual.
+template <int XP>
+__device__ __forceinline__ float piece_residual(float v) {
+    if constexpr (XP == 2) {
+        const float p0 = __uint_as_float(__float_as_uint(v) & 0xFFF00000u);
+        const float2 d = e4m3x2_to_float2(e4m3x2(p0, (v - p0) * 16.f));
+        return (v - d.x) - d.y * 0.0625f;
+    } else {
+        const float a0 = round4(v), ar = v - a0, a1 = round4(ar);
+        const float2 d01 = e4m3x2_to_float2(e4m3x2(a0, a1 * 16.f));
+        const float d2 = e4m3x2_to_float2(e4m3x2((ar - a1) * 16.f, 0.f)).x;
+        return ((v - d01.x) - d01.y * 0.0625f) - d2 * 0.0625f;
+    }
+}
+
+// An element whose scaled exponent e' = E + es - 254 (E its biased fp32
+// exponent) is at least kExactExp is carried to 2^-12 relative or better: two
+// pieces carry bf16 exactly down to e' = -6 (e4m3's subnormal spacing 2^-9
+// reaches the last bit of p0 and of 16 p1 there), and three pieces keep fp32
+// to 2^-12 while the third stays in e4m3's normal range (e' >= -2).  Only the
+// others need their residual formed.
+template <int XP>
+constexpr int kExactExp = XP == 2 ? -6 : -2;
 
 // 8-bit form: the activation table of cnt K-groups, group xg0 + sl (mod G) in
 // slot sl, from bf16 (XP = 2) or fp32 (XP = 3) x, built by warps w = 0 .. nwarps - 1 of the calling
@@ -487,6 +553,70 @@ __device__ __forceinline__ void table_chunk(uint32_t sbase, int c, int lane, uin
         asm volatile("st.shared.b32 [%0], %1;" ::"r"(sbase + kOffXc + (uint32_t)(c >> 2) * 4u),
                      "r"((uint32_t)(263 - es) << 23)
                      : "memory");
+    // The elements the pieces carry with a relative error above 2^-11: their
+    // residuals make the correction exact (the warp's 32 chunks are one
+    // group, so the group's list is compacted with a warp prefix sum).
+    // Quick test first: the smallest nonzero |x| of the chunk (|x| - 1 as
+    // unsigned bits, which sends 0 to the top) against the exponent bound te.
+    const int te = max(254 + kExactExp<XP> - es, 1);     // candidates have E < te
+    bool any;
+    if constexpr (XP == 2) {
+        const uint32_t t0 = ((xa.x | 0x80008000u) - 0x00010001u) & 0x7FFF7FFFu;
+        const uint32_t t1 = ((xa.y | 0x80008000u) - 0x00010001u) & 0x7FFF7FFFu;
+        const uint32_t t2 = ((xa.z | 0x80008000u) - 0x00010001u) & 0x7FFF7FFFu;
+        const uint32_t t3 = ((xa.w | 0x80008000u) - 0x00010001u) & 0x7FFF7FFFu;
+        const uint32_t m2 = umin16x2(umin16x2(t0, t1), umin16x2(t2, t3));
+        any = min(m2 & 0xFFFFu, m2 >> 16) < ((uint32_t)te << 7);
+    } else {
+        const uint32_t w8[8] = {xa.x, xa.y, xa.z, xa.w, xb.x, xb.y, xb.z, xb.w};
+        uint32_t m = 0xFFFFFFFFu;
+#pragma unroll
+        for (int e = 0; e < 8; ++e) m = min(m, (w8[e] & 0x7FFFFFFFu) - 1u);
+        any = m < ((uint32_t)te << 23);
+    }
+    const uint32_t slot = (uint32_t)(c >> 5);
+    if (!__any_sync(0xffffffffu, any)) return;
+    float f[8];
+    if constexpr (XP == 2) {
+        const uint32_t w4[4] = {xa.x, xa.y, xa.z, xa.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            f[2 * e] = __uint_as_float(w4[e] << 16);
+            f[2 * e + 1] = __uint_as_float(w4[e] & 0xFFFF0000u);
+        }
+    } else {
+        const uint32_t w8[8] = {xa.x, xa.y, xa.z, xa.w, xb.x, xb.y, xb.z, xb.w};
+#pragma unroll
+        for (int e = 0; e < 8; ++e) f[e] = __uint_as_float(w8[e]);
+    }
+    uint32_t cand = 0;
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+        const int E = (int)((__float_as_uint(f[e]) >> 23) & 0xFFu);
+        if (f[e] != 0.f && E < te) cand |= 1u << e;
+    }
+    const float inv_sc = __uint_as_float((uint32_t)(254 - es) << 23);
+    float rsum = 0.f;
+#pragma unroll
+    for (int e = 0; e < 8; ++e)
+        if (cand & (1u << e)) rsum += fabsf(piece_residual<XP>(f[e] * sc));
+    rsum *= inv_sc;
+    const bool nz = rsum != 0.f;
+    // the block's sum: lanes 4j .. 4j + 3 hold block j's 32 elements
+    rsum += __shfl_xor_sync(0xffffffffu, rsum, 1);
+    rsum += __shfl_xor_sync(0xffffffffu, rsum, 2);
+    if ((lane & 3) == 0)
+        asm volatile("st.shared.f32 [%0], %1;" ::"r"(sbase + kOffXr + (uint32_t)(c >> 2) * 4u),
+                     "f"(rsum * (kSums ? 15.f : 8.f) * (1.f + kPieceEps))
+                     : "memory");
+    // the group's flag: the sign bit of block 0's read-back factor (a
+    // positive power of two), stored by lane 0, which holds block 0's es
+    if (__any_sync(0xffffffffu, nz) && lane == 0) {
+        asm volatile("st.shared.b32 [%0], %1;" ::"r"(sbase + kOffXc + slot * 32u),
+                     "r"(((uint32_t)(263 - es) << 23) | 0x80000000u)
+                     : "memory");
+        asm volatile("st.shared.b32 [%0], %1;" ::"r"(sbase + kOffXflag), "r"(1u) : "memory");
+    }
 }
 
 template <bool kCoherent, int XP, bool kSums = false>
@@ -506,6 +636,118 @@ __device__ __forceinline__ void build_x_table(uint32_t sbase, const void* x, int
         for (int j = 0; j < 4; ++j)
             if (c0 + j * stride < nch) table_chunk<XP, kSums>(sbase, c0 + j * stride + lane, lane, xa[j], xb[j]);
     }
+}
+
+// The row's weight at element k (0..255) of a unit, exact in fp32, from the
+// row's 144 raw bytes b[]: Q4_0 d_j (c - 8) (block j = k / 32, code k % 32 of
+// its 16 bytes: low nibbles first); Q4_K d sc_j q, the part the pieces
+// multiply (its min term dmin m_j is applied to the exact sum of x).
+template <int FMT>
+__device__ __forceinline__ float unit_weight(const uint8_t* b, int k) {
+    if constexpr (FMT == kFmtQ4) {
+        const uint8_t* blk = b + 18 * (k >> 5);
+        const int e = k & 31;
+        const uint32_t byte = blk[2 + (e & 15)];
+        const int code = (int)((e < 16) ? (byte & 15u) : (byte >> 4));
+        return half_bits_to_float((uint32_t)blk[0] | ((uint32_t)blk[1] << 8)) * (float)(code - 8);
+    } else {
+        const int j = k >> 5;
+        const uint32_t byte = b[16 + 32 * (k >> 6) + (k & 31)];
+        const uint32_t q = (j & 1) ? (byte >> 4) : (byte & 15u);
+        const uint32_t sc = j < 4 ? (b[4 + j] & 63u) : ((b[4 + j + 4] & 15u) | ((uint32_t)(b[4 + j - 4] >> 6) << 4));
+        return half_bits_to_float((uint32_t)b[0] | ((uint32_t)b[1] << 8)) * (float)sc * (float)q;
+    }
+}
+
+// 8-bit form, one unit of one row: its term of the read-back's error check.
+// With t_j the computed scaled dot of block j (what the read-back adds) and
+// R_j the table's sum of |x_k - pieces_k| over block j, E = sum_j Wmax_j R_j
+// bounds what the pieces miss (Wmax_j: the block's largest |weight|, 8 |d_j|
+// for Q4_0, 15 |d sc_j| for Q4_K), and L = sum_j |t_j| - E is a lower bound
+// of the row's sum |w x| over the unit (|t_j| <= sum_k |w_k x_k| + the
+// block's error).  The term is q = E (1 + eps) - eps sum_j |t_j|: a segment of
+// units whose terms sum to at most 0 has E <= eps L, so its error is at most
+// eps of its sum |w x|.  The table holds a_j = (1 + eps) Wmax_j R_j per unit
+// of the block scale (|d_j| for Q4_0, |d sc_j| for Q4_K), so q = sum_j
+// scale_j (a_j - eps c_j |D_j|) with D_j the block's two columns combined.
+template <int FMT>
+__device__ __forceinline__ float unit_check_term(const uint32_t (&dv)[16], const uint32_t (&dd)[4], const float (&c)[8],
+                                                 const float (&a)[8]) {
+    float q = 0.f;
+    if constexpr (FMT == kFmtQ4) {
+#pragma unroll
+        for (int p = 0; p < 4; ++p) {
+            const float2 d = half2_to_float2(dd[p]);
+            const float D0 = fmaf(__uint_as_float(dv[4 * p + 1]), 0.0625f, __uint_as_float(dv[4 * p]));
+            const float D1 = fmaf(__uint_as_float(dv[4 * p + 3]), 0.0625f, __uint_as_float(dv[4 * p + 2]));
+            q = fmaf(fabsf(d.x), fmaf(-kPieceEps * fabsf(c[2 * p]), fabsf(D0), a[2 * p]), q);
+            q = fmaf(fabsf(d.y), fmaf(-kPieceEps * c[2 * p + 1], fabsf(D1), a[2 * p + 1]), q);
+        }
+    } else {
+        const float dq = fabsf(half2_to_float2(dd[0]).x);
+        const uint32_t s03 = dd[1], s8b = dd[3];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            uint32_t sc;
+            if (j < 4) {
+                sc = (s03 >> (8 * j)) & 63u;
+            } else {
+                const uint32_t lo = (s8b >> (8 * (j - 4))) & 0xFFu;
+                sc = (lo & 15u) | (((s03 >> (8 * (j - 4) + 6)) & 3u) << 4);
+            }
+            const float D = fmaf(__uint_as_float(dv[2 * j + 1]), 0.0625f, __uint_as_float(dv[2 * j]));
+            q = fmaf(dq * (float)sc, fmaf(-kPieceEps * fabsf(c[j]), fabsf(D), a[j]), q);
+        }
+    }
+    return q;
+}
+
+// Whether table slot sl's group has a flag (its read-back factor c_0 < 0).
+__device__ __forceinline__ bool group_flagged(uint32_t sbase, int sl) {
+    return (lds32(sbase + kOffXc + (uint32_t)sl * 32u) >> 31) != 0u;
+}
+
+// The check itself, over a segment of a row's units: the segment needs its
+// residuals added exactly when the sum of its units' check terms is above 0,
+// i.e. when the pieces may miss more than eps of the segment's sum |w x|.
+__device__ __forceinline__ bool segment_needs_correction(float q) { return q > 0.f; }
+
+// The exact sum of w_k r_k over a unit's 256 elements, r_k = x_k minus what
+// its pieces carry, formed again from x (group g, elements 256 g ..
+// 256 g + 255; block scales from table slot sl) and the row's raw bytes read
+// from global memory at wrow (16-byte aligned; the stage holding them has
+// long been released).  For the segments the read-back check flags; slow, and
+// exact up to fp32 rounding.
+template <int FMT, int XP, bool kCoherent>
+__device__ __noinline__ float unit_correction(const uint8_t* wrow, const void* x, int g, uint32_t sbase, int sl) {
+    uint8_t b[144];
+#pragma unroll
+    for (int j = 0; j < 9; ++j)
+        *reinterpret_cast<uint4*>(b + 16 * j) = __ldg(reinterpret_cast<const uint4*>(wrow) + j);
+    float corr = 0.f;
+    for (int k = 0; k < kGroupK; ++k) {
+        const uint32_t cb = lds32(sbase + kOffXc + (uint32_t)sl * 32u + (uint32_t)(k >> 5) * 4u);
+        const int es = 263 - (int)((cb >> 23) & 0xFFu);
+        const float sc = __uint_as_float((uint32_t)es << 23), inv_sc = __uint_as_float((uint32_t)(254 - es) << 23);
+        const size_t i = (size_t)g * kGroupK + (size_t)k;
+        float xv;
+        if constexpr (XP == 2) {
+            unsigned short h;
+            if constexpr (kCoherent)
+                asm volatile("ld.global.cg.u16 %0, [%1];" : "=h"(h) : "l"(static_cast<const uint16_t*>(x) + i) : "memory");
+            else
+                h = __ldg(static_cast<const unsigned short*>(x) + i);
+            xv = __uint_as_float((uint32_t)h << 16);
+        } else {
+            if constexpr (kCoherent)
+                asm volatile("ld.global.cg.f32 %0, [%1];" : "=f"(xv) : "l"(static_cast<const float*>(x) + i) : "memory");
+            else
+                xv = __ldg(static_cast<const float*>(x) + i);
+        }
+        const float r = piece_residual<XP>(xv * sc) * inv_sc;
+        if (r != 0.f) corr = fmaf(unit_weight<FMT>(b, k), r, corr);
+    }
+    return corr;
 }
 
 }  // namespace qtc
