@@ -82,6 +82,10 @@ def _declare(L):
     L.oracle_q4k_split_scale.argtypes = [P, P, ctypes.c_int, i64, i64, P]
     L.oracle_q4k_scale_min.restype = None
     L.oracle_q4k_scale_min.argtypes = [P, ctypes.c_int, P, P]
+    L.oracle_mixbit_dequant.restype = ctypes.c_int
+    L.oracle_mixbit_dequant.argtypes = [ctypes.c_int, P, P, P, i64, i64, i64, P]
+    L.oracle_qmv_mixbit.restype = ctypes.c_int
+    L.oracle_qmv_mixbit.argtypes = [ctypes.c_int, P, P, P, i64, P, ctypes.c_int, i64, i64, P, P, P]
 
 
 def _ptr(a: np.ndarray):
@@ -214,3 +218,32 @@ def q4k_scale_min(scale_bytes, j: int):
     m = ctypes.c_int()
     lib().oracle_q4k_scale_min(_ptr(sb), j, ctypes.byref(sc), ctypes.byref(m))
     return sc.value, m.value
+
+
+# ---------------------------------------------------------------- mixed-bit
+
+def _mixbit_arrays(bits, qp, sc, bi):
+    qp = np.ascontiguousarray(qp, dtype=np.uint32)
+    sc = np.ascontiguousarray(sc, dtype=np.uint16)
+    bi = np.ascontiguousarray(bi if bi is not None else np.zeros(1, np.uint16), dtype=np.uint16)
+    return qp, sc, bi
+
+
+def mixbit_dequant(bits: int, qp, sc, bi, group: int, N: int, K: int) -> np.ndarray:
+    """W[n, k] as fp32 (the exact weight rounded once) for a mixed-bit matrix:
+    words qp (uint32), fp16 scale bits sc and bias bits bi (int4 only)."""
+    qp, sc, bi = _mixbit_arrays(bits, qp, sc, bi)
+    out = np.empty((N, K), dtype=np.float32)
+    _check(lib().oracle_mixbit_dequant(bits, _ptr(qp), _ptr(sc), _ptr(bi), group, N, K, _ptr(out)),
+           "mixbit_dequant")
+    return out
+
+
+def qmv_mixbit(bits: int, qp, sc, bi, group: int, x: np.ndarray, N: int, K: int):
+    """Returns (y, S, S2) in fp64: y = W x, S = sum |w x|, S2 the split's scale."""
+    qp, sc, bi = _mixbit_arrays(bits, qp, sc, bi)
+    x, xt = _act(x)
+    y, S, S2 = (np.empty(N, dtype=np.float64) for _ in range(3))
+    _check(lib().oracle_qmv_mixbit(bits, _ptr(qp), _ptr(sc), _ptr(bi), group, _ptr(x), xt, N, K,
+                                   _ptr(y), _ptr(S), _ptr(S2)), "qmv_mixbit")
+    return y, S, S2

@@ -34,6 +34,10 @@
  *    of GELU (SafeC Gemma 4 design notes, "Gated FFN").
  *  - Small-M product Y = X W^T for a few token rows (gem architecture,
  *    "Ownership boundaries": prompt tiles up to 32 tokens).
+ *  - Mixed-bit matrices (int2-symmetric, int4-affine, int8) of a QAT
+ *    checkpoint's hand-written decode loop (Core AI model zoo, Gemma-4-E2B
+ *    raw-Metal port, "What shipped"); their layout is described above
+ *    mixbit_field.
  *
  * Error scale: next to every output the oracle also returns
  * S = sum_k |w_k * x_k| (fp64), the scale the parity tolerances use.
@@ -376,6 +380,102 @@ int oracle_q4k_split_scale(const uint8_t *w, const void *x, int xdtype,
             }
         }
         S2[n] = s2;
+    }
+    free(xd);
+    return 0;
+}
+
+/* ------------------------------------------------------- mixed-bit formats */
+
+/* The mixed-bit matrices of a QAT checkpoint driven by hand-written
+ * matrix-vector kernels (Core AI model zoo, Gemma-4-E2B raw-Metal port, "What
+ * shipped" and "Architecture": int2-symmetric, int4-affine and int8 matvecs
+ * over quantized words qp, scales sc and biases bi).  The page gives no byte
+ * layout; this oracle reads the one the library documents:
+ *  - qp: 32-bit little-endian words, row after row; weight k of a row holds
+ *    bits [(k * b) % 32, (k * b) % 32 + b) of word (k * b) / 32 of that row
+ *    (b = 2, 4 or 8 bits, lowest bits first);
+ *  - sc, bi: IEEE binary16, one per group of G consecutive weights of a row,
+ *    [N][K / G] row-major;
+ *  - b = 2: q = the two's-complement value of the field (-2 .. 1), w = sc * q;
+ *    b = 4: c = the unsigned field (0 .. 15), w = sc * c + bi;
+ *    b = 8: q = the two's-complement byte (-128 .. 127), w = sc * q. */
+static int mixbit_field(const uint32_t *row, int bits, int64_t k)
+{
+    int64_t bit = k * bits;
+    uint32_t word = row[bit / 32];
+    int v = (int)((word >> (bit % 32)) & ((1u << bits) - 1u));
+    if (bits != 4 && v >= (1 << (bits - 1)))
+        v -= 1 << bits;                        /* two's complement */
+    return v;
+}
+
+/* The exact weight of row n, input k (fp64). */
+static double mixbit_weight(int bits, const uint32_t *qp, const uint16_t *sc, const uint16_t *bi,
+                            int64_t group, int64_t K, int64_t n, int64_t k)
+{
+    const uint32_t *row = qp + n * (K * bits / 32);
+    int64_t g = n * (K / group) + k / group;
+    double s = oracle_fp16_to_f64(sc[g]);
+    double v = s * (double)mixbit_field(row, bits, k);
+    if (bits == 4)
+        v += oracle_fp16_to_f64(bi[g]);
+    return v;
+}
+
+static int mixbit_shape_ok(int bits, int64_t group, int64_t K)
+{
+    if (bits != 2 && bits != 4 && bits != 8)
+        return 0;
+    if (K <= 0 || group <= 0 || K % group || (K * bits) % 32)
+        return 0;
+    return 1;
+}
+
+/* Dequantize to fp32: the exact weight (fp64) rounded to float once. */
+int oracle_mixbit_dequant(int bits, const uint32_t *qp, const uint16_t *sc, const uint16_t *bi,
+                          int64_t group, int64_t N, int64_t K, float *out)
+{
+    if (!mixbit_shape_ok(bits, group, K))
+        return -1;
+    for (int64_t n = 0; n < N; n++)
+        for (int64_t k = 0; k < K; k++)
+            out[n * K + k] = (float)mixbit_weight(bits, qp, sc, bi, group, K, n, k);
+    return 0;
+}
+
+/* y[n] = sum_k w[n,k] x[k] in fp64, k ascending; S[n] = sum_k |w x|; and
+ * S2[n] = sum_k (|sc q| + |bi|) |x|, the scale of the affine split
+ * sc * sum(c x) + bi * sum(x), whose two sums are formed apart (S2 = S for
+ * the symmetric formats, which have no bias). */
+int oracle_qmv_mixbit(int bits, const uint32_t *qp, const uint16_t *sc, const uint16_t *bi,
+                      int64_t group, const void *x, int xdtype, int64_t N, int64_t K,
+                      double *y, double *S, double *S2)
+{
+    if (!mixbit_shape_ok(bits, group, K))
+        return -1;
+    double *xd = widen_activations(x, xdtype, K);
+    if (!xd)
+        return -2;
+    for (int64_t n = 0; n < N; n++) {
+        double acc = 0.0, sabs = 0.0, s2 = 0.0;
+        const uint32_t *row = qp + n * (K * bits / 32);
+        for (int64_t k = 0; k < K; k++) {
+            double w = mixbit_weight(bits, qp, sc, bi, group, K, n, k);
+            double p = w * xd[k];
+            acc += p;
+            sabs += fabs(p);
+            int64_t g = n * (K / group) + k / group;
+            double t = fabs(oracle_fp16_to_f64(sc[g]) * (double)mixbit_field(row, bits, k));
+            if (bits == 4)
+                t += fabs(oracle_fp16_to_f64(bi[g]));
+            s2 += t * fabs(xd[k]);
+        }
+        y[n] = acc;
+        if (S)
+            S[n] = sabs;
+        if (S2)
+            S2[n] = s2;
     }
     free(xd);
     return 0;

@@ -213,3 +213,48 @@ def random_with_scale_bits(fmt: str, N: int, K: int, seed: int, d_pool: np.ndarr
         return _assemble(d, q.view(np.uint8), Q8_0_BLOCK_BYTES)
     qs = g.integers(0, 256, size=nb * 16, dtype=np.uint8)
     return _assemble(d, qs, Q4_0_BLOCK_BYTES)
+
+
+# ------------------------------------------------------------ mixed-bit formats
+# Quantized words qp (uint32), fp16 scales sc and (4-bit affine only) fp16
+# biases bi, one scale/bias per group of `group` weights of a row.  Field k of
+# a row occupies bits (k * b) % 32 .. of word (k * b) // 32 of that row,
+# lowest bits first.  The generator draws raw field values uniformly over all
+# 2^b patterns.
+
+MIXBIT_BITS = (2, 4, 8)
+
+
+def pack_fields(fields: np.ndarray, bits: int) -> np.ndarray:
+    """Pack a [N, K] array of raw b-bit field values (0 .. 2^b - 1) into uint32
+    words, row after row, lowest bits first."""
+    f = np.asarray(fields, dtype=np.uint32)
+    N, K = f.shape
+    per = 32 // bits
+    f = f.reshape(N, K // per, per)
+    shifts = (np.arange(per, dtype=np.uint32) * bits)
+    return np.bitwise_or.reduce(f << shifts, axis=2).astype(np.uint32).reshape(-1)
+
+
+def mixbit_weights(bits: int, N: int, K: int, group: int, seed: int, stream: int = 0, layer: int = 0):
+    """Random mixed-bit matrix: (qp words, sc bits, bi bits or None).  Scales are
+    fp16(|N(0, 0.02)| / r) with r = 2, 8, 127 for 2, 4 and 8 bits; 4-bit biases
+    are fp16(-z * scale) with z uniform in [6, 9] (a zero point near the middle
+    of the code range)."""
+    if bits not in MIXBIT_BITS or K % group or (K * bits) % 32:
+        raise ValueError("unsupported mixed-bit shape")
+    g = rng(seed, stream, layer)
+    ng = N * (K // group)
+    r = {2: 2.0, 4: 8.0, 8: 127.0}[bits]
+    sc = (np.abs(g.standard_normal(ng)) * 0.02 / r).astype(np.float16)
+    fields = g.integers(0, 1 << bits, size=(N, K), dtype=np.uint32)
+    bi = None
+    if bits == 4:
+        z = g.uniform(6.0, 9.0, ng)
+        bi = (-z * sc.astype(np.float64)).astype(np.float16).view(np.uint16)
+    return pack_fields(fields, bits), sc.view(np.uint16), bi
+
+
+def mixbit_bytes(bits: int, N: int, K: int, group: int) -> int:
+    """Bytes of a mixed-bit matrix: words, scales and (4-bit) biases."""
+    return N * K * bits // 8 + N * (K // group) * 2 * (2 if bits == 4 else 1)

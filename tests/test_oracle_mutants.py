@@ -30,7 +30,8 @@ MUTANTS = {
     "fp16_implicit_bit_dropped": ("v = ldexp((double)(1024 + m), e - 25);", "v = ldexp((double)(m), e - 25);"),
     "bf16_bias_off_by_one": ("v = ldexp((double)(128 + m), e - 134);", "v = ldexp((double)(128 + m), e - 133);"),
     "round_ties_away": ("(frac == 0.5 && fmod(fl, 2.0) != 0.0)", "(frac == 0.5)"),
-    "abs_dropped_from_scale": ("sabs += fabs(p);", "sabs += p;"),
+    "abs_dropped_from_scale": ("                sabs += fabs(p);", "                sabs += p;"),
+    "mixbit_abs_dropped_from_scale": ("            sabs += fabs(p);\n            int64_t g", "            sabs += p;\n            int64_t g"),
     "first_block_skipped": ("for (int64_t b = 0; b < nb; b++) {\n            decode_block(fmt, w + (n * nb + b) * "
                             "block_size(fmt), wb);\n            for (int k = 0; k < be; k++) {\n                double p",
                             "for (int64_t b = 1; b < nb; b++) {\n            decode_block(fmt, w + (n * nb + b) * "
@@ -63,6 +64,20 @@ MUTANTS = {
     "q4k_split_min_doubled": ("fabs(dmin * (double)m);\n                s2 +=", "fabs(2.0 * dmin * (double)m);\n                s2 +="),
     "q4k_split_min_dropped": ("double t = fabs(d * (double)sc * (double)q4k_code(blk + 16, e)) + fabs(dmin * (double)m);",
                               "double t = fabs(d * (double)sc * (double)q4k_code(blk + 16, e));"),
+    "mixbit_fields_msb_first": ("int v = (int)((word >> (bit % 32)) & ((1u << bits) - 1u));",
+                                "int v = (int)((word >> (32 - bits - bit % 32)) & ((1u << bits) - 1u));"),
+    "mixbit_int2_unsigned": ("if (bits != 4 && v >= (1 << (bits - 1)))", "if (bits == 8 && v >= (1 << (bits - 1)))"),
+    "mixbit_int8_unsigned": ("if (bits != 4 && v >= (1 << (bits - 1)))", "if (bits == 2 && v >= (1 << (bits - 1)))"),
+    "mixbit_int4_signed": ("if (bits != 4 && v >= (1 << (bits - 1)))", "if (v >= (1 << (bits - 1)))"),
+    "mixbit_bias_dropped": ("    if (bits == 4)\n        v += oracle_fp16_to_f64(bi[g]);",
+                            "    if (bits == 4)\n        v += 0.0;"),
+    "mixbit_bias_sign": ("    if (bits == 4)\n        v += oracle_fp16_to_f64(bi[g]);",
+                         "    if (bits == 4)\n        v -= oracle_fp16_to_f64(bi[g]);"),
+    "mixbit_group_without_row": ("const uint32_t *row = qp + n * (K * bits / 32);\n    int64_t g = n * (K / group) + k / group;",
+                                 "const uint32_t *row = qp + n * (K * bits / 32);\n    int64_t g = k / group;"),
+    "mixbit_row_stride": ("const uint32_t *row = qp + n * (K * bits / 32);\n    int64_t g",
+                          "const uint32_t *row = qp + n * (K / 32);\n    int64_t g"),
+    "mixbit_split_bias_dropped": ("t += fabs(oracle_fp16_to_f64(bi[g]));", "t += 0.0;"),
 }
 
 
@@ -81,6 +96,7 @@ def test_pins_catch_mutant(name, tmp_path):
     r = subprocess.run([sys.executable, "-m", "pytest", "-x", "-q", "-p", "no:cacheprovider",
                         os.path.join(ROOT, "tests", "test_oracle_scalars.py"),
                         os.path.join(ROOT, "tests", "test_oracle_products.py"),
-                        os.path.join(ROOT, "tests", "test_oracle_q4k.py")],
+                        os.path.join(ROOT, "tests", "test_oracle_q4k.py"),
+                        os.path.join(ROOT, "tests", "test_oracle_mixbit.py")],
                        cwd=ROOT, env=env, capture_output=True, text=True, timeout=600)
     assert r.returncode != 0, f"mutant {name} survived the pins:\n{r.stdout[-2000:]}"
