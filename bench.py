@@ -406,6 +406,40 @@ def supplementary_kernels(torch, qbw, hbm_peak):
     run("qmv_q4_k 21504x5376 bf16->f32", w.numel() + 2 * K + 4 * N, copies,
         lambda i: (lambda: qbw.qmv_q4_k(ws[i], xk, y, 1, N, K)))
     del ws, w
+    # the down projection 5376 x 21504 (Q4_0, bf16 -> bf16) on a GELU(g) * u
+    # activation with g, u ~ N(0, 6.6^2), the spread the sweep's first layer
+    # produces: most of its elements sit far below their block's largest, so
+    # the 8-bit form's error check runs on every unit
+    N, K = 5376, 21504
+    w = torch.from_numpy(synth.q4_0_weights(N, K, seed=20)).to(dev)
+    copies = max(2, int(np.ceil(2.2 * l2 / w.numel())))
+    ws = [w.clone() for _ in range(copies)]
+    grng = np.random.default_rng(5)
+    gg, uu = grng.standard_normal(K) * 6.6, grng.standard_normal(K) * 6.6
+    act = 0.5 * gg * (1.0 + np.tanh(np.sqrt(2.0 / np.pi) * (gg + 0.044715 * gg ** 3))) * uu
+    xg = bf16(synth.f32_to_bf16_bits(act.astype(np.float32)))
+    xn = bf16(synth.activations(K, seed=20, dtype="bf16"))
+    yb = torch.empty(N, dtype=torch.bfloat16, device=dev)
+    run("qmv_q4_0 5376x21504 bf16->bf16 N(0,1) x", w.numel() + 2 * K + 2 * N, copies,
+        lambda i: (lambda: qbw.qmv_q4_0(ws[i], xn, yb, 1, N, K)))
+    run("qmv_q4_0 5376x21504 bf16->bf16 GELU(g)*u x", w.numel() + 2 * K + 2 * N, copies,
+        lambda i: (lambda: qbw.qmv_q4_0(ws[i], xg, yb, 1, N, K)))
+    del ws, w
+    # the mixed-bit formats (int2-symmetric, int4-affine, int8), 21504 x 5376,
+    # groups of 32, bf16 -> fp32
+    N, K, G = 21504, 5376, 32
+    xm = bf16(synth.activations(K, seed=9, dtype="bf16"))
+    y = torch.empty(N, device=dev)
+    for bits in (2, 4, 8):
+        qp, sc, bi = synth.mixbit_weights(bits, N, K, G, seed=9)
+        nbytes = synth.mixbit_bytes(bits, N, K, G)
+        copies = max(2, int(np.ceil(2.2 * l2 / nbytes)))
+        mats = [(torch.from_numpy(qp.view(np.uint8).copy()).to(dev), torch.from_numpy(sc.view(np.uint8).copy()).to(dev),
+                 torch.from_numpy(bi.view(np.uint8).copy()).to(dev) if bi is not None else None) for _ in range(copies)]
+        name = {2: "int2-symmetric", 4: "int4-affine", 8: "int8"}[bits]
+        run(f"qmv_mixbit {name} {N}x{K} G={G} bf16->f32", nbytes + 2 * K + 4 * N, copies,
+            lambda i, mats=mats, bits=bits: (lambda: qbw.qmv_mixbit(bits, *mats[i], G, xm, y, 1, N, K)))
+        del mats
     # small-M tiles
     for (N, K) in ((5376, 5376), (5376, 21504)):
         w = torch.from_numpy(synth.q4_0_weights(N, K, seed=3)).to(dev)

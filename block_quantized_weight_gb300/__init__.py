@@ -78,6 +78,10 @@ def _declare(L):
     for name in ("qdequant_q8_0", "qdequant_q4_0", "qdequant_q4_k"):
         getattr(L, name).restype = i32
         getattr(L, name).argtypes = [P, P, i64, i64, P]
+    L.qmv_mixbit.restype = i32
+    L.qmv_mixbit.argtypes = [i32, P, P, P, i64, P, i32, P, i32, i64, i64, i64, P]
+    L.qdequant_mixbit.restype = i32
+    L.qdequant_mixbit.argtypes = [i32, P, P, P, i64, P, i64, i64, P]
     L.qbw_fault_read.restype = i32
     L.qbw_fault_read.argtypes = [ctypes.POINTER(ctypes.c_uint32), i32, P]
     L.qbw_selftest_wait.restype = i32
@@ -152,6 +156,25 @@ def qmv_q4_k(w, x, y, M: int, N: int, K: int, stream=None):
     _check(L.qmv_q4_k(_ptr(w), _ptr(x), _dtype_code(x), _ptr(y), _dtype_code(y), M, N, K, _stream(stream)),
            "qmv_q4_k")
     return y
+
+
+def qmv_mixbit(bits: int, qp, sc, bi, group: int, x, y, M: int, N: int, K: int, stream=None):
+    """y = W x for a mixed-bit matrix: ``bits`` 2 (int2-symmetric), 4
+    (int4-affine, ``bi`` required) or 8 (int8); words ``qp``, fp16 scale bits
+    ``sc`` and bias bits ``bi`` (device tensors), one scale per ``group``
+    weights of a row."""
+    L = load()
+    _check(L.qmv_mixbit(bits, _ptr(qp), _ptr(sc), _ptr(bi) if bi is not None else None, group, _ptr(x),
+                        _dtype_code(x), _ptr(y), _dtype_code(y), M, N, K, _stream(stream)), "qmv_mixbit")
+    return y
+
+
+def qdequant_mixbit(bits: int, qp, sc, bi, group: int, out, N: int, K: int, stream=None):
+    """out[n, k] = w[n, k] (fp32) for a mixed-bit matrix (test-only)."""
+    L = load()
+    _check(L.qdequant_mixbit(bits, _ptr(qp), _ptr(sc), _ptr(bi) if bi is not None else None, group, _ptr(out),
+                             N, K, _stream(stream)), "qdequant_mixbit")
+    return out
 
 
 def qmv_gateup_q4_0(w_gate, w_up, x, out, M: int, N: int, K: int, stream=None):

@@ -580,6 +580,59 @@ qbw_status qdequant_q8_0(const void* w, float* out, int64_t N, int64_t K, void* 
     return dequant_common(kFmtQ8, w, out, N, K, stream);
 }
 
+// Shared argument checks of the mixed-bit entry points: kind (2, 4, 8 bits),
+// group G (a multiple of 16 dividing K), K (rows of whole 16-byte word groups,
+// at most what the staged activations allow), pointers and alignment.
+static qbw_status mixbit_args(qbw_mixbit kind, const void* qp, const void* sc, const void* bi, int64_t group,
+                              int64_t N, int64_t K, size_t* wbytes) {
+    const int bits = (int)kind;
+    if (bits != 2 && bits != 4 && bits != 8) return QBW_EINVAL;
+    if (!qp || !sc || (bits == 4 && !bi)) return QBW_EINVAL;
+    if (N < 1 || N > INT32_MAX || K < 16 || K > (int64_t(1) << 24)) return QBW_ESHAPE;
+    if (group < 16 || group % 16 != 0 || K % group != 0 || (K * bits) % 128 != 0) return QBW_ESHAPE;
+    if ((uintptr_t)qp % 16 || (uintptr_t)sc % 4 || (bits == 4 && (uintptr_t)bi % 4)) return QBW_EALIGN;
+    *wbytes = (size_t)N * (size_t)K * bits / 8;
+    return QBW_OK;
+}
+
+qbw_status qmv_mixbit(qbw_mixbit kind, const void* qp, const void* sc, const void* bi, int64_t group, const void* x,
+                      qbw_dtype xt, void* y, qbw_dtype yt, int64_t M, int64_t N, int64_t K, void* stream) {
+    size_t wbytes = 0;
+    qbw_status st = mixbit_args(kind, qp, sc, bi, group, N, K, &wbytes);
+    if (st != QBW_OK) return st;
+    if (!x || !y) return QBW_EINVAL;
+    if (!valid_dtype(xt) || !valid_dtype(yt)) return QBW_EDTYPE;
+    if (M != 1) return QBW_ESHAPE;
+    if (qmv_mixbit_smem_bytes((int)kind, K, group) > kMixMaxSmem) return QBW_ESHAPE;
+    if ((uintptr_t)x % 16 || (uintptr_t)y % dtype_size(yt)) return QBW_EALIGN;
+    const size_t ybytes = (size_t)N * dtype_size(yt), sbytes = (size_t)N * (size_t)(K / group) * 2;
+    if (overlaps(y, ybytes, x, (size_t)K * dtype_size(xt)) || overlaps(y, ybytes, qp, wbytes) ||
+        overlaps(y, ybytes, sc, sbytes) || (kind == QBW_MIXBIT_INT4_AFFINE && overlaps(y, ybytes, bi, sbytes)))
+        return QBW_EINVAL;
+    DeviceInfo* di = nullptr;
+    st = device_info(&di);
+    if (st != QBW_OK) return st;
+    cudaError_t e = launch_qmv_mixbit((int)kind, qp, sc, bi, (int)group, x, xt == QBW_BF16, y, yt == QBW_BF16, (int)N,
+                                      (int)K, di->sm_count, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? QBW_OK : QBW_ECUDA;
+}
+
+qbw_status qdequant_mixbit(qbw_mixbit kind, const void* qp, const void* sc, const void* bi, int64_t group, float* out,
+                           int64_t N, int64_t K, void* stream) {
+    size_t wbytes = 0;
+    qbw_status st = mixbit_args(kind, qp, sc, bi, group, N, K, &wbytes);
+    if (st != QBW_OK) return st;
+    if (!out) return QBW_EINVAL;
+    if ((uintptr_t)out % 4) return QBW_EALIGN;
+    if (overlaps(out, (size_t)N * K * 4, qp, wbytes)) return QBW_EINVAL;
+    DeviceInfo* di = nullptr;
+    st = device_info(&di);
+    if (st != QBW_OK) return st;
+    cudaError_t e = launch_dequant_mixbit((int)kind, qp, sc, bi, (int)group, out, (int)N, (int)K, di->sm_count,
+                                          static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? QBW_OK : QBW_ECUDA;
+}
+
 qbw_status qbw_selftest_wait(int which, uint32_t limit_us, void* stream) {
     if (which < 0 || which > 1 || limit_us < 1 || limit_us > 2000000) return QBW_EINVAL;
     DeviceInfo* di = nullptr;

@@ -85,6 +85,16 @@ cudaError_t launch_dequant(int fmt, const uint8_t* w, float* out, int64_t N, int
 cudaError_t launch_embed(int fmt, const uint8_t* w, const int32_t* ids, int64_t n_ids, int64_t N, int64_t K, void* out,
                          int out_bf16, unsigned int* fault, int sm_count, cudaStream_t stream);
 
+// qmv_mixbit.cu: the mixed-bit (2-, 4-, 8-bit) matrix-vector product and its
+// dequantizer.  x is staged in shared memory beside the warps' copy rings:
+// qmv_mixbit_smem_bytes(bits, K, group) must not exceed kMixMaxSmem.
+constexpr size_t kMixMaxSmem = 227 * 1024;
+size_t qmv_mixbit_smem_bytes(int bits, int64_t K, int64_t group);
+cudaError_t launch_qmv_mixbit(int bits, const void* qp, const void* sc, const void* bi, int G, const void* x,
+                              int x_bf16, void* y, int y_bf16, int N, int K, int sm_count, cudaStream_t stream);
+cudaError_t launch_dequant_mixbit(int bits, const void* qp, const void* sc, const void* bi, int G, float* out, int N,
+                                  int K, int sm_count, cudaStream_t stream);
+
 // qmm_noalloc.cu: the next qmm_q4_0_smallM_noalloc call on `device` zero-fills
 // its static scratch again (called when qbw_fault_read finds a fault).
 void noalloc_scratch_mark_dirty(int device);

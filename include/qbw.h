@@ -277,6 +277,57 @@ qbw_status qmv_q4_k(const void *w, const void *x, qbw_dtype xt, void *y, qbw_dty
 qbw_status qdequant_q4_k(const void *w, float *out, int64_t N, int64_t K, void *stream);
 
 /*
+ * Mixed-bit matrices -- int2-symmetric, int4-affine and int8 weights as a QAT
+ * checkpoint ships them for hand-written decode kernels (Core AI model zoo,
+ * Gemma-4-E2B raw-Metal port, "What shipped" and "Architecture": mixed-bit
+ * matvecs over quantized words qp, scales sc and biases bi).  The page gives
+ * no byte layout; this library reads the following one.
+ *
+ *   qp : N rows of K * b / 32 little-endian 32-bit words, rows back to back;
+ *        weight k of a row is bits [(k b) % 32, (k b) % 32 + b) of word
+ *        (k b) / 32 of that row (b = 2, 4, 8; lowest bits first)
+ *   sc : fp16 scales, one per group of `group` consecutive weights of a row,
+ *        [N][K / group] row-major
+ *   bi : fp16 biases, same shape as sc (int4-affine only; ignored otherwise)
+ *   QBW_MIXBIT_INT2_SYM    : q = the field as a two's-complement 2-bit value
+ *                            (-2 .. 1), w = sc q
+ *   QBW_MIXBIT_INT4_AFFINE : c = the field as unsigned (0 .. 15), w = sc c + bi
+ *   QBW_MIXBIT_INT8_SYM    : q = the field as a two's-complement byte, w = sc q
+ *
+ * Ranges: group a multiple of 16 dividing K; K * b a multiple of 128 (rows of
+ * whole 16-byte word groups: K % 64 for 2 bits, % 32 for 4, % 16 for 8), else
+ * QBW_ESHAPE.  qp 16-byte aligned, sc and bi 4-byte aligned (QBW_EALIGN).
+ */
+typedef enum qbw_mixbit {
+    QBW_MIXBIT_INT2_SYM = 2,
+    QBW_MIXBIT_INT4_AFFINE = 4,
+    QBW_MIXBIT_INT8_SYM = 8
+} qbw_mixbit;
+
+/*
+ * qmv_mixbit -- y = W x for a mixed-bit matrix, one token (M == 1).  The int4
+ * form is summed as sc * sum(c x) + bi * sum(x) per group, so its rounding
+ * scales with sum (|sc c| + |bi|) |x|.
+ *
+ *   x : K activations of xt, 16-byte aligned;  y : N outputs of yt
+ *   M == 1; N >= 1; K as above, and small enough that the activations (4 K
+ *   bytes, 4.5 K for int4) and the copy rings (40 to 64 KB) fit one CTA's
+ *   shared memory (227 KB): K up to 37,000 in every format and group size,
+ *   else QBW_ESHAPE
+ */
+qbw_status qmv_mixbit(qbw_mixbit kind, const void *qp, const void *sc, const void *bi, int64_t group,
+                      const void *x, qbw_dtype xt, void *y, qbw_dtype yt, int64_t M, int64_t N, int64_t K,
+                      void *stream);
+
+/*
+ * qdequant_mixbit -- out[n*K + k] = w[n, k] in fp32 (sc q exactly; sc c + bi
+ * rounded once to nearest).  For testing.  Arguments as qmv_mixbit; out 4-byte
+ * aligned.
+ */
+qbw_status qdequant_mixbit(qbw_mixbit kind, const void *qp, const void *sc, const void *bi, int64_t group,
+                           float *out, int64_t N, int64_t K, void *stream);
+
+/*
  * qembed_q8_0 -- token-table lookup: out[i, :] = W[ids[i], :], dequantized.
  *
  * The embedding side of the Q8_0 token table that the decode loop reads once

@@ -32,7 +32,7 @@ def test_header_declares_the_entry_points():
     names = declared_functions()
     for n in ("qmv_q8_0", "qmv_q4_0", "qmv_gateup_q4_0", "qmm_q4_0_smallM", "qmm_q4_0_smallM_workspace_bytes",
               "qdequant_q8_0", "qdequant_q4_0", "qmv_q4_k", "qdequant_q4_k", "qbw_status_str", "qbw_version",
-              "qbw_fault_read"):
+              "qbw_fault_read", "qmv_mixbit", "qdequant_mixbit"):
         assert n in names
 
 
@@ -150,3 +150,23 @@ def test_chain_calls_reject_null_arguments_before_touching_a_device(lib):
     assert L.qbw_chain_create(None, 1, None) == 1
     assert L.qbw_chain_run(None, None) == 1
     assert L.qbw_chain_destroy(None) == 1
+
+
+def test_mixbit_validation(lib):
+    f = lib.qmv_mixbit
+    w, sc, bi, x, y = P(ADDR), P(ADDR + (1 << 28)), P(ADDR + (1 << 29)), P(ADDR + (1 << 30)), P(ADDR + (3 << 30))
+    assert f(3, w, sc, bi, 32, x, F32, y, F32, 1, 16, 256, None) == 1          # unknown kind
+    assert f(4, w, sc, None, 32, x, F32, y, F32, 1, 16, 256, None) == 1        # int4 needs biases
+    assert f(2, w, sc, None, 32, x, F32, y, F32, 1, 16, 96, None) == 2         # 96 * 2 bits: not whole word groups
+    assert f(8, w, sc, None, 24, x, F32, y, F32, 1, 16, 96, None) == 2         # group not a multiple of 16
+    assert f(8, w, sc, None, 64, x, F32, y, F32, 1, 16, 96, None) == 2         # 96 % 64
+    assert f(8, w, sc, None, 32, x, F32, y, F32, 2, 16, 256, None) == 2        # M != 1
+    assert f(8, w, sc, None, 64, x, F32, y, F32, 1, 16, 65536, None) == 2      # x does not fit shared memory
+    assert f(8, P(ADDR + 8), sc, None, 32, x, F32, y, F32, 1, 16, 256, None) == 4
+    assert f(8, w, sc, None, 32, P(ADDR + (1 << 30) + 4), F32, y, F32, 1, 16, 256, None) == 4
+    assert f(8, w, sc, None, 32, x, 7, y, F32, 1, 16, 256, None) == 3
+    assert f(8, w, sc, None, 32, x, F32, P(ADDR + 64), F32, 1, 16, 256, None) == 1    # y overlaps the words
+    g = lib.qdequant_mixbit
+    assert g(4, w, sc, None, 32, y, 16, 256, None) == 1
+    assert g(2, w, sc, None, 32, P(ADDR + (3 << 30) + 2), 16, 256, None) == 4
+    assert g(8, w, P(ADDR + (1 << 28) + 2), None, 32, y, 16, 256, None) == 4       # scales 4-byte aligned

@@ -1,0 +1,117 @@
+"""GPU parity of the mixed-bit matrices (int2-symmetric, int4-affine, int8)
+through the C ABI, against the CPU oracle on the same seeded words, scales and
+biases.
+
+* Dequantization is bit-exact: sc q is exact in fp32, and sc c + bi is rounded
+  once on both sides.
+* y = W x is compared element by element with the matvec rule on the split's
+  scale: |y - y_ref| <= 2e-3 S2 (+ the bf16 output rounding), S2 = sum (|sc q|
+  + |bi|) |x| (S2 = S for the symmetric formats; the int4 kernel forms
+  sc * sum(c x) and bi * sum(x) apart).
+Shapes cover one and two rows per warp item, ragged row counts, rows shorter
+than one pass of the warp, groups smaller and larger than a 16-byte word
+group, per-channel scales (group = K), and the 31B profile's 5376 x 21504 and
+21504 x 5376 shapes in full.
+"""
+import numpy as np
+import pytest
+
+import synth
+from tolerance import check_matvec, to_f64
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+
+
+def dev(a):
+    if a is None:
+        return None
+    return torch.from_numpy(np.ascontiguousarray(a).view(np.uint8).copy()).cuda()
+
+
+def dev_act(a):
+    if a.dtype == np.uint16:
+        return torch.from_numpy(a.view(np.int16).copy()).view(torch.bfloat16).cuda()
+    return torch.from_numpy(a.copy()).cuda()
+
+
+def run(qbw, bits, qp, sc, bi, G, x, N, K, odt=torch.float32):
+    y = torch.full((N,), float("nan"), dtype=odt, device="cuda")
+    qbw.qmv_mixbit(bits, dev(qp), dev(sc), dev(bi), G, dev_act(x), y, 1, N, K)
+    torch.cuda.synchronize()
+    assert qbw.fault_read(clear=True) == 0
+    return y
+
+
+SHAPES = [(1, 64, 32), (7, 128, 16), (2, 256, 256), (300, 2304, 32), (33, 1024, 64), (1000, 5376, 32),
+          (129, 4096, 128), (64, 512, 512)]
+
+
+@pytest.mark.parametrize("bits", [2, 4, 8])
+@pytest.mark.parametrize("N,K,G", SHAPES)
+def test_dequant_bit_exact(qbw, oracle, bits, N, K, G):
+    qp, sc, bi = synth.mixbit_weights(bits, N, K, G, seed=N + K + G + bits)
+    out = torch.empty(N, K, dtype=torch.float32, device="cuda")
+    qbw.qdequant_mixbit(bits, dev(qp), dev(sc), dev(bi), G, out, N, K)
+    torch.cuda.synchronize()
+    ref = oracle.mixbit_dequant(bits, qp, sc, bi, G, N, K)
+    assert np.array_equal(out.cpu().numpy().view(np.uint32), ref.view(np.uint32))
+
+
+@pytest.mark.parametrize("bits", [2, 4, 8])
+@pytest.mark.parametrize("N,K,G", SHAPES)
+@pytest.mark.parametrize("xdt,odt", [("f32", torch.float32), ("bf16", torch.bfloat16), ("bf16", torch.float32)])
+def test_qmv_small(qbw, oracle, bits, N, K, G, xdt, odt):
+    qp, sc, bi = synth.mixbit_weights(bits, N, K, G, seed=3 * N + K + bits)
+    x = synth.activations(K, seed=K + bits, dtype=xdt)
+    y = run(qbw, bits, qp, sc, bi, G, x, N, K, odt)
+    y_ref, _, S2 = oracle.qmv_mixbit(bits, qp, sc, bi, G, x, N, K)
+    check_matvec(to_f64(y), y_ref, S2, out_bf16=(odt == torch.bfloat16), what=f"mixbit{bits} N={N} K={K} G={G}")
+
+
+@pytest.mark.parametrize("bits", [2, 4, 8])
+@pytest.mark.parametrize("N,K", [(21504, 5376), (5376, 21504)])
+def test_qmv_full_size(qbw, oracle, bits, N, K):
+    # the 31B profile's FFN shapes, groups of 32, every row compared
+    qp, sc, bi = synth.mixbit_weights(bits, N, K, 32, seed=7 + bits)
+    x = synth.activations(K, seed=8, dtype="bf16")
+    y = run(qbw, bits, qp, sc, bi, 32, x, N, K)
+    y_ref, _, S2 = oracle.qmv_mixbit(bits, qp, sc, bi, 32, x, N, K)
+    check_matvec(to_f64(y), y_ref, S2, what=f"mixbit{bits} full {N}x{K}")
+
+
+@pytest.mark.parametrize("bits,field,value", [(2, 2, -2), (2, 1, 1), (4, 15, 15), (4, 0, 0), (8, 128, -128)])
+def test_constant_fields(qbw, oracle, bits, field, value):
+    # every field equal: y[n] = sum over groups of (sc value + bi) * sum(x over the group)
+    N, K, G = 130, 1024, 64
+    qp = synth.pack_fields(np.full((N, K), field, dtype=np.uint32), bits)
+    _, sc, bi = synth.mixbit_weights(bits, N, K, G, seed=field + 1)
+    x = synth.activations(K, seed=field + 2)
+    y = to_f64(run(qbw, bits, qp, sc, bi, G, x, N, K))
+    xs = x.astype(np.float64).reshape(K // G, G).sum(axis=1)
+    s = sc.view(np.float16).astype(np.float64).reshape(N, K // G)
+    wv = s * value + (bi.view(np.float16).astype(np.float64).reshape(N, K // G) if bits == 4 else 0.0)
+    ref = (wv * xs).sum(axis=1)
+    _, _, S2 = oracle.qmv_mixbit(bits, qp, sc, bi, G, x, N, K)
+    check_matvec(y, ref, S2, what=f"constant mixbit{bits}")
+
+
+def test_zero_scales_give_exact_zero(qbw):
+    N, K, G = 66, 512, 32
+    for bits in (2, 4, 8):
+        qp, sc, bi = synth.mixbit_weights(bits, N, K, G, seed=bits)
+        sc = np.zeros_like(sc)
+        bi = np.zeros_like(bi) if bi is not None else None
+        y = run(qbw, bits, qp, sc, bi, G, synth.activations(K, seed=1), N, K)
+        assert torch.all(y == 0)
+
+
+def test_deterministic(qbw):
+    N, K, G = 3000, 4096, 32
+    for bits in (2, 4, 8):
+        qp, sc, bi = synth.mixbit_weights(bits, N, K, G, seed=11)
+        x = synth.activations(K, seed=12, dtype="bf16")
+        a = run(qbw, bits, qp, sc, bi, G, x, N, K)
+        b = run(qbw, bits, qp, sc, bi, G, x, N, K)
+        assert torch.equal(a.view(torch.int32), b.view(torch.int32))
