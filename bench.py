@@ -486,24 +486,47 @@ def supplementary_kernels(torch, qbw, hbm_peak):
     return res
 
 
-def cpu_baseline(layer0_host, x_bits, budget_s):
+def host_cpu():
+    """The host's CPU model (lscpu, else /proc/cpuinfo) and the size of this
+    process's CPU affinity set."""
+    model = ""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.strip().startswith("Model name:"):
+                model = line.split(":", 1)[1].strip()
+                break
+    except Exception:
+        pass
+    if not model:
+        try:
+            for line in open("/proc/cpuinfo"):
+                if line.lower().startswith(("model name", "cpu part")):
+                    model = line.split(":", 1)[1].strip()
+                    break
+        except OSError:
+            pass
+    return model or "unknown", len(os.sched_getaffinity(0))
+
+
+def cpu_sweep_sample(layer0_host, x_bits, budget_s, threads):
     """The oracle, as it stands, on a bounded sample of the sweep: layer 0's
-    seven matrices in order, in chunks of 256 rows, repeated until
-    ``budget_s`` elapse."""
+    seven matrices in order, in chunks of rows, repeated until ``budget_s``
+    elapse; ``threads``: its OpenMP build over all cores."""
     import oracle
-    oracle.lib()
     rng = np.random.default_rng(0)
     xs = {name: (x_bits if name in ("q", "k", "v") else
                  synth.f32_to_bf16_bits(rng.standard_normal(K).astype(np.float32)))
           for name, N, K in MATRICES}
-    done_bytes, passes = 0, 0.0
+    chunk = 4096 if threads else 256
+    done_bytes = 0
     t0 = time.time()
     while time.time() - t0 < budget_s:
         for name, N, K in MATRICES:
             rb = synth.row_bytes("q4_0", K)
-            for n in range(0, N, 256):
-                n1 = min(N, n + 256)
-                oracle.qmv_rows("q4_0", layer0_host[name], xs[name], n, n1, K)
+            for n in range(0, N, chunk):
+                n1 = min(N, n + chunk)
+                oracle.qmv_rows("q4_0", layer0_host[name], xs[name], n, n1, K, threads=threads)
                 done_bytes += (n1 - n) * rb
                 if time.time() - t0 >= budget_s:
                     break
@@ -511,6 +534,70 @@ def cpu_baseline(layer0_host, x_bits, budget_s):
                 break
     dt = time.time() - t0
     return done_bytes / dt / 1e9, dt, done_bytes, done_bytes / sum(weight_bytes(N, K) for _, N, K in MATRICES)
+
+
+def cpu_configs():
+    """The oracle's time per call on configs 1 to 4 (one thread and all
+    cores), best of two calls; the small-M tile at M = 8 (the oracle's cost
+    grows linearly in M)."""
+    import oracle
+    res = {}
+
+    def timed(name, nbytes, fn):
+        for threads in (False, True):
+            dt = 1e30
+            for _ in range(2):              # best of two (the first all-core call starts the thread pool)
+                t0 = time.perf_counter()
+                fn(threads)
+                dt = min(dt, time.perf_counter() - t0)
+            res.setdefault(name, {})["all_cores" if threads else "one_thread"] = {
+                "us_per_call": round(dt * 1e6, 1), "GB_per_s": round(nbytes / dt / 1e9, 4)}
+
+    N = K = 2048
+    w, x = synth.q8_0_weights(N, K, seed=0), synth.activations(K, seed=0)
+    timed("config 1: qmv_q8_0 2048x2048 f32", w.size + 8 * K,
+          lambda t: oracle.qmv_rows("q8_0", w, x, 0, N, K, threads=t))
+    N, K = 21504, 5376
+    w, x = synth.q4_0_weights(N, K, seed=1), synth.activations(K, seed=1)
+    timed("config 2: qmv_q4_0 21504x5376 f32", w.size + 4 * K + 4 * N,
+          lambda t: oracle.qmv_rows("q4_0", w, x, 0, N, K, threads=t))
+    wu, xb = synth.q4_0_weights(N, K, seed=2, stream=1), synth.activations(K, seed=2, dtype="bf16")
+    timed("config 3: gateup_q4_0 2x21504x5376 bf16", 2 * w.size + 2 * K + 4 * N,
+          lambda t: oracle.gateup_q4_0(w, wu, xb, N, K, threads=t))
+    for (N, K) in ((5376, 5376), (5376, 21504)):
+        w, X = synth.q4_0_weights(N, K, seed=3), synth.activations((8, K), seed=3, dtype="bf16")
+        timed(f"config 4: qmm_q4_0 M=8 {N}x{K} bf16", w.size + 2 * 8 * (K + N),
+              lambda t: oracle.qmm_q4_0(w, X, 8, N, K, threads=t))
+    return res
+
+
+def cpu_baseline(layer0_host, x_bits, budget_s):
+    """The CPU oracle as the reported baseline: the sweep sample on all cores
+    (the OpenMP build) and on one thread, the host's CPU, and per-config
+    times."""
+    import oracle
+    oracle.lib()
+    model, cores = host_cpu()
+    os.environ.setdefault("OMP_NUM_THREADS", str(cores))
+    one = cpu_sweep_sample(layer0_host, x_bits, budget_s / 2, threads=False)
+    try:
+        oracle.lib_mt()
+        allc = cpu_sweep_sample(layer0_host, x_bits, budget_s / 2, threads=True)
+    except (OSError, subprocess.CalledProcessError) as e:
+        log(f"OpenMP oracle unavailable: {e}")
+        allc = None
+    base = allc or one
+    out = {"value": round(base[0], 4), "unit": UNIT, "cores": cores if allc else 1, "kind": "oracle",
+           "sample": f"oracle qmv_q4_0 over layer 0's seven matrices, {base[3]:.2f} passes ({base[2]} weight "
+                     f"bytes) in {base[1]:.1f} s, {'all ' + str(cores) + ' cores (OpenMP over rows)' if allc else 'one thread'}",
+           "cpu_model": model, "affinity_cpus": cores,
+           "one_thread": {"value": round(one[0], 4), "unit": UNIT, "cores": 1,
+                          "sample": f"{one[3]:.2f} passes in {one[1]:.1f} s"}}
+    try:
+        out["per_config"] = cpu_configs()
+    except Exception as e:     # the baseline is reported, never required
+        log(f"per-config oracle timing failed: {e}")
+    return out
 
 
 def gpu_arm(args):
@@ -605,10 +692,7 @@ def gpu_arm(args):
     chained = None if args.no_kernels else sweep_as_one_launch(torch, qbw, sweep, x0_dev, stream, graph, step_bytes)
     cpu = None
     if not args.no_cpu and ws == 1:
-        v, dt, nbytes, rows = cpu_baseline(sweep.layer0_host, x0, args.cpu_seconds)
-        cpu = {"value": round(v, 4), "unit": UNIT, "cores": 1, "kind": "oracle",
-               "sample": f"oracle qmv_q4_0 over layer 0's seven matrices, {rows:.2f} passes "
-                         f"({nbytes} weight bytes) in {dt:.1f} s, single-threaded on the host"}
+        cpu = cpu_baseline(sweep.layer0_host, x0, args.cpu_seconds)
     line = {
         "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": ws, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms / args.steps, 4), "higher_is_better": True,
@@ -684,12 +768,24 @@ def profile_case(args):
     name = args.profile
     copies = 4
     if name == "q8_0":
+        # 2048 x 2048 (4.5 MB) over 64 rotating copies (285 MB, larger than L2)
         N = K = 2048
-        ws = [torch.from_numpy(synth.q8_0_weights(N, K, seed=0)).to(dev) for _ in range(copies)]
+        copies = 64
+        w0 = torch.from_numpy(synth.q8_0_weights(N, K, seed=0)).to(dev)
+        ws = [w0.clone() for _ in range(copies)]
         x = torch.from_numpy(synth.activations(K, seed=0)).to(dev)
         y = torch.empty(N, device=dev)
         call = lambda i: qbw.qmv_q8_0(ws[i % copies], x, y, 1, N, K)
         nbytes = ws[0].numel() + 4 * K + 4 * N
+    elif name == "q8_0_lmhead":
+        # the 262144 x 5376 Q8_0 token table as LM head (1.5 GB), bf16 x
+        N, K = 262144, 5376
+        ws = [torch.from_numpy(synth.q8_0_weights(N, K, seed=12)).to(dev)]
+        xb = torch.from_numpy(synth.activations(K, seed=12, dtype="bf16").view(np.int16).copy()).view(
+            torch.bfloat16).to(dev)
+        y = torch.empty(N, device=dev)
+        call = lambda i: qbw.qmv_q8_0(ws[0], xb, y, 1, N, K)
+        nbytes = ws[0].numel() + 2 * K + 4 * N
     elif name == "q4_0":
         N, K = 21504, 5376
         ws = [torch.from_numpy(synth.q4_0_weights(N, K, seed=1)).to(dev) for _ in range(copies)]
@@ -763,6 +859,13 @@ def reference_arm(args):
         return
     import oracle
     oracle.lib()
+    model, cores = host_cpu()
+    os.environ.setdefault("OMP_NUM_THREADS", str(cores))
+    try:
+        oracle.lib_mt()
+        threads = True
+    except (OSError, subprocess.CalledProcessError):
+        threads, cores = False, 1
     # one layer's first matrices, regenerated exactly as the GPU arm does
     mats = {name: synth.q4_0_weights(N, K, seed=SEED, stream=mi, layer=0) for mi, (name, N, K) in enumerate(MATRICES)
             if name in ("q", "k", "v")}
@@ -770,14 +873,14 @@ def reference_arm(args):
     rb = synth.row_bytes("q4_0", HIDDEN)
     # size one step so that warmup + steps stay within about two minutes
     t0 = time.time()
-    oracle.qmv_rows("q4_0", mats["q"], x, 0, 64, HIDDEN)
-    per_row = (time.time() - t0) / 64
+    oracle.qmv_rows("q4_0", mats["q"], x, 0, 1024, HIDDEN, threads=threads)
+    per_row = (time.time() - t0) / 1024
     step_s = min(1.0, 120.0 / max(1, args.steps + args.warmup))
     rows = max(8, int(step_s / per_row))
     rows = min(rows, QDIM)
 
     def one_step():
-        oracle.qmv_rows("q4_0", mats["q"], x, 0, rows, HIDDEN)
+        oracle.qmv_rows("q4_0", mats["q"], x, 0, rows, HIDDEN, threads=threads)
 
     for _ in range(args.warmup):
         one_step()
@@ -788,12 +891,13 @@ def reference_arm(args):
     nbytes = rows * rb
     value = nbytes * args.steps / dt / 1e9
     sample = (f"oracle qmv_q4_0 on the first {rows} rows of layer 0's q matrix (5376 inputs) per step, "
-              f"single-threaded")
+              + (f"all {cores} cores of the host ({model}; OpenMP over rows)" if threads else "one thread"))
     line = {"impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": UNIT, "n_gpus": ws,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt * 1e3 / args.steps, 3),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": {"workload": WORKLOAD, "sample_bytes_per_step": nbytes},
-            "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "cores": 1, "kind": "oracle", "sample": sample},
+            "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample,
+                             "cpu_model": model, "affinity_cpus": len(os.sched_getaffinity(0))},
             "e2e": {"value": round(value, 4), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
@@ -807,10 +911,14 @@ def main():
     ap.add_argument("--no-kernels", action="store_true", help="skip the single-matrix supplementary numbers")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
-    ap.add_argument("--profile", choices=["q8_0", "q4_0", "q4_0_bf16", "q4_k", "gateup", "qmm", "sweep"],
+    ap.add_argument("--profile", choices=["q8_0", "q8_0_lmhead", "q4_0", "q4_0_bf16", "q4_k", "gateup", "qmm", "sweep"],
                     help="run only one small case (for profiler captures): a single-matrix workload, or the "
                          "sweep's launches over 6 layers")
     args = ap.parse_args()
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    if args.gpus != ws and not args.profile:
+        ap.error(f"--gpus {args.gpus} needs {args.gpus} processes (launch with torchrun --nproc-per-node "
+                 f"{args.gpus}); this run has WORLD_SIZE={ws}")
     if args.profile:
         profile_case(args)
         return

@@ -29,16 +29,34 @@ F32, BF16 = 0, 1
 _FMT = {"q8_0": 0, "q4_0": 1, "q4_k": 2}
 
 
-def build(force: bool = False) -> str:
-    """Compile the oracle into ``oracle/_build/liboracle.so`` (plain gcc, no SIMD flags)."""
+_LIB_MT_PATH = os.path.join(_OUT_DIR, "liboracle_mt.so")
+_lib_mt = None
+
+
+def build(force: bool = False, mt: bool = False) -> str:
+    """Compile the oracle into ``oracle/_build/liboracle.so`` (plain gcc, no SIMD
+    flags), or with ``mt`` the same source with OpenMP into ``liboracle_mt.so``
+    (rows of a product split over threads; used only for the all-core CPU
+    baseline)."""
     os.makedirs(_OUT_DIR, exist_ok=True)
-    if force or not os.path.exists(_LIB_PATH) or os.path.getmtime(_LIB_PATH) < os.path.getmtime(_SRC):
-        tmp = _LIB_PATH + f".{os.getpid()}.tmp"
+    path = _LIB_MT_PATH if mt else _LIB_PATH
+    if force or not os.path.exists(path) or os.path.getmtime(path) < os.path.getmtime(_SRC):
+        tmp = path + f".{os.getpid()}.tmp"
         subprocess.check_call([
             "gcc", "-O2", "-std=c11", "-ffp-contract=off", "-fno-fast-math", "-fPIC", "-shared",
-            "-Wall", "-Wextra", "-o", tmp, _SRC, "-lm"])
-        os.replace(tmp, _LIB_PATH)
-    return _LIB_PATH
+            "-Wall", "-Wextra"] + (["-fopenmp"] if mt else ["-Wno-unknown-pragmas"]) + ["-o", tmp, _SRC, "-lm"])
+        os.replace(tmp, path)
+    return path
+
+
+def lib_mt():
+    """The OpenMP build of the oracle (same arithmetic per row)."""
+    global _lib_mt
+    with _lock:
+        if _lib_mt is None:
+            _lib_mt = ctypes.CDLL(build(mt=True))
+            _declare(_lib_mt)
+    return _lib_mt
 
 
 def lib():
@@ -170,34 +188,35 @@ def qmv(fmt: str, w: np.ndarray, x: np.ndarray, N: int, K: int):
     return y, S
 
 
-def qmv_rows(fmt: str, w: np.ndarray, x: np.ndarray, n0: int, n1: int, K: int):
-    """Rows [n0, n1) of y = W x, with S; ``w`` still holds the whole matrix."""
+def qmv_rows(fmt: str, w: np.ndarray, x: np.ndarray, n0: int, n1: int, K: int, threads: bool = False):
+    """Rows [n0, n1) of y = W x, with S; ``w`` still holds the whole matrix.
+    ``threads``: the OpenMP build (rows split over the host's cores)."""
     w = _weights(w)
     x, xt = _act(x)
     y = np.empty(n1 - n0, dtype=np.float64)
     S = np.empty(n1 - n0, dtype=np.float64)
-    _check(lib().oracle_qmv_rows(_FMT[fmt], _ptr(w), _ptr(x), xt, n0, n1, K, _ptr(y), _ptr(S)),
-           "qmv_rows")
+    L = lib_mt() if threads else lib()
+    _check(L.oracle_qmv_rows(_FMT[fmt], _ptr(w), _ptr(x), xt, n0, n1, K, _ptr(y), _ptr(S)), "qmv_rows")
     return y, S
 
 
-def gateup_q4_0(wg: np.ndarray, wu: np.ndarray, x: np.ndarray, N: int, K: int):
+def gateup_q4_0(wg: np.ndarray, wu: np.ndarray, x: np.ndarray, N: int, K: int, threads: bool = False):
     """Returns dict with g, u, out = gelu_tanh(g) * u, Sg, Su (all fp64)."""
     wg, wu = _weights(wg), _weights(wu)
     x, xt = _act(x)
     r = {k: np.empty(N, dtype=np.float64) for k in ("g", "u", "out", "Sg", "Su")}
-    _check(lib().oracle_gateup_q4_0(_ptr(wg), _ptr(wu), _ptr(x), xt, N, K, _ptr(r["g"]), _ptr(r["u"]),
+    _check((lib_mt() if threads else lib()).oracle_gateup_q4_0(_ptr(wg), _ptr(wu), _ptr(x), xt, N, K, _ptr(r["g"]), _ptr(r["u"]),
                                     _ptr(r["out"]), _ptr(r["Sg"]), _ptr(r["Su"])), "gateup")
     return r
 
 
-def qmm_q4_0(w: np.ndarray, X: np.ndarray, M: int, N: int, K: int):
+def qmm_q4_0(w: np.ndarray, X: np.ndarray, M: int, N: int, K: int, threads: bool = False):
     """Y[m, n] = sum_k X[m, k] W[n, k] and S[m, n] (fp64)."""
     w = _weights(w)
     X, xt = _act(X)
     Y = np.empty((M, N), dtype=np.float64)
     S = np.empty((M, N), dtype=np.float64)
-    _check(lib().oracle_qmm_q4_0(_ptr(w), _ptr(X), xt, M, N, K, _ptr(Y), _ptr(S)), "qmm")
+    _check((lib_mt() if threads else lib()).oracle_qmm_q4_0(_ptr(w), _ptr(X), xt, M, N, K, _ptr(Y), _ptr(S)), "qmm")
     return Y, S
 
 

@@ -9,7 +9,9 @@
  * and its own GELU.
  *
  * Everything is scalar C, accumulated in double precision in ascending k, with
- * no SIMD intrinsics and no reordering beyond the textbook definition.
+ * no SIMD intrinsics and no reordering beyond the textbook definition.  Built
+ * with OpenMP (for the all-core CPU baseline only), the independent rows of a
+ * product are split over threads; each row's arithmetic is unchanged.
  *
  * What is computed, and where the pages define it:
  *  - Q8_0 block: w = d * q, d an IEEE binary16 scale, q a signed byte
@@ -247,8 +249,11 @@ static void matvec_rows(int fmt, const uint8_t *w, const double *x,
 {
     int be = block_elems(fmt);
     int64_t nb = K / be;
-    double wb[ORACLE_QK_K];
+    /* rows are independent: the OpenMP build of this file (the all-core CPU
+     * baseline) splits them over threads, each row computed as above */
+#pragma omp parallel for schedule(static)
     for (int64_t n = n0; n < n1; n++) {
+        double wb[ORACLE_QK_K];
         double acc = 0.0, sabs = 0.0;
         for (int64_t b = 0; b < nb; b++) {
             decode_block(fmt, w + (n * nb + b) * block_size(fmt), wb);
