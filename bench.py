@@ -689,7 +689,7 @@ def gpu_arm(args):
         return
 
     supp = {} if args.no_kernels else supplementary_kernels(torch, qbw, hbm_peak)
-    chained = None if args.no_kernels else sweep_as_one_launch(torch, qbw, sweep, x0_dev, stream, graph, step_bytes)
+    chained = {} if args.no_kernels else sweep_as_chain(torch, qbw, sweep, x0_dev, stream, graph, step_bytes)
     cpu = None
     if not args.no_cpu and ws == 1:
         cpu = cpu_baseline(sweep.layer0_host, x0, args.cpu_seconds)
@@ -712,7 +712,8 @@ def gpu_arm(args):
         "clocks": clocks.summary(t_start - 0.05, t_end + 0.05),
         "cpu_baseline": cpu,
         "kernels": supp,
-        "sweep_as_one_launch": chained,
+        "sweep_as_one_launch": chained.get("sweep_as_one_launch"),
+        "sweep_as_prefetching_launches": chained.get("sweep_as_prefetching_launches"),
         "per_kernel_in_sweep": {k: {"launches": v["launches"], "ms": round(v["ms"], 4),
                                     "GB_per_s": round(v["bytes"] / (v["ms"] * 1e-3) / 1e9, 1)}
                                 for k, v in per_kernel.items()},
@@ -723,36 +724,52 @@ def gpu_arm(args):
         torch.distributed.destroy_process_group()
 
 
-def sweep_as_one_launch(torch, qbw, sweep, x0_dev, stream, graph, step_bytes, replays=50):
-    """The same token as one chained launch (qbw_chain_run over the sweep's
-    240 steps and buffers), against the graph of 240 launches: its time and
-    whether its final activation equals the graph's bit for bit."""
+def sweep_chain_steps(sweep):
+    """The sweep's 240 launches as chain steps, on the sweep's own buffers."""
     steps = []
     for L in range(sweep.layers):
         steps += [(sweep.qkv_view(L), None, sweep.h, sweep.qkv, QDIM + 2 * KVDIM, HIDDEN),
                   (sweep.view(L, "o"), None, sweep.q, sweep.o, HIDDEN, QDIM),
                   (sweep.view(L, "gate"), sweep.view(L, "up"), sweep.o, sweep.a, FFN, HIDDEN),
                   (sweep.view(L, "down"), None, sweep.a, sweep.h, HIDDEN, FFN)]
-    chain = qbw.Chain(steps)
+    return steps
+
+
+def sweep_as_chain(torch, qbw, sweep, x0_dev, stream, graph, step_bytes, replays=50):
+    """The same token through a chain over the sweep's 240 steps and buffers,
+    in its two forms: one cooperative launch with a grid barrier between steps
+    (qbw_chain_run), and one launch per step in which each launch prefetches
+    the next step's first weight tiles into L2 (qbw_chain_run_launches).  For
+    each, its time and whether its final activation equals the graph of 240
+    separate launches bit for bit."""
+    chain = qbw.Chain(sweep_chain_steps(sweep))
+    forms = {"sweep_as_one_launch": (chain.run, 1, "qbw_chain_run: the 240 steps as one cooperative launch "
+                                                   "with a grid barrier between steps"),
+             "sweep_as_prefetching_launches": (chain.run_launches, Sweep.LAUNCHES_PER_STEP,
+                                               "qbw_chain_run_launches: one launch per step, each prefetching "
+                                               "the next step's first weight tiles into L2")}
+    out = {}
     try:
         with torch.cuda.stream(stream):
             sweep.h.copy_(x0_dev)
             graph.replay()
             h_graph = sweep.h.clone()
-            sweep.h.copy_(x0_dev)
-            chain.run(stream)
-        torch.cuda.synchronize()
-        same = bool(torch.equal(h_graph.view(torch.int16), sweep.h.view(torch.int16)))
-        g = capture(torch, lambda: chain.run(torch.cuda.current_stream()), stream)
-        time_graph(torch, g, 3, stream)
-        ms = time_graph(torch, g, replays, stream) / replays
-        assert qbw.fault_read(clear=True, stream=stream) == 0, "the chained launch recorded a fault"
+        for key, (run, launches, what) in forms.items():
+            with torch.cuda.stream(stream):
+                sweep.h.copy_(x0_dev)
+                run(stream)
+            torch.cuda.synchronize()
+            same = bool(torch.equal(h_graph.view(torch.int16), sweep.h.view(torch.int16)))
+            g = capture(torch, lambda: run(torch.cuda.current_stream()), stream)
+            time_graph(torch, g, 3, stream)
+            ms = time_graph(torch, g, replays, stream) / replays
+            assert qbw.fault_read(clear=True, stream=stream) == 0, f"{key} recorded a fault"
+            out[key] = {"ms_per_step": round(ms, 4), "GB_per_s": round(step_bytes / (ms * 1e-3) / 1e9, 1),
+                        "tok_per_s": round(1e3 / ms, 2), "final_activation_bit_identical_to_graph": same,
+                        "launches_per_step": launches, "what": what}
     finally:
         chain.close()
-    return {"ms_per_step": round(ms, 4), "GB_per_s": round(step_bytes / (ms * 1e-3) / 1e9, 1),
-            "tok_per_s": round(1e3 / ms, 2), "final_activation_bit_identical_to_graph": same,
-            "launches_per_step": 1,
-            "what": "qbw_chain_run: the 240 steps as one cooperative launch with a grid barrier between steps"}
+    return out
 
 
 def profile_case(args):

@@ -90,6 +90,8 @@ def _declare(L):
     L.qbw_chain_create.argtypes = [ctypes.POINTER(_ChainStep), i32, ctypes.POINTER(P)]
     L.qbw_chain_run.restype = i32
     L.qbw_chain_run.argtypes = [P, P]
+    L.qbw_chain_run_launches.restype = i32
+    L.qbw_chain_run_launches.argtypes = [P, P]
     L.qbw_chain_destroy.restype = i32
     L.qbw_chain_destroy.argtypes = [P]
 
@@ -265,6 +267,11 @@ class Chain:
 
     def run(self, stream=None):
         _check(load().qbw_chain_run(self._h, _stream(stream)), "qbw_chain_run")
+
+    def run_launches(self, stream=None):
+        """One launch per step, each prefetching the next step's first weight
+        tiles into L2 (qbw_chain_run_launches)."""
+        _check(load().qbw_chain_run_launches(self._h, _stream(stream)), "qbw_chain_run_launches")
 
     def close(self):
         if getattr(self, "_h", None):

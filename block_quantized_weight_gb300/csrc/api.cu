@@ -33,7 +33,7 @@ cudaError_t launch_selftest_wait(int which, uint64_t limit_ns, unsigned int* fau
 bool qmv_tc_supported(int nmat, int64_t N, int64_t K, int sm_count);
 cudaError_t launch_qmv_tc(int fmt, int nmat, int ntok, const CUtensorMap* tmap_w, const void* const* w,
                           const void* x, int x_bf16, void* y, int y_bf16, int N, int K, int sm_count,
-                          unsigned int* fault, cudaStream_t stream);
+                          unsigned int* fault, cudaStream_t stream, const QtcNextLaunch* next = nullptr);
 int qmm_tc_tile_rows();
 bool qmv_chain_step_supported(int nmat, int64_t N, int64_t K, int ctas);
 void qmv_chain_fill_step(ChainStepDesc* d, int nmat, int64_t N, int64_t K);
@@ -462,6 +462,8 @@ struct qbw_chain_s {
     int device = -1;
     int nsteps = 0;
     int ctas = 0;
+    int sm_count = 0;
+    std::vector<qbw::ChainStepDesc> host;   // the step descriptors, for runs as separate launches
     qbw::ChainStepDesc* steps = nullptr;
     unsigned int* bar = nullptr;          // [0] grid barrier counter, [1] abort flag
     unsigned long long* share = nullptr;
@@ -729,6 +731,8 @@ qbw_status qbw_chain_create(const qbw_chain_step* steps, int nsteps, qbw_chain* 
     cudaGetDevice(&ch->device);
     ch->nsteps = nsteps;
     ch->ctas = ctas;
+    ch->sm_count = di->sm_count;
+    ch->host = host;
     ch->fault = di->fault;
     const size_t share_bytes = qmv_chain_share_bytes(ctas);
     if (cudaMalloc(&ch->steps, sizeof(ChainStepDesc) * (size_t)nsteps) != cudaSuccess ||
@@ -752,6 +756,39 @@ qbw_status qbw_chain_run(qbw_chain chain, void* stream) {
     cudaError_t e = launch_qmv_chain(chain->steps, chain->nsteps, chain->ctas, chain->bar, chain->share,
                                      chain->fault, static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? QBW_OK : QBW_ECUDA;
+}
+
+qbw_status qbw_chain_run_launches(qbw_chain chain, void* stream) {
+    if (!chain) return QBW_EINVAL;
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess) return QBW_ECUDA;
+    if (dev != chain->device) return QBW_EINVAL;
+    DeviceInfo* di = nullptr;
+    qbw_status st = device_info(&di);
+    if (st != QBW_OK) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    for (int i = 0; i < chain->nsteps; ++i) {
+        const ChainStepDesc& d = chain->host[(size_t)i];
+        if (!qmv_tc_supported(d.nmat, d.N, d.K, di->sm_count)) return QBW_ESHAPE;
+    }
+    for (int i = 0; i < chain->nsteps; ++i) {
+        const ChainStepDesc& d = chain->host[(size_t)i];
+        QtcNextLaunch next;
+        next.units = 0;
+        if (i + 1 < chain->nsteps) {
+            const ChainStepDesc& n = chain->host[(size_t)i + 1];
+            next.tmap[0] = n.tmap[0];
+            next.tmap[1] = n.tmap[1];
+            next.units = n.units;
+            next.groups = n.groups;
+            next.nmat = n.nmat;
+        }
+        const void* wp[2] = {d.w[0], d.w[1]};
+        cudaError_t e = launch_qmv_tc(kFmtQ4, d.nmat, 1, d.tmap, wp, d.x, 1, d.y, d.y_bf16, d.N, d.K, di->sm_count,
+                                      di->fault, s, &next);
+        if (e != cudaSuccess) return QBW_ECUDA;
+    }
+    return QBW_OK;
 }
 
 qbw_status qbw_fault_read(uint32_t* code, int clear, void* stream) {

@@ -102,6 +102,14 @@ void noalloc_scratch_mark_dirty(int device);
 // Largest dynamic shared memory the streaming kernels may request.
 cudaError_t prepare_qmv_stream(int fmt, int nmat, int R, size_t smem);
 
+// The launch after a tensor-core M = 1 launch on the same stream, for the
+// L2 prefetch of its first weight tiles: its tensor maps (the up matrix in
+// [1] for gate+up) and unit split (units = tiles x groups x nmat).
+struct QtcNextLaunch {
+    CUtensorMap tmap[2];
+    int32_t units, groups, nmat;
+};
+
 // One step of a chained product (qmv_chain.cu), in device memory (aligned as
 // its tensor maps require): y = W x (nmat = 1) or gelu_tanh(Wg x) * (Wu x)
 // (nmat = 2), Q4_0 weights, bf16 x.

@@ -163,6 +163,17 @@ __device__ __forceinline__ void qmv_tc_body(const QtcParams& p) {
                 tma_load_2d(sbase + (uint32_t)s * kRawStageBytes, &p.tmap_w[mat], g * kGroupWords, t * kTileRows,
                             full_bar(bar0, s), policy_evict_first());
             }
+            // every copy of this launch is issued: warm L2 with the first units
+            // (a ring's worth) that this CTA index loads in the next launch
+            if (ok && p.next_units > 0 && cta < p.next_ctas) {
+                const int v0 = unit_begin(cta, p.next_units, p.next_ctas);
+                const int v1 = unit_begin(cta + 1, p.next_units, p.next_ctas);
+                for (int i = 0; i < kStages && v0 + i < v1; ++i) {
+                    const int u = v0 + i, ug = u / p.next_nmat, mat = u - ug * p.next_nmat, t = ug / p.next_groups,
+                              g = ug - t * p.next_groups;
+                    tma_prefetch_2d(&p.next_tmap[mat], g * kGroupWords, t * kTileRows);
+                }
+            }
         }
     } else {
         if (warp == 0) {
@@ -770,7 +781,7 @@ size_t qmv_tc_smem_bytes() { return kSmemBytes; }
 // two tokens.
 cudaError_t launch_qmv_tc(int fmt, int nmat, int ntok, const CUtensorMap* tmap_w, const void* const* w,
                           const void* x, int x_bf16, void* y, int y_bf16, int N, int K, int sm_count,
-                          unsigned int* fault, cudaStream_t stream) {
+                          unsigned int* fault, cudaStream_t stream, const QtcNextLaunch* next) {
     if (nmat * ntok > 2 || (ntok == 2 && !x_bf16)) return cudaErrorInvalidValue;
     if (fmt == kFmtQ4K && nmat * ntok != 1) return cudaErrorInvalidValue;
     QtcParams p;
@@ -779,6 +790,16 @@ cudaError_t launch_qmv_tc(int fmt, int nmat, int ntok, const CUtensorMap* tmap_w
     p.w[0] = static_cast<const uint8_t*>(w[0]);
     p.w[1] = static_cast<const uint8_t*>(w[nmat == 2 ? 1 : 0]);
     p.row_bytes = weight_row_bytes(fmt, K);
+    p.next_units = 0;
+    p.next_groups = p.next_nmat = p.next_ctas = 1;
+    if (next && next->units > 0) {
+        p.next_tmap[0] = next->tmap[0];
+        p.next_tmap[1] = next->tmap[next->nmat == 2 ? 1 : 0];
+        p.next_units = next->units;
+        p.next_groups = next->groups;
+        p.next_nmat = next->nmat;
+        p.next_ctas = next->units < sm_count ? next->units : sm_count;
+    }
     p.x = x;
     p.y = y;
     p.fault = fault;

@@ -77,6 +77,12 @@ static_assert(kOffB % 1024 == 0, "B operand needs 1024-byte alignment");
 
 struct QtcParams {
     CUtensorMap tmap_w[2];   // Q4_0 rows as 8-byte words, box (18, 128); [1]: the up matrix of gate+up
+    // the launch that follows on the stream when a chain runs as separate
+    // launches (next_units = 0: none): its weights' tensor maps and unit
+    // split, so that each CTA's producer can prefetch into L2 the first units
+    // the same CTA index loads there
+    CUtensorMap next_tmap[2];
+    int32_t next_units, next_groups, next_nmat, next_ctas;
     const void* x;
     void* y;
     unsigned int* fault;

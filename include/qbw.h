@@ -402,6 +402,20 @@ typedef struct qbw_chain_s *qbw_chain;
 
 qbw_status qbw_chain_create(const qbw_chain_step *steps, int nsteps, qbw_chain *out);
 qbw_status qbw_chain_run(qbw_chain chain, void *stream);
+
+/*
+ * qbw_chain_run_launches -- enqueue the chain as one kernel launch per step
+ * on `stream` (the tensor-core kernel of qmv_q4_0 / qmv_gateup_q4_0, each
+ * launched as a programmatic dependent of the one before), instead of one
+ * cooperative launch.  Each step's results are bit-identical to the separate
+ * call; what the chain adds is that every launch, once it has issued its last
+ * weight copy, prefetches into L2 the first weight tiles its CTAs will load in
+ * the next step, so the next launch's first copies come from L2 rather than
+ * HBM.  May be captured in a CUDA graph.  QBW_EINVAL as for qbw_chain_run;
+ * QBW_ESHAPE for a step the tensor-core kernel does not take (more than
+ * 524,288 rows).  Allocates nothing; the chain's own scratch is not used.
+ */
+qbw_status qbw_chain_run_launches(qbw_chain chain, void *stream);
 qbw_status qbw_chain_destroy(qbw_chain chain);
 
 /*

@@ -1,6 +1,7 @@
-"""GPU parity of chained products (qbw_chain_create / qbw_chain_run): several
-dependent Q4_0 matrix-vector products, each step's activations an earlier
-step's output, in one launch.
+"""GPU parity of chained products (qbw_chain_create / qbw_chain_run and
+qbw_chain_run_launches): several dependent Q4_0 matrix-vector products, each
+step's activations an earlier step's output, in one launch or one launch per
+step.
 
 Each step is checked against the CPU oracle applied to the step's actual
 input, the chain's own bf16 output of the earlier step read back after the
@@ -94,8 +95,11 @@ def test_chain_single_step_matches_bound(qbw, oracle):
 HIDDEN, QDIM, KVDIM, FFN = 5376, 8192, 4096, 21504
 
 
-def test_chain_decode_layers_match_separate_calls(qbw, oracle):
-    # two layers of the decode sweep: h -> q|k|v -> o(q) -> gate+up(o) -> down -> h
+@pytest.mark.parametrize("mode", ["one_launch", "launches"])
+def test_chain_decode_layers_match_separate_calls(qbw, oracle, mode):
+    # two layers of the decode sweep: h -> q|k|v -> o(q) -> gate+up(o) -> down -> h;
+    # run as one cooperative launch, or as one launch per step that prefetches
+    # the next step's first weight tiles into L2 (qbw_chain_run_launches)
     layers = 2
     W = []
     for layer in range(layers):
@@ -118,7 +122,10 @@ def test_chain_decode_layers_match_separate_calls(qbw, oracle):
                   (W[L]["d"], None, a[L], hs[L + 1], HIDDEN, FFN)]
     chain = qbw.Chain(steps)
     try:
-        chain.run()
+        if mode == "launches":
+            chain.run_launches()
+        else:
+            chain.run()
         torch.cuda.synchronize()
         assert qbw.fault_read(clear=True) == 0
         # each step against the separate call on the chain's own input, bit for bit
