@@ -28,11 +28,14 @@
 // a byte permute puts qs[j] and qs[j + 1] in bytes 0 and 2 of a word; a LOP3
 // keeps their low nibbles and ORs in the bf16 exponent of 128, which gives
 // the pair (128 + c_j, 128 + c_j+1) exactly; the same after a 4-bit shift
-// gives codes j + 16 and j + 17.  A packed bf16 add of -128 leaves the exact
-// integers c, and one packed bf16 fma gives c d - 8 d = d (c - 8), rounded
-// once, with d the block's fp16 scale rounded to bf16.  Each weight is thus
-// within 2^-7 of its exact value relative (two roundings to 8 significant
-// bits, 2^-8 each), inside the 1e-2 bound on sum |w x| of the tensor-core path.
+// gives codes j + 16 and j + 17.  A packed bf16 add of -136 leaves the exact
+// integers c - 8.  The block's fp16 scale d is carried as two bf16 parts, d_hi = bf16(d) and
+// d_lo = bf16(d - d_hi), and the weight is fma(c - 8, d_hi, (c - 8) d_lo),
+// rounded once to bf16.  The argument of that final rounding is within about
+// 2^-15 of (c - 8) d relative (d_lo's own rounding and that of the small
+// product), so each weight is within 2^-8 (1 + 2^-7) of its exact value
+// relative: one rounding to 8 significant bits, well inside the 1e-2 bound
+// on sum |w x| of the tensor-core path.
 //
 // Split K, two ways.  With at most 8 splits per tile, the splits of a tile run
 // as one thread-block cluster: each CTA leaves its partial tile (128 rows x M,
@@ -87,16 +90,17 @@ constexpr uint32_t kDCol = kAStages * kAColsPerStage;     // accumulator D_j of 
 constexpr uint32_t kRawStageBytes = kTileRows * kGroupBytes;   // 18432
 constexpr int kReduceItems = 3;               // row x 4-column items per thread in the split-K sum: 480 x 3 >= 128 x 8
 
-// bf16x2 constants
-constexpr uint32_t kBf16Minus128 = 0xC300C300u;
-constexpr uint32_t kBf16Minus8 = 0xC100C100u;
+// bf16x2 constant: (-136, -136)
+constexpr uint32_t kBf16Minus136 = 0xC308C308u;
 
-// (128 + c) pair -> d (c - 8) pair: (t - 128) is the exact integer c, and
-// fma(c, d, -8 d) rounds once (-8 d is exact).
-__device__ __forceinline__ uint32_t scale_pair(uint32_t t, uint32_t dd, uint32_t m8dd, uint32_t m128) {
-    uint32_t c, r;
-    asm("add.rn.bf16x2 %0, %1, %2;" : "=r"(c) : "r"(t), "r"(m128));
-    asm("fma.rn.bf16x2 %0, %1, %2, %3;" : "=r"(r) : "r"(c), "r"(dd), "r"(m8dd));
+// (128 + c) pair -> d (c - 8) pair: (t - 136) is the exact integer c - 8, the
+// product with d_lo is rounded (tiny), and the fma with d_hi rounds the weight
+// once.
+__device__ __forceinline__ uint32_t scale_pair(uint32_t t, uint32_t dhi, uint32_t dlo, uint32_t m136) {
+    uint32_t c, lo, r;
+    asm("add.rn.bf16x2 %0, %1, %2;" : "=r"(c) : "r"(t), "r"(m136));
+    asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(lo) : "r"(c), "r"(dlo));
+    asm("fma.rn.bf16x2 %0, %1, %2, %3;" : "=r"(r) : "r"(c), "r"(dhi), "r"(lo));
     return r;
 }
 
@@ -108,10 +112,11 @@ template <int OFF, int SW, int SH>
 __device__ __forceinline__ void dequant_block(const uint32_t (&v)[36], uint32_t* col) {
     const uint32_t dbits = SH ? (v[SW] >> 16) : (v[SW] & 0xFFFFu);
     const float d = half_bits_to_float(dbits);
-    const uint32_t m128 = kBf16Minus128, m8 = kBf16Minus8;
-    uint32_t dd, m8dd;
-    asm("cvt.rn.bf16x2.f32 %0, %1, %1;" : "=r"(dd) : "f"(d));
-    asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(m8dd) : "r"(dd), "r"(m8));   // (-8 d, -8 d): exact
+    const uint32_t m136 = kBf16Minus136;
+    uint32_t dhi, dlo;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %1;" : "=r"(dhi) : "f"(d));
+    const float rest = d - __uint_as_float(dhi << 16);     // exact in fp32
+    asm("cvt.rn.bf16x2.f32 %0, %1, %1;" : "=r"(dlo) : "f"(rest));
 #pragma unroll
     for (int j = 0; j < 16; j += 2) {
         // qs[j] and qs[j + 1] share a word: OFF + j is even and OFF % 4 is 0 or 2
@@ -119,8 +124,8 @@ __device__ __forceinline__ void dequant_block(const uint32_t (&v)[36], uint32_t*
         uint32_t lo, hi;
         if ((byte & 3) == 0) nibble_pairs<0>(v[byte >> 2], lo, hi);
         else nibble_pairs<2>(v[byte >> 2], lo, hi);
-        col[j >> 1] = scale_pair(lo, dd, m8dd, m128);         // elements j, j + 1
-        col[8 + (j >> 1)] = scale_pair(hi, dd, m8dd, m128);   // elements 16 + j, 17 + j
+        col[j >> 1] = scale_pair(lo, dhi, dlo, m136);         // elements j, j + 1
+        col[8 + (j >> 1)] = scale_pair(hi, dhi, dlo, m136);   // elements 16 + j, 17 + j
     }
 }
 

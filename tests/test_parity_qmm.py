@@ -197,3 +197,24 @@ def test_qmm_workspace_shared_across_shapes(qbw):
         torch.cuda.synchronize()
         assert torch.equal(Y_shared.view(torch.int32), Y_fresh.view(torch.int32)), (M, N, K)
     assert qbw.fault_read(clear=True) == 0
+
+
+@pytest.mark.parametrize("M,N,K", [(32, 2048, 256), (8, 4096, 512)])
+def test_qmm_weight_rounded_once(qbw, oracle, M, N, K):
+    # Token m is the unit vector e_k(m), so Y[m, n] is the tile's bf16 weight
+    # W[n, k(m)] itself (one product with 1, fp32 sums of zeros).  Rounded once
+    # from the exact (c - 8) d it is within 2^-8 (1 + 2^-7) of it, relative; a
+    # scale rounded to bf16 before the product would put a quarter of the
+    # weights beyond that.
+    w = synth.q4_0_weights(N, K, seed=M + N)
+    ks = (np.arange(M) * 37 + 5) % K
+    X = np.zeros((M, K), dtype=np.uint16)
+    X[np.arange(M), ks] = 0x3F80                      # bf16 1.0
+    Y = run_qmm(qbw, w, X, M, N, K, torch.float32)
+    W = oracle.dequant("q4_0", w, N, K).astype(np.float64)   # exact (c - 8) d
+    ref = W[:, ks].T                                  # [M, N]
+    err = np.abs(Y - ref)
+    assert np.all(err <= 2.0 ** -8 * (1 + 2.0 ** -7) * np.abs(ref)), \
+        f"max relative error {np.max(err / np.maximum(np.abs(ref), 1e-300)):.3e}"
+    # and each value is a bf16 number
+    assert np.all((Y.astype(np.float32).view(np.uint32) & 0xFFFF) == 0)
