@@ -843,8 +843,26 @@ def profile_case(args):
                       .view(torch.bfloat16).to(dev))
         call = lambda i: sweep.launches()
         nbytes = sum(b for _, _, b in sweep._specs)
-    elif name == "qmm":
-        M, N, K = 32, 5376, 21504
+    elif name.startswith("mixbit"):
+        # one mixed-bit matrix, 21504 x 5376, groups of 32, bf16 x, rotating
+        # copies larger than L2 together
+        bits = int(name[len("mixbit"):])
+        N, K, G = 21504, 5376, 32
+        qp, sc, bi = synth.mixbit_weights(bits, N, K, G, seed=9)
+        nb = synth.mixbit_bytes(bits, N, K, G)
+        copies = max(2, int(np.ceil(300e6 / nb)))
+        mats = [(torch.from_numpy(qp.view(np.uint8).copy()).to(dev), torch.from_numpy(sc.view(np.uint8).copy()).to(dev),
+                 torch.from_numpy(bi.view(np.uint8).copy()).to(dev) if bi is not None else None) for _ in range(copies)]
+        xb = torch.from_numpy(synth.activations(K, seed=9, dtype="bf16").view(np.int16).copy()).view(
+            torch.bfloat16).to(dev)
+        y = torch.empty(N, device=dev)
+        call = lambda i: qbw.qmv_mixbit(bits, *mats[i % copies], G, xb, y, 1, N, K)
+        nbytes = nb + 2 * K + 4 * N
+    elif name in ("qmm", "qmm8", "qmm8_5376"):
+        # M = 32 (whole-tile splits) or M = 8 (stream-K) over 5376 x 21504, or
+        # M = 8 over 5376 x 5376 (cluster splits)
+        M, N, K = {"qmm": (32, 5376, 21504), "qmm8": (8, 5376, 21504), "qmm8_5376": (8, 5376, 5376)}[name]
+        copies = max(copies, int(np.ceil(300e6 / (N * K // 32 * 18))))
         ws = [torch.from_numpy(synth.q4_0_weights(N, K, seed=3)).to(dev) for _ in range(copies)]
         X = torch.from_numpy(synth.activations((M, K), seed=3, dtype="bf16").view(np.int16).copy()).view(
             torch.bfloat16).to(dev)
@@ -928,7 +946,8 @@ def main():
     ap.add_argument("--no-kernels", action="store_true", help="skip the single-matrix supplementary numbers")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
-    ap.add_argument("--profile", choices=["q8_0", "q8_0_lmhead", "q4_0", "q4_0_bf16", "q4_k", "gateup", "qmm", "sweep"],
+    ap.add_argument("--profile", choices=["q8_0", "q8_0_lmhead", "q4_0", "q4_0_bf16", "q4_k", "gateup", "qmm", "sweep",
+                                          "mixbit2", "mixbit4", "mixbit8", "qmm8", "qmm8_5376"],
                     help="run only one small case (for profiler captures): a single-matrix workload, or the "
                          "sweep's launches over 6 layers")
     args = ap.parse_args()
