@@ -19,7 +19,9 @@
 // warp 4g + q of the set handles rows 32q .. 32q + 31 (the TMEM lanes of its
 // quarter) over the whole group.  Warp 12 lane 0 issues the TMA copies.
 // Warps 13, 14 and 15 (lane 0) issue the MMAs: issuer j takes set j's groups
-// (all 16 K-steps of each) into its own accumulator D_j.  One thread issues a
+// (all 16 K-steps of each) into its own accumulator D_j.  A group's A stage is
+// published in two halves of 128 K, each with its own pair of mbarriers, so
+// the MMAs on the first half run while the set decodes the second.  One thread issues a
 // narrow (N <= 32) MMA only about every 50 cycles, well below what the tensor
 // core retires, and issuing threads overlap, so three issuers keep up with
 // three sets.  Warps 0..3 read D_0 + D_1 + D_2 back.
@@ -159,18 +161,19 @@ struct QmmParams {
 };
 
 // Barrier layout shared by every role: full[kStages], empty[kStages],
-// afull[kAStages], aempty[kAStages], dfull, 8 bytes each from bar0.
-constexpr int kBarriers = 2 * kStages + 2 * kAStages + 1;
+// afull[kAStages][2], aempty[kAStages][2] (per half of the group's K), dfull,
+// 8 bytes each from bar0.
+constexpr int kBarriers = 2 * kStages + 4 * kAStages + 1;
 __device__ __forceinline__ uint32_t full_bar_at(uint32_t bar0, int s) { return bar0 + 8u * (uint32_t)s; }
 __device__ __forceinline__ uint32_t empty_bar_at(uint32_t bar0, int s) { return bar0 + 8u * (uint32_t)(kStages + s); }
-__device__ __forceinline__ uint32_t afull_bar_at(uint32_t bar0, int a) {
-    return bar0 + 8u * (uint32_t)(2 * kStages + a);
+__device__ __forceinline__ uint32_t afull_bar_at(uint32_t bar0, int a, int h) {
+    return bar0 + 8u * (uint32_t)(2 * kStages + 2 * a + h);
 }
-__device__ __forceinline__ uint32_t aempty_bar_at(uint32_t bar0, int a) {
-    return bar0 + 8u * (uint32_t)(2 * kStages + kAStages + a);
+__device__ __forceinline__ uint32_t aempty_bar_at(uint32_t bar0, int a, int h) {
+    return bar0 + 8u * (uint32_t)(2 * kStages + 2 * kAStages + 2 * a + h);
 }
 __device__ __forceinline__ uint32_t dfull_bar_at(uint32_t bar0) {
-    return bar0 + 8u * (uint32_t)(2 * kStages + 2 * kAStages);
+    return bar0 + 8u * (uint32_t)(2 * kStages + 4 * kAStages);
 }
 
 // v[q] = sum of the included accumulators' column q (16 columns from taddr;
@@ -231,11 +234,13 @@ __device__ __forceinline__ bool dequant_warp(int g, uint32_t raw_row, uint32_t a
         __syncwarp();
         if (lane == 0) mbar_arrive(empty_bar_at(bar0, s));     // raw W of stage s read
         uint32_t c0[32], c1[32];
+        const uint32_t par = (uint32_t)((i / kSets) - 1) & 1u;
+        // ---- first half of the group's K (block pairs 0, 1): the MMAs on it
+        // run while the second half is decoded
         dequant_pair<0>(v, c0);
         if (i >= kSets) {
-            // the MMAs of group i - 3 have finished reading A stage g
-            const bool free = mbar_wait_bounded(aempty_bar_at(bar0, g), (uint32_t)((i / kSets) - 1) & 1u, fault,
-                                                kFaultMmaWaitTimeout);
+            // the MMAs of group i - 3 have finished reading this half of A stage g
+            const bool free = mbar_wait_bounded(aempty_bar_at(bar0, g, 0), par, fault, kFaultMmaWaitTimeout);
             if (!__all_sync(0xffffffffu, free)) return false;
             tc_fence_after();
         }
@@ -243,8 +248,17 @@ __device__ __forceinline__ bool dequant_warp(int g, uint32_t raw_row, uint32_t a
         dequant_pair<1>(v, c1);
         tmem_wait_st();
         tmem_st32(a_taddr + 32u, c1);
-        dequant_pair<2>(v, c0);
         tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(afull_bar_at(bar0, g, 0));
+        // ---- second half (block pairs 2, 3)
+        dequant_pair<2>(v, c0);
+        if (i >= kSets) {
+            const bool free = mbar_wait_bounded(aempty_bar_at(bar0, g, 1), par, fault, kFaultMmaWaitTimeout);
+            if (!__all_sync(0xffffffffu, free)) return false;
+            tc_fence_after();
+        }
         tmem_st32(a_taddr + 64u, c0);
         dequant_pair<3>(v, c1);
         tmem_wait_st();
@@ -252,7 +266,7 @@ __device__ __forceinline__ bool dequant_warp(int g, uint32_t raw_row, uint32_t a
         tmem_wait_st();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(afull_bar_at(bar0, g));
+        if (lane == 0) mbar_arrive(afull_bar_at(bar0, g, 1));
     }
     return true;
 }
@@ -293,14 +307,20 @@ __device__ __forceinline__ bool issue_mmas(uint32_t tmem, uint32_t sbase, uint32
         const uint32_t d_tmem = seg1 ? d_seg1 : d_seg0;
         const uint32_t acc0 = (seg1 ? i - kSets >= nA : i > J) ? 1u : 0u;
         ok = mbar_wait_bounded(full_bar_at(bar0, s), sphase, fault, kFaultMmaWaitTimeout) &&
-             mbar_wait_bounded(afull_bar_at(bar0, J), aphase, fault, kFaultMmaWaitTimeout);
+             mbar_wait_bounded(afull_bar_at(bar0, J, 0), aphase, fault, kFaultMmaWaitTimeout);
         if (!ok) break;
         tc_fence_after();
         tc_mma(d_tmem, a_tmem, ds + koff[0], idesc, acc0);
 #pragma unroll
-        for (int k = 1; k < kSteps; ++k) tc_mma(d_tmem, a_tmem + 8u * (uint32_t)k, ds + koff[k], idesc, 1u);
-        tc_commit(empty_bar_at(bar0, s));     // X tile of stage s consumed
-        tc_commit(aempty_bar_at(bar0, J));    // TMEM A stage J consumed
+        for (int k = 1; k < kSteps / 2; ++k) tc_mma(d_tmem, a_tmem + 8u * (uint32_t)k, ds + koff[k], idesc, 1u);
+        tc_commit(aempty_bar_at(bar0, J, 0));     // first half of TMEM A stage J consumed
+        ok = mbar_wait_bounded(afull_bar_at(bar0, J, 1), aphase, fault, kFaultMmaWaitTimeout);
+        if (!ok) break;
+        tc_fence_after();
+#pragma unroll
+        for (int k = kSteps / 2; k < kSteps; ++k) tc_mma(d_tmem, a_tmem + 8u * (uint32_t)k, ds + koff[k], idesc, 1u);
+        tc_commit(empty_bar_at(bar0, s));         // X tile of stage s consumed
+        tc_commit(aempty_bar_at(bar0, J, 1));     // second half consumed
         aphase ^= 1u;
     }
     // completes when every MMA issued above has finished, even after a
@@ -401,10 +421,11 @@ __global__ void __launch_bounds__(kThreads, 1) qmm_q4_0_tc_kernel(const __grid_c
                 mbar_init(full_bar_at(bar0, s), 1);
                 mbar_init(empty_bar_at(bar0, s), 4 + 1);   // the group's 4 dequantizing warps + its issuer's commit
             }
-            for (int a = 0; a < kAStages; ++a) {
-                mbar_init(afull_bar_at(bar0, a), 4);
-                mbar_init(aempty_bar_at(bar0, a), 1);
-            }
+            for (int a = 0; a < kAStages; ++a)
+                for (int h = 0; h < 2; ++h) {
+                    mbar_init(afull_bar_at(bar0, a, h), 4);
+                    mbar_init(aempty_bar_at(bar0, a, h), 1);
+                }
             mbar_init(dfull_bar, kIssuers);
             fence_mbar_init();
         }
