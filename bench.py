@@ -819,6 +819,28 @@ def profile_case(args):
         y = torch.empty(N, device=dev)
         call = lambda i: qbw.qmv_q4_0(ws[i % copies], xb, y, 1, N, K)
         nbytes = ws[0].numel() + 2 * K + 4 * N
+    elif name == "q4_0_stream":
+        # 4096 x 5376 Q4_0 (12.4 MB, below the tensor-core threshold): the
+        # streaming kernel, over 25 rotating copies (310 MB, larger than L2)
+        N, K = 4096, 5376
+        copies = 25
+        ws = [torch.from_numpy(synth.q4_0_weights(N, K, seed=1)).to(dev) for _ in range(copies)]
+        x = torch.from_numpy(synth.activations(K, seed=1)).to(dev)
+        y = torch.empty(N, device=dev)
+        call = lambda i: qbw.qmv_q4_0(ws[i % copies], x, y, 1, N, K)
+        nbytes = ws[0].numel() + 4 * K + 4 * N
+    elif name == "qmm2_qkv":
+        # two tokens over the 16384 x 5376 q|k|v matrix (49.5 MB): the
+        # tensor-core M = 1 kernel's bf16-code form, both tokens in one B
+        N, K, M = 16384, 5376, 2
+        copies = 7
+        ws = [torch.from_numpy(synth.q4_0_weights(N, K, seed=3)).to(dev) for _ in range(copies)]
+        X = torch.from_numpy(synth.activations((M, K), seed=3, dtype="bf16").view(np.int16).copy()).view(
+            torch.bfloat16).to(dev)
+        Y = torch.empty(M, N, dtype=torch.bfloat16, device=dev)
+        work = torch.zeros(256, dtype=torch.uint8, device=dev)
+        call = lambda i: qbw.qmm_q4_0_smallM(ws[i % copies], X, Y, M, N, K, work)
+        nbytes = ws[0].numel() + 2 * M * K + 2 * M * N
     elif name == "q4_k":
         N, K = 21504, 5376
         ws = [torch.from_numpy(synth.q4_k_weights(N, K, seed=1)).to(dev) for _ in range(copies)]
@@ -947,7 +969,8 @@ def main():
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--profile", choices=["q8_0", "q8_0_lmhead", "q4_0", "q4_0_bf16", "q4_k", "gateup", "qmm", "sweep",
-                                          "mixbit2", "mixbit4", "mixbit8", "qmm8", "qmm8_5376"],
+                                          "mixbit2", "mixbit4", "mixbit8", "qmm8", "qmm8_5376", "q4_0_stream",
+                                          "qmm2_qkv"],
                     help="run only one small case (for profiler captures): a single-matrix workload, or the "
                          "sweep's launches over 6 layers")
     args = ap.parse_args()

@@ -27,8 +27,6 @@ namespace qbw {
 namespace {
 
 constexpr int kMixThreads = 256;
-constexpr int kMixRows = 2;          // rows per warp item
-static_assert(kMixRows == 2, "the final store picks acc[0] or acc[1]");
 
 struct MixParams {
     const uint4* qp;        // [N][wq] word groups
@@ -129,42 +127,51 @@ __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commi
 template <int N>
 __device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
 
-// Each lane streams its own 16-byte word groups (one per row) and the 4-byte
-// words that hold their scales (and biases) through a ring of kMixStages
-// stages in shared memory, with cp.async: kMixStages - 1 steps are in flight
-// while it computes one.  A lane reads back only what it copied itself.
-constexpr int kMixStages = 4;
+// Each lane streams its own 16-byte word groups (one per row of the warp's
+// item of ROWS rows) and the 4-byte words that hold their scales (and
+// biases) through a ring of STAGES stages in shared memory, with cp.async:
+// STAGES - 1 steps are in flight while it computes one.  A lane reads back
+// only what it copied itself.  Two shapes of the ring (mix_shape): 4 rows
+// and 3 stages for 4- and 8-bit matrices of K <= 8192 (the activations a row
+// item shares are read once for 4 rows), else 2 rows and 4 stages (smaller
+// rings beside long activation vectors, more CTAs per SM).
+struct MixShape {
+    int rows, stages;
+};
+__host__ __device__ constexpr MixShape mix_shape(int bits, int64_t K) {
+    return (bits >= 4 && K <= 8192) ? MixShape{4, 3} : MixShape{2, 4};
+}
 
 // Scale groups per 16-byte word group: 1 when a group covers it, else E / G.
-template <int BITS, int SW>
+template <int BITS, int SW, int ROWS, int STAGES>
 struct MixRing {
     // [stage][row][lane] word groups, then [stage][row][sw][lane] scale words
     // (and bias words for 4 bits)
-    static constexpr uint32_t kQBytes = kMixStages * kMixRows * 32 * 16;
-    static constexpr uint32_t kSBytes = kMixStages * kMixRows * SW * 32 * 4;
+    static constexpr uint32_t kQBytes = STAGES * ROWS * 32 * 16;
+    static constexpr uint32_t kSBytes = STAGES * ROWS * SW * 32 * 4;
     static constexpr uint32_t kWarpBytes = kQBytes + kSBytes * (BITS == 4 ? 2 : 1);
     __device__ static uint32_t q(uint32_t base, int st, int r, int lane) {
-        return base + (uint32_t)(((st * kMixRows + r) * 32 + lane) * 16);
+        return base + (uint32_t)(((st * ROWS + r) * 32 + lane) * 16);
     }
     __device__ static uint32_t sc(uint32_t base, int st, int r, int k, int lane) {
-        return base + kQBytes + (uint32_t)((((st * kMixRows + r) * SW + k) * 32 + lane) * 4);
+        return base + kQBytes + (uint32_t)((((st * ROWS + r) * SW + k) * 32 + lane) * 4);
     }
     __device__ static uint32_t bi(uint32_t base, int st, int r, int k, int lane) {
         return sc(base, st, r, k, lane) + kSBytes;
     }
 };
 
-// A step of a warp: item `it` (rows it * kMixRows ..), word group c of each
+// A step of a warp: item `it` (rows it * ROWS ..), word group c of each
 // row, in ring stage st.
-template <int BITS, int SW>
+template <int BITS, int SW, int ROWS, int STAGES>
 __device__ __forceinline__ void issue_step(const MixParams& p, uint32_t ring, int st, int it, int c, int items,
                                            int gpr, int lane) {
-    using R = MixRing<BITS, SW>;
+    using R = MixRing<BITS, SW, ROWS, STAGES>;
     constexpr int E = kElems<BITS>;
-    const int n0 = it * kMixRows;
+    const int n0 = it * ROWS;
     const int g0 = c < p.wq ? group_of(p, c * E) : 0;
 #pragma unroll
-    for (int r = 0; r < kMixRows; ++r) {
+    for (int r = 0; r < ROWS; ++r) {
         const bool live = it < items && n0 + r < p.N && c < p.wq;
         const size_t row = live ? (size_t)(n0 + r) : 0;
         cp_async16(R::q(ring, st, r, lane), p.qp + row * p.wq + (live ? c : 0), live);
@@ -198,16 +205,16 @@ __device__ __forceinline__ float ring_half(uint32_t a, uint32_t odd) {
 
 // Dynamic shared memory: x as fp32 in swizzled chunks [K], (4-bit) the per-word
 // sums of x [K / 8], then each warp's ring.
-template <int BITS, int SW>
+template <int BITS, int SW, int ROWS, int STAGES>
 __global__ void __launch_bounds__(kMixThreads) qmv_mixbit_kernel(const __grid_constant__ MixParams p) {
-    using R = MixRing<BITS, SW>;
+    using R = MixRing<BITS, SW, ROWS, STAGES>;
     extern __shared__ __align__(16) float xs[];
     float* xw_sum = xs + p.K;
     constexpr int E = kElems<BITS>, EW = kWordElems<BITS>;
     const int lane = threadIdx.x & 31;
     const int warp = (int)(blockIdx.x * (kMixThreads / 32) + (threadIdx.x >> 5));
     const int nwarps = (int)(gridDim.x * (kMixThreads / 32));
-    const int items = (p.N + kMixRows - 1) / kMixRows;
+    const int items = (p.N + ROWS - 1) / ROWS;
     const int gpr = p.K / p.G;                           // groups per row
     const int S = (p.wq + 31) / 32;                      // steps per item
     const int my_items = warp < items ? (items - warp + nwarps - 1) / nwarps : 0;
@@ -218,8 +225,9 @@ __global__ void __launch_bounds__(kMixThreads) qmv_mixbit_kernel(const __grid_co
     // issued before the activations are waited for and staged
     MixCursor iss;
 #pragma unroll
-    for (int t = 0; t < kMixStages - 1; ++t) {
-        if (t < T) issue_step<BITS, SW>(p, ring, t, warp + iss.j * nwarps, lane + 32 * iss.cs, items, gpr, lane);
+    for (int t = 0; t < STAGES - 1; ++t) {
+        if (t < T)
+            issue_step<BITS, SW, ROWS, STAGES>(p, ring, t, warp + iss.j * nwarps, lane + 32 * iss.cs, items, gpr, lane);
         iss.next(S);
         cp_async_commit();
     }
@@ -256,27 +264,28 @@ __global__ void __launch_bounds__(kMixThreads) qmv_mixbit_kernel(const __grid_co
         }
         __syncthreads();
     }
-    float acc[kMixRows];
+    float acc[ROWS];
 #pragma unroll
-    for (int r = 0; r < kMixRows; ++r) acc[r] = 0.f;
+    for (int r = 0; r < ROWS; ++r) acc[r] = 0.f;
     MixCursor cur;
-    int st = 0, ist = kMixStages - 1;              // stages of the step consumed and issued next
+    int st = 0, ist = STAGES - 1;                  // stages of the step consumed and issued next
     for (int t = 0; t < T; ++t) {
-        // step t + kMixStages - 1 into the stage step t - 1 has freed
-        if (t + kMixStages - 1 < T)
-            issue_step<BITS, SW>(p, ring, ist, warp + iss.j * nwarps, lane + 32 * iss.cs, items, gpr, lane);
+        // step t + STAGES - 1 into the stage step t - 1 has freed
+        if (t + STAGES - 1 < T)
+            issue_step<BITS, SW, ROWS, STAGES>(p, ring, ist, warp + iss.j * nwarps, lane + 32 * iss.cs, items, gpr,
+                                               lane);
         iss.next(S);
-        ist = ist + 1 == kMixStages ? 0 : ist + 1;
+        ist = ist + 1 == STAGES ? 0 : ist + 1;
         cp_async_commit();
-        cp_async_wait<kMixStages - 1>();          // step t's copies have landed
+        cp_async_wait<STAGES - 1>();              // step t's copies have landed
         const int c = lane + 32 * cur.cs;
-        const int n0 = (warp + cur.j * nwarps) * kMixRows;
+        const int n0 = (warp + cur.j * nwarps) * ROWS;
         if (c < p.wq) {
             const int g0 = group_of(p, c * E);
-            uint4 q[kMixRows];
-            uint64_t dot[kMixRows][SW];
+            uint4 q[ROWS];
+            uint64_t dot[ROWS][SW];
 #pragma unroll
-            for (int r = 0; r < kMixRows; ++r) {
+            for (int r = 0; r < ROWS; ++r) {
                 q[r] = ld_shared16(R::q(ring, st, r, lane));
 #pragma unroll
                 for (int k = 0; k < SW; ++k) dot[r][k] = 0ull;
@@ -295,7 +304,7 @@ __global__ void __launch_bounds__(kMixThreads) qmv_mixbit_kernel(const __grid_co
                 }
                 constexpr int kWordsPerGroup = 4 / SW;
 #pragma unroll
-                for (int r = 0; r < kMixRows; ++r) {
+                for (int r = 0; r < ROWS; ++r) {
                     const uint32_t w = wi == 0 ? q[r].x : wi == 1 ? q[r].y : wi == 2 ? q[r].z : q[r].w;
                     word_dot<BITS>(dot[r][wi / kWordsPerGroup], w, xv);
                 }
@@ -303,7 +312,7 @@ __global__ void __launch_bounds__(kMixThreads) qmv_mixbit_kernel(const __grid_co
             // per scale group of the step: acc += sc * dot (+ bi * sum x); the
             // scale element's index parity picks its half of the copied word
 #pragma unroll
-            for (int r = 0; r < kMixRows; ++r) {
+            for (int r = 0; r < ROWS; ++r) {
 #pragma unroll
                 for (int k = 0; k < SW; ++k) {
                     const uint32_t odd = (uint32_t)((n0 + r) * gpr + g0 + k) & 1u;
@@ -317,20 +326,23 @@ __global__ void __launch_bounds__(kMixThreads) qmv_mixbit_kernel(const __grid_co
         if (cur.cs == S - 1) {
             // the item's last step: reduce and store its rows
 #pragma unroll
-            for (int r = 0; r < kMixRows; ++r) {
+            for (int r = 0; r < ROWS; ++r) {
 #pragma unroll
                 for (int o = 16; o > 0; o >>= 1) acc[r] += __shfl_xor_sync(0xffffffffu, acc[r], o);
             }
-            if (lane < kMixRows && n0 + lane < p.N) {
-                const float v = lane == 0 ? acc[0] : acc[1];
+            if (lane < ROWS && n0 + lane < p.N) {
+                float v = acc[0];
+#pragma unroll
+                for (int r = 1; r < ROWS; ++r)
+                    if (lane == r) v = acc[r];
                 if (p.y_bf16) store_out<__nv_bfloat16>(p.y, n0 + lane, v);
                 else store_out<float>(p.y, n0 + lane, v);
             }
 #pragma unroll
-            for (int r = 0; r < kMixRows; ++r) acc[r] = 0.f;
+            for (int r = 0; r < ROWS; ++r) acc[r] = 0.f;
         }
         cur.next(S);
-        st = st + 1 == kMixStages ? 0 : st + 1;
+        st = st + 1 == STAGES ? 0 : st + 1;
     }
     cp_async_wait<0>();
 }
@@ -356,27 +368,27 @@ __global__ void dequant_mixbit_kernel(const uint32_t* qp, const uint16_t* sc, co
     }
 }
 
-template <int BITS, int SW>
+template <int BITS, int SW, int ROWS, int STAGES>
 cudaError_t launch_mix(const MixParams& p, int sm_count, cudaStream_t stream) {
     const size_t smem = qmv_mixbit_smem_bytes(BITS, p.K, p.G);
-    static_assert(MixRing<BITS, SW>::kWarpBytes * (kMixThreads / 32) ==
-                      (size_t)kMixStages * kMixRows * 32 * (16 + SW * 4 * (BITS == 4 ? 2 : 1)) * (kMixThreads / 32),
+    static_assert(MixRing<BITS, SW, ROWS, STAGES>::kWarpBytes * (kMixThreads / 32) ==
+                      (size_t)STAGES * ROWS * 32 * (16 + SW * 4 * (BITS == 4 ? 2 : 1)) * (kMixThreads / 32),
                   "ring size");
     static thread_local int prepared = -1;
     int dev = 0;
     cudaGetDevice(&dev);
     if (prepared != dev) {
-        cudaError_t e = cudaFuncSetAttribute(qmv_mixbit_kernel<BITS, SW>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        cudaError_t e = cudaFuncSetAttribute(qmv_mixbit_kernel<BITS, SW, ROWS, STAGES>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              (int)kMixMaxSmem);
         if (e != cudaSuccess) return e;
         prepared = dev;
     }
     int per_sm = 0;
-    cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, qmv_mixbit_kernel<BITS, SW>, kMixThreads,
+    cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, qmv_mixbit_kernel<BITS, SW, ROWS, STAGES>, kMixThreads,
                                                                   smem);
     if (e != cudaSuccess) return e;
     if (per_sm < 1) per_sm = 1;
-    const int items = (p.N + kMixRows - 1) / kMixRows;
+    const int items = (p.N + ROWS - 1) / ROWS;
     const int warps_per_cta = kMixThreads / 32;
     int ctas = sm_count * per_sm;
     if (ctas * warps_per_cta > items) ctas = (items + warps_per_cta - 1) / warps_per_cta;
@@ -390,21 +402,29 @@ cudaError_t launch_mix(const MixParams& p, int sm_count, cudaStream_t stream) {
     cfg.stream = stream;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, qmv_mixbit_kernel<BITS, SW>, p);
+    return cudaLaunchKernelEx(&cfg, qmv_mixbit_kernel<BITS, SW, ROWS, STAGES>, p);
 }
 
-template <int BITS>
+template <int BITS, int ROWS, int STAGES>
 cudaError_t launch_mix_sw(const MixParams& p, int sm_count, cudaStream_t stream) {
     constexpr int E = kElems<BITS>;
     const int sw = p.G >= E ? 1 : E / p.G;
-    if (sw == 1) return launch_mix<BITS, 1>(p, sm_count, stream);
+    if (sw == 1) return launch_mix<BITS, 1, ROWS, STAGES>(p, sm_count, stream);
     if constexpr (E >= 32) {
-        if (sw == 2) return launch_mix<BITS, 2>(p, sm_count, stream);
+        if (sw == 2) return launch_mix<BITS, 2, ROWS, STAGES>(p, sm_count, stream);
     }
     if constexpr (E >= 64) {
-        if (sw == 4) return launch_mix<BITS, 4>(p, sm_count, stream);
+        if (sw == 4) return launch_mix<BITS, 4, ROWS, STAGES>(p, sm_count, stream);
     }
     return cudaErrorInvalidValue;
+}
+
+template <int BITS>
+cudaError_t launch_mix_shape(const MixParams& p, int sm_count, cudaStream_t stream) {
+    if (mix_shape(BITS, p.K).rows == 4) {
+        if constexpr (BITS >= 4) return launch_mix_sw<BITS, 4, 3>(p, sm_count, stream);
+    }
+    return launch_mix_sw<BITS, 2, 4>(p, sm_count, stream);
 }
 
 }  // namespace
@@ -412,7 +432,8 @@ cudaError_t launch_mix_sw(const MixParams& p, int sm_count, cudaStream_t stream)
 // x, the 4-bit per-word sums, then the 8 warps' rings
 size_t qmv_mixbit_smem_bytes(int bits, int64_t K, int64_t group) {
     const int64_t E = 128 / bits, sw = group >= E ? 1 : E / group;
-    const size_t ring = (size_t)kMixStages * kMixRows * 32 * (16 + (size_t)sw * 4 * (bits == 4 ? 2 : 1));
+    const MixShape sh = mix_shape(bits, K);
+    const size_t ring = (size_t)sh.stages * sh.rows * 32 * (16 + (size_t)sw * 4 * (bits == 4 ? 2 : 1));
     return (((size_t)K * 4 + (bits == 4 ? (size_t)(K / 8) * 4 : 0)) + 127) / 128 * 128 + (kMixThreads / 32) * ring;
 }
 
@@ -434,9 +455,9 @@ cudaError_t launch_qmv_mixbit(int bits, const void* qp, const void* sc, const vo
     p.x_bf16 = x_bf16;
     p.y_bf16 = y_bf16;
     switch (bits) {
-        case 2: return launch_mix_sw<2>(p, sm_count, stream);
-        case 4: return launch_mix_sw<4>(p, sm_count, stream);
-        case 8: return launch_mix_sw<8>(p, sm_count, stream);
+        case 2: return launch_mix_shape<2>(p, sm_count, stream);
+        case 4: return launch_mix_shape<4>(p, sm_count, stream);
+        case 8: return launch_mix_shape<8>(p, sm_count, stream);
         default: return cudaErrorInvalidValue;
     }
 }
