@@ -650,7 +650,13 @@ def gpu_arm(args):
     # step's result out to pinned host memory, every step
     h_in = torch.from_numpy(x0.view(np.int16).copy()).view(torch.bfloat16).pin_memory()
     h_out = torch.empty(HIDDEN, dtype=torch.bfloat16).pin_memory()
-    e2e_steps = max(3, min(args.steps, 200))
+    e2e_steps = max(50, min(args.steps, 200))
+    with torch.cuda.stream(stream):
+        for _ in range(3):                # untimed: the first host copies of the pinned buffers
+            sweep.h.copy_(h_in, non_blocking=True)
+            graph.replay()
+            h_out.copy_(sweep.h, non_blocking=True)
+            stream.synchronize()
     torch.cuda.synchronize()
     t0 = time.perf_counter()
     with torch.cuda.stream(stream):
