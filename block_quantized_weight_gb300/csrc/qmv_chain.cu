@@ -20,6 +20,7 @@
 // The launch is cooperative: all CTAs are resident together, which the grid
 // barrier requires.
 #include <algorithm>
+#include <cstddef>
 #include <cstdint>
 
 #include "qbw_device.cuh"
@@ -95,11 +96,29 @@ __device__ __forceinline__ unsigned long long wait_share(const unsigned long lon
     }
 }
 
+// A step descriptor's scalar fields (the 64 bytes after its two tensor maps),
+// as the decode warps keep them in shared memory.
+struct StepScalars {
+    const void* x;
+    void* y;
+    const uint8_t* w[2];
+    int32_t N, K, nmat, y_bf16;
+    int32_t tiles, groups, units, reserved;
+};
+static_assert(sizeof(StepScalars) == 64 && offsetof(ChainStepDesc, x) == 2 * sizeof(CUtensorMap) &&
+                  offsetof(ChainStepDesc, reserved) == offsetof(ChainStepDesc, x) + 60,
+              "StepScalars mirrors the fields of ChainStepDesc after its tensor maps");
+
+__device__ __forceinline__ void cp_async4_sh(uint32_t dst, const void* src) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(dst), "l"(src) : "memory");
+}
+
 // the step's unit range of this CTA and its first and last tiles
 struct StepRange {
     int G, nmat, GU, u0, u1, n, tile0, tile1;
     bool contrib0, fin1;
-    __device__ __forceinline__ void init(const ChainStepDesc& st, int cta, int ctas) {
+    template <typename Desc>
+    __device__ __forceinline__ void init(const Desc& st, int cta, int ctas) {
         G = st.groups;
         nmat = st.nmat;
         GU = G * nmat;
@@ -258,8 +277,23 @@ __global__ void __launch_bounds__(kThreads, 1) qmv_chain_kernel(const __grid_con
         const int row = 32 * q + lane;
         int I_base = 0;     // this CTA's units in the earlier steps
         int k = 0;          // the set's units so far, over all steps
+        // Step s's scalar fields in slot s % 2 of a 128-byte cache in the second
+        // B buffer (which the bf16 8-bit form leaves unused): threads 0..15 copy
+        // step s + 1's while step s runs, and wait for them before the step's
+        // last barrier, so no step starts on a read of device memory.
+        const uint32_t dcache = sbase + kOffB2;
+        auto fetch_scalars = [&](int s2) {
+            if (threadIdx.x < 16 && s2 < p.nsteps)
+                cp_async4_sh(dcache + 64u * (uint32_t)(s2 & 1) + 4u * threadIdx.x,
+                             reinterpret_cast<const uint32_t*>(&p.steps[s2].x) + threadIdx.x);
+            asm volatile("cp.async.commit_group;" ::: "memory");
+        };
+        fetch_scalars(0);
+        asm volatile("cp.async.wait_group 0;" ::: "memory");
+        dequant_sync();
         for (int s = 0; s < p.nsteps; ++s) {
-            const ChainStepDesc& st = p.steps[s];
+            const StepScalars& st = *reinterpret_cast<const StepScalars*>(smem + kOffB2 + 64u * (uint32_t)(s & 1));
+            fetch_scalars(s + 1);
             StepRange r;
             r.init(st, cta, ctas);
             const int G = r.G, nmat = r.nmat, u0 = r.u0, n = r.n, tile0 = r.tile0;
@@ -532,6 +566,7 @@ __global__ void __launch_bounds__(kThreads, 1) qmv_chain_kernel(const __grid_con
             for (int i = threadIdx.x; i < kSets * kMaxLocalTiles * 2 * kTileRows; i += kDequantThreads) part[i] = 0.f;
             if (threadIdx.x < 4) qcount[threadIdx.x] = 0u;
             I_base += n;
+            asm volatile("cp.async.wait_group 0;" ::: "memory");     // step s + 1's scalars landed
             if (s + 1 < p.nsteps) {
                 // the step's outputs, written by every CTA, are the next steps' inputs
                 __threadfence();
