@@ -115,3 +115,23 @@ def test_deterministic(qbw):
         a = run(qbw, bits, qp, sc, bi, G, x, N, K)
         b = run(qbw, bits, qp, sc, bi, G, x, N, K)
         assert torch.equal(a.view(torch.int32), b.view(torch.int32))
+
+
+@pytest.mark.parametrize("bits,K", [(2, 41728), (4, 36864), (8, 47872)])
+def test_largest_k(qbw, oracle, bits, K):
+    # the longest rows each format takes with groups of 16 (the activations and
+    # the copy rings fill one CTA's 227 KB of shared memory), and one step more
+    # is rejected
+    N, G = 300, 16
+    qp, sc, bi = synth.mixbit_weights(bits, N, K, G, seed=bits + 40)
+    x = synth.activations(K, seed=bits + 41, dtype="bf16")
+    y = run(qbw, bits, qp, sc, bi, G, x, N, K)
+    y_ref, _, S2 = oracle.qmv_mixbit(bits, qp, sc, bi, G, x, N, K)
+    check_matvec(to_f64(y), y_ref, S2, what=f"mixbit{bits} K={K}")
+    K2 = K + 256
+    qp2, sc2, bi2 = synth.mixbit_weights(bits, 2, K2, G, seed=1)
+    y2 = torch.empty(2, dtype=torch.float32, device="cuda")
+    with pytest.raises(qbw.QbwError) as err:
+        qbw.qmv_mixbit(bits, dev(qp2), dev(sc2), dev(bi2), G, dev_act(synth.activations(K2, seed=2, dtype="bf16")),
+                       y2, 1, 2, K2)
+    assert err.value.status == 2           # QBW_ESHAPE
