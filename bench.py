@@ -863,6 +863,15 @@ def profile_case(args):
         y = torch.empty(N, device=dev)
         call = lambda i: qbw.qmv_gateup_q4_0(wg[i % 2], wu[i % 2], xb, y, 1, N, K)
         nbytes = 2 * wg[0].numel() + 2 * K + 4 * N
+    elif name == "chain":
+        # the sweep's steps over 2 layers as one cooperative chain launch
+        sweep = Sweep(torch, qbw, dev, layers=2)
+        sweep.fill()
+        sweep.h.copy_(torch.from_numpy(synth.activations(HIDDEN, seed=SEED, dtype="bf16").view(np.int16).copy())
+                      .view(torch.bfloat16).to(dev))
+        chain = qbw.Chain(sweep_chain_steps(sweep))
+        call = lambda i: chain.run()
+        nbytes = sum(b for _, _, b in sweep._specs)
     elif name == "sweep":
         # the sweep's own launches over a few layers (1.6 GB of weights)
         sweep = Sweep(torch, qbw, dev, layers=6)
@@ -976,7 +985,7 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--profile", choices=["q8_0", "q8_0_lmhead", "q4_0", "q4_0_bf16", "q4_k", "gateup", "qmm", "sweep",
                                           "mixbit2", "mixbit4", "mixbit8", "qmm8", "qmm8_5376", "q4_0_stream",
-                                          "qmm2_qkv"],
+                                          "qmm2_qkv", "chain"],
                     help="run only one small case (for profiler captures): a single-matrix workload, or the "
                          "sweep's launches over 6 layers")
     args = ap.parse_args()
