@@ -427,7 +427,8 @@ __device__ __forceinline__ void qmv_tc_body(const QtcParams& p) {
                 uint32_t dd[4];
     #pragma unroll
                 for (int P = 0; P < 4; ++P) dd[P] = (FMT == kFmtQ4K) ? v[P] : scale_pair(v, P);
-                uint32_t c0[32], c1[32];
+                uint32_t c0[32];
+                [[maybe_unused]] uint32_t c1[32];     // not used by the one-operand Q4_K form
                 // B chunk of a B-writing lane: x_hi and x_lo as bf16, written in the
                 // K-half its slot belongs to
                 uint4 bhi = make_uint4(0u, 0u, 0u, 0u), blo = bhi;
@@ -479,7 +480,8 @@ __device__ __forceinline__ void qmv_tc_body(const QtcParams& p) {
                 // 8-bit form: this unit's group in the table; the B-writing lanes'
                 // pieces of their slot
                 int cur_sl = 0;
-                uint2 bp0 = make_uint2(0u, 0u), bp1 = bp0, bp2 = bp0;
+                uint2 bp0 = make_uint2(0u, 0u);
+                [[maybe_unused]] uint2 bp1 = bp0, bp2 = bp0;     // the 8-bit forms' second and third pieces
                 if constexpr (F8) {
                     cur_sl = g - xg0;
                     if (cur_sl < 0) cur_sl += G;
