@@ -315,7 +315,7 @@ __global__ void __launch_bounds__(kMixThreads) qmv_mixbit_kernel(const __grid_co
             for (int r = 0; r < ROWS; ++r) {
 #pragma unroll
                 for (int k = 0; k < SW; ++k) {
-                    const uint32_t odd = (uint32_t)((n0 + r) * gpr + g0 + k) & 1u;
+                    const uint32_t odd = ((uint32_t)(n0 + r) * (uint32_t)gpr + (uint32_t)(g0 + k)) & 1u;
                     const float2 d = unpack2f(dot[r][k]);
                     acc[r] = fmaf(ring_half(R::sc(ring, st, r, k, lane), odd), d.x + d.y, acc[r]);
                     if constexpr (BITS == 4)
