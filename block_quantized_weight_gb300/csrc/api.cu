@@ -35,6 +35,9 @@ cudaError_t launch_qmv_tc(int fmt, int nmat, int ntok, const CUtensorMap* tmap_w
                           const void* x, int x_bf16, void* y, int y_bf16, int N, int K, int sm_count,
                           unsigned int* fault, cudaStream_t stream, const QtcNextLaunch* next = nullptr);
 int qmm_tc_tile_rows();
+bool qmv_mix4_tc_supported(int64_t N, int64_t K, int sm_count);
+cudaError_t launch_qmv_mix4_tc(const CUtensorMap* tmaps, const void* qp, const void* sc, const void* x, void* y,
+                               int y_bf16, int N, int K, int sm_count, unsigned int* fault, cudaStream_t stream);
 bool qmv_chain_step_supported(int nmat, int64_t N, int64_t K, int ctas);
 void qmv_chain_fill_step(ChainStepDesc* d, int nmat, int64_t N, int64_t K);
 int qmv_chain_ctas(int sm_count);
@@ -243,6 +246,39 @@ bool encode_q4_tile_map(CUtensorMap* m, const void* w, int64_t N, int64_t K) {
     return enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT64, 2, const_cast<void*>(w), dims, strides, box, estr,
                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// The int4-affine mixed-bit matrices with groups of 32, for the tensor-core
+// kernel: m[0] the codes as [N][K / 16] 8-byte words, box (16, 128) (one
+// 256-element K-group of a 128-row tile, 128 bytes per row) with the 128-byte
+// swizzle; m[1], m[2] the fp16 scales and biases as [N][K / 128] 8-byte
+// words, box (2, 128) (the group's 8 of each per row).  Needs K % 256 == 0 and
+// 16-byte aligned arrays.
+bool encode_mix4_maps(CUtensorMap* m, const void* qp, const void* sc, const void* bi, int64_t N, int64_t K) {
+    PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+    if (!enc) return false;
+    const cuuint32_t rows = (cuuint32_t)qmm_tc_tile_rows();
+    cuuint32_t estr[2] = {1, 1};
+    {
+        cuuint64_t dims[2] = {(cuuint64_t)(K / 16), (cuuint64_t)N};
+        cuuint64_t strides[1] = {(cuuint64_t)(K / 2)};
+        cuuint32_t box[2] = {16, rows};
+        if (enc(&m[0], CU_TENSOR_MAP_DATA_TYPE_UINT64, 2, const_cast<void*>(qp), dims, strides, box, estr,
+                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return false;
+    }
+    const void* sb[2] = {sc, bi};
+    for (int i = 0; i < 2; ++i) {
+        cuuint64_t dims[2] = {(cuuint64_t)(K / 128), (cuuint64_t)N};
+        cuuint64_t strides[1] = {(cuuint64_t)(K / 16)};
+        cuuint32_t box[2] = {2, rows};
+        if (enc(&m[1 + i], CU_TENSOR_MAP_DATA_TYPE_UINT64, 2, const_cast<void*>(sb[i]), dims, strides, box, estr,
+                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return false;
+    }
+    return true;
 }
 
 bool encode_x_map(CUtensorMap* m, const void* X, int64_t M, int64_t K, int nt) {
@@ -597,6 +633,13 @@ static qbw_status mixbit_args(qbw_mixbit kind, const void* qp, const void* sc, c
     return QBW_OK;
 }
 
+// Bytes of int4 codes from which the mixed-bit product takes the tensor cores:
+// below them the CUDA-core kernel's shorter start-up wins, and more so for
+// short rows (GB300, CUDA-graph replay, groups of 32, bf16 x: 2048 x 5376 6.8
+// vs 7.7 us, 4096 x 4096 6.1 vs 6.0 us, 4096 x 2048 5.5 vs 3.6 us, 16384 x 2048
+// 7.3 vs 8.5 us, 21504 x 5376 14.5 vs 27.3 us).
+constexpr double mix4_tc_min_bytes(int64_t K) { return K > 4096 ? 5e6 : 10e6; }
+
 qbw_status qmv_mixbit(qbw_mixbit kind, const void* qp, const void* sc, const void* bi, int64_t group, const void* x,
                       qbw_dtype xt, void* y, qbw_dtype yt, int64_t M, int64_t N, int64_t K, void* stream) {
     size_t wbytes = 0;
@@ -614,8 +657,21 @@ qbw_status qmv_mixbit(qbw_mixbit kind, const void* qp, const void* sc, const voi
     DeviceInfo* di = nullptr;
     st = device_info(&di);
     if (st != QBW_OK) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    // int4-affine with groups of 32 and bf16 x: the tensor-core 8-bit form from
+    // mix4_tc_min_bytes of codes
+    if (kind == QBW_MIXBIT_INT4_AFFINE && group == 32 && xt == QBW_BF16 && K % 256 == 0 &&
+        (double)wbytes >= mix4_tc_min_bytes(K) && (uintptr_t)sc % 16 == 0 && (uintptr_t)bi % 16 == 0 &&
+        qmv_mix4_tc_supported(N, K, di->sm_count)) {
+        CUtensorMap maps[3];
+        if (encode_mix4_maps(maps, qp, sc, bi, N, K)) {
+            cudaError_t e = launch_qmv_mix4_tc(maps, qp, sc, x, y, yt == QBW_BF16, (int)N, (int)K, di->sm_count,
+                                               di->fault, s);
+            return e == cudaSuccess ? QBW_OK : QBW_ECUDA;
+        }
+    }
     cudaError_t e = launch_qmv_mixbit((int)kind, qp, sc, bi, (int)group, x, xt == QBW_BF16, y, yt == QBW_BF16, (int)N,
-                                      (int)K, di->sm_count, static_cast<cudaStream_t>(stream));
+                                      (int)K, di->sm_count, s);
     return e == cudaSuccess ? QBW_OK : QBW_ECUDA;
 }
 

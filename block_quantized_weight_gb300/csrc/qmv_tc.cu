@@ -98,9 +98,15 @@ __device__ __forceinline__ void qmv_tc_body(const QtcParams& p) {
     static_assert(NCH <= 2, "at most two sums per row");
     static_assert(FMT == kFmtQ4 || (NMAT == 1 && NTOK == 1), "Q4_K: one matrix, one token");
     static_assert(F8 == 0 || ((F8 == 2 || F8 == 3) && NTOK == 1), "8-bit form: one token");
+    // the int4-affine mixed-bit matrices: 8-bit form with bf16 activations only
+    // (their scales and biases take the B2 region)
+    constexpr bool MIX = FMT == kFmtMix4;
+    static_assert(!MIX || F8 == 2, "mixed-bit form: two pieces");
     // the 8-bit form of Q4_K: one A operand (codes 0..15), 8 K-steps per unit
     constexpr bool Q4K8 = F8 != 0 && FMT == kFmtQ4K;
-    constexpr int kSteps = Q4K8 ? 8 : 16;
+    // one A operand of codes 0..15 (Q4_K or the mixed-bit form)
+    constexpr bool ONE_OP = Q4K8 || MIX;
+    constexpr int kSteps = ONE_OP ? 8 : 16;
     extern __shared__ __align__(1024) uint8_t smem[];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int ctas = (int)gridDim.x, cta = (int)blockIdx.x;
@@ -125,7 +131,9 @@ __device__ __forceinline__ void qmv_tc_body(const QtcParams& p) {
 
     // zero B operands (only their fixed activation positions are ever written
     // again) and the per-set partial rows
-    for (int i = threadIdx.x; i < (int)(2 * kSets * kBBytes / 16); i += kThreads)     // B and B2
+    // (B2 too, except where it is the mixed-bit form's scale ring, which the
+    // copies below start filling at once)
+    for (int i = threadIdx.x; i < (int)((MIX ? 1 : 2) * kSets * kBBytes / 16); i += kThreads)
         sts128(sbase + kOffB + 16u * (uint32_t)i, make_uint4(0u, 0u, 0u, 0u));
     for (int i = threadIdx.x; i < kSets * kMaxLocalTiles * 2 * kTileRows; i += kThreads) part[i] = 0.f;
     for (int i = threadIdx.x; i < kProducerWarp * 32 * 3; i += kThreads)       // acc_q and fixups
@@ -150,7 +158,8 @@ __device__ __forceinline__ void qmv_tc_body(const QtcParams& p) {
         asm volatile("bar.arrive 1, %0;" ::"n"(kThreads) : "memory");
         if (lane == 0) {
             prefetch_tmap(&p.tmap_w[0]);
-            if (NMAT == 2) prefetch_tmap(&p.tmap_w[1]);
+            if (NMAT == 2 || MIX) prefetch_tmap(&p.tmap_w[1]);
+            if constexpr (MIX) prefetch_tmap(&p.tmap_bi);
             // weights do not depend on the preceding grid: start streaming now
             for (int i = 0; i < n && ok; ++i) {
                 const int s = i % kStages;
@@ -159,9 +168,20 @@ __device__ __forceinline__ void qmv_tc_body(const QtcParams& p) {
                                            kFaultBulkWaitTimeout);
                 if (!ok) break;
                 const int u = u0 + i, ug = u / NMAT, mat = u - ug * NMAT, t = ug / G, g = ug - t * G;
-                mbar_arrive_expect_tx(full_bar(bar0, s), kRawStageBytes);
-                tma_load_2d(sbase + (uint32_t)s * kRawStageBytes, &p.tmap_w[mat], g * kGroupWords, t * kTileRows,
-                            full_bar(bar0, s), policy_evict_first());
+                if constexpr (MIX) {
+                    // codes (16 words of a row), then scales and biases (2 words each)
+                    const uint32_t sdst = sbase + kOffB2 + (uint32_t)s * kMixScaleBytes;
+                    mbar_arrive_expect_tx(full_bar(bar0, s), kMixStageBytes);
+                    tma_load_2d(sbase + (uint32_t)s * kRawStageBytes, &p.tmap_w[0], g * 16, t * kTileRows,
+                                full_bar(bar0, s), policy_evict_first());
+                    tma_load_2d(sdst, &p.tmap_w[1], g * 2, t * kTileRows, full_bar(bar0, s), policy_evict_first());
+                    tma_load_2d(sdst + kMixScaleBytes / 2, &p.tmap_bi, g * 2, t * kTileRows, full_bar(bar0, s),
+                                policy_evict_first());
+                } else {
+                    mbar_arrive_expect_tx(full_bar(bar0, s), kRawStageBytes);
+                    tma_load_2d(sbase + (uint32_t)s * kRawStageBytes, &p.tmap_w[mat], g * kGroupWords,
+                                t * kTileRows, full_bar(bar0, s), policy_evict_first());
+                }
             }
             // every copy of this launch is issued: warm L2 with the first units
             // (a ring's worth) that this CTA index loads in the next launch
@@ -245,7 +265,7 @@ __device__ __forceinline__ void qmv_tc_body(const QtcParams& p) {
         const uint32_t lanes = (uint32_t)(32 * q) << 16;
         const uint32_t a_taddr = tmem + lanes + (uint32_t)set * kACols;
         const uint32_t d_taddr = tmem + lanes + kDCol + 32u * (uint32_t)set;   // + 16 (k % 2)
-        const uint32_t raw_row = (uint32_t)(32 * q + lane) * 144u;
+        const uint32_t raw_row = (uint32_t)(32 * q + lane) * (MIX ? 128u : 144u);
         const uint32_t bbuf = sbase + kOffB + (uint32_t)set * kBBytes;
         // The lane's 8-element slot xl of the group's activations: Q4_0, lanes
         // 0..7 load slots 8q .. 8q + 7 and write them into B; Q4_K, every lane
@@ -280,7 +300,7 @@ __device__ __forceinline__ void qmv_tc_body(const QtcParams& p) {
         if constexpr (F8) {
             const int cnt = n > 0 ? min(G, (u1 - 1) / NMAT - u0 / NMAT + 1) : 0;
             if (cnt > kXtGroups) record_fault(p.fault, kFaultPlan);
-            build_x_table<false, F8, Q4K8>(sbase, p.x, xg0, G, min(cnt, kXtGroups), warp, lane, kProducerWarp);
+            build_x_table<false, F8, ONE_OP>(sbase, p.x, xg0, G, min(cnt, kXtGroups), warp, lane, kProducerWarp);
             asm volatile("bar.sync 2, %0;" ::"n"(kProducerWarp * 32) : "memory");
         }
         bool counted = !contrib0;
@@ -334,8 +354,13 @@ __device__ __forceinline__ void qmv_tc_body(const QtcParams& p) {
                     if (sl < 0) sl += G;
                     if (sl >= kXtGroups) sl = 0;
                     if (!group_flagged(sbase, sl)) continue;     // no residuals
-                    corr += unit_correction<FMT, F8 ? F8 : 2, false>(p.w[m] + nrow * p.row_bytes + (int64_t)g * 144,
-                                                                      p.x, g, sbase, sl);
+                    if constexpr (MIX)
+                        corr += unit_correction<FMT, 2, false>(
+                            p.w[0] + nrow * (p.K / 2) + (int64_t)g * 128, p.x, g, sbase, sl,
+                            reinterpret_cast<const uint8_t*>(p.msc + nrow * (p.K / 32) + (int64_t)g * 8));
+                    else
+                        corr += unit_correction<FMT, F8 ? F8 : 2, false>(
+                            p.w[m] + nrow * p.row_bytes + (int64_t)g * 144, p.x, g, sbase, sl);
                 }
                 return corr;
             };
@@ -378,6 +403,7 @@ __device__ __forceinline__ void qmv_tc_body(const QtcParams& p) {
                 }
             };
             uint32_t pend_dd[4] = {0u, 0u, 0u, 0u};
+            [[maybe_unused]] uint32_t pend_bb[4] = {0u, 0u, 0u, 0u};     // the mixed-bit form's biases
             float pend_sx = 0.f;     // Q4_K: the previous unit's sub-block sum of this lane's group of 4
             int pend_sl = 0;         // 8-bit form: the previous unit's table slot
             // 8-bit form, a unit of a flagged group (the sign of its c_0; after
@@ -414,19 +440,42 @@ __device__ __forceinline__ void qmv_tc_body(const QtcParams& p) {
                 }
                 const uint32_t src = sbase + (uint32_t)s * kRawStageBytes + raw_row;
                 uint32_t v[36];
+                uint32_t dd[4];
+                [[maybe_unused]] uint32_t bb[4];
+                if constexpr (MIX) {
+                    // the row's 8 swizzled code chunks, then its scales and biases
     #pragma unroll
-                for (int j = 0; j < 9; ++j) {
-                    const uint4 w = lds128(src + 16u * (uint32_t)j);
-                    v[4 * j] = w.x;
-                    v[4 * j + 1] = w.y;
-                    v[4 * j + 2] = w.z;
-                    v[4 * j + 3] = w.w;
+                    for (int j = 0; j < 8; ++j) {
+                        const uint4 w = lds128(src + ((uint32_t)(j ^ (row & 7)) << 4));
+                        v[4 * j] = w.x;
+                        v[4 * j + 1] = w.y;
+                        v[4 * j + 2] = w.z;
+                        v[4 * j + 3] = w.w;
+                    }
+                    const uint32_t ssrc = sbase + kOffB2 + (uint32_t)s * kMixScaleBytes + (uint32_t)row * 16u;
+                    const uint4 sv = lds128(ssrc), bv = lds128(ssrc + kMixScaleBytes / 2);
+                    dd[0] = sv.x;
+                    dd[1] = sv.y;
+                    dd[2] = sv.z;
+                    dd[3] = sv.w;
+                    bb[0] = bv.x;
+                    bb[1] = bv.y;
+                    bb[2] = bv.z;
+                    bb[3] = bv.w;
+                } else {
+    #pragma unroll
+                    for (int j = 0; j < 9; ++j) {
+                        const uint4 w = lds128(src + 16u * (uint32_t)j);
+                        v[4 * j] = w.x;
+                        v[4 * j + 1] = w.y;
+                        v[4 * j + 2] = w.z;
+                        v[4 * j + 3] = w.w;
+                    }
+    #pragma unroll
+                    for (int P = 0; P < 4; ++P) dd[P] = (FMT == kFmtQ4K) ? v[P] : scale_pair(v, P);
                 }
                 __syncwarp();
                 if (lane == 0) mbar_arrive(empty_bar(bar0, s));     // raw rows of stage s read
-                uint32_t dd[4];
-    #pragma unroll
-                for (int P = 0; P < 4; ++P) dd[P] = (FMT == kFmtQ4K) ? v[P] : scale_pair(v, P);
                 uint32_t c0[32];
                 [[maybe_unused]] uint32_t c1[32];     // not used by the one-operand Q4_K form
                 // B chunk of a B-writing lane: x_hi and x_lo as bf16, written in the
@@ -491,6 +540,10 @@ __device__ __forceinline__ void qmv_tc_body(const QtcParams& p) {
                         const uint4 tq = lds128(sbase + kOffXt + ch * 16u);
                         bp0 = make_uint2(tq.x, tq.y);
                         bp1 = make_uint2(tq.z, tq.w);
+                        if constexpr (MIX) {     // the code words' order of weights
+                            bp0 = perm_mix4(bp0);
+                            bp1 = perm_mix4(bp1);
+                        }
                         if constexpr (F8 == 3)
                             asm volatile("ld.shared.v2.b32 {%0, %1}, [%2];"
                                          : "=r"(bp2.x), "=r"(bp2.y)
@@ -499,7 +552,8 @@ __device__ __forceinline__ void qmv_tc_body(const QtcParams& p) {
                 }
                 const uint32_t prev = (uint32_t)(k - 1) & 1u;     // completion parity of the previous unit
                 // ---- half 0: K 0..127 (block pairs 0, 1; B atoms 0, 1 written by warps 0, 1)
-                if constexpr (Q4K8) codes_q4k_e4m3<0>(v, c0);
+                if constexpr (MIX) codes_mix4_e4m3<0>(v, c0);
+                else if constexpr (Q4K8) codes_q4k_e4m3<0>(v, c0);
                 else if constexpr (F8) codes_pair_e4m3<0>(v, c0);
                 else codes_pair<FMT, 0>(v, c0);
                 if (k > 0) {
@@ -511,7 +565,7 @@ __device__ __forceinline__ void qmv_tc_body(const QtcParams& p) {
                     tc_fence_after();
                 }
                 if (bwriter && bhalf == 0) {
-                    if constexpr (Q4K8) {
+                    if constexpr (ONE_OP) {
                         sts64(k8_p0, bp0);
                         sts64(k8_p1, bp1);
                         if constexpr (F8 == 3) sts64(k8_p1 + (kOffB2 - kOffB), bp2);
@@ -531,7 +585,7 @@ __device__ __forceinline__ void qmv_tc_body(const QtcParams& p) {
                     fence_proxy_async_smem();     // B visible to the tensor core
                 }
                 tmem_st32(a_taddr, c0);
-                if constexpr (!Q4K8) {
+                if constexpr (!ONE_OP) {
                     if constexpr (F8) codes_pair_e4m3<1>(v, c1);
                     else codes_pair<FMT, 1>(v, c1);
                     tmem_wait_st();
@@ -542,7 +596,8 @@ __device__ __forceinline__ void qmv_tc_body(const QtcParams& p) {
                 __syncwarp();
                 if (lane == 0) mbar_arrive(afull_bar(bar0, set, 0));
                 // ---- half 1: K 128..255 (block pairs 2, 3; B atoms 2, 3 written by warps 2, 3)
-                if constexpr (Q4K8) codes_q4k_e4m3<1>(v, c0);
+                if constexpr (MIX) codes_mix4_e4m3<1>(v, c0);
+                else if constexpr (Q4K8) codes_q4k_e4m3<1>(v, c0);
                 else if constexpr (F8) codes_pair_e4m3<2>(v, c0);
                 else codes_pair<FMT, 2>(v, c0);
                 if (k > 0) {
@@ -554,7 +609,7 @@ __device__ __forceinline__ void qmv_tc_body(const QtcParams& p) {
                     tc_fence_after();
                 }
                 if (bwriter && bhalf == 1) {
-                    if constexpr (Q4K8) {
+                    if constexpr (ONE_OP) {
                         sts64(k8_p0, bp0);
                         sts64(k8_p1, bp1);
                         if constexpr (F8 == 3) sts64(k8_p1 + (kOffB2 - kOffB), bp2);
@@ -573,7 +628,7 @@ __device__ __forceinline__ void qmv_tc_body(const QtcParams& p) {
                     }
                     fence_proxy_async_smem();
                 }
-                if constexpr (Q4K8) {
+                if constexpr (ONE_OP) {
                     tmem_st32(a_taddr + 32u, c0);
                 } else {
                     tmem_st32(a_taddr + 64u, c0);
@@ -593,7 +648,15 @@ __device__ __forceinline__ void qmv_tc_body(const QtcParams& p) {
                     tmem_ld16(d_taddr + 16u * prev, dv);
                     tmem_wait_ld();
                     float r0, r1 = 0.f;
-                    if constexpr (Q4K8) {
+                    if constexpr (MIX) {
+                        float c[8], sx[8];
+                        table_f8(sbase, kOffXc, pend_sl, c);
+                        table_f8(sbase, kOffXs, pend_sl, sx);
+                        r0 = unit_dot_mix4_e4m3(dv, pend_dd, pend_bb, c, sx);
+                        add_unit(r0, r1);
+                        if constexpr (kGuard)
+                            if (__float_as_uint(c[0]) >> 31) check_unit(dv, c);
+                    } else if constexpr (Q4K8) {
                         float c[8], sx[8];
                         table_f8(sbase, kOffXc, pend_sl, c);
                         table_f8(sbase, kOffXs, pend_sl, sx);
@@ -617,7 +680,10 @@ __device__ __forceinline__ void qmv_tc_body(const QtcParams& p) {
                     }
                 }
     #pragma unroll
-                for (int P = 0; P < 4; ++P) pend_dd[P] = dd[P];
+                for (int P = 0; P < 4; ++P) {
+                    pend_dd[P] = dd[P];
+                    if constexpr (MIX) pend_bb[P] = bb[P];
+                }
                 pend_sx = cur_sx;
                 pend_sl = cur_sl;
                 pend_tile = t;
@@ -633,7 +699,15 @@ __device__ __forceinline__ void qmv_tc_body(const QtcParams& p) {
                     tmem_ld16(d_taddr + 16u * last_par, dv);
                     tmem_wait_ld();
                     float r0, r1 = 0.f;
-                    if constexpr (Q4K8) {
+                    if constexpr (MIX) {
+                        float c[8], sx[8];
+                        table_f8(sbase, kOffXc, pend_sl, c);
+                        table_f8(sbase, kOffXs, pend_sl, sx);
+                        r0 = unit_dot_mix4_e4m3(dv, pend_dd, pend_bb, c, sx);
+                        add_unit(r0, r1);
+                        if constexpr (kGuard)
+                            if (__float_as_uint(c[0]) >> 31) check_unit(dv, c);
+                    } else if constexpr (Q4K8) {
                         float c[8], sx[8];
                         table_f8(sbase, kOffXc, pend_sl, c);
                         table_f8(sbase, kOffXs, pend_sl, sx);
@@ -758,6 +832,54 @@ __global__ void __launch_bounds__(kThreads, 1) qmv_q4_k_tc_e4m3_kernel(const __g
     qmv_tc_body<kFmtQ4K, 1, 1, XP>(p);
 }
 
+// the int4-affine mixed-bit matrices (groups of 32) in the 8-bit operand
+// form, bf16 activations
+__global__ void __launch_bounds__(kThreads, 1) qmv_mix4_tc_e4m3_kernel(const __grid_constant__ QtcParams p) {
+    qmv_tc_body<kFmtMix4, 1, 1, 2>(p);
+}
+
+// Every kernel of this file may take kSmemBytes of dynamic shared memory (once
+// per device and thread).
+cudaError_t prepare_qtc_kernels() {
+    static thread_local int prepared_device = -1;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (prepared_device == dev) return cudaSuccess;
+    for (auto f : {qmv_q4_0_tc_kernel<1, 1>, qmv_q4_0_tc_kernel<2, 1>, qmv_q4_0_tc_kernel<1, 2>,
+                   qmv_q4_0_tc_e4m3_kernel<1, 2>, qmv_q4_0_tc_e4m3_kernel<2, 2>, qmv_q4_0_tc_e4m3_kernel<1, 3>,
+                   qmv_q4_0_tc_e4m3_kernel<2, 3>, qmv_q4_k_tc_kernel, qmv_q4_k_tc_e4m3_kernel<2>,
+                   qmv_q4_k_tc_e4m3_kernel<3>, qmv_mix4_tc_e4m3_kernel}) {
+        cudaError_t e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+        if (e != cudaSuccess) return e;
+    }
+    prepared_device = dev;
+    return cudaSuccess;
+}
+
+cudaError_t launch_qtc(void (*kernel)(QtcParams), const QtcParams& p, int ctas, cudaStream_t stream) {
+    cudaError_t e = prepare_qtc_kernels();
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.gridDim = dim3((unsigned)ctas);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = kSmemBytes;
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, p);
+}
+
+// Whether the 8-bit form's activation table holds every K-group that a CTA's
+// unit range needs (one token, nmat matrices; CTAs = min(units, SMs)).
+bool table_fits(int nmat, int units, int groups, int sm_count) {
+    const int ctas = units < sm_count ? units : sm_count;
+    const int per_cta = (units + ctas - 1) / ctas;
+    return std::min(groups, (per_cta - 1) / nmat + 2) <= kXtGroups;
+}
+
 }  // namespace
 
 // The tensor-core M = 1 path takes K % 256 == 0, at most kQtcMaxTiles tiles
@@ -791,6 +913,7 @@ cudaError_t launch_qmv_tc(int fmt, int nmat, int ntok, const CUtensorMap* tmap_w
     p.tmap_w[1] = tmap_w[nmat == 2 ? 1 : 0];
     p.w[0] = static_cast<const uint8_t*>(w[0]);
     p.w[1] = static_cast<const uint8_t*>(w[nmat == 2 ? 1 : 0]);
+    p.msc = nullptr;
     p.row_bytes = weight_row_bytes(fmt, K);
     p.next_units = 0;
     p.next_groups = p.next_nmat = p.next_ctas = 1;
@@ -814,38 +937,51 @@ cudaError_t launch_qmv_tc(int fmt, int nmat, int ntok, const CUtensorMap* tmap_w
     p.y_bf16 = y_bf16;
     const int ctas = p.units < sm_count ? p.units : sm_count;
     // the 8-bit form needs every K-group of a CTA's unit range in its table
-    const int per_cta = (p.units + ctas - 1) / ctas;
-    const bool f8 = ntok == 1 && std::min(p.groups, (per_cta - 1) / nmat + 2) <= kXtGroups;
+    const bool f8 = ntok == 1 && table_fits(nmat, p.units, p.groups, sm_count);
     auto kernel = fmt == kFmtQ4K ? (f8 ? (x_bf16 ? qmv_q4_k_tc_e4m3_kernel<2> : qmv_q4_k_tc_e4m3_kernel<3>)
                                        : qmv_q4_k_tc_kernel)
                   : f8 ? (x_bf16 ? (nmat == 2 ? qmv_q4_0_tc_e4m3_kernel<2, 2> : qmv_q4_0_tc_e4m3_kernel<1, 2>)
                                  : (nmat == 2 ? qmv_q4_0_tc_e4m3_kernel<2, 3> : qmv_q4_0_tc_e4m3_kernel<1, 3>))
                   : (nmat == 2 ? qmv_q4_0_tc_kernel<2, 1>
                                : (ntok == 2 ? qmv_q4_0_tc_kernel<1, 2> : qmv_q4_0_tc_kernel<1, 1>));
-    static thread_local int prepared_device = -1;
-    int dev = 0;
-    cudaGetDevice(&dev);
-    if (prepared_device != dev) {
-        for (auto f : {qmv_q4_0_tc_kernel<1, 1>, qmv_q4_0_tc_kernel<2, 1>, qmv_q4_0_tc_kernel<1, 2>,
-                       qmv_q4_0_tc_e4m3_kernel<1, 2>, qmv_q4_0_tc_e4m3_kernel<2, 2>, qmv_q4_0_tc_e4m3_kernel<1, 3>,
-                       qmv_q4_0_tc_e4m3_kernel<2, 3>, qmv_q4_k_tc_kernel, qmv_q4_k_tc_e4m3_kernel<2>,
-                       qmv_q4_k_tc_e4m3_kernel<3>}) {
-            cudaError_t e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
-            if (e != cudaSuccess) return e;
-        }
-        prepared_device = dev;
-    }
-    cudaLaunchConfig_t cfg = {};
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.gridDim = dim3((unsigned)ctas);
-    cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = kSmemBytes;
-    cfg.stream = stream;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, kernel, p);
+    return launch_qtc(kernel, p, ctas, stream);
+}
+
+// The int4-affine mixed-bit form takes what the Q4_0 path takes (K % 256 == 0,
+// tile and CTA limits) and an activation table that holds every K-group of a
+// CTA's unit range.
+bool qmv_mix4_tc_supported(int64_t N, int64_t K, int sm_count) {
+    if (!qmv_tc_supported(1, N, K, sm_count)) return false;
+    const int tiles = (int)((N + kTileRows - 1) / kTileRows), groups = (int)(K / kGroupK);
+    return table_fits(1, tiles * groups, groups, sm_count);
+}
+
+// tmaps: the codes ([N][K / 16] 8-byte words, box (16, 128), 128-byte
+// swizzle), scales and biases ([N][K / 128] 8-byte words, box (2, 128)); qp
+// and sc the same arrays, for the read-back correction; bf16 x.
+cudaError_t launch_qmv_mix4_tc(const CUtensorMap* tmaps, const void* qp, const void* sc, const void* x, void* y,
+                               int y_bf16, int N, int K, int sm_count, unsigned int* fault, cudaStream_t stream) {
+    QtcParams p;
+    p.tmap_w[0] = tmaps[0];
+    p.tmap_w[1] = tmaps[1];
+    p.tmap_bi = tmaps[2];
+    p.w[0] = p.w[1] = static_cast<const uint8_t*>(qp);
+    p.msc = static_cast<const uint16_t*>(sc);
+    p.row_bytes = K / 2;
+    p.next_units = 0;
+    p.next_groups = p.next_nmat = p.next_ctas = 1;
+    p.x = x;
+    p.y = y;
+    p.fault = fault;
+    p.N = N;
+    p.K = K;
+    p.tiles = (N + kTileRows - 1) / kTileRows;
+    p.groups = K / kGroupK;
+    p.units = p.tiles * p.groups;
+    p.x_bf16 = 1;
+    p.y_bf16 = y_bf16;
+    if (!table_fits(1, p.units, p.groups, sm_count)) return cudaErrorInvalidValue;
+    return launch_qtc(qmv_mix4_tc_e4m3_kernel, p, p.units < sm_count ? p.units : sm_count, stream);
 }
 
 }  // namespace qbw

@@ -37,6 +37,18 @@ constexpr uint32_t kOffB = kStages * kRawStageBytes;                          //
 // 8-bit form with fp32 activations: a second B per set, the third pieces
 constexpr uint32_t kOffB2 = kOffB + kSets * kBBytes;
 constexpr uint32_t kOffPart = kOffB2 + kSets * kBBytes;
+// The int4-affine mixed-bit form (kFmtMix4, bf16 activations only): a unit's
+// codes, 128 bytes per row, land at the start of its stage with the 128-byte
+// swizzle (16-byte chunk j of row r at 16 (j ^ (r mod 8))); its 8 fp16 scales
+// and 8 fp16 biases per row (16 bytes each, row after row) land in the B2
+// region, which only the fp32 form's third pieces use otherwise: stage s's
+// scales at kOffB2 + s kMixScaleBytes, its biases 2 KB further on.
+constexpr uint32_t kMixCodeBytes = kTileRows * 128;
+constexpr uint32_t kMixScaleBytes = 2 * kTileRows * 16;
+constexpr uint32_t kMixStageBytes = kMixCodeBytes + kMixScaleBytes;
+static_assert(kMixCodeBytes <= kRawStageBytes && kStages * kMixScaleBytes <= kSets * kBBytes,
+              "the mixed-bit form's stages fit the raw ring and the B2 region");
+static_assert(kRawStageBytes % 1024 == 0 && kOffB2 % 1024 == 0, "swizzled copies want 1024-byte aligned stages");
 constexpr uint32_t kOffBar = kOffPart + kSets * kMaxLocalTiles * 2 * kTileRows * 4;
 constexpr int kBars = 2 * kStages + 4 * kSets + 1;
 constexpr uint32_t kOffSlot = kOffBar + 8 * kBars;
@@ -83,6 +95,12 @@ struct QtcParams {
     // the same CTA index loads there
     CUtensorMap next_tmap[2];
     int32_t next_units, next_groups, next_nmat, next_ctas;
+    // the int4-affine mixed-bit form: tmap_w[0] views the codes as 8-byte
+    // words, box (16, 128); tmap_w[1] the fp16 scales and tmap_bi the fp16
+    // biases as 8-byte words, box (2, 128); msc the scales again, for the
+    // read-back correction ([N][K / 32])
+    CUtensorMap tmap_bi;
+    const uint16_t* msc;
     const void* x;
     void* y;
     unsigned int* fault;
@@ -216,6 +234,32 @@ __device__ __forceinline__ void codes_q4k_e4m3(const uint32_t (&v)[36], uint32_t
     }
 }
 
+// int4-affine mixed-bit form: half H of a unit (groups 4H .. 4H + 3 of 32
+// weights, code words 16H .. 16H + 15 of the row's 32) -> 32 TMEM columns of
+// e4m3 codes 0..15 (exact, b 2^-9), one K-step of 8 columns per group.  Word
+// i of a group holds its weights 8i .. 8i + 7, nibble e = weight 8i + e; the
+// even nibbles go to column 2i of the K-step and the odd ones to column 2i +
+// 1, so K positions 8i .. 8i + 7 hold weights 8i + 0, 2, 4, 6, 1, 3, 5, 7
+// (perm_mix4 puts the activation pieces of B in the same order).
+template <int H>
+__device__ __forceinline__ void codes_mix4_e4m3(const uint32_t (&v)[36], uint32_t (&col)[32]) {
+#pragma unroll
+    for (int t = 0; t < 16; ++t) {
+        const uint32_t w = v[16 * H + t];
+        col[2 * t] = w & 0x0F0F0F0Fu;
+        col[2 * t + 1] = (w >> 4) & 0x0F0F0F0Fu;
+    }
+}
+
+// The eight bytes of an activation chunk's piece (element order) in the order
+// codes_mix4_e4m3 gives a code word's weights: the even elements, then the odd.
+__device__ __forceinline__ uint2 perm_mix4(uint2 b) {
+    uint32_t lo, hi;
+    asm("prmt.b32 %0, %1, %2, 0x6420;" : "=r"(lo) : "r"(b.x), "r"(b.y));
+    asm("prmt.b32 %0, %1, %2, 0x7531;" : "=r"(hi) : "r"(b.x), "r"(b.y));
+    return make_uint2(lo, hi);
+}
+
 // fp16 scales of blocks 2P (low half) and 2P + 1 (high half) of the group:
 // block 2P's in the low half of word 9P, block 2P + 1's in the high half of
 // word 9P + 4.
@@ -318,6 +362,26 @@ __device__ __forceinline__ float unit_dot_q4k_e4m3(const uint32_t (&dv)[16], con
         }
         r = fmaf(dm.x * (float)sc * fabsf(c[j]), fmaf(__uint_as_float(dv[2 * j + 1]), 0.0625f, __uint_as_float(dv[2 * j])), r);
         r = fmaf(-dm.y * (float)m, sx[j], r);
+    }
+    return r;
+}
+
+// 8-bit form of the int4-affine mixed-bit matrices: r0 = sum_j (sc_j c_j)
+// (D[2j] + D[2j + 1] / 16) + bi_j sx_j, j = 0..7 in order: the split of w = sc
+// c + bi, whose codes the pieces multiply while each bias takes its group's
+// exact sum of x.  sc[] and bi[] hold the unit's eight fp16 scales and biases
+// (group 2p in the low half of word p), c[j] the read-back factors and sx[j]
+// the groups' activation sums.
+__device__ __forceinline__ float unit_dot_mix4_e4m3(const uint32_t (&dv)[16], const uint32_t (&sc)[4],
+                                                    const uint32_t (&bi)[4], const float (&c)[8], const float (&sx)[8]) {
+    float r = 0.f;
+#pragma unroll
+    for (int p = 0; p < 4; ++p) {
+        const float2 s = half2_to_float2(sc[p]), b = half2_to_float2(bi[p]);
+        r = fmaf(s.x * fabsf(c[2 * p]), fmaf(__uint_as_float(dv[4 * p + 1]), 0.0625f, __uint_as_float(dv[4 * p])), r);
+        r = fmaf(b.x, sx[2 * p], r);
+        r = fmaf(s.y * c[2 * p + 1], fmaf(__uint_as_float(dv[4 * p + 3]), 0.0625f, __uint_as_float(dv[4 * p + 2])), r);
+        r = fmaf(b.y, sx[2 * p + 1], r);
     }
     return r;
 }
@@ -647,10 +711,16 @@ __device__ __forceinline__ void build_x_table(uint32_t sbase, const void* x, int
 // The row's weight at element k (0..255) of a unit, exact in fp32, from the
 // row's 144 raw bytes b[]: Q4_0 d_j (c - 8) (block j = k / 32, code k % 32 of
 // its 16 bytes: low nibbles first); Q4_K d sc_j q, the part the pieces
-// multiply (its min term dmin m_j is applied to the exact sum of x).
+// multiply (its min term dmin m_j is applied to the exact sum of x); the
+// int4-affine form sc_j c (nibble k of the 128 code bytes, lowest first, then
+// the eight fp16 scales at byte 128; its bias takes the exact sum of x).
 template <int FMT>
 __device__ __forceinline__ float unit_weight(const uint8_t* b, int k) {
-    if constexpr (FMT == kFmtQ4) {
+    if constexpr (FMT == kFmtMix4) {
+        const uint32_t code = ((uint32_t)b[k >> 1] >> (4 * (k & 1))) & 15u;
+        const int j = k >> 5;
+        return half_bits_to_float((uint32_t)b[128 + 2 * j] | ((uint32_t)b[129 + 2 * j] << 8)) * (float)code;
+    } else if constexpr (FMT == kFmtQ4) {
         const uint8_t* blk = b + 18 * (k >> 5);
         const int e = k & 31;
         const uint32_t byte = blk[2 + (e & 15)];
@@ -680,7 +750,9 @@ template <int FMT>
 __device__ __forceinline__ float unit_check_term(const uint32_t (&dv)[16], const uint32_t (&dd)[4], const float (&c)[8],
                                                  const float (&a)[8]) {
     float q = 0.f;
-    if constexpr (FMT == kFmtQ4) {
+    if constexpr (FMT == kFmtQ4 || FMT == kFmtMix4) {
+        // dd[p]: the scales of blocks 2p and 2p + 1 as an fp16 pair (Q4_0's d,
+        // the mixed-bit form's sc)
 #pragma unroll
         for (int p = 0; p < 4; ++p) {
             const float2 d = half2_to_float2(dd[p]);
@@ -722,14 +794,17 @@ __device__ __forceinline__ bool segment_needs_correction(float q) { return q > 0
 // its pieces carry, formed again from x (group g, elements 256 g ..
 // 256 g + 255; block scales from table slot sl) and the row's raw bytes read
 // from global memory at wrow (16-byte aligned; the stage holding them has
-// long been released).  For the segments the read-back check flags; slow, and
-// exact up to fp32 rounding.
+// long been released): 144 bytes, or for the int4-affine form 128 code bytes
+// and the 16 bytes of scales at srow.  For the segments the read-back check
+// flags; slow, and exact up to fp32 rounding.
 template <int FMT, int XP, bool kCoherent>
-__device__ __noinline__ float unit_correction(const uint8_t* wrow, const void* x, int g, uint32_t sbase, int sl) {
+__device__ __noinline__ float unit_correction(const uint8_t* wrow, const void* x, int g, uint32_t sbase, int sl,
+                                              const uint8_t* srow = nullptr) {
     uint8_t b[144];
 #pragma unroll
     for (int j = 0; j < 9; ++j)
-        *reinterpret_cast<uint4*>(b + 16 * j) = __ldg(reinterpret_cast<const uint4*>(wrow) + j);
+        *reinterpret_cast<uint4*>(b + 16 * j) =
+            __ldg(reinterpret_cast<const uint4*>(FMT == kFmtMix4 && j == 8 ? srow : wrow + 16 * j));
     float corr = 0.f;
     for (int k = 0; k < kGroupK; ++k) {
         const uint32_t cb = lds32(sbase + kOffXc + (uint32_t)sl * 32u + (uint32_t)(k >> 5) * 4u);

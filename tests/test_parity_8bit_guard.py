@@ -17,7 +17,7 @@ correction the small elements' error is a large fraction of S.
 Per K-group of 256 inputs (K = 2048, eight groups), the case mixes:
 * plain N(0,1) activations;
 * outlier blocks: one element 2^16 at a position whose code is 8 (Q4_0; code 0
-  with dmin = 0 for Q4_K) in every row, n small elements in [1, 2) with their
+  with dmin = 0 for Q4_K, with zero biases for int4-affine) in every row, n small elements in [1, 2) with their
   last mantissa bit set (scaled to about 2^-9, so most of their bits fall below
   e4m3's subnormal spacing), zeros elsewhere, with n from 4 to 31.
 """
@@ -152,6 +152,35 @@ def test_q4_k_outliers_on_zero_weights(qbw, oracle, xdt):
     y_ref, _ = oracle.qmv("q4_k", w, x, N, K)
     S2 = oracle.q4k_split_scale(w, x, N, K)       # equals S here (dmin = 0)
     check_matvec(to_f64(y), y_ref, S2, what=f"q4_k outliers {xdt}")
+
+
+def zero_mix4_codes(qp, bi, outliers):
+    """Bias 0 in every group and code 0 at every outlier position of an
+    int4-affine matrix (nibble k of a row in byte k / 2, low nibble first), so
+    the outliers meet weights that are exactly 0."""
+    q = qp.view(np.uint8).reshape(N, K // 2)
+    for blk, pos in outliers:
+        k = 32 * blk + pos
+        q[:, k // 2] &= 0xF0 if k % 2 == 0 else 0x0F
+    bi[:] = 0
+    return qp, bi
+
+
+@pytest.mark.parametrize("xdt", ["bf16", "f32"])
+def test_mixbit4_outliers_on_zero_weights(qbw, oracle, xdt):
+    # 16384 x 2048 int4 codes are 16.8 MB: bf16 x takes the tensor-core form
+    # (groups of 32), fp32 x the CUDA-core kernel
+    x, outliers = worst_case_activations(xdt, seed=51 if xdt == "bf16" else 52)
+    qp, sc, bi = synth.mixbit_weights(4, N, K, 32, seed=53)
+    qp, bi = zero_mix4_codes(qp, bi, outliers)
+    y = torch.full((N,), float("nan"), dtype=torch.float32, device="cuda")
+    qbw.qmv_mixbit(4, dev_u8(qp.view(np.uint8)), dev_u8(sc.view(np.uint8)), dev_u8(bi.view(np.uint8)), 32,
+                   dev_act(x), y, 1, N, K)
+    torch.cuda.synchronize()
+    assert qbw.fault_read(clear=True) == 0
+    y_ref, S, S2 = oracle.qmv_mixbit(4, qp, sc, bi, 32, x, N, K)
+    assert np.array_equal(S, S2)                 # no bias term
+    check_matvec(to_f64(y), y_ref, S2, what=f"mixbit4 outliers {xdt}")
 
 
 def test_chain_step_outliers_on_zero_weights(qbw, oracle):

@@ -135,3 +135,68 @@ def test_largest_k(qbw, oracle, bits, K):
         qbw.qmv_mixbit(bits, dev(qp2), dev(sc2), dev(bi2), G, dev_act(synth.activations(K2, seed=2, dtype="bf16")),
                        y2, 1, 2, K2)
     assert err.value.status == 2           # QBW_ESHAPE
+
+
+# int4-affine, groups of 32, bf16 x, at least 8 MB of codes: the tensor-core
+# form.  (rows, K): a ragged last tile, the shortest rows (one K-group), the
+# 31B profile's K, and long rows (84 K-groups)
+TC_SHAPES = [(3077, 5376), (62501, 256), (12000, 1536), (4000, 21504)]
+
+
+@pytest.mark.parametrize("N,K", TC_SHAPES)
+@pytest.mark.parametrize("odt", [torch.float32, torch.bfloat16])
+def test_tc_int4(qbw, oracle, N, K, odt):
+    qp, sc, bi = synth.mixbit_weights(4, N, K, 32, seed=N + K)
+    x = synth.activations(K, seed=K + 5, dtype="bf16")
+    y = run(qbw, 4, qp, sc, bi, 32, x, N, K, odt)
+    y_ref, _, S2 = oracle.qmv_mixbit(4, qp, sc, bi, 32, x, N, K)
+    check_matvec(to_f64(y), y_ref, S2, out_bf16=(odt == torch.bfloat16), what=f"tc int4 {N}x{K}")
+
+
+@pytest.mark.parametrize("field", [0, 15, 8])
+def test_tc_int4_constant_fields(qbw, oracle, field):
+    # every code equal: y[n] = sum over groups of (sc c + bi) * sum(x over the group)
+    N, K, G = 3077, 5376, 32
+    qp = synth.pack_fields(np.full((N, K), field, dtype=np.uint32), 4)
+    _, sc, bi = synth.mixbit_weights(4, N, K, G, seed=field + 3)
+    x = synth.activations(K, seed=field + 4, dtype="bf16")
+    y = to_f64(run(qbw, 4, qp, sc, bi, G, x, N, K))
+    xs = (x.astype(np.uint32) << 16).view(np.float32).astype(np.float64).reshape(K // G, G).sum(axis=1)
+    s = sc.view(np.float16).astype(np.float64).reshape(N, K // G)
+    b = bi.view(np.float16).astype(np.float64).reshape(N, K // G)
+    ref = ((s * field + b) * xs).sum(axis=1)
+    _, _, S2 = oracle.qmv_mixbit(4, qp, sc, bi, G, x, N, K)
+    check_matvec(y, ref, S2, what=f"tc constant int4 {field}")
+
+
+def test_tc_int4_zero_scales_and_biases(qbw):
+    N, K = 3077, 5376
+    qp, sc, bi = synth.mixbit_weights(4, N, K, 32, seed=2)
+    y = run(qbw, 4, qp, np.zeros_like(sc), np.zeros_like(bi), 32, synth.activations(K, seed=3, dtype="bf16"), N, K)
+    assert torch.all(y == 0)
+
+
+def test_tc_int4_deterministic(qbw):
+    N, K = 21504, 5376
+    qp, sc, bi = synth.mixbit_weights(4, N, K, 32, seed=21)
+    x = synth.activations(K, seed=22, dtype="bf16")
+    a = run(qbw, 4, qp, sc, bi, 32, x, N, K)
+    b = run(qbw, 4, qp, sc, bi, 32, x, N, K)
+    assert torch.equal(a.view(torch.int32), b.view(torch.int32))
+
+
+def test_tc_int4_unaligned_scales_fall_back(qbw, oracle):
+    # scales and biases 4 bytes past a 16-byte boundary: the CUDA-core kernel
+    N, K = 3077, 5376
+    qp, sc, bi = synth.mixbit_weights(4, N, K, 32, seed=31)
+    x = synth.activations(K, seed=32, dtype="bf16")
+    sc_buf = torch.zeros(sc.nbytes + 16, dtype=torch.uint8, device="cuda")
+    bi_buf = torch.zeros(bi.nbytes + 16, dtype=torch.uint8, device="cuda")
+    sc_buf[4:4 + sc.nbytes] = dev(sc)
+    bi_buf[4:4 + bi.nbytes] = dev(bi)
+    y = torch.full((N,), float("nan"), dtype=torch.float32, device="cuda")
+    qbw.qmv_mixbit(4, dev(qp), sc_buf[4:4 + sc.nbytes], bi_buf[4:4 + bi.nbytes], 32, dev_act(x), y, 1, N, K)
+    torch.cuda.synchronize()
+    assert qbw.fault_read(clear=True) == 0
+    y_ref, _, S2 = oracle.qmv_mixbit(4, qp, sc, bi, 32, x, N, K)
+    check_matvec(to_f64(y), y_ref, S2, what="int4 unaligned scales")
