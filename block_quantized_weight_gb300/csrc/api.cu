@@ -35,9 +35,10 @@ cudaError_t launch_qmv_tc(int fmt, int nmat, int ntok, const CUtensorMap* tmap_w
                           const void* x, int x_bf16, void* y, int y_bf16, int N, int K, int sm_count,
                           unsigned int* fault, cudaStream_t stream, const QtcNextLaunch* next = nullptr);
 int qmm_tc_tile_rows();
-bool qmv_mix4_tc_supported(int64_t N, int64_t K, int sm_count);
-cudaError_t launch_qmv_mix4_tc(const CUtensorMap* tmaps, const void* qp, const void* sc, const void* x, void* y,
-                               int y_bf16, int N, int K, int sm_count, unsigned int* fault, cudaStream_t stream);
+bool qmv_mix_tc_supported(int64_t N, int64_t K, int sm_count);
+cudaError_t launch_qmv_mix_tc(int bits, const CUtensorMap* tmaps, const void* qp, const void* sc, const void* x,
+                              void* y, int y_bf16, int N, int K, int sm_count, unsigned int* fault,
+                              cudaStream_t stream);
 bool qmv_chain_step_supported(int nmat, int64_t N, int64_t K, int ctas);
 void qmv_chain_fill_step(ChainStepDesc* d, int nmat, int64_t N, int64_t K);
 int qmv_chain_ctas(int sm_count);
@@ -248,28 +249,30 @@ bool encode_q4_tile_map(CUtensorMap* m, const void* w, int64_t N, int64_t K) {
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// The int4-affine mixed-bit matrices with groups of 32, for the tensor-core
-// kernel: m[0] the codes as [N][K / 16] 8-byte words, box (16, 128) (one
-// 256-element K-group of a 128-row tile, 128 bytes per row) with the 128-byte
-// swizzle; m[1], m[2] the fp16 scales and biases as [N][K / 128] 8-byte
-// words, box (2, 128) (the group's 8 of each per row).  Needs K % 256 == 0 and
-// 16-byte aligned arrays.
-bool encode_mix4_maps(CUtensorMap* m, const void* qp, const void* sc, const void* bi, int64_t N, int64_t K) {
+// The int4-affine (bits = 4) or int2-symmetric (bits = 2) mixed-bit matrices
+// with groups of 32, for the tensor-core kernel: m[0] the codes as [N][K b /
+// 64] 8-byte words, box (4 b, 128) (one 256-element K-group of a 128-row
+// tile, 32 b bytes per row) with the 128-byte (int4) or 64-byte (int2)
+// swizzle; m[1] and, for int4, m[2] the fp16 scales and biases as [N][K / 128]
+// 8-byte words, box (2, 128) (the group's 8 of each per row).  Needs K % 256
+// == 0 and 16-byte aligned arrays.
+bool encode_mix_maps(CUtensorMap* m, int bits, const void* qp, const void* sc, const void* bi, int64_t N,
+                     int64_t K) {
     PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
     if (!enc) return false;
     const cuuint32_t rows = (cuuint32_t)qmm_tc_tile_rows();
     cuuint32_t estr[2] = {1, 1};
     {
-        cuuint64_t dims[2] = {(cuuint64_t)(K / 16), (cuuint64_t)N};
-        cuuint64_t strides[1] = {(cuuint64_t)(K / 2)};
-        cuuint32_t box[2] = {16, rows};
+        cuuint64_t dims[2] = {(cuuint64_t)(K * bits / 64), (cuuint64_t)N};
+        cuuint64_t strides[1] = {(cuuint64_t)(K * bits / 8)};
+        cuuint32_t box[2] = {(cuuint32_t)(4 * bits), rows};      // 256 weights of b bits
         if (enc(&m[0], CU_TENSOR_MAP_DATA_TYPE_UINT64, 2, const_cast<void*>(qp), dims, strides, box, estr,
-                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+                CU_TENSOR_MAP_INTERLEAVE_NONE, bits == 4 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
+                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
             return false;
     }
     const void* sb[2] = {sc, bi};
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < (bits == 4 ? 2 : 1); ++i) {
         cuuint64_t dims[2] = {(cuuint64_t)(K / 128), (cuuint64_t)N};
         cuuint64_t strides[1] = {(cuuint64_t)(K / 16)};
         cuuint32_t box[2] = {2, rows};
@@ -633,12 +636,16 @@ static qbw_status mixbit_args(qbw_mixbit kind, const void* qp, const void* sc, c
     return QBW_OK;
 }
 
-// Bytes of int4 codes from which the mixed-bit product takes the tensor cores:
+// Bytes of codes from which the mixed-bit product takes the tensor cores:
 // below them the CUDA-core kernel's shorter start-up wins, and more so for
-// short rows (GB300, CUDA-graph replay, groups of 32, bf16 x: 2048 x 5376 6.8
-// vs 7.7 us, 4096 x 4096 6.1 vs 6.0 us, 4096 x 2048 5.5 vs 3.6 us, 16384 x 2048
-// 7.3 vs 8.5 us, 21504 x 5376 14.5 vs 27.3 us).
-constexpr double mix4_tc_min_bytes(int64_t K) { return K > 4096 ? 5e6 : 10e6; }
+// short rows (GB300, CUDA-graph replay, groups of 32, bf16 x, tensor cores vs
+// CUDA cores; int4: 2048 x 5376 6.7 vs 7.7 us, 4096 x 4096 6.1 vs 6.0, 4096 x
+// 2048 5.5 vs 3.5, 16384 x 2048 7.2 vs 8.5, 21504 x 5376 14.5 vs 27.3; int2:
+// 2048 x 5376 6.7 vs 4.7, 3077 x 5376 6.7 vs 6.8, 4096 x 4096 6.0 vs 6.2,
+// 4096 x 2048 5.4 vs 3.3, 16384 x 2048 7.1 vs 8.1, 21504 x 5376 13.5 vs 24.9).
+constexpr double mix_tc_min_bytes(int bits, int64_t K) {
+    return bits == 4 ? (K > 4096 ? 5e6 : 10e6) : (K > 4096 ? 4e6 : 5e6);
+}
 
 qbw_status qmv_mixbit(qbw_mixbit kind, const void* qp, const void* sc, const void* bi, int64_t group, const void* x,
                       qbw_dtype xt, void* y, qbw_dtype yt, int64_t M, int64_t N, int64_t K, void* stream) {
@@ -658,15 +665,16 @@ qbw_status qmv_mixbit(qbw_mixbit kind, const void* qp, const void* sc, const voi
     st = device_info(&di);
     if (st != QBW_OK) return st;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    // int4-affine with groups of 32 and bf16 x: the tensor-core 8-bit form from
-    // mix4_tc_min_bytes of codes
-    if (kind == QBW_MIXBIT_INT4_AFFINE && group == 32 && xt == QBW_BF16 && K % 256 == 0 &&
-        (double)wbytes >= mix4_tc_min_bytes(K) && (uintptr_t)sc % 16 == 0 && (uintptr_t)bi % 16 == 0 &&
-        qmv_mix4_tc_supported(N, K, di->sm_count)) {
+    // int4-affine and int2-symmetric with groups of 32 and bf16 x: the
+    // tensor-core 8-bit form from mix_tc_min_bytes of codes
+    const int bits = (int)kind;
+    if ((bits == 4 || bits == 2) && group == 32 && xt == QBW_BF16 && K % 256 == 0 &&
+        (double)wbytes >= mix_tc_min_bytes(bits, K) && (uintptr_t)sc % 16 == 0 &&
+        (bits == 2 || (uintptr_t)bi % 16 == 0) && qmv_mix_tc_supported(N, K, di->sm_count)) {
         CUtensorMap maps[3];
-        if (encode_mix4_maps(maps, qp, sc, bi, N, K)) {
-            cudaError_t e = launch_qmv_mix4_tc(maps, qp, sc, x, y, yt == QBW_BF16, (int)N, (int)K, di->sm_count,
-                                               di->fault, s);
+        if (encode_mix_maps(maps, bits, qp, sc, bi, N, K)) {
+            cudaError_t e = launch_qmv_mix_tc(bits, maps, qp, sc, x, y, yt == QBW_BF16, (int)N, (int)K,
+                                              di->sm_count, di->fault, s);
             return e == cudaSuccess ? QBW_OK : QBW_ECUDA;
         }
     }

@@ -98,9 +98,10 @@ __device__ __forceinline__ void qmv_tc_body(const QtcParams& p) {
     static_assert(NCH <= 2, "at most two sums per row");
     static_assert(FMT == kFmtQ4 || (NMAT == 1 && NTOK == 1), "Q4_K: one matrix, one token");
     static_assert(F8 == 0 || ((F8 == 2 || F8 == 3) && NTOK == 1), "8-bit form: one token");
-    // the int4-affine mixed-bit matrices: 8-bit form with bf16 activations only
-    // (their scales and biases take the B2 region)
-    constexpr bool MIX = FMT == kFmtMix4;
+    // the int4-affine (MIX4) and int2-symmetric (MIX2) mixed-bit matrices:
+    // 8-bit form with bf16 activations only (their scales and biases take the
+    // B2 region)
+    constexpr bool MIX4 = FMT == kFmtMix4, MIX2 = FMT == kFmtMix2, MIX = MIX4 || MIX2;
     static_assert(!MIX || F8 == 2, "mixed-bit form: two pieces");
     // the 8-bit form of Q4_K: one A operand (codes 0..15), 8 K-steps per unit
     constexpr bool Q4K8 = F8 != 0 && FMT == kFmtQ4K;
@@ -159,7 +160,7 @@ __device__ __forceinline__ void qmv_tc_body(const QtcParams& p) {
         if (lane == 0) {
             prefetch_tmap(&p.tmap_w[0]);
             if (NMAT == 2 || MIX) prefetch_tmap(&p.tmap_w[1]);
-            if constexpr (MIX) prefetch_tmap(&p.tmap_bi);
+            if constexpr (MIX4) prefetch_tmap(&p.tmap_bi);
             // weights do not depend on the preceding grid: start streaming now
             for (int i = 0; i < n && ok; ++i) {
                 const int s = i % kStages;
@@ -169,14 +170,15 @@ __device__ __forceinline__ void qmv_tc_body(const QtcParams& p) {
                 if (!ok) break;
                 const int u = u0 + i, ug = u / NMAT, mat = u - ug * NMAT, t = ug / G, g = ug - t * G;
                 if constexpr (MIX) {
-                    // codes (16 words of a row), then scales and biases (2 words each)
+                    // codes (16 or 8 words of a row), then scales and biases (2 words each)
                     const uint32_t sdst = sbase + kOffB2 + (uint32_t)s * kMixScaleBytes;
-                    mbar_arrive_expect_tx(full_bar(bar0, s), kMixStageBytes);
-                    tma_load_2d(sbase + (uint32_t)s * kRawStageBytes, &p.tmap_w[0], g * 16, t * kTileRows,
-                                full_bar(bar0, s), policy_evict_first());
+                    mbar_arrive_expect_tx(full_bar(bar0, s), MIX4 ? kMixStageBytes : kMix2StageBytes);
+                    tma_load_2d(sbase + (uint32_t)s * kRawStageBytes, &p.tmap_w[0], g * (MIX4 ? 16 : 8),
+                                t * kTileRows, full_bar(bar0, s), policy_evict_first());
                     tma_load_2d(sdst, &p.tmap_w[1], g * 2, t * kTileRows, full_bar(bar0, s), policy_evict_first());
-                    tma_load_2d(sdst + kMixScaleBytes / 2, &p.tmap_bi, g * 2, t * kTileRows, full_bar(bar0, s),
-                                policy_evict_first());
+                    if constexpr (MIX4)
+                        tma_load_2d(sdst + kMixScaleBytes / 2, &p.tmap_bi, g * 2, t * kTileRows, full_bar(bar0, s),
+                                    policy_evict_first());
                 } else {
                     mbar_arrive_expect_tx(full_bar(bar0, s), kRawStageBytes);
                     tma_load_2d(sbase + (uint32_t)s * kRawStageBytes, &p.tmap_w[mat], g * kGroupWords,
@@ -265,7 +267,7 @@ __device__ __forceinline__ void qmv_tc_body(const QtcParams& p) {
         const uint32_t lanes = (uint32_t)(32 * q) << 16;
         const uint32_t a_taddr = tmem + lanes + (uint32_t)set * kACols;
         const uint32_t d_taddr = tmem + lanes + kDCol + 32u * (uint32_t)set;   // + 16 (k % 2)
-        const uint32_t raw_row = (uint32_t)(32 * q + lane) * (MIX ? 128u : 144u);
+        const uint32_t raw_row = (uint32_t)(32 * q + lane) * (MIX4 ? 128u : (MIX2 ? 64u : 144u));
         const uint32_t bbuf = sbase + kOffB + (uint32_t)set * kBBytes;
         // The lane's 8-element slot xl of the group's activations: Q4_0, lanes
         // 0..7 load slots 8q .. 8q + 7 and write them into B; Q4_K, every lane
@@ -300,7 +302,9 @@ __device__ __forceinline__ void qmv_tc_body(const QtcParams& p) {
         if constexpr (F8) {
             const int cnt = n > 0 ? min(G, (u1 - 1) / NMAT - u0 / NMAT + 1) : 0;
             if (cnt > kXtGroups) record_fault(p.fault, kFaultPlan);
-            build_x_table<false, F8, ONE_OP>(sbase, p.x, xg0, G, min(cnt, kXtGroups), warp, lane, kProducerWarp);
+            // (with the groups' sums of x where a min or bias term takes them)
+            build_x_table<false, F8, Q4K8 || MIX4>(sbase, p.x, xg0, G, min(cnt, kXtGroups), warp, lane,
+                                                   kProducerWarp);
             asm volatile("bar.sync 2, %0;" ::"n"(kProducerWarp * 32) : "memory");
         }
         bool counted = !contrib0;
@@ -356,7 +360,7 @@ __device__ __forceinline__ void qmv_tc_body(const QtcParams& p) {
                     if (!group_flagged(sbase, sl)) continue;     // no residuals
                     if constexpr (MIX)
                         corr += unit_correction<FMT, 2, false>(
-                            p.w[0] + nrow * (p.K / 2) + (int64_t)g * 128, p.x, g, sbase, sl,
+                            p.w[0] + nrow * p.row_bytes + (int64_t)g * (MIX4 ? 128 : 64), p.x, g, sbase, sl,
                             reinterpret_cast<const uint8_t*>(p.msc + nrow * (p.K / 32) + (int64_t)g * 8));
                     else
                         corr += unit_correction<FMT, F8 ? F8 : 2, false>(
@@ -443,25 +447,29 @@ __device__ __forceinline__ void qmv_tc_body(const QtcParams& p) {
                 uint32_t dd[4];
                 [[maybe_unused]] uint32_t bb[4];
                 if constexpr (MIX) {
-                    // the row's 8 swizzled code chunks, then its scales and biases
+                    // the row's 8 (4) swizzled code chunks, then its scales (and biases)
     #pragma unroll
-                    for (int j = 0; j < 8; ++j) {
-                        const uint4 w = lds128(src + ((uint32_t)(j ^ (row & 7)) << 4));
+                    for (int j = 0; j < (MIX4 ? 8 : 4); ++j) {
+                        const uint32_t sw = MIX4 ? (uint32_t)(row & 7) : (uint32_t)((row >> 1) & 3);
+                        const uint4 w = lds128(src + (((uint32_t)j ^ sw) << 4));
                         v[4 * j] = w.x;
                         v[4 * j + 1] = w.y;
                         v[4 * j + 2] = w.z;
                         v[4 * j + 3] = w.w;
                     }
                     const uint32_t ssrc = sbase + kOffB2 + (uint32_t)s * kMixScaleBytes + (uint32_t)row * 16u;
-                    const uint4 sv = lds128(ssrc), bv = lds128(ssrc + kMixScaleBytes / 2);
+                    const uint4 sv = lds128(ssrc);
                     dd[0] = sv.x;
                     dd[1] = sv.y;
                     dd[2] = sv.z;
                     dd[3] = sv.w;
-                    bb[0] = bv.x;
-                    bb[1] = bv.y;
-                    bb[2] = bv.z;
-                    bb[3] = bv.w;
+                    if constexpr (MIX4) {
+                        const uint4 bv = lds128(ssrc + kMixScaleBytes / 2);
+                        bb[0] = bv.x;
+                        bb[1] = bv.y;
+                        bb[2] = bv.z;
+                        bb[3] = bv.w;
+                    }
                 } else {
     #pragma unroll
                     for (int j = 0; j < 9; ++j) {
@@ -552,7 +560,8 @@ __device__ __forceinline__ void qmv_tc_body(const QtcParams& p) {
                 }
                 const uint32_t prev = (uint32_t)(k - 1) & 1u;     // completion parity of the previous unit
                 // ---- half 0: K 0..127 (block pairs 0, 1; B atoms 0, 1 written by warps 0, 1)
-                if constexpr (MIX) codes_mix4_e4m3<0>(v, c0);
+                if constexpr (MIX4) codes_mix4_e4m3<0>(v, c0);
+                else if constexpr (MIX2) codes_mix2_e4m3<0>(v, c0);
                 else if constexpr (Q4K8) codes_q4k_e4m3<0>(v, c0);
                 else if constexpr (F8) codes_pair_e4m3<0>(v, c0);
                 else codes_pair<FMT, 0>(v, c0);
@@ -596,7 +605,8 @@ __device__ __forceinline__ void qmv_tc_body(const QtcParams& p) {
                 __syncwarp();
                 if (lane == 0) mbar_arrive(afull_bar(bar0, set, 0));
                 // ---- half 1: K 128..255 (block pairs 2, 3; B atoms 2, 3 written by warps 2, 3)
-                if constexpr (MIX) codes_mix4_e4m3<1>(v, c0);
+                if constexpr (MIX4) codes_mix4_e4m3<1>(v, c0);
+                else if constexpr (MIX2) codes_mix2_e4m3<1>(v, c0);
                 else if constexpr (Q4K8) codes_q4k_e4m3<1>(v, c0);
                 else if constexpr (F8) codes_pair_e4m3<2>(v, c0);
                 else codes_pair<FMT, 2>(v, c0);
@@ -648,7 +658,15 @@ __device__ __forceinline__ void qmv_tc_body(const QtcParams& p) {
                     tmem_ld16(d_taddr + 16u * prev, dv);
                     tmem_wait_ld();
                     float r0, r1 = 0.f;
-                    if constexpr (MIX) {
+                    if constexpr (MIX2) {
+                        // sum_j (sc_j c_j) (D[2j] + D[2j + 1] / 16), as Q4_0's d_j
+                        float c[8];
+                        table_f8(sbase, kOffXc, pend_sl, c);
+                        r0 = unit_dot_e4m3(dv, pend_dd, c);
+                        add_unit(r0, r1);
+                        if constexpr (kGuard)
+                            if (__float_as_uint(c[0]) >> 31) check_unit(dv, c);
+                    } else if constexpr (MIX4) {
                         float c[8], sx[8];
                         table_f8(sbase, kOffXc, pend_sl, c);
                         table_f8(sbase, kOffXs, pend_sl, sx);
@@ -682,7 +700,7 @@ __device__ __forceinline__ void qmv_tc_body(const QtcParams& p) {
     #pragma unroll
                 for (int P = 0; P < 4; ++P) {
                     pend_dd[P] = dd[P];
-                    if constexpr (MIX) pend_bb[P] = bb[P];
+                    if constexpr (MIX4) pend_bb[P] = bb[P];
                 }
                 pend_sx = cur_sx;
                 pend_sl = cur_sl;
@@ -699,7 +717,15 @@ __device__ __forceinline__ void qmv_tc_body(const QtcParams& p) {
                     tmem_ld16(d_taddr + 16u * last_par, dv);
                     tmem_wait_ld();
                     float r0, r1 = 0.f;
-                    if constexpr (MIX) {
+                    if constexpr (MIX2) {
+                        // sum_j (sc_j c_j) (D[2j] + D[2j + 1] / 16), as Q4_0's d_j
+                        float c[8];
+                        table_f8(sbase, kOffXc, pend_sl, c);
+                        r0 = unit_dot_e4m3(dv, pend_dd, c);
+                        add_unit(r0, r1);
+                        if constexpr (kGuard)
+                            if (__float_as_uint(c[0]) >> 31) check_unit(dv, c);
+                    } else if constexpr (MIX4) {
                         float c[8], sx[8];
                         table_f8(sbase, kOffXc, pend_sl, c);
                         table_f8(sbase, kOffXs, pend_sl, sx);
@@ -838,6 +864,11 @@ __global__ void __launch_bounds__(kThreads, 1) qmv_mix4_tc_e4m3_kernel(const __g
     qmv_tc_body<kFmtMix4, 1, 1, 2>(p);
 }
 
+// the int2-symmetric mixed-bit matrices (groups of 32), likewise
+__global__ void __launch_bounds__(kThreads, 1) qmv_mix2_tc_e4m3_kernel(const __grid_constant__ QtcParams p) {
+    qmv_tc_body<kFmtMix2, 1, 1, 2>(p);
+}
+
 // Every kernel of this file may take kSmemBytes of dynamic shared memory (once
 // per device and thread).
 cudaError_t prepare_qtc_kernels() {
@@ -848,7 +879,7 @@ cudaError_t prepare_qtc_kernels() {
     for (auto f : {qmv_q4_0_tc_kernel<1, 1>, qmv_q4_0_tc_kernel<2, 1>, qmv_q4_0_tc_kernel<1, 2>,
                    qmv_q4_0_tc_e4m3_kernel<1, 2>, qmv_q4_0_tc_e4m3_kernel<2, 2>, qmv_q4_0_tc_e4m3_kernel<1, 3>,
                    qmv_q4_0_tc_e4m3_kernel<2, 3>, qmv_q4_k_tc_kernel, qmv_q4_k_tc_e4m3_kernel<2>,
-                   qmv_q4_k_tc_e4m3_kernel<3>, qmv_mix4_tc_e4m3_kernel}) {
+                   qmv_q4_k_tc_e4m3_kernel<3>, qmv_mix4_tc_e4m3_kernel, qmv_mix2_tc_e4m3_kernel}) {
         cudaError_t e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
         if (e != cudaSuccess) return e;
     }
@@ -947,27 +978,30 @@ cudaError_t launch_qmv_tc(int fmt, int nmat, int ntok, const CUtensorMap* tmap_w
     return launch_qtc(kernel, p, ctas, stream);
 }
 
-// The int4-affine mixed-bit form takes what the Q4_0 path takes (K % 256 == 0,
-// tile and CTA limits) and an activation table that holds every K-group of a
-// CTA's unit range.
-bool qmv_mix4_tc_supported(int64_t N, int64_t K, int sm_count) {
+// The mixed-bit forms take what the Q4_0 path takes (K % 256 == 0, tile and
+// CTA limits) and an activation table that holds every K-group of a CTA's
+// unit range.
+bool qmv_mix_tc_supported(int64_t N, int64_t K, int sm_count) {
     if (!qmv_tc_supported(1, N, K, sm_count)) return false;
     const int tiles = (int)((N + kTileRows - 1) / kTileRows), groups = (int)(K / kGroupK);
     return table_fits(1, tiles * groups, groups, sm_count);
 }
 
-// tmaps: the codes ([N][K / 16] 8-byte words, box (16, 128), 128-byte
-// swizzle), scales and biases ([N][K / 128] 8-byte words, box (2, 128)); qp
-// and sc the same arrays, for the read-back correction; bf16 x.
-cudaError_t launch_qmv_mix4_tc(const CUtensorMap* tmaps, const void* qp, const void* sc, const void* x, void* y,
-                               int y_bf16, int N, int K, int sm_count, unsigned int* fault, cudaStream_t stream) {
+// bits = 4 or 2.  tmaps: the codes ([N][K b / 64] 8-byte words, box (4 b,
+// 128), the 128- or 64-byte swizzle), the scales and, for int4, the biases
+// ([N][K / 128] 8-byte words, box (2, 128)); qp and sc the same arrays, for
+// the read-back correction; bf16 x.
+cudaError_t launch_qmv_mix_tc(int bits, const CUtensorMap* tmaps, const void* qp, const void* sc, const void* x,
+                              void* y, int y_bf16, int N, int K, int sm_count, unsigned int* fault,
+                              cudaStream_t stream) {
+    if (bits != 2 && bits != 4) return cudaErrorInvalidValue;
     QtcParams p;
     p.tmap_w[0] = tmaps[0];
     p.tmap_w[1] = tmaps[1];
-    p.tmap_bi = tmaps[2];
+    p.tmap_bi = tmaps[bits == 4 ? 2 : 1];
     p.w[0] = p.w[1] = static_cast<const uint8_t*>(qp);
     p.msc = static_cast<const uint16_t*>(sc);
-    p.row_bytes = K / 2;
+    p.row_bytes = (int64_t)K * bits / 8;
     p.next_units = 0;
     p.next_groups = p.next_nmat = p.next_ctas = 1;
     p.x = x;
@@ -981,7 +1015,8 @@ cudaError_t launch_qmv_mix4_tc(const CUtensorMap* tmaps, const void* qp, const v
     p.x_bf16 = 1;
     p.y_bf16 = y_bf16;
     if (!table_fits(1, p.units, p.groups, sm_count)) return cudaErrorInvalidValue;
-    return launch_qtc(qmv_mix4_tc_e4m3_kernel, p, p.units < sm_count ? p.units : sm_count, stream);
+    return launch_qtc(bits == 4 ? qmv_mix4_tc_e4m3_kernel : qmv_mix2_tc_e4m3_kernel, p,
+                      p.units < sm_count ? p.units : sm_count, stream);
 }
 
 }  // namespace qbw

@@ -37,15 +37,17 @@ constexpr uint32_t kOffB = kStages * kRawStageBytes;                          //
 // 8-bit form with fp32 activations: a second B per set, the third pieces
 constexpr uint32_t kOffB2 = kOffB + kSets * kBBytes;
 constexpr uint32_t kOffPart = kOffB2 + kSets * kBBytes;
-// The int4-affine mixed-bit form (kFmtMix4, bf16 activations only): a unit's
-// codes, 128 bytes per row, land at the start of its stage with the 128-byte
-// swizzle (16-byte chunk j of row r at 16 (j ^ (r mod 8))); its 8 fp16 scales
-// and 8 fp16 biases per row (16 bytes each, row after row) land in the B2
-// region, which only the fp32 form's third pieces use otherwise: stage s's
+// The mixed-bit forms (kFmtMix4, kFmtMix2; bf16 activations only): a unit's
+// codes, 128 (int4) or 64 (int2) bytes per row, land at the start of its stage
+// with the 128-byte swizzle (16-byte chunk j of row r at 16 (j ^ (r mod 8)))
+// or the 64-byte swizzle (at 16 (j ^ (r / 2 mod 4))); its 8 fp16 scales and,
+// for int4, 8 fp16 biases per row (16 bytes each, row after row) land in the
+// B2 region, which only the fp32 form's third pieces use otherwise: stage s's
 // scales at kOffB2 + s kMixScaleBytes, its biases 2 KB further on.
 constexpr uint32_t kMixCodeBytes = kTileRows * 128;
 constexpr uint32_t kMixScaleBytes = 2 * kTileRows * 16;
 constexpr uint32_t kMixStageBytes = kMixCodeBytes + kMixScaleBytes;
+constexpr uint32_t kMix2StageBytes = kTileRows * 64 + kTileRows * 16;
 static_assert(kMixCodeBytes <= kRawStageBytes && kStages * kMixScaleBytes <= kSets * kBBytes,
               "the mixed-bit form's stages fit the raw ring and the B2 region");
 static_assert(kRawStageBytes % 1024 == 0 && kOffB2 % 1024 == 0, "swizzled copies want 1024-byte aligned stages");
@@ -251,8 +253,29 @@ __device__ __forceinline__ void codes_mix4_e4m3(const uint32_t (&v)[36], uint32_
     }
 }
 
+// int2-symmetric mixed-bit form: half H of a unit (groups 4H .. 4H + 3, code
+// words 8H .. 8H + 7 of the row's 16; a word holds 16 weights, field e in bits
+// 2e, 2e + 1) -> 32 TMEM columns of e4m3 values q 2^-9 (exact), one K-step of
+// 8 columns per group.  The fields of a 4-weight column are picked as the
+// nibbles of a byte-permute selector (w >> 2s masked with 0x3333: fields s,
+// s + 2, s + 4, s + 6) into a table of the four e4m3 bytes 0, +1, -2, -1 (the
+// two's-complement values 0, 1, -2, -1), so K positions 8i .. 8i + 7 of a
+// group hold its weights 8i + 0, 2, 4, 6, 1, 3, 5, 7, as in the int4 form.
+template <int H>
+__device__ __forceinline__ void codes_mix2_e4m3(const uint32_t (&v)[36], uint32_t (&col)[32]) {
+    constexpr uint32_t kTable = 0x81820100u;     // byte f: e4m3 of the field's value f - 4 (f >> 1)
+#pragma unroll
+    for (int t = 0; t < 8; ++t) {
+        const uint32_t w = v[8 * H + t];
+        const uint32_t sel[4] = {w & 0x3333u, (w >> 2) & 0x3333u, (w >> 16) & 0x3333u, (w >> 18) & 0x3333u};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) asm("prmt.b32 %0, %1, 0, %2;" : "=r"(col[4 * t + i]) : "r"(kTable), "r"(sel[i]));
+    }
+}
+
 // The eight bytes of an activation chunk's piece (element order) in the order
-// codes_mix4_e4m3 gives a code word's weights: the even elements, then the odd.
+// codes_mix4_e4m3 and codes_mix2_e4m3 give a chunk's weights: the even
+// elements, then the odd.
 __device__ __forceinline__ uint2 perm_mix4(uint2 b) {
     uint32_t lo, hi;
     asm("prmt.b32 %0, %1, %2, 0x6420;" : "=r"(lo) : "r"(b.x), "r"(b.y));
@@ -713,10 +736,16 @@ __device__ __forceinline__ void build_x_table(uint32_t sbase, const void* x, int
 // its 16 bytes: low nibbles first); Q4_K d sc_j q, the part the pieces
 // multiply (its min term dmin m_j is applied to the exact sum of x); the
 // int4-affine form sc_j c (nibble k of the 128 code bytes, lowest first, then
-// the eight fp16 scales at byte 128; its bias takes the exact sum of x).
+// the eight fp16 scales at byte 128; its bias takes the exact sum of x); the
+// int2 form sc_j q (2-bit field k of the 64 code bytes, scales at byte 64).
 template <int FMT>
 __device__ __forceinline__ float unit_weight(const uint8_t* b, int k) {
-    if constexpr (FMT == kFmtMix4) {
+    if constexpr (FMT == kFmtMix2) {
+        // field k of the 64 code bytes (two's complement), scales at byte 64
+        const int f = (int)(((uint32_t)b[k >> 2] >> (2 * (k & 3))) & 3u);
+        const int j = k >> 5;
+        return half_bits_to_float((uint32_t)b[64 + 2 * j] | ((uint32_t)b[65 + 2 * j] << 8)) * (float)(f - 4 * (f >> 1));
+    } else if constexpr (FMT == kFmtMix4) {
         const uint32_t code = ((uint32_t)b[k >> 1] >> (4 * (k & 1))) & 15u;
         const int j = k >> 5;
         return half_bits_to_float((uint32_t)b[128 + 2 * j] | ((uint32_t)b[129 + 2 * j] << 8)) * (float)code;
@@ -750,9 +779,9 @@ template <int FMT>
 __device__ __forceinline__ float unit_check_term(const uint32_t (&dv)[16], const uint32_t (&dd)[4], const float (&c)[8],
                                                  const float (&a)[8]) {
     float q = 0.f;
-    if constexpr (FMT == kFmtQ4 || FMT == kFmtMix4) {
+    if constexpr (FMT == kFmtQ4 || FMT == kFmtMix4 || FMT == kFmtMix2) {
         // dd[p]: the scales of blocks 2p and 2p + 1 as an fp16 pair (Q4_0's d,
-        // the mixed-bit form's sc)
+        // the mixed-bit forms' sc)
 #pragma unroll
         for (int p = 0; p < 4; ++p) {
             const float2 d = half2_to_float2(dd[p]);
@@ -794,17 +823,20 @@ __device__ __forceinline__ bool segment_needs_correction(float q) { return q > 0
 // its pieces carry, formed again from x (group g, elements 256 g ..
 // 256 g + 255; block scales from table slot sl) and the row's raw bytes read
 // from global memory at wrow (16-byte aligned; the stage holding them has
-// long been released): 144 bytes, or for the int4-affine form 128 code bytes
-// and the 16 bytes of scales at srow.  For the segments the read-back check
-// flags; slow, and exact up to fp32 rounding.
+// long been released): 144 bytes, or for the mixed-bit forms 128 (int4) or
+// 64 (int2) code bytes and the 16 bytes of scales at srow.  For the segments
+// the read-back check flags; slow, and exact up to fp32 rounding.
 template <int FMT, int XP, bool kCoherent>
 __device__ __noinline__ float unit_correction(const uint8_t* wrow, const void* x, int g, uint32_t sbase, int sl,
                                               const uint8_t* srow = nullptr) {
+    // 16-byte pieces of the row's unit: codes, then (mixed-bit) the scales
+    constexpr int kCodeChunks = FMT == kFmtMix2 ? 4 : (FMT == kFmtMix4 ? 8 : 9);
+    constexpr bool kScales = FMT == kFmtMix2 || FMT == kFmtMix4;
     uint8_t b[144];
 #pragma unroll
-    for (int j = 0; j < 9; ++j)
+    for (int j = 0; j < kCodeChunks + (kScales ? 1 : 0); ++j)
         *reinterpret_cast<uint4*>(b + 16 * j) =
-            __ldg(reinterpret_cast<const uint4*>(FMT == kFmtMix4 && j == 8 ? srow : wrow + 16 * j));
+            __ldg(reinterpret_cast<const uint4*>(j == kCodeChunks ? srow : wrow + 16 * j));
     float corr = 0.f;
     for (int k = 0; k < kGroupK; ++k) {
         const uint32_t cb = lds32(sbase + kOffXc + (uint32_t)sl * 32u + (uint32_t)(k >> 5) * 4u);

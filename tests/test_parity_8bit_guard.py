@@ -183,6 +183,23 @@ def test_mixbit4_outliers_on_zero_weights(qbw, oracle, xdt):
     check_matvec(to_f64(y), y_ref, S2, what=f"mixbit4 outliers {xdt}")
 
 
+@pytest.mark.parametrize("xdt", ["bf16", "f32"])
+def test_mixbit2_outliers_on_zero_weights(qbw, oracle, xdt):
+    # 16384 x 2048 int2 fields are 8.4 MB: bf16 x takes the tensor-core form
+    x, outliers = worst_case_activations(xdt, seed=61 if xdt == "bf16" else 62)
+    qp, sc, _ = synth.mixbit_weights(2, N, K, 32, seed=63)
+    q = qp.view(np.uint8).reshape(N, K // 4)
+    for blk, pos in outliers:
+        k = 32 * blk + pos
+        q[:, k // 4] &= np.uint8(0xFF ^ (3 << (2 * (k % 4))))      # field 0: weight 0
+    y = torch.full((N,), float("nan"), dtype=torch.float32, device="cuda")
+    qbw.qmv_mixbit(2, dev_u8(qp.view(np.uint8)), dev_u8(sc.view(np.uint8)), None, 32, dev_act(x), y, 1, N, K)
+    torch.cuda.synchronize()
+    assert qbw.fault_read(clear=True) == 0
+    y_ref, S, _ = oracle.qmv_mixbit(2, qp, sc, None, 32, x, N, K)
+    check_matvec(to_f64(y), y_ref, S, what=f"mixbit2 outliers {xdt}")
+
+
 def test_chain_step_outliers_on_zero_weights(qbw, oracle):
     # the chained form builds the same table and applies the same correction;
     # one step, its x the worst case, bit-identical to the separate call

@@ -12,6 +12,12 @@ Shapes cover one and two rows per warp item, ragged row counts, rows shorter
 than one pass of the warp, groups smaller and larger than a 16-byte word
 group, per-channel scales (group = K), and the 31B profile's 5376 x 21504 and
 21504 x 5376 shapes in full.
+
+int4-affine and int2-symmetric matrices with groups of 32 and bf16 x take the
+tensor-core 8-bit form from 5 MB (int4) or 4 MB (int2) of codes (10 and 5 MB
+for K <= 4096): the test_tc* cases cover ragged tiles, short and long rows,
+constant fields, zero scales, repeatability and the fallback to the CUDA-core
+kernel for scale arrays that are not 16-byte aligned.
 """
 import numpy as np
 import pytest
@@ -137,66 +143,81 @@ def test_largest_k(qbw, oracle, bits, K):
     assert err.value.status == 2           # QBW_ESHAPE
 
 
-# int4-affine, groups of 32, bf16 x, at least 8 MB of codes: the tensor-core
-# form.  (rows, K): a ragged last tile, the shortest rows (one K-group), the
-# 31B profile's K, and long rows (84 K-groups)
-TC_SHAPES = [(3077, 5376), (62501, 256), (12000, 1536), (4000, 21504)]
+# int4-affine and int2-symmetric, groups of 32, bf16 x, at least 5 MB (int4)
+# or 4 MB (int2) of codes (10 and 5 MB for K <= 4096): the tensor-core form.
+# (rows, K): a ragged last tile, the shortest rows (one K-group), the 31B
+# profile's K, and long rows (84 K-groups)
+TC_SHAPES = {4: [(3077, 5376), (80001, 256), (14000, 1536), (4000, 21504)],
+             2: [(3077, 5376), (125001, 256), (24000, 1536), (4000, 21504)]}
+TC_CASES = [(b, N, K) for b in (4, 2) for N, K in TC_SHAPES[b]]
 
 
-@pytest.mark.parametrize("N,K", TC_SHAPES)
+def two_complement(field, bits):
+    return field - (1 << bits) if bits != 4 and field >= (1 << (bits - 1)) else field
+
+
+@pytest.mark.parametrize("bits,N,K", TC_CASES)
 @pytest.mark.parametrize("odt", [torch.float32, torch.bfloat16])
-def test_tc_int4(qbw, oracle, N, K, odt):
-    qp, sc, bi = synth.mixbit_weights(4, N, K, 32, seed=N + K)
+def test_tc(qbw, oracle, bits, N, K, odt):
+    qp, sc, bi = synth.mixbit_weights(bits, N, K, 32, seed=N + K + bits)
     x = synth.activations(K, seed=K + 5, dtype="bf16")
-    y = run(qbw, 4, qp, sc, bi, 32, x, N, K, odt)
-    y_ref, _, S2 = oracle.qmv_mixbit(4, qp, sc, bi, 32, x, N, K)
-    check_matvec(to_f64(y), y_ref, S2, out_bf16=(odt == torch.bfloat16), what=f"tc int4 {N}x{K}")
+    y = run(qbw, bits, qp, sc, bi, 32, x, N, K, odt)
+    y_ref, _, S2 = oracle.qmv_mixbit(bits, qp, sc, bi, 32, x, N, K)
+    check_matvec(to_f64(y), y_ref, S2, out_bf16=(odt == torch.bfloat16), what=f"tc int{bits} {N}x{K}")
 
 
-@pytest.mark.parametrize("field", [0, 15, 8])
-def test_tc_int4_constant_fields(qbw, oracle, field):
-    # every code equal: y[n] = sum over groups of (sc c + bi) * sum(x over the group)
+@pytest.mark.parametrize("bits,field", [(4, 0), (4, 15), (4, 8), (2, 0), (2, 1), (2, 2), (2, 3)])
+def test_tc_constant_fields(qbw, oracle, bits, field):
+    # every code equal: y[n] = sum over groups of (sc q + bi) * sum(x over the group)
     N, K, G = 3077, 5376, 32
-    qp = synth.pack_fields(np.full((N, K), field, dtype=np.uint32), 4)
-    _, sc, bi = synth.mixbit_weights(4, N, K, G, seed=field + 3)
+    qp = synth.pack_fields(np.full((N, K), field, dtype=np.uint32), bits)
+    _, sc, bi = synth.mixbit_weights(bits, N, K, G, seed=field + 3)
     x = synth.activations(K, seed=field + 4, dtype="bf16")
-    y = to_f64(run(qbw, 4, qp, sc, bi, G, x, N, K))
+    y = to_f64(run(qbw, bits, qp, sc, bi, G, x, N, K))
     xs = (x.astype(np.uint32) << 16).view(np.float32).astype(np.float64).reshape(K // G, G).sum(axis=1)
     s = sc.view(np.float16).astype(np.float64).reshape(N, K // G)
-    b = bi.view(np.float16).astype(np.float64).reshape(N, K // G)
-    ref = ((s * field + b) * xs).sum(axis=1)
-    _, _, S2 = oracle.qmv_mixbit(4, qp, sc, bi, G, x, N, K)
-    check_matvec(y, ref, S2, what=f"tc constant int4 {field}")
+    b = bi.view(np.float16).astype(np.float64).reshape(N, K // G) if bits == 4 else 0.0
+    ref = ((s * two_complement(field, bits) + b) * xs).sum(axis=1)
+    _, _, S2 = oracle.qmv_mixbit(bits, qp, sc, bi, G, x, N, K)
+    if bits == 2 and field == 0:
+        assert np.all(y == 0)          # every weight is 0
+    check_matvec(y, ref, S2, what=f"tc constant int{bits} {field}")
 
 
-def test_tc_int4_zero_scales_and_biases(qbw):
+@pytest.mark.parametrize("bits", [4, 2])
+def test_tc_zero_scales(qbw, bits):
     N, K = 3077, 5376
-    qp, sc, bi = synth.mixbit_weights(4, N, K, 32, seed=2)
-    y = run(qbw, 4, qp, np.zeros_like(sc), np.zeros_like(bi), 32, synth.activations(K, seed=3, dtype="bf16"), N, K)
+    qp, sc, bi = synth.mixbit_weights(bits, N, K, 32, seed=2)
+    y = run(qbw, bits, qp, np.zeros_like(sc), None if bi is None else np.zeros_like(bi), 32,
+            synth.activations(K, seed=3, dtype="bf16"), N, K)
     assert torch.all(y == 0)
 
 
-def test_tc_int4_deterministic(qbw):
+@pytest.mark.parametrize("bits", [4, 2])
+def test_tc_deterministic(qbw, bits):
     N, K = 21504, 5376
-    qp, sc, bi = synth.mixbit_weights(4, N, K, 32, seed=21)
+    qp, sc, bi = synth.mixbit_weights(bits, N, K, 32, seed=21)
     x = synth.activations(K, seed=22, dtype="bf16")
-    a = run(qbw, 4, qp, sc, bi, 32, x, N, K)
-    b = run(qbw, 4, qp, sc, bi, 32, x, N, K)
+    a = run(qbw, bits, qp, sc, bi, 32, x, N, K)
+    b = run(qbw, bits, qp, sc, bi, 32, x, N, K)
     assert torch.equal(a.view(torch.int32), b.view(torch.int32))
 
 
-def test_tc_int4_unaligned_scales_fall_back(qbw, oracle):
-    # scales and biases 4 bytes past a 16-byte boundary: the CUDA-core kernel
+@pytest.mark.parametrize("bits", [4, 2])
+def test_tc_unaligned_scales_fall_back(qbw, oracle, bits):
+    # scales (and biases) 4 bytes past a 16-byte boundary: the CUDA-core kernel
     N, K = 3077, 5376
-    qp, sc, bi = synth.mixbit_weights(4, N, K, 32, seed=31)
+    qp, sc, bi = synth.mixbit_weights(bits, N, K, 32, seed=31)
     x = synth.activations(K, seed=32, dtype="bf16")
-    sc_buf = torch.zeros(sc.nbytes + 16, dtype=torch.uint8, device="cuda")
-    bi_buf = torch.zeros(bi.nbytes + 16, dtype=torch.uint8, device="cuda")
-    sc_buf[4:4 + sc.nbytes] = dev(sc)
-    bi_buf[4:4 + bi.nbytes] = dev(bi)
+
+    def shifted(a):
+        buf = torch.zeros(a.nbytes + 16, dtype=torch.uint8, device="cuda")
+        buf[4:4 + a.nbytes] = dev(a)
+        return buf[4:4 + a.nbytes]
+
     y = torch.full((N,), float("nan"), dtype=torch.float32, device="cuda")
-    qbw.qmv_mixbit(4, dev(qp), sc_buf[4:4 + sc.nbytes], bi_buf[4:4 + bi.nbytes], 32, dev_act(x), y, 1, N, K)
+    qbw.qmv_mixbit(bits, dev(qp), shifted(sc), None if bi is None else shifted(bi), 32, dev_act(x), y, 1, N, K)
     torch.cuda.synchronize()
     assert qbw.fault_read(clear=True) == 0
-    y_ref, _, S2 = oracle.qmv_mixbit(4, qp, sc, bi, 32, x, N, K)
-    check_matvec(to_f64(y), y_ref, S2, what="int4 unaligned scales")
+    y_ref, _, S2 = oracle.qmv_mixbit(bits, qp, sc, bi, 32, x, N, K)
+    check_matvec(to_f64(y), y_ref, S2, what=f"int{bits} unaligned scales")
