@@ -655,22 +655,26 @@ qbw_status qmv_mixbit(qbw_mixbit kind, const void* qp, const void* sc, const voi
     if (!x || !y) return QBW_EINVAL;
     if (!valid_dtype(xt) || !valid_dtype(yt)) return QBW_EDTYPE;
     if (M != 1) return QBW_ESHAPE;
-    if (qmv_mixbit_smem_bytes((int)kind, K, group) > kMixMaxSmem) return QBW_ESHAPE;
     if ((uintptr_t)x % 16 || (uintptr_t)y % dtype_size(yt)) return QBW_EALIGN;
     const size_t ybytes = (size_t)N * dtype_size(yt), sbytes = (size_t)N * (size_t)(K / group) * 2;
     if (overlaps(y, ybytes, x, (size_t)K * dtype_size(xt)) || overlaps(y, ybytes, qp, wbytes) ||
         overlaps(y, ybytes, sc, sbytes) || (kind == QBW_MIXBIT_INT4_AFFINE && overlaps(y, ybytes, bi, sbytes)))
         return QBW_EINVAL;
+    // int4-affine and int2-symmetric with groups of 32 and bf16 x: the
+    // tensor-core 8-bit form from mix_tc_min_bytes of codes (and where the
+    // device's plan allows it); otherwise the CUDA-core kernel, which stages x
+    // in shared memory, so its rows are bounded
+    const int bits = (int)kind;
+    const bool tc_form = (bits == 4 || bits == 2) && group == 32 && xt == QBW_BF16 && K % 256 == 0 &&
+                         (double)wbytes >= mix_tc_min_bytes(bits, K) && (uintptr_t)sc % 16 == 0 &&
+                         (bits == 2 || (uintptr_t)bi % 16 == 0);
+    const bool cuda_fits = qmv_mixbit_smem_bytes(bits, K, group) <= kMixMaxSmem;
+    if (!tc_form && !cuda_fits) return QBW_ESHAPE;
     DeviceInfo* di = nullptr;
     st = device_info(&di);
     if (st != QBW_OK) return st;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    // int4-affine and int2-symmetric with groups of 32 and bf16 x: the
-    // tensor-core 8-bit form from mix_tc_min_bytes of codes
-    const int bits = (int)kind;
-    if ((bits == 4 || bits == 2) && group == 32 && xt == QBW_BF16 && K % 256 == 0 &&
-        (double)wbytes >= mix_tc_min_bytes(bits, K) && (uintptr_t)sc % 16 == 0 &&
-        (bits == 2 || (uintptr_t)bi % 16 == 0) && qmv_mix_tc_supported(N, K, di->sm_count)) {
+    if (tc_form && qmv_mix_tc_supported(N, K, di->sm_count)) {
         CUtensorMap maps[3];
         if (encode_mix_maps(maps, bits, qp, sc, bi, N, K)) {
             cudaError_t e = launch_qmv_mix_tc(bits, maps, qp, sc, x, y, yt == QBW_BF16, (int)N, (int)K,
@@ -678,6 +682,7 @@ qbw_status qmv_mixbit(qbw_mixbit kind, const void* qp, const void* sc, const voi
             return e == cudaSuccess ? QBW_OK : QBW_ECUDA;
         }
     }
+    if (!cuda_fits) return QBW_ESHAPE;
     cudaError_t e = launch_qmv_mixbit((int)kind, qp, sc, bi, (int)group, x, xt == QBW_BF16, y, yt == QBW_BF16, (int)N,
                                       (int)K, di->sm_count, s);
     return e == cudaSuccess ? QBW_OK : QBW_ECUDA;

@@ -257,9 +257,11 @@ __device__ __forceinline__ void codes_mix4_e4m3(const uint32_t (&v)[36], uint32_
 // words 8H .. 8H + 7 of the row's 16; a word holds 16 weights, field e in bits
 // 2e, 2e + 1) -> 32 TMEM columns of e4m3 values q 2^-9 (exact), one K-step of
 // 8 columns per group.  The fields of a 4-weight column are picked as the
-// nibbles of a byte-permute selector (w >> 2s masked with 0x3333: fields s,
-// s + 2, s + 4, s + 6) into a table of the four e4m3 bytes 0, +1, -2, -1 (the
-// two's-complement values 0, 1, -2, -1), so K positions 8i .. 8i + 7 of a
+// nibbles of a byte-permute selector into a table of the four e4m3 bytes 0,
+// +1, -2, -1 (the two's-complement values 0, 1, -2, -1): w masked with
+// 0x33333333 holds fields 0, 2, 4, 6 in its low and 8, 10, 12, 14 in its high
+// 16 bits, w >> 2 so masked fields 1, 3, 5, 7 and 9, 11, 13, 15 (the permute
+// reads the low 16 bits of its selector).  So K positions 8i .. 8i + 7 of a
 // group hold its weights 8i + 0, 2, 4, 6, 1, 3, 5, 7, as in the int4 form.
 template <int H>
 __device__ __forceinline__ void codes_mix2_e4m3(const uint32_t (&v)[36], uint32_t (&col)[32]) {
@@ -267,7 +269,8 @@ __device__ __forceinline__ void codes_mix2_e4m3(const uint32_t (&v)[36], uint32_
 #pragma unroll
     for (int t = 0; t < 8; ++t) {
         const uint32_t w = v[8 * H + t];
-        const uint32_t sel[4] = {w & 0x3333u, (w >> 2) & 0x3333u, (w >> 16) & 0x3333u, (w >> 18) & 0x3333u};
+        const uint32_t e = w & 0x33333333u, o = (w >> 2) & 0x33333333u;
+        const uint32_t sel[4] = {e, o, e >> 16, o >> 16};
 #pragma unroll
         for (int i = 0; i < 4; ++i) asm("prmt.b32 %0, %1, 0, %2;" : "=r"(col[4 * t + i]) : "r"(kTable), "r"(sel[i]));
     }

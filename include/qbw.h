@@ -318,10 +318,11 @@ typedef enum qbw_mixbit {
  * scratch above.  Every other call takes the CUDA-core kernel.
  *
  *   x : K activations of xt, 16-byte aligned;  y : N outputs of yt
- *   M == 1; N >= 1; K as above, and small enough that the activations (4 K
- *   bytes, 4.5 K for int4) and the copy rings (40 to 98 KB; the larger rings
- *   only for K <= 8192) fit one CTA's shared memory (227 KB): K up to 37,000
- *   in every format and group size, else QBW_ESHAPE
+ *   M == 1; N >= 1; K as above.  On the CUDA-core kernel K must also be small
+ *   enough that the activations (4 K bytes, 4.5 K for int4) and the copy rings
+ *   (40 to 98 KB; the larger rings only for K <= 8192) fit one CTA's shared
+ *   memory (227 KB): K up to 37,000 in every format and group size, else
+ *   QBW_ESHAPE.  Calls that take the tensor cores have no such bound.
  */
 qbw_status qmv_mixbit(qbw_mixbit kind, const void *qp, const void *sc, const void *bi, int64_t group,
                       const void *x, qbw_dtype xt, void *y, qbw_dtype yt, int64_t M, int64_t N, int64_t K,

@@ -221,3 +221,20 @@ def test_tc_unaligned_scales_fall_back(qbw, oracle, bits):
     assert qbw.fault_read(clear=True) == 0
     y_ref, _, S2 = oracle.qmv_mixbit(bits, qp, sc, bi, 32, x, N, K)
     check_matvec(to_f64(y), y_ref, S2, what=f"int{bits} unaligned scales")
+
+
+@pytest.mark.parametrize("bits", [4, 2])
+def test_tc_long_rows(qbw, oracle, bits):
+    # K = 86016 (336 K-groups): beyond what the CUDA-core kernel can stage,
+    # taken by the tensor-core form (every 128-row tile split across about 67
+    # CTAs); the same row length with fp32 x (CUDA cores) is rejected
+    N, K = 200, 86016
+    qp, sc, bi = synth.mixbit_weights(bits, N, K, 32, seed=71 + bits)
+    x = synth.activations(K, seed=72, dtype="bf16")
+    y = run(qbw, bits, qp, sc, bi, 32, x, N, K)
+    y_ref, _, S2 = oracle.qmv_mixbit(bits, qp, sc, bi, 32, x, N, K)
+    check_matvec(to_f64(y), y_ref, S2, what=f"tc int{bits} K={K}")
+    y32 = torch.empty(N, dtype=torch.float32, device="cuda")
+    with pytest.raises(qbw.QbwError) as err:
+        qbw.qmv_mixbit(bits, dev(qp), dev(sc), dev(bi), 32, dev_act(synth.activations(K, seed=72)), y32, 1, N, K)
+    assert err.value.status == 2           # QBW_ESHAPE
