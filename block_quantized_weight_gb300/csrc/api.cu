@@ -249,13 +249,14 @@ bool encode_q4_tile_map(CUtensorMap* m, const void* w, int64_t N, int64_t K) {
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// The int4-affine (bits = 4) or int2-symmetric (bits = 2) mixed-bit matrices
-// with groups of 32, for the tensor-core kernel: m[0] the codes as [N][K b /
-// 64] 8-byte words, box (4 b, 128) (one 256-element K-group of a 128-row
-// tile, 32 b bytes per row) with the 128-byte (int4) or 64-byte (int2)
-// swizzle; m[1] and, for int4, m[2] the fp16 scales and biases as [N][K / 128]
-// 8-byte words, box (2, 128) (the group's 8 of each per row).  Needs K % 256
-// == 0 and 16-byte aligned arrays.
+// The int4-affine (bits = 4), int2-symmetric (bits = 2) or int8 (bits = 8)
+// mixed-bit matrices with groups of 32, for the tensor-core kernel: m[0] the
+// codes as [N][K b / 64] 8-byte words, box (4 b, 128) (one 256-element K-group
+// of a 128-row tile, 32 b bytes per row; int8: half of it, 128 bytes, per
+// copy) with the 128-byte (int4, int8) or 64-byte (int2) swizzle; m[1] and,
+// for int4, m[2] the fp16 scales and biases as [N][K / 128] 8-byte words, box
+// (2, 128) (the group's 8 of each per row).  Needs K % 256 == 0 and 16-byte
+// aligned arrays.
 bool encode_mix_maps(CUtensorMap* m, int bits, const void* qp, const void* sc, const void* bi, int64_t N,
                      int64_t K) {
     PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
@@ -265,9 +266,9 @@ bool encode_mix_maps(CUtensorMap* m, int bits, const void* qp, const void* sc, c
     {
         cuuint64_t dims[2] = {(cuuint64_t)(K * bits / 64), (cuuint64_t)N};
         cuuint64_t strides[1] = {(cuuint64_t)(K * bits / 8)};
-        cuuint32_t box[2] = {(cuuint32_t)(4 * bits), rows};      // 256 weights of b bits
+        cuuint32_t box[2] = {(cuuint32_t)(bits == 8 ? 16 : 4 * bits), rows};      // 256 weights of b bits (int8: 128)
         if (enc(&m[0], CU_TENSOR_MAP_DATA_TYPE_UINT64, 2, const_cast<void*>(qp), dims, strides, box, estr,
-                CU_TENSOR_MAP_INTERLEAVE_NONE, bits == 4 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
+                CU_TENSOR_MAP_INTERLEAVE_NONE, bits == 2 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B,
                 CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
             return false;
     }
@@ -642,9 +643,12 @@ static qbw_status mixbit_args(qbw_mixbit kind, const void* qp, const void* sc, c
 // CUDA cores; int4: 2048 x 5376 6.7 vs 7.7 us, 4096 x 4096 6.1 vs 6.0, 4096 x
 // 2048 5.5 vs 3.5, 16384 x 2048 7.2 vs 8.5, 21504 x 5376 14.5 vs 27.3; int2:
 // 2048 x 5376 6.7 vs 4.7, 3077 x 5376 6.7 vs 6.8, 4096 x 4096 6.0 vs 6.2,
-// 4096 x 2048 5.4 vs 3.3, 16384 x 2048 7.1 vs 8.1, 21504 x 5376 13.5 vs 24.9).
+// 4096 x 2048 5.4 vs 3.3, 16384 x 2048 7.1 vs 8.1, 21504 x 5376 13.5 vs 24.9;
+// int8: 2048 x 5376 8.2 vs 8.3, 3077 x 5376 8.6 vs 8.7, 5376 x 5376 9.9 vs
+// 12.8, 4096 x 4096 7.9 vs 6.6, 16384 x 2048 9.7 vs 9.0, 21504 x 5376 23.6 vs
+// 29.9).
 constexpr double mix_tc_min_bytes(int bits, int64_t K) {
-    return bits == 4 ? (K > 4096 ? 5e6 : 10e6) : (K > 4096 ? 4e6 : 5e6);
+    return bits == 8 ? (K > 4096 ? 16e6 : 64e6) : bits == 4 ? (K > 4096 ? 5e6 : 10e6) : (K > 4096 ? 4e6 : 5e6);
 }
 
 qbw_status qmv_mixbit(qbw_mixbit kind, const void* qp, const void* sc, const void* bi, int64_t group, const void* x,
@@ -665,7 +669,7 @@ qbw_status qmv_mixbit(qbw_mixbit kind, const void* qp, const void* sc, const voi
     // device's plan allows it); otherwise the CUDA-core kernel, which stages x
     // in shared memory, so its rows are bounded
     const int bits = (int)kind;
-    const bool tc_form = (bits == 4 || bits == 2) && group == 32 && xt == QBW_BF16 && K % 256 == 0 &&
+    const bool tc_form = group == 32 && xt == QBW_BF16 && K % 256 == 0 &&
                          (double)wbytes >= mix_tc_min_bytes(bits, K) && (uintptr_t)sc % 16 == 0 &&
                          (bits == 2 || (uintptr_t)bi % 16 == 0);
     const bool cuda_fits = qmv_mixbit_smem_bytes(bits, K, group) <= kMixMaxSmem;

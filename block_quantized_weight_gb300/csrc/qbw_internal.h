@@ -20,10 +20,10 @@ enum FaultCode : unsigned int {
     kFaultGridWait = 6,          // a chain's CTAs waited in vain for the others between steps
 };
 
-// kFmtMix4, kFmtMix2: the int4-affine and int2-symmetric mixed-bit matrices
-// with groups of 32 (codes, scales and, for int4, biases in their own
-// arrays), on the tensor-core M = 1 kernel only
-enum : int { kFmtQ8 = 0, kFmtQ4 = 1, kFmtQ4K = 2, kFmtMix4 = 3, kFmtMix2 = 4 };
+// kFmtMix4, kFmtMix2, kFmtMix8: the int4-affine, int2-symmetric and int8
+// mixed-bit matrices with groups of 32 (codes, scales and, for int4, biases in
+// their own arrays), on the tensor-core M = 1 kernel only
+enum : int { kFmtQ8 = 0, kFmtQ4 = 1, kFmtQ4K = 2, kFmtMix4 = 3, kFmtMix2 = 4, kFmtMix8 = 5 };
 
 // Bytes of one row of K weights: Q8_0 34 and Q4_0 18 per 32 weights; Q4_K
 // 144 per 256-weight super-block.

@@ -102,7 +102,11 @@ __device__ __forceinline__ void qmv_tc_body(const QtcParams& p) {
     // 8-bit form with bf16 activations only (their scales and biases take the
     // B2 region)
     constexpr bool MIX4 = FMT == kFmtMix4, MIX2 = FMT == kFmtMix2, MIX = MIX4 || MIX2;
-    static_assert(!MIX || F8 == 2, "mixed-bit form: two pieces");
+    // the int8 mixed-bit matrices: the two-operand 8-bit form (q = l + 16 h),
+    // bf16 activations; a unit's 256 code bytes per row take two ring stages of
+    // 128 bytes each, both with the unit's scales
+    constexpr bool MIX8 = FMT == kFmtMix8;
+    static_assert(!(MIX || MIX8) || F8 == 2, "mixed-bit forms: two pieces");
     // the 8-bit form of Q4_K: one A operand (codes 0..15), 8 K-steps per unit
     constexpr bool Q4K8 = F8 != 0 && FMT == kFmtQ4K;
     // one A operand of codes 0..15 (Q4_K or the mixed-bit form)
@@ -159,10 +163,30 @@ __device__ __forceinline__ void qmv_tc_body(const QtcParams& p) {
         asm volatile("bar.arrive 1, %0;" ::"n"(kThreads) : "memory");
         if (lane == 0) {
             prefetch_tmap(&p.tmap_w[0]);
-            if (NMAT == 2 || MIX) prefetch_tmap(&p.tmap_w[1]);
+            if (NMAT == 2 || MIX || MIX8) prefetch_tmap(&p.tmap_w[1]);
             if constexpr (MIX4) prefetch_tmap(&p.tmap_bi);
             // weights do not depend on the preceding grid: start streaming now
-            for (int i = 0; i < n && ok; ++i) {
+            if constexpr (MIX8) {
+                // unit i's halves in ring stages (2i) % 6 and (2i + 1) % 6: codes
+                // (16 words of a row), then the unit's scales (2 words)
+                for (int i = 0; i < n && ok; ++i) {
+                    const int u = u0 + i, t = u / G, g = u - t * G;
+                    for (int hs = 0; hs < 2; ++hs) {
+                        const int q = 2 * i + hs, s = q % kStages;
+                        if (q >= kStages)
+                            ok = mbar_wait_bounded(empty_bar(bar0, s), (uint32_t)((q / kStages) - 1) & 1u, p.fault,
+                                                   kFaultBulkWaitTimeout);
+                        if (!ok) break;
+                        const uint32_t dst = sbase + (uint32_t)s * kRawStageBytes;
+                        mbar_arrive_expect_tx(full_bar(bar0, s), kMix8StageBytes);
+                        tma_load_2d(dst, &p.tmap_w[0], g * 32 + 16 * hs, t * kTileRows, full_bar(bar0, s),
+                                    policy_evict_first());
+                        tma_load_2d(dst + kMixCodeBytes, &p.tmap_w[1], g * 2, t * kTileRows, full_bar(bar0, s),
+                                    policy_evict_first());
+                    }
+                }
+            }
+            for (int i = 0; i < (MIX8 ? 0 : n) && ok; ++i) {
                 const int s = i % kStages;
                 if (i >= kStages)
                     ok = mbar_wait_bounded(empty_bar(bar0, s), (uint32_t)((i / kStages) - 1) & 1u, p.fault,
@@ -267,7 +291,7 @@ __device__ __forceinline__ void qmv_tc_body(const QtcParams& p) {
         const uint32_t lanes = (uint32_t)(32 * q) << 16;
         const uint32_t a_taddr = tmem + lanes + (uint32_t)set * kACols;
         const uint32_t d_taddr = tmem + lanes + kDCol + 32u * (uint32_t)set;   // + 16 (k % 2)
-        const uint32_t raw_row = (uint32_t)(32 * q + lane) * (MIX4 ? 128u : (MIX2 ? 64u : 144u));
+        const uint32_t raw_row = (uint32_t)(32 * q + lane) * ((MIX4 || MIX8) ? 128u : (MIX2 ? 64u : 144u));
         const uint32_t bbuf = sbase + kOffB + (uint32_t)set * kBBytes;
         // The lane's 8-element slot xl of the group's activations: Q4_0, lanes
         // 0..7 load slots 8q .. 8q + 7 and write them into B; Q4_K, every lane
@@ -303,8 +327,8 @@ __device__ __forceinline__ void qmv_tc_body(const QtcParams& p) {
             const int cnt = n > 0 ? min(G, (u1 - 1) / NMAT - u0 / NMAT + 1) : 0;
             if (cnt > kXtGroups) record_fault(p.fault, kFaultPlan);
             // (with the groups' sums of x where a min or bias term takes them)
-            build_x_table<false, F8, Q4K8 || MIX4>(sbase, p.x, xg0, G, min(cnt, kXtGroups), warp, lane,
-                                                   kProducerWarp);
+            build_x_table<false, F8, Q4K8 || MIX4, MIX8>(sbase, p.x, xg0, G, min(cnt, kXtGroups), warp, lane,
+                                                         kProducerWarp);
             asm volatile("bar.sync 2, %0;" ::"n"(kProducerWarp * 32) : "memory");
         }
         bool counted = !contrib0;
@@ -358,10 +382,10 @@ __device__ __forceinline__ void qmv_tc_body(const QtcParams& p) {
                     if (sl < 0) sl += G;
                     if (sl >= kXtGroups) sl = 0;
                     if (!group_flagged(sbase, sl)) continue;     // no residuals
-                    if constexpr (MIX)
+                    if constexpr (MIX || MIX8)
                         corr += unit_correction<FMT, 2, false>(
-                            p.w[0] + nrow * p.row_bytes + (int64_t)g * (MIX4 ? 128 : 64), p.x, g, sbase, sl,
-                            reinterpret_cast<const uint8_t*>(p.msc + nrow * (p.K / 32) + (int64_t)g * 8));
+                            p.w[0] + nrow * p.row_bytes + (int64_t)g * (MIX8 ? 256 : (MIX4 ? 128 : 64)), p.x, g,
+                            sbase, sl, reinterpret_cast<const uint8_t*>(p.msc + nrow * (p.K / 32) + (int64_t)g * 8));
                     else
                         corr += unit_correction<FMT, F8 ? F8 : 2, false>(
                             p.w[m] + nrow * p.row_bytes + (int64_t)g * 144, p.x, g, sbase, sl);
@@ -421,7 +445,10 @@ __device__ __forceinline__ void qmv_tc_body(const QtcParams& p) {
             int k = 0;
             for (int i = set; i < n; i += kSets, ++k) {
                 const int u = u0 + i, ug = u / NMAT, mat = u - ug * NMAT, t = ug / G, g = ug - t * G;
-                const int s = i % kStages;
+                // the unit's ring stage and its completion parity (the int8 form:
+                // its first half's stage; the second follows it)
+                const int s = MIX8 ? (2 * i) % kStages : i % kStages;
+                const uint32_t spar = (uint32_t)((MIX8 ? 2 * i : i) / kStages) & 1u;
                 // this lane's eight activations of the group, loaded before the waits
                 uint4 xr0 = make_uint4(0u, 0u, 0u, 0u), xr1 = xr0;
                 if (loads_x) {
@@ -436,8 +463,7 @@ __device__ __forceinline__ void qmv_tc_body(const QtcParams& p) {
                         xr1 = __ldg(reinterpret_cast<const uint4*>(static_cast<const float*>(p.x) + e + 4));
                     }
                 }
-                const bool got = mbar_wait_bounded(full_bar(bar0, s), (uint32_t)(i / kStages) & 1u, p.fault,
-                                                   kFaultBulkWaitTimeout);
+                const bool got = mbar_wait_bounded(full_bar(bar0, s), spar, p.fault, kFaultBulkWaitTimeout);
                 if (!__all_sync(0xffffffffu, got)) {
                     ok = false;
                     break;
@@ -446,7 +472,22 @@ __device__ __forceinline__ void qmv_tc_body(const QtcParams& p) {
                 uint32_t v[36];
                 uint32_t dd[4];
                 [[maybe_unused]] uint32_t bb[4];
-                if constexpr (MIX) {
+                if constexpr (MIX8) {
+                    // the first half's 8 swizzled code chunks, then the unit's scales
+    #pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        const uint4 w = lds128(src + (((uint32_t)j ^ (uint32_t)(row & 7)) << 4));
+                        v[4 * j] = w.x;
+                        v[4 * j + 1] = w.y;
+                        v[4 * j + 2] = w.z;
+                        v[4 * j + 3] = w.w;
+                    }
+                    const uint4 sv = lds128(sbase + (uint32_t)s * kRawStageBytes + kMixCodeBytes + (uint32_t)row * 16u);
+                    dd[0] = sv.x;
+                    dd[1] = sv.y;
+                    dd[2] = sv.z;
+                    dd[3] = sv.w;
+                } else if constexpr (MIX) {
                     // the row's 8 (4) swizzled code chunks, then its scales (and biases)
     #pragma unroll
                     for (int j = 0; j < (MIX4 ? 8 : 4); ++j) {
@@ -539,6 +580,7 @@ __device__ __forceinline__ void qmv_tc_body(const QtcParams& p) {
                 int cur_sl = 0;
                 uint2 bp0 = make_uint2(0u, 0u);
                 [[maybe_unused]] uint2 bp1 = bp0, bp2 = bp0;     // the 8-bit forms' second and third pieces
+                [[maybe_unused]] uint2 bq0 = bp0, bq1 = bp0;     // the int8 form's pieces times 16
                 if constexpr (F8) {
                     cur_sl = g - xg0;
                     if (cur_sl < 0) cur_sl += G;
@@ -552,6 +594,10 @@ __device__ __forceinline__ void qmv_tc_body(const QtcParams& p) {
                             bp0 = perm_mix4(bp0);
                             bp1 = perm_mix4(bp1);
                         }
+                        if constexpr (MIX8) {    // the second K-step's pieces: 16 x
+                            bq0 = times16_e4m3(bp0);
+                            bq1 = times16_e4m3(bp1);
+                        }
                         if constexpr (F8 == 3)
                             asm volatile("ld.shared.v2.b32 {%0, %1}, [%2];"
                                          : "=r"(bp2.x), "=r"(bp2.y)
@@ -562,6 +608,7 @@ __device__ __forceinline__ void qmv_tc_body(const QtcParams& p) {
                 // ---- half 0: K 0..127 (block pairs 0, 1; B atoms 0, 1 written by warps 0, 1)
                 if constexpr (MIX4) codes_mix4_e4m3<0>(v, c0);
                 else if constexpr (MIX2) codes_mix2_e4m3<0>(v, c0);
+                else if constexpr (MIX8) codes_mix8_e4m3<0>(v, c0);
                 else if constexpr (Q4K8) codes_q4k_e4m3<0>(v, c0);
                 else if constexpr (F8) codes_pair_e4m3<0>(v, c0);
                 else codes_pair<FMT, 0>(v, c0);
@@ -581,8 +628,8 @@ __device__ __forceinline__ void qmv_tc_body(const QtcParams& p) {
                     } else if constexpr (F8) {
                         sts64(f8_p0, bp0);
                         sts64(f8_p1, bp1);
-                        sts64(f8_n0, make_uint2(bp0.x ^ 0x80808080u, bp0.y ^ 0x80808080u));
-                        sts64(f8_n1, make_uint2(bp1.x ^ 0x80808080u, bp1.y ^ 0x80808080u));
+                        sts64(f8_n0, MIX8 ? bq0 : make_uint2(bp0.x ^ 0x80808080u, bp0.y ^ 0x80808080u));
+                        sts64(f8_n1, MIX8 ? bq1 : make_uint2(bp1.x ^ 0x80808080u, bp1.y ^ 0x80808080u));
                         if constexpr (F8 == 3) {     // third pieces: B2, the second piece's rows
                             sts64(f8_p1 + (kOffB2 - kOffB), bp2);
                             sts64(f8_n1 + (kOffB2 - kOffB), make_uint2(bp2.x ^ 0x80808080u, bp2.y ^ 0x80808080u));
@@ -595,7 +642,8 @@ __device__ __forceinline__ void qmv_tc_body(const QtcParams& p) {
                 }
                 tmem_st32(a_taddr, c0);
                 if constexpr (!ONE_OP) {
-                    if constexpr (F8) codes_pair_e4m3<1>(v, c1);
+                    if constexpr (MIX8) codes_mix8_e4m3<1>(v, c1);
+                    else if constexpr (F8) codes_pair_e4m3<1>(v, c1);
                     else codes_pair<FMT, 1>(v, c1);
                     tmem_wait_st();
                     tmem_st32(a_taddr + 32u, c1);
@@ -605,8 +653,30 @@ __device__ __forceinline__ void qmv_tc_body(const QtcParams& p) {
                 __syncwarp();
                 if (lane == 0) mbar_arrive(afull_bar(bar0, set, 0));
                 // ---- half 1: K 128..255 (block pairs 2, 3; B atoms 2, 3 written by warps 2, 3)
+                if constexpr (MIX8) {
+                    // the second half's codes, in the unit's next ring stage
+                    const int s1 = (2 * i + 1) % kStages;
+                    const bool got1 = mbar_wait_bounded(full_bar(bar0, s1), (uint32_t)((2 * i + 1) / kStages) & 1u,
+                                                        p.fault, kFaultBulkWaitTimeout);
+                    if (!__all_sync(0xffffffffu, got1)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t src1 = sbase + (uint32_t)s1 * kRawStageBytes + raw_row;
+    #pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        const uint4 w = lds128(src1 + (((uint32_t)j ^ (uint32_t)(row & 7)) << 4));
+                        v[4 * j] = w.x;
+                        v[4 * j + 1] = w.y;
+                        v[4 * j + 2] = w.z;
+                        v[4 * j + 3] = w.w;
+                    }
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(empty_bar(bar0, s1));
+                }
                 if constexpr (MIX4) codes_mix4_e4m3<1>(v, c0);
                 else if constexpr (MIX2) codes_mix2_e4m3<1>(v, c0);
+                else if constexpr (MIX8) codes_mix8_e4m3<0>(v, c0);
                 else if constexpr (Q4K8) codes_q4k_e4m3<1>(v, c0);
                 else if constexpr (F8) codes_pair_e4m3<2>(v, c0);
                 else codes_pair<FMT, 2>(v, c0);
@@ -626,8 +696,8 @@ __device__ __forceinline__ void qmv_tc_body(const QtcParams& p) {
                     } else if constexpr (F8) {
                         sts64(f8_p0, bp0);
                         sts64(f8_p1, bp1);
-                        sts64(f8_n0, make_uint2(bp0.x ^ 0x80808080u, bp0.y ^ 0x80808080u));
-                        sts64(f8_n1, make_uint2(bp1.x ^ 0x80808080u, bp1.y ^ 0x80808080u));
+                        sts64(f8_n0, MIX8 ? bq0 : make_uint2(bp0.x ^ 0x80808080u, bp0.y ^ 0x80808080u));
+                        sts64(f8_n1, MIX8 ? bq1 : make_uint2(bp1.x ^ 0x80808080u, bp1.y ^ 0x80808080u));
                         if constexpr (F8 == 3) {     // third pieces: B2, the second piece's rows
                             sts64(f8_p1 + (kOffB2 - kOffB), bp2);
                             sts64(f8_n1 + (kOffB2 - kOffB), make_uint2(bp2.x ^ 0x80808080u, bp2.y ^ 0x80808080u));
@@ -642,7 +712,8 @@ __device__ __forceinline__ void qmv_tc_body(const QtcParams& p) {
                     tmem_st32(a_taddr + 32u, c0);
                 } else {
                     tmem_st32(a_taddr + 64u, c0);
-                    if constexpr (F8) codes_pair_e4m3<3>(v, c1);
+                    if constexpr (MIX8) codes_mix8_e4m3<1>(v, c1);
+                    else if constexpr (F8) codes_pair_e4m3<3>(v, c1);
                     else codes_pair<FMT, 3>(v, c1);
                     tmem_wait_st();
                     tmem_st32(a_taddr + 96u, c1);
@@ -869,6 +940,11 @@ __global__ void __launch_bounds__(kThreads, 1) qmv_mix2_tc_e4m3_kernel(const __g
     qmv_tc_body<kFmtMix2, 1, 1, 2>(p);
 }
 
+// the int8 mixed-bit matrices (groups of 32), the two-operand 8-bit form
+__global__ void __launch_bounds__(kThreads, 1) qmv_mix8_tc_e4m3_kernel(const __grid_constant__ QtcParams p) {
+    qmv_tc_body<kFmtMix8, 1, 1, 2>(p);
+}
+
 // Every kernel of this file may take kSmemBytes of dynamic shared memory (once
 // per device and thread).
 cudaError_t prepare_qtc_kernels() {
@@ -879,7 +955,8 @@ cudaError_t prepare_qtc_kernels() {
     for (auto f : {qmv_q4_0_tc_kernel<1, 1>, qmv_q4_0_tc_kernel<2, 1>, qmv_q4_0_tc_kernel<1, 2>,
                    qmv_q4_0_tc_e4m3_kernel<1, 2>, qmv_q4_0_tc_e4m3_kernel<2, 2>, qmv_q4_0_tc_e4m3_kernel<1, 3>,
                    qmv_q4_0_tc_e4m3_kernel<2, 3>, qmv_q4_k_tc_kernel, qmv_q4_k_tc_e4m3_kernel<2>,
-                   qmv_q4_k_tc_e4m3_kernel<3>, qmv_mix4_tc_e4m3_kernel, qmv_mix2_tc_e4m3_kernel}) {
+                   qmv_q4_k_tc_e4m3_kernel<3>, qmv_mix4_tc_e4m3_kernel, qmv_mix2_tc_e4m3_kernel,
+                   qmv_mix8_tc_e4m3_kernel}) {
         cudaError_t e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
         if (e != cudaSuccess) return e;
     }
@@ -987,14 +1064,14 @@ bool qmv_mix_tc_supported(int64_t N, int64_t K, int sm_count) {
     return table_fits(1, tiles * groups, groups, sm_count);
 }
 
-// bits = 4 or 2.  tmaps: the codes ([N][K b / 64] 8-byte words, box (4 b,
-// 128), the 128- or 64-byte swizzle), the scales and, for int4, the biases
+// bits = 4, 2 or 8.  tmaps: the codes ([N][K b / 64] 8-byte words, box (4 b,
+// 128) or for int8 (16, 128), the 128- or 64-byte swizzle), the scales and, for int4, the biases
 // ([N][K / 128] 8-byte words, box (2, 128)); qp and sc the same arrays, for
 // the read-back correction; bf16 x.
 cudaError_t launch_qmv_mix_tc(int bits, const CUtensorMap* tmaps, const void* qp, const void* sc, const void* x,
                               void* y, int y_bf16, int N, int K, int sm_count, unsigned int* fault,
                               cudaStream_t stream) {
-    if (bits != 2 && bits != 4) return cudaErrorInvalidValue;
+    if (bits != 2 && bits != 4 && bits != 8) return cudaErrorInvalidValue;
     QtcParams p;
     p.tmap_w[0] = tmaps[0];
     p.tmap_w[1] = tmaps[1];
@@ -1015,8 +1092,8 @@ cudaError_t launch_qmv_mix_tc(int bits, const CUtensorMap* tmaps, const void* qp
     p.x_bf16 = 1;
     p.y_bf16 = y_bf16;
     if (!table_fits(1, p.units, p.groups, sm_count)) return cudaErrorInvalidValue;
-    return launch_qtc(bits == 4 ? qmv_mix4_tc_e4m3_kernel : qmv_mix2_tc_e4m3_kernel, p,
-                      p.units < sm_count ? p.units : sm_count, stream);
+    return launch_qtc(bits == 4 ? qmv_mix4_tc_e4m3_kernel : (bits == 2 ? qmv_mix2_tc_e4m3_kernel : qmv_mix8_tc_e4m3_kernel),
+                      p, p.units < sm_count ? p.units : sm_count, stream);
 }
 
 }  // namespace qbw

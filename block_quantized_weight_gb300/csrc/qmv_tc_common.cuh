@@ -48,6 +48,11 @@ constexpr uint32_t kMixCodeBytes = kTileRows * 128;
 constexpr uint32_t kMixScaleBytes = 2 * kTileRows * 16;
 constexpr uint32_t kMixStageBytes = kMixCodeBytes + kMixScaleBytes;
 constexpr uint32_t kMix2StageBytes = kTileRows * 64 + kTileRows * 16;
+// int8: a unit's 256 code bytes per row take two ring stages; each holds 128
+// of them (128-byte swizzle) and, after them, the unit's 8 scales per row
+constexpr uint32_t kMix8StageBytes = kMixCodeBytes + kTileRows * 16;
+static_assert(kMix8StageBytes <= kRawStageBytes && kStages % 2 == 0 && (kStages / 2) % kSets == 0,
+              "the int8 form's half-units fill the ring two stages per unit, each set on its own pair");
 static_assert(kMixCodeBytes <= kRawStageBytes && kStages * kMixScaleBytes <= kSets * kBBytes,
               "the mixed-bit form's stages fit the raw ring and the B2 region");
 static_assert(kRawStageBytes % 1024 == 0 && kOffB2 % 1024 == 0, "swizzled copies want 1024-byte aligned stages");
@@ -274,6 +279,52 @@ __device__ __forceinline__ void codes_mix2_e4m3(const uint32_t (&v)[36], uint32_
 #pragma unroll
         for (int i = 0; i < 4; ++i) asm("prmt.b32 %0, %1, 0, %2;" : "=r"(col[4 * t + i]) : "r"(kTable), "r"(sel[i]));
     }
+}
+
+// int8 mixed-bit form: block pair P (blocks 2P, 2P + 1) of the half-unit
+// whose 32 code words are v[0..31] (a block's 32 bytes are words 8b .. 8b +
+// 7, byte = element) -> 32 TMEM columns, as the two-operand Q4_0 form: block
+// b's first K-step (8 columns) holds l = q & 15 (e4m3 bytes l 2^-9, exact)
+// and its second holds h = q >> 4 (-8 .. 7) as a signed e4m3 byte h 2^-9
+// (exact), against B columns of x and 16 x, so q = l + 16 h.  The signed byte
+// is sign | magnitude: with m the byte's sign replicated (a byte permute in
+// sign mode), magnitude = (n ^ (m & 15)) + (m & 1) for the high nibble n, and
+// the sign bit m & 0x80 joins it in one multiply-add.
+template <int P>
+__device__ __forceinline__ void codes_mix8_e4m3(const uint32_t (&v)[36], uint32_t (&col)[32]) {
+#pragma unroll
+    for (int b = 0; b < 2; ++b) {
+#pragma unroll
+        for (int t = 0; t < 8; ++t) {
+            const uint32_t w = v[16 * P + 8 * b + t];
+            uint32_t m;
+            asm("prmt.b32 %0, %1, 0, 0xBA98;" : "=r"(m) : "r"(w));
+            const uint32_t n = (w >> 4) & 0x0F0F0F0Fu;
+            col[16 * b + t] = w & 0x0F0F0F0Fu;
+            col[16 * b + 8 + t] = (m & 0x01010101u) * 0x81u + (n ^ (m & 0x0F0F0F0Fu));
+        }
+    }
+}
+
+// Eight e4m3 activation pieces times 16, exactly (the int8 form's second
+// K-step): through fp16, where the product is exact and the result, below 2^8,
+// is representable in e4m3 again.
+__device__ __forceinline__ uint2 times16_e4m3(uint2 b) {
+    const uint32_t w[2] = {b.x, b.y};
+    uint32_t r[2];
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+        uint32_t h0, h1;
+        asm("{\n\t.reg .b16 t;\n\tcvt.u16.u32 t, %1;\n\tcvt.rn.f16x2.e4m3x2 %0, t;\n\t}" : "=r"(h0) : "r"(w[i] & 0xFFFFu));
+        asm("{\n\t.reg .b16 t;\n\tcvt.u16.u32 t, %1;\n\tcvt.rn.f16x2.e4m3x2 %0, t;\n\t}" : "=r"(h1) : "r"(w[i] >> 16));
+        asm("mul.rn.f16x2 %0, %0, %1;" : "+r"(h0) : "r"(0x4C004C00u));     // x 16
+        asm("mul.rn.f16x2 %0, %0, %1;" : "+r"(h1) : "r"(0x4C004C00u));
+        unsigned short e0, e1;
+        asm("cvt.rn.satfinite.e4m3x2.f16x2 %0, %1;" : "=h"(e0) : "r"(h0));
+        asm("cvt.rn.satfinite.e4m3x2.f16x2 %0, %1;" : "=h"(e1) : "r"(h1));
+        r[i] = (uint32_t)e0 | ((uint32_t)e1 << 16);
+    }
+    return make_uint2(r[0], r[1]);
 }
 
 // The eight bytes of an activation chunk's piece (element order) in the order
@@ -597,7 +648,11 @@ __device__ __forceinline__ void load_x_chunk(const void* x, int xg0, int G, int 
     }
 }
 
-template <int XP, bool kSums>
+// kLow: the int8 form's table, whose second K-step multiplies the pieces by
+// 16: each block's largest |x| goes to [2^3, 2^4) instead of [2^7, 2^8), so
+// that 16 times a piece stays below 2^8 (e4m3 reaches 448), and the bound on
+// what the pieces miss takes Wmax = 128 (|q| <= 128) per unit of the scale.
+template <int XP, bool kSums, bool kLow = false>
 __device__ __forceinline__ void table_chunk(uint32_t sbase, int c, int lane, uint4 xa, uint4 xb) {
     if constexpr (kSums) {
         // the block's sum of x (Q4_K's min term): 8 elements per lane, 4 lanes
@@ -633,7 +688,7 @@ __device__ __forceinline__ void table_chunk(uint32_t sbase, int c, int lane, uin
     }
     mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
     mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-    const int es = min(max(261 - (int)mx, 9), 253);
+    const int es = min(max((kLow ? 257 : 261) - (int)mx, 9), 253);
     const float sc = __uint_as_float((uint32_t)es << 23);
     uint2 q0, q1, q2;
     if constexpr (XP == 2) {
@@ -703,7 +758,7 @@ __device__ __forceinline__ void table_chunk(uint32_t sbase, int c, int lane, uin
     rsum += __shfl_xor_sync(0xffffffffu, rsum, 2);
     if ((lane & 3) == 0)
         asm volatile("st.shared.f32 [%0], %1;" ::"r"(sbase + kOffXr + (uint32_t)(c >> 2) * 4u),
-                     "f"(rsum * (kSums ? 15.f : 8.f) * (1.f + kPieceEps))
+                     "f"(rsum * (kLow ? 128.f : (kSums ? 15.f : 8.f)) * (1.f + kPieceEps))
                      : "memory");
     // the group's flag: the sign bit of block 0's read-back factor (a
     // positive power of two), stored by lane 0, which holds block 0's es
@@ -715,7 +770,7 @@ __device__ __forceinline__ void table_chunk(uint32_t sbase, int c, int lane, uin
     }
 }
 
-template <bool kCoherent, int XP, bool kSums = false>
+template <bool kCoherent, int XP, bool kSums = false, bool kLow = false>
 __device__ __forceinline__ void build_x_table(uint32_t sbase, const void* x, int xg0, int G, int cnt, int w,
                                               int lane, int nwarps) {
     // a warp's chunks are 32 consecutive ones (block j = lanes 4j .. 4j + 3);
@@ -730,7 +785,8 @@ __device__ __forceinline__ void build_x_table(uint32_t sbase, const void* x, int
             if (c0 + j * stride < nch) load_x_chunk<kCoherent, XP>(x, xg0, G, c0 + j * stride + lane, xa[j], xb[j]);
 #pragma unroll
         for (int j = 0; j < 4; ++j)
-            if (c0 + j * stride < nch) table_chunk<XP, kSums>(sbase, c0 + j * stride + lane, lane, xa[j], xb[j]);
+            if (c0 + j * stride < nch)
+                table_chunk<XP, kSums, kLow>(sbase, c0 + j * stride + lane, lane, xa[j], xb[j]);
     }
 }
 
@@ -740,10 +796,16 @@ __device__ __forceinline__ void build_x_table(uint32_t sbase, const void* x, int
 // multiply (its min term dmin m_j is applied to the exact sum of x); the
 // int4-affine form sc_j c (nibble k of the 128 code bytes, lowest first, then
 // the eight fp16 scales at byte 128; its bias takes the exact sum of x); the
-// int2 form sc_j q (2-bit field k of the 64 code bytes, scales at byte 64).
+// int2 form sc_j q (2-bit field k of the 64 code bytes, scales at byte 64);
+// the int8 form sc_j q (byte k of the 256 code bytes, scales at byte 256).
 template <int FMT>
 __device__ __forceinline__ float unit_weight(const uint8_t* b, int k) {
-    if constexpr (FMT == kFmtMix2) {
+    if constexpr (FMT == kFmtMix8) {
+        // byte k of the 256 code bytes (two's complement), scales at byte 256
+        const int j = k >> 5;
+        return half_bits_to_float((uint32_t)b[256 + 2 * j] | ((uint32_t)b[257 + 2 * j] << 8)) *
+               (float)(int)(int8_t)b[k];
+    } else if constexpr (FMT == kFmtMix2) {
         // field k of the 64 code bytes (two's complement), scales at byte 64
         const int f = (int)(((uint32_t)b[k >> 2] >> (2 * (k & 3))) & 3u);
         const int j = k >> 5;
@@ -782,7 +844,7 @@ template <int FMT>
 __device__ __forceinline__ float unit_check_term(const uint32_t (&dv)[16], const uint32_t (&dd)[4], const float (&c)[8],
                                                  const float (&a)[8]) {
     float q = 0.f;
-    if constexpr (FMT == kFmtQ4 || FMT == kFmtMix4 || FMT == kFmtMix2) {
+    if constexpr (FMT == kFmtQ4 || FMT == kFmtMix4 || FMT == kFmtMix2 || FMT == kFmtMix8) {
         // dd[p]: the scales of blocks 2p and 2p + 1 as an fp16 pair (Q4_0's d,
         // the mixed-bit forms' sc)
 #pragma unroll
@@ -826,16 +888,16 @@ __device__ __forceinline__ bool segment_needs_correction(float q) { return q > 0
 // its pieces carry, formed again from x (group g, elements 256 g ..
 // 256 g + 255; block scales from table slot sl) and the row's raw bytes read
 // from global memory at wrow (16-byte aligned; the stage holding them has
-// long been released): 144 bytes, or for the mixed-bit forms 128 (int4) or
-// 64 (int2) code bytes and the 16 bytes of scales at srow.  For the segments
-// the read-back check flags; slow, and exact up to fp32 rounding.
+// long been released): 144 bytes, or for the mixed-bit forms 256 (int8), 128
+// (int4) or 64 (int2) code bytes and the 16 bytes of scales at srow.  For the
+// segments the read-back check flags; slow, and exact up to fp32 rounding.
 template <int FMT, int XP, bool kCoherent>
 __device__ __noinline__ float unit_correction(const uint8_t* wrow, const void* x, int g, uint32_t sbase, int sl,
                                               const uint8_t* srow = nullptr) {
     // 16-byte pieces of the row's unit: codes, then (mixed-bit) the scales
-    constexpr int kCodeChunks = FMT == kFmtMix2 ? 4 : (FMT == kFmtMix4 ? 8 : 9);
-    constexpr bool kScales = FMT == kFmtMix2 || FMT == kFmtMix4;
-    uint8_t b[144];
+    constexpr int kCodeChunks = FMT == kFmtMix8 ? 16 : (FMT == kFmtMix2 ? 4 : (FMT == kFmtMix4 ? 8 : 9));
+    constexpr bool kScales = FMT == kFmtMix2 || FMT == kFmtMix4 || FMT == kFmtMix8;
+    uint8_t b[FMT == kFmtMix8 ? 272 : 144];
 #pragma unroll
     for (int j = 0; j < kCodeChunks + (kScales ? 1 : 0); ++j)
         *reinterpret_cast<uint4*>(b + 16 * j) =

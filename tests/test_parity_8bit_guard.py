@@ -200,6 +200,25 @@ def test_mixbit2_outliers_on_zero_weights(qbw, oracle, xdt):
     check_matvec(to_f64(y), y_ref, S, what=f"mixbit2 outliers {xdt}")
 
 
+@pytest.mark.parametrize("xdt", ["bf16", "f32"])
+def test_mixbit8_outliers_on_zero_weights(qbw, oracle, xdt):
+    # 32768 x 2048 int8 codes are 67 MB: bf16 x takes the tensor-core form,
+    # whose table puts each block's largest |x| lower (its second K-step takes
+    # 16 x) and bounds the pieces' loss with |q| <= 128
+    N8 = 32768
+    x, outliers = worst_case_activations(xdt, seed=81 if xdt == "bf16" else 82)
+    qp, sc, _ = synth.mixbit_weights(8, N8, K, 32, seed=83)
+    q = qp.view(np.uint8).reshape(N8, K)
+    for blk, pos in outliers:
+        q[:, 32 * blk + pos] = 0                                   # weight 0
+    y = torch.full((N8,), float("nan"), dtype=torch.float32, device="cuda")
+    qbw.qmv_mixbit(8, dev_u8(qp.view(np.uint8)), dev_u8(sc.view(np.uint8)), None, 32, dev_act(x), y, 1, N8, K)
+    torch.cuda.synchronize()
+    assert qbw.fault_read(clear=True) == 0
+    y_ref, S, _ = oracle.qmv_mixbit(8, qp, sc, None, 32, x, N8, K)
+    check_matvec(to_f64(y), y_ref, S, what=f"mixbit8 outliers {xdt}")
+
+
 def test_chain_step_outliers_on_zero_weights(qbw, oracle):
     # the chained form builds the same table and applies the same correction;
     # one step, its x the worst case, bit-identical to the separate call

@@ -13,9 +13,9 @@ than one pass of the warp, groups smaller and larger than a 16-byte word
 group, per-channel scales (group = K), and the 31B profile's 5376 x 21504 and
 21504 x 5376 shapes in full.
 
-int4-affine and int2-symmetric matrices with groups of 32 and bf16 x take the
-tensor-core 8-bit form from 5 MB (int4) or 4 MB (int2) of codes (10 and 5 MB
-for K <= 4096): the test_tc* cases cover ragged tiles, short and long rows,
+int4-affine, int2-symmetric and int8 matrices with groups of 32 and bf16 x
+take the tensor-core 8-bit form from 5 MB (int4), 4 MB (int2) or 16 MB (int8)
+of codes (10, 5 and 64 MB for K <= 4096): the test_tc* cases cover ragged tiles, short and long rows,
 constant fields, zero scales, repeatability and the fallback to the CUDA-core
 kernel for scale arrays that are not 16-byte aligned.
 """
@@ -143,13 +143,15 @@ def test_largest_k(qbw, oracle, bits, K):
     assert err.value.status == 2           # QBW_ESHAPE
 
 
-# int4-affine and int2-symmetric, groups of 32, bf16 x, at least 5 MB (int4)
-# or 4 MB (int2) of codes (10 and 5 MB for K <= 4096): the tensor-core form.
+# int4-affine, int2-symmetric and int8, groups of 32, bf16 x, at least 5 MB
+# (int4), 4 MB (int2) or 16 MB (int8) of codes (10, 5 and 64 MB for K <= 4096):
+# the tensor-core form.
 # (rows, K): a ragged last tile, the shortest rows (one K-group), the 31B
 # profile's K, and long rows (84 K-groups)
 TC_SHAPES = {4: [(3077, 5376), (80001, 256), (14000, 1536), (4000, 21504)],
-             2: [(3077, 5376), (125001, 256), (24000, 1536), (4000, 21504)]}
-TC_CASES = [(b, N, K) for b in (4, 2) for N, K in TC_SHAPES[b]]
+             2: [(3077, 5376), (125001, 256), (24000, 1536), (4000, 21504)],
+             8: [(3077, 5376), (250001, 256), (42000, 1536), (2000, 21504)]}
+TC_CASES = [(b, N, K) for b in (4, 2, 8) for N, K in TC_SHAPES[b]]
 
 
 def two_complement(field, bits):
@@ -166,7 +168,8 @@ def test_tc(qbw, oracle, bits, N, K, odt):
     check_matvec(to_f64(y), y_ref, S2, out_bf16=(odt == torch.bfloat16), what=f"tc int{bits} {N}x{K}")
 
 
-@pytest.mark.parametrize("bits,field", [(4, 0), (4, 15), (4, 8), (2, 0), (2, 1), (2, 2), (2, 3)])
+@pytest.mark.parametrize("bits,field", [(4, 0), (4, 15), (4, 8), (2, 0), (2, 1), (2, 2), (2, 3), (8, 0), (8, 127),
+                                        (8, 128), (8, 255), (8, 17)])
 def test_tc_constant_fields(qbw, oracle, bits, field):
     # every code equal: y[n] = sum over groups of (sc q + bi) * sum(x over the group)
     N, K, G = 3077, 5376, 32
@@ -179,12 +182,12 @@ def test_tc_constant_fields(qbw, oracle, bits, field):
     b = bi.view(np.float16).astype(np.float64).reshape(N, K // G) if bits == 4 else 0.0
     ref = ((s * two_complement(field, bits) + b) * xs).sum(axis=1)
     _, _, S2 = oracle.qmv_mixbit(bits, qp, sc, bi, G, x, N, K)
-    if bits == 2 and field == 0:
+    if bits != 4 and field == 0:
         assert np.all(y == 0)          # every weight is 0
     check_matvec(y, ref, S2, what=f"tc constant int{bits} {field}")
 
 
-@pytest.mark.parametrize("bits", [4, 2])
+@pytest.mark.parametrize("bits", [4, 2, 8])
 def test_tc_zero_scales(qbw, bits):
     N, K = 3077, 5376
     qp, sc, bi = synth.mixbit_weights(bits, N, K, 32, seed=2)
@@ -193,7 +196,7 @@ def test_tc_zero_scales(qbw, bits):
     assert torch.all(y == 0)
 
 
-@pytest.mark.parametrize("bits", [4, 2])
+@pytest.mark.parametrize("bits", [4, 2, 8])
 def test_tc_deterministic(qbw, bits):
     N, K = 21504, 5376
     qp, sc, bi = synth.mixbit_weights(bits, N, K, 32, seed=21)
@@ -203,7 +206,7 @@ def test_tc_deterministic(qbw, bits):
     assert torch.equal(a.view(torch.int32), b.view(torch.int32))
 
 
-@pytest.mark.parametrize("bits", [4, 2])
+@pytest.mark.parametrize("bits", [4, 2, 8])
 def test_tc_unaligned_scales_fall_back(qbw, oracle, bits):
     # scales (and biases) 4 bytes past a 16-byte boundary: the CUDA-core kernel
     N, K = 3077, 5376
@@ -223,7 +226,7 @@ def test_tc_unaligned_scales_fall_back(qbw, oracle, bits):
     check_matvec(to_f64(y), y_ref, S2, what=f"int{bits} unaligned scales")
 
 
-@pytest.mark.parametrize("bits", [4, 2])
+@pytest.mark.parametrize("bits", [4, 2, 8])
 def test_tc_long_rows(qbw, oracle, bits):
     # K = 86016 (336 K-groups): beyond what the CUDA-core kernel can stage,
     # taken by the tensor-core form (every 128-row tile split across about 67
