@@ -426,9 +426,11 @@ def supplementary_kernels(torch, qbw, hbm_peak):
         lambda i: (lambda: qbw.qmv_q4_0(ws[i], xg, yb, 1, N, K)))
     del ws, w
     # the mixed-bit formats (int2-symmetric, int4-affine, int8), 21504 x 5376,
-    # groups of 32, bf16 -> fp32
+    # groups of 32: bf16 -> fp32 (the tensor-core forms) and fp32 -> fp32 (the
+    # CUDA-core kernel)
     N, K, G = 21504, 5376, 32
     xm = bf16(synth.activations(K, seed=9, dtype="bf16"))
+    xm32 = torch.from_numpy(synth.activations(K, seed=9)).to(dev)
     y = torch.empty(N, device=dev)
     for bits in (2, 4, 8):
         qp, sc, bi = synth.mixbit_weights(bits, N, K, G, seed=9)
@@ -439,6 +441,8 @@ def supplementary_kernels(torch, qbw, hbm_peak):
         name = {2: "int2-symmetric", 4: "int4-affine", 8: "int8"}[bits]
         run(f"qmv_mixbit {name} {N}x{K} G={G} bf16->f32", nbytes + 2 * K + 4 * N, copies,
             lambda i, mats=mats, bits=bits: (lambda: qbw.qmv_mixbit(bits, *mats[i], G, xm, y, 1, N, K)))
+        run(f"qmv_mixbit {name} {N}x{K} G={G} f32->f32 (CUDA cores)", nbytes + 4 * K + 4 * N, copies,
+            lambda i, mats=mats, bits=bits: (lambda: qbw.qmv_mixbit(bits, *mats[i], G, xm32, y, 1, N, K)))
         del mats
     # small-M tiles
     for (N, K) in ((5376, 5376), (5376, 21504)):
@@ -881,20 +885,25 @@ def profile_case(args):
         call = lambda i: sweep.launches()
         nbytes = sum(b for _, _, b in sweep._specs)
     elif name.startswith("mixbit"):
-        # one mixed-bit matrix, 21504 x 5376, groups of 32, bf16 x, rotating
-        # copies larger than L2 together
-        bits = int(name[len("mixbit"):])
+        # one mixed-bit matrix, 21504 x 5376, groups of 32, bf16 x (the
+        # tensor-core forms), rotating copies larger than L2 together; with the
+        # suffix "_f32", fp32 x (the CUDA-core kernel)
+        f32x = name.endswith("_f32")
+        bits = int(name[len("mixbit"):].replace("_f32", ""))
         N, K, G = 21504, 5376, 32
         qp, sc, bi = synth.mixbit_weights(bits, N, K, G, seed=9)
         nb = synth.mixbit_bytes(bits, N, K, G)
         copies = max(2, int(np.ceil(300e6 / nb)))
         mats = [(torch.from_numpy(qp.view(np.uint8).copy()).to(dev), torch.from_numpy(sc.view(np.uint8).copy()).to(dev),
                  torch.from_numpy(bi.view(np.uint8).copy()).to(dev) if bi is not None else None) for _ in range(copies)]
-        xb = torch.from_numpy(synth.activations(K, seed=9, dtype="bf16").view(np.int16).copy()).view(
-            torch.bfloat16).to(dev)
+        if f32x:
+            xb = torch.from_numpy(synth.activations(K, seed=9)).to(dev)
+        else:
+            xb = torch.from_numpy(synth.activations(K, seed=9, dtype="bf16").view(np.int16).copy()).view(
+                torch.bfloat16).to(dev)
         y = torch.empty(N, device=dev)
         call = lambda i: qbw.qmv_mixbit(bits, *mats[i % copies], G, xb, y, 1, N, K)
-        nbytes = nb + 2 * K + 4 * N
+        nbytes = nb + (4 if f32x else 2) * K + 4 * N
     elif name in ("qmm", "qmm8", "qmm8_5376"):
         # M = 32 (whole-tile splits) or M = 8 (stream-K) over 5376 x 21504, or
         # M = 8 over 5376 x 5376 (cluster splits)
@@ -984,7 +993,8 @@ def main():
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--profile", choices=["q8_0", "q8_0_lmhead", "q4_0", "q4_0_bf16", "q4_k", "gateup", "qmm", "sweep",
-                                          "mixbit2", "mixbit4", "mixbit8", "qmm8", "qmm8_5376", "q4_0_stream",
+                                          "mixbit2", "mixbit4", "mixbit8", "mixbit2_f32", "mixbit4_f32",
+                                          "mixbit8_f32", "qmm8", "qmm8_5376", "q4_0_stream",
                                           "qmm2_qkv", "chain"],
                     help="run only one small case (for profiler captures): a single-matrix workload, or the "
                          "sweep's launches over 6 layers")
