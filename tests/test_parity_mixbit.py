@@ -146,11 +146,12 @@ def test_largest_k(qbw, oracle, bits, K):
 # int4-affine, int2-symmetric and int8, groups of 32, bf16 x, at least 5 MB
 # (int4), 4 MB (int2) or 16 MB (int8) of codes (10, 5 and 64 MB for K <= 4096):
 # the tensor-core form.
-# (rows, K): a ragged last tile, the shortest rows (one K-group), the 31B
-# profile's K, and long rows (84 K-groups)
+# (rows, K): a ragged last tile, the shortest rows (one K-group; int8: two, as
+# one K-group would need more rows than the split plan's tile limit allows
+# at its size threshold), the 31B profile's K, and long rows (84 K-groups)
 TC_SHAPES = {4: [(3077, 5376), (80001, 256), (14000, 1536), (4000, 21504)],
-             2: [(3077, 5376), (125001, 256), (24000, 1536), (4000, 21504)],
-             8: [(3077, 5376), (250001, 256), (42000, 1536), (2000, 21504)]}
+             2: [(3077, 5376), (78200, 256), (24000, 1536), (4000, 21504)],
+             8: [(3077, 5376), (125001, 512), (42000, 1536), (2000, 21504)]}
 TC_CASES = [(b, N, K) for b in (4, 2, 8) for N, K in TC_SHAPES[b]]
 
 
