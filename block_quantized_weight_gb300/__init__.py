@@ -80,6 +80,8 @@ def _declare(L):
         getattr(L, name).argtypes = [P, P, i64, i64, P]
     L.qmv_mixbit.restype = i32
     L.qmv_mixbit.argtypes = [i32, P, P, P, i64, P, i32, P, i32, i64, i64, i64, P]
+    L.qmv_mixbit_route.restype = i32
+    L.qmv_mixbit_route.argtypes = [i32, P, P, P, i64, i32, i64, i64, ctypes.POINTER(ctypes.c_int)]
     L.qdequant_mixbit.restype = i32
     L.qdequant_mixbit.argtypes = [i32, P, P, P, i64, P, i64, i64, P]
     L.qbw_fault_read.restype = i32
@@ -169,6 +171,16 @@ def qmv_mixbit(bits: int, qp, sc, bi, group: int, x, y, M: int, N: int, K: int, 
     _check(L.qmv_mixbit(bits, _ptr(qp), _ptr(sc), _ptr(bi) if bi is not None else None, group, _ptr(x),
                         _dtype_code(x), _ptr(y), _dtype_code(y), M, N, K, _stream(stream)), "qmv_mixbit")
     return y
+
+
+def qmv_mixbit_route(bits: int, qp, sc, bi, group: int, x, N: int, K: int) -> bool:
+    """Whether qmv_mixbit with these arguments (activations like ``x``) takes
+    the tensor-core form on the current device (test-only; launches nothing)."""
+    L = load()
+    tc = ctypes.c_int(-1)
+    _check(L.qmv_mixbit_route(bits, _ptr(qp), _ptr(sc), _ptr(bi) if bi is not None else None, group, _dtype_code(x),
+                              N, K, ctypes.byref(tc)), "qmv_mixbit_route")
+    return tc.value == 1
 
 
 def qdequant_mixbit(bits: int, qp, sc, bi, group: int, out, N: int, K: int, stream=None):

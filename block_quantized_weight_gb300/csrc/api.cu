@@ -651,6 +651,27 @@ constexpr double mix_tc_min_bytes(int bits, int64_t K) {
     return bits == 8 ? (K > 4096 ? 16e6 : 64e6) : bits == 4 ? (K > 4096 ? 5e6 : 10e6) : (K > 4096 ? 4e6 : 5e6);
 }
 
+// Which kernel a mixed-bit product takes (shared by qmv_mixbit and
+// qmv_mixbit_route).  Before the device is looked up: whether the call has the
+// tensor-core form's shape (groups of 32, bf16 x, K % 256, size, scale
+// alignment) and whether the CUDA-core kernel can stage its rows; after it,
+// whether the device's plan takes the call and its tensor maps encode.
+struct MixRoute {
+    bool tc_form, cuda_fits;
+};
+static MixRoute mix_route(int bits, const void* sc, const void* bi, int64_t group, qbw_dtype xt, size_t wbytes,
+                          int64_t K) {
+    MixRoute r;
+    r.tc_form = group == 32 && xt == QBW_BF16 && K % 256 == 0 && (double)wbytes >= mix_tc_min_bytes(bits, K) &&
+                (uintptr_t)sc % 16 == 0 && (bits != 4 || (uintptr_t)bi % 16 == 0);
+    r.cuda_fits = qmv_mixbit_smem_bytes(bits, K, group) <= kMixMaxSmem;
+    return r;
+}
+static bool mix_tc_maps(const MixRoute& r, int bits, const void* qp, const void* sc, const void* bi, int64_t N,
+                        int64_t K, const DeviceInfo& di, CUtensorMap* maps) {
+    return r.tc_form && qmv_mix_tc_supported(N, K, di.sm_count) && encode_mix_maps(maps, bits, qp, sc, bi, N, K);
+}
+
 qbw_status qmv_mixbit(qbw_mixbit kind, const void* qp, const void* sc, const void* bi, int64_t group, const void* x,
                       qbw_dtype xt, void* y, qbw_dtype yt, int64_t M, int64_t N, int64_t K, void* stream) {
     size_t wbytes = 0;
@@ -664,32 +685,47 @@ qbw_status qmv_mixbit(qbw_mixbit kind, const void* qp, const void* sc, const voi
     if (overlaps(y, ybytes, x, (size_t)K * dtype_size(xt)) || overlaps(y, ybytes, qp, wbytes) ||
         overlaps(y, ybytes, sc, sbytes) || (kind == QBW_MIXBIT_INT4_AFFINE && overlaps(y, ybytes, bi, sbytes)))
         return QBW_EINVAL;
-    // int4-affine and int2-symmetric with groups of 32 and bf16 x: the
-    // tensor-core 8-bit form from mix_tc_min_bytes of codes (and where the
-    // device's plan allows it); otherwise the CUDA-core kernel, which stages x
-    // in shared memory, so its rows are bounded
+    // groups of 32 and bf16 x: the tensor-core 8-bit form from
+    // mix_tc_min_bytes of codes (where the device's plan allows it); otherwise
+    // the CUDA-core kernel, which stages x in shared memory, so its rows are
+    // bounded
     const int bits = (int)kind;
-    const bool tc_form = group == 32 && xt == QBW_BF16 && K % 256 == 0 &&
-                         (double)wbytes >= mix_tc_min_bytes(bits, K) && (uintptr_t)sc % 16 == 0 &&
-                         (bits == 2 || (uintptr_t)bi % 16 == 0);
-    const bool cuda_fits = qmv_mixbit_smem_bytes(bits, K, group) <= kMixMaxSmem;
-    if (!tc_form && !cuda_fits) return QBW_ESHAPE;
+    const MixRoute r = mix_route(bits, sc, bi, group, xt, wbytes, K);
+    if (!r.tc_form && !r.cuda_fits) return QBW_ESHAPE;
     DeviceInfo* di = nullptr;
     st = device_info(&di);
     if (st != QBW_OK) return st;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    if (tc_form && qmv_mix_tc_supported(N, K, di->sm_count)) {
-        CUtensorMap maps[3];
-        if (encode_mix_maps(maps, bits, qp, sc, bi, N, K)) {
-            cudaError_t e = launch_qmv_mix_tc(bits, maps, qp, sc, x, y, yt == QBW_BF16, (int)N, (int)K,
-                                              di->sm_count, di->fault, s);
-            return e == cudaSuccess ? QBW_OK : QBW_ECUDA;
-        }
+    CUtensorMap maps[3];
+    if (mix_tc_maps(r, bits, qp, sc, bi, N, K, *di, maps)) {
+        cudaError_t e = launch_qmv_mix_tc(bits, maps, qp, sc, x, y, yt == QBW_BF16, (int)N, (int)K, di->sm_count,
+                                          di->fault, s);
+        return e == cudaSuccess ? QBW_OK : QBW_ECUDA;
     }
-    if (!cuda_fits) return QBW_ESHAPE;
+    if (!r.cuda_fits) return QBW_ESHAPE;
     cudaError_t e = launch_qmv_mixbit((int)kind, qp, sc, bi, (int)group, x, xt == QBW_BF16, y, yt == QBW_BF16, (int)N,
                                       (int)K, di->sm_count, s);
     return e == cudaSuccess ? QBW_OK : QBW_ECUDA;
+}
+
+qbw_status qmv_mixbit_route(qbw_mixbit kind, const void* qp, const void* sc, const void* bi, int64_t group,
+                            qbw_dtype xt, int64_t N, int64_t K, int* tensor_cores) {
+    if (!tensor_cores) return QBW_EINVAL;
+    size_t wbytes = 0;
+    qbw_status st = mixbit_args(kind, qp, sc, bi, group, N, K, &wbytes);
+    if (st != QBW_OK) return st;
+    if (!valid_dtype(xt)) return QBW_EDTYPE;
+    const int bits = (int)kind;
+    const MixRoute r = mix_route(bits, sc, bi, group, xt, wbytes, K);
+    if (!r.tc_form && !r.cuda_fits) return QBW_ESHAPE;
+    DeviceInfo* di = nullptr;
+    st = device_info(&di);
+    if (st != QBW_OK) return st;
+    CUtensorMap maps[3];
+    const bool tc = mix_tc_maps(r, bits, qp, sc, bi, N, K, *di, maps);
+    if (!tc && !r.cuda_fits) return QBW_ESHAPE;
+    *tensor_cores = tc ? 1 : 0;
+    return QBW_OK;
 }
 
 qbw_status qdequant_mixbit(qbw_mixbit kind, const void* qp, const void* sc, const void* bi, int64_t group, float* out,

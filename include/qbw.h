@@ -330,6 +330,16 @@ qbw_status qmv_mixbit(qbw_mixbit kind, const void *qp, const void *sc, const voi
                       void *stream);
 
 /*
+ * qmv_mixbit_route -- which kernel qmv_mixbit takes for these arguments on the
+ * current device: *tensor_cores = 1 for the tensor-core form, 0 for the
+ * CUDA-core kernel.  For testing.  Arguments as qmv_mixbit (xt the activation
+ * type); returns the status qmv_mixbit's argument checks would give, before
+ * any launch.  Launches nothing.
+ */
+qbw_status qmv_mixbit_route(qbw_mixbit kind, const void *qp, const void *sc, const void *bi, int64_t group,
+                            qbw_dtype xt, int64_t N, int64_t K, int *tensor_cores);
+
+/*
  * qdequant_mixbit -- out[n*K + k] = w[n, k] in fp32 (sc q exactly; sc c + bi
  * rounded once to nearest).  For testing.  Arguments as qmv_mixbit; out 4-byte
  * aligned.

@@ -159,11 +159,17 @@ def two_complement(field, bits):
     return field - (1 << bits) if bits != 4 and field >= (1 << (bits - 1)) else field
 
 
+def route(qbw, bits, qp, sc, bi, G, x, N, K):
+    """Whether the call takes the tensor-core form (asked of the library)."""
+    return qbw.qmv_mixbit_route(bits, dev(qp), dev(sc), dev(bi), G, dev_act(x), N, K)
+
+
 @pytest.mark.parametrize("bits,N,K", TC_CASES)
 @pytest.mark.parametrize("odt", [torch.float32, torch.bfloat16])
 def test_tc(qbw, oracle, bits, N, K, odt):
     qp, sc, bi = synth.mixbit_weights(bits, N, K, 32, seed=N + K + bits)
     x = synth.activations(K, seed=K + 5, dtype="bf16")
+    assert route(qbw, bits, qp, sc, bi, 32, x, N, K), "the case no longer takes the tensor-core form"
     y = run(qbw, bits, qp, sc, bi, 32, x, N, K, odt)
     y_ref, _, S2 = oracle.qmv_mixbit(bits, qp, sc, bi, 32, x, N, K)
     check_matvec(to_f64(y), y_ref, S2, out_bf16=(odt == torch.bfloat16), what=f"tc int{bits} {N}x{K}")
@@ -177,6 +183,7 @@ def test_tc_constant_fields(qbw, oracle, bits, field):
     qp = synth.pack_fields(np.full((N, K), field, dtype=np.uint32), bits)
     _, sc, bi = synth.mixbit_weights(bits, N, K, G, seed=field + 3)
     x = synth.activations(K, seed=field + 4, dtype="bf16")
+    assert route(qbw, bits, qp, sc, bi, G, x, N, K)
     y = to_f64(run(qbw, bits, qp, sc, bi, G, x, N, K))
     xs = (x.astype(np.uint32) << 16).view(np.float32).astype(np.float64).reshape(K // G, G).sum(axis=1)
     s = sc.view(np.float16).astype(np.float64).reshape(N, K // G)
@@ -219,8 +226,11 @@ def test_tc_unaligned_scales_fall_back(qbw, oracle, bits):
         buf[4:4 + a.nbytes] = dev(a)
         return buf[4:4 + a.nbytes]
 
+    sc_s, bi_s = shifted(sc), None if bi is None else shifted(bi)
+    assert route(qbw, bits, qp, sc, bi, 32, x, N, K)                   # aligned: tensor cores
+    assert not qbw.qmv_mixbit_route(bits, dev(qp), sc_s, bi_s, 32, dev_act(x), N, K)
     y = torch.full((N,), float("nan"), dtype=torch.float32, device="cuda")
-    qbw.qmv_mixbit(bits, dev(qp), shifted(sc), None if bi is None else shifted(bi), 32, dev_act(x), y, 1, N, K)
+    qbw.qmv_mixbit(bits, dev(qp), sc_s, bi_s, 32, dev_act(x), y, 1, N, K)
     torch.cuda.synchronize()
     assert qbw.fault_read(clear=True) == 0
     y_ref, _, S2 = oracle.qmv_mixbit(bits, qp, sc, bi, 32, x, N, K)
@@ -235,6 +245,7 @@ def test_tc_long_rows(qbw, oracle, bits):
     N, K = 200, 86016
     qp, sc, bi = synth.mixbit_weights(bits, N, K, 32, seed=71 + bits)
     x = synth.activations(K, seed=72, dtype="bf16")
+    assert route(qbw, bits, qp, sc, bi, 32, x, N, K)
     y = run(qbw, bits, qp, sc, bi, 32, x, N, K)
     y_ref, _, S2 = oracle.qmv_mixbit(bits, qp, sc, bi, 32, x, N, K)
     check_matvec(to_f64(y), y_ref, S2, what=f"tc int{bits} K={K}")
@@ -242,3 +253,21 @@ def test_tc_long_rows(qbw, oracle, bits):
     with pytest.raises(qbw.QbwError) as err:
         qbw.qmv_mixbit(bits, dev(qp), dev(sc), dev(bi), 32, dev_act(synth.activations(K, seed=72)), y32, 1, N, K)
     assert err.value.status == 2           # QBW_ESHAPE
+
+
+@pytest.mark.parametrize("bits", [2, 4, 8])
+def test_route_cuda_core_cases(qbw, bits):
+    # what stays on the CUDA-core kernel: fp32 x, groups other than 32, rows not
+    # a multiple of 256, and matrices below the size thresholds
+    N, K = 21504, 5376
+    qp, sc, bi = synth.mixbit_weights(bits, N, K, 32, seed=91)
+    xb = synth.activations(K, seed=92, dtype="bf16")
+    assert route(qbw, bits, qp, sc, bi, 32, xb, N, K)
+    assert not route(qbw, bits, qp, sc, bi, 32, synth.activations(K, seed=92), N, K)
+    qp64, sc64, bi64 = synth.mixbit_weights(bits, N, K, 64, seed=93)
+    assert not route(qbw, bits, qp64, sc64, bi64, 64, xb, N, K)
+    K2 = 5376 - 64                                             # 5312: K % 256 != 0
+    qp2, sc2, bi2 = synth.mixbit_weights(bits, N, K2, 32, seed=94)
+    assert not route(qbw, bits, qp2, sc2, bi2, 32, synth.activations(K2, seed=95, dtype="bf16"), N, K2)
+    qs, ss, bs = synth.mixbit_weights(bits, 300, K, 32, seed=96)
+    assert not route(qbw, bits, qs, ss, bs, 32, xb, 300, K)
