@@ -1,6 +1,7 @@
 // qmv_tc.cu -- the M = 1 (and two-token) Q4_0 matrix-vector product y = W x,
-// the fused Q4_0 gate+up, and the Q4_K product, on the fifth-generation tensor
-// cores (tcgen05), for K a multiple of 256.  A Q4_K super-block (256 weights,
+// the fused Q4_0 gate+up, the Q4_K product and the mixed-bit (int2, int4,
+// int8; groups of 32) products, on the fifth-generation tensor cores
+// (tcgen05), for K a multiple of 256.  A Q4_K super-block (256 weights,
 // 144 bytes) is exactly one unit's row segment; its codes enter A exactly
 // (0..15), and the read-back applies d sc_j to each sub-block's dot product
 // and subtracts dmin m_j times the sub-block's activation sum (the algebraic
@@ -109,7 +110,7 @@ __device__ __forceinline__ void qmv_tc_body(const QtcParams& p) {
     static_assert(!(MIX || MIX8) || F8 == 2, "mixed-bit forms: two pieces");
     // the 8-bit form of Q4_K: one A operand (codes 0..15), 8 K-steps per unit
     constexpr bool Q4K8 = F8 != 0 && FMT == kFmtQ4K;
-    // one A operand of codes 0..15 (Q4_K or the mixed-bit form)
+    // one A operand of codes (Q4_K's 0..15, the int4 and int2 mixed-bit forms)
     constexpr bool ONE_OP = Q4K8 || MIX;
     constexpr int kSteps = ONE_OP ? 8 : 16;
     extern __shared__ __align__(1024) uint8_t smem[];
