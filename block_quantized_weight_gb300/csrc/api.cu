@@ -36,9 +36,9 @@ cudaError_t launch_qmv_tc(int fmt, int nmat, int ntok, const CUtensorMap* tmap_w
                           unsigned int* fault, cudaStream_t stream, const QtcNextLaunch* next = nullptr);
 int qmm_tc_tile_rows();
 bool qmv_mix_tc_supported(int64_t N, int64_t K, int sm_count);
-cudaError_t launch_qmv_mix_tc(int bits, const CUtensorMap* tmaps, const void* qp, const void* sc, const void* x,
-                              void* y, int y_bf16, int N, int K, int sm_count, unsigned int* fault,
-                              cudaStream_t stream);
+cudaError_t launch_qmv_mix_tc(int bits, const CUtensorMap* tmaps, const void* qp, const void* sc, const void* bi,
+                              int gshift, const void* x, void* y, int y_bf16, int N, int K, int sm_count,
+                              unsigned int* fault, cudaStream_t stream);
 bool qmv_chain_step_supported(int nmat, int64_t N, int64_t K, int ctas);
 void qmv_chain_fill_step(ChainStepDesc* d, int nmat, int64_t N, int64_t K);
 int qmv_chain_ctas(int sm_count);
@@ -255,10 +255,11 @@ bool encode_q4_tile_map(CUtensorMap* m, const void* w, int64_t N, int64_t K) {
 // of a 128-row tile, 32 b bytes per row; int8: half of it, 128 bytes, per
 // copy) with the 128-byte (int4, int8) or 64-byte (int2) swizzle; m[1] and,
 // for int4, m[2] the fp16 scales and biases as [N][K / 128] 8-byte words, box
-// (2, 128) (the group's 8 of each per row).  Needs K % 256 == 0 and 16-byte
-// aligned arrays.
+// (2, 128) (the group's 8 of each per row; larger groups' scales and biases
+// are read by the kernel's threads, without a map).  Needs K % 256 == 0 and
+// 16-byte aligned arrays.
 bool encode_mix_maps(CUtensorMap* m, int bits, const void* qp, const void* sc, const void* bi, int64_t N,
-                     int64_t K) {
+                     int64_t K, int64_t group) {
     PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
     if (!enc) return false;
     const cuuint32_t rows = (cuuint32_t)qmm_tc_tile_rows();
@@ -273,7 +274,7 @@ bool encode_mix_maps(CUtensorMap* m, int bits, const void* qp, const void* sc, c
             return false;
     }
     const void* sb[2] = {sc, bi};
-    for (int i = 0; i < (bits == 4 ? 2 : 1); ++i) {
+    for (int i = 0; i < (group != 32 ? 0 : bits == 4 ? 2 : 1); ++i) {
         cuuint64_t dims[2] = {(cuuint64_t)(K / 128), (cuuint64_t)N};
         cuuint64_t strides[1] = {(cuuint64_t)(K / 16)};
         cuuint32_t box[2] = {2, rows};
@@ -653,8 +654,8 @@ constexpr double mix_tc_min_bytes(int bits, int64_t K) {
 
 // Which kernel a mixed-bit product takes (shared by qmv_mixbit and
 // qmv_mixbit_route).  Before the device is looked up: whether the call has the
-// tensor-core form's shape (groups of 32, bf16 x, K % 256, size, scale
-// alignment) and whether the CUDA-core kernel can stage its rows; after it,
+// tensor-core form's shape (groups of 32 or a larger power of two, bf16 x, K %
+// 256, size, scale alignment) and whether the CUDA-core kernel can stage its rows; after it,
 // whether the device's plan takes the call and its tensor maps encode.
 struct MixRoute {
     bool tc_form, cuda_fits;
@@ -662,14 +663,16 @@ struct MixRoute {
 static MixRoute mix_route(int bits, const void* sc, const void* bi, int64_t group, qbw_dtype xt, size_t wbytes,
                           int64_t K) {
     MixRoute r;
-    r.tc_form = group == 32 && xt == QBW_BF16 && K % 256 == 0 && (double)wbytes >= mix_tc_min_bytes(bits, K) &&
+    r.tc_form = group >= 32 && (group & (group - 1)) == 0 && xt == QBW_BF16 && K % 256 == 0 &&
+                (double)wbytes >= mix_tc_min_bytes(bits, K) &&
                 (uintptr_t)sc % 16 == 0 && (bits != 4 || (uintptr_t)bi % 16 == 0);
     r.cuda_fits = qmv_mixbit_smem_bytes(bits, K, group) <= kMixMaxSmem;
     return r;
 }
-static bool mix_tc_maps(const MixRoute& r, int bits, const void* qp, const void* sc, const void* bi, int64_t N,
-                        int64_t K, const DeviceInfo& di, CUtensorMap* maps) {
-    return r.tc_form && qmv_mix_tc_supported(N, K, di.sm_count) && encode_mix_maps(maps, bits, qp, sc, bi, N, K);
+static bool mix_tc_maps(const MixRoute& r, int bits, const void* qp, const void* sc, const void* bi,
+                        int64_t group, int64_t N, int64_t K, const DeviceInfo& di, CUtensorMap* maps) {
+    return r.tc_form && qmv_mix_tc_supported(N, K, di.sm_count) &&
+           encode_mix_maps(maps, bits, qp, sc, bi, N, K, group);
 }
 
 qbw_status qmv_mixbit(qbw_mixbit kind, const void* qp, const void* sc, const void* bi, int64_t group, const void* x,
@@ -685,8 +688,9 @@ qbw_status qmv_mixbit(qbw_mixbit kind, const void* qp, const void* sc, const voi
     if (overlaps(y, ybytes, x, (size_t)K * dtype_size(xt)) || overlaps(y, ybytes, qp, wbytes) ||
         overlaps(y, ybytes, sc, sbytes) || (kind == QBW_MIXBIT_INT4_AFFINE && overlaps(y, ybytes, bi, sbytes)))
         return QBW_EINVAL;
-    // groups of 32 and bf16 x: the tensor-core 8-bit form from
-    // mix_tc_min_bytes of codes (where the device's plan allows it); otherwise
+    // groups of 32 (or a larger power of two) and bf16 x: the tensor-core
+    // 8-bit form from mix_tc_min_bytes of codes (where the device's plan allows
+    // it); otherwise
     // the CUDA-core kernel, which stages x in shared memory, so its rows are
     // bounded
     const int bits = (int)kind;
@@ -697,9 +701,11 @@ qbw_status qmv_mixbit(qbw_mixbit kind, const void* qp, const void* sc, const voi
     if (st != QBW_OK) return st;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     CUtensorMap maps[3];
-    if (mix_tc_maps(r, bits, qp, sc, bi, N, K, *di, maps)) {
-        cudaError_t e = launch_qmv_mix_tc(bits, maps, qp, sc, x, y, yt == QBW_BF16, (int)N, (int)K, di->sm_count,
-                                          di->fault, s);
+    if (mix_tc_maps(r, bits, qp, sc, bi, group, N, K, *di, maps)) {
+        int gshift = 5;
+        while ((int64_t(1) << gshift) < group) ++gshift;
+        cudaError_t e = launch_qmv_mix_tc(bits, maps, qp, sc, bi, gshift, x, y, yt == QBW_BF16, (int)N, (int)K,
+                                          di->sm_count, di->fault, s);
         return e == cudaSuccess ? QBW_OK : QBW_ECUDA;
     }
     if (!r.cuda_fits) return QBW_ESHAPE;
@@ -722,7 +728,7 @@ qbw_status qmv_mixbit_route(qbw_mixbit kind, const void* qp, const void* sc, con
     st = device_info(&di);
     if (st != QBW_OK) return st;
     CUtensorMap maps[3];
-    const bool tc = mix_tc_maps(r, bits, qp, sc, bi, N, K, *di, maps);
+    const bool tc = mix_tc_maps(r, bits, qp, sc, bi, group, N, K, *di, maps);
     if (!tc && !r.cuda_fits) return QBW_ESHAPE;
     *tensor_cores = tc ? 1 : 0;
     return QBW_OK;

@@ -164,9 +164,12 @@ __device__ __forceinline__ void qmv_tc_body(const QtcParams& p) {
         asm volatile("bar.arrive 1, %0;" ::"n"(kThreads) : "memory");
         if (lane == 0) {
             prefetch_tmap(&p.tmap_w[0]);
-            if (NMAT == 2 || MIX || MIX8) prefetch_tmap(&p.tmap_w[1]);
-            if constexpr (MIX4) prefetch_tmap(&p.tmap_bi);
+            if (NMAT == 2 || ((MIX || MIX8) && p.mgshift == 5)) prefetch_tmap(&p.tmap_w[1]);
+            if (MIX4 && p.mgshift == 5) prefetch_tmap(&p.tmap_bi);
             // weights do not depend on the preceding grid: start streaming now
+            // the mixed-bit forms copy their scales (and biases) with the codes
+            // for groups of 32; the threads read larger groups' themselves
+            const bool sc_tma = !(MIX || MIX8) || p.mgshift == 5;
             if constexpr (MIX8) {
                 // unit i's halves in ring stages (2i) % 6 and (2i + 1) % 6: codes
                 // (16 words of a row), then the unit's scales (2 words)
@@ -179,11 +182,12 @@ __device__ __forceinline__ void qmv_tc_body(const QtcParams& p) {
                                                    kFaultBulkWaitTimeout);
                         if (!ok) break;
                         const uint32_t dst = sbase + (uint32_t)s * kRawStageBytes;
-                        mbar_arrive_expect_tx(full_bar(bar0, s), kMix8StageBytes);
+                        mbar_arrive_expect_tx(full_bar(bar0, s), sc_tma ? kMix8StageBytes : kMixCodeBytes);
                         tma_load_2d(dst, &p.tmap_w[0], g * 32 + 16 * hs, t * kTileRows, full_bar(bar0, s),
                                     policy_evict_first());
-                        tma_load_2d(dst + kMixCodeBytes, &p.tmap_w[1], g * 2, t * kTileRows, full_bar(bar0, s),
-                                    policy_evict_first());
+                        if (sc_tma)
+                            tma_load_2d(dst + kMixCodeBytes, &p.tmap_w[1], g * 2, t * kTileRows, full_bar(bar0, s),
+                                        policy_evict_first());
                     }
                 }
             }
@@ -197,13 +201,18 @@ __device__ __forceinline__ void qmv_tc_body(const QtcParams& p) {
                 if constexpr (MIX) {
                     // codes (16 or 8 words of a row), then scales and biases (2 words each)
                     const uint32_t sdst = sbase + kOffB2 + (uint32_t)s * kMixScaleBytes;
-                    mbar_arrive_expect_tx(full_bar(bar0, s), MIX4 ? kMixStageBytes : kMix2StageBytes);
+                    const uint32_t code_bytes = kTileRows * (MIX4 ? 128u : 64u);
+                    mbar_arrive_expect_tx(full_bar(bar0, s), sc_tma ? (MIX4 ? kMixStageBytes : kMix2StageBytes)
+                                                                    : code_bytes);
                     tma_load_2d(sbase + (uint32_t)s * kRawStageBytes, &p.tmap_w[0], g * (MIX4 ? 16 : 8),
                                 t * kTileRows, full_bar(bar0, s), policy_evict_first());
-                    tma_load_2d(sdst, &p.tmap_w[1], g * 2, t * kTileRows, full_bar(bar0, s), policy_evict_first());
-                    if constexpr (MIX4)
-                        tma_load_2d(sdst + kMixScaleBytes / 2, &p.tmap_bi, g * 2, t * kTileRows, full_bar(bar0, s),
+                    if (sc_tma) {
+                        tma_load_2d(sdst, &p.tmap_w[1], g * 2, t * kTileRows, full_bar(bar0, s),
                                     policy_evict_first());
+                        if constexpr (MIX4)
+                            tma_load_2d(sdst + kMixScaleBytes / 2, &p.tmap_bi, g * 2, t * kTileRows,
+                                        full_bar(bar0, s), policy_evict_first());
+                    }
                 } else {
                     mbar_arrive_expect_tx(full_bar(bar0, s), kRawStageBytes);
                     tma_load_2d(sbase + (uint32_t)s * kRawStageBytes, &p.tmap_w[mat], g * kGroupWords,
@@ -383,10 +392,13 @@ __device__ __forceinline__ void qmv_tc_body(const QtcParams& p) {
                     if (sl < 0) sl += G;
                     if (sl >= kXtGroups) sl = 0;
                     if (!group_flagged(sbase, sl)) continue;     // no residuals
-                    if constexpr (MIX || MIX8)
+                    if constexpr (MIX || MIX8) {
+                        uint32_t s8[4];
+                        mix_unit_values(p.msc + nrow * (p.K >> p.mgshift), g, p.mgshift, s8);
                         corr += unit_correction<FMT, 2, false>(
                             p.w[0] + nrow * p.row_bytes + (int64_t)g * (MIX8 ? 256 : (MIX4 ? 128 : 64)), p.x, g,
-                            sbase, sl, reinterpret_cast<const uint8_t*>(p.msc + nrow * (p.K / 32) + (int64_t)g * 8));
+                            sbase, sl, make_uint4(s8[0], s8[1], s8[2], s8[3]));
+                    }
                     else
                         corr += unit_correction<FMT, F8 ? F8 : 2, false>(
                             p.w[m] + nrow * p.row_bytes + (int64_t)g * 144, p.x, g, sbase, sl);
@@ -464,6 +476,23 @@ __device__ __forceinline__ void qmv_tc_body(const QtcParams& p) {
                         xr1 = __ldg(reinterpret_cast<const uint4*>(static_cast<const float*>(p.x) + e + 4));
                     }
                 }
+                // the block scales (and int4 biases) of this unit and row; the
+                // mixed-bit forms with groups larger than 32 read theirs from
+                // global memory here, ahead of the stage wait (they are needed at
+                // the read-back, one unit later)
+                uint32_t dd[4];
+                [[maybe_unused]] uint32_t bb[4];
+                if constexpr (MIX || MIX8) {
+                    if (p.mgshift != 5) {
+    #pragma unroll
+                        for (int P = 0; P < 4; ++P) dd[P] = bb[P] = 0u;
+                        const int64_t nrow = (int64_t)t * kTileRows + row;
+                        if (nrow < p.N) {
+                            mix_unit_values(p.msc + nrow * (p.K >> p.mgshift), g, p.mgshift, dd);
+                            if constexpr (MIX4) mix_unit_values(p.mbi + nrow * (p.K >> p.mgshift), g, p.mgshift, bb);
+                        }
+                    }
+                }
                 const bool got = mbar_wait_bounded(full_bar(bar0, s), spar, p.fault, kFaultBulkWaitTimeout);
                 if (!__all_sync(0xffffffffu, got)) {
                     ok = false;
@@ -471,8 +500,6 @@ __device__ __forceinline__ void qmv_tc_body(const QtcParams& p) {
                 }
                 const uint32_t src = sbase + (uint32_t)s * kRawStageBytes + raw_row;
                 uint32_t v[36];
-                uint32_t dd[4];
-                [[maybe_unused]] uint32_t bb[4];
                 if constexpr (MIX8) {
                     // the first half's 8 swizzled code chunks, then the unit's scales
     #pragma unroll
@@ -483,11 +510,14 @@ __device__ __forceinline__ void qmv_tc_body(const QtcParams& p) {
                         v[4 * j + 2] = w.z;
                         v[4 * j + 3] = w.w;
                     }
-                    const uint4 sv = lds128(sbase + (uint32_t)s * kRawStageBytes + kMixCodeBytes + (uint32_t)row * 16u);
-                    dd[0] = sv.x;
-                    dd[1] = sv.y;
-                    dd[2] = sv.z;
-                    dd[3] = sv.w;
+                    if (p.mgshift == 5) {
+                        const uint4 sv =
+                            lds128(sbase + (uint32_t)s * kRawStageBytes + kMixCodeBytes + (uint32_t)row * 16u);
+                        dd[0] = sv.x;
+                        dd[1] = sv.y;
+                        dd[2] = sv.z;
+                        dd[3] = sv.w;
+                    }
                 } else if constexpr (MIX) {
                     // the row's 8 (4) swizzled code chunks, then its scales (and biases)
     #pragma unroll
@@ -499,18 +529,20 @@ __device__ __forceinline__ void qmv_tc_body(const QtcParams& p) {
                         v[4 * j + 2] = w.z;
                         v[4 * j + 3] = w.w;
                     }
-                    const uint32_t ssrc = sbase + kOffB2 + (uint32_t)s * kMixScaleBytes + (uint32_t)row * 16u;
-                    const uint4 sv = lds128(ssrc);
-                    dd[0] = sv.x;
-                    dd[1] = sv.y;
-                    dd[2] = sv.z;
-                    dd[3] = sv.w;
-                    if constexpr (MIX4) {
-                        const uint4 bv = lds128(ssrc + kMixScaleBytes / 2);
-                        bb[0] = bv.x;
-                        bb[1] = bv.y;
-                        bb[2] = bv.z;
-                        bb[3] = bv.w;
+                    if (p.mgshift == 5) {
+                        const uint32_t ssrc = sbase + kOffB2 + (uint32_t)s * kMixScaleBytes + (uint32_t)row * 16u;
+                        const uint4 sv = lds128(ssrc);
+                        dd[0] = sv.x;
+                        dd[1] = sv.y;
+                        dd[2] = sv.z;
+                        dd[3] = sv.w;
+                        if constexpr (MIX4) {
+                            const uint4 bv = lds128(ssrc + kMixScaleBytes / 2);
+                            bb[0] = bv.x;
+                            bb[1] = bv.y;
+                            bb[2] = bv.z;
+                            bb[3] = bv.w;
+                        }
                     }
                 } else {
     #pragma unroll
@@ -1022,7 +1054,8 @@ cudaError_t launch_qmv_tc(int fmt, int nmat, int ntok, const CUtensorMap* tmap_w
     p.tmap_w[1] = tmap_w[nmat == 2 ? 1 : 0];
     p.w[0] = static_cast<const uint8_t*>(w[0]);
     p.w[1] = static_cast<const uint8_t*>(w[nmat == 2 ? 1 : 0]);
-    p.msc = nullptr;
+    p.msc = p.mbi = nullptr;
+    p.mgshift = 0;
     p.row_bytes = weight_row_bytes(fmt, K);
     p.next_units = 0;
     p.next_groups = p.next_nmat = p.next_ctas = 1;
@@ -1065,20 +1098,25 @@ bool qmv_mix_tc_supported(int64_t N, int64_t K, int sm_count) {
     return table_fits(1, tiles * groups, groups, sm_count);
 }
 
-// bits = 4, 2 or 8.  tmaps: the codes ([N][K b / 64] 8-byte words, box (4 b,
-// 128) or for int8 (16, 128), the 128- or 64-byte swizzle), the scales and, for int4, the biases
-// ([N][K / 128] 8-byte words, box (2, 128)); qp and sc the same arrays, for
-// the read-back correction; bf16 x.
-cudaError_t launch_qmv_mix_tc(int bits, const CUtensorMap* tmaps, const void* qp, const void* sc, const void* x,
-                              void* y, int y_bf16, int N, int K, int sm_count, unsigned int* fault,
-                              cudaStream_t stream) {
+// bits = 4, 2 or 8; groups of 2^gshift weights (gshift >= 5).  tmaps: the
+// codes ([N][K b / 64] 8-byte words, box (4 b, 128) or for int8 (16, 128), the
+// 128- or 64-byte swizzle), and for groups of 32 the scales and, for int4,
+// the biases ([N][K / 128] 8-byte words, box (2, 128)); qp, sc and bi the same
+// arrays (sc and bi read directly for larger groups and for the read-back
+// correction); bf16 x.
+cudaError_t launch_qmv_mix_tc(int bits, const CUtensorMap* tmaps, const void* qp, const void* sc, const void* bi,
+                              int gshift, const void* x, void* y, int y_bf16, int N, int K, int sm_count,
+                              unsigned int* fault, cudaStream_t stream) {
     if (bits != 2 && bits != 4 && bits != 8) return cudaErrorInvalidValue;
+    if (gshift < 5 || (K >> gshift) << gshift != K) return cudaErrorInvalidValue;
     QtcParams p;
     p.tmap_w[0] = tmaps[0];
-    p.tmap_w[1] = tmaps[1];
-    p.tmap_bi = tmaps[bits == 4 ? 2 : 1];
+    p.tmap_w[1] = tmaps[gshift == 5 ? 1 : 0];
+    p.tmap_bi = tmaps[gshift == 5 && bits == 4 ? 2 : 0];
     p.w[0] = p.w[1] = static_cast<const uint8_t*>(qp);
     p.msc = static_cast<const uint16_t*>(sc);
+    p.mbi = static_cast<const uint16_t*>(bits == 4 ? bi : sc);
+    p.mgshift = gshift;
     p.row_bytes = (int64_t)K * bits / 8;
     p.next_units = 0;
     p.next_groups = p.next_nmat = p.next_ctas = 1;

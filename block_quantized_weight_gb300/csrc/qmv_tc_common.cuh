@@ -102,12 +102,16 @@ struct QtcParams {
     // the same CTA index loads there
     CUtensorMap next_tmap[2];
     int32_t next_units, next_groups, next_nmat, next_ctas;
-    // the int4-affine mixed-bit form: tmap_w[0] views the codes as 8-byte
-    // words, box (16, 128); tmap_w[1] the fp16 scales and tmap_bi the fp16
-    // biases as 8-byte words, box (2, 128); msc the scales again, for the
-    // read-back correction ([N][K / 32])
+    // the mixed-bit forms: tmap_w[0] views the codes as 8-byte words; with
+    // groups of 32 (mgshift = 5) tmap_w[1] the fp16 scales and tmap_bi the fp16
+    // biases as 8-byte words, box (2, 128).  msc and mbi are the scales and
+    // biases ([N][K >> mgshift], one per 2^mgshift weights of a row), which
+    // the threads read themselves for larger groups (and for the read-back
+    // correction)
     CUtensorMap tmap_bi;
     const uint16_t* msc;
+    const uint16_t* mbi;
+    int32_t mgshift;
     const void* x;
     void* y;
     unsigned int* fault;
@@ -441,6 +445,38 @@ __device__ __forceinline__ float unit_dot_q4k_e4m3(const uint32_t (&dv)[16], con
         r = fmaf(-dm.y * (float)m, sx[j], r);
     }
     return r;
+}
+
+// A mixed-bit unit's eight block values (scales or biases; block 2p in the low
+// half of v[p]) from the row's fp16 array of one value per 2^gshift weights
+// (gshift >= 5: groups of 32 or more, a power of two), read from global memory
+// (the row's array 16-byte aligned for groups of 32, 8 for 64, 4 for 128):
+// block j of unit g takes value (256 g + 32 j) >> gshift.
+__device__ __forceinline__ void mix_unit_values(const uint16_t* row, int g, int gshift, uint32_t (&v)[4]) {
+    const uint16_t* first = row + ((int64_t)g << 8 >> gshift);
+    if (gshift == 5) {
+        const uint4 w = __ldg(reinterpret_cast<const uint4*>(first));
+        v[0] = w.x;
+        v[1] = w.y;
+        v[2] = w.z;
+        v[3] = w.w;
+    } else if (gshift == 6) {
+        // four values, one per block pair
+        const uint2 w = __ldg(reinterpret_cast<const uint2*>(first));
+        v[0] = __byte_perm(w.x, 0u, 0x1010);
+        v[1] = __byte_perm(w.x, 0u, 0x3232);
+        v[2] = __byte_perm(w.y, 0u, 0x1010);
+        v[3] = __byte_perm(w.y, 0u, 0x3232);
+    } else if (gshift == 7) {
+        // two values, one per four blocks
+        const uint32_t w = __ldg(reinterpret_cast<const unsigned int*>(first));
+        v[0] = v[1] = __byte_perm(w, 0u, 0x1010);
+        v[2] = v[3] = __byte_perm(w, 0u, 0x3232);
+    } else {
+        // one value for the whole unit
+        const uint32_t h = __ldg(first);
+        v[0] = v[1] = v[2] = v[3] = h | (h << 16);
+    }
 }
 
 // 8-bit form of the int4-affine mixed-bit matrices: r0 = sum_j (sc_j c_j)
@@ -889,19 +925,20 @@ __device__ __forceinline__ bool segment_needs_correction(float q) { return q > 0
 // 256 g + 255; block scales from table slot sl) and the row's raw bytes read
 // from global memory at wrow (16-byte aligned; the stage holding them has
 // long been released): 144 bytes, or for the mixed-bit forms 256 (int8), 128
-// (int4) or 64 (int2) code bytes and the 16 bytes of scales at srow.  For the
-// segments the read-back check flags; slow, and exact up to fp32 rounding.
+// (int4) or 64 (int2) code bytes and the unit's eight block scales sc8 (block
+// 2p in the low half of word p).  For the segments the read-back check flags;
+// slow, and exact up to fp32 rounding.
 template <int FMT, int XP, bool kCoherent>
 __device__ __noinline__ float unit_correction(const uint8_t* wrow, const void* x, int g, uint32_t sbase, int sl,
-                                              const uint8_t* srow = nullptr) {
+                                              uint4 sc8 = make_uint4(0u, 0u, 0u, 0u)) {
     // 16-byte pieces of the row's unit: codes, then (mixed-bit) the scales
     constexpr int kCodeChunks = FMT == kFmtMix8 ? 16 : (FMT == kFmtMix2 ? 4 : (FMT == kFmtMix4 ? 8 : 9));
     constexpr bool kScales = FMT == kFmtMix2 || FMT == kFmtMix4 || FMT == kFmtMix8;
     uint8_t b[FMT == kFmtMix8 ? 272 : 144];
 #pragma unroll
-    for (int j = 0; j < kCodeChunks + (kScales ? 1 : 0); ++j)
-        *reinterpret_cast<uint4*>(b + 16 * j) =
-            __ldg(reinterpret_cast<const uint4*>(j == kCodeChunks ? srow : wrow + 16 * j));
+    for (int j = 0; j < kCodeChunks; ++j)
+        *reinterpret_cast<uint4*>(b + 16 * j) = __ldg(reinterpret_cast<const uint4*>(wrow + 16 * j));
+    if constexpr (kScales) *reinterpret_cast<uint4*>(b + 16 * kCodeChunks) = sc8;
     float corr = 0.f;
     for (int k = 0; k < kGroupK; ++k) {
         const uint32_t cb = lds32(sbase + kOffXc + (uint32_t)sl * 32u + (uint32_t)(k >> 5) * 4u);

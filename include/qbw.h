@@ -32,7 +32,7 @@
  * arrays of the library's module, besides a 4-byte fault word
  * (qbw_fault_read):
  *   - the split-tile scratch of the tensor-core M = 1 kernels (qmv_q4_0,
- *     qmv_gateup_q4_0, qmv_q4_k and qmv_mixbit (groups of 32) at the sizes
+ *     qmv_gateup_q4_0, qmv_q4_k and qmv_mixbit at the sizes
  *     that take them, and qmm_q4_0_smallM with M <= 2): 32 slots of 160 CTAs x
  *     2 x 128 tagged 64-bit words, 10,485,760 bytes.  When a 128-row output
  *     tile is split between two CTAs, the CTA that does not write it publishes its partial
@@ -309,9 +309,9 @@ typedef enum qbw_mixbit {
  * form is summed as sc * sum(c x) + bi * sum(x) per group, so its rounding
  * scales with sum (|sc c| + |bi|) |x|.
  *
- * Group 32, bf16 x, K % 256 == 0, sc (and bi) 16-byte aligned and at least 5
- * MB (int4), 4 MB (int2) or 16 MB (int8) of codes (10, 5 and 64 MB when K <=
- * 4096) run on the tensor cores, like qmv_q4_k: the codes enter the MMA
+ * Groups of 32 (or a larger power of two), bf16 x, K % 256 == 0, sc (and bi)
+ * 16-byte aligned and at least 5 MB (int4), 4 MB (int2) or 16 MB (int8) of
+ * codes (10, 5 and 64 MB when K <= 4096) run on the tensor cores, like qmv_q4_k: the codes enter the MMA
  * exactly (int8 as its low nibble and its signed high nibble), x as two e4m3
  * pieces per element under a power-of-two scale per 32 elements, and the rows
  * whose pieces may miss more than 2^-11 of sum |sc q x| get the missed part

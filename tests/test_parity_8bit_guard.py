@@ -219,6 +219,36 @@ def test_mixbit8_outliers_on_zero_weights(qbw, oracle, xdt):
     check_matvec(to_f64(y), y_ref, S, what=f"mixbit8 outliers {xdt}")
 
 
+@pytest.mark.parametrize("bits", [4, 8])
+def test_mixbit_outliers_on_zero_weights_groups_of_128(qbw, oracle, bits):
+    # groups of 128: the kernel reads the scales itself, and the exact
+    # correction expands them per 32-weight block
+    G = 128
+    n = N if bits == 4 else 32768              # int8: 67 MB, above its size threshold for K <= 4096
+    x, outliers = worst_case_activations("bf16", seed=91 + bits)
+    qp, sc, bi = synth.mixbit_weights(bits, n, K, G, seed=93 + bits)
+    if bits == 4:
+        q = qp.view(np.uint8).reshape(n, K // 2)
+        for blk, pos in outliers:
+            k = 32 * blk + pos
+            q[:, k // 2] &= 0xF0 if k % 2 == 0 else 0x0F
+        bi[:] = 0
+    else:
+        q = qp.view(np.uint8).reshape(n, K)
+        for blk, pos in outliers:
+            q[:, 32 * blk + pos] = 0
+    dev_bi = dev_u8(bi.view(np.uint8)) if bi is not None else None
+    assert qbw.qmv_mixbit_route(bits, dev_u8(qp.view(np.uint8)), dev_u8(sc.view(np.uint8)), dev_bi, G,
+                                dev_act(x), n, K)
+    y = torch.full((n,), float("nan"), dtype=torch.float32, device="cuda")
+    qbw.qmv_mixbit(bits, dev_u8(qp.view(np.uint8)), dev_u8(sc.view(np.uint8)), dev_bi, G, dev_act(x), y, 1, n, K)
+    torch.cuda.synchronize()
+    assert qbw.fault_read(clear=True) == 0
+    y_ref, S, S2 = oracle.qmv_mixbit(bits, qp, sc, bi, G, x, n, K)
+    assert np.array_equal(S, S2)                 # no bias term
+    check_matvec(to_f64(y), y_ref, S2, what=f"mixbit{bits} G={G} outliers")
+
+
 def test_chain_step_outliers_on_zero_weights(qbw, oracle):
     # the chained form builds the same table and applies the same correction;
     # one step, its x the worst case, bit-identical to the separate call

@@ -257,17 +257,51 @@ def test_tc_long_rows(qbw, oracle, bits):
 
 @pytest.mark.parametrize("bits", [2, 4, 8])
 def test_route_cuda_core_cases(qbw, bits):
-    # what stays on the CUDA-core kernel: fp32 x, groups other than 32, rows not
-    # a multiple of 256, and matrices below the size thresholds
+    # what stays on the CUDA-core kernel: fp32 x, groups below 32 or not a power
+    # of two, rows not a multiple of 256, and matrices below the size thresholds
     N, K = 21504, 5376
     qp, sc, bi = synth.mixbit_weights(bits, N, K, 32, seed=91)
     xb = synth.activations(K, seed=92, dtype="bf16")
     assert route(qbw, bits, qp, sc, bi, 32, xb, N, K)
     assert not route(qbw, bits, qp, sc, bi, 32, synth.activations(K, seed=92), N, K)
-    qp64, sc64, bi64 = synth.mixbit_weights(bits, N, K, 64, seed=93)
-    assert not route(qbw, bits, qp64, sc64, bi64, 64, xb, N, K)
+    for G in (16, 48):                                         # not a power of two of at least 32
+        qpg, scg, big = synth.mixbit_weights(bits, N, K, G, seed=93)
+        assert not route(qbw, bits, qpg, scg, big, G, xb, N, K)
     K2 = 5376 - 64                                             # 5312: K % 256 != 0
     qp2, sc2, bi2 = synth.mixbit_weights(bits, N, K2, 32, seed=94)
     assert not route(qbw, bits, qp2, sc2, bi2, 32, synth.activations(K2, seed=95, dtype="bf16"), N, K2)
     qs, ss, bs = synth.mixbit_weights(bits, 300, K, 32, seed=96)
     assert not route(qbw, bits, qs, ss, bs, 32, xb, 300, K)
+
+
+# larger groups (a power of two): the threads read the scales and biases from
+# global memory; K = 6144 for groups of 512 (5376 is not a multiple of 512)
+GROUP_CASES = [(b, G, 3077, 5376) for b in (2, 4, 8) for G in (64, 128, 256)] + \
+              [(b, 512, 3000, 6144) for b in (2, 4, 8)]
+
+
+@pytest.mark.parametrize("bits,G,N,K", GROUP_CASES)
+def test_tc_larger_groups(qbw, oracle, bits, G, N, K):
+    qp, sc, bi = synth.mixbit_weights(bits, N, K, G, seed=G + bits)
+    x = synth.activations(K, seed=G + 1, dtype="bf16")
+    assert route(qbw, bits, qp, sc, bi, G, x, N, K), "the case no longer takes the tensor-core form"
+    y = run(qbw, bits, qp, sc, bi, G, x, N, K)
+    y_ref, _, S2 = oracle.qmv_mixbit(bits, qp, sc, bi, G, x, N, K)
+    check_matvec(to_f64(y), y_ref, S2, what=f"tc int{bits} G={G} {N}x{K}")
+
+
+@pytest.mark.parametrize("bits", [4, 2, 8])
+def test_tc_larger_groups_constant_fields(qbw, oracle, bits):
+    N, K, G = 3077, 5376, 128
+    field = {4: 11, 2: 3, 8: 200}[bits]
+    qp = synth.pack_fields(np.full((N, K), field, dtype=np.uint32), bits)
+    _, sc, bi = synth.mixbit_weights(bits, N, K, G, seed=5)
+    x = synth.activations(K, seed=6, dtype="bf16")
+    assert route(qbw, bits, qp, sc, bi, G, x, N, K)
+    y = to_f64(run(qbw, bits, qp, sc, bi, G, x, N, K))
+    xs = (x.astype(np.uint32) << 16).view(np.float32).astype(np.float64).reshape(K // G, G).sum(axis=1)
+    s = sc.view(np.float16).astype(np.float64).reshape(N, K // G)
+    b = bi.view(np.float16).astype(np.float64).reshape(N, K // G) if bits == 4 else 0.0
+    ref = ((s * two_complement(field, bits) + b) * xs).sum(axis=1)
+    _, _, S2 = oracle.qmv_mixbit(bits, qp, sc, bi, G, x, N, K)
+    check_matvec(y, ref, S2, what=f"tc constant int{bits} G={G}")
