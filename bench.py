@@ -425,25 +425,32 @@ def supplementary_kernels(torch, qbw, hbm_peak):
     run("qmv_q4_0 5376x21504 bf16->bf16 GELU(g)*u x", w.numel() + 2 * K + 2 * N, copies,
         lambda i: (lambda: qbw.qmv_q4_0(ws[i], xg, yb, 1, N, K)))
     del ws, w
-    # the mixed-bit formats (int2-symmetric, int4-affine, int8), 21504 x 5376,
-    # groups of 32: bf16 -> fp32 (the tensor-core forms) and fp32 -> fp32 (the
-    # CUDA-core kernel)
-    N, K, G = 21504, 5376, 32
+    # the mixed-bit formats (int2-symmetric, int4-affine, int8), 21504 x 5376:
+    # groups of 32, bf16 -> fp32 and fp32 -> fp32 (the tensor-core forms), and
+    # groups of 16, bf16 -> fp32 (the CUDA-core kernel)
+    N, K = 21504, 5376
     xm = bf16(synth.activations(K, seed=9, dtype="bf16"))
     xm32 = torch.from_numpy(synth.activations(K, seed=9)).to(dev)
     y = torch.empty(N, device=dev)
     for bits in (2, 4, 8):
-        qp, sc, bi = synth.mixbit_weights(bits, N, K, G, seed=9)
-        nbytes = synth.mixbit_bytes(bits, N, K, G)
-        copies = max(2, int(np.ceil(2.2 * l2 / nbytes)))
-        mats = [(torch.from_numpy(qp.view(np.uint8).copy()).to(dev), torch.from_numpy(sc.view(np.uint8).copy()).to(dev),
-                 torch.from_numpy(bi.view(np.uint8).copy()).to(dev) if bi is not None else None) for _ in range(copies)]
         name = {2: "int2-symmetric", 4: "int4-affine", 8: "int8"}[bits]
-        run(f"qmv_mixbit {name} {N}x{K} G={G} bf16->f32", nbytes + 2 * K + 4 * N, copies,
-            lambda i, mats=mats, bits=bits: (lambda: qbw.qmv_mixbit(bits, *mats[i], G, xm, y, 1, N, K)))
-        run(f"qmv_mixbit {name} {N}x{K} G={G} f32->f32 (CUDA cores)", nbytes + 4 * K + 4 * N, copies,
-            lambda i, mats=mats, bits=bits: (lambda: qbw.qmv_mixbit(bits, *mats[i], G, xm32, y, 1, N, K)))
-        del mats
+        for G in (32, 16):
+            qp, sc, bi = synth.mixbit_weights(bits, N, K, G, seed=9)
+            nbytes = synth.mixbit_bytes(bits, N, K, G)
+            copies = max(2, int(np.ceil(2.2 * l2 / nbytes)))
+            mats = [(torch.from_numpy(qp.view(np.uint8).copy()).to(dev),
+                     torch.from_numpy(sc.view(np.uint8).copy()).to(dev),
+                     torch.from_numpy(bi.view(np.uint8).copy()).to(dev) if bi is not None else None)
+                    for _ in range(copies)]
+            if G == 32:
+                run(f"qmv_mixbit {name} {N}x{K} G={G} bf16->f32", nbytes + 2 * K + 4 * N, copies,
+                    lambda i, mats=mats, bits=bits, G=G: (lambda: qbw.qmv_mixbit(bits, *mats[i], G, xm, y, 1, N, K)))
+                run(f"qmv_mixbit {name} {N}x{K} G={G} f32->f32", nbytes + 4 * K + 4 * N, copies,
+                    lambda i, mats=mats, bits=bits, G=G: (lambda: qbw.qmv_mixbit(bits, *mats[i], G, xm32, y, 1, N, K)))
+            else:
+                run(f"qmv_mixbit {name} {N}x{K} G={G} bf16->f32 (CUDA cores)", nbytes + 2 * K + 4 * N, copies,
+                    lambda i, mats=mats, bits=bits, G=G: (lambda: qbw.qmv_mixbit(bits, *mats[i], G, xm, y, 1, N, K)))
+            del mats
     # small-M tiles
     for (N, K) in ((5376, 5376), (5376, 21504)):
         w = torch.from_numpy(synth.q4_0_weights(N, K, seed=3)).to(dev)
@@ -887,10 +894,11 @@ def profile_case(args):
     elif name.startswith("mixbit"):
         # one mixed-bit matrix, 21504 x 5376, groups of 32, bf16 x (the
         # tensor-core forms), rotating copies larger than L2 together; with the
-        # suffix "_f32", fp32 x (the CUDA-core kernel)
+        # suffix "_f32", fp32 x (the tensor-core forms' three-piece variant);
+        # with "_g16", groups of 16 (the CUDA-core kernel)
         f32x = name.endswith("_f32")
-        bits = int(name[len("mixbit"):].replace("_f32", ""))
-        N, K, G = 21504, 5376, 32
+        bits = int(name[len("mixbit"):].replace("_f32", "").replace("_g16", ""))
+        N, K, G = 21504, 5376, (16 if name.endswith("_g16") else 32)
         qp, sc, bi = synth.mixbit_weights(bits, N, K, G, seed=9)
         nb = synth.mixbit_bytes(bits, N, K, G)
         copies = max(2, int(np.ceil(300e6 / nb)))
@@ -994,7 +1002,7 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--profile", choices=["q8_0", "q8_0_lmhead", "q4_0", "q4_0_bf16", "q4_k", "gateup", "qmm", "sweep",
                                           "mixbit2", "mixbit4", "mixbit8", "mixbit2_f32", "mixbit4_f32",
-                                          "mixbit8_f32", "qmm8", "qmm8_5376", "q4_0_stream",
+                                          "mixbit8_f32", "mixbit2_g16", "mixbit4_g16", "mixbit8_g16", "qmm8", "qmm8_5376", "q4_0_stream",
                                           "qmm2_qkv", "chain"],
                     help="run only one small case (for profiler captures): a single-matrix workload, or the "
                          "sweep's launches over 6 layers")

@@ -37,8 +37,8 @@ cudaError_t launch_qmv_tc(int fmt, int nmat, int ntok, const CUtensorMap* tmap_w
 int qmm_tc_tile_rows();
 bool qmv_mix_tc_supported(int64_t N, int64_t K, int sm_count);
 cudaError_t launch_qmv_mix_tc(int bits, const CUtensorMap* tmaps, const void* qp, const void* sc, const void* bi,
-                              int gshift, const void* x, void* y, int y_bf16, int N, int K, int sm_count,
-                              unsigned int* fault, cudaStream_t stream);
+                              int gshift, const void* x, int x_bf16, void* y, int y_bf16, int N, int K,
+                              int sm_count, unsigned int* fault, cudaStream_t stream);
 bool qmv_chain_step_supported(int nmat, int64_t N, int64_t K, int ctas);
 void qmv_chain_fill_step(ChainStepDesc* d, int nmat, int64_t N, int64_t K);
 int qmv_chain_ctas(int sm_count);
@@ -654,8 +654,8 @@ constexpr double mix_tc_min_bytes(int bits, int64_t K) {
 
 // Which kernel a mixed-bit product takes (shared by qmv_mixbit and
 // qmv_mixbit_route).  Before the device is looked up: whether the call has the
-// tensor-core form's shape (groups of 32 or a larger power of two, bf16 x, K %
-// 256, size, scale alignment) and whether the CUDA-core kernel can stage its rows; after it,
+// tensor-core form's shape (groups of 32 or a larger power of two, K % 256,
+// size, scale alignment) and whether the CUDA-core kernel can stage its rows; after it,
 // whether the device's plan takes the call and its tensor maps encode.
 struct MixRoute {
     bool tc_form, cuda_fits;
@@ -663,7 +663,7 @@ struct MixRoute {
 static MixRoute mix_route(int bits, const void* sc, const void* bi, int64_t group, qbw_dtype xt, size_t wbytes,
                           int64_t K) {
     MixRoute r;
-    r.tc_form = group >= 32 && (group & (group - 1)) == 0 && xt == QBW_BF16 && K % 256 == 0 &&
+    r.tc_form = group >= 32 && (group & (group - 1)) == 0 && K % 256 == 0 &&
                 (double)wbytes >= mix_tc_min_bytes(bits, K) &&
                 (uintptr_t)sc % 16 == 0 && (bits != 4 || (uintptr_t)bi % 16 == 0);
     r.cuda_fits = qmv_mixbit_smem_bytes(bits, K, group) <= kMixMaxSmem;
@@ -688,9 +688,9 @@ qbw_status qmv_mixbit(qbw_mixbit kind, const void* qp, const void* sc, const voi
     if (overlaps(y, ybytes, x, (size_t)K * dtype_size(xt)) || overlaps(y, ybytes, qp, wbytes) ||
         overlaps(y, ybytes, sc, sbytes) || (kind == QBW_MIXBIT_INT4_AFFINE && overlaps(y, ybytes, bi, sbytes)))
         return QBW_EINVAL;
-    // groups of 32 (or a larger power of two) and bf16 x: the tensor-core
-    // 8-bit form from mix_tc_min_bytes of codes (where the device's plan allows
-    // it); otherwise
+    // groups of 32 (or a larger power of two): the tensor-core 8-bit form
+    // (bf16 or fp32 x) from mix_tc_min_bytes of codes (where the device's plan
+    // allows it); otherwise
     // the CUDA-core kernel, which stages x in shared memory, so its rows are
     // bounded
     const int bits = (int)kind;
@@ -704,8 +704,8 @@ qbw_status qmv_mixbit(qbw_mixbit kind, const void* qp, const void* sc, const voi
     if (mix_tc_maps(r, bits, qp, sc, bi, group, N, K, *di, maps)) {
         int gshift = 5;
         while ((int64_t(1) << gshift) < group) ++gshift;
-        cudaError_t e = launch_qmv_mix_tc(bits, maps, qp, sc, bi, gshift, x, y, yt == QBW_BF16, (int)N, (int)K,
-                                          di->sm_count, di->fault, s);
+        cudaError_t e = launch_qmv_mix_tc(bits, maps, qp, sc, bi, gshift, x, xt == QBW_BF16, y, yt == QBW_BF16,
+                                          (int)N, (int)K, di->sm_count, di->fault, s);
         return e == cudaSuccess ? QBW_OK : QBW_ECUDA;
     }
     if (!r.cuda_fits) return QBW_ESHAPE;

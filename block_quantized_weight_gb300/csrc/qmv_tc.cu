@@ -107,7 +107,12 @@ __device__ __forceinline__ void qmv_tc_body(const QtcParams& p) {
     // bf16 activations; a unit's 256 code bytes per row take two ring stages of
     // 128 bytes each, both with the unit's scales
     constexpr bool MIX8 = FMT == kFmtMix8;
-    static_assert(!(MIX || MIX8) || F8 == 2, "mixed-bit forms: two pieces");
+    static_assert(!(MIX || MIX8) || F8 == 2 || F8 == 3, "mixed-bit forms: the 8-bit form");
+    // where a mixed-bit form's scales (and biases) come from: copied with the
+    // codes for groups of 32 (int2 and int4 into the B2 region, which the
+    // fp32 form needs for its third pieces, so only with bf16 x; int8 into
+    // its ring stages); otherwise read by the threads from global memory
+    const bool mix_sc_copied = !(MIX || MIX8) || (p.mgshift == 5 && (F8 == 2 || MIX8));
     // the 8-bit form of Q4_K: one A operand (codes 0..15), 8 K-steps per unit
     constexpr bool Q4K8 = F8 != 0 && FMT == kFmtQ4K;
     // one A operand of codes (Q4_K's 0..15, the int4 and int2 mixed-bit forms)
@@ -137,9 +142,10 @@ __device__ __forceinline__ void qmv_tc_body(const QtcParams& p) {
 
     // zero B operands (only their fixed activation positions are ever written
     // again) and the per-set partial rows
-    // (B2 too, except where it is the mixed-bit form's scale ring, which the
-    // copies below start filling at once)
-    for (int i = threadIdx.x; i < (int)((MIX ? 1 : 2) * kSets * kBBytes / 16); i += kThreads)
+    // (B2 too, except where it is the int2 / int4 forms' scale ring, which the
+    // copies below start filling at once; the fp32 forms' third pieces need it
+    // zero like B)
+    for (int i = threadIdx.x; i < (int)((MIX && mix_sc_copied ? 1 : 2) * kSets * kBBytes / 16); i += kThreads)
         sts128(sbase + kOffB + 16u * (uint32_t)i, make_uint4(0u, 0u, 0u, 0u));
     for (int i = threadIdx.x; i < kSets * kMaxLocalTiles * 2 * kTileRows; i += kThreads) part[i] = 0.f;
     for (int i = threadIdx.x; i < kProducerWarp * 32 * 3; i += kThreads)       // acc_q and fixups
@@ -164,12 +170,10 @@ __device__ __forceinline__ void qmv_tc_body(const QtcParams& p) {
         asm volatile("bar.arrive 1, %0;" ::"n"(kThreads) : "memory");
         if (lane == 0) {
             prefetch_tmap(&p.tmap_w[0]);
-            if (NMAT == 2 || ((MIX || MIX8) && p.mgshift == 5)) prefetch_tmap(&p.tmap_w[1]);
-            if (MIX4 && p.mgshift == 5) prefetch_tmap(&p.tmap_bi);
+            if (NMAT == 2 || ((MIX || MIX8) && mix_sc_copied)) prefetch_tmap(&p.tmap_w[1]);
+            if (MIX4 && mix_sc_copied) prefetch_tmap(&p.tmap_bi);
             // weights do not depend on the preceding grid: start streaming now
-            // the mixed-bit forms copy their scales (and biases) with the codes
-            // for groups of 32; the threads read larger groups' themselves
-            const bool sc_tma = !(MIX || MIX8) || p.mgshift == 5;
+            const bool sc_tma = mix_sc_copied;
             if constexpr (MIX8) {
                 // unit i's halves in ring stages (2i) % 6 and (2i + 1) % 6: codes
                 // (16 words of a row), then the unit's scales (2 words)
@@ -395,7 +399,7 @@ __device__ __forceinline__ void qmv_tc_body(const QtcParams& p) {
                     if constexpr (MIX || MIX8) {
                         uint32_t s8[4];
                         mix_unit_values(p.msc + nrow * (p.K >> p.mgshift), g, p.mgshift, s8);
-                        corr += unit_correction<FMT, 2, false>(
+                        corr += unit_correction<FMT, F8, false>(
                             p.w[0] + nrow * p.row_bytes + (int64_t)g * (MIX8 ? 256 : (MIX4 ? 128 : 64)), p.x, g,
                             sbase, sl, make_uint4(s8[0], s8[1], s8[2], s8[3]));
                     }
@@ -483,7 +487,7 @@ __device__ __forceinline__ void qmv_tc_body(const QtcParams& p) {
                 uint32_t dd[4];
                 [[maybe_unused]] uint32_t bb[4];
                 if constexpr (MIX || MIX8) {
-                    if (p.mgshift != 5) {
+                    if (!mix_sc_copied) {
     #pragma unroll
                         for (int P = 0; P < 4; ++P) dd[P] = bb[P] = 0u;
                         const int64_t nrow = (int64_t)t * kTileRows + row;
@@ -510,7 +514,7 @@ __device__ __forceinline__ void qmv_tc_body(const QtcParams& p) {
                         v[4 * j + 2] = w.z;
                         v[4 * j + 3] = w.w;
                     }
-                    if (p.mgshift == 5) {
+                    if (mix_sc_copied) {
                         const uint4 sv =
                             lds128(sbase + (uint32_t)s * kRawStageBytes + kMixCodeBytes + (uint32_t)row * 16u);
                         dd[0] = sv.x;
@@ -529,7 +533,7 @@ __device__ __forceinline__ void qmv_tc_body(const QtcParams& p) {
                         v[4 * j + 2] = w.z;
                         v[4 * j + 3] = w.w;
                     }
-                    if (p.mgshift == 5) {
+                    if (mix_sc_copied) {
                         const uint32_t ssrc = sbase + kOffB2 + (uint32_t)s * kMixScaleBytes + (uint32_t)row * 16u;
                         const uint4 sv = lds128(ssrc);
                         dd[0] = sv.x;
@@ -613,7 +617,7 @@ __device__ __forceinline__ void qmv_tc_body(const QtcParams& p) {
                 int cur_sl = 0;
                 uint2 bp0 = make_uint2(0u, 0u);
                 [[maybe_unused]] uint2 bp1 = bp0, bp2 = bp0;     // the 8-bit forms' second and third pieces
-                [[maybe_unused]] uint2 bq0 = bp0, bq1 = bp0;     // the int8 form's pieces times 16
+                [[maybe_unused]] uint2 bq0 = bp0, bq1 = bp0, bq2 = bp0;     // the int8 form's pieces times 16
                 if constexpr (F8) {
                     cur_sl = g - xg0;
                     if (cur_sl < 0) cur_sl += G;
@@ -623,18 +627,20 @@ __device__ __forceinline__ void qmv_tc_body(const QtcParams& p) {
                         const uint4 tq = lds128(sbase + kOffXt + ch * 16u);
                         bp0 = make_uint2(tq.x, tq.y);
                         bp1 = make_uint2(tq.z, tq.w);
-                        if constexpr (MIX) {     // the code words' order of weights
-                            bp0 = perm_mix4(bp0);
-                            bp1 = perm_mix4(bp1);
-                        }
-                        if constexpr (MIX8) {    // the second K-step's pieces: 16 x
-                            bq0 = times16_e4m3(bp0);
-                            bq1 = times16_e4m3(bp1);
-                        }
                         if constexpr (F8 == 3)
                             asm volatile("ld.shared.v2.b32 {%0, %1}, [%2];"
                                          : "=r"(bp2.x), "=r"(bp2.y)
                                          : "r"(sbase + kOffXt2 + ch * 8u));
+                        if constexpr (MIX) {     // the code words' order of weights
+                            bp0 = perm_mix4(bp0);
+                            bp1 = perm_mix4(bp1);
+                            if constexpr (F8 == 3) bp2 = perm_mix4(bp2);
+                        }
+                        if constexpr (MIX8) {    // the second K-step's pieces: 16 x
+                            bq0 = times16_e4m3(bp0);
+                            bq1 = times16_e4m3(bp1);
+                            if constexpr (F8 == 3) bq2 = times16_e4m3(bp2);
+                        }
                     }
                 }
                 const uint32_t prev = (uint32_t)(k - 1) & 1u;     // completion parity of the previous unit
@@ -665,7 +671,8 @@ __device__ __forceinline__ void qmv_tc_body(const QtcParams& p) {
                         sts64(f8_n1, MIX8 ? bq1 : make_uint2(bp1.x ^ 0x80808080u, bp1.y ^ 0x80808080u));
                         if constexpr (F8 == 3) {     // third pieces: B2, the second piece's rows
                             sts64(f8_p1 + (kOffB2 - kOffB), bp2);
-                            sts64(f8_n1 + (kOffB2 - kOffB), make_uint2(bp2.x ^ 0x80808080u, bp2.y ^ 0x80808080u));
+                            sts64(f8_n1 + (kOffB2 - kOffB),
+                                  MIX8 ? bq2 : make_uint2(bp2.x ^ 0x80808080u, bp2.y ^ 0x80808080u));
                         }
                     } else {
                         sts128(b_hi, bhi);
@@ -733,7 +740,8 @@ __device__ __forceinline__ void qmv_tc_body(const QtcParams& p) {
                         sts64(f8_n1, MIX8 ? bq1 : make_uint2(bp1.x ^ 0x80808080u, bp1.y ^ 0x80808080u));
                         if constexpr (F8 == 3) {     // third pieces: B2, the second piece's rows
                             sts64(f8_p1 + (kOffB2 - kOffB), bp2);
-                            sts64(f8_n1 + (kOffB2 - kOffB), make_uint2(bp2.x ^ 0x80808080u, bp2.y ^ 0x80808080u));
+                            sts64(f8_n1 + (kOffB2 - kOffB),
+                                  MIX8 ? bq2 : make_uint2(bp2.x ^ 0x80808080u, bp2.y ^ 0x80808080u));
                         }
                     } else {
                         sts128(b_hi, bhi);
@@ -964,18 +972,21 @@ __global__ void __launch_bounds__(kThreads, 1) qmv_q4_k_tc_e4m3_kernel(const __g
 
 // the int4-affine mixed-bit matrices (groups of 32) in the 8-bit operand
 // form, bf16 activations
+template <int XP>
 __global__ void __launch_bounds__(kThreads, 1) qmv_mix4_tc_e4m3_kernel(const __grid_constant__ QtcParams p) {
-    qmv_tc_body<kFmtMix4, 1, 1, 2>(p);
+    qmv_tc_body<kFmtMix4, 1, 1, XP>(p);
 }
 
 // the int2-symmetric mixed-bit matrices (groups of 32), likewise
+template <int XP>
 __global__ void __launch_bounds__(kThreads, 1) qmv_mix2_tc_e4m3_kernel(const __grid_constant__ QtcParams p) {
-    qmv_tc_body<kFmtMix2, 1, 1, 2>(p);
+    qmv_tc_body<kFmtMix2, 1, 1, XP>(p);
 }
 
 // the int8 mixed-bit matrices (groups of 32), the two-operand 8-bit form
+template <int XP>
 __global__ void __launch_bounds__(kThreads, 1) qmv_mix8_tc_e4m3_kernel(const __grid_constant__ QtcParams p) {
-    qmv_tc_body<kFmtMix8, 1, 1, 2>(p);
+    qmv_tc_body<kFmtMix8, 1, 1, XP>(p);
 }
 
 // Every kernel of this file may take kSmemBytes of dynamic shared memory (once
@@ -988,8 +999,9 @@ cudaError_t prepare_qtc_kernels() {
     for (auto f : {qmv_q4_0_tc_kernel<1, 1>, qmv_q4_0_tc_kernel<2, 1>, qmv_q4_0_tc_kernel<1, 2>,
                    qmv_q4_0_tc_e4m3_kernel<1, 2>, qmv_q4_0_tc_e4m3_kernel<2, 2>, qmv_q4_0_tc_e4m3_kernel<1, 3>,
                    qmv_q4_0_tc_e4m3_kernel<2, 3>, qmv_q4_k_tc_kernel, qmv_q4_k_tc_e4m3_kernel<2>,
-                   qmv_q4_k_tc_e4m3_kernel<3>, qmv_mix4_tc_e4m3_kernel, qmv_mix2_tc_e4m3_kernel,
-                   qmv_mix8_tc_e4m3_kernel}) {
+                   qmv_q4_k_tc_e4m3_kernel<3>, qmv_mix4_tc_e4m3_kernel<2>, qmv_mix2_tc_e4m3_kernel<2>,
+                   qmv_mix8_tc_e4m3_kernel<2>, qmv_mix4_tc_e4m3_kernel<3>, qmv_mix2_tc_e4m3_kernel<3>,
+                   qmv_mix8_tc_e4m3_kernel<3>}) {
         cudaError_t e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
         if (e != cudaSuccess) return e;
     }
@@ -1103,10 +1115,11 @@ bool qmv_mix_tc_supported(int64_t N, int64_t K, int sm_count) {
 // 128- or 64-byte swizzle), and for groups of 32 the scales and, for int4,
 // the biases ([N][K / 128] 8-byte words, box (2, 128)); qp, sc and bi the same
 // arrays (sc and bi read directly for larger groups and for the read-back
-// correction); bf16 x.
+// correction); bf16 x (two pieces) or fp32 x (three; int2 and int4 then read
+// their scales directly, as the third pieces take the B2 region).
 cudaError_t launch_qmv_mix_tc(int bits, const CUtensorMap* tmaps, const void* qp, const void* sc, const void* bi,
-                              int gshift, const void* x, void* y, int y_bf16, int N, int K, int sm_count,
-                              unsigned int* fault, cudaStream_t stream) {
+                              int gshift, const void* x, int x_bf16, void* y, int y_bf16, int N, int K,
+                              int sm_count, unsigned int* fault, cudaStream_t stream) {
     if (bits != 2 && bits != 4 && bits != 8) return cudaErrorInvalidValue;
     if (gshift < 5 || (K >> gshift) << gshift != K) return cudaErrorInvalidValue;
     QtcParams p;
@@ -1128,11 +1141,14 @@ cudaError_t launch_qmv_mix_tc(int bits, const CUtensorMap* tmaps, const void* qp
     p.tiles = (N + kTileRows - 1) / kTileRows;
     p.groups = K / kGroupK;
     p.units = p.tiles * p.groups;
-    p.x_bf16 = 1;
+    p.x_bf16 = x_bf16;
     p.y_bf16 = y_bf16;
     if (!table_fits(1, p.units, p.groups, sm_count)) return cudaErrorInvalidValue;
-    return launch_qtc(bits == 4 ? qmv_mix4_tc_e4m3_kernel : (bits == 2 ? qmv_mix2_tc_e4m3_kernel : qmv_mix8_tc_e4m3_kernel),
-                      p, p.units < sm_count ? p.units : sm_count, stream);
+    auto kernel = x_bf16 ? (bits == 4 ? qmv_mix4_tc_e4m3_kernel<2>
+                                      : (bits == 2 ? qmv_mix2_tc_e4m3_kernel<2> : qmv_mix8_tc_e4m3_kernel<2>))
+                         : (bits == 4 ? qmv_mix4_tc_e4m3_kernel<3>
+                                      : (bits == 2 ? qmv_mix2_tc_e4m3_kernel<3> : qmv_mix8_tc_e4m3_kernel<3>));
+    return launch_qtc(kernel, p, p.units < sm_count ? p.units : sm_count, stream);
 }
 
 }  // namespace qbw

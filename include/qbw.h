@@ -309,14 +309,14 @@ typedef enum qbw_mixbit {
  * form is summed as sc * sum(c x) + bi * sum(x) per group, so its rounding
  * scales with sum (|sc c| + |bi|) |x|.
  *
- * Groups of 32 (or a larger power of two), bf16 x, K % 256 == 0, sc (and bi)
- * 16-byte aligned and at least 5 MB (int4), 4 MB (int2) or 16 MB (int8) of
- * codes (10, 5 and 64 MB when K <= 4096) run on the tensor cores, like qmv_q4_k: the codes enter the MMA
- * exactly (int8 as its low nibble and its signed high nibble), x as two e4m3
- * pieces per element under a power-of-two scale per 32 elements, and the rows
- * whose pieces may miss more than 2^-11 of sum |sc q x| get the missed part
- * added exactly; they use the split-tile scratch above.  Every other call
- * takes the CUDA-core kernel.
+ * Groups of 32 (or a larger power of two), K % 256 == 0, sc (and bi) 16-byte
+ * aligned and at least 5 MB (int4), 4 MB (int2) or 16 MB (int8) of codes (10,
+ * 5 and 64 MB when K <= 4096) run on the tensor cores, like qmv_q4_k: the
+ * codes enter the MMA exactly (int8 as its low nibble and its signed high
+ * nibble), x as two (bf16) or three (fp32) e4m3 pieces per element under a
+ * power-of-two scale per 32 elements, and the rows whose pieces may miss more
+ * than 2^-11 of sum |sc q x| get the missed part added exactly; they use the
+ * split-tile scratch above.  Every other call takes the CUDA-core kernel.
  *
  *   x : K activations of xt, 16-byte aligned;  y : N outputs of yt
  *   M == 1; N >= 1; K as above.  On the CUDA-core kernel K must also be small

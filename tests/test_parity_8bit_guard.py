@@ -168,8 +168,8 @@ def zero_mix4_codes(qp, bi, outliers):
 
 @pytest.mark.parametrize("xdt", ["bf16", "f32"])
 def test_mixbit4_outliers_on_zero_weights(qbw, oracle, xdt):
-    # 16384 x 2048 int4 codes are 16.8 MB: bf16 x takes the tensor-core form
-    # (groups of 32), fp32 x the CUDA-core kernel
+    # 16384 x 2048 int4 codes are 16.8 MB: the tensor-core form, bf16 x in two
+    # pieces, fp32 x in three
     x, outliers = worst_case_activations(xdt, seed=51 if xdt == "bf16" else 52)
     qp, sc, bi = synth.mixbit_weights(4, N, K, 32, seed=53)
     qp, bi = zero_mix4_codes(qp, bi, outliers)
@@ -185,7 +185,7 @@ def test_mixbit4_outliers_on_zero_weights(qbw, oracle, xdt):
 
 @pytest.mark.parametrize("xdt", ["bf16", "f32"])
 def test_mixbit2_outliers_on_zero_weights(qbw, oracle, xdt):
-    # 16384 x 2048 int2 fields are 8.4 MB: bf16 x takes the tensor-core form
+    # 16384 x 2048 int2 fields are 8.4 MB: the tensor-core form (bf16 or fp32 x)
     x, outliers = worst_case_activations(xdt, seed=61 if xdt == "bf16" else 62)
     qp, sc, _ = synth.mixbit_weights(2, N, K, 32, seed=63)
     q = qp.view(np.uint8).reshape(N, K // 4)
@@ -202,7 +202,7 @@ def test_mixbit2_outliers_on_zero_weights(qbw, oracle, xdt):
 
 @pytest.mark.parametrize("xdt", ["bf16", "f32"])
 def test_mixbit8_outliers_on_zero_weights(qbw, oracle, xdt):
-    # 32768 x 2048 int8 codes are 67 MB: bf16 x takes the tensor-core form,
+    # 32768 x 2048 int8 codes are 67 MB: the tensor-core form (bf16 or fp32 x),
     # whose table puts each block's largest |x| lower (its second K-step takes
     # 16 x) and bounds the pieces' loss with |q| <= 128
     N8 = 32768

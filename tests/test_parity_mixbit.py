@@ -13,9 +13,10 @@ than one pass of the warp, groups smaller and larger than a 16-byte word
 group, per-channel scales (group = K), and the 31B profile's 5376 x 21504 and
 21504 x 5376 shapes in full.
 
-int4-affine, int2-symmetric and int8 matrices with groups of 32 and bf16 x
-take the tensor-core 8-bit form from 5 MB (int4), 4 MB (int2) or 16 MB (int8)
-of codes (10, 5 and 64 MB for K <= 4096): the test_tc* cases cover ragged tiles, short and long rows,
+int4-affine, int2-symmetric and int8 matrices with groups of 32 (or a larger
+power of two) take the tensor-core 8-bit form, with bf16 or fp32 x, from 5 MB
+(int4), 4 MB (int2) or 16 MB (int8) of codes (10, 5 and 64 MB for K <= 4096):
+the test_tc* cases cover ragged tiles, short and long rows,
 constant fields, zero scales, repeatability and the fallback to the CUDA-core
 kernel for scale arrays that are not 16-byte aligned.
 """
@@ -165,10 +166,12 @@ def route(qbw, bits, qp, sc, bi, G, x, N, K):
 
 
 @pytest.mark.parametrize("bits,N,K", TC_CASES)
-@pytest.mark.parametrize("odt", [torch.float32, torch.bfloat16])
-def test_tc(qbw, oracle, bits, N, K, odt):
+@pytest.mark.parametrize("xdt,odt", [("bf16", torch.float32), ("bf16", torch.bfloat16), ("f32", torch.float32)])
+def test_tc(qbw, oracle, bits, N, K, xdt, odt):
+    # bf16 x: two pieces per activation; fp32 x: three, the third in a second B
+    # (int2 and int4 then read their scales from global memory)
     qp, sc, bi = synth.mixbit_weights(bits, N, K, 32, seed=N + K + bits)
-    x = synth.activations(K, seed=K + 5, dtype="bf16")
+    x = synth.activations(K, seed=K + 5, dtype=xdt)
     assert route(qbw, bits, qp, sc, bi, 32, x, N, K), "the case no longer takes the tensor-core form"
     y = run(qbw, bits, qp, sc, bi, 32, x, N, K, odt)
     y_ref, _, S2 = oracle.qmv_mixbit(bits, qp, sc, bi, 32, x, N, K)
@@ -241,29 +244,33 @@ def test_tc_unaligned_scales_fall_back(qbw, oracle, bits):
 def test_tc_long_rows(qbw, oracle, bits):
     # K = 86016 (336 K-groups): beyond what the CUDA-core kernel can stage,
     # taken by the tensor-core form (every 128-row tile split across about 67
-    # CTAs); the same row length with fp32 x (CUDA cores) is rejected
+    # CTAs), with bf16 and fp32 x; the same rows with groups of 16 (CUDA cores
+    # only) are rejected
     N, K = 200, 86016
     qp, sc, bi = synth.mixbit_weights(bits, N, K, 32, seed=71 + bits)
-    x = synth.activations(K, seed=72, dtype="bf16")
-    assert route(qbw, bits, qp, sc, bi, 32, x, N, K)
-    y = run(qbw, bits, qp, sc, bi, 32, x, N, K)
-    y_ref, _, S2 = oracle.qmv_mixbit(bits, qp, sc, bi, 32, x, N, K)
-    check_matvec(to_f64(y), y_ref, S2, what=f"tc int{bits} K={K}")
+    for xdt in ("bf16", "f32"):
+        x = synth.activations(K, seed=72, dtype=xdt)
+        assert route(qbw, bits, qp, sc, bi, 32, x, N, K)
+        y = run(qbw, bits, qp, sc, bi, 32, x, N, K)
+        y_ref, _, S2 = oracle.qmv_mixbit(bits, qp, sc, bi, 32, x, N, K)
+        check_matvec(to_f64(y), y_ref, S2, what=f"tc int{bits} K={K} {xdt}")
+    qp16, sc16, bi16 = synth.mixbit_weights(bits, N, K, 16, seed=73)
     y32 = torch.empty(N, dtype=torch.float32, device="cuda")
     with pytest.raises(qbw.QbwError) as err:
-        qbw.qmv_mixbit(bits, dev(qp), dev(sc), dev(bi), 32, dev_act(synth.activations(K, seed=72)), y32, 1, N, K)
+        qbw.qmv_mixbit(bits, dev(qp16), dev(sc16), dev(bi16), 16, dev_act(synth.activations(K, seed=72, dtype="bf16")),
+                       y32, 1, N, K)
     assert err.value.status == 2           # QBW_ESHAPE
 
 
 @pytest.mark.parametrize("bits", [2, 4, 8])
 def test_route_cuda_core_cases(qbw, bits):
-    # what stays on the CUDA-core kernel: fp32 x, groups below 32 or not a power
-    # of two, rows not a multiple of 256, and matrices below the size thresholds
+    # what stays on the CUDA-core kernel: groups below 32 or not a power of two,
+    # rows not a multiple of 256, and matrices below the size thresholds
     N, K = 21504, 5376
     qp, sc, bi = synth.mixbit_weights(bits, N, K, 32, seed=91)
     xb = synth.activations(K, seed=92, dtype="bf16")
     assert route(qbw, bits, qp, sc, bi, 32, xb, N, K)
-    assert not route(qbw, bits, qp, sc, bi, 32, synth.activations(K, seed=92), N, K)
+    assert route(qbw, bits, qp, sc, bi, 32, synth.activations(K, seed=92), N, K)      # fp32 x too
     for G in (16, 48):                                         # not a power of two of at least 32
         qpg, scg, big = synth.mixbit_weights(bits, N, K, G, seed=93)
         assert not route(qbw, bits, qpg, scg, big, G, xb, N, K)
@@ -281,9 +288,10 @@ GROUP_CASES = [(b, G, 3077, 5376) for b in (2, 4, 8) for G in (64, 128, 256)] + 
 
 
 @pytest.mark.parametrize("bits,G,N,K", GROUP_CASES)
-def test_tc_larger_groups(qbw, oracle, bits, G, N, K):
+@pytest.mark.parametrize("xdt", ["bf16", "f32"])
+def test_tc_larger_groups(qbw, oracle, bits, G, N, K, xdt):
     qp, sc, bi = synth.mixbit_weights(bits, N, K, G, seed=G + bits)
-    x = synth.activations(K, seed=G + 1, dtype="bf16")
+    x = synth.activations(K, seed=G + 1, dtype=xdt)
     assert route(qbw, bits, qp, sc, bi, G, x, N, K), "the case no longer takes the tensor-core form"
     y = run(qbw, bits, qp, sc, bi, G, x, N, K)
     y_ref, _, S2 = oracle.qmv_mixbit(bits, qp, sc, bi, G, x, N, K)
