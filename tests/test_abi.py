@@ -166,6 +166,14 @@ def test_mixbit_validation(lib):
     assert f(8, w, sc, None, 32, P(ADDR + (1 << 30) + 4), F32, y, F32, 1, 16, 256, None) == 4
     assert f(8, w, sc, None, 32, x, 7, y, F32, 1, 16, 256, None) == 3
     assert f(8, w, sc, None, 32, x, F32, P(ADDR + 64), F32, 1, 16, 256, None) == 1    # y overlaps the words
+    r = lib.qmv_mixbit_route                                                     # no device needed for these
+    tc = ctypes.c_int(-1)
+    assert r(3, w, sc, bi, 32, F32, 16, 256, ctypes.byref(tc)) == 1             # unknown kind
+    assert r(8, w, sc, None, 32, F32, 16, 256, None) == 1                        # no result pointer
+    assert r(8, w, sc, None, 32, 7, 16, 256, ctypes.byref(tc)) == 3              # unknown activation type
+    assert r(8, w, sc, None, 64, BF16, 16, 65536, ctypes.byref(tc)) == 2         # neither kernel takes it
+    assert r(8, P(ADDR + 8), sc, None, 32, BF16, 16, 256, ctypes.byref(tc)) == 4
+    assert tc.value == -1                                                          # untouched on error
     g = lib.qdequant_mixbit
     assert g(4, w, sc, None, 32, y, 16, 256, None) == 1
     assert g(2, w, sc, None, 32, P(ADDR + (3 << 30) + 2), 16, 256, None) == 4
