@@ -311,7 +311,9 @@ typedef enum qbw_mixbit {
  *
  * Groups of 32 (or a larger power of two), K % 256 == 0, sc (and bi) 16-byte
  * aligned and at least 5 MB (int4), 4 MB (int2) or 16 MB (int8) of codes (10,
- * 5 and 64 MB when K <= 4096) run on the tensor cores, like qmv_q4_k: the
+ * 5 and 64 MB when K <= 4096) run on the tensor cores where their launch plan
+ * takes the shape (its row tiles and K-groups per CTA are bounded;
+ * qmv_mixbit_route reports the outcome), like qmv_q4_k: the
  * codes enter the MMA exactly (int8 as its low nibble and its signed high
  * nibble), x as two (bf16) or three (fp32) e4m3 pieces per element under a
  * power-of-two scale per 32 elements, and the rows whose pieces may miss more
